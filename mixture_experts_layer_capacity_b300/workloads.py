@@ -1,0 +1,148 @@
+"""Synthetic workloads and their seeded input generators.
+
+This module holds shapes, seeds and random draws only -- none of the layer's
+arithmetic.  The CUDA path and the tests (which hand the same tensors to the
+CPU oracle) both take their inputs from here.
+
+Recipe: one ``torch.Generator`` per tensor on the target device, seeded
+``seed * 100 + tensor_id`` with ids x=0, W_r=1, b_r=2, W_gate=3, W_up=4,
+W_down=5, Ws_gate=6, Ws_up=7, Ws_down=8.  Each draw is fp32 N(0, 1), scaled by
+the standard deviation and cast to the workload dtype.  Stacked expert weights
+are drawn one expert at a time from that tensor's generator (so the fp32
+temporary stays one expert large).  x ~ N(0, 1); every weight ~ N(0, 1/d_in)
+where d_in is the reduction dimension (D for W_r, W_gate, W_up, Ws_gate,
+Ws_up; F for W_down; S for Ws_down).
+
+Weight layout (reduction dimension contiguous, "K-major"):
+  W_r [E, D]; W_gate, W_up [E, F, D]; W_down [E, D, F];
+  Ws_gate, Ws_up [S, D]; Ws_down [D, S].
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+
+import torch
+
+GATING_SOFTMAX_SELECTED = 0      # Mixtral: softmax over the k chosen scores
+GATING_SOFTMAX_ALL = 1           # Switch / Qwen2: softmax over all, keep k
+GATING_SOFTMAX_ALL_RENORM = 2    # softmax over all, renormalised over the k
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int            # tokens
+    D: int            # d_model
+    E: int            # routed experts
+    F: int            # d_expert (hidden width of one routed expert)
+    k: int            # experts per token
+    S: int = 0        # hidden width of the shared expert; 0 = none
+    mode: int = GATING_SOFTMAX_SELECTED
+    gamma: float = 0.0    # capacity factor; <= 0 = dropless
+    dtype: str = "bf16"   # "bf16" or "fp32"
+    alpha: float = 0.01   # balance-loss coefficient
+    bias: str = "none"    # router logit bias: "none", "normal_var2", "zipf1.1"
+    description: str = ""
+
+    def with_T(self, T: int) -> "Workload":
+        return replace(self, T=T, name=f"{self.name.split('@')[0]}@T={T}")
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+
+WORKLOADS = {
+    "tiny_fp32": Workload(
+        "tiny_fp32", T=256, D=64, E=4, F=128, k=2, S=0,
+        mode=GATING_SOFTMAX_SELECTED, gamma=0.0, dtype="fp32",
+        description="tiny fp32 layer, top-2 softmax over selected, dropless"),
+    "switch_top1_capacity": Workload(
+        "switch_top1_capacity", T=4096, D=512, E=8, F=2048, k=1, S=0,
+        mode=GATING_SOFTMAX_ALL, gamma=1.0, dtype="bf16", alpha=0.01,
+        bias="normal_var2",
+        description="Switch-style top-1, raw probability, capacity factor 1.0 "
+                    "with token-order drops, biased router for imbalance"),
+    "mixtral_prefill": Workload(
+        "mixtral_prefill", T=8192, D=4096, E=8, F=14336, k=2,
+        mode=GATING_SOFTMAX_SELECTED, description="Mixtral-8x7B-shaped, T=8192"),
+    "mixtral_decode": Workload(
+        "mixtral_decode", T=64, D=4096, E=8, F=14336, k=2,
+        mode=GATING_SOFTMAX_SELECTED, description="Mixtral-8x7B-shaped, T=64"),
+    "qwen2_57b_prefill": Workload(
+        "qwen2_57b_prefill", T=8192, D=3584, E=64, F=2560, k=8, S=20480,
+        mode=GATING_SOFTMAX_ALL,
+        description="Qwen2-57B-A14B-shaped, shared expert d=20480, T=8192"),
+    "qwen2_57b_decode": Workload(
+        "qwen2_57b_decode", T=64, D=3584, E=64, F=2560, k=8, S=20480,
+        mode=GATING_SOFTMAX_ALL,
+        description="Qwen2-57B-A14B-shaped, shared expert d=20480, T=64"),
+    "dsv3_prefill": Workload(
+        "dsv3_prefill", T=16384, D=7168, E=256, F=2048, k=8, S=2048,
+        mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1",
+        description="DeepSeek-V3-shaped, renormalised top-8, Zipf-skewed bias, T=16384"),
+    "dsv3_decode": Workload(
+        "dsv3_decode", T=64, D=7168, E=256, F=2048, k=8, S=2048,
+        mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1",
+        description="DeepSeek-V3-shaped, renormalised top-8, Zipf-skewed bias, T=64"),
+}
+
+_TID = {"x": 0, "W_r": 1, "b_r": 2, "W_gate": 3, "W_up": 4, "W_down": 5,
+        "Ws_gate": 6, "Ws_up": 7, "Ws_down": 8}
+
+
+def _gen(device, seed, name):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 100 + _TID[name])
+    return g
+
+
+def _normal(shape, std, g, device, dtype):
+    return (torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+            * std).to(dtype)
+
+
+def _stacked(E, rows, cols, std, g, device, dtype):
+    out = torch.empty((E, rows, cols), device=device, dtype=dtype)
+    for e in range(E):
+        out[e] = _normal((rows, cols), std, g, device, dtype)
+    return out
+
+
+def make_inputs(w: Workload, seed: int = 0, device="cuda", weights: bool = True):
+    """Seeded synthetic inputs for workload ``w`` on ``device``.
+
+    Returns a dict with x, W_r, b_r (None if the workload has no bias), and,
+    when ``weights`` is true, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down
+    (the shared ones None when S = 0).  b_r is fp32; the rest use the
+    workload dtype.
+    """
+    dt = w.torch_dtype
+    dev = torch.device(device)
+    out = {}
+    out["x"] = _normal((w.T, w.D), 1.0, _gen(dev, seed, "x"), dev, dt)
+    out["W_r"] = _normal((w.E, w.D), 1.0 / math.sqrt(w.D), _gen(dev, seed, "W_r"), dev, dt)
+    if w.bias == "normal_var2":
+        out["b_r"] = _normal((w.E,), math.sqrt(2.0), _gen(dev, seed, "b_r"), dev,
+                             torch.float32)
+    elif w.bias == "zipf1.1":
+        # log of a Zipf(1.1) weight per expert: low-numbered experts favoured.
+        out["b_r"] = (-1.1 * torch.log(torch.arange(1, w.E + 1, dtype=torch.float64))
+                      ).to(torch.float32).to(dev)
+    else:
+        out["b_r"] = None
+    if not weights:
+        return out
+    sD, sF = 1.0 / math.sqrt(w.D), 1.0 / math.sqrt(w.F)
+    out["W_gate"] = _stacked(w.E, w.F, w.D, sD, _gen(dev, seed, "W_gate"), dev, dt)
+    out["W_up"] = _stacked(w.E, w.F, w.D, sD, _gen(dev, seed, "W_up"), dev, dt)
+    out["W_down"] = _stacked(w.E, w.D, w.F, sF, _gen(dev, seed, "W_down"), dev, dt)
+    if w.S > 0:
+        sS = 1.0 / math.sqrt(w.S)
+        out["Ws_gate"] = _normal((w.S, w.D), sD, _gen(dev, seed, "Ws_gate"), dev, dt)
+        out["Ws_up"] = _normal((w.S, w.D), sD, _gen(dev, seed, "Ws_up"), dev, dt)
+        out["Ws_down"] = _normal((w.D, w.S), sS, _gen(dev, seed, "Ws_down"), dev, dt)
+    else:
+        out["Ws_gate"] = out["Ws_up"] = out["Ws_down"] = None
+    return out

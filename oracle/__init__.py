@@ -1,0 +1,206 @@
+"""CPU oracle for one mixture-of-experts FFN layer's forward pass.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the
+benchmark's CPU-baseline leg are the only callers.  The arithmetic lives in
+``moe_oracle.c`` (plain loops, fp64); this module compiles it with gcc and
+marshals numpy arrays.  It imports nothing from the CUDA package, and the
+CUDA package imports nothing from here.
+
+Every function cites the page passage it follows in the C source.  The
+sampled-row helper :func:`moe_rows` combines per-expert outputs with the same
+definition as ``oracle_moe_forward`` (y_t = shared + sum of kept, weighted
+expert outputs; [M17] 17.2 equation) for layers whose weights do not fit in
+host memory as fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+MODE_SOFTMAX_SELECTED = 0
+MODE_SOFTMAX_ALL = 1
+MODE_SOFTMAX_ALL_RENORM = 2
+
+_ERRORS = {-1: "bad argument", -2: "out of host memory", -3: "non-finite router score"}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (gcc, -O2, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+               _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        vp = ctypes.c_void_p
+        lib.oracle_router_logits.argtypes = [i64, i64, i64, vp, vp, vp, vp]
+        lib.oracle_router_logits.restype = None
+        lib.oracle_route.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp]
+        lib.oracle_route.restype = i32
+        lib.oracle_capacity.argtypes = [i64, i64, i64, f64]
+        lib.oracle_capacity.restype = i64
+        lib.oracle_apply_capacity.argtypes = [i64, i64, i64, i64, vp, vp, vp]
+        lib.oracle_apply_capacity.restype = None
+        lib.oracle_aux_loss.argtypes = [i64, i64, i64, f64, vp, vp]
+        lib.oracle_aux_loss.restype = f64
+        lib.oracle_swiglu_rows.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
+        lib.oracle_swiglu_rows.restype = i32
+        lib.oracle_moe_forward.argtypes = (
+            [i64, i64, i64, i64, i64, i64, i32, f64, f64] + [vp] * 9 + [vp] * 9)
+        lib.oracle_moe_forward.restype = i32
+        _lib = lib
+        return lib
+
+
+def _f32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def _f64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _check(rc):
+    if rc != 0:
+        raise RuntimeError(f"oracle: {_ERRORS.get(rc, rc)}")
+
+
+def router_logits(x, W_r, bias=None):
+    """Router scores s = x W_r^T (+ bias), float64 [T, E]."""
+    x, W_r = _f32(x), _f32(W_r)
+    T, D = x.shape
+    E = W_r.shape[0]
+    b = None if bias is None else _f32(bias)
+    s = np.empty((T, E), dtype=np.float64)
+    _load().oracle_router_logits(T, D, E, _ptr(x), _ptr(W_r), _ptr(b), _ptr(s))
+    return s
+
+
+def route(s, k, mode):
+    """Top-k routing of scores s [T, E] -> (idx int32 [T,k], w f64 [T,k],
+    P_sum f64 [E], counts int64 [E])."""
+    s = _f64(s)
+    T, E = s.shape
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    P_sum = np.empty(E, dtype=np.float64)
+    counts = np.empty(E, dtype=np.int64)
+    _check(_load().oracle_route(T, E, k, mode, _ptr(s), _ptr(idx), _ptr(w),
+                                _ptr(P_sum), _ptr(counts)))
+    return idx, w, P_sum, counts
+
+
+def capacity(T, k, E, gamma):
+    """Expert capacity ceil(gamma*T*k/E); -1 when gamma <= 0 (dropless)."""
+    return int(_load().oracle_capacity(T, k, E, float(gamma)))
+
+
+def apply_capacity(idx, E, C):
+    """Token-order capacity truncation -> (dropped uint8 [T,k], kept int64 [E])."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    T, k = idx.shape
+    dropped = np.empty((T, k), dtype=np.uint8)
+    kept = np.empty(E, dtype=np.int64)
+    _load().oracle_apply_capacity(T, k, E, int(C), _ptr(idx), _ptr(dropped), _ptr(kept))
+    return dropped, kept
+
+
+def aux_loss(T, k, E, alpha, counts, P_sum):
+    """alpha * E * sum_e f_e P_e from demand counts and probability sums."""
+    counts = np.ascontiguousarray(counts, dtype=np.int64)
+    P_sum = _f64(P_sum)
+    return float(_load().oracle_aux_loss(T, k, E, float(alpha), _ptr(counts), _ptr(P_sum)))
+
+
+def swiglu_rows(x_rows, Wg, Wu, Wd):
+    """One SwiGLU expert on rows x [n, D]; Wg, Wu [F, D]; Wd [D, F] -> f64 [n, D]."""
+    x_rows, Wg, Wu, Wd = _f32(x_rows), _f32(Wg), _f32(Wu), _f32(Wd)
+    n, D = x_rows.shape
+    F = Wg.shape[0]
+    out = np.empty((n, D), dtype=np.float64)
+    _check(_load().oracle_swiglu_rows(n, D, F, _ptr(x_rows), _ptr(Wg), _ptr(Wu),
+                                      _ptr(Wd), _ptr(out)))
+    return out
+
+
+def moe_forward(x, W_r, W_gate, W_up, W_down, *, k, mode, gamma=0.0, alpha=0.0,
+                bias=None, Ws_gate=None, Ws_up=None, Ws_down=None, s_in=None):
+    """The whole layer on the host.  Returns a dict with s, idx, w, dropped,
+    counts, kept, aux, y.  s_in routes on given scores instead of the
+    oracle's own."""
+    x, W_r = _f32(x), _f32(W_r)
+    W_gate, W_up, W_down = _f32(W_gate), _f32(W_up), _f32(W_down)
+    T, D = x.shape
+    E, F, _ = W_gate.shape
+    S = 0 if Ws_gate is None else int(np.asarray(Ws_gate).shape[0])
+    Wsg = None if S == 0 else _f32(Ws_gate)
+    Wsu = None if S == 0 else _f32(Ws_up)
+    Wsd = None if S == 0 else _f32(Ws_down)
+    b = None if bias is None else _f32(bias)
+    sin = None if s_in is None else _f64(s_in)
+    out = dict(
+        s=np.empty((T, E), np.float64), idx=np.empty((T, k), np.int32),
+        w=np.empty((T, k), np.float64), dropped=np.empty((T, k), np.uint8),
+        counts=np.empty(E, np.int64), kept=np.empty(E, np.int64),
+        aux=np.empty(1, np.float64), y=np.empty((T, D), np.float64))
+    _check(_load().oracle_moe_forward(
+        T, D, E, F, k, S, mode, float(gamma), float(alpha),
+        _ptr(x), _ptr(W_r), _ptr(b), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
+        _ptr(Wsg), _ptr(Wsu), _ptr(Wsd), _ptr(sin),
+        _ptr(out["s"]), _ptr(out["idx"]), _ptr(out["w"]), _ptr(out["dropped"]),
+        _ptr(out["counts"]), _ptr(out["kept"]), _ptr(out["aux"]), _ptr(out["y"])))
+    out["aux"] = float(out["aux"][0])
+    return out
+
+
+def moe_rows(x_rows, idx, w, dropped, expert_weights, shared=None):
+    """y rows for a sample of tokens, expert by expert.
+
+    x_rows [n, D]: the sampled tokens' inputs; idx/w/dropped [n, k]: their
+    routing (taken from a routing of the whole batch);
+    expert_weights(e) -> (Wg [F,D], Wu [F,D], Wd [D,F]) as float32;
+    shared: None or (Wsg, Wsu, Wsd).
+    Same definition as oracle_moe_forward: y = shared + sum_j kept * w * FFN.
+    """
+    x_rows = _f32(x_rows)
+    n, D = x_rows.shape
+    idx = np.asarray(idx)
+    w = np.asarray(w, dtype=np.float64)
+    dropped = np.asarray(dropped)
+    y = np.zeros((n, D), dtype=np.float64)
+    for e in sorted(set(int(v) for v in idx[dropped == 0].ravel())):
+        rows, slots = np.nonzero((idx == e) & (dropped == 0))
+        Wg, Wu, Wd = expert_weights(e)
+        out = swiglu_rows(x_rows[rows], Wg, Wu, Wd)
+        y[rows] += w[rows, slots][:, None] * out
+    if shared is not None:
+        y += swiglu_rows(x_rows, *shared)
+    return y

@@ -1,0 +1,369 @@
+/*
+ * moe_oracle.c -- plain, slow CPU oracle for the forward pass of one
+ * mixture-of-experts (MoE) feed-forward layer with top-k gating, an optional
+ * expert capacity, an always-on shared expert and the load-balancing loss.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package's smoke check
+ * and the benchmark's CPU-baseline leg may load this file.  The CUDA library
+ * never calls it, shares no code, header, table or helper with it, and does
+ * not fall back to it.
+ *
+ * Precision: fp32 inputs are widened exactly to double; every dot product,
+ * softmax, SiLU, weight and sum is taken in double (fp64).  Loops run over
+ * tokens, then experts, in the order the definitions below are written.
+ *
+ * Sources (page titles; the section or equation follows each citation):
+ *   [M17]  "Mixture of Experts" (transformers-and-math, module 17)
+ *   [SFR]  "Mixture of Experts: Sparse FFNs, Routers, and Shared Experts"
+ *   [AEV]  "Mixture of experts" (AI engineering visualised)
+ *   [MPF]  "Mixture of Experts: More Parameters, Same FLOPs"
+ *   [FRT]  "Mixture of experts" (frontiers track)
+ *
+ * Parity pins (the tests that tie this file to the pages, not to itself):
+ *   - worked example of [MPF] "The router": probabilities (0.50, 0.30, 0.15,
+ *     0.05) at top-2 give weights 0.625 / 0.375;
+ *   - softmax-over-selected weights sum to 1 ([M17] 17.2, [FRT] gate eq.);
+ *   - closed forms of the balance loss ([M17] 17.4 and its exercise,
+ *     [MPF] "Keeping the load even", [FRT] balance eq.);
+ *   - the capacity exercise of [M17] 17.5 (C = 640) and the capacity
+ *     invariants (per-expert kept count <= C, token-order priority checked by
+ *     an independent recount);
+ *   - one expert with k = 1 equals the dense SwiGLU MLP ([MPF] "A bug worth
+ *     knowing about");
+ *   - a dense "run every expert on every token, mask by routing" brute force
+ *     on tiny inputs, and top-k selection against a full sort;
+ *   - permuting the experts permutes the indices and leaves y unchanged.
+ * Every exported function below is pinned by at least one of these.
+ *
+ * Weight layout: W_gate and W_up hold, per expert, F rows of D values
+ * (row f = the coefficients of hidden unit f); W_down holds D rows of F
+ * values.  [MPF] "An MoE tiny GPT" stores the transposes ([E,D,F], [E,F,D]);
+ * the arithmetic is the same.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG (-1)
+#define ORACLE_NO_MEMORY (-2)
+#define ORACLE_NONFINITE (-3)
+
+/* Gating modes.
+ *   0: softmax over the k selected scores ([M17] 17.2 "Mixtral";
+ *      [FRT] "Where the experts live", gate equation; [SFR] Router);
+ *   1: softmax over all E scores, keep the k largest, no renormalisation
+ *      ([M17] 17.2 "Switch Transformer and Qwen2"); with k = 1 this is the
+ *      raw top-1 probability ([MPF] "The router", last remark);
+ *   2: softmax over all E, renormalised over the chosen k
+ *      ([MPF] "The router", equation MoE(x)). */
+#define MODE_SOFTMAX_SELECTED 0
+#define MODE_SOFTMAX_ALL 1
+#define MODE_SOFTMAX_ALL_RENORM 2
+
+/* Router scores: s[t][e] = sum_d x[t][d] * W_r[e][d] (+ bias[e]).
+ * [MPF] "The router" (one score per expert, x W_r); [FRT] "Where the experts
+ * live" (s = W_r x); [SFR] Router (a bias-free linear layer).  The optional
+ * per-expert bias is part of the synthetic workloads, not of the pages. */
+void oracle_router_logits(int64_t T, int64_t D, int64_t E, const float *x,
+                          const float *W_r, const float *bias, double *s)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d)
+                acc += (double)x[t * D + d] * (double)W_r[e * D + d];
+            if (bias)
+                acc += (double)bias[e];
+            s[t * E + e] = acc;
+        }
+    }
+}
+
+/* Softmax of one row of scores over all E experts, largest score subtracted
+ * first ([MPF] "The router": a softmax turns the scores into probabilities). */
+static void softmax_row(int64_t E, const double *s, double *p)
+{
+    double m = s[0];
+    for (int64_t e = 1; e < E; ++e)
+        if (s[e] > m)
+            m = s[e];
+    double z = 0.0;
+    for (int64_t e = 0; e < E; ++e) {
+        p[e] = exp(s[e] - m);
+        z += p[e];
+    }
+    for (int64_t e = 0; e < E; ++e)
+        p[e] /= z;
+}
+
+/* Top-k selection: k rounds, each taking the largest score not yet taken; on
+ * equal scores the lower expert index wins (the pages leave tie order open;
+ * this is the reading the whole build uses).  idx[0] is the largest. */
+static void topk_row(int64_t E, int64_t k, const double *s, unsigned char *taken,
+                     int32_t *idx)
+{
+    memset(taken, 0, (size_t)E);
+    for (int64_t j = 0; j < k; ++j) {
+        int64_t best = -1;
+        for (int64_t e = 0; e < E; ++e) {
+            if (taken[e])
+                continue;
+            if (best < 0 || s[e] > s[best])
+                best = e;
+        }
+        idx[j] = (int32_t)best;
+        taken[best] = 1;
+    }
+}
+
+/* Routing of T tokens from their scores s[T][E]:
+ *   idx[t][0..k-1]  chosen experts, largest score first;
+ *   w[t][0..k-1]    gate weights for the given mode;
+ *   P_sum[e]        sum over tokens of the full-softmax probability of e
+ *                   (the balance loss's P_e is P_sum[e] / T);
+ *   counts[e]       assignments (t, j) with idx[t][j] == e, before capacity.
+ * Returns ORACLE_OK, ORACLE_BAD_ARG or ORACLE_NONFINITE (a score is NaN/Inf). */
+int oracle_route(int64_t T, int64_t E, int64_t k, int mode, const double *s,
+                 int32_t *idx, double *w, double *P_sum, int64_t *counts)
+{
+    if (T < 0 || E < 1 || k < 1 || k > E || mode < 0 || mode > 2)
+        return ORACLE_BAD_ARG;
+    for (int64_t i = 0; i < T * E; ++i)
+        if (!isfinite(s[i]))
+            return ORACLE_NONFINITE;
+    double *p = (double *)malloc(sizeof(double) * (size_t)E);
+    unsigned char *taken = (unsigned char *)malloc((size_t)E);
+    if (!p || !taken) {
+        free(p);
+        free(taken);
+        return ORACLE_NO_MEMORY;
+    }
+    for (int64_t e = 0; e < E; ++e) {
+        P_sum[e] = 0.0;
+        counts[e] = 0;
+    }
+    for (int64_t t = 0; t < T; ++t) {
+        const double *st = s + t * E;
+        int32_t *it = idx + t * k;
+        double *wt = w + t * k;
+        softmax_row(E, st, p);
+        topk_row(E, k, st, taken, it);
+        if (mode == MODE_SOFTMAX_SELECTED) {
+            /* g_i = e^{s_i} / sum_{j in top-k} e^{s_j}; the largest selected
+             * score (it[0]) is subtracted for range only. */
+            double m = st[it[0]], z = 0.0;
+            for (int64_t j = 0; j < k; ++j)
+                z += exp(st[it[j]] - m);
+            for (int64_t j = 0; j < k; ++j)
+                wt[j] = exp(st[it[j]] - m) / z;
+        } else if (mode == MODE_SOFTMAX_ALL) {
+            for (int64_t j = 0; j < k; ++j)
+                wt[j] = p[it[j]];
+        } else {
+            /* w_e = p_e / sum_{e' in top-k} p_{e'} */
+            double z = 0.0;
+            for (int64_t j = 0; j < k; ++j)
+                z += p[it[j]];
+            for (int64_t j = 0; j < k; ++j)
+                wt[j] = p[it[j]] / z;
+        }
+        for (int64_t e = 0; e < E; ++e)
+            P_sum[e] += p[e];
+        for (int64_t j = 0; j < k; ++j)
+            counts[it[j]] += 1;
+    }
+    free(p);
+    free(taken);
+    return ORACLE_OK;
+}
+
+/* Expert capacity C = ceil(gamma * k * T / E) ([M17] 17.5 equation;
+ * [AEV] "Capacity": phi times the fair share Tk/E; [MPF] "Keeping the load
+ * even": a capacity factor times kN/E).  gamma <= 0 means dropless: -1. */
+int64_t oracle_capacity(int64_t T, int64_t k, int64_t E, double gamma)
+{
+    if (gamma <= 0.0)
+        return -1;
+    return (int64_t)ceil(gamma * (double)(T * k) / (double)E);
+}
+
+/* Capacity truncation in token order: walk t = 0..T-1 and j = 0..k-1; the
+ * assignment (t, j) is kept iff fewer than C earlier assignments were kept by
+ * expert idx[t][j].  An over-capacity assignment is dropped by that expert
+ * only; the token keeps its other experts and its weights are not
+ * renormalised ([M17] 17.5; [SFR] "Capacity factor": tokens arriving at a full
+ * expert skip it; [AEV] "Capacity").  C < 0: nothing is dropped.
+ * dropped[t][j] = 1 for a dropped assignment; kept[e] = assignments kept. */
+void oracle_apply_capacity(int64_t T, int64_t k, int64_t E, int64_t C,
+                           const int32_t *idx, uint8_t *dropped, int64_t *kept)
+{
+    for (int64_t e = 0; e < E; ++e)
+        kept[e] = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t j = 0; j < k; ++j) {
+            int32_t e = idx[t * k + j];
+            if (C < 0 || kept[e] < C) {
+                kept[e] += 1;
+                dropped[t * k + j] = 0;
+            } else {
+                dropped[t * k + j] = 1;
+            }
+        }
+    }
+}
+
+/* Load-balancing loss aux = alpha * E * sum_e f_e * P_e with
+ *   f_e = counts[e] / (T * k)   (fraction of token assignments, [FRT]
+ *                                "Keeping the load balanced"; sums to 1),
+ *   P_e = P_sum[e] / T          (mean router probability).
+ * [M17] 17.4 equation; [SFR] "Auxiliary load-balancing loss"; [MPF] "Keeping
+ * the load even".  T = 0 gives 0 (no tokens, no loss). */
+double oracle_aux_loss(int64_t T, int64_t k, int64_t E, double alpha,
+                       const int64_t *counts, const double *P_sum)
+{
+    if (T <= 0)
+        return 0.0;
+    double acc = 0.0;
+    for (int64_t e = 0; e < E; ++e) {
+        double f = (double)counts[e] / (double)(T * k);
+        double P = P_sum[e] / (double)T;
+        acc += f * P;
+    }
+    return alpha * (double)E * acc;
+}
+
+/* SiLU(a) = a * sigmoid(a) = a / (1 + e^{-a}). */
+static double silu(double a)
+{
+    return a / (1.0 + exp(-a));
+}
+
+/* One SwiGLU feed-forward network on one token:
+ *   h_f = silu(sum_d W_gate[f][d] x_d) * (sum_d W_up[f][d] x_d),
+ *   out_d = sum_f W_down[d][f] h_f
+ * ([MPF] "An MoE tiny GPT": (silu(h G) * (h U)) D; [FRT] "Counting the
+ * parameters yourself": three weight matrices per gated expert).
+ * h is caller scratch of F doubles. */
+static void swiglu_token(int64_t D, int64_t F, const float *x, const float *Wg,
+                         const float *Wu, const float *Wd, double *h, double *out)
+{
+    for (int64_t f = 0; f < F; ++f) {
+        double g = 0.0, u = 0.0;
+        for (int64_t d = 0; d < D; ++d) {
+            g += (double)Wg[f * D + d] * (double)x[d];
+            u += (double)Wu[f * D + d] * (double)x[d];
+        }
+        h[f] = silu(g) * u;
+    }
+    for (int64_t d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int64_t f = 0; f < F; ++f)
+            acc += (double)Wd[d * F + f] * h[f];
+        out[d] = acc;
+    }
+}
+
+/* One SwiGLU expert applied to n token rows x[n][D] -> out[n][D].  Rows are
+ * independent; OpenMP (when compiled in) splits them over host threads
+ * without changing any row's arithmetic. */
+int oracle_swiglu_rows(int64_t n, int64_t D, int64_t F, const float *x,
+                       const float *Wg, const float *Wu, const float *Wd,
+                       double *out)
+{
+    if (n < 0 || D < 1 || F < 1)
+        return ORACLE_BAD_ARG;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *h = (double *)malloc(sizeof(double) * (size_t)F);
+        if (!h) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < n; ++r)
+            if (h)
+                swiglu_token(D, F, x + r * D, Wg, Wu, Wd, h, out + r * D);
+        free(h);
+    }
+    return err ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
+/* The whole layer ([M17] 17.2 equation with the shared expert):
+ *   y_t = FFN_shared(x_t) + sum_{j < k, kept} w_tj * FFN_{idx_tj}(x_t)
+ * computed token by token.  The residual connection is the caller's: y
+ * excludes x ([SFR] "Capacity factor": dropped tokens pass on the residual).
+ *
+ * s_in: scores to route on (e.g. another implementation's fp32 scores widened
+ * to double); NULL to use the oracle's own oracle_router_logits().  The scores
+ * used are written to s_out.  S = 0: no shared expert (Wsg/Wsu/Wsd unused).
+ * Output arrays: s_out[T][E], idx[T][k], w[T][k], dropped[T][k], counts[E],
+ * kept[E], aux[1], y[T][D]. */
+int oracle_moe_forward(int64_t T, int64_t D, int64_t E, int64_t F, int64_t k,
+                       int64_t S, int mode, double gamma, double alpha,
+                       const float *x, const float *W_r, const float *bias,
+                       const float *Wg, const float *Wu, const float *Wd,
+                       const float *Wsg, const float *Wsu, const float *Wsd,
+                       const double *s_in, double *s_out, int32_t *idx,
+                       double *w, uint8_t *dropped, int64_t *counts,
+                       int64_t *kept, double *aux, double *y)
+{
+    if (T < 0 || D < 1 || E < 1 || F < 1 || k < 1 || k > E || S < 0)
+        return ORACLE_BAD_ARG;
+    if (s_in)
+        memcpy(s_out, s_in, sizeof(double) * (size_t)(T * E));
+    else
+        oracle_router_logits(T, D, E, x, W_r, bias, s_out);
+
+    double *P_sum = (double *)malloc(sizeof(double) * (size_t)E);
+    if (!P_sum)
+        return ORACLE_NO_MEMORY;
+    int rc = oracle_route(T, E, k, mode, s_out, idx, w, P_sum, counts);
+    if (rc != ORACLE_OK) {
+        free(P_sum);
+        return rc;
+    }
+    int64_t C = oracle_capacity(T, k, E, gamma);
+    oracle_apply_capacity(T, k, E, C, idx, dropped, kept);
+    *aux = oracle_aux_loss(T, k, E, alpha, counts, P_sum);
+    free(P_sum);
+
+    int err = 0;
+#pragma omp parallel
+    {
+        int64_t hmax = F > S ? F : S;
+        double *h = (double *)malloc(sizeof(double) * (size_t)hmax);
+        double *o = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!h || !o) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t) {
+            if (!h || !o)
+                continue;
+            double *yt = y + t * D;
+            for (int64_t d = 0; d < D; ++d)
+                yt[d] = 0.0;
+            for (int64_t j = 0; j < k; ++j) {
+                if (dropped[t * k + j])
+                    continue;
+                int64_t e = idx[t * k + j];
+                swiglu_token(D, F, x + t * D, Wg + e * F * D, Wu + e * F * D,
+                             Wd + e * D * F, h, o);
+                for (int64_t d = 0; d < D; ++d)
+                    yt[d] += w[t * k + j] * o[d];
+            }
+            if (S > 0) {
+                swiglu_token(D, S, x + t * D, Wsg, Wsu, Wsd, h, o);
+                for (int64_t d = 0; d < D; ++d)
+                    yt[d] += o[d];
+            }
+        }
+        free(h);
+        free(o);
+    }
+    return err ? ORACLE_NO_MEMORY : ORACLE_OK;
+}

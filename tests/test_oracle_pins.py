@@ -1,0 +1,353 @@
+"""Pins of the CPU oracle to what the pages and the mathematics fix.
+
+Each test ties the oracle to something other than itself: a worked example
+printed on the pages, a closed form, an exercise, an independent brute force
+(numpy matrix products, a full sort, an explicit recount), or an invariant.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+from conftest import GOLDEN
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _silu(a):
+    return a / (1.0 + np.exp(-a))
+
+
+def _dense_swiglu(X, Wg, Wu, Wd):
+    """numpy matrix form of one SwiGLU network over all rows of X (fp64)."""
+    X = X.astype(np.float64)
+    return (_silu(X @ Wg.astype(np.float64).T) * (X @ Wu.astype(np.float64).T)) \
+        @ Wd.astype(np.float64).T
+
+
+def _rand_layer(rng, T, D, E, F, S=0):
+    x = rng.standard_normal((T, D)).astype(np.float32)
+    Wr = (rng.standard_normal((E, D)) / math.sqrt(D)).astype(np.float32)
+    Wg = (rng.standard_normal((E, F, D)) / math.sqrt(D)).astype(np.float32)
+    Wu = (rng.standard_normal((E, F, D)) / math.sqrt(D)).astype(np.float32)
+    Wd = (rng.standard_normal((E, D, F)) / math.sqrt(F)).astype(np.float32)
+    sh = {}
+    if S:
+        sh = dict(Ws_gate=(rng.standard_normal((S, D)) / math.sqrt(D)).astype(np.float32),
+                  Ws_up=(rng.standard_normal((S, D)) / math.sqrt(D)).astype(np.float32),
+                  Ws_down=(rng.standard_normal((D, S)) / math.sqrt(S)).astype(np.float32))
+    return x, Wr, Wg, Wu, Wd, sh
+
+
+# --- gating -----------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_worked_example(mode):
+    g = _load("worked_example.json")
+    p = np.array(g["probs"])
+    s = np.log(p)[None, :]
+    idx, w, P_sum, counts = oracle.route(s, g["k"], mode)
+    assert idx[0].tolist() == g["chosen"]
+    if mode in (0, 2):
+        np.testing.assert_allclose(w[0], g["weights_renormalised"], rtol=0, atol=1e-12)
+    else:
+        # softmax over all, no renormalisation: the raw probabilities, sum < 1
+        np.testing.assert_allclose(w[0], p[g["chosen"]], rtol=0, atol=1e-12)
+        assert abs(w[0].sum() - g["selected_prob_sum"]) < 1e-12
+    np.testing.assert_allclose(P_sum, p, atol=1e-12)
+
+
+def test_selected_softmax_sums_to_one_and_modes_agree():
+    rng = np.random.default_rng(1)
+    s = rng.standard_normal((500, 16)) * 3
+    for k in (1, 2, 5, 16):
+        _, w0, _, _ = oracle.route(s, k, 0)
+        _, w1, _, _ = oracle.route(s, k, 1)
+        _, w2, _, _ = oracle.route(s, k, 2)
+        np.testing.assert_allclose(w0.sum(1), 1.0, atol=1e-12)
+        np.testing.assert_allclose(w2.sum(1), 1.0, atol=1e-12)
+        # modes 0 and 2 are the same function in exact arithmetic
+        np.testing.assert_allclose(w0, w2, atol=1e-12)
+        assert np.all(w1.sum(1) <= 1.0 + 1e-12)
+        if k == 16:
+            np.testing.assert_allclose(w1.sum(1), 1.0, atol=1e-12)
+
+
+def test_mode1_weights_are_softmax_probabilities():
+    rng = np.random.default_rng(2)
+    s = rng.standard_normal((64, 12)) * 2
+    idx, w, P_sum, _ = oracle.route(s, 3, 1)
+    z = np.exp(s - s.max(1, keepdims=True))
+    p = z / z.sum(1, keepdims=True)
+    np.testing.assert_allclose(w, np.take_along_axis(p, idx.astype(np.int64), 1), atol=1e-14)
+    np.testing.assert_allclose(P_sum, p.sum(0), atol=1e-12)
+
+
+def test_top1_renormalised_weight_is_exactly_one():
+    rng = np.random.default_rng(3)
+    s = rng.standard_normal((100, 8))
+    _, w, _, _ = oracle.route(s, 1, 2)
+    assert np.all(w == 1.0)
+    _, w1, _, _ = oracle.route(s, 1, 1)
+    z = np.exp(s - s.max(1, keepdims=True))
+    np.testing.assert_allclose(w1[:, 0], (z / z.sum(1, keepdims=True)).max(1), atol=1e-14)
+
+
+@pytest.mark.parametrize("E,k", [(5, 1), (5, 2), (6, 3), (8, 8), (16, 4)])
+def test_topk_against_full_sort_with_ties(E, k):
+    rng = np.random.default_rng(E * 10 + k)
+    # small integers: many exact ties, the order must go to the lower index
+    s = rng.integers(-2, 3, size=(300, E)).astype(np.float64)
+    idx, _, _, counts = oracle.route(s, k, 1)
+    for t in range(s.shape[0]):
+        want = sorted(range(E), key=lambda e: (-s[t, e], e))[:k]
+        assert idx[t].tolist() == want
+    assert counts.sum() == s.shape[0] * k
+    np.testing.assert_array_equal(counts, np.bincount(idx.ravel(), minlength=E))
+
+
+def test_topk_maximises_subset_sum():
+    rng = np.random.default_rng(7)
+    E = 6
+    s = rng.standard_normal((50, E))
+    for k in (1, 2, 3, 4):
+        idx, _, _, _ = oracle.route(s, k, 0)
+        for t in range(s.shape[0]):
+            best = max(sum(s[t, list(c)]) for c in itertools.combinations(range(E), k))
+            assert abs(sum(s[t, idx[t]]) - best) < 1e-12
+            assert len(set(idx[t].tolist())) == k
+
+
+def test_nonfinite_scores_rejected():
+    s = np.zeros((2, 4))
+    s[1, 2] = np.nan
+    with pytest.raises(RuntimeError):
+        oracle.route(s, 2, 0)
+
+
+# --- balance loss -----------------------------------------------------------
+
+def test_balance_loss_closed_forms():
+    g = _load("balance_loss_exercise.json")
+    E, k, alpha = g["E"], g["k"], g["alpha"]
+    T = 8 * E
+    # even split: token t strongly prefers expert t % E (probability ~ 1)
+    s = np.zeros((T, E))
+    s[np.arange(T), np.arange(T) % E] = 60.0
+    idx, _, P_sum, counts = oracle.route(s, k, 1)
+    assert np.all(counts == T // E)
+    assert abs(oracle.aux_loss(T, k, E, alpha, counts, P_sum) - g["even_split"]) < 1e-12
+    # collapse: every token to expert 0 with probability 1
+    s = np.zeros((T, E))
+    s[:, 0] = 60.0
+    idx, _, P_sum, counts = oracle.route(s, k, 1)
+    assert counts[0] == T
+    assert abs(oracle.aux_loss(T, k, E, alpha, counts, P_sum)
+               - g["all_to_one_expert_prob_one"]) < 1e-12
+
+
+def test_balance_loss_even_split_top2_is_alpha():
+    # f_e counts assignments over T*k, so an even top-2 split still gives alpha
+    E, k, T, alpha = 8, 2, 64, 0.01
+    s = np.zeros((T, E))
+    s[np.arange(T), (2 * np.arange(T)) % E] = 60.0
+    s[np.arange(T), (2 * np.arange(T) + 1) % E] = 59.0
+    idx, _, P_sum, counts = oracle.route(s, k, 0)
+    assert np.all(counts == T * k // E)
+    # P_e: each token splits ~ (1, e^-1)/(1+e^-1) between its two experts
+    a = oracle.aux_loss(T, k, E, alpha, counts, P_sum)
+    assert abs(a - alpha) < 1e-12
+
+
+def test_balance_loss_zero_tokens():
+    assert oracle.aux_loss(0, 2, 4, 0.01, np.zeros(4, np.int64), np.zeros(4)) == 0.0
+
+
+# --- capacity ---------------------------------------------------------------
+
+def test_capacity_exercise_and_switch_workload():
+    g = _load("capacity_exercise.json")
+    assert oracle.capacity(g["T"], g["k"], g["E"], g["gamma"]) == g["C"]
+    # Switch-style workload: T=4096, top-1, E=8, factor 1.0 -> the fair share
+    assert oracle.capacity(4096, 1, 8, 1.0) == 512
+    assert oracle.capacity(4096, 1, 8, 0.0) == -1
+    assert oracle.capacity(4096, 1, 8, -1.0) == -1
+    # rounding up
+    assert oracle.capacity(10, 1, 3, 1.0) == 4
+    assert oracle.capacity(1, 1, 8, 1.0) == 1
+
+
+@pytest.mark.parametrize("gamma", [0.25, 0.5, 1.0, 1.25])
+def test_capacity_token_order_against_recount(gamma):
+    rng = np.random.default_rng(int(gamma * 100))
+    T, E, k = 257, 8, 2
+    # skewed scores so that low experts overflow
+    s = rng.standard_normal((T, E)) + np.linspace(2, 0, E)
+    idx, _, _, counts = oracle.route(s, k, 0)
+    C = oracle.capacity(T, k, E, gamma)
+    dropped, kept = oracle.apply_capacity(idx, E, C)
+    assert np.all(kept <= C)
+    assert kept.sum() + dropped.sum() == T * k
+    np.testing.assert_array_equal(kept, np.minimum(counts, C))
+    # independent recount: the first C tokens (in token order) of each expert stay
+    want = np.zeros((T, k), np.uint8)
+    for e in range(E):
+        rows, slots = np.nonzero(idx == e)
+        order = np.argsort(rows, kind="stable")
+        rows, slots = rows[order], slots[order]
+        want[rows[C:], slots[C:]] = 1
+    np.testing.assert_array_equal(dropped, want)
+
+
+def test_capacity_large_factor_is_dropless():
+    rng = np.random.default_rng(5)
+    s = rng.standard_normal((100, 4))
+    idx, _, _, counts = oracle.route(s, 2, 0)
+    d_big, k_big = oracle.apply_capacity(idx, 4, oracle.capacity(100, 2, 4, 1e6))
+    d_none, k_none = oracle.apply_capacity(idx, 4, -1)
+    assert d_big.sum() == 0 and d_none.sum() == 0
+    np.testing.assert_array_equal(k_big, counts)
+    np.testing.assert_array_equal(k_none, counts)
+
+
+# --- experts and the whole layer -----------------------------------------------
+
+def test_router_logits_against_matmul():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((33, 40)).astype(np.float32)
+    Wr = rng.standard_normal((7, 40)).astype(np.float32)
+    b = rng.standard_normal(7).astype(np.float32)
+    s = oracle.router_logits(x, Wr, b)
+    np.testing.assert_allclose(s, x.astype(np.float64) @ Wr.astype(np.float64).T + b,
+                               rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_single_expert_is_the_dense_mlp(mode):
+    rng = np.random.default_rng(20 + mode)
+    x, Wr, Wg, Wu, Wd, _ = _rand_layer(rng, 40, 16, 1, 24)
+    out = oracle.moe_forward(x, Wr, Wg, Wu, Wd, k=1, mode=mode)
+    ref = _dense_swiglu(x, Wg[0], Wu[0], Wd[0])
+    np.testing.assert_allclose(out["y"], ref, rtol=1e-11, atol=1e-11)
+    assert np.all(out["w"] == 1.0)
+
+
+def _numpy_layer(x, Wr, Wg, Wu, Wd, k, mode, gamma, sh):
+    """Brute force: run every expert on every token, then mask by routing."""
+    T, E = x.shape[0], Wr.shape[0]
+    s = x.astype(np.float64) @ Wr.astype(np.float64).T
+    z = np.exp(s - s.max(1, keepdims=True))
+    p = z / z.sum(1, keepdims=True)
+    order = np.array([sorted(range(E), key=lambda e: (-s[t, e], e))[:k] for t in range(T)])
+    sel_s = np.take_along_axis(s, order, 1)
+    sel_p = np.take_along_axis(p, order, 1)
+    if mode == 0:
+        ez = np.exp(sel_s - sel_s[:, :1])
+        w = ez / ez.sum(1, keepdims=True)
+    elif mode == 1:
+        w = sel_p
+    else:
+        w = sel_p / sel_p.sum(1, keepdims=True)
+    mask = np.ones((T, k))
+    if gamma > 0:
+        C = math.ceil(gamma * T * k / E)
+        for e in range(E):
+            rows, slots = np.nonzero(order == e)
+            o = np.argsort(rows, kind="stable")
+            mask[rows[o][C:], slots[o][C:]] = 0.0
+    Y = np.stack([_dense_swiglu(x, Wg[e], Wu[e], Wd[e]) for e in range(E)])  # [E,T,D]
+    y = np.zeros((T, x.shape[1]))
+    for j in range(k):
+        y += (mask[:, j] * w[:, j])[:, None] * Y[order[:, j], np.arange(T)]
+    if sh:
+        y += _dense_swiglu(x, sh["Ws_gate"], sh["Ws_up"], sh["Ws_down"])
+    counts = np.bincount(order.ravel(), minlength=E)
+    f = counts / (T * k)
+    aux = 0.01 * E * float(np.sum(f * p.mean(0)))
+    return dict(y=y, idx=order, w=w, dropped=(mask == 0).astype(np.uint8),
+                counts=counts, aux=aux)
+
+
+@pytest.mark.parametrize("mode,gamma,S", [(0, 0.0, 0), (1, 0.5, 4), (2, 1.0, 0), (0, 0.75, 6)])
+def test_layer_against_dense_bruteforce(mode, gamma, S):
+    rng = np.random.default_rng(100 + mode + S)
+    T, D, E, F, k = 24, 8, 5, 6, 2
+    x, Wr, Wg, Wu, Wd, sh = _rand_layer(rng, T, D, E, F, S)
+    out = oracle.moe_forward(x, Wr, Wg, Wu, Wd, k=k, mode=mode, gamma=gamma,
+                             alpha=0.01, **sh)
+    ref = _numpy_layer(x, Wr, Wg, Wu, Wd, k, mode, gamma, sh)
+    np.testing.assert_array_equal(out["idx"], ref["idx"])
+    np.testing.assert_array_equal(out["dropped"], ref["dropped"])
+    np.testing.assert_array_equal(out["counts"], ref["counts"])
+    np.testing.assert_allclose(out["w"], ref["w"], atol=1e-12)
+    np.testing.assert_allclose(out["y"], ref["y"], rtol=1e-10, atol=1e-10)
+    assert abs(out["aux"] - ref["aux"]) < 1e-12
+    if gamma > 0:
+        assert out["dropped"].sum() > 0
+
+
+def test_shared_expert_is_added_unweighted():
+    rng = np.random.default_rng(31)
+    x, Wr, Wg, Wu, Wd, sh = _rand_layer(rng, 20, 8, 4, 6, S=10)
+    with_sh = oracle.moe_forward(x, Wr, Wg, Wu, Wd, k=2, mode=1, **sh)
+    without = oracle.moe_forward(x, Wr, Wg, Wu, Wd, k=2, mode=1)
+    np.testing.assert_allclose(with_sh["y"] - without["y"],
+                               _dense_swiglu(x, sh["Ws_gate"], sh["Ws_up"], sh["Ws_down"]),
+                               rtol=1e-10, atol=1e-10)
+    # two shared experts of widths 4 and 6 equal one of width 10
+    halves = [oracle.swiglu_rows(x, sh["Ws_gate"][a:b], sh["Ws_up"][a:b], sh["Ws_down"][:, a:b])
+              for a, b in ((0, 4), (4, 10))]
+    np.testing.assert_allclose(with_sh["y"] - without["y"], halves[0] + halves[1],
+                               rtol=1e-10, atol=1e-10)
+
+
+def test_dropped_top1_token_gets_shared_only():
+    rng = np.random.default_rng(32)
+    x, Wr, Wg, Wu, Wd, sh = _rand_layer(rng, 64, 8, 4, 6, S=5)
+    out = oracle.moe_forward(x, Wr, Wg, Wu, Wd, k=1, mode=1, gamma=0.25, **sh)
+    d = out["dropped"][:, 0] == 1
+    assert d.sum() > 0
+    sh_only = _dense_swiglu(x, sh["Ws_gate"], sh["Ws_up"], sh["Ws_down"])
+    np.testing.assert_allclose(out["y"][d], sh_only[d], rtol=1e-10, atol=1e-10)
+
+
+def test_expert_permutation_invariance():
+    rng = np.random.default_rng(41)
+    x, Wr, Wg, Wu, Wd, _ = _rand_layer(rng, 30, 8, 6, 5)
+    perm = rng.permutation(6)
+    a = oracle.moe_forward(x, Wr, Wg, Wu, Wd, k=3, mode=2)
+    b = oracle.moe_forward(x, Wr[perm], Wg[perm], Wu[perm], Wd[perm], k=3, mode=2)
+    inv = np.argsort(perm)
+    np.testing.assert_array_equal(perm[b["idx"]], a["idx"])
+    np.testing.assert_array_equal(b["counts"], a["counts"][perm])
+    assert inv[perm[0]] == 0
+    np.testing.assert_allclose(a["y"], b["y"], rtol=1e-11, atol=1e-11)
+
+
+def test_sampled_rows_match_whole_layer():
+    rng = np.random.default_rng(51)
+    x, Wr, Wg, Wu, Wd, sh = _rand_layer(rng, 40, 8, 4, 6, S=3)
+    full = oracle.moe_forward(x, Wr, Wg, Wu, Wd, k=2, mode=0, gamma=0.6, **sh)
+    rows = np.array([0, 3, 17, 39])
+    y = oracle.moe_rows(x[rows], full["idx"][rows], full["w"][rows], full["dropped"][rows],
+                        lambda e: (Wg[e], Wu[e], Wd[e]),
+                        shared=(sh["Ws_gate"], sh["Ws_up"], sh["Ws_down"]))
+    np.testing.assert_allclose(y, full["y"][rows], rtol=1e-12, atol=1e-12)
+
+
+def test_routing_on_given_scores():
+    rng = np.random.default_rng(61)
+    x, Wr, Wg, Wu, Wd, _ = _rand_layer(rng, 16, 8, 4, 6)
+    s = rng.standard_normal((16, 4))
+    out = oracle.moe_forward(x, Wr, Wg, Wu, Wd, k=2, mode=0, s_in=s)
+    np.testing.assert_array_equal(out["s"], s)
+    idx, w, _, _ = oracle.route(s, 2, 0)
+    np.testing.assert_array_equal(out["idx"], idx)
