@@ -1,0 +1,161 @@
+/*
+ * moe.h -- C ABI of libmoe.so: the forward pass of one mixture-of-experts
+ * (MoE) feed-forward layer on one NVIDIA B300 (sm_103a).
+ *
+ * The layer (page titles cited; section or equation after each):
+ *   s   = x W_r^T (+ b_r)                  router scores
+ *         ("Mixture of Experts: More Parameters, Same FLOPs", 'The router';
+ *          "Mixture of experts" (frontiers track), 'Where the experts live')
+ *   idx = top-k of s, largest first, lower expert index first on equal scores
+ *   w   = gate weights, by gating mode (see moe_gating_mode)
+ *   C   = ceil(capacity_factor * T * k / E)   expert capacity
+ *         ("Mixture of Experts" (module 17), 17.5 equation); assignments
+ *         beyond C, in token order, are dropped by that expert only
+ *   y_t = FFN_shared(x_t) + sum_{j<k, kept} w_tj FFN_{idx_tj}(x_t)
+ *         (module 17, 17.2 equation), FFN(v) = W_down (silu(W_gate v) * (W_up v))
+ *   aux = alpha * E * sum_e f_e P_e, f_e = n_e / (T k), P_e = mean_t p_te
+ *         (module 17, 17.4 equation; "Mixture of experts" (frontiers track),
+ *          'Keeping the load balanced'); n_e counts assignments before capacity.
+ * The residual connection is not added: y excludes x.
+ *
+ * Conventions (all entry points):
+ *   - Every tensor pointer is DEVICE memory allocated and owned by the caller;
+ *     the library allocates nothing and keeps no pointer after a call returns.
+ *   - Work is enqueued on `stream` and the call returns without waiting; no
+ *     entry point except moe_read_device_status synchronises.
+ *   - Errors the host can detect return a non-zero moe_status before anything
+ *     is launched and leave every output untouched.
+ *   - Row-major, dense, contiguous tensors.  "K-major" weights: each output
+ *     row is contiguous over the reduction dimension.
+ *   - dtype applies to x, the expert weights, W_r and y; router scores, gate
+ *     weights and statistics are fp32 in every dtype.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad enum, ... */
+    MOE_ERR_UNSUPPORTED = 2,   /* a shape outside the supported set below */
+    MOE_ERR_WORKSPACE = 3,     /* workspace too small or not 256-byte aligned */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+    MOE_ERR_DEVICE_STATUS = 5  /* a kernel reported an error (see below) */
+} moe_status;
+
+/* Gate weights for the k selected experts of a token.
+ *   MOE_GATE_SOFTMAX_SELECTED: w_j = e^{s_j} / sum_{j' in top-k} e^{s_j'}
+ *     (Mixtral; module 17, 17.2; frontiers track, gate equation); sums to 1.
+ *   MOE_GATE_SOFTMAX_ALL: p = softmax(s) over all E, w_j = p_{idx_j}, no
+ *     renormalisation (Switch Transformer / Qwen2; module 17, 17.2); with
+ *     k = 1 this is the raw top-1 probability ('The router', last remark).
+ *   MOE_GATE_SOFTMAX_ALL_RENORM: w_j = p_{idx_j} / sum_{j'} p_{idx_j'}
+ *     ('The router', equation MoE(x)); w = 1 when k = 1. */
+typedef enum {
+    MOE_GATE_SOFTMAX_SELECTED = 0,
+    MOE_GATE_SOFTMAX_ALL = 1,
+    MOE_GATE_SOFTMAX_ALL_RENORM = 2
+} moe_gating_mode;
+
+typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP32 = 1 } moe_dtype;
+
+/* Layer shape and options.  Supported:
+ *   T >= 0 tokens, T * top_k < 2^31;
+ *   1 <= n_experts <= 256; 1 <= top_k <= min(8, n_experts);
+ *   d_model, d_expert >= 1; d_shared >= 0 (0 = no shared expert);
+ *   bf16: d_model, d_expert and d_shared multiples of 64;
+ *   fp32: any sizes (SIMT path, for small layers and exact checks).
+ * capacity_factor <= 0 means dropless.  aux_alpha scales aux_loss. */
+typedef struct {
+    int32_t T;
+    int32_t d_model;
+    int32_t n_experts;
+    int32_t d_expert;
+    int32_t top_k;
+    int32_t d_shared;
+    int32_t dtype;          /* moe_dtype */
+    int32_t gating_mode;    /* moe_gating_mode */
+    float capacity_factor;
+    float aux_alpha;
+} moe_config;
+
+/* Device status codes written by kernels (read with moe_read_device_status). */
+#define MOE_DEVICE_OK 0
+#define MOE_DEVICE_NONFINITE_SCORE 1   /* a router score was NaN/Inf */
+#define MOE_DEVICE_PIPELINE_TIMEOUT 2  /* a bounded in-kernel wait ran out */
+
+/* Bytes of scratch moe_forward needs for `cfg` (x gathered by expert, the
+ * SwiGLU hidden rows, per-expert scan tables, ...).  Returns
+ * MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for an invalid config. */
+MOE_API moe_status moe_workspace_size(const moe_config *cfg, size_t *bytes);
+
+/* Expert capacity the library uses for `cfg`: ceil(capacity_factor * T *
+ * top_k / n_experts) computed in double, or -1 when dropless
+ * (module 17, 17.5 equation).  Host only; no GPU needed. */
+MOE_API int64_t moe_capacity(const moe_config *cfg);
+
+/* The forward pass (one call = the whole layer, enqueued on `stream`).
+ *
+ * Inputs (device, dtype = cfg->dtype unless stated):
+ *   x            [T, d_model]
+ *   W_r          [E, d_model]               router, K-major
+ *   router_bias  [E] fp32, or NULL          added to the scores before
+ *                                           selection and weighting
+ *   W_gate, W_up [E, d_expert, d_model]     K-major
+ *   W_down       [E, d_model, d_expert]     K-major
+ *   Ws_gate, Ws_up [d_shared, d_model]; Ws_down [d_model, d_shared];
+ *                                           all NULL when d_shared == 0
+ * Outputs (device):
+ *   y             [T, d_model] dtype
+ *   router_logits [T, E] fp32   the scores s the routing used (bias included)
+ *   topk_idx      [T, k] int32  selected experts, largest score first
+ *   topk_w        [T, k] fp32   gate weights (not renormalised after drops)
+ *   dropped_mask  [T, k] uint8  1 = dropped by capacity
+ *   expert_counts [E] int32     assignments per expert before capacity
+ *   kept_counts   [E] int32     assignments per expert after capacity
+ *   aux_loss      [1] fp32      balance loss (0 when T == 0)
+ * workspace: device, 256-byte aligned, >= moe_workspace_size(cfg) bytes;
+ *   its contents on entry are ignored.
+ * When T == 0 only expert_counts, kept_counts, aux_loss and workspace must
+ * be non-NULL; they are zeroed and nothing else is touched.
+ * Inputs must be finite; a non-finite score sets MOE_DEVICE_NONFINITE_SCORE
+ * (outputs then stay in bounds but are unspecified).
+ * Returns MOE_OK once everything is enqueued. */
+MOE_API moe_status moe_forward(const moe_config *cfg,
+                       const void *x, const void *W_r, const float *router_bias,
+                       const void *W_gate, const void *W_up, const void *W_down,
+                       const void *Ws_gate, const void *Ws_up, const void *Ws_down,
+                       void *y, float *router_logits, int32_t *topk_idx,
+                       float *topk_w, uint8_t *dropped_mask,
+                       int32_t *expert_counts, int32_t *kept_counts,
+                       float *aux_loss, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* Waits for `stream`, then reads the device status word the last
+ * moe_forward on this workspace wrote: *code = MOE_DEVICE_OK or one of the
+ * MOE_DEVICE_* codes.  Returns MOE_ERR_DEVICE_STATUS when *code != 0,
+ * MOE_ERR_CUDA if the stream reported an error. */
+MOE_API moe_status moe_read_device_status(const moe_config *cfg, const void *workspace,
+                                  cudaStream_t stream, int32_t *code);
+
+/* Static, human-readable name of a status. */
+MOE_API const char *moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,183 @@
+"""Thin ctypes binding of libmoe.so (C ABI in include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  PyTorch provides device memory and the stream.  The library is
+loaded on first use; if it is missing, loading raises -- there is no other
+implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_DEVICE_STATUS = 5
+
+MOE_DTYPE_BF16 = 0
+MOE_DTYPE_FP32 = 1
+
+MOE_DEVICE_OK = 0
+MOE_DEVICE_NONFINITE_SCORE = 1
+MOE_DEVICE_PIPELINE_TIMEOUT = 2
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32),
+                ("n_experts", ctypes.c_int32), ("d_expert", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("d_shared", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("gating_mode", ctypes.c_int32),
+                ("capacity_factor", ctypes.c_float), ("aux_alpha", ctypes.c_float)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if libmoe.so was not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m mixture_experts_layer_capacity_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, cfgp = ctypes.c_void_p, ctypes.POINTER(MoeConfig)
+        L.moe_workspace_size.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_workspace_size.restype = ctypes.c_int
+        L.moe_capacity.argtypes = [cfgp]
+        L.moe_capacity.restype = ctypes.c_int64
+        L.moe_forward.argtypes = [cfgp] + [vp] * 18 + [ctypes.c_size_t, vp]
+        L.moe_forward.restype = ctypes.c_int
+        L.moe_read_device_status.argtypes = [cfgp, vp, vp, ctypes.POINTER(ctypes.c_int32)]
+        L.moe_read_device_status.restype = ctypes.c_int
+        L.moe_status_string.argtypes = [ctypes.c_int]
+        L.moe_status_string.restype = ctypes.c_char_p
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def make_config(T, d_model, n_experts, d_expert, top_k, d_shared=0, dtype="bf16",
+                gating_mode=0, capacity_factor=0.0, aux_alpha=0.01) -> MoeConfig:
+    dt = {"bf16": MOE_DTYPE_BF16, "fp32": MOE_DTYPE_FP32}.get(dtype, dtype)
+    return MoeConfig(int(T), int(d_model), int(n_experts), int(d_expert), int(top_k),
+                     int(d_shared), int(dt), int(gating_mode), float(capacity_factor),
+                     float(aux_alpha))
+
+
+def config_of(w) -> MoeConfig:
+    """MoeConfig of a workloads.Workload."""
+    return make_config(w.T, w.D, w.E, w.F, w.k, w.S, w.dtype, w.mode, w.gamma, w.alpha)
+
+
+def workspace_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t(0)
+    st = lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_workspace_size")
+    return int(n.value)
+
+
+def capacity(cfg: MoeConfig) -> int:
+    return int(lib().moe_capacity(ctypes.byref(cfg)))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    if isinstance(a, torch.Tensor):
+        if not a.is_contiguous():
+            raise ValueError("tensors passed to libmoe must be contiguous")
+        return a.data_ptr()
+    raise TypeError(f"unsupported argument type {type(a)}")
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def moe_forward(cfg: MoeConfig, x, W_r, router_bias, W_gate, W_up, W_down,
+                Ws_gate, Ws_up, Ws_down, y, router_logits, topk_idx, topk_w,
+                dropped_mask, expert_counts, kept_counts, aux_loss, workspace,
+                workspace_bytes=None, stream=None) -> None:
+    """Same arguments as the C function; tensors or raw device pointers.
+    Raises MoeError on a non-OK status."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    args = [x, W_r, router_bias, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y,
+            router_logits, topk_idx, topk_w, dropped_mask, expert_counts, kept_counts,
+            aux_loss, workspace]
+    st = lib().moe_forward(ctypes.byref(cfg), *[_ptr(a) for a in args],
+                           ctypes.c_size_t(int(workspace_bytes)), _stream(stream))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_forward")
+
+
+def read_device_status(cfg: MoeConfig, workspace, stream=None) -> int:
+    """Synchronises the stream and returns the device status code."""
+    code = ctypes.c_int32(0)
+    st = lib().moe_read_device_status(ctypes.byref(cfg), _ptr(workspace), _stream(stream),
+                                      ctypes.byref(code))
+    if st not in (MOE_OK, MOE_ERR_DEVICE_STATUS):
+        raise MoeError(st, "moe_read_device_status")
+    return int(code.value)
+
+
+# ---------------------------------------------------------------- convenience
+def alloc_outputs(cfg: MoeConfig, device="cuda"):
+    """Output tensors and workspace for one call, allocated with torch."""
+    T, D, E, k = cfg.T, cfg.d_model, cfg.n_experts, cfg.top_k
+    dt = torch.bfloat16 if cfg.dtype == MOE_DTYPE_BF16 else torch.float32
+    ws_bytes = workspace_size(cfg)
+    return dict(
+        y=torch.empty((T, D), dtype=dt, device=device),
+        router_logits=torch.empty((T, E), dtype=torch.float32, device=device),
+        topk_idx=torch.empty((T, k), dtype=torch.int32, device=device),
+        topk_w=torch.empty((T, k), dtype=torch.float32, device=device),
+        dropped_mask=torch.empty((T, k), dtype=torch.uint8, device=device),
+        expert_counts=torch.empty((E,), dtype=torch.int32, device=device),
+        kept_counts=torch.empty((E,), dtype=torch.int32, device=device),
+        aux_loss=torch.empty((1,), dtype=torch.float32, device=device),
+        workspace=torch.empty((max(ws_bytes, 256),), dtype=torch.uint8, device=device),
+    )
+
+
+def forward(cfg: MoeConfig, inputs: dict, outs: dict | None = None, stream=None) -> dict:
+    """Runs the layer on `inputs` (keys as workloads.make_inputs returns) and
+    returns the output dict (allocated if not given)."""
+    if outs is None:
+        outs = alloc_outputs(cfg, inputs["x"].device)
+    moe_forward(cfg, inputs["x"], inputs["W_r"], inputs.get("b_r"), inputs["W_gate"],
+                inputs["W_up"], inputs["W_down"], inputs.get("Ws_gate"), inputs.get("Ws_up"),
+                inputs.get("Ws_down"), outs["y"], outs["router_logits"], outs["topk_idx"],
+                outs["topk_w"], outs["dropped_mask"], outs["expert_counts"],
+                outs["kept_counts"], outs["aux_loss"], outs["workspace"], stream=stream)
+    return outs

@@ -1,0 +1,243 @@
+// moe_api.cu -- the C ABI of libmoe.so (declared in include/moe.h):
+// argument validation, capacity, workspace layout, and the launch sequence
+//   router -> gate -> scan/finalize -> scatter -> experts -> combine
+// on the caller's stream, with no host synchronisation.
+#include <cmath>
+#include <cstring>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+moe_status validate_config(const moe_config *c)
+{
+    if (!c)
+        return MOE_ERR_INVALID_ARG;
+    if (c->T < 0 || c->d_model < 1 || c->d_expert < 1 || c->d_shared < 0 || c->n_experts < 1 ||
+        c->top_k < 1 || c->top_k > c->n_experts)
+        return MOE_ERR_INVALID_ARG;
+    if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_FP32)
+        return MOE_ERR_INVALID_ARG;
+    if (c->gating_mode < MOE_GATE_SOFTMAX_SELECTED || c->gating_mode > MOE_GATE_SOFTMAX_ALL_RENORM)
+        return MOE_ERR_INVALID_ARG;
+    if (std::isnan(c->capacity_factor) || std::isinf(c->capacity_factor) ||
+        !std::isfinite(c->aux_alpha))
+        return MOE_ERR_INVALID_ARG;
+    if (c->n_experts > kMaxExperts || c->top_k > kMaxTopK)
+        return MOE_ERR_UNSUPPORTED;
+    if ((long long)c->T * c->top_k >= (1ll << 31))
+        return MOE_ERR_UNSUPPORTED;
+    if (c->dtype == MOE_DTYPE_BF16) {
+        if (c->d_model % 64 || c->d_expert % 64 || c->d_shared % 64)
+            return MOE_ERR_UNSUPPORTED;
+    } else {
+        // the SIMT path launches one grid row per 8 output rows
+        if ((long long)c->T * c->top_k > 500000)
+            return MOE_ERR_UNSUPPORTED;
+    }
+    return MOE_OK;
+}
+
+// C = ceil(capacity_factor * T * k / E) in double; -1 when dropless.
+int64_t capacity_of(const moe_config *c)
+{
+    if (!(c->capacity_factor > 0.0f))
+        return -1;
+    return (int64_t)std::ceil((double)c->capacity_factor * (double)((int64_t)c->T * c->top_k) /
+                              (double)c->n_experts);
+}
+
+WorkspaceLayout layout_of(const moe_config *c)
+{
+    WorkspaceLayout L{};
+    const int64_t T = c->T, E = c->n_experts, k = c->top_k;
+    const int64_t D = c->d_model, F = c->d_expert, S = c->d_shared;
+    const size_t esz = c->dtype == MOE_DTYPE_BF16 ? 2 : 4;
+    L.nchunk = (int)((T + kChunk - 1) / kChunk);
+    L.C = capacity_of(c);
+    const int64_t TK = T * k;
+    L.R_max = L.C < 0 ? TK : std::min<int64_t>(TK, E * L.C);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 1024);
+        return o;
+    };
+    L.status = take(64);
+    L.hist = take(sizeof(int32_t) * E * L.nchunk);
+    L.ppart = take(sizeof(float) * E * L.nchunk);
+    L.rank = take((size_t)TK);
+    L.psum = take(sizeof(double) * E);
+    L.seg_off = take(sizeof(int32_t) * (E + 1));
+    L.mtile = take(sizeof(int32_t) * (E + 1));
+    L.row_of = take(sizeof(int32_t) * TK);
+    L.x_perm = take(esz * L.R_max * D);
+    L.h = take(esz * L.R_max * F);
+    L.z = take(esz * L.R_max * D);
+    L.hs = take(S > 0 ? esz * T * S : 0);
+    L.zs = take(S > 0 ? esz * T * D : 0);
+    L.total = off;
+    return L;
+}
+
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 1;
+    if (dev < 64 && cached[dev] > 0)
+        return cached[dev];
+    int n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        n = 1;
+    if (dev < 64)
+        cached[dev] = n;
+    return n;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status moe_workspace_size(const moe_config *cfg, size_t *bytes)
+{
+    if (!bytes)
+        return MOE_ERR_INVALID_ARG;
+    const moe_status st = validate_config(cfg);
+    if (st != MOE_OK)
+        return st;
+    *bytes = layout_of(cfg).total;
+    return MOE_OK;
+}
+
+int64_t moe_capacity(const moe_config *cfg)
+{
+    if (validate_config(cfg) != MOE_OK)
+        return -1;
+    return capacity_of(cfg);
+}
+
+moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r,
+                       const float *router_bias, const void *W_gate, const void *W_up,
+                       const void *W_down, const void *Ws_gate, const void *Ws_up,
+                       const void *Ws_down, void *y, float *router_logits, int32_t *topk_idx,
+                       float *topk_w, uint8_t *dropped_mask, int32_t *expert_counts,
+                       int32_t *kept_counts, float *aux_loss, void *workspace,
+                       size_t workspace_bytes, cudaStream_t stream)
+{
+    moe_status st = validate_config(cfg);
+    if (st != MOE_OK)
+        return st;
+    const moe_config &c = *cfg;
+    if (!expert_counts || !kept_counts || !aux_loss)
+        return MOE_ERR_INVALID_ARG;
+    // with T == 0 nothing per token or per weight is touched (empty tensors
+    // may have null data pointers)
+    if (c.T > 0) {
+        if (!x || !W_r || !W_gate || !W_up || !W_down || !y || !router_logits || !topk_idx ||
+            !topk_w || !dropped_mask)
+            return MOE_ERR_INVALID_ARG;
+        if (c.d_shared > 0 && (!Ws_gate || !Ws_up || !Ws_down))
+            return MOE_ERR_INVALID_ARG;
+    }
+    const WorkspaceLayout L = layout_of(cfg);
+    if (!workspace || workspace_bytes < L.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MOE_ERR_WORKSPACE;
+    if (c.dtype == MOE_DTYPE_BF16) {
+        // tensor-map bases and 16-byte vector accesses
+        if (!aligned16(x) || !aligned16(W_r) || !aligned16(W_gate) || !aligned16(W_up) ||
+            !aligned16(W_down) || !aligned16(y) ||
+            (c.d_shared > 0 && (!aligned16(Ws_gate) || !aligned16(Ws_up) || !aligned16(Ws_down))))
+            return MOE_ERR_INVALID_ARG;
+    }
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    const int E = c.n_experts;
+
+    auto cuda_ok = [](cudaError_t e) { return e == cudaSuccess; };
+    if (!cuda_ok(cudaMemsetAsync(status, 0, 64, stream)))
+        return MOE_ERR_CUDA;
+    if (c.T == 0) {
+        if (!cuda_ok(cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, stream)) ||
+            !cuda_ok(cudaMemsetAsync(kept_counts, 0, sizeof(int32_t) * E, stream)) ||
+            !cuda_ok(cudaMemsetAsync(aux_loss, 0, sizeof(float), stream)))
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+
+    // 1. router scores
+    cudaError_t err;
+    if (c.dtype == MOE_DTYPE_BF16 && c.T >= 512)
+        err = launch_router_tc(c, x, W_r, router_logits, status, stream);
+    else
+        err = launch_router_simt(c, x, W_r, router_logits, stream);
+    if (!cuda_ok(err))
+        return MOE_ERR_CUDA;
+    // 2. softmax, top-k, gate weights, chunk statistics
+    if (!cuda_ok(launch_gate(c, L, ws, router_logits, router_bias, topk_idx, topk_w, stream)))
+        return MOE_ERR_CUDA;
+    // 3. demand counts, capacity, segments, balance loss
+    if (!cuda_ok(launch_scan_finalize(c, L, ws, expert_counts, kept_counts, aux_loss, stream)))
+        return MOE_ERR_CUDA;
+    // 4. positions, drops, gather of x into expert order
+    if (!cuda_ok(launch_scatter(c, L, ws, x, topk_idx, dropped_mask, stream)))
+        return MOE_ERR_CUDA;
+    // 5. experts (routed segments and the shared expert)
+    if (c.dtype == MOE_DTYPE_BF16)
+        err = launch_experts_tc(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
+                                stream);
+    else
+        err = launch_experts_simt(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
+                                  stream);
+    if (!cuda_ok(err))
+        return MOE_ERR_CUDA;
+    // 6. weighted combine (+ shared expert)
+    if (!cuda_ok(launch_combine(c, L, ws, topk_w, y, stream)))
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_read_device_status(const moe_config *cfg, const void *workspace,
+                                  cudaStream_t stream, int32_t *code)
+{
+    const moe_status st = validate_config(cfg);
+    if (st != MOE_OK)
+        return st;
+    if (!workspace || !code)
+        return MOE_ERR_INVALID_ARG;
+    const WorkspaceLayout L = layout_of(cfg);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, static_cast<const uint8_t *>(workspace) + L.status, sizeof(v),
+                        cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    *code = v;
+    return v == MOE_DEVICE_OK ? MOE_OK : MOE_ERR_DEVICE_STATUS;
+}
+
+const char *moe_status_string(moe_status s)
+{
+    switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: unsupported shape or option";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small or misaligned";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+    case MOE_ERR_DEVICE_STATUS: return "MOE_ERR_DEVICE_STATUS: a kernel reported an error";
+    }
+    return "unknown moe_status";
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// moe_common.cuh -- small device helpers shared by the SIMT kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace moe {
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename TE>
+__device__ __forceinline__ TE from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v)
+{
+    return __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float silu_f32(float a) { return a / (1.0f + __expf(-a)); }
+
+// Sum over the warp; every lane receives lane 0's result, so all lanes hold
+// bit-identical values whatever order the butterfly used.
+__device__ __forceinline__ float warp_sum_bcast(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return __shfl_sync(0xffffffffu, v, 0);
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ void set_status(int32_t *status, int32_t code)
+{
+    if (status)
+        atomicCAS(status, 0, code);
+}
+
+}  // namespace moe

@@ -1,0 +1,89 @@
+// moe_experts_simt.cu -- the expert feed-forward networks on SIMT cores, for
+// the fp32 dtype (exact-precision checks and small layers).  One thread per
+// output element, fp32 accumulation:
+//   h[r][f] = silu(sum_d x_perm[r][d] W_gate[e][f][d]) * (sum_d x_perm[r][d] W_up[e][f][d])
+//   z[r][d] = sum_f h[r][f] W_down[e][d][f]
+// where e is the expert whose segment holds row r ("Mixture of Experts: More
+// Parameters, Same FLOPs", 'An MoE tiny GPT': the SwiGLU expert).  The shared
+// expert is the same computation over all T rows of x with one segment.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+// Largest segment e in [0, nseg) with seg_off[e] <= r (skips empty segments).
+__device__ __forceinline__ int segment_of(const int32_t *seg_off, int nseg, int r)
+{
+    int lo = 0, hi = nseg;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (seg_off[mid] <= r)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+template <bool SWIGLU>
+__global__ void simt_seg_gemm_f32_kernel(const float *__restrict__ A, const float *__restrict__ B0,
+                                         const float *__restrict__ B1, long long b_seg_elems,
+                                         int N, int K, const int32_t *__restrict__ seg_off,
+                                         int nseg, int dense_rows, float *__restrict__ out)
+{
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    const int r = blockIdx.y * blockDim.y + threadIdx.y;
+    const int rows = seg_off ? seg_off[nseg] : dense_rows;
+    if (r >= rows || n >= N)
+        return;
+    const int e = seg_off ? segment_of(seg_off, nseg, r) : 0;
+    const float *a = A + (size_t)r * K;
+    const float *b0 = B0 + (size_t)e * b_seg_elems + (size_t)n * K;
+    float g = 0.f, u = 0.f;
+    if (SWIGLU) {
+        const float *b1 = B1 + (size_t)e * b_seg_elems + (size_t)n * K;
+        for (int kk = 0; kk < K; ++kk) {
+            const float av = a[kk];
+            g = fmaf(av, __ldg(b0 + kk), g);
+            u = fmaf(av, __ldg(b1 + kk), u);
+        }
+        out[(size_t)r * N + n] = (g / (1.0f + expf(-g))) * u;
+    } else {
+        for (int kk = 0; kk < K; ++kk)
+            g = fmaf(a[kk], __ldg(b0 + kk), g);
+        out[(size_t)r * N + n] = g;
+    }
+}
+
+cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                                const void *x, const void *W_gate, const void *W_up,
+                                const void *W_down, const void *Ws_gate, const void *Ws_up,
+                                const void *Ws_down, cudaStream_t stream)
+{
+    if (c.dtype != MOE_DTYPE_FP32)
+        return cudaErrorInvalidValue;
+    const int D = c.d_model, F = c.d_expert, S = c.d_shared, E = c.n_experts;
+    const int32_t *seg = reinterpret_cast<const int32_t *>(ws + L.seg_off);
+    float *xp = reinterpret_cast<float *>(ws + L.x_perm);
+    float *h = reinterpret_cast<float *>(ws + L.h);
+    float *z = reinterpret_cast<float *>(ws + L.z);
+    const dim3 block(32, 8);
+    const unsigned rb = (unsigned)((L.R_max + 7) / 8);
+    simt_seg_gemm_f32_kernel<true><<<dim3((F + 31) / 32, rb), block, 0, stream>>>(
+        xp, (const float *)W_gate, (const float *)W_up, (long long)F * D, F, D, seg, E, 0, h);
+    simt_seg_gemm_f32_kernel<false><<<dim3((D + 31) / 32, rb), block, 0, stream>>>(
+        h, (const float *)W_down, nullptr, (long long)D * F, D, F, seg, E, 0, z);
+    if (S > 0) {
+        float *hs = reinterpret_cast<float *>(ws + L.hs);
+        float *zs = reinterpret_cast<float *>(ws + L.zs);
+        const unsigned tb = (unsigned)((c.T + 7) / 8);
+        simt_seg_gemm_f32_kernel<true><<<dim3((S + 31) / 32, tb), block, 0, stream>>>(
+            (const float *)x, (const float *)Ws_gate, (const float *)Ws_up, 0, S, D, nullptr, 1,
+            c.T, hs);
+        simt_seg_gemm_f32_kernel<false><<<dim3((D + 31) / 32, tb), block, 0, stream>>>(
+            hs, (const float *)Ws_down, nullptr, 0, D, S, nullptr, 1, c.T, zs);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

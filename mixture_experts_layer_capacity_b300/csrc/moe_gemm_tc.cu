@@ -1,0 +1,586 @@
+// moe_gemm_tc.cu -- tensor-core GEMMs of the MoE layer for bf16 (sm_103a):
+//   router:  logits[T,E]  = x[T,D] . W_r[E,D]^T                  (fp32 out)
+//   GEMM1:   h[r,F]       = silu(x_perm[r,:] . W_gate[e]^T) * (x_perm[r,:] . W_up[e]^T)
+//   GEMM2:   z[r,D]       = h[r,:] . W_down[e]^T
+// for every row r of expert e's segment, plus the same two GEMMs over all T
+// rows for the shared expert ("Mixture of Experts: More Parameters, Same
+// FLOPs", 'An MoE tiny GPT': the SwiGLU expert; "Mixture of Experts"
+// (module 17), 17.2 equation: the shared expert on every token).
+//
+// Design (one CTA per SM, persistent over a tile list built on the device):
+//   - tile = 128 rows of one segment x BN output columns; tiles are ordered
+//     segment-major, then column tile, then row tile, so the CTAs running at
+//     the same time share weight tiles through L2;
+//   - warp 0: TMA producer (128-byte-swizzled K-major boxes of 64 elements)
+//     into a STAGES-deep shared-memory ring guarded by mbarriers;
+//   - warp 1: allocates TMEM and issues tcgen05.mma (M=128, N=BN*NB, K=16)
+//     into one of two TMEM accumulators, committing to the ring's "empty"
+//     barriers and to the accumulator's "full" barrier;
+//   - warps 2-5: epilogue; each thread owns one accumulator row (TMEM lane),
+//     loads it with tcgen05.ld, applies SiLU*up (GEMM1) or converts, and
+//     stores straight to global memory, then frees the accumulator so the
+//     next tile's MMAs overlap this epilogue.
+// For GEMM1 the gate and up tiles of the same columns are stacked in one
+// 256-row B operand, so one N=256 MMA produces both accumulators.
+// Every mbarrier wait is bounded; on timeout the CTA records
+// MOE_DEVICE_PIPELINE_TIMEOUT, drains its own copies and MMAs, frees TMEM and
+// returns.
+#include <algorithm>
+#include <cstdio>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+enum { EPI_F32 = 0, EPI_BF16 = 1, EPI_SWIGLU = 2 };
+
+struct TcParams {
+    const int32_t *seg_off;  // grouped: [nseg+1] first A row of each segment; null = dense
+    const int32_t *mtile;    // grouped: [nseg+1] prefix sum of 128-row tiles per segment
+    int nseg;
+    int dense_rows;          // rows of A when dense
+    int K;                   // reduction length (multiple of 64)
+    int n_tiles;             // output column tiles per segment
+    int N_valid;             // output columns that exist
+    int b_seg_rows;          // B rows per segment (F or D), 0 when dense
+    void *out;
+    long long ld_out;        // output row stride, elements
+    int32_t *status;
+};
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any tile
+constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s
+constexpr int kThreads = 192;
+
+template <int BN, int NB, int STAGES>
+struct TcShape {
+    static constexpr int UMMA_N = BN * NB;
+    static constexpr int A_BYTES = kTileM * 64 * 2;
+    static constexpr int B_BYTES = BN * 64 * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
+    static constexpr int TMEM_COLS = 2 * UMMA_N <= 32    ? 32
+                                     : 2 * UMMA_N <= 64  ? 64
+                                     : 2 * UMMA_N <= 128 ? 128
+                                     : 2 * UMMA_N <= 256 ? 256
+                                                         : 512;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
+    static_assert(UMMA_N % 16 == 0 && UMMA_N >= 16 && UMMA_N <= 256, "UMMA N");
+    static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+struct TileInfo {
+    int a_row0, rows, seg, n_idx;
+};
+
+__device__ __forceinline__ int tile_count(const TcParams &p)
+{
+    if (!p.mtile)
+        return ((p.dense_rows + kTileM - 1) / kTileM) * p.n_tiles;
+    return p.mtile[p.nseg] * p.n_tiles;
+}
+
+__device__ __forceinline__ TileInfo tile_info(const TcParams &p, int g)
+{
+    TileInfo ti;
+    if (!p.mtile) {
+        const int mt = (p.dense_rows + kTileM - 1) / kTileM;
+        ti.n_idx = g / mt;
+        const int m = g - ti.n_idx * mt;
+        ti.seg = 0;
+        ti.a_row0 = m * kTileM;
+        ti.rows = min(kTileM, p.dense_rows - ti.a_row0);
+        return ti;
+    }
+    int lo = 0, hi = p.nseg;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.mtile[mid] * p.n_tiles <= g)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const int mt0 = p.mtile[lo], mt_e = p.mtile[lo + 1] - mt0;
+    const int local = g - mt0 * p.n_tiles;
+    ti.n_idx = local / mt_e;
+    const int m = local - ti.n_idx * mt_e;
+    ti.seg = lo;
+    const int s0 = p.seg_off[lo];
+    ti.a_row0 = s0 + m * kTileM;
+    ti.rows = min(kTileM, p.seg_off[lo + 1] - ti.a_row0);
+    return ti;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Stores 32 bf16 values (as 16 packed words) of one output row.
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const uint32_t (&pk)[16],
+                                               int col, int n_valid)
+{
+    if (col + 32 <= n_valid) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&pk[i]);
+            if (col + 2 * i < n_valid)
+                dst[2 * i] = v.x;
+            if (col + 2 * i + 1 < n_valid)
+                dst[2 * i + 1] = v.y;
+        }
+    }
+}
+
+template <int BN, int NB, int EPI, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
+                   const __grid_constant__ CUtensorMap mB1, const TcParams p)
+{
+    using S = TcShape<BN, NB, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * S::STAGE_BYTES);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *tfull = bars + 2 * STAGES;
+    uint64_t *tempty = bars + 2 * STAGES + 2;
+    uint64_t *mma_done = bars + 2 * STAGES + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4 * 32);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&mA);
+        tma_prefetch_desc(&mB0);
+        if (NB == 2)
+            tma_prefetch_desc(&mB1);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, S::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int ntiles = tile_count(p);
+    const int nk = (p.K + 63) / 64;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int s = 0;
+            uint32_t ph = 0;
+            long long fills = 0;
+            bool ok = true;
+            for (int g = blockIdx.x; g < ntiles && ok; g += gridDim.x) {
+                const TileInfo ti = tile_info(p, g);
+                const int b_row = ti.seg * p.b_seg_rows + ti.n_idx * BN;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sa = smem + s * S::STAGE_BYTES;
+                    uint8_t *sb = sa + S::A_BYTES;
+                    mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
+                    tma_load_2d(sa, &mA, &full[s], kb * 64, ti.a_row0);
+                    tma_load_2d(sb, &mB0, &full[s], kb * 64, b_row);
+                    if (NB == 2)
+                        tma_load_2d(sb + S::B_BYTES, &mB1, &full[s], kb * 64, b_row);
+                    ++fills;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
+                // wait (bounded) for this CTA's copies still in flight
+                const long long first = fills > STAGES ? fills - STAGES : 0;
+                for (long long f = first; f < fills; ++f)
+                    mbar_wait(&full[f % STAGES], (uint32_t)((f / STAGES) & 1), nullptr,
+                              kDrainLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(kTileM, S::UMMA_N);
+            int s = 0;
+            uint32_t ph = 0, b = 0, tph = 0;
+            bool ok = true;
+            for (int g = blockIdx.x; g < ntiles && ok; g += gridDim.x) {
+                if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * S::UMMA_N;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(&full[s], ph, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = smem_u32(smem + s * S::STAGE_BYTES);
+                    const uint64_t adesc = sdesc_kmajor_sw128(sa);
+                    const uint64_t bdesc = sdesc_kmajor_sw128(sa + S::A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                  (kb > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(&empty[s]);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                umma_commit(&tfull[b]);
+                b ^= 1u;
+                if (b == 0)
+                    tph ^= 1u;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
+            }
+            // all MMAs of this CTA complete before TMEM is released
+            umma_commit(mma_done);
+            mbar_wait(mma_done, 0, nullptr, kDrainLimitNs);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int q = warp & 3;             // TMEM lane quarter this warp may access
+        const int r = q * 32 + lane;        // accumulator row of this thread
+        uint32_t b = 0, tph = 0;
+        for (int g = blockIdx.x; g < ntiles; g += gridDim.x) {
+            const TileInfo ti = tile_info(p, g);
+            if (!mbar_wait(&tfull[b], tph, abort_flag, kWaitLimitNs)) {
+                *abort_flag = 1;
+                set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + b * S::UMMA_N + ((uint32_t)(q * 32) << 16);
+            const bool row_ok = r < ti.rows;
+            const long long orow = (long long)ti.a_row0 + r;
+            if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t gv[32], uv[32];
+                    tmem_ld32(taddr + c0, gv);
+                    tmem_ld32(taddr + BN + c0, uv);
+                    tmem_wait_ld();
+                    if (row_ok) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float g0 = __uint_as_float(gv[2 * i]);
+                            const float g1 = __uint_as_float(gv[2 * i + 1]);
+                            const float u0 = __uint_as_float(uv[2 * i]);
+                            const float u1 = __uint_as_float(uv[2 * i + 1]);
+                            pk[i] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
+                        }
+                        const int col = ti.n_idx * BN + c0;
+                        __nv_bfloat16 *dst =
+                            reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * p.ld_out + col;
+                        store_row_bf16(dst, pk, col, p.N_valid);
+                    }
+                }
+            } else if constexpr (EPI == EPI_BF16) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + c0, v);
+                    tmem_wait_ld();
+                    if (row_ok) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]),
+                                                __uint_as_float(v[2 * i + 1]));
+                        const int col = ti.n_idx * BN + c0;
+                        __nv_bfloat16 *dst =
+                            reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * p.ld_out + col;
+                        store_row_bf16(dst, pk, col, p.N_valid);
+                    }
+                }
+            } else {
+                constexpr int CH = BN < 32 ? 16 : 32;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += CH) {
+                    uint32_t v[32];
+                    if constexpr (CH == 16) {
+                        uint32_t v16[16];
+                        tmem_ld16(taddr + c0, v16);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            v[i] = v16[i];
+                    } else {
+                        tmem_ld32(taddr + c0, v);
+                        tmem_wait_ld();
+                    }
+                    if (row_ok) {
+                        const int col = ti.n_idx * BN + c0;
+                        float *dst = reinterpret_cast<float *>(p.out) + orow * p.ld_out + col;
+#pragma unroll
+                        for (int i = 0; i < CH; ++i)
+                            if (col + i < p.N_valid)
+                                dst[i] = __uint_as_float(v[i]);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&tempty[b]);
+            b ^= 1u;
+            if (b == 0)
+                tph ^= 1u;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, S::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, k] (k contiguous), boxes of 64 x box_rows, 128-byte
+// swizzle; out-of-range elements read as zero.
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t k, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn || rows == 0 || k == 0 || (reinterpret_cast<uintptr_t>(base) & 15u))
+        return false;
+    cuuint64_t dims[2] = {k, rows};
+    cuuint64_t strides[1] = {k * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int NB, int EPI, int STAGES>
+cudaError_t launch_tc(const CUtensorMap &mA, const CUtensorMap &mB0, const CUtensorMap &mB1,
+                      const TcParams &p, long long max_tiles, cudaStream_t stream)
+{
+    using S = TcShape<BN, NB, STAGES>;
+    auto kern = tc_gemm_kernel<BN, NB, EPI, STAGES>;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    static uint64_t configured = 0;  // bit per device
+    if (dev < 64 && !(configured & (1ull << dev))) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   S::SMEM_BYTES);
+        if (err != cudaSuccess)
+            return err;
+        configured |= 1ull << dev;
+    }
+    const long long grid = std::min<long long>(max_tiles, sm_count());
+    if (grid < 1)
+        return cudaSuccess;
+    kern<<<(unsigned)grid, kThreads, S::SMEM_BYTES, stream>>>(mA, mB0, mB1, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r,
+                             float *logits, int32_t *status, cudaStream_t stream)
+{
+    const int E = c.n_experts, D = c.d_model, T = c.T;
+    const int bn = E <= 16 ? 16 : E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256;
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, x, (uint64_t)T, (uint64_t)D, kTileM) ||
+        !make_map(&mB, W_r, (uint64_t)E, (uint64_t)D, (uint32_t)bn))
+        return cudaErrorInvalidValue;
+    TcParams p{};
+    p.seg_off = nullptr;
+    p.mtile = nullptr;
+    p.nseg = 1;
+    p.dense_rows = T;
+    p.K = D;
+    p.n_tiles = 1;
+    p.N_valid = E;
+    p.b_seg_rows = 0;
+    p.out = logits;
+    p.ld_out = E;
+    p.status = status;
+    const long long tiles = (T + kTileM - 1) / kTileM;
+    switch (bn) {
+    case 16: return launch_tc<16, 1, EPI_F32, 6>(mA, mB, mB, p, tiles, stream);
+    case 32: return launch_tc<32, 1, EPI_F32, 6>(mA, mB, mB, p, tiles, stream);
+    case 64: return launch_tc<64, 1, EPI_F32, 6>(mA, mB, mB, p, tiles, stream);
+    case 128: return launch_tc<128, 1, EPI_F32, 6>(mA, mB, mB, p, tiles, stream);
+    default: return launch_tc<256, 1, EPI_F32, 4>(mA, mB, mB, p, tiles, stream);
+    }
+}
+
+cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                              const void *x, const void *W_gate, const void *W_up,
+                              const void *W_down, const void *Ws_gate, const void *Ws_up,
+                              const void *Ws_down, cudaStream_t stream)
+{
+    const int D = c.d_model, F = c.d_expert, S = c.d_shared, E = c.n_experts, T = c.T;
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    const int32_t *seg = reinterpret_cast<const int32_t *>(ws + L.seg_off);
+    const int32_t *mtile = reinterpret_cast<const int32_t *>(ws + L.mtile);
+    void *xp = ws + L.x_perm, *h = ws + L.h, *z = ws + L.z;
+    const long long R = L.R_max;
+    const long long mt_bound = R / kTileM + E;  // >= sum_e ceil(kept_e / 128)
+    const bool wide_down = D > 1024;           // 256-column tiles for the down projection
+    cudaError_t err;
+
+    // GEMM1 (routed): h = silu(x_perm W_gate^T) * (x_perm W_up^T)
+    {
+        CUtensorMap mA, mG, mU;
+        if (!make_map(&mA, xp, (uint64_t)R, (uint64_t)D, kTileM) ||
+            !make_map(&mG, W_gate, (uint64_t)E * F, (uint64_t)D, 128) ||
+            !make_map(&mU, W_up, (uint64_t)E * F, (uint64_t)D, 128))
+            return cudaErrorInvalidValue;
+        TcParams p{};
+        p.seg_off = seg;
+        p.mtile = mtile;
+        p.nseg = E;
+        p.K = D;
+        p.n_tiles = (F + 127) / 128;
+        p.N_valid = F;
+        p.b_seg_rows = F;
+        p.out = h;
+        p.ld_out = F;
+        p.status = status;
+        err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_bound * p.n_tiles, stream);
+        if (err != cudaSuccess)
+            return err;
+    }
+    // GEMM2 (routed): z = h W_down^T
+    {
+        const int bn = wide_down ? 256 : 128;
+        CUtensorMap mA, mB;
+        if (!make_map(&mA, h, (uint64_t)R, (uint64_t)F, kTileM) ||
+            !make_map(&mB, W_down, (uint64_t)E * D, (uint64_t)F, (uint32_t)bn))
+            return cudaErrorInvalidValue;
+        TcParams p{};
+        p.seg_off = seg;
+        p.mtile = mtile;
+        p.nseg = E;
+        p.K = F;
+        p.n_tiles = (D + bn - 1) / bn;
+        p.N_valid = D;
+        p.b_seg_rows = D;
+        p.out = z;
+        p.ld_out = D;
+        p.status = status;
+        err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt_bound * p.n_tiles, stream)
+                        : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt_bound * p.n_tiles, stream);
+        if (err != cudaSuccess)
+            return err;
+    }
+    if (S > 0) {
+        void *hs = ws + L.hs, *zs = ws + L.zs;
+        const long long mt = (T + kTileM - 1) / kTileM;
+        {
+            CUtensorMap mA, mG, mU;
+            if (!make_map(&mA, x, (uint64_t)T, (uint64_t)D, kTileM) ||
+                !make_map(&mG, Ws_gate, (uint64_t)S, (uint64_t)D, 128) ||
+                !make_map(&mU, Ws_up, (uint64_t)S, (uint64_t)D, 128))
+                return cudaErrorInvalidValue;
+            TcParams p{};
+            p.nseg = 1;
+            p.dense_rows = T;
+            p.K = D;
+            p.n_tiles = (S + 127) / 128;
+            p.N_valid = S;
+            p.out = hs;
+            p.ld_out = S;
+            p.status = status;
+            err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt * p.n_tiles, stream);
+            if (err != cudaSuccess)
+                return err;
+        }
+        {
+            const int bn = wide_down ? 256 : 128;
+            CUtensorMap mA, mB;
+            if (!make_map(&mA, hs, (uint64_t)T, (uint64_t)S, kTileM) ||
+                !make_map(&mB, Ws_down, (uint64_t)D, (uint64_t)S, (uint32_t)bn))
+                return cudaErrorInvalidValue;
+            TcParams p{};
+            p.nseg = 1;
+            p.dense_rows = T;
+            p.K = S;
+            p.n_tiles = (D + bn - 1) / bn;
+            p.N_valid = D;
+            p.out = zs;
+            p.ld_out = D;
+            p.status = status;
+            err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt * p.n_tiles, stream)
+                            : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt * p.n_tiles, stream);
+            if (err != cudaSuccess)
+                return err;
+        }
+    }
+    return cudaSuccess;
+}
+
+}  // namespace moe

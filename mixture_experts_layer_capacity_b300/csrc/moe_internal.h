@@ -1,0 +1,74 @@
+// moe_internal.h -- host-side internals of libmoe.so: workspace layout and
+// the kernel launchers the C ABI sequences.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kChunk = 32;       // tokens per routing chunk (one bit each in a 32-bit mask)
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+constexpr int kTileM = 128;      // rows per tensor-core tile (UMMA M)
+
+// Byte offsets of the scratch regions inside the caller's workspace.  Every
+// region starts on a 1024-byte boundary.
+struct WorkspaceLayout {
+    size_t status;   // int32[4]  device status word (+ padding)
+    size_t hist;     // int32[E][nchunk]  per-chunk expert counts, then exclusive bases
+    size_t ppart;    // float[E][nchunk]  per-chunk sums of softmax probabilities
+    size_t rank;     // uint8[T*k]        rank of an assignment among its chunk's tokens
+    size_t psum;     // double[E]         sum over tokens of the softmax probabilities
+    size_t seg_off;  // int32[E+1]        first x_perm row of each expert's segment
+    size_t mtile;    // int32[E+1]        prefix sum of 128-row tiles per segment
+    size_t row_of;   // int32[T*k]        x_perm row of an assignment, -1 if dropped
+    size_t x_perm;   // dtype[R_max, D]   token rows gathered in expert order
+    size_t h;        // dtype[R_max, F]   SwiGLU hidden rows of the routed experts
+    size_t z;        // dtype[R_max, D]   routed expert outputs (unweighted)
+    size_t hs;       // dtype[T, S]       shared-expert hidden rows
+    size_t zs;       // dtype[T, D]       shared-expert outputs
+    size_t total;
+    int64_t R_max;   // rows of x_perm: T*k dropless, else min(T*k, E*C)
+    int64_t C;       // capacity, -1 dropless
+    int nchunk;      // ceil(T / kChunk)
+};
+
+moe_status validate_config(const moe_config *cfg);
+int64_t capacity_of(const moe_config *cfg);
+WorkspaceLayout layout_of(const moe_config *cfg);
+
+// Launchers (all enqueue on `stream`; return cudaGetLastError()).
+cudaError_t launch_router_simt(const moe_config &c, const void *x, const void *W_r,
+                               float *logits, cudaStream_t stream);
+cudaError_t launch_gate(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                        float *logits, const float *bias, int32_t *topk_idx, float *topk_w,
+                        cudaStream_t stream);
+cudaError_t launch_scan_finalize(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                                 int32_t *expert_counts, int32_t *kept_counts, float *aux_loss,
+                                 cudaStream_t stream);
+cudaError_t launch_scatter(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                           const void *x, const int32_t *topk_idx, uint8_t *dropped_mask,
+                           cudaStream_t stream);
+cudaError_t launch_combine(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                           const float *topk_w, void *y, cudaStream_t stream);
+cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                                const void *x, const void *W_gate, const void *W_up,
+                                const void *W_down, const void *Ws_gate, const void *Ws_up,
+                                const void *Ws_down, cudaStream_t stream);
+
+// Tensor-core (tcgen05 + TMA) paths, bf16 only.  Return cudaErrorInvalidValue
+// if a tensor map cannot be encoded.
+cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r,
+                             float *logits, int32_t *status, cudaStream_t stream);
+cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                              const void *x, const void *W_gate, const void *W_up,
+                              const void *W_down, const void *Ws_gate, const void *Ws_up,
+                              const void *Ws_down, cudaStream_t stream);
+
+int sm_count();
+
+}  // namespace moe

@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/moe.h declares, and validates its arguments and
+computes the capacity on the host before touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import ROOT
+from mixture_experts_layer_capacity_b300 import binding as B
+from mixture_experts_layer_capacity_b300.workloads import WORKLOADS
+
+
+def _declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        txt = open(h).read()
+        names |= set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", txt))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared_symbols()
+    assert "moe_forward" in names and len(names) >= 5
+    L = B.lib()
+    for n in names:
+        assert hasattr(L, n), f"libmoe.so does not export {n}"
+
+
+def test_no_internal_symbols_leak():
+    out = os.popen(f"nm -D --defined-only {B.LIB_PATH}").read().split("\n")
+    exported = [l.split()[-1] for l in out if " T " in l]
+    assert all(n.startswith("moe_") for n in exported), exported
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_capacity_matches_oracle(name):
+    w = WORKLOADS[name]
+    cfg = B.config_of(w)
+    want = oracle.capacity(w.T, w.k, w.E, float(np.float32(w.gamma)))
+    assert B.capacity(cfg) == want
+
+
+@pytest.mark.parametrize("T,k,E,gamma", [(4096, 8, 64, 1.25), (4096, 1, 8, 1.0),
+                                         (1000, 2, 7, 1.1), (33, 3, 5, 0.3), (1, 1, 8, 2.0),
+                                         (100, 2, 4, 0.0), (100, 2, 4, -3.0)])
+def test_capacity_formula(T, k, E, gamma):
+    cfg = B.make_config(T, 64, E, 64, k, capacity_factor=gamma)
+    assert B.capacity(cfg) == oracle.capacity(T, k, E, float(np.float32(gamma)))
+
+
+def test_workspace_size_and_validation():
+    ok = B.make_config(4096, 512, 8, 2048, 1, capacity_factor=1.0)
+    n1 = B.workspace_size(ok)
+    assert n1 > 0
+    # more tokens never need less scratch
+    assert B.workspace_size(B.make_config(8192, 512, 8, 2048, 1, capacity_factor=1.0)) >= n1
+    bad = [
+        (dict(T=-1), B.MOE_ERR_INVALID_ARG),
+        (dict(top_k=0), B.MOE_ERR_INVALID_ARG),
+        (dict(top_k=9, n_experts=16), B.MOE_ERR_UNSUPPORTED),
+        (dict(top_k=3, n_experts=2), B.MOE_ERR_INVALID_ARG),
+        (dict(n_experts=257), B.MOE_ERR_UNSUPPORTED),
+        (dict(d_model=100), B.MOE_ERR_UNSUPPORTED),     # bf16 needs multiples of 64
+        (dict(d_expert=96), B.MOE_ERR_UNSUPPORTED),
+        (dict(d_shared=32), B.MOE_ERR_UNSUPPORTED),
+        (dict(gating_mode=3), B.MOE_ERR_INVALID_ARG),
+        (dict(dtype=7), B.MOE_ERR_INVALID_ARG),
+        (dict(capacity_factor=float("nan")), B.MOE_ERR_INVALID_ARG),
+    ]
+    base = dict(T=64, d_model=128, n_experts=8, d_expert=128, top_k=2)
+    for over, code in bad:
+        kw = dict(base)
+        kw.update(over)
+        cfg = B.make_config(**kw)
+        with pytest.raises(B.MoeError) as ei:
+            B.workspace_size(cfg)
+        assert ei.value.status == code, over
+    # fp32 accepts any sizes
+    assert B.workspace_size(B.make_config(10, 5, 3, 7, 2, dtype="fp32")) > 0
+
+
+def _call(cfg, ptrs, ws_bytes):
+    L = B.lib()
+    args = [ptrs.get(n) for n in ("x", "W_r", "b", "Wg", "Wu", "Wd", "Wsg", "Wsu", "Wsd", "y",
+                                  "logits", "idx", "w", "drop", "cnt", "kept", "aux", "ws")]
+    return L.moe_forward(ctypes.byref(cfg), *args, ctypes.c_size_t(ws_bytes), None)
+
+
+def test_forward_rejects_bad_arguments_before_launching():
+    cfg = B.make_config(64, 128, 8, 128, 2, d_shared=128)
+    need = B.workspace_size(cfg)
+    fake = {n: 4096 * (i + 1) for i, n in enumerate(
+        ("x", "W_r", "Wg", "Wu", "Wd", "Wsg", "Wsu", "Wsd", "y", "logits", "idx", "w",
+         "drop", "cnt", "kept", "aux"))}
+    fake["ws"] = 1 << 20
+    # a missing output
+    p = dict(fake)
+    p["y"] = None
+    assert _call(cfg, p, need) == B.MOE_ERR_INVALID_ARG
+    # shared expert declared but its weights missing
+    p = dict(fake)
+    p["Wsd"] = None
+    assert _call(cfg, p, need) == B.MOE_ERR_INVALID_ARG
+    # workspace too small / misaligned / missing
+    assert _call(cfg, fake, need - 1) == B.MOE_ERR_WORKSPACE
+    p = dict(fake)
+    p["ws"] = (1 << 20) + 128
+    assert _call(cfg, p, need) == B.MOE_ERR_WORKSPACE
+    p["ws"] = None
+    assert _call(cfg, p, need) == B.MOE_ERR_WORKSPACE
+    # bf16 tensors must be 16-byte aligned (tensor-map bases)
+    p = dict(fake)
+    p["x"] = 4096 + 8
+    assert _call(cfg, p, need) == B.MOE_ERR_INVALID_ARG
+    # invalid config
+    bad = B.make_config(64, 128, 8, 128, 0)
+    assert _call(bad, fake, need) == B.MOE_ERR_INVALID_ARG
+
+
+def test_status_strings():
+    for s in range(6):
+        assert B.status_string(s).startswith("MOE_")
+    assert "unknown" in B.status_string(42)

@@ -1,0 +1,163 @@
+"""CUDA path vs the CPU oracle, through the C ABI, on seeded inputs.
+
+Small layers span several tiles and ragged tails and are checked on every
+token; the benchmark-sized workloads are checked on all routing outputs and
+on a seeded sample of y rows, in the launch configuration the benchmark
+uses (one moe_forward call on the current stream)."""
+import numpy as np
+import pytest
+import torch
+
+import parity
+from mixture_experts_layer_capacity_b300 import binding as B
+from mixture_experts_layer_capacity_b300.workloads import WORKLOADS, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    # name, T, D, E, F, k, S, mode, gamma, bias
+    ("multi_tile_top2", 1000, 256, 8, 384, 2, 192, 0, 0.0, "none"),
+    ("ragged_cols_capacity", 777, 192, 16, 320, 4, 0, 1, 0.75, "normal_var2"),
+    ("simt_router_e64", 300, 128, 64, 128, 8, 256, 2, 1.0, "none"),
+    ("tc_router_e256_zipf", 2048, 512, 256, 128, 8, 0, 2, 0.0, "zipf1.1"),
+    ("top1_heavy_drops", 1536, 256, 8, 256, 1, 128, 1, 0.5, "normal_var2"),
+    ("k_equals_e", 640, 128, 4, 192, 4, 0, 0, 0.0, "none"),
+    ("ragged_chunk_t33", 33, 128, 8, 128, 2, 64, 0, 1.25, "none"),
+]
+
+
+def _w(name, T, D, E, F, k, S, mode, gamma, bias, dtype="bf16"):
+    return Workload(name, T=T, D=D, E=E, F=F, k=k, S=S, mode=mode, gamma=gamma,
+                    dtype=dtype, alpha=0.01, bias=bias)
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    torch.cuda.synchronize()
+
+
+def test_tiny_fp32_workload():
+    w = WORKLOADS["tiny_fp32"]
+    _, inp, outs, code = parity.run(w)
+    assert code == B.MOE_DEVICE_OK
+    rep = parity.check(w, inp, outs)
+    assert rep["y_rows"] == w.T
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_bf16_layers(case):
+    w = _w(*case)
+    _, inp, outs, code = parity.run(w, seed=3)
+    assert code == B.MOE_DEVICE_OK
+    parity.check(w, inp, outs)
+
+
+@pytest.mark.parametrize("case", SMALL[:4], ids=[c[0] for c in SMALL[:4]])
+def test_small_fp32_layers(case):
+    w = _w(*case, dtype="fp32")
+    _, inp, outs, code = parity.run(w, seed=4)
+    assert code == B.MOE_DEVICE_OK
+    parity.check(w, inp, outs)
+
+
+def test_switch_capacity_workload_every_token():
+    w = WORKLOADS["switch_top1_capacity"]
+    _, inp, outs, code = parity.run(w)
+    assert code == B.MOE_DEVICE_OK
+    rep = parity.check(w, inp, outs)
+    # the biased router overloads some experts: drops must happen here
+    assert int(outs["dropped_mask"].sum()) > 0
+    assert int(outs["kept_counts"].max()) == B.capacity(B.config_of(w))
+    print(rep)
+
+
+@pytest.mark.parametrize("name", ["mixtral_decode", "qwen2_57b_decode", "dsv3_decode",
+                                  "mixtral_prefill", "qwen2_57b_prefill", "dsv3_prefill"])
+def test_benchmark_sized_workloads_sampled(name):
+    w = WORKLOADS[name]
+    _, inp, outs, code = parity.run(w)
+    assert code == B.MOE_DEVICE_OK
+    rng = np.random.default_rng(7)
+    logit_rows = np.sort(rng.choice(w.T, size=min(w.T, 64), replace=False))
+    rep = parity.check(w, inp, outs, logit_rows=logit_rows, y_sample_n=6)
+    print(name, rep)
+    del inp, outs
+    torch.cuda.empty_cache()
+
+
+def test_deterministic():
+    w = _w(*SMALL[1])
+    cfg = B.config_of(w)
+    inp = make_inputs(w, 5, "cuda")
+    a = B.forward(cfg, inp)
+    b = B.forward(cfg, inp)
+    for key in ("y", "router_logits", "topk_idx", "topk_w", "dropped_mask",
+                "expert_counts", "kept_counts", "aux_loss"):
+        assert torch.equal(a[key], b[key]), key
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_single_token(dtype):
+    w = _w("one_token", 1, 128, 8, 128, 2, 64, 0, 1.0, "none", dtype=dtype)
+    _, inp, outs, code = parity.run(w, seed=8)
+    assert code == B.MOE_DEVICE_OK
+    parity.check(w, inp, outs)
+
+
+def test_zero_tokens():
+    w = _w("empty", 0, 128, 8, 128, 2, 0, 0, 1.0, "none")
+    cfg = B.config_of(w)
+    inp = make_inputs(w, 0, "cuda")
+    outs = B.alloc_outputs(cfg)
+    outs["expert_counts"].fill_(7)
+    outs["aux_loss"].fill_(3.0)
+    B.forward(cfg, inp, outs)
+    torch.cuda.synchronize()
+    assert int(outs["expert_counts"].abs().sum()) == 0
+    assert float(outs["aux_loss"][0]) == 0.0
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_one_expert_is_the_dense_mlp(mode):
+    w = _w("dense", 700, 192, 1, 256, 1, 0, mode, 0.0, "none")
+    _, inp, outs, code = parity.run(w, seed=9)
+    assert code == B.MOE_DEVICE_OK
+    assert torch.all(outs["topk_w"] == 1.0)
+    parity.check(w, inp, outs)
+
+
+def test_nonfinite_input_sets_status():
+    w = _w("nan", 64, 64, 4, 64, 2, 0, 0, 0.0, "none", dtype="fp32")
+    cfg = B.config_of(w)
+    inp = make_inputs(w, 1, "cuda")
+    inp["x"][5, 3] = float("nan")
+    outs = B.forward(cfg, inp)
+    code = B.read_device_status(cfg, outs["workspace"])
+    assert code == B.MOE_DEVICE_NONFINITE_SCORE
+    idx = outs["topk_idx"].cpu()
+    assert int(idx.min()) >= 0 and int(idx.max()) < w.E
+
+
+def test_runs_on_a_side_stream_and_in_a_cuda_graph():
+    w = _w(*SMALL[0])
+    cfg = B.config_of(w)
+    inp = make_inputs(w, 2, "cuda")
+    ref = B.forward(cfg, inp)
+    s = torch.cuda.Stream()
+    outs = B.alloc_outputs(cfg)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        B.forward(cfg, inp, outs, stream=s)
+    s.synchronize()
+    assert torch.equal(outs["y"], ref["y"])
+    g = torch.cuda.CUDAGraph()
+    outs2 = B.alloc_outputs(cfg)
+    with torch.cuda.graph(g):
+        B.forward(cfg, inp, outs2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(outs2["y"], ref["y"])
+    assert torch.equal(outs2["topk_idx"], ref["topk_idx"])
