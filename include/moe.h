@@ -151,6 +151,19 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
 MOE_API moe_status moe_read_device_status(const moe_config *cfg, const void *workspace,
                                   cudaStream_t stream, int32_t *code);
 
+/* Stage timing (optional; for benchmarks and profiling).  While `events`
+ * is non-NULL, every moe_forward call records events[i] on its stream at the
+ * stage boundaries below, so that cudaEventElapsedTime(events[i],
+ * events[i+1]) is the device time of stage i:
+ *   0 start | 1 router scores | 2 gating | 3 scan + finalize | 4 scatter |
+ *   5 routed gate/up GEMM | 6 routed down GEMM | 7 shared gate/up GEMM |
+ *   8 shared down GEMM | 9 combine (end)
+ * (stages 7 and 8 are empty without a shared expert).  n_events must be
+ * MOE_NUM_STAGE_EVENTS.  The events are the caller's; the setting is
+ * process-wide and not thread-safe.  Pass NULL to stop. */
+#define MOE_NUM_STAGE_EVENTS 10
+MOE_API moe_status moe_set_stage_events(cudaEvent_t *events, int n_events);
+
 /* Static, human-readable name of a status. */
 MOE_API const char *moe_status_string(moe_status status);
 

@@ -69,6 +69,8 @@ def lib():
         L.moe_forward.restype = ctypes.c_int
         L.moe_read_device_status.argtypes = [cfgp, vp, vp, ctypes.POINTER(ctypes.c_int32)]
         L.moe_read_device_status.restype = ctypes.c_int
+        L.moe_set_stage_events.argtypes = [vp, ctypes.c_int]
+        L.moe_set_stage_events.restype = ctypes.c_int
         L.moe_status_string.argtypes = [ctypes.c_int]
         L.moe_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -90,6 +92,14 @@ def make_config(T, d_model, n_experts, d_expert, top_k, d_shared=0, dtype="bf16"
 def config_of(w) -> MoeConfig:
     """MoeConfig of a workloads.Workload."""
     return make_config(w.T, w.D, w.E, w.F, w.k, w.S, w.dtype, w.mode, w.gamma, w.alpha)
+
+
+def router_is_fused(cfg: MoeConfig) -> bool:
+    """Whether moe_forward computes the router scores inside its gating kernel
+    (E <= 16 and E*d_model*elem_size <= 64 KiB) rather than in a router kernel."""
+    esz = 2 if cfg.dtype == MOE_DTYPE_BF16 else 4
+    return cfg.n_experts <= 16 and cfg.d_model % 8 == 0 and \
+        cfg.n_experts * cfg.d_model * esz <= 64 * 1024
 
 
 def workspace_size(cfg: MoeConfig) -> int:
@@ -149,6 +159,40 @@ def read_device_status(cfg: MoeConfig, workspace, stream=None) -> int:
     if st not in (MOE_OK, MOE_ERR_DEVICE_STATUS):
         raise MoeError(st, "moe_read_device_status")
     return int(code.value)
+
+
+NUM_STAGE_EVENTS = 10
+STAGES = ("router", "gate", "scan_finalize", "scatter", "gemm1_routed", "gemm2_routed",
+          "gemm1_shared", "gemm2_shared", "combine")
+
+
+class StageEvents:
+    """CUDA events moe_forward records at its stage boundaries (see
+    moe_set_stage_events).  Use as a context manager around the calls to
+    time; ``elapsed_ms()`` then gives the device time of each stage of the
+    last call."""
+
+    def __init__(self):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(NUM_STAGE_EVENTS)]
+        for e in self.events:       # torch creates the CUDA event on first record
+            e.record()
+        torch.cuda.synchronize()
+        self._arr = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[e.cuda_event for e in self.events])
+
+    def __enter__(self):
+        st = lib().moe_set_stage_events(ctypes.cast(self._arr, ctypes.c_void_p),
+                                        NUM_STAGE_EVENTS)
+        if st != MOE_OK:
+            raise MoeError(st, "moe_set_stage_events")
+        return self
+
+    def __exit__(self, *exc):
+        lib().moe_set_stage_events(None, 0)
+        return False
+
+    def elapsed_ms(self) -> dict:
+        ev = self.events
+        return {name: ev[i].elapsed_time(ev[i + 1]) for i, name in enumerate(STAGES)}
 
 
 # ---------------------------------------------------------------- convenience

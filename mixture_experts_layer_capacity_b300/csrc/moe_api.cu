@@ -2,6 +2,7 @@
 // argument validation, capacity, workspace layout, and the launch sequence
 //   router -> gate -> scan/finalize -> scatter -> experts -> combine
 // on the caller's stream, with no host synchronisation.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -87,6 +88,8 @@ WorkspaceLayout layout_of(const moe_config *c)
     L.total = off;
     return L;
 }
+
+std::atomic<cudaEvent_t *> g_stage_events{nullptr};
 
 int sm_count()
 {
@@ -177,34 +180,46 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r,
         return MOE_OK;
     }
 
+    cudaEvent_t *ev = g_stage_events.load();
+    if (!cuda_ok(record_stage(ev, 0, stream)))
+        return MOE_ERR_CUDA;
     // 1. router scores
-    cudaError_t err;
-    if (c.dtype == MOE_DTYPE_BF16 && c.T >= 512)
-        err = launch_router_tc(c, x, W_r, router_logits, status, stream);
-    else
-        err = launch_router_simt(c, x, W_r, router_logits, stream);
-    if (!cuda_ok(err))
+    //    (small routers run inside the gating kernel instead)
+    cudaError_t err = cudaSuccess;
+    const bool fused = router_fused(c) && aligned16(x) && aligned16(W_r);
+    if (!fused) {
+        if (c.dtype == MOE_DTYPE_BF16 && c.T >= 512)
+            err = launch_router_tc(c, x, W_r, router_logits, status, stream);
+        else
+            err = launch_router_simt(c, x, W_r, router_logits, stream);
+    }
+    if (!cuda_ok(err) || !cuda_ok(record_stage(ev, 1, stream)))
         return MOE_ERR_CUDA;
     // 2. softmax, top-k, gate weights, chunk statistics
-    if (!cuda_ok(launch_gate(c, L, ws, router_logits, router_bias, topk_idx, topk_w, stream)))
+    if (!cuda_ok(launch_gate(c, L, ws, fused ? x : nullptr, fused ? W_r : nullptr, router_logits,
+                             router_bias, topk_idx, topk_w, stream)) ||
+        !cuda_ok(record_stage(ev, 2, stream)))
         return MOE_ERR_CUDA;
     // 3. demand counts, capacity, segments, balance loss
-    if (!cuda_ok(launch_scan_finalize(c, L, ws, expert_counts, kept_counts, aux_loss, stream)))
+    if (!cuda_ok(launch_scan_finalize(c, L, ws, expert_counts, kept_counts, aux_loss, stream)) ||
+        !cuda_ok(record_stage(ev, 3, stream)))
         return MOE_ERR_CUDA;
     // 4. positions, drops, gather of x into expert order
-    if (!cuda_ok(launch_scatter(c, L, ws, x, topk_idx, dropped_mask, stream)))
+    if (!cuda_ok(launch_scatter(c, L, ws, x, topk_idx, dropped_mask, stream)) ||
+        !cuda_ok(record_stage(ev, 4, stream)))
         return MOE_ERR_CUDA;
     // 5. experts (routed segments and the shared expert)
     if (c.dtype == MOE_DTYPE_BF16)
         err = launch_experts_tc(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
-                                stream);
+                                stream, ev);
     else
         err = launch_experts_simt(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
-                                  stream);
+                                  stream, ev);
     if (!cuda_ok(err))
         return MOE_ERR_CUDA;
     // 6. weighted combine (+ shared expert)
-    if (!cuda_ok(launch_combine(c, L, ws, topk_w, y, stream)))
+    if (!cuda_ok(launch_combine(c, L, ws, topk_w, y, stream)) ||
+        !cuda_ok(record_stage(ev, 9, stream)))
         return MOE_ERR_CUDA;
     return MOE_OK;
 }
@@ -225,6 +240,14 @@ moe_status moe_read_device_status(const moe_config *cfg, const void *workspace,
         return MOE_ERR_CUDA;
     *code = v;
     return v == MOE_DEVICE_OK ? MOE_OK : MOE_ERR_DEVICE_STATUS;
+}
+
+moe_status moe_set_stage_events(cudaEvent_t *events, int n_events)
+{
+    if (events && n_events != MOE_NUM_STAGE_EVENTS)
+        return MOE_ERR_INVALID_ARG;
+    g_stage_events.store(events);
+    return MOE_OK;
 }
 
 const char *moe_status_string(moe_status s)

@@ -19,7 +19,20 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v)
     return __float2bfloat16_rn(v);
 }
 
-__device__ __forceinline__ float silu_f32(float a) { return a / (1.0f + __expf(-a)); }
+// SiLU with the fast exponential and reciprocal (the result is rounded to
+// bf16 or checked at 1e-4 relative, far above their error).
+__device__ __forceinline__ float silu_f32(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
+
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible (no-op when launched normally).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid in the stream to be scheduled (it still waits in
+// griddep_wait for this grid to complete).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // Sum over the warp; every lane receives lane 0's result, so all lanes hold
 // bit-identical values whatever order the butterfly used.

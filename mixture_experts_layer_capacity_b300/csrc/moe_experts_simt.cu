@@ -31,6 +31,8 @@ __global__ void simt_seg_gemm_f32_kernel(const float *__restrict__ A, const floa
                                          int N, int K, const int32_t *__restrict__ seg_off,
                                          int nseg, int dense_rows, float *__restrict__ out)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int n = blockIdx.x * blockDim.x + threadIdx.x;
     const int r = blockIdx.y * blockDim.y + threadIdx.y;
     const int rows = seg_off ? seg_off[nseg] : dense_rows;
@@ -58,7 +60,7 @@ __global__ void simt_seg_gemm_f32_kernel(const float *__restrict__ A, const floa
 cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                                 const void *x, const void *W_gate, const void *W_up,
                                 const void *W_down, const void *Ws_gate, const void *Ws_up,
-                                const void *Ws_down, cudaStream_t stream)
+                                const void *Ws_down, cudaStream_t stream, cudaEvent_t *ev)
 {
     if (c.dtype != MOE_DTYPE_FP32)
         return cudaErrorInvalidValue;
@@ -69,19 +71,41 @@ cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, u
     float *z = reinterpret_cast<float *>(ws + L.z);
     const dim3 block(32, 8);
     const unsigned rb = (unsigned)((L.R_max + 7) / 8);
-    simt_seg_gemm_f32_kernel<true><<<dim3((F + 31) / 32, rb), block, 0, stream>>>(
-        xp, (const float *)W_gate, (const float *)W_up, (long long)F * D, F, D, seg, E, 0, h);
-    simt_seg_gemm_f32_kernel<false><<<dim3((D + 31) / 32, rb), block, 0, stream>>>(
-        h, (const float *)W_down, nullptr, (long long)D * F, D, F, seg, E, 0, z);
+    const float *nil = nullptr;
+    const int32_t *noseg = nullptr;
+    cudaError_t err = launch_pdl(simt_seg_gemm_f32_kernel<true>, dim3((F + 31) / 32, rb), block, 0,
+                                 stream, (const float *)xp, (const float *)W_gate,
+                                 (const float *)W_up, (long long)F * D, F, D, seg, E, 0, h);
+    if (err == cudaSuccess)
+        err = record_stage(ev, 5, stream);
+    if (err == cudaSuccess)
+        err = launch_pdl(simt_seg_gemm_f32_kernel<false>, dim3((D + 31) / 32, rb), block, 0,
+                         stream, (const float *)h, (const float *)W_down, nil,
+                         (long long)D * F, D, F, seg, E, 0, z);
+    if (err == cudaSuccess)
+        err = record_stage(ev, 6, stream);
+    if (err != cudaSuccess)
+        return err;
     if (S > 0) {
         float *hs = reinterpret_cast<float *>(ws + L.hs);
         float *zs = reinterpret_cast<float *>(ws + L.zs);
         const unsigned tb = (unsigned)((c.T + 7) / 8);
-        simt_seg_gemm_f32_kernel<true><<<dim3((S + 31) / 32, tb), block, 0, stream>>>(
-            (const float *)x, (const float *)Ws_gate, (const float *)Ws_up, 0, S, D, nullptr, 1,
-            c.T, hs);
-        simt_seg_gemm_f32_kernel<false><<<dim3((D + 31) / 32, tb), block, 0, stream>>>(
-            hs, (const float *)Ws_down, nullptr, 0, D, S, nullptr, 1, c.T, zs);
+        err = launch_pdl(simt_seg_gemm_f32_kernel<true>, dim3((S + 31) / 32, tb), block, 0,
+                         stream, (const float *)x, (const float *)Ws_gate, (const float *)Ws_up,
+                         0LL, S, D, noseg, 1, c.T, hs);
+        if (err == cudaSuccess)
+            err = record_stage(ev, 7, stream);
+        if (err == cudaSuccess)
+            err = launch_pdl(simt_seg_gemm_f32_kernel<false>, dim3((D + 31) / 32, tb), block, 0,
+                             stream, (const float *)hs, (const float *)Ws_down, nil, 0LL, D, S,
+                             noseg, 1, c.T, zs);
+        if (err == cudaSuccess)
+            err = record_stage(ev, 8, stream);
+        if (err != cudaSuccess)
+            return err;
+    } else {
+        record_stage(ev, 7, stream);
+        record_stage(ev, 8, stream);
     }
     return cudaGetLastError();
 }

@@ -70,7 +70,8 @@ struct TcShape {
                                      : 2 * UMMA_N <= 128 ? 128
                                      : 2 * UMMA_N <= 256 ? 256
                                                          : 512;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
+    static constexpr int TABLE_BYTES = 2 * (kMaxExperts + 1) * 4 + 8;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + TABLE_BYTES + 1024;
     static_assert(UMMA_N % 16 == 0 && UMMA_N >= 16 && UMMA_N <= 256, "UMMA N");
     static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -80,17 +81,20 @@ struct TileInfo {
     int a_row0, rows, seg, n_idx;
 };
 
-__device__ __forceinline__ int tile_count(const TcParams &p)
+// The segment tables (seg_off, mtile) are copied into shared memory at
+// kernel start; s_seg/s_mt point there (null when dense).
+__device__ __forceinline__ int tile_count(const TcParams &p, const int *s_mt)
 {
-    if (!p.mtile)
+    if (!s_mt)
         return ((p.dense_rows + kTileM - 1) / kTileM) * p.n_tiles;
-    return p.mtile[p.nseg] * p.n_tiles;
+    return s_mt[p.nseg] * p.n_tiles;
 }
 
-__device__ __forceinline__ TileInfo tile_info(const TcParams &p, int g)
+__device__ __forceinline__ TileInfo tile_info(const TcParams &p, const int *s_seg,
+                                              const int *s_mt, int g)
 {
     TileInfo ti;
-    if (!p.mtile) {
+    if (!s_mt) {
         const int mt = (p.dense_rows + kTileM - 1) / kTileM;
         ti.n_idx = g / mt;
         const int m = g - ti.n_idx * mt;
@@ -102,19 +106,19 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams &p, int g)
     int lo = 0, hi = p.nseg;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (p.mtile[mid] * p.n_tiles <= g)
+        if (s_mt[mid] * p.n_tiles <= g)
             lo = mid;
         else
             hi = mid;
     }
-    const int mt0 = p.mtile[lo], mt_e = p.mtile[lo + 1] - mt0;
+    const int mt0 = s_mt[lo], mt_e = s_mt[lo + 1] - mt0;
     const int local = g - mt0 * p.n_tiles;
     ti.n_idx = local / mt_e;
     const int m = local - ti.n_idx * mt_e;
     ti.seg = lo;
-    const int s0 = p.seg_off[lo];
+    const int s0 = s_seg[lo];
     ti.a_row0 = s0 + m * kTileM;
-    ti.rows = min(kTileM, p.seg_off[lo + 1] - ti.a_row0);
+    ti.rows = min(kTileM, s_seg[lo + 1] - ti.a_row0);
     return ti;
 }
 
@@ -162,6 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *mma_done = bars + 2 * STAGES + 4;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *tables = reinterpret_cast<int *>(smem + STAGES * S::STAGE_BYTES + 256);
+    const int *s_seg = p.mtile ? tables : nullptr;
+    const int *s_mt = p.mtile ? tables + (kMaxExperts + 1) : nullptr;
 
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
@@ -189,12 +196,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, S::TMEM_COLS);
         tmem_relinquish();
     }
+    // everything above touched only this CTA's shared memory and TMEM; from
+    // here on global memory written by the previous kernel is read
+    griddep_wait();
+    griddep_launch_dependents();
+    if (p.mtile) {
+        for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
+            tables[i] = p.seg_off[i];
+            tables[kMaxExperts + 1 + i] = p.mtile[i];
+        }
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int ntiles = tile_count(p);
+    const int ntiles = tile_count(p, s_mt);
     const int nk = (p.K + 63) / 64;
 
     if (warp == 0) {
@@ -205,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long fills = 0;
             bool ok = true;
             for (int g = blockIdx.x; g < ntiles && ok; g += gridDim.x) {
-                const TileInfo ti = tile_info(p, g);
+                const TileInfo ti = tile_info(p, s_seg, s_mt, g);
                 const int b_row = ti.seg * p.b_seg_rows + ti.n_idx * BN;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -290,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q * 32 + lane;        // accumulator row of this thread
         uint32_t b = 0, tph = 0;
         for (int g = blockIdx.x; g < ntiles; g += gridDim.x) {
-            const TileInfo ti = tile_info(p, g);
+            const TileInfo ti = tile_info(p, s_seg, s_mt, g);
             if (!mbar_wait(&tfull[b], tph, abort_flag, kWaitLimitNs)) {
                 *abort_flag = 1;
                 set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
@@ -440,8 +457,8 @@ cudaError_t launch_tc(const CUtensorMap &mA, const CUtensorMap &mB0, const CUten
     const long long grid = std::min<long long>(max_tiles, sm_count());
     if (grid < 1)
         return cudaSuccess;
-    kern<<<(unsigned)grid, kThreads, S::SMEM_BYTES, stream>>>(mA, mB0, mB1, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), (size_t)S::SMEM_BYTES, stream,
+                      mA, mB0, mB1, p);
 }
 
 }  // namespace
@@ -480,7 +497,7 @@ cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r
 cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                               const void *x, const void *W_gate, const void *W_up,
                               const void *W_down, const void *Ws_gate, const void *Ws_up,
-                              const void *Ws_down, cudaStream_t stream)
+                              const void *Ws_down, cudaStream_t stream, cudaEvent_t *ev)
 {
     const int D = c.d_model, F = c.d_expert, S = c.d_shared, E = c.n_experts, T = c.T;
     int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
@@ -511,6 +528,8 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
         p.ld_out = F;
         p.status = status;
         err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_bound * p.n_tiles, stream);
+        if (err == cudaSuccess)
+            err = record_stage(ev, 5, stream);
         if (err != cudaSuccess)
             return err;
     }
@@ -534,6 +553,8 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
         p.status = status;
         err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt_bound * p.n_tiles, stream)
                         : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt_bound * p.n_tiles, stream);
+        if (err == cudaSuccess)
+            err = record_stage(ev, 6, stream);
         if (err != cudaSuccess)
             return err;
     }
@@ -556,6 +577,8 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.ld_out = S;
             p.status = status;
             err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt * p.n_tiles, stream);
+            if (err == cudaSuccess)
+                err = record_stage(ev, 7, stream);
             if (err != cudaSuccess)
                 return err;
         }
@@ -576,9 +599,17 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.status = status;
             err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt * p.n_tiles, stream)
                             : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt * p.n_tiles, stream);
+            if (err == cudaSuccess)
+                err = record_stage(ev, 8, stream);
             if (err != cudaSuccess)
                 return err;
         }
+    } else {
+        err = record_stage(ev, 7, stream);
+        if (err == cudaSuccess)
+            err = record_stage(ev, 8, stream);
+        if (err != cudaSuccess)
+            return err;
     }
     return cudaSuccess;
 }

@@ -2,6 +2,7 @@
 // the kernel launchers the C ABI sequences.  Not part of the public ABI.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -18,7 +19,7 @@ constexpr int kTileM = 128;      // rows per tensor-core tile (UMMA M)
 // Byte offsets of the scratch regions inside the caller's workspace.  Every
 // region starts on a 1024-byte boundary.
 struct WorkspaceLayout {
-    size_t status;   // int32[4]  device status word (+ padding)
+    size_t status;   // int32[16] device status word, then the scan's block counter
     size_t hist;     // int32[E][nchunk]  per-chunk expert counts, then exclusive bases
     size_t ppart;    // float[E][nchunk]  per-chunk sums of softmax probabilities
     size_t rank;     // uint8[T*k]        rank of an assignment among its chunk's tokens
@@ -44,9 +45,12 @@ WorkspaceLayout layout_of(const moe_config *cfg);
 // Launchers (all enqueue on `stream`; return cudaGetLastError()).
 cudaError_t launch_router_simt(const moe_config &c, const void *x, const void *W_r,
                                float *logits, cudaStream_t stream);
+// True when the router GEMM runs inside the gating kernel (W_r staged in
+// shared memory); launch_gate then reads x and W_r itself.
+bool router_fused(const moe_config &c);
 cudaError_t launch_gate(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
-                        float *logits, const float *bias, int32_t *topk_idx, float *topk_w,
-                        cudaStream_t stream);
+                        const void *x, const void *W_r, float *logits, const float *bias,
+                        int32_t *topk_idx, float *topk_w, cudaStream_t stream);
 cudaError_t launch_scan_finalize(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                                  int32_t *expert_counts, int32_t *kept_counts, float *aux_loss,
                                  cudaStream_t stream);
@@ -58,17 +62,59 @@ cudaError_t launch_combine(const moe_config &c, const WorkspaceLayout &L, uint8_
 cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                                 const void *x, const void *W_gate, const void *W_up,
                                 const void *W_down, const void *Ws_gate, const void *Ws_up,
-                                const void *Ws_down, cudaStream_t stream);
+                                const void *Ws_down, cudaStream_t stream,
+                                cudaEvent_t *ev = nullptr);
+
+// Records ev[i] on `stream` when ev is not null.  Under stream capture the
+// record becomes an external event node of the graph, so that replays
+// timestamp it (a plain record would only order the capture).
+inline cudaError_t record_stage(cudaEvent_t *ev, int i, cudaStream_t stream)
+{
+    if (!ev)
+        return cudaSuccess;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t err = cudaStreamIsCapturing(stream, &cap);
+    if (err != cudaSuccess)
+        return err;
+    if (cap == cudaStreamCaptureStatusActive)
+        return cudaEventRecordWithFlags(ev[i], stream, cudaEventRecordExternal);
+    return cudaEventRecord(ev[i], stream);
+}
 
 // Tensor-core (tcgen05 + TMA) paths, bf16 only.  Return cudaErrorInvalidValue
 // if a tensor map cannot be encoded.
 cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r,
                              float *logits, int32_t *status, cudaStream_t stream);
+// `ev` (nullable): stage events 5..8 are recorded after each GEMM.
 cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                               const void *x, const void *W_gate, const void *W_up,
                               const void *W_down, const void *Ws_gate, const void *Ws_up,
-                              const void *Ws_down, cudaStream_t stream);
+                              const void *Ws_down, cudaStream_t stream,
+                              cudaEvent_t *ev = nullptr);
 
 int sm_count();
+
+// Launches `kern` on `stream` with programmatic stream serialization, so
+// that it may be scheduled while the previous kernel drains.  Every kernel
+// launched this way calls griddep_wait() before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// Stage events set by moe_set_stage_events (null = not recording).
+extern std::atomic<cudaEvent_t *> g_stage_events;
 
 }  // namespace moe

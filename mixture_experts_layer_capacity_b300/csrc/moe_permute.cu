@@ -68,68 +68,76 @@ __device__ __forceinline__ double block_sum_256(double v, double *sh)
     return r;
 }
 
-// One block per expert.
+// One block per expert: exclusive prefix of the chunk counts, the demand
+// count n_e and P_sum_e.  The last block to finish (block counter) then
+// computes kept_e = min(n_e, C), the segment offsets, the 128-row tile prefix
+// and the balance loss from all experts' results.
 __global__ void __launch_bounds__(kScanThreads)
-    scan_kernel(int32_t *hist, const float *ppart, double *psum, int32_t *expert_counts,
-                int nchunk)
+    scan_finalize_kernel(int32_t *hist, const float *ppart, double *psum, int32_t *expert_counts,
+                         int nchunk, int E, int T, int k, long long C, float alpha,
+                         int32_t *kept_counts, int32_t *seg_off, int32_t *mtile, float *aux_loss,
+                         int32_t *block_counter)
 {
     __shared__ int shi[8];
     __shared__ double shd[kScanThreads];
+    __shared__ int is_last;
+    griddep_wait();
+    griddep_launch_dependents();
     const int e = blockIdx.x;
-    int32_t *h = hist + (size_t)e * nchunk;
-    const float *pp = ppart + (size_t)e * nchunk;
-    const int per = (nchunk + kScanThreads - 1) / kScanThreads;
-    const int beg = min(nchunk, (int)threadIdx.x * per), end = min(nchunk, beg + per);
-    int local = 0;
-    double pl = 0.0;
-    for (int c = beg; c < end; ++c) {
-        local += h[c];
-        pl += (double)pp[c];
+    {
+        int32_t *h = hist + (size_t)e * nchunk;
+        const float *pp = ppart + (size_t)e * nchunk;
+        const int per = (nchunk + kScanThreads - 1) / kScanThreads;
+        const int beg = min(nchunk, (int)threadIdx.x * per), end = min(nchunk, beg + per);
+        int local = 0;
+        double pl = 0.0;
+        for (int c = beg; c < end; ++c) {
+            local += h[c];
+            pl += (double)pp[c];
+        }
+        int total;
+        int run = block_excl_scan_256(local, shi, &total);
+        for (int c = beg; c < end; ++c) {
+            const int v = h[c];
+            h[c] = run;
+            run += v;
+        }
+        const double ps = block_sum_256(pl, shd);
+        if (threadIdx.x == 0) {
+            expert_counts[e] = total;
+            psum[e] = ps;
+            __threadfence();
+            is_last = (atomicAdd(block_counter, 1) == E - 1);
+        }
+        __syncthreads();
     }
-    int total;
-    int run = block_excl_scan_256(local, shi, &total);
-    for (int c = beg; c < end; ++c) {
-        const int v = h[c];
-        h[c] = run;
-        run += v;
-    }
-    const double ps = block_sum_256(pl, shd);
-    if (threadIdx.x == 0) {
-        expert_counts[e] = total;
-        psum[e] = ps;
-    }
-}
+    if (!is_last)
+        return;
+    __threadfence();
 
-__global__ void __launch_bounds__(kScanThreads)
-    finalize_kernel(const int32_t *expert_counts, const double *psum, int E, int T, int k,
-                    long long C, float alpha, int32_t *kept_counts, int32_t *seg_off,
-                    int32_t *mtile, float *aux_loss)
-{
-    __shared__ int shi[8];
-    __shared__ double shd[kScanThreads];
-    const int e = threadIdx.x;
-    const int n = e < E ? expert_counts[e] : 0;
+    const int x = threadIdx.x;  // expert handled by this thread in the finalize
+    const int n = x < E ? __ldcg(expert_counts + x) : 0;
     const int kept = (C < 0) ? n : (int)min((long long)n, C);
-    if (e < E)
-        kept_counts[e] = kept;
+    if (x < E)
+        kept_counts[x] = kept;
     int total;
     const int off = block_excl_scan_256(kept, shi, &total);
-    if (e < E)
-        seg_off[e] = off;
-    if (e == 0)
+    if (x < E)
+        seg_off[x] = off;
+    if (x == 0)
         seg_off[E] = total;
     const int mt = (kept + kTileM - 1) / kTileM;
     int mt_total;
     const int moff = block_excl_scan_256(mt, shi, &mt_total);
-    if (e < E)
-        mtile[e] = moff;
-    if (e == 0)
+    if (x < E)
+        mtile[x] = moff;
+    if (x == 0)
         mtile[E] = mt_total;
     double term = 0.0;
-    if (e < E && T > 0)
-        term = ((double)n / ((double)T * (double)k)) * (psum[e] / (double)T);
+    if (x < E && T > 0)
+        term = ((double)n / ((double)T * (double)k)) * (__ldcg(psum + x) / (double)T);
     const double sum = block_sum_256(term, shd);
-    if (e == 0)
+    if (x == 0)
         *aux_loss = (float)((double)alpha * (double)E * sum);
 }
 
@@ -137,16 +145,14 @@ cudaError_t launch_scan_finalize(const moe_config &c, const WorkspaceLayout &L, 
                                  int32_t *expert_counts, int32_t *kept_counts, float *aux_loss,
                                  cudaStream_t stream)
 {
-    int32_t *hist = reinterpret_cast<int32_t *>(ws + L.hist);
-    const float *ppart = reinterpret_cast<const float *>(ws + L.ppart);
-    double *psum = reinterpret_cast<double *>(ws + L.psum);
-    scan_kernel<<<c.n_experts, kScanThreads, 0, stream>>>(hist, ppart, psum, expert_counts,
-                                                          L.nchunk);
-    finalize_kernel<<<1, kScanThreads, 0, stream>>>(
-        expert_counts, psum, c.n_experts, c.T, c.top_k, (long long)L.C, c.aux_alpha,
-        kept_counts, reinterpret_cast<int32_t *>(ws + L.seg_off),
-        reinterpret_cast<int32_t *>(ws + L.mtile), aux_loss);
-    return cudaGetLastError();
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    return launch_pdl(scan_finalize_kernel, dim3(c.n_experts), dim3(kScanThreads), 0, stream,
+                      reinterpret_cast<int32_t *>(ws + L.hist),
+                      reinterpret_cast<const float *>(ws + L.ppart),
+                      reinterpret_cast<double *>(ws + L.psum), expert_counts, L.nchunk,
+                      c.n_experts, c.T, c.top_k, (long long)L.C, c.aux_alpha, kept_counts,
+                      reinterpret_cast<int32_t *>(ws + L.seg_off),
+                      reinterpret_cast<int32_t *>(ws + L.mtile), aux_loss, status + 8);
 }
 
 // -------------------------------------------------------------------- scatter
@@ -159,6 +165,8 @@ __global__ void __launch_bounds__(128)
                    size_t row_bytes, uint8_t *dropped, int32_t *row_of, uint8_t *x_perm)
 {
     __shared__ long long rows[kMaxTopK];
+    griddep_wait();
+    griddep_launch_dependents();
     const int t = blockIdx.x;
     if ((int)threadIdx.x < k) {
         const int j = threadIdx.x;
@@ -195,14 +203,12 @@ cudaError_t launch_scatter(const moe_config &c, const WorkspaceLayout &L, uint8_
     auto *seg = reinterpret_cast<const int32_t *>(ws + L.seg_off);
     auto *row_of = reinterpret_cast<int32_t *>(ws + L.row_of);
     if (row_bytes % 16 == 0)
-        scatter_kernel<16><<<c.T, 128, 0, stream>>>(
-            (const uint8_t *)x, topk_idx, ws + L.rank, args_base, seg, (long long)L.C, c.top_k,
-            L.nchunk, row_bytes, dropped_mask, row_of, ws + L.x_perm);
-    else
-        scatter_kernel<4><<<c.T, 128, 0, stream>>>(
-            (const uint8_t *)x, topk_idx, ws + L.rank, args_base, seg, (long long)L.C, c.top_k,
-            L.nchunk, row_bytes, dropped_mask, row_of, ws + L.x_perm);
-    return cudaGetLastError();
+        return launch_pdl(scatter_kernel<16>, dim3(c.T), dim3(128), 0, stream, (const uint8_t *)x,
+                          topk_idx, (const uint8_t *)(ws + L.rank), args_base, seg, (long long)L.C,
+                          c.top_k, L.nchunk, row_bytes, dropped_mask, row_of, ws + L.x_perm);
+    return launch_pdl(scatter_kernel<4>, dim3(c.T), dim3(128), 0, stream, (const uint8_t *)x,
+                      topk_idx, (const uint8_t *)(ws + L.rank), args_base, seg, (long long)L.C,
+                      c.top_k, L.nchunk, row_bytes, dropped_mask, row_of, ws + L.x_perm);
 }
 
 // -------------------------------------------------------------------- combine
@@ -215,6 +221,8 @@ __global__ void __launch_bounds__(128)
 {
     __shared__ int rows[kMaxTopK];
     __shared__ float ws[kMaxTopK];
+    griddep_wait();
+    griddep_launch_dependents();
     const int t = blockIdx.x;
     if ((int)threadIdx.x < k) {
         rows[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
@@ -267,6 +275,8 @@ __global__ void __launch_bounds__(128)
 {
     __shared__ int rows[kMaxTopK];
     __shared__ float ws[kMaxTopK];
+    griddep_wait();
+    griddep_launch_dependents();
     const int t = blockIdx.x;
     if ((int)threadIdx.x < k) {
         rows[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
@@ -292,16 +302,14 @@ cudaError_t launch_combine(const moe_config &c, const WorkspaceLayout &L, uint8_
     const int32_t *row_of = reinterpret_cast<const int32_t *>(ws + L.row_of);
     const bool shared = c.d_shared > 0;
     if (c.dtype == MOE_DTYPE_BF16)
-        combine_bf16_kernel<<<c.T, 128, 0, stream>>>(
-            reinterpret_cast<const __nv_bfloat16 *>(ws + L.z),
-            shared ? reinterpret_cast<const __nv_bfloat16 *>(ws + L.zs) : nullptr, topk_w, row_of,
-            (__nv_bfloat16 *)y, c.top_k, c.d_model);
-    else
-        combine_f32_kernel<<<c.T, 128, 0, stream>>>(
-            reinterpret_cast<const float *>(ws + L.z),
-            shared ? reinterpret_cast<const float *>(ws + L.zs) : nullptr, topk_w, row_of,
-            (float *)y, c.top_k, c.d_model);
-    return cudaGetLastError();
+        return launch_pdl(combine_bf16_kernel, dim3(c.T), dim3(128), 0, stream,
+                          reinterpret_cast<const __nv_bfloat16 *>(ws + L.z),
+                          shared ? reinterpret_cast<const __nv_bfloat16 *>(ws + L.zs) : nullptr,
+                          topk_w, row_of, (__nv_bfloat16 *)y, c.top_k, c.d_model);
+    return launch_pdl(combine_f32_kernel, dim3(c.T), dim3(128), 0, stream,
+                      reinterpret_cast<const float *>(ws + L.z),
+                      shared ? reinterpret_cast<const float *>(ws + L.zs) : nullptr, topk_w,
+                      row_of, (float *)y, c.top_k, c.d_model);
 }
 
 }  // namespace moe
