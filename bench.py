@@ -149,7 +149,7 @@ def stage_work(w, kept_total, touched):
                          b * (F * D * touched + kept_total * F + kept_total * D)),
         "gemm1_shared": (4 * D * S * T, b * (2 * S * D + T * D + T * S)),
         "gemm2_shared": (2 * D * S * T, b * (S * D + T * S + T * D)),
-        "scatter": (0, b * (T * D + kept_total * D)),
+        "dispatch": (0, b * (T * D + kept_total * D)),
         "combine": (0, b * (kept_total * D + (T * D if S else 0) + T * D)),
     }
 
@@ -279,22 +279,27 @@ def run_ours(args, rank, world, device):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    # The timed step replays one moe_forward captured in a CUDA graph, with
-    # the library's stage events captured inside it.
-    stage_ev = B.StageEvents()
+    # The timed step replays one moe_forward captured in a CUDA graph.  A
+    # second graph of the same call carries the library's stage events (each
+    # event node costs ~1 us and breaks launch overlap, so it is timed in a
+    # separate pass and gives the per-kernel durations).
     graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        B.forward(cfg, inputs, outs)
+    stage_ev = B.StageEvents()
+    graph_st = torch.cuda.CUDAGraph()
     with stage_ev:
-        with torch.cuda.graph(graph):
+        with torch.cuda.graph(graph_st):
             B.forward(cfg, inputs, outs)
     for _ in range(args.warmup):
         flush.fill_(1)
         graph.replay()
+        graph_st.replay()
     torch.cuda.synchronize()
 
     K = args.steps
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    stage_sum = {n: 0.0 for n in B.STAGES}
     clocks = ClockSampler(device)
     barrier()
     clocks.start()
@@ -304,9 +309,6 @@ def run_ours(args, rank, world, device):
         ev_s[i].record(stream)
         graph.replay()
         ev_e[i].record(stream)
-        ev_e[i].synchronize()                       # stage events are re-recorded each replay
-        for n, v in stage_ev.elapsed_ms().items():
-            stage_sum[n] += v
     barrier()
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
@@ -319,10 +321,28 @@ def run_ours(args, rank, world, device):
     total_ms_max = float(t.item())
     ms_per_step = total_ms_max / K
     value = world * w.T * K / (total_ms_max / 1e3)
-    stages = {n: v / K for n, v in stage_sum.items()}
     code = B.read_device_status(cfg, outs["workspace"])
     if code != B.MOE_DEVICE_OK:
         raise RuntimeError(f"device status {code} after the timed steps")
+
+    # per-stage device time: the instrumented graph, same flush, read per step
+    Ks = min(K, 200)
+    stage_sum = {n: 0.0 for n in B.STAGES}
+    st_s = torch.cuda.Event(enable_timing=True)
+    st_e = torch.cuda.Event(enable_timing=True)
+    st_total = 0.0
+    barrier()
+    for i in range(Ks):
+        flush.fill_(i & 0xFF)
+        st_s.record(stream)
+        graph_st.replay()
+        st_e.record(stream)
+        st_e.synchronize()                          # stage events are re-recorded each replay
+        st_total += st_s.elapsed_time(st_e)
+        for n, v in stage_ev.elapsed_ms().items():
+            stage_sum[n] += v
+    stages = {n: v / Ks for n, v in stage_sum.items()}
+    staged_ms = st_total / Ks
 
     # the same steps as direct moe_forward calls (no graph), for reference
     Kq = min(K, 200)
@@ -399,16 +419,20 @@ def run_ours(args, rank, world, device):
     h2d = x_h.numel() * x_h.element_size()
     d2h = y_h.numel() * y_h.element_size() + 4
 
-    # router (unless fused into the gate), gate, scan+finalize, scatter,
-    # GEMM1, GEMM2 (+ two shared-expert GEMMs), combine
-    from mixture_experts_layer_capacity_b300.binding import router_is_fused
-    launches_per_step = 7 - (1 if router_is_fused(cfg) else 0) + (2 if w.S else 0)
+    # router (unless fused into dispatch), dispatch, GEMM1, GEMM2 (+ two
+    # shared-expert GEMMs), combine (unless GEMM2 writes y)
+    launches_per_step = (0 if B.router_is_fused(cfg) else 1) + 3 + (2 if w.S else 0) + \
+        (0 if B.direct_y(cfg) else 1)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": workload_config(w, "flushed between timed steps (512 MiB write)"),
+        "launch": "one moe_forward captured in a CUDA graph, replayed per step",
+        "eager": {"value": world * w.T / (eager_ms / 1e3), "ms_per_step": eager_ms,
+                  "note": "direct moe_forward calls, no graph"},
+        "instrumented_ms_per_step": staged_ms,
         "roofline": roof,
         "layer_roofline": layer,
         "stages_ms": stages,

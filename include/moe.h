@@ -155,13 +155,16 @@ MOE_API moe_status moe_read_device_status(const moe_config *cfg, const void *wor
  * is non-NULL, every moe_forward call records events[i] on its stream at the
  * stage boundaries below, so that cudaEventElapsedTime(events[i],
  * events[i+1]) is the device time of stage i:
- *   0 start | 1 router scores | 2 gating | 3 scan + finalize | 4 scatter |
- *   5 routed gate/up GEMM | 6 routed down GEMM | 7 shared gate/up GEMM |
- *   8 shared down GEMM | 9 combine (end)
- * (stages 7 and 8 are empty without a shared expert).  n_events must be
+ *   0 start | 1 router scores | 2 dispatch (gating, counts, capacity,
+ *   gather) | 3 routed gate/up GEMM | 4 routed down GEMM | 5 shared gate/up
+ *   GEMM | 6 shared down GEMM | 7 combine (end)
+ * (stage 1 is empty when the router runs inside the dispatch kernel, stages
+ * 5-6 without a shared expert, and stage 7 when k = 1 without a shared expert
+ * in bf16, where the down projection writes y).  Recorded during stream
+ * capture they become event nodes of the graph.  n_events must be
  * MOE_NUM_STAGE_EVENTS.  The events are the caller's; the setting is
  * process-wide and not thread-safe.  Pass NULL to stop. */
-#define MOE_NUM_STAGE_EVENTS 10
+#define MOE_NUM_STAGE_EVENTS 8
 MOE_API moe_status moe_set_stage_events(cudaEvent_t *events, int n_events);
 
 /* Static, human-readable name of a status. */

@@ -102,6 +102,11 @@ def router_is_fused(cfg: MoeConfig) -> bool:
         cfg.n_experts * cfg.d_model * esz <= 64 * 1024
 
 
+def direct_y(cfg: MoeConfig) -> bool:
+    """Whether the down projection writes y itself (no combine kernel)."""
+    return cfg.top_k == 1 and cfg.d_shared == 0 and cfg.dtype == MOE_DTYPE_BF16
+
+
 def workspace_size(cfg: MoeConfig) -> int:
     n = ctypes.c_size_t(0)
     st = lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n))
@@ -161,9 +166,9 @@ def read_device_status(cfg: MoeConfig, workspace, stream=None) -> int:
     return int(code.value)
 
 
-NUM_STAGE_EVENTS = 10
-STAGES = ("router", "gate", "scan_finalize", "scatter", "gemm1_routed", "gemm2_routed",
-          "gemm1_shared", "gemm2_shared", "combine")
+NUM_STAGE_EVENTS = 8
+STAGES = ("router", "dispatch", "gemm1_routed", "gemm2_routed", "gemm1_shared",
+          "gemm2_shared", "combine")
 
 
 class StageEvents:

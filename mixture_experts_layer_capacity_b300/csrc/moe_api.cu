@@ -80,6 +80,8 @@ WorkspaceLayout layout_of(const moe_config *c)
     L.seg_off = take(sizeof(int32_t) * (E + 1));
     L.mtile = take(sizeof(int32_t) * (E + 1));
     L.row_of = take(sizeof(int32_t) * TK);
+    L.row_tok = take(sizeof(int32_t) * L.R_max);
+    L.row_w = take(sizeof(float) * L.R_max);
     L.x_perm = take(esz * L.R_max * D);
     L.h = take(esz * L.R_max * F);
     L.z = take(esz * L.R_max * D);
@@ -183,8 +185,7 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r,
     cudaEvent_t *ev = g_stage_events.load();
     if (!cuda_ok(record_stage(ev, 0, stream)))
         return MOE_ERR_CUDA;
-    // 1. router scores
-    //    (small routers run inside the gating kernel instead)
+    // 1. router scores (small routers run inside the dispatch kernel instead)
     cudaError_t err = cudaSuccess;
     const bool fused = router_fused(c) && aligned16(x) && aligned16(W_r);
     if (!fused) {
@@ -195,31 +196,29 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r,
     }
     if (!cuda_ok(err) || !cuda_ok(record_stage(ev, 1, stream)))
         return MOE_ERR_CUDA;
-    // 2. softmax, top-k, gate weights, chunk statistics
-    if (!cuda_ok(launch_gate(c, L, ws, fused ? x : nullptr, fused ? W_r : nullptr, router_logits,
-                             router_bias, topk_idx, topk_w, stream)) ||
+    // 2. gating, demand counts, capacity, segments, balance loss, gather of x
+    //    into expert order (one cooperative kernel)
+    if (!cuda_ok(launch_dispatch(c, L, ws, x, W_r, fused, router_logits, router_bias, topk_idx,
+                                 topk_w, dropped_mask, expert_counts, kept_counts, aux_loss, y,
+                                 stream)) ||
         !cuda_ok(record_stage(ev, 2, stream)))
         return MOE_ERR_CUDA;
-    // 3. demand counts, capacity, segments, balance loss
-    if (!cuda_ok(launch_scan_finalize(c, L, ws, expert_counts, kept_counts, aux_loss, stream)) ||
-        !cuda_ok(record_stage(ev, 3, stream)))
-        return MOE_ERR_CUDA;
-    // 4. positions, drops, gather of x into expert order
-    if (!cuda_ok(launch_scatter(c, L, ws, x, topk_idx, dropped_mask, stream)) ||
-        !cuda_ok(record_stage(ev, 4, stream)))
-        return MOE_ERR_CUDA;
-    // 5. experts (routed segments and the shared expert)
+    // 3. experts (routed segments and the shared expert)
     if (c.dtype == MOE_DTYPE_BF16)
-        err = launch_experts_tc(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
+        err = launch_experts_tc(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y,
                                 stream, ev);
     else
         err = launch_experts_simt(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
                                   stream, ev);
     if (!cuda_ok(err))
         return MOE_ERR_CUDA;
-    // 6. weighted combine (+ shared expert)
-    if (!cuda_ok(launch_combine(c, L, ws, topk_w, y, stream)) ||
-        !cuda_ok(record_stage(ev, 9, stream)))
+    // 4. weighted combine (+ shared expert), unless the down projection
+    //    already wrote y
+    if (!(direct_y(c) && c.dtype == MOE_DTYPE_BF16)) {
+        if (!cuda_ok(launch_combine(c, L, ws, topk_w, y, stream)))
+            return MOE_ERR_CUDA;
+    }
+    if (!cuda_ok(record_stage(ev, 7, stream)))
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

@@ -1,0 +1,123 @@
+// moe_combine.cu -- the weighted combine:
+//   y_t = sum_{j<k, kept} w_tj z[row_tj] (+ z_shared[t])
+// with fp32 accumulation in the fixed order j = 0..k-1, then the shared
+// expert.  Dropped assignments contribute nothing and the remaining weights
+// are not renormalised; the residual connection is the caller's.
+//
+// Sources: "Mixture of Experts" (module 17), 17.2 equation (shared expert plus
+// the gate-weighted routed experts) and 17.5 (a dropped token keeps its other
+// experts and the residual); "Mixture of Experts: Sparse FFNs, Routers, and
+// Shared Experts" (the combine loop: out[tok] += weight * expert(x[tok])).
+#include <cuda_bf16.h>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+// One block per token: y_t = sum_{j<k, kept} w_tj z[row_tj] (+ zs[t]), fp32
+// accumulation in the fixed order j = 0..k-1, then the shared expert.
+__global__ void __launch_bounds__(128)
+    combine_bf16_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__restrict__ zs,
+                        const float *__restrict__ topk_w, const int32_t *__restrict__ row_of,
+                        __nv_bfloat16 *__restrict__ y, int k, int D, const int32_t *status)
+{
+    __shared__ int rows[kMaxTopK];
+    __shared__ float ws[kMaxTopK];
+    griddep_wait();
+    griddep_launch_dependents();
+    if (*(volatile const int32_t *)status != 0)
+        return;  // an earlier kernel failed; y is left unspecified
+    const int t = blockIdx.x;
+    if ((int)threadIdx.x < k) {
+        rows[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
+        ws[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
+    }
+    __syncthreads();
+    const int nv = D / 8;
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            acc[i] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int r = rows[j];
+            if (r < 0)
+                continue;
+            const float wj = ws[j];
+            const uint4 q = reinterpret_cast<const uint4 *>(z + (size_t)r * D)[v];
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&q);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(h[i]);
+                acc[2 * i] = fmaf(wj, f.x, acc[2 * i]);
+                acc[2 * i + 1] = fmaf(wj, f.y, acc[2 * i + 1]);
+            }
+        }
+        if (zs) {
+            const uint4 q = reinterpret_cast<const uint4 *>(zs + (size_t)t * D)[v];
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&q);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(h[i]);
+                acc[2 * i] += f.x;
+                acc[2 * i + 1] += f.y;
+            }
+        }
+        uint4 out;
+        __nv_bfloat162 *o = reinterpret_cast<__nv_bfloat162 *>(&out);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        reinterpret_cast<uint4 *>(y + (size_t)t * D)[v] = out;
+    }
+}
+
+__global__ void __launch_bounds__(128)
+    combine_f32_kernel(const float *__restrict__ z, const float *__restrict__ zs,
+                       const float *__restrict__ topk_w, const int32_t *__restrict__ row_of,
+                       float *__restrict__ y, int k, int D, const int32_t *status)
+{
+    __shared__ int rows[kMaxTopK];
+    __shared__ float ws[kMaxTopK];
+    griddep_wait();
+    griddep_launch_dependents();
+    if (*(volatile const int32_t *)status != 0)
+        return;  // an earlier kernel failed; y is left unspecified
+    const int t = blockIdx.x;
+    if ((int)threadIdx.x < k) {
+        rows[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
+        ws[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
+    }
+    __syncthreads();
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float acc = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int r = rows[j];
+            if (r >= 0)
+                acc = fmaf(ws[j], z[(size_t)r * D + d], acc);
+        }
+        if (zs)
+            acc += zs[(size_t)t * D + d];
+        y[(size_t)t * D + d] = acc;
+    }
+}
+
+cudaError_t launch_combine(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                           const float *topk_w, void *y, cudaStream_t stream)
+{
+    const int32_t *row_of = reinterpret_cast<const int32_t *>(ws + L.row_of);
+    const int32_t *status = reinterpret_cast<const int32_t *>(ws + L.status);
+    const bool shared = c.d_shared > 0;
+    if (c.dtype == MOE_DTYPE_BF16)
+        return launch_pdl(combine_bf16_kernel, dim3(c.T), dim3(128), 0, stream,
+                          reinterpret_cast<const __nv_bfloat16 *>(ws + L.z),
+                          shared ? reinterpret_cast<const __nv_bfloat16 *>(ws + L.zs) : nullptr,
+                          topk_w, row_of, (__nv_bfloat16 *)y, c.top_k, c.d_model, status);
+    return launch_pdl(combine_f32_kernel, dim3(c.T), dim3(128), 0, stream,
+                      reinterpret_cast<const float *>(ws + L.z),
+                      shared ? reinterpret_cast<const float *>(ws + L.zs) : nullptr, topk_w,
+                      row_of, (float *)y, c.top_k, c.d_model, status);
+}
+
+}  // namespace moe

@@ -29,10 +29,13 @@ template <bool SWIGLU>
 __global__ void simt_seg_gemm_f32_kernel(const float *__restrict__ A, const float *__restrict__ B0,
                                          const float *__restrict__ B1, long long b_seg_elems,
                                          int N, int K, const int32_t *__restrict__ seg_off,
-                                         int nseg, int dense_rows, float *__restrict__ out)
+                                         int nseg, int dense_rows, float *__restrict__ out,
+                                         const int32_t *status)
 {
     griddep_wait();
     griddep_launch_dependents();
+    if (*(volatile const int32_t *)status != 0)
+        return;  // an earlier kernel failed
     const int n = blockIdx.x * blockDim.x + threadIdx.x;
     const int r = blockIdx.y * blockDim.y + threadIdx.y;
     const int rows = seg_off ? seg_off[nseg] : dense_rows;
@@ -66,6 +69,7 @@ cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, u
         return cudaErrorInvalidValue;
     const int D = c.d_model, F = c.d_expert, S = c.d_shared, E = c.n_experts;
     const int32_t *seg = reinterpret_cast<const int32_t *>(ws + L.seg_off);
+    const int32_t *status = reinterpret_cast<const int32_t *>(ws + L.status);
     float *xp = reinterpret_cast<float *>(ws + L.x_perm);
     float *h = reinterpret_cast<float *>(ws + L.h);
     float *z = reinterpret_cast<float *>(ws + L.z);
@@ -75,15 +79,15 @@ cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, u
     const int32_t *noseg = nullptr;
     cudaError_t err = launch_pdl(simt_seg_gemm_f32_kernel<true>, dim3((F + 31) / 32, rb), block, 0,
                                  stream, (const float *)xp, (const float *)W_gate,
-                                 (const float *)W_up, (long long)F * D, F, D, seg, E, 0, h);
+                                 (const float *)W_up, (long long)F * D, F, D, seg, E, 0, h, status);
     if (err == cudaSuccess)
-        err = record_stage(ev, 5, stream);
+        err = record_stage(ev, 3, stream);
     if (err == cudaSuccess)
         err = launch_pdl(simt_seg_gemm_f32_kernel<false>, dim3((D + 31) / 32, rb), block, 0,
                          stream, (const float *)h, (const float *)W_down, nil,
-                         (long long)D * F, D, F, seg, E, 0, z);
+                         (long long)D * F, D, F, seg, E, 0, z, status);
     if (err == cudaSuccess)
-        err = record_stage(ev, 6, stream);
+        err = record_stage(ev, 4, stream);
     if (err != cudaSuccess)
         return err;
     if (S > 0) {
@@ -92,20 +96,20 @@ cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, u
         const unsigned tb = (unsigned)((c.T + 7) / 8);
         err = launch_pdl(simt_seg_gemm_f32_kernel<true>, dim3((S + 31) / 32, tb), block, 0,
                          stream, (const float *)x, (const float *)Ws_gate, (const float *)Ws_up,
-                         0LL, S, D, noseg, 1, c.T, hs);
+                         0LL, S, D, noseg, 1, c.T, hs, status);
         if (err == cudaSuccess)
-            err = record_stage(ev, 7, stream);
+            err = record_stage(ev, 5, stream);
         if (err == cudaSuccess)
             err = launch_pdl(simt_seg_gemm_f32_kernel<false>, dim3((D + 31) / 32, tb), block, 0,
                              stream, (const float *)hs, (const float *)Ws_down, nil, 0LL, D, S,
-                             noseg, 1, c.T, zs);
+                             noseg, 1, c.T, zs, status);
         if (err == cudaSuccess)
-            err = record_stage(ev, 8, stream);
+            err = record_stage(ev, 6, stream);
         if (err != cudaSuccess)
             return err;
     } else {
-        record_stage(ev, 7, stream);
-        record_stage(ev, 8, stream);
+        record_stage(ev, 5, stream);
+        record_stage(ev, 6, stream);
     }
     return cudaGetLastError();
 }

@@ -39,7 +39,10 @@
 
 namespace moe {
 
-enum { EPI_F32 = 0, EPI_BF16 = 1, EPI_SWIGLU = 2 };
+// Epilogues: fp32 store (router scores), bf16 store (z), SiLU(gate) * up in
+// bf16 (h), and bf16 store of w_row * acc straight into the row's token of y
+// (down projection when every token has one expert and no shared expert).
+enum { EPI_F32 = 0, EPI_BF16 = 1, EPI_SWIGLU = 2, EPI_BF16_Y = 3 };
 
 struct TcParams {
     const int32_t *seg_off;  // grouped: [nseg+1] first A row of each segment; null = dense
@@ -52,6 +55,8 @@ struct TcParams {
     int b_seg_rows;          // B rows per segment (F or D), 0 when dense
     void *out;
     long long ld_out;        // output row stride, elements
+    const int32_t *row_tok;  // EPI_BF16_Y: token of each A row
+    const float *row_w;      // EPI_BF16_Y: gate weight of each A row
     int32_t *status;
 };
 
@@ -200,7 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // here on global memory written by the previous kernel is read
     griddep_wait();
     griddep_launch_dependents();
-    if (p.mtile) {
+    // an earlier kernel of this forward pass failed: do no work
+    const bool failed = *(volatile const int32_t *)p.status != 0;
+    if (p.mtile && !failed) {
         for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
             tables[i] = p.seg_off[i];
             tables[kMaxExperts + 1 + i] = p.mtile[i];
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int ntiles = tile_count(p, s_mt);
+    const int ntiles = failed ? 0 : tile_count(p, s_mt);
     const int nk = (p.K + 63) / 64;
 
     if (warp == 0) {
@@ -337,6 +344,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int col = ti.n_idx * BN + c0;
                         __nv_bfloat16 *dst =
                             reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * p.ld_out + col;
+                        store_row_bf16(dst, pk, col, p.N_valid);
+                    }
+                }
+            } else if constexpr (EPI == EPI_BF16_Y) {
+                int tok = 0;
+                float wr = 0.f;
+                if (row_ok) {
+                    tok = p.row_tok[orow];
+                    wr = p.row_w[orow];
+                }
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + c0, v);
+                    tmem_wait_ld();
+                    if (row_ok) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16x2(wr * __uint_as_float(v[2 * i]),
+                                                wr * __uint_as_float(v[2 * i + 1]));
+                        const int col = ti.n_idx * BN + c0;
+                        __nv_bfloat16 *dst =
+                            reinterpret_cast<__nv_bfloat16 *>(p.out) + (long long)tok * p.ld_out + col;
                         store_row_bf16(dst, pk, col, p.N_valid);
                     }
                 }
@@ -497,7 +528,7 @@ cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r
 cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                               const void *x, const void *W_gate, const void *W_up,
                               const void *W_down, const void *Ws_gate, const void *Ws_up,
-                              const void *Ws_down, cudaStream_t stream, cudaEvent_t *ev)
+                              const void *Ws_down, void *y, cudaStream_t stream, cudaEvent_t *ev)
 {
     const int D = c.d_model, F = c.d_expert, S = c.d_shared, E = c.n_experts, T = c.T;
     int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
@@ -529,7 +560,7 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
         p.status = status;
         err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_bound * p.n_tiles, stream);
         if (err == cudaSuccess)
-            err = record_stage(ev, 5, stream);
+            err = record_stage(ev, 3, stream);
         if (err != cudaSuccess)
             return err;
     }
@@ -551,10 +582,19 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
         p.out = z;
         p.ld_out = D;
         p.status = status;
-        err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt_bound * p.n_tiles, stream)
-                        : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt_bound * p.n_tiles, stream);
+        const long long tiles = mt_bound * p.n_tiles;
+        if (direct_y(c)) {
+            p.out = y;
+            p.row_tok = reinterpret_cast<const int32_t *>(ws + L.row_tok);
+            p.row_w = reinterpret_cast<const float *>(ws + L.row_w);
+            err = wide_down ? launch_tc<256, 1, EPI_BF16_Y, 4>(mA, mB, mB, p, tiles, stream)
+                            : launch_tc<128, 1, EPI_BF16_Y, 6>(mA, mB, mB, p, tiles, stream);
+        } else {
+            err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, tiles, stream)
+                            : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream);
+        }
         if (err == cudaSuccess)
-            err = record_stage(ev, 6, stream);
+            err = record_stage(ev, 4, stream);
         if (err != cudaSuccess)
             return err;
     }
@@ -578,7 +618,7 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.status = status;
             err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt * p.n_tiles, stream);
             if (err == cudaSuccess)
-                err = record_stage(ev, 7, stream);
+                err = record_stage(ev, 5, stream);
             if (err != cudaSuccess)
                 return err;
         }
@@ -600,14 +640,14 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt * p.n_tiles, stream)
                             : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt * p.n_tiles, stream);
             if (err == cudaSuccess)
-                err = record_stage(ev, 8, stream);
+                err = record_stage(ev, 6, stream);
             if (err != cudaSuccess)
                 return err;
         }
     } else {
-        err = record_stage(ev, 7, stream);
+        err = record_stage(ev, 5, stream);
         if (err == cudaSuccess)
-            err = record_stage(ev, 8, stream);
+            err = record_stage(ev, 6, stream);
         if (err != cudaSuccess)
             return err;
     }

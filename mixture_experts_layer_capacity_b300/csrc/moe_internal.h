@@ -27,6 +27,8 @@ struct WorkspaceLayout {
     size_t seg_off;  // int32[E+1]        first x_perm row of each expert's segment
     size_t mtile;    // int32[E+1]        prefix sum of 128-row tiles per segment
     size_t row_of;   // int32[T*k]        x_perm row of an assignment, -1 if dropped
+    size_t row_tok;  // int32[R_max]      token of each x_perm row (direct-y mode)
+    size_t row_w;    // float[R_max]      gate weight of each x_perm row (direct-y mode)
     size_t x_perm;   // dtype[R_max, D]   token rows gathered in expert order
     size_t h;        // dtype[R_max, F]   SwiGLU hidden rows of the routed experts
     size_t z;        // dtype[R_max, D]   routed expert outputs (unweighted)
@@ -42,21 +44,21 @@ moe_status validate_config(const moe_config *cfg);
 int64_t capacity_of(const moe_config *cfg);
 WorkspaceLayout layout_of(const moe_config *cfg);
 
-// Launchers (all enqueue on `stream`; return cudaGetLastError()).
+// Launchers (all enqueue on `stream`; return the launch's error).
 cudaError_t launch_router_simt(const moe_config &c, const void *x, const void *W_r,
                                float *logits, cudaStream_t stream);
-// True when the router GEMM runs inside the gating kernel (W_r staged in
-// shared memory); launch_gate then reads x and W_r itself.
+// True when the router GEMM runs inside the dispatch kernel (W_r staged in
+// shared memory: E <= 16 and E * d_model * elem_size <= 64 KiB).
 bool router_fused(const moe_config &c);
-cudaError_t launch_gate(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
-                        const void *x, const void *W_r, float *logits, const float *bias,
-                        int32_t *topk_idx, float *topk_w, cudaStream_t stream);
-cudaError_t launch_scan_finalize(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
-                                 int32_t *expert_counts, int32_t *kept_counts, float *aux_loss,
-                                 cudaStream_t stream);
-cudaError_t launch_scatter(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
-                           const void *x, const int32_t *topk_idx, uint8_t *dropped_mask,
-                           cudaStream_t stream);
+// True when the down projection writes y itself (k = 1, no shared expert, bf16):
+// each kept row goes straight to its token, scaled by its gate weight.
+bool direct_y(const moe_config &c);
+// Routing, capacity and dispatch in one cooperative kernel (see moe_dispatch.cu).
+cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                            const void *x, const void *W_r, bool fused, float *logits,
+                            const float *bias, int32_t *topk_idx, float *topk_w,
+                            uint8_t *dropped_mask, int32_t *expert_counts, int32_t *kept_counts,
+                            float *aux_loss, void *y, cudaStream_t stream);
 cudaError_t launch_combine(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                            const float *topk_w, void *y, cudaStream_t stream);
 cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
@@ -85,11 +87,11 @@ inline cudaError_t record_stage(cudaEvent_t *ev, int i, cudaStream_t stream)
 // if a tensor map cannot be encoded.
 cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r,
                              float *logits, int32_t *status, cudaStream_t stream);
-// `ev` (nullable): stage events 5..8 are recorded after each GEMM.
+// `ev` (nullable): stage events 3..6 are recorded after each GEMM.
 cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                               const void *x, const void *W_gate, const void *W_up,
                               const void *W_down, const void *Ws_gate, const void *Ws_up,
-                              const void *Ws_down, cudaStream_t stream,
+                              const void *Ws_down, void *y, cudaStream_t stream,
                               cudaEvent_t *ev = nullptr);
 
 int sm_count();
