@@ -144,6 +144,42 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
                        float *aux_loss, void *workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* Size of the library's static device scratch used by moe_forward_no_alloc. */
+#define MOE_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* The forward pass without a caller workspace, for callers that cannot
+ * allocate device memory: for example a host program that links only this C
+ * library and has no device allocator of its own, or a serving loop that must
+ * not call cudaMalloc in its steady state (cudaMalloc can synchronise the
+ * device).  (The pages have no counterpart to this entry point; it is a
+ * property of this library, not of the layer.)
+ *
+ * Same arguments and results as moe_forward, minus the workspace: the
+ * scratch is a 64 MiB array (MOE_STATIC_SCRATCH_BYTES) that the library holds
+ * in device memory on every GPU that loads it, until the process exits.  The
+ * function allocates nothing and calls no allocating routine.
+ *   - Layers whose moe_workspace_size exceeds MOE_STATIC_SCRATCH_BYTES are
+ *     rejected with MOE_ERR_WORKSPACE before anything is launched (for bf16:
+ *     roughly decode-sized batches of the large layers, and batches of a few
+ *     thousand tokens of small layers, fit).
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress, with the device current); make that first
+ *     call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     each call clears what must start at zero on its own stream.  Calls whose
+ *     work overlaps on the GPU (other streams, other host threads) race on
+ *     the array: serialise them.
+ *   - The device status word lives in the shared array, so
+ *     moe_read_device_status does not apply to this entry point. */
+MOE_API moe_status moe_forward_no_alloc(const moe_config *cfg,
+                       const void *x, const void *W_r, const float *router_bias,
+                       const void *W_gate, const void *W_up, const void *W_down,
+                       const void *Ws_gate, const void *Ws_up, const void *Ws_down,
+                       void *y, float *router_logits, int32_t *topk_idx,
+                       float *topk_w, uint8_t *dropped_mask,
+                       int32_t *expert_counts, int32_t *kept_counts,
+                       float *aux_loss, cudaStream_t stream);
+
 /* Waits for `stream`, then reads the device status word the last
  * moe_forward on this workspace wrote: *code = MOE_DEVICE_OK or one of the
  * MOE_DEVICE_* codes.  Returns MOE_ERR_DEVICE_STATUS when *code != 0,

@@ -67,6 +67,8 @@ def lib():
         L.moe_capacity.restype = ctypes.c_int64
         L.moe_forward.argtypes = [cfgp] + [vp] * 18 + [ctypes.c_size_t, vp]
         L.moe_forward.restype = ctypes.c_int
+        L.moe_forward_no_alloc.argtypes = [cfgp] + [vp] * 17 + [vp]
+        L.moe_forward_no_alloc.restype = ctypes.c_int
         L.moe_read_device_status.argtypes = [cfgp, vp, vp, ctypes.POINTER(ctypes.c_int32)]
         L.moe_read_device_status.restype = ctypes.c_int
         L.moe_set_stage_events.argtypes = [vp, ctypes.c_int]
@@ -154,6 +156,26 @@ def moe_forward(cfg: MoeConfig, x, W_r, router_bias, W_gate, W_up, W_down,
                            ctypes.c_size_t(int(workspace_bytes)), _stream(stream))
     if st != MOE_OK:
         raise MoeError(st, "moe_forward")
+
+
+STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def moe_forward_no_alloc(cfg: MoeConfig, x, W_r, router_bias, W_gate, W_up, W_down,
+                         Ws_gate, Ws_up, Ws_down, y, router_logits, topk_idx, topk_w,
+                         dropped_mask, expert_counts, kept_counts, aux_loss,
+                         stream=None) -> None:
+    """moe_forward without a workspace argument: the library uses its own
+    static device scratch (for callers that cannot allocate device memory).
+    Raises MoeError on a non-OK status (MOE_ERR_WORKSPACE when the layer
+    needs more than STATIC_SCRATCH_BYTES of scratch)."""
+    args = [x, W_r, router_bias, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y,
+            router_logits, topk_idx, topk_w, dropped_mask, expert_counts, kept_counts,
+            aux_loss]
+    st = lib().moe_forward_no_alloc(ctypes.byref(cfg), *[_ptr(a) for a in args],
+                                    _stream(stream))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_forward_no_alloc")
 
 
 def read_device_status(cfg: MoeConfig, workspace, stream=None) -> int:
