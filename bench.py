@@ -156,8 +156,11 @@ def stage_work(w, kept_total, touched):
 
 def profile_traffic(stage, workload):
     """DRAM bytes per launch of `stage` from a committed ncu summary, if the
-    summary was taken on the current GEMM source (else None)."""
-    src = os.path.join(ROOT, "mixture_experts_layer_capacity_b300", "csrc", "moe_gemm_tc.cu")
+    summary was taken on the current source of that stage's kernel (else
+    None)."""
+    src_name = {"dispatch": "moe_dispatch.cu", "combine": "moe_combine.cu",
+                "router": "moe_gemm_tc.cu"}.get(stage, "moe_gemm_tc.cu")
+    src = os.path.join(ROOT, "mixture_experts_layer_capacity_b300", "csrc", src_name)
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     except OSError:
