@@ -96,6 +96,7 @@ typedef struct {
 #define MOE_DEVICE_OK 0
 #define MOE_DEVICE_NONFINITE_SCORE 1   /* a router score was NaN/Inf */
 #define MOE_DEVICE_PIPELINE_TIMEOUT 2  /* a bounded in-kernel wait ran out */
+#define MOE_DEVICE_LAUNCH_MISMATCH 3   /* a kernel got less shared memory than its layout needs */
 
 /* Bytes of scratch moe_forward needs for `cfg` (x gathered by expert, the
  * SwiGLU hidden rows, per-expert scan tables, ...).  Returns

@@ -29,6 +29,7 @@ MOE_DTYPE_FP32 = 1
 MOE_DEVICE_OK = 0
 MOE_DEVICE_NONFINITE_SCORE = 1
 MOE_DEVICE_PIPELINE_TIMEOUT = 2
+MOE_DEVICE_LAUNCH_MISMATCH = 3
 
 
 class MoeError(RuntimeError):

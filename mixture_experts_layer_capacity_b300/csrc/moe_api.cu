@@ -62,7 +62,8 @@ WorkspaceLayout layout_of(const moe_config *c)
     const int64_t T = c->T, E = c->n_experts, k = c->top_k;
     const int64_t D = c->d_model, F = c->d_expert, S = c->d_shared;
     const size_t esz = c->dtype == MOE_DTYPE_BF16 ? 2 : 4;
-    L.nchunk = (int)((T + kChunk - 1) / kChunk);
+    L.nchunk = (int)std::max<int64_t>(std::min<int64_t>(T, kMaxDispatchBlocks),
+                                     (T + kChunk - 1) / kChunk);
     L.C = capacity_of(c);
     const int64_t TK = T * k;
     L.R_max = L.C < 0 ? TK : std::min<int64_t>(TK, E * L.C);
@@ -73,9 +74,9 @@ WorkspaceLayout layout_of(const moe_config *c)
         return o;
     };
     L.status = take(64);
-    L.hist = take(sizeof(int32_t) * E * L.nchunk);
+    L.bcount = take(sizeof(int32_t) * E * L.nchunk);
     L.ppart = take(sizeof(float) * E * L.nchunk);
-    L.rank = take((size_t)TK);
+    L.rank = take(sizeof(int32_t) * TK);
     L.psum = take(sizeof(double) * E);
     L.seg_off = take(sizeof(int32_t) * (E + 1));
     L.mtile = take(sizeof(int32_t) * (E + 1));
@@ -199,17 +200,25 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r,
     // 2. gating, demand counts, capacity, segments, balance loss, gather of x
     //    into expert order (one cooperative kernel)
     if (!cuda_ok(launch_dispatch(c, L, ws, x, W_r, fused, router_logits, router_bias, topk_idx,
-                                 topk_w, dropped_mask, expert_counts, kept_counts, aux_loss, y,
-                                 stream)) ||
+                                 topk_w, dropped_mask, expert_counts, kept_counts, y, stream)) ||
         !cuda_ok(record_stage(ev, 2, stream)))
         return MOE_ERR_CUDA;
-    // 3. experts (routed segments and the shared expert)
+    // 3. experts (routed segments and the shared expert); the first expert
+    //    kernel also evaluates the balance loss from the dispatch's sums
+    AuxArgs aux;
+    aux.psum = reinterpret_cast<const double *>(ws + L.psum);
+    aux.counts = expert_counts;
+    aux.out = aux_loss;
+    aux.E = E;
+    aux.T = c.T;
+    aux.k = c.top_k;
+    aux.alpha = c.aux_alpha;
     if (c.dtype == MOE_DTYPE_BF16)
         err = launch_experts_tc(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y,
-                                stream, ev);
+                                aux, stream, ev);
     else
         err = launch_experts_simt(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
-                                  stream, ev);
+                                  aux, stream, ev);
     if (!cuda_ok(err))
         return MOE_ERR_CUDA;
     // 4. weighted combine (+ shared expert), unless the down projection

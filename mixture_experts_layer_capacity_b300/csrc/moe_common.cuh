@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#include "moe_internal.h"
+
 namespace moe {
 
 __device__ __forceinline__ float to_f32(float v) { return v; }
@@ -50,6 +52,22 @@ __device__ __forceinline__ float warp_max(float v)
     for (int o = 16; o > 0; o >>= 1)
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
+}
+
+// The balance loss of AuxArgs, by one warp: lane l sums the terms of
+// experts l, l+32, ... in order, then a fixed butterfly; lane 0 writes it.
+__device__ __forceinline__ void balance_loss_warp(const AuxArgs &a)
+{
+    const int lane = threadIdx.x & 31;
+    double sum = 0.0;
+    for (int e = lane; e < a.E; e += 32)
+        sum += ((double)__ldcg(a.counts + e) / ((double)a.T * (double)a.k)) *
+               (__ldcg(a.psum + e) / (double)a.T);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0)
+        *a.out = (float)((double)a.alpha * (double)a.E * sum);
 }
 
 __device__ __forceinline__ void set_status(int32_t *status, int32_t code)

@@ -1,22 +1,29 @@
-// moe_dispatch.cu -- routing and dispatch in one cooperative kernel:
+// moe_dispatch.cu -- routing and dispatch in one cooperative kernel with a
+// single grid-wide barrier.  Block b owns a contiguous run of tokens (whole
+// chunks of cs = 8, 16 or 32 tokens):
 //
-//   phase 1 (gate):     per chunk of 32 tokens, one warp per token: (the
-//                       router GEMM itself when W_r fits in shared memory),
-//                       softmax over all E, top-k with the lower index first on
-//                       equal scores, gate weights, the chunk's per-expert
-//                       counts and probability sums, and each assignment's rank
-//                       among the chunk's earlier tokens;
-//   phase 2 (scan):     per expert, exclusive prefix of the chunk counts, so
-//                       that base + rank = the number of earlier tokens that
-//                       chose the expert; demand count n_e; P_sum_e.  The last
-//                       block to finish computes kept_e = min(n_e, C), the
-//                       segment offsets, the 128-row tile prefix and the
-//                       balance loss;
-//   phase 3 (scatter):  one warp per token: position of each assignment, the
-//                       capacity decision, and x copied into the rows of its
-//                       experts' segments.
-// Phases are separated by grid-wide barriers (all blocks are co-resident:
-// cooperative launch); every barrier wait is bounded in time.
+//   phase 1 (gate):     chunk by chunk, one warp per token: (the router GEMM
+//                       itself when W_r fits in shared memory), softmax over
+//                       all E, top-k with the lower index first on equal
+//                       scores, gate weights; the chunk's per-expert
+//                       probability sums; each assignment's rank among the
+//                       block's earlier tokens that chose the same expert
+//                       (a running count plus the popcount of a per-chunk
+//                       token bitmask); finally the block's per-expert counts;
+//   -- grid barrier --
+//   phase 2 (scatter):  every block reads all blocks' counts and derives,
+//                       identically, the demand counts n_e, kept_e = min(n_e, C),
+//                       the segment offsets and the 128-row tile prefix, plus
+//                       its own per-expert base (tokens of earlier blocks).
+//                       The global token-order position of an assignment is
+//                       base + rank; it is kept iff position < C.  The block
+//                       writes its assignments' rows and copies x into the
+//                       rows of its experts' segments.  Per-expert
+//                       probability sums (fp64, fixed order) are spread over
+//                       the blocks; the first expert kernel, which starts
+//                       after this one completes, evaluates the balance loss.
+// All blocks are co-resident (cooperative launch); the barrier wait is
+// bounded in time.
 //
 // Sources: "Mixture of Experts: More Parameters, Same FLOPs" ('The router');
 // "Mixture of Experts" (module 17), 17.2 (softmax over the selected vs over
@@ -34,10 +41,11 @@
 
 namespace moe {
 
-constexpr int kDispatchThreads = kChunk * 32;  // one warp per token of a chunk
+constexpr int kDispatchThreads = kChunk * 32;  // 32 warps: one per token of a chunk
 constexpr int kFusedMaxE = 16;
 constexpr int kFusedMaxWrBytes = 64 * 1024;
 constexpr uint64_t kBarrierLimitNs = 2000000000ull;
+constexpr size_t kStageMaxBytes = 96 * 1024;  // most x bytes a block stages in shared memory
 
 enum { ROUTER_NONE = 0, ROUTER_BF16 = 1, ROUTER_F32 = 2 };
 
@@ -46,7 +54,11 @@ struct DispatchParams {
     const float *bias;      // [E] or null
     const void *x;          // [T,D]
     const void *W_r;        // [E,D] (fused router only)
-    int T, E, k, mode, nchunk, D;
+    int T, E, k, mode, D;
+    int cs;                 // tokens per chunk (1, 2, 4, 8, 16 or 32)
+    int nchunk;             // ceil(T / cs)
+    int cpb;                // chunks per block
+    int x_staged;           // 1: the block's x rows are staged in shared memory (cpb == 1)
     long long C;            // capacity, -1 = dropless
     float alpha;
     size_t row_bytes;       // D * element size
@@ -55,10 +67,9 @@ struct DispatchParams {
     uint8_t *dropped;       // [T,k]
     int32_t *expert_counts; // [E]
     int32_t *kept_counts;   // [E]
-    float *aux_loss;        // [1]
-    int32_t *hist;          // [E][nchunk] chunk counts, then exclusive bases
-    float *ppart;           // [E][nchunk]
-    uint8_t *rank;          // [T*k]
+    int32_t *bcount;        // [E][gridDim.x] per-block expert counts
+    float *ppart;           // [E][nchunk] per-chunk probability sums
+    int32_t *rank;          // [T*k] rank among the block's earlier tokens of the expert
     double *psum;           // [E]
     int32_t *seg_off;       // [E+1]
     int32_t *mtile;         // [E+1]
@@ -67,7 +78,7 @@ struct DispatchParams {
     int32_t *row_tok;       // [R_max] token of each x_perm row (direct-y mode), or null
     float *row_w;           // [R_max] gate weight of each row (direct-y mode), or null
     uint8_t *y_zero;        // y [T,D]: rows of fully dropped tokens are zeroed (direct-y)
-    int32_t *status;        // [0] status word, [8] scan counter, [9] barrier counter
+    int32_t *status;        // [0] status word, [9] barrier counter
 };
 
 // ------------------------------------------------------------ block helpers
@@ -108,21 +119,6 @@ __device__ __forceinline__ int block_excl_scan(int v, int *sh, int *total)
     return r;
 }
 
-// Fixed-order tree sum of one double per thread (blockDim.x a power of two).
-__device__ __forceinline__ double block_sum(double v, double *sh)
-{
-    sh[threadIdx.x] = v;
-    __syncthreads();
-    for (int s = blockDim.x / 2; s > 0; s >>= 1) {
-        if ((int)threadIdx.x < s)
-            sh[threadIdx.x] += sh[threadIdx.x + s];
-        __syncthreads();
-    }
-    const double r = sh[0];
-    __syncthreads();
-    return r;
-}
-
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
 {
     unsigned v;
@@ -130,10 +126,10 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
     return v;
 }
 
-// Grid-wide barrier on a monotonically increasing counter; `target` = number
-// of arrivals this barrier completes at.  Bounded: on timeout the status word
-// records MOE_DEVICE_PIPELINE_TIMEOUT and false is returned (the caller then
-// stops; downstream kernels see the status and skip their work).
+// Grid-wide barrier on a counter that starts at zero; `target` = number of
+// blocks.  Bounded: on timeout the status word records
+// MOE_DEVICE_PIPELINE_TIMEOUT and false is returned (the caller then stops;
+// downstream kernels see the status and skip their work).
 __device__ bool grid_barrier(unsigned *counter, unsigned target, int32_t *status, int *sh_ok)
 {
     __syncthreads();
@@ -144,7 +140,7 @@ __device__ bool grid_barrier(unsigned *counter, unsigned target, int32_t *status
         if (ld_acquire(counter) < target) {
             const uint64_t t0 = global_timer_ns();
             while (ld_acquire(counter) < target) {
-                __nanosleep(64);
+                __nanosleep(32);
                 if (global_timer_ns() - t0 > kBarrierLimitNs) {
                     set_status(status, MOE_DEVICE_PIPELINE_TIMEOUT);
                     ok = false;
@@ -160,94 +156,301 @@ __device__ bool grid_barrier(unsigned *counter, unsigned target, int32_t *status
 }
 
 // ------------------------------------------------------------ fused router
-template <int RT>
-__device__ __forceinline__ void router_slice(const uint8_t *x_row, const uint8_t *wr_s, int D,
-                                             int E, int v, float (&acc)[kFusedMaxE])
+__device__ __forceinline__ void cvt8(const uint4 &q, float (&f)[8])
 {
-    float xf[8];
-    if (RT == ROUTER_BF16) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(x_row) + v);
-        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&q);
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&q);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __bfloat1622float2(h[i]);
-            xf[2 * i] = f.x;
-            xf[2 * i + 1] = f.y;
+    for (int i = 0; i < 4; ++i) {
+        const float2 g = __bfloat1622float2(h[i]);
+        f[2 * i] = g.x;
+        f[2 * i + 1] = g.y;
+    }
+}
+
+__device__ __forceinline__ void cvt8(const float4 &a, const float4 &b, float (&f)[8])
+{
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr)
+                 : "memory");
+    return r;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t r;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"(addr) : "memory");
+    return r;
+}
+
+// Eight consecutive elements (8-element vector v of a bf16 or fp32 row that
+// starts at shared-memory address `row`) as fp32.
+template <int RT>
+__device__ __forceinline__ void lds8(uint32_t row, int v, float (&f)[8])
+{
+    if (RT == ROUTER_BF16) {
+        cvt8(lds128(row + (uint32_t)v * 16u), f);
+    } else {
+        const uint4 a = lds128(row + (uint32_t)v * 32u), b = lds128(row + (uint32_t)v * 32u + 16u);
+        cvt8(make_float4(__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
+                         __uint_as_float(a.w)),
+             make_float4(__uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z),
+                         __uint_as_float(b.w)),
+             f);
+    }
+}
+
+// acc[e] += x[8v .. 8v+7] . W_r[r_e][8v .. 8v+7] for e < EM, r_e = min(e, E-1)
+// (W_r staged in shared memory at `wr`, row stride `wstride` bytes): no
+// branch on E, so the loads of all EM rows can be issued together; the sums
+// of e >= E are discarded later.
+template <int RT, int EM>
+__device__ __forceinline__ void router_fma(const float (&xf)[8], uint32_t wr, uint32_t wstride,
+                                           int E, int v, float (&acc)[EM])
+{
+#pragma unroll
+    for (int e = 0; e < EM; ++e) {
+        float wf[8];
+        lds8<RT>(wr + (uint32_t)min(e, E - 1) * wstride, v, wf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            acc[e] = fmaf(xf[i], wf[i], acc[e]);
+    }
+}
+
+// Sum of each of the EM values over the warp's 32 lanes, halving the vector
+// at each exchange (EM - 1 + 5 - log2(EM) shuffles instead of 5 * EM).
+// Afterwards lane L holds the sum of value L / (32 / EM).
+template <int EM>
+__device__ __forceinline__ float warp_sum_vector(float (&a)[EM])
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int half = EM / 2, o = 16; half >= 1; half /= 2, o /= 2) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = up ? a[i] : a[i + half];
+            const float keep = up ? a[i + half] : a[i];
+            a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float r = a[0];
+#pragma unroll
+    for (int o = 16 / EM; o > 0; o >>= 1)
+        r += __shfl_xor_sync(0xffffffffu, r, o);
+    return r;
+}
+
+// CUDA-core router, one warp's part of one token's scores: the 8-element
+// vectors part*32+lane, part*32+lane + nparts*32, ... of the token's row
+// against W_r (staged in shared memory).  The row is in shared memory
+// (x_smem, staged) or in global memory (x_glob; read several vectors at a
+// time so that the loads overlap).  Writes out[e] (e < E) = this part's sum.
+template <int RT, int EM>
+__device__ __forceinline__ void router_part(uint32_t x_smem, const uint8_t *x_glob, uint32_t wr,
+                                            uint32_t wstride, int D, int E, int part, int nparts,
+                                            float *out)
+{
+    const int lane = threadIdx.x & 31;
+    float acc[EM];
+#pragma unroll
+    for (int e = 0; e < EM; ++e)
+        acc[e] = 0.f;
+    const int nv = D / 8, step = nparts * 32;
+    if (!x_glob) {
+        for (int v = part * 32 + lane; v < nv; v += step) {
+            float xf[8];
+            lds8<RT>(x_smem, v, xf);
+            router_fma<RT, EM>(xf, wr, wstride, E, v, acc);
         }
     } else {
-        const float4 *xr = reinterpret_cast<const float4 *>(x_row) + 2 * v;
-        const float4 a = __ldg(xr), b = __ldg(xr + 1);
-        xf[0] = a.x; xf[1] = a.y; xf[2] = a.z; xf[3] = a.w;
-        xf[4] = b.x; xf[5] = b.y; xf[6] = b.z; xf[7] = b.w;
+        constexpr int B = RT == ROUTER_BF16 ? 4 : 2;
+        for (int v0 = part * 32 + lane; v0 < nv; v0 += step * B) {
+            if (RT == ROUTER_BF16) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(x_glob);
+                uint4 q[B];
+#pragma unroll
+                for (int u = 0; u < B; ++u)
+                    if (v0 + step * u < nv)
+                        q[u] = __ldg(src + v0 + step * u);
+#pragma unroll
+                for (int u = 0; u < B; ++u)
+                    if (v0 + step * u < nv) {
+                        float xf[8];
+                        cvt8(q[u], xf);
+                        router_fma<RT, EM>(xf, wr, wstride, E, v0 + step * u, acc);
+                    }
+            } else {
+                const float4 *src = reinterpret_cast<const float4 *>(x_glob);
+                float4 qa[B], qb[B];
+#pragma unroll
+                for (int u = 0; u < B; ++u)
+                    if (v0 + step * u < nv) {
+                        qa[u] = __ldg(src + 2 * (v0 + step * u));
+                        qb[u] = __ldg(src + 2 * (v0 + step * u) + 1);
+                    }
+#pragma unroll
+                for (int u = 0; u < B; ++u)
+                    if (v0 + step * u < nv) {
+                        float xf[8];
+                        cvt8(qa[u], qb[u], xf);
+                        router_fma<RT, EM>(xf, wr, wstride, E, v0 + step * u, acc);
+                    }
+            }
+        }
+    }
+    const float r = warp_sum_vector<EM>(acc);
+    constexpr int kGroup = 32 / EM;
+    const int e = lane / kGroup;
+    if (lane % kGroup == 0 && e < E)
+        out[e] = r;
+}
+
+// D += A * B on the tensor cores, m16n8k16, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+constexpr int kRouterMmaWarps = 8;
+
+// Tensor-core router for bf16: scores of the chunk's nt (<= 32) tokens,
+// staged in shared memory (rows at xs, stride xstride bytes), against W_r
+// (rows at wr, stride wstride).  Warp q < kRouterMmaWarps takes the 16-wide
+// k-steps q, q+8, ... of D; the A fragments are token rows (tokens >= nt
+// read as zero), the B fragments W_r rows (rows >= E clamped to E-1, their
+// sums unused).  Writes this warp's partial sums to rp[(q*32 + token)*16 + e].
+template <int EM>
+__device__ __forceinline__ void router_mma(uint32_t xs, uint32_t xstride, int nt, uint32_t wr,
+                                           uint32_t wstride, int D, int E, int q, float *rp)
+{
+    constexpr int NT = EM > 8 ? 2 : 1;  // 8-expert n-tiles
+    const int lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
+    const int mt = nt > 16 ? 2 : 1;
+    float c[2][NT][4];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                c[m][n][i] = 0.f;
+    for (int ks = q; ks < D / 16; ks += kRouterMmaWarps) {
+        const uint32_t kb = (uint32_t)(ks * 16 + tq * 2) * 2u;
+        uint32_t b[NT][2];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const uint32_t row = wr + (uint32_t)min(n * 8 + g, E - 1) * wstride + kb;
+            b[n][0] = lds32(row);
+            b[n][1] = lds32(row + 16u);
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            if (m < mt) {
+                const int r0 = m * 16 + g, r1 = r0 + 8;
+                const uint32_t a0 = r0 < nt ? lds32(xs + (uint32_t)r0 * xstride + kb) : 0u;
+                const uint32_t a1 = r1 < nt ? lds32(xs + (uint32_t)r1 * xstride + kb) : 0u;
+                const uint32_t a2 = r0 < nt ? lds32(xs + (uint32_t)r0 * xstride + kb + 16u) : 0u;
+                const uint32_t a3 = r1 < nt ? lds32(xs + (uint32_t)r1 * xstride + kb + 16u) : 0u;
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+                    mma_16816(c[m][n], a0, a1, a2, a3, b[n][0], b[n][1]);
+            }
+        }
     }
 #pragma unroll
-    for (int e = 0; e < kFusedMaxE; ++e) {
-        if (e < E) {
-            float wf[8];
-            if (RT == ROUTER_BF16) {
-                const uint4 q = reinterpret_cast<const uint4 *>(wr_s + (size_t)e * D * 2)[v];
-                const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&q);
+    for (int m = 0; m < 2; ++m) {
+        if (m < mt) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 f = __bfloat1622float2(h[i]);
-                    wf[2 * i] = f.x;
-                    wf[2 * i + 1] = f.y;
+            for (int n = 0; n < NT; ++n) {
+                const int r0 = m * 16 + g, col = n * 8 + tq * 2;
+                if (r0 < nt) {
+                    rp[(q * 32 + r0) * kFusedMaxE + col] = c[m][n][0];
+                    rp[(q * 32 + r0) * kFusedMaxE + col + 1] = c[m][n][1];
                 }
-            } else {
-                const float4 *wr = reinterpret_cast<const float4 *>(wr_s + (size_t)e * D * 4) + 2 * v;
-                const float4 a = wr[0], b = wr[1];
-                wf[0] = a.x; wf[1] = a.y; wf[2] = a.z; wf[3] = a.w;
-                wf[4] = b.x; wf[5] = b.y; wf[6] = b.z; wf[7] = b.w;
+                if (r0 + 8 < nt) {
+                    rp[(q * 32 + r0 + 8) * kFusedMaxE + col] = c[m][n][2];
+                    rp[(q * 32 + r0 + 8) * kFusedMaxE + col + 1] = c[m][n][3];
+                }
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                acc[e] = fmaf(xf[i], wf[i], acc[e]);
         }
     }
 }
 
+// Integer key with the order of the finite floats (-0 and +0 equal).
+__device__ __forceinline__ int order_key(float v)
+{
+    const int i = __float_as_int(v + 0.0f);
+    return i >= 0 ? i : i ^ 0x7FFFFFFF;
+}
+
+__device__ __forceinline__ float key_value(int key)
+{
+    return __int_as_float(key >= 0 ? key : key ^ 0x7FFFFFFF);
+}
+
 // ------------------------------------------------------------ phase 1: gate
-// Routes token t (one warp); returns nothing, writes outputs and the chunk's
-// shared-memory statistics (pbuf row, mask bits, ibuf row).
+// Routes token t (one warp, slot tt of the chunk); writes the per-token
+// outputs and the chunk's shared-memory statistics (pbuf row, mask bits,
+// ibuf row).  x_row: the token's row (shared or global memory).
+// rpart: the token's router partial sums (fused router), nparts of them at
+// a stride of pstride floats, summed in order.
 template <int EPL, int RT>
-__device__ __forceinline__ void gate_token(const DispatchParams &p, const uint8_t *wr_s, int t,
-                                           int tt, float *pbuf, int32_t *ibuf, uint32_t *mask)
+__device__ __forceinline__ void gate_token(const DispatchParams &p, const float *rpart,
+                                           int nparts, int pstride, int t, int tt, float *pbuf,
+                                           int32_t *ibuf, float *wbuf, uint32_t *mask)
 {
     const int lane = threadIdx.x & 31;
     const int E = p.E, k = p.k;
     float s[EPL];
-    if constexpr (RT != ROUTER_NONE) {
-        float acc[kFusedMaxE];
+    // scores: the fused router's partial sums (parts in order), or the
+    // router GEMM's output; then the optional bias.  All loads come before
+    // the stores to the scores so that they overlap.
 #pragma unroll
-        for (int e = 0; e < kFusedMaxE; ++e)
-            acc[e] = 0.f;
-        const uint8_t *x_row = static_cast<const uint8_t *>(p.x) + (size_t)t * p.row_bytes;
-        for (int v = lane; v < p.D / 8; v += 32)
-            router_slice<RT>(x_row, wr_s, p.D, E, v, acc);
-        s[0] = -FLT_MAX;
-#pragma unroll
-        for (int e = 0; e < kFusedMaxE; ++e) {
-            if (e < E) {
-                const float v = warp_sum_bcast(acc[e]);
-                if (lane == e)
-                    s[0] = v;
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        float v = -FLT_MAX;
+        if (e < E) {
+            if (RT != ROUTER_NONE) {
+                v = rpart[e];
+                for (int q = 1; q < nparts; ++q)
+                    v += rpart[q * pstride + e];
+            } else {
+                v = p.logits[(size_t)t * E + e];
             }
         }
+        s[i] = v;
+    }
+    if (p.bias) {
+        float bv[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+            bv[i] = lane + 32 * i < E ? __ldg(p.bias + lane + 32 * i) : 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+            s[i] += bv[i];
     }
     bool bad = false;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
         if (e < E) {
-            float v = (RT != ROUTER_NONE) ? s[i] : p.logits[(size_t)t * E + e];
-            if (p.bias)
-                v += p.bias[e];
             if (RT != ROUTER_NONE || p.bias)
-                p.logits[(size_t)t * E + e] = v;
-            bad |= !isfinite(v);
-            s[i] = v;
-        } else {
-            s[i] = -FLT_MAX;
+                p.logits[(size_t)t * E + e] = s[i];
+            bad |= !isfinite(s[i]);
         }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0)
@@ -275,217 +478,363 @@ __device__ __forceinline__ void gate_token(const DispatchParams &p, const uint8_
             pbuf[tt * E + e] = ex[i] / z;
     }
 
-    // top-k: k rounds of a warp arg-max; equal scores go to the lower index
+    // top-k: k rounds of a warp arg-max over order keys (redux max), equal
+    // scores resolved to the lower expert index (redux min); lane j keeps
+    // round j's expert and score
+    int key[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+        key[i] = (lane + 32 * i < E) ? order_key(s[i]) : INT_MIN;
     uint32_t taken = 0u;
-    float sel_s[kMaxTopK];
-    int sel_e[kMaxTopK];
+    float my_s = 0.f, s_top = 0.f;
+    int my_e = 0;
+    for (int j = 0; j < k; ++j) {
+        int bk = INT_MIN, be = INT_MAX;
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-        sel_s[j] = 0.f;
-        sel_e[j] = 0;
-        if (j < k) {
-            float bv = -FLT_MAX;
-            int be = INT_MAX;
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && !((taken >> i) & 1u)) {
-                    if (be == INT_MAX || s[i] > bv) {
-                        bv = s[i];
-                        be = e;
-                    }
-                }
+        for (int i = 0; i < EPL; ++i) {
+            if (lane + 32 * i < E && !((taken >> i) & 1u) && (be == INT_MAX || key[i] > bk)) {
+                bk = key[i];
+                be = lane + 32 * i;
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if (be == INT_MAX || be >= E)
-                be = 0;  // unreachable with k <= E; keeps indices in bounds
-            sel_s[j] = bv;
-            sel_e[j] = be;
-            if ((be & 31) == lane)
-                taken |= 1u << (be >> 5);
+        }
+        const int mk = __reduce_max_sync(0xffffffffu, bk);
+        int win = __reduce_min_sync(0xffffffffu, bk == mk ? be : INT_MAX);
+        if (win == INT_MAX || win >= E)
+            win = 0;  // unreachable with k <= E; keeps indices in bounds
+        if ((win & 31) == lane)
+            taken |= 1u << (win >> 5);
+        const float sv = key_value(mk);
+        if (j == 0)
+            s_top = sv;
+        if (lane == j) {
+            my_s = sv;
+            my_e = win;
         }
     }
 
-    // gate weights (every lane computes the same values)
-    float w[kMaxTopK];
+    // gate weights, lane j for assignment j
+    float w = 0.f;
     if (p.mode == MOE_GATE_SOFTMAX_SELECTED) {
-        float zs = 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-            w[j] = (j < k) ? expf(sel_s[j] - sel_s[0]) : 0.f;
-            zs += w[j];
-        }
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-            w[j] = w[j] / zs;
+        const float ev = lane < k ? expf(my_s - s_top) : 0.f;
+        w = ev / warp_sum_bcast(ev);
     } else {
-        float zs = 0.f;
+        w = lane < k ? expf(my_s - m) / z : 0.f;
+        if (p.mode == MOE_GATE_SOFTMAX_ALL_RENORM)
+            w = w / warp_sum_bcast(w);
+    }
+    if (lane < k) {
+        p.topk_idx[(size_t)t * k + lane] = my_e;
+        p.topk_w[(size_t)t * k + lane] = w;
+        atomicOr(&mask[my_e], 1u << tt);
+        ibuf[tt * k + lane] = my_e;
+        wbuf[tt * k + lane] = w;
+    }
+}
+
+// ---------------------------------------------------------- phase 2 helpers
+// Copies token t's x row (src: shared or global memory) into its kept rows
+// of x_perm; this warp handles the 16-byte vectors part*32+lane, stepping by
+// nparts*32 (four loads in flight before their stores).
+__device__ __forceinline__ void copy_row(const DispatchParams &p, const uint8_t *src,
+                                         const long long (&rows)[kMaxTopK], int part, int nparts)
+{
+    const int lane = threadIdx.x & 31, k = p.k;
+    const size_t nv = p.row_bytes / 16;
+    if (nv * 16 == p.row_bytes) {
+        const size_t step = (size_t)nparts * 32;
+        size_t v = (size_t)part * 32 + lane;
+        for (; v + 3 * step < nv; v += 4 * step) {
+            uint4 q[4];
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-            w[j] = (j < k) ? expf(sel_s[j] - m) / z : 0.f;
-            zs += w[j];
-        }
-        if (p.mode == MOE_GATE_SOFTMAX_ALL_RENORM) {
+            for (int u = 0; u < 4; ++u)
+                q[u] = reinterpret_cast<const uint4 *>(src)[v + u * step];
 #pragma unroll
             for (int j = 0; j < kMaxTopK; ++j)
-                w[j] = w[j] / zs;
-        }
-    }
+                if (j < k && rows[j] >= 0) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.x_perm + (size_t)rows[j] * p.row_bytes);
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-        if (j < k && lane == j) {
-            p.topk_idx[(size_t)t * k + j] = sel_e[j];
-            p.topk_w[(size_t)t * k + j] = w[j];
-            atomicOr(&mask[sel_e[j]], 1u << tt);
-            ibuf[tt * k + j] = sel_e[j];
+                    for (int u = 0; u < 4; ++u)
+                        dst[v + u * step] = q[u];
+                }
+        }
+        for (; v < nv; v += step) {
+            const uint4 q = reinterpret_cast<const uint4 *>(src)[v];
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j)
+                if (j < k && rows[j] >= 0)
+                    reinterpret_cast<uint4 *>(p.x_perm + (size_t)rows[j] * p.row_bytes)[v] = q;
+        }
+    } else {  // fp32 rows whose size is not a multiple of 16 bytes
+        const size_t nw = p.row_bytes / 4;
+        for (size_t v = (size_t)part * 32 + lane; v < nw; v += (size_t)nparts * 32) {
+            const uint32_t q = reinterpret_cast<const uint32_t *>(src)[v];
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j)
+                if (j < k && rows[j] >= 0)
+                    reinterpret_cast<uint32_t *>(p.x_perm + (size_t)rows[j] * p.row_bytes)[v] = q;
         }
     }
 }
 
+// Probability sums of the experts e = b, b+G, ... (this warp; fp64, lanes
+// over chunks in a fixed order, then a fixed butterfly).  The balance loss
+// itself is evaluated by the first expert kernel.
+__device__ __forceinline__ void prob_sums(const DispatchParams &p, int b, int G)
+{
+    const int lane = threadIdx.x & 31, E = p.E;
+    for (int e = b; e < E; e += G) {
+        const float *pp = p.ppart + (size_t)e * p.nchunk;
+        double acc = 0.0;
+        for (int c0 = lane; c0 < p.nchunk; c0 += 32 * 4) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = c0 + 32 * u < p.nchunk ? __ldcg(pp + c0 + 32 * u) : 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                acc += (double)v[u];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0)
+            p.psum[e] = acc;
+    }
+}
+
 // --------------------------------------------------------- the whole kernel
-template <int EPL, int RT>
+// EPL: experts per lane (ceil(E / 32)); RT: fused router type; EM: the
+// fused router's expert count rounded up to 4, 8 or 16.
+template <int EPL, int RT, int EM>
 __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchParams p)
 {
     extern __shared__ __align__(16) uint8_t dsm[];
     __shared__ int sh_int[33];
-    __shared__ double sh_dbl[kDispatchThreads];
     __shared__ int sh_flag;
-    const int E = p.E, k = p.k;
-    const size_t wr_bytes =
-        RT == ROUTER_NONE ? 0 : (size_t)E * p.D * (RT == ROUTER_BF16 ? 2 : 4);
-    float *pbuf = reinterpret_cast<float *>(dsm + wr_bytes);
-    int32_t *ibuf = reinterpret_cast<int32_t *>(pbuf + kChunk * E);
-    uint32_t *mask = reinterpret_cast<uint32_t *>(ibuf + kChunk * k);
-    unsigned *bar_counter = reinterpret_cast<unsigned *>(p.status + 9);
-    const unsigned G = gridDim.x;
+    const int E = p.E, k = p.k, cs = p.cs;
+    // staged rows carry 16 bytes of padding so that the tensor-core router's
+    // fragment loads from consecutive rows fall in different banks
+    const uint32_t wrow = RT == ROUTER_NONE ? 0u : (uint32_t)p.D * (RT == ROUTER_BF16 ? 2u : 4u);
+    const uint32_t wstride = wrow + 16u;
+    const size_t wr_bytes = RT == ROUTER_NONE ? 0 : (size_t)E * wstride;
+    const uint32_t xstride = (uint32_t)p.row_bytes + 16u;
+    const int G = gridDim.x, b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if constexpr (RT != ROUTER_NONE) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.W_r);
-        uint4 *dst = reinterpret_cast<uint4 *>(dsm);
-        for (size_t i = threadIdx.x; i < wr_bytes / 16; i += blockDim.x)
-            dst[i] = __ldg(src + i);
+    const int c_beg = b * p.cpb, c_end = min(p.nchunk, c_beg + p.cpb);
+    const int t_beg = c_beg * cs, t_end = min(p.T, c_end * cs);
+    const int ntok = t_end - t_beg;
+    const size_t xs_bytes = p.x_staged ? (size_t)cs * xstride : 0;
+    uint8_t *xs = dsm + wr_bytes;                                   // staged x rows
+    float *pbuf = reinterpret_cast<float *>(xs + xs_bytes);         // [cs][E]
+    int32_t *ibuf = reinterpret_cast<int32_t *>(pbuf + kChunk * E); // [cs][k]
+    uint32_t *mask = reinterpret_cast<uint32_t *>(ibuf + kChunk * k);  // [E]
+    int32_t *run = reinterpret_cast<int32_t *>(mask + E);          // [E] block-local counts
+    int32_t *s_base = run + E;                                      // [E] counts of earlier blocks
+    int32_t *s_n = s_base + E;                                      // [E] demand counts
+    int32_t *s_seg = s_n + E;                                       // [E+1] segment offsets
+    float *rpart = reinterpret_cast<float *>(s_seg + E + 1);        // [8][32][16] router parts
+    int32_t *rbuf = reinterpret_cast<int32_t *>(rpart + kRouterMmaWarps * kChunk * kFusedMaxE);
+    float *wbuf = reinterpret_cast<float *>(rbuf + kChunk * kMaxTopK);  // [32][k] ranks, weights
+    unsigned *bar_counter = reinterpret_cast<unsigned *>(p.status + 9);
+    // the layout above must fit the shared memory this launch received (the
+    // same test in every block, so no block is left waiting at the barrier)
+    if ((size_t)(reinterpret_cast<uint8_t *>(wbuf + kChunk * kMaxTopK) - dsm) >
+        dynamic_smem_bytes()) {
+        if (b == 0 && threadIdx.x == 0)
+            set_status(p.status, MOE_DEVICE_LAUNCH_MISMATCH);
+        return;
     }
 
-    // ---- phase 1: gate, chunk by chunk
-    for (int chunk = blockIdx.x; chunk < p.nchunk; chunk += G) {
+    // W_r (fused router) and this block's x rows (when staged) into shared
+    // memory, four 16-byte loads in flight per thread
+    {
+        const long long vpw = wrow > 0 ? wrow / 16 : 1, vpx = (long long)(p.row_bytes / 16);
+        const long long n_w = RT == ROUTER_NONE ? 0 : (long long)E * vpw;
+        const long long n = n_w + (p.x_staged ? (long long)ntok * vpx : 0);
+        const uint4 *wsrc = reinterpret_cast<const uint4 *>(p.W_r);
+        const uint4 *xsrc = reinterpret_cast<const uint4 *>(
+            static_cast<const uint8_t *>(p.x) + (size_t)t_beg * p.row_bytes);
+        for (long long i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {
+            uint4 q[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const long long i = i0 + (long long)u * blockDim.x;
+                if (i < n_w)
+                    q[u] = __ldg(wsrc + i);
+                else if (i < n)
+                    q[u] = __ldg(xsrc + (i - n_w));
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const long long i = i0 + (long long)u * blockDim.x;
+                if (i < n_w)
+                    *reinterpret_cast<uint4 *>(dsm + (i / vpw) * wstride + (i % vpw) * 16) = q[u];
+                else if (i < n)
+                    *reinterpret_cast<uint4 *>(xs + ((i - n_w) / vpx) * xstride +
+                                               ((i - n_w) % vpx) * 16) = q[u];
+            }
+        }
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        run[e] = 0;
+
+    // ---- phase 1: gate this block's chunks in token order
+    for (int chunk = c_beg; chunk < c_end; ++chunk) {
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             mask[e] = 0u;
         __syncthreads();
-        const int t = chunk * kChunk + warp;
-        if (t < p.T) {
-            gate_token<EPL, RT>(p, dsm, t, warp, pbuf, ibuf, mask);
-        } else {
-            for (int e = lane; e < E; e += 32)
-                pbuf[warp * E + e] = 0.f;
+        // fused router: on the tensor cores for staged bf16 rows, else on
+        // the CUDA cores with 32 / cs warps per token, each over a slice of D
+        const bool mma_router = RT == ROUTER_BF16 && p.x_staged && cs >= 8;
+        const int wpt = kChunk / cs;
+        if constexpr (RT != ROUTER_NONE) {
+            const uint32_t wr = smem_u32(dsm);
+            if (mma_router) {
+                if (warp < kRouterMmaWarps)
+                    router_mma<EM>(smem_u32(xs), xstride, min(cs, p.T - chunk * cs), wr, wstride,
+                                   p.D, E, warp, rpart);
+            } else {
+                const int tt = warp / wpt, part = warp - (warp / wpt) * wpt;
+                const int t = chunk * cs + tt;
+                if (t < p.T) {
+                    const uint32_t x_smem = smem_u32(xs) + (uint32_t)(t - t_beg) * xstride;
+                    const uint8_t *x_glob =
+                        p.x_staged ? nullptr
+                                   : static_cast<const uint8_t *>(p.x) + (size_t)t * p.row_bytes;
+                    router_part<RT, EM>(x_smem, x_glob, wr, wstride, p.D, E, part, wpt,
+                                        rpart + (size_t)warp * kFusedMaxE);
+                }
+            }
+            __syncthreads();
         }
-        __syncthreads();
-        for (int e = threadIdx.x; e < E; e += blockDim.x) {
-            p.hist[(size_t)e * p.nchunk + chunk] = __popc(mask[e]);
-            float acc = 0.f;
-#pragma unroll 8
-            for (int u = 0; u < kChunk; ++u)
-                acc += pbuf[u * E + e];
-            p.ppart[(size_t)e * p.nchunk + chunk] = acc;
-        }
-        for (int i = threadIdx.x; i < kChunk * k; i += blockDim.x) {
-            const int u = i / k, j = i % k;
-            const int tok = chunk * kChunk + u;
-            if (tok < p.T) {
-                const int e = ibuf[u * k + j];
-                p.rank[(size_t)tok * k + j] = (uint8_t)__popc(mask[e] & ((1u << u) - 1u));
+        const int t = chunk * cs + warp;
+        if (warp < cs) {
+            if (t < p.T) {
+                if (mma_router)
+                    gate_token<EPL, RT>(p, rpart + (size_t)warp * kFusedMaxE, kRouterMmaWarps,
+                                        kChunk * kFusedMaxE, t, warp, pbuf, ibuf, wbuf, mask);
+                else
+                    gate_token<EPL, RT>(p, rpart + (size_t)warp * wpt * kFusedMaxE, wpt,
+                                        kFusedMaxE, t, warp, pbuf, ibuf, wbuf, mask);
+            } else {
+                for (int e = lane; e < E; e += 32)
+                    pbuf[warp * E + e] = 0.f;
             }
         }
         __syncthreads();
-    }
-    if (!grid_barrier(bar_counter, G, p.status, &sh_flag))
-        return;
-
-    // ---- phase 2: per-expert scan; the last expert done finalizes
-    for (int e = blockIdx.x; e < E; e += G) {
-        int32_t *h = p.hist + (size_t)e * p.nchunk;
-        const float *pp = p.ppart + (size_t)e * p.nchunk;
-        const int per = (p.nchunk + blockDim.x - 1) / blockDim.x;
-        const int beg = min(p.nchunk, (int)threadIdx.x * per);
-        const int end = min(p.nchunk, beg + per);
-        int local = 0;
-        double pl = 0.0;
-        for (int c = beg; c < end; ++c) {
-            local += __ldcg(h + c);
-            pl += (double)__ldcg(pp + c);
+        // ranks: tokens of earlier chunks of this block (run, before this
+        // chunk's counts are added) plus earlier tokens of this chunk
+        for (int i = threadIdx.x; i < cs * k; i += blockDim.x) {
+            const int u = i / k, j = i - (i / k) * k;
+            const int tok = chunk * cs + u;
+            if (tok < p.T) {
+                const int e = ibuf[u * k + j];
+                const int r = run[e] + __popc(mask[e] & ((1u << u) - 1u));
+                p.rank[(size_t)tok * k + j] = r;
+                rbuf[u * k + j] = r;
+            }
         }
-        int total;
-        int run = block_excl_scan(local, sh_int, &total);
-        for (int c = beg; c < end; ++c) {
-            const int v = __ldcg(h + c);
-            h[c] = run;
-            run += v;
-        }
-        const double ps = block_sum(pl, sh_dbl);
-        if (threadIdx.x == 0) {
-            p.expert_counts[e] = total;
-            p.psum[e] = ps;
-            __threadfence();
-            sh_flag = (atomicAdd(reinterpret_cast<unsigned *>(p.status + 8), 1u) ==
-                       (unsigned)E - 1u);
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            float acc = 0.f;
+            for (int u = 0; u < cs; ++u)
+                acc += pbuf[u * E + e];
+            p.ppart[(size_t)e * p.nchunk + chunk] = acc;
         }
         __syncthreads();
-        if (sh_flag) {
-            __threadfence();
-            const int x = threadIdx.x;  // this thread's expert in the finalize
-            const int n = x < E ? __ldcg(p.expert_counts + x) : 0;
-            const int kept = (p.C < 0) ? n : (int)min((long long)n, p.C);
-            if (x < E)
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            run[e] += __popc(mask[e]);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        p.bcount[(size_t)e * G + b] = run[e];
+    if (!grid_barrier(bar_counter, (unsigned)G, p.status, &sh_flag))
+        return;
+
+    // ---- phase 2a: per expert, tokens of earlier blocks and the total
+    // (warp w: experts w, w+32, ..., four at a time)
+    for (int e0 = warp; e0 < E; e0 += 32 * 4) {
+        int pre[4] = {0, 0, 0, 0}, tot[4] = {0, 0, 0, 0};
+        for (int bb = lane; bb < G; bb += 32) {
+            int v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = e0 + 32 * u;
+                v[u] = e < E ? __ldcg(p.bcount + (size_t)e * G + bb) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                tot[u] += v[u];
+                pre[u] += bb < b ? v[u] : 0;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + 32 * u;
+            const int ps = __reduce_add_sync(0xffffffffu, pre[u]);
+            const int ts = __reduce_add_sync(0xffffffffu, tot[u]);
+            if (lane == 0 && e < E) {
+                s_base[e] = ps;
+                s_n[e] = ts;
+            }
+        }
+    }
+    __syncthreads();
+    // ---- phase 2b: kept counts, segment offsets, 128-row tile prefix (the
+    // same in every block; block 0 publishes them)
+    {
+        const int x = threadIdx.x;
+        const int n = x < E ? s_n[x] : 0;
+        const int kept = (p.C < 0) ? n : (int)min((long long)n, p.C);
+        int tot;
+        const int off = block_excl_scan(kept, sh_int, &tot);
+        if (x < E)
+            s_seg[x] = off;
+        if (x == 0)
+            s_seg[E] = tot;
+        const int mt = (kept + kTileM - 1) / kTileM;
+        int mt_total;
+        const int moff = block_excl_scan(mt, sh_int, &mt_total);
+        if (b == 0) {
+            if (x < E) {
+                p.expert_counts[x] = n;
                 p.kept_counts[x] = kept;
-            int tot;
-            const int off = block_excl_scan(kept, sh_int, &tot);
-            if (x < E)
                 p.seg_off[x] = off;
-            if (x == 0)
-                p.seg_off[E] = tot;
-            const int mt = (kept + kTileM - 1) / kTileM;
-            int mt_total;
-            const int moff = block_excl_scan(mt, sh_int, &mt_total);
-            if (x < E)
                 p.mtile[x] = moff;
-            if (x == 0)
+            }
+            if (x == 0) {
+                p.seg_off[E] = tot;
                 p.mtile[E] = mt_total;
-            double term = 0.0;
-            if (x < E && p.T > 0)
-                term = ((double)n / ((double)p.T * (double)k)) *
-                       (__ldcg(p.psum + x) / (double)p.T);
-            const double sum = block_sum(term, sh_dbl);
-            if (x == 0)
-                *p.aux_loss = (float)((double)p.alpha * (double)E * sum);
+            }
         }
-        __syncthreads();
     }
-    if (!grid_barrier(bar_counter, 2 * G, p.status, &sh_flag))
-        return;
+    __syncthreads();
 
-    // ---- phase 3: scatter, one warp per token
-    const size_t nv = p.row_bytes / 16;
-    for (int t = blockIdx.x * kChunk + warp; t < p.T; t += G * kChunk) {
+    // ---- phase 2c/2d: the last warp computes this block's probability sums;
+    // the other warps place the block's assignments and copy x into x_perm
+    if (warp == 31) {
+        prob_sums(p, b, G);
+        return;
+    }
+    constexpr int kCopyWarps = 31;
+    const int nparts = ntok >= kCopyWarps ? 1 : ntok >= 16 ? 2 : ntok >= 8 ? 4 : ntok >= 4 ? 8 : 31;
+    for (int task = warp; task < ntok * nparts; task += kCopyWarps) {
+        const int t = t_beg + task / nparts, part = task - (task / nparts) * nparts;
         long long row = -1;
         if (lane < k) {
-            const int e = __ldcg(p.topk_idx + (size_t)t * k + lane);
-            const long long pos = (long long)__ldcg(p.hist + (size_t)e * p.nchunk + t / kChunk) +
-                                  __ldcg(p.rank + (size_t)t * k + lane);
+            const size_t tk = (size_t)t * k + lane;
+            // a one-chunk block still holds its assignments in shared memory
+            const int u = (t - t_beg) * k + lane;
+            const int e = p.cpb == 1 ? ibuf[u] : __ldcg(p.topk_idx + tk);
+            const long long pos = (long long)s_base[e] + (p.cpb == 1 ? rbuf[u] : __ldcg(p.rank + tk));
             const bool kept = (p.C < 0) || (pos < p.C);
-            row = kept ? (long long)__ldcg(p.seg_off + e) + pos : -1;
-            p.dropped[(size_t)t * k + lane] = kept ? 0 : 1;
-            p.row_of[(size_t)t * k + lane] = (int32_t)row;
-            if (p.row_tok && row >= 0) {
-                p.row_tok[row] = t;
-                p.row_w[row] = __ldcg(p.topk_w + (size_t)t * k + lane);
+            row = kept ? (long long)s_seg[e] + pos : -1;
+            if (part == 0) {
+                p.dropped[tk] = kept ? 0 : 1;
+                p.row_of[tk] = (int32_t)row;
+                if (p.row_tok && row >= 0) {
+                    p.row_tok[row] = t;
+                    p.row_w[row] = p.cpb == 1 ? wbuf[u] : __ldcg(p.topk_w + tk);
+                }
             }
         }
         long long rows[kMaxTopK];
@@ -495,29 +844,13 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
             rows[j] = __shfl_sync(0xffffffffu, row, j);
             any |= (j < k && rows[j] >= 0);
         }
-        const uint8_t *src = static_cast<const uint8_t *>(p.x) + (size_t)t * p.row_bytes;
-        if (nv * 16 == p.row_bytes) {
-            for (size_t v = lane; v < nv; v += 32) {
-                const uint4 val = __ldg(reinterpret_cast<const uint4 *>(src) + v);
-#pragma unroll
-                for (int j = 0; j < kMaxTopK; ++j)
-                    if (j < k && rows[j] >= 0)
-                        reinterpret_cast<uint4 *>(p.x_perm + (size_t)rows[j] * p.row_bytes)[v] =
-                            val;
-            }
-        } else {  // fp32 rows whose size is not a multiple of 16 bytes
-            for (size_t v = lane; v < p.row_bytes / 4; v += 32) {
-                const uint32_t val = __ldg(reinterpret_cast<const uint32_t *>(src) + v);
-#pragma unroll
-                for (int j = 0; j < kMaxTopK; ++j)
-                    if (j < k && rows[j] >= 0)
-                        reinterpret_cast<uint32_t *>(p.x_perm + (size_t)rows[j] * p.row_bytes)[v] =
-                            val;
-            }
-        }
+        const uint8_t *src = p.x_staged
+                                 ? xs + (size_t)(t - t_beg) * xstride
+                                 : static_cast<const uint8_t *>(p.x) + (size_t)t * p.row_bytes;
+        copy_row(p, src, rows, part, nparts);
         if (p.y_zero && !any) {
             uint4 *dst = reinterpret_cast<uint4 *>(p.y_zero + (size_t)t * p.row_bytes);
-            for (size_t v = lane; v < nv; v += 32)
+            for (size_t v = (size_t)part * 32 + lane; v < p.row_bytes / 16; v += (size_t)nparts * 32)
                 dst[v] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
@@ -532,10 +865,22 @@ bool router_fused(const moe_config &c)
 
 bool direct_y(const moe_config &c) { return c.top_k == 1 && c.d_shared == 0; }
 
-template <int EPL, int RT>
-static cudaError_t launch_dispatch_t(const DispatchParams &p, size_t smem, cudaStream_t stream)
+// Dynamic shared memory of the dispatch kernel: staged W_r rows (fused
+// router; wr_bytes = E * (row bytes + 16)), staged x rows (xs_bytes =
+// chunk * (row bytes + 16)), pbuf [32][E] floats, ibuf [32][k], then mask,
+// run, base, n [E], the segment offsets [E+1], the router's partial sums
+// [8][32][16], and the chunk's ranks and gate weights [32][8].
+static size_t dispatch_smem(size_t wr_bytes, size_t xs_bytes, int E, int k)
 {
-    auto kern = dispatch_kernel<EPL, RT>;
+    return wr_bytes + xs_bytes + (size_t)kChunk * (E + k) * 4 + (size_t)4 * E * 4 +
+           (size_t)(E + 1) * 4 + (size_t)kRouterMmaWarps * kChunk * kFusedMaxE * 4 +
+           (size_t)2 * kChunk * kMaxTopK * 4;
+}
+
+template <int EPL, int RT, int EM = 1>
+static cudaError_t launch_dispatch_t(DispatchParams &p, size_t wr_bytes, cudaStream_t stream)
+{
+    auto kern = dispatch_kernel<EPL, RT, EM>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
@@ -543,8 +888,8 @@ static cudaError_t launch_dispatch_t(const DispatchParams &p, size_t smem, cudaS
     static uint64_t configured = 0;
     static int max_blocks[64] = {0};
     if (dev < 64 && !(configured & (1ull << dev))) {
-        const size_t smem_max = kFusedMaxWrBytes + kChunk * (kMaxExperts + kMaxTopK) * 4 +
-                                kMaxExperts * 4;
+        const size_t smem_max = dispatch_smem(kFusedMaxWrBytes + kFusedMaxE * 16,
+                                              kStageMaxBytes + kChunk * 16, kMaxExperts, kMaxTopK);
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)smem_max);
         if (err != cudaSuccess)
@@ -557,8 +902,24 @@ static cudaError_t launch_dispatch_t(const DispatchParams &p, size_t smem, cudaS
         max_blocks[dev] = std::max(1, per_sm) * sm_count();
         configured |= 1ull << dev;
     }
-    const int want = std::max(p.nchunk, p.E);
-    const int grid = std::max(1, std::min(want, dev < 64 ? max_blocks[dev] : sm_count()));
+    const int maxb = std::max(1, std::min(kMaxDispatchBlocks,
+                                          dev < 64 ? max_blocks[dev] : sm_count()));
+    // The smallest chunk (1, 2, ..., 32 tokens) whose chunk count fits one
+    // chunk per co-resident block; else 32-token chunks, several per block.
+    int cs = kChunk;
+    for (int c = 1; c < kChunk; c *= 2)
+        if ((p.T + c - 1) / c <= maxb) {
+            cs = c;
+            break;
+        }
+    p.cs = cs;
+    p.nchunk = (p.T + cs - 1) / cs;
+    p.cpb = (p.nchunk + maxb - 1) / maxb;
+    const int grid = std::max(1, (p.nchunk + p.cpb - 1) / p.cpb);
+    p.x_staged = (p.cpb == 1 && p.row_bytes % 16 == 0 &&
+                  (size_t)cs * p.row_bytes <= kStageMaxBytes) ? 1 : 0;
+    const size_t smem = dispatch_smem(wr_bytes, p.x_staged ? (size_t)cs * (p.row_bytes + 16) : 0,
+                                      p.E, p.k);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kDispatchThreads);
@@ -576,7 +937,7 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
                             const void *x, const void *W_r, bool fused, float *logits,
                             const float *bias, int32_t *topk_idx, float *topk_w,
                             uint8_t *dropped_mask, int32_t *expert_counts, int32_t *kept_counts,
-                            float *aux_loss, void *y, cudaStream_t stream)
+                            void *y, cudaStream_t stream)
 {
     DispatchParams p;
     const size_t esz = c.dtype == MOE_DTYPE_BF16 ? 2 : 4;
@@ -588,7 +949,6 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
     p.E = c.n_experts;
     p.k = c.top_k;
     p.mode = c.gating_mode;
-    p.nchunk = L.nchunk;
     p.D = c.d_model;
     p.C = L.C;
     p.alpha = c.aux_alpha;
@@ -598,10 +958,9 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
     p.dropped = dropped_mask;
     p.expert_counts = expert_counts;
     p.kept_counts = kept_counts;
-    p.aux_loss = aux_loss;
-    p.hist = reinterpret_cast<int32_t *>(ws + L.hist);
+    p.bcount = reinterpret_cast<int32_t *>(ws + L.bcount);
     p.ppart = reinterpret_cast<float *>(ws + L.ppart);
-    p.rank = ws + L.rank;
+    p.rank = reinterpret_cast<int32_t *>(ws + L.rank);
     p.psum = reinterpret_cast<double *>(ws + L.psum);
     p.seg_off = reinterpret_cast<int32_t *>(ws + L.seg_off);
     p.mtile = reinterpret_cast<int32_t *>(ws + L.mtile);
@@ -612,19 +971,25 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
     p.row_w = dy ? reinterpret_cast<float *>(ws + L.row_w) : nullptr;
     p.y_zero = dy ? static_cast<uint8_t *>(y) : nullptr;
     p.status = reinterpret_cast<int32_t *>(ws + L.status);
-    const size_t smem = (fused ? (size_t)c.n_experts * c.d_model * esz : 0) +
-                        (size_t)kChunk * (c.n_experts + c.top_k) * 4 + (size_t)c.n_experts * 4;
-    if (fused)
-        return c.dtype == MOE_DTYPE_BF16 ? launch_dispatch_t<1, ROUTER_BF16>(p, smem, stream)
-                                         : launch_dispatch_t<1, ROUTER_F32>(p, smem, stream);
+    const size_t wr_bytes = fused ? (size_t)c.n_experts * (c.d_model * esz + 16) : 0;
+    if (fused) {
+        const int E = c.n_experts;
+        if (c.dtype == MOE_DTYPE_BF16)
+            return E <= 4   ? launch_dispatch_t<1, ROUTER_BF16, 4>(p, wr_bytes, stream)
+                   : E <= 8 ? launch_dispatch_t<1, ROUTER_BF16, 8>(p, wr_bytes, stream)
+                            : launch_dispatch_t<1, ROUTER_BF16, 16>(p, wr_bytes, stream);
+        return E <= 4   ? launch_dispatch_t<1, ROUTER_F32, 4>(p, wr_bytes, stream)
+               : E <= 8 ? launch_dispatch_t<1, ROUTER_F32, 8>(p, wr_bytes, stream)
+                        : launch_dispatch_t<1, ROUTER_F32, 16>(p, wr_bytes, stream);
+    }
     const int epl = (c.n_experts + 31) / 32;
     if (epl <= 1)
-        return launch_dispatch_t<1, ROUTER_NONE>(p, smem, stream);
+        return launch_dispatch_t<1, ROUTER_NONE>(p, wr_bytes, stream);
     if (epl <= 2)
-        return launch_dispatch_t<2, ROUTER_NONE>(p, smem, stream);
+        return launch_dispatch_t<2, ROUTER_NONE>(p, wr_bytes, stream);
     if (epl <= 4)
-        return launch_dispatch_t<4, ROUTER_NONE>(p, smem, stream);
-    return launch_dispatch_t<8, ROUTER_NONE>(p, smem, stream);
+        return launch_dispatch_t<4, ROUTER_NONE>(p, wr_bytes, stream);
+    return launch_dispatch_t<8, ROUTER_NONE>(p, wr_bytes, stream);
 }
 
 }  // namespace moe

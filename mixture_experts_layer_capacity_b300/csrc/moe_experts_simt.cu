@@ -30,12 +30,14 @@ __global__ void simt_seg_gemm_f32_kernel(const float *__restrict__ A, const floa
                                          const float *__restrict__ B1, long long b_seg_elems,
                                          int N, int K, const int32_t *__restrict__ seg_off,
                                          int nseg, int dense_rows, float *__restrict__ out,
-                                         const int32_t *status)
+                                         const int32_t *status, AuxArgs aux)
 {
     griddep_wait();
     griddep_launch_dependents();
     if (*(volatile const int32_t *)status != 0)
         return;  // an earlier kernel failed
+    if (aux.out && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.y == 0)
+        balance_loss_warp(aux);
     const int n = blockIdx.x * blockDim.x + threadIdx.x;
     const int r = blockIdx.y * blockDim.y + threadIdx.y;
     const int rows = seg_off ? seg_off[nseg] : dense_rows;
@@ -63,7 +65,8 @@ __global__ void simt_seg_gemm_f32_kernel(const float *__restrict__ A, const floa
 cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                                 const void *x, const void *W_gate, const void *W_up,
                                 const void *W_down, const void *Ws_gate, const void *Ws_up,
-                                const void *Ws_down, cudaStream_t stream, cudaEvent_t *ev)
+                                const void *Ws_down, const AuxArgs &aux, cudaStream_t stream,
+                                cudaEvent_t *ev)
 {
     if (c.dtype != MOE_DTYPE_FP32)
         return cudaErrorInvalidValue;
@@ -77,15 +80,17 @@ cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, u
     const unsigned rb = (unsigned)((L.R_max + 7) / 8);
     const float *nil = nullptr;
     const int32_t *noseg = nullptr;
+    AuxArgs none = aux;
+    none.out = nullptr;
     cudaError_t err = launch_pdl(simt_seg_gemm_f32_kernel<true>, dim3((F + 31) / 32, rb), block, 0,
                                  stream, (const float *)xp, (const float *)W_gate,
-                                 (const float *)W_up, (long long)F * D, F, D, seg, E, 0, h, status);
+                                 (const float *)W_up, (long long)F * D, F, D, seg, E, 0, h, status, aux);
     if (err == cudaSuccess)
         err = record_stage(ev, 3, stream);
     if (err == cudaSuccess)
         err = launch_pdl(simt_seg_gemm_f32_kernel<false>, dim3((D + 31) / 32, rb), block, 0,
                          stream, (const float *)h, (const float *)W_down, nil,
-                         (long long)D * F, D, F, seg, E, 0, z, status);
+                         (long long)D * F, D, F, seg, E, 0, z, status, none);
     if (err == cudaSuccess)
         err = record_stage(ev, 4, stream);
     if (err != cudaSuccess)
@@ -96,13 +101,13 @@ cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, u
         const unsigned tb = (unsigned)((c.T + 7) / 8);
         err = launch_pdl(simt_seg_gemm_f32_kernel<true>, dim3((S + 31) / 32, tb), block, 0,
                          stream, (const float *)x, (const float *)Ws_gate, (const float *)Ws_up,
-                         0LL, S, D, noseg, 1, c.T, hs, status);
+                         0LL, S, D, noseg, 1, c.T, hs, status, none);
         if (err == cudaSuccess)
             err = record_stage(ev, 5, stream);
         if (err == cudaSuccess)
             err = launch_pdl(simt_seg_gemm_f32_kernel<false>, dim3((D + 31) / 32, tb), block, 0,
                              stream, (const float *)hs, (const float *)Ws_down, nil, 0LL, D, S,
-                             noseg, 1, c.T, zs, status);
+                             noseg, 1, c.T, zs, status, none);
         if (err == cudaSuccess)
             err = record_stage(ev, 6, stream);
         if (err != cudaSuccess)

@@ -58,6 +58,7 @@ struct TcParams {
     const int32_t *row_tok;  // EPI_BF16_Y: token of each A row
     const float *row_w;      // EPI_BF16_Y: gate weight of each A row
     int32_t *status;
+    AuxArgs aux;             // balance loss to evaluate (aux.out null: none)
 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any tile
@@ -310,6 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------- epilogue
+        // (the first epilogue warp of CTA 0 first evaluates the balance loss,
+        // while the first tile's operands are still in flight)
+        if (p.aux.out && !failed && blockIdx.x == 0 && warp == 2)
+            balance_loss_warp(p.aux);
         const int q = warp & 3;             // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;        // accumulator row of this thread
         uint32_t b = 0, tph = 0;
@@ -528,7 +533,8 @@ cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r
 cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                               const void *x, const void *W_gate, const void *W_up,
                               const void *W_down, const void *Ws_gate, const void *Ws_up,
-                              const void *Ws_down, void *y, cudaStream_t stream, cudaEvent_t *ev)
+                              const void *Ws_down, void *y, const AuxArgs &aux,
+                              cudaStream_t stream, cudaEvent_t *ev)
 {
     const int D = c.d_model, F = c.d_expert, S = c.d_shared, E = c.n_experts, T = c.T;
     int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
@@ -558,6 +564,7 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
         p.out = h;
         p.ld_out = F;
         p.status = status;
+        p.aux = aux;
         err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_bound * p.n_tiles, stream);
         if (err == cudaSuccess)
             err = record_stage(ev, 3, stream);

@@ -11,7 +11,8 @@
 
 namespace moe {
 
-constexpr int kChunk = 32;       // tokens per routing chunk (one bit each in a 32-bit mask)
+constexpr int kChunk = 32;       // most tokens per routing chunk (one bit each in a 32-bit mask)
+constexpr int kMaxDispatchBlocks = 256;  // most blocks of the dispatch kernel
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 constexpr int kTileM = 128;      // rows per tensor-core tile (UMMA M)
@@ -20,9 +21,9 @@ constexpr int kTileM = 128;      // rows per tensor-core tile (UMMA M)
 // region starts on a 1024-byte boundary.
 struct WorkspaceLayout {
     size_t status;   // int32[16] device status word, then the scan's block counter
-    size_t hist;     // int32[E][nchunk]  per-chunk expert counts, then exclusive bases
+    size_t bcount;   // int32[E][blocks]  per-block expert counts of the dispatch kernel
     size_t ppart;    // float[E][nchunk]  per-chunk sums of softmax probabilities
-    size_t rank;     // uint8[T*k]        rank of an assignment among its chunk's tokens
+    size_t rank;     // int32[T*k]        rank of an assignment among its block's tokens
     size_t psum;     // double[E]         sum over tokens of the softmax probabilities
     size_t seg_off;  // int32[E+1]        first x_perm row of each expert's segment
     size_t mtile;    // int32[E+1]        prefix sum of 128-row tiles per segment
@@ -37,7 +38,21 @@ struct WorkspaceLayout {
     size_t total;
     int64_t R_max;   // rows of x_perm: T*k dropless, else min(T*k, E*C)
     int64_t C;       // capacity, -1 dropless
-    int nchunk;      // ceil(T / kChunk)
+    int nchunk;      // the most routing chunks: max(min(T, kMaxDispatchBlocks), ceil(T / kChunk))
+};
+
+// Inputs of the balance loss aux = alpha * E * sum_e f_e P_e, with
+// f_e = n_e / (T k) and P_e = psum_e / T ("Mixture of Experts" (module 17),
+// 17.4 equation; "Mixture of experts" (frontiers track), balance equation of
+// 'Keeping the load balanced').  psum and counts are written by the dispatch
+// kernel; the first expert kernel, which starts after it has completed,
+// evaluates the loss.
+struct AuxArgs {
+    const double *psum;      // [E] sum over tokens of the softmax probabilities
+    const int32_t *counts;   // [E] demand counts n_e
+    float *out;              // [1], or null: nothing to compute
+    int E, T, k;
+    float alpha;
 };
 
 moe_status validate_config(const moe_config *cfg);
@@ -58,13 +73,14 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
                             const void *x, const void *W_r, bool fused, float *logits,
                             const float *bias, int32_t *topk_idx, float *topk_w,
                             uint8_t *dropped_mask, int32_t *expert_counts, int32_t *kept_counts,
-                            float *aux_loss, void *y, cudaStream_t stream);
+                            void *y, cudaStream_t stream);
 cudaError_t launch_combine(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                            const float *topk_w, void *y, cudaStream_t stream);
+// `aux`: the balance loss, evaluated by the first expert kernel.
 cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                                 const void *x, const void *W_gate, const void *W_up,
                                 const void *W_down, const void *Ws_gate, const void *Ws_up,
-                                const void *Ws_down, cudaStream_t stream,
+                                const void *Ws_down, const AuxArgs &aux, cudaStream_t stream,
                                 cudaEvent_t *ev = nullptr);
 
 // Records ev[i] on `stream` when ev is not null.  Under stream capture the
@@ -87,12 +103,13 @@ inline cudaError_t record_stage(cudaEvent_t *ev, int i, cudaStream_t stream)
 // if a tensor map cannot be encoded.
 cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r,
                              float *logits, int32_t *status, cudaStream_t stream);
-// `ev` (nullable): stage events 3..6 are recorded after each GEMM.
+// `ev` (nullable): stage events 3..6 are recorded after each GEMM.  `aux`:
+// the balance loss, evaluated by the first expert kernel.
 cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                               const void *x, const void *W_gate, const void *W_up,
                               const void *W_down, const void *Ws_gate, const void *Ws_up,
-                              const void *Ws_down, void *y, cudaStream_t stream,
-                              cudaEvent_t *ev = nullptr);
+                              const void *Ws_down, void *y, const AuxArgs &aux,
+                              cudaStream_t stream, cudaEvent_t *ev = nullptr);
 
 int sm_count();
 
