@@ -155,6 +155,106 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const uint32_
     }
 }
 
+// Epilogue of one accumulator row (TMEM lane) of a tile: this thread owns
+// output row `orow` (stored only when row_ok), columns n_idx*BN ... of the
+// tile.  taddr: TMEM address of the row's first accumulator column.
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_row(const TcParams &p, uint32_t taddr, bool row_ok,
+                                             long long orow, int n_idx)
+{
+    if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(taddr + c0, gv);
+            tmem_ld32(taddr + BN + c0, uv);
+            tmem_wait_ld();
+            if (row_ok) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float g0 = __uint_as_float(gv[2 * i]);
+                    const float g1 = __uint_as_float(gv[2 * i + 1]);
+                    const float u0 = __uint_as_float(uv[2 * i]);
+                    const float u1 = __uint_as_float(uv[2 * i + 1]);
+                    pk[i] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
+                }
+                const int col = n_idx * BN + c0;
+                __nv_bfloat16 *dst =
+                    reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * p.ld_out + col;
+                store_row_bf16(dst, pk, col, p.N_valid);
+            }
+        }
+    } else if constexpr (EPI == EPI_BF16_Y) {
+        int tok = 0;
+        float wr = 0.f;
+        if (row_ok) {
+            tok = p.row_tok[orow];
+            wr = p.row_w[orow];
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c0, v);
+            tmem_wait_ld();
+            if (row_ok) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(wr * __uint_as_float(v[2 * i]),
+                                        wr * __uint_as_float(v[2 * i + 1]));
+                const int col = n_idx * BN + c0;
+                __nv_bfloat16 *dst =
+                    reinterpret_cast<__nv_bfloat16 *>(p.out) + (long long)tok * p.ld_out + col;
+                store_row_bf16(dst, pk, col, p.N_valid);
+            }
+        }
+    } else if constexpr (EPI == EPI_BF16) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c0, v);
+            tmem_wait_ld();
+            if (row_ok) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]),
+                                        __uint_as_float(v[2 * i + 1]));
+                const int col = n_idx * BN + c0;
+                __nv_bfloat16 *dst =
+                    reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * p.ld_out + col;
+                store_row_bf16(dst, pk, col, p.N_valid);
+            }
+        }
+    } else {
+        constexpr int CH = BN < 32 ? 16 : 32;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += CH) {
+            uint32_t v[32];
+            if constexpr (CH == 16) {
+                uint32_t v16[16];
+                tmem_ld16(taddr + c0, v16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    v[i] = v16[i];
+            } else {
+                tmem_ld32(taddr + c0, v);
+                tmem_wait_ld();
+            }
+            if (row_ok) {
+                const int col = n_idx * BN + c0;
+                float *dst = reinterpret_cast<float *>(p.out) + orow * p.ld_out + col;
+#pragma unroll
+                for (int i = 0; i < CH; ++i)
+                    if (col + i < p.N_valid)
+                        dst[i] = __uint_as_float(v[i]);
+            }
+        }
+    }
+}
+
 template <int BN, int NB, int EPI, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
@@ -329,97 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t taddr = tmem_base + b * S::UMMA_N + ((uint32_t)(q * 32) << 16);
             const bool row_ok = r < ti.rows;
             const long long orow = (long long)ti.a_row0 + r;
-            if constexpr (EPI == EPI_SWIGLU) {
-#pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    uint32_t gv[32], uv[32];
-                    tmem_ld32(taddr + c0, gv);
-                    tmem_ld32(taddr + BN + c0, uv);
-                    tmem_wait_ld();
-                    if (row_ok) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float g0 = __uint_as_float(gv[2 * i]);
-                            const float g1 = __uint_as_float(gv[2 * i + 1]);
-                            const float u0 = __uint_as_float(uv[2 * i]);
-                            const float u1 = __uint_as_float(uv[2 * i + 1]);
-                            pk[i] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
-                        }
-                        const int col = ti.n_idx * BN + c0;
-                        __nv_bfloat16 *dst =
-                            reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * p.ld_out + col;
-                        store_row_bf16(dst, pk, col, p.N_valid);
-                    }
-                }
-            } else if constexpr (EPI == EPI_BF16_Y) {
-                int tok = 0;
-                float wr = 0.f;
-                if (row_ok) {
-                    tok = p.row_tok[orow];
-                    wr = p.row_w[orow];
-                }
-#pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(taddr + c0, v);
-                    tmem_wait_ld();
-                    if (row_ok) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16x2(wr * __uint_as_float(v[2 * i]),
-                                                wr * __uint_as_float(v[2 * i + 1]));
-                        const int col = ti.n_idx * BN + c0;
-                        __nv_bfloat16 *dst =
-                            reinterpret_cast<__nv_bfloat16 *>(p.out) + (long long)tok * p.ld_out + col;
-                        store_row_bf16(dst, pk, col, p.N_valid);
-                    }
-                }
-            } else if constexpr (EPI == EPI_BF16) {
-#pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(taddr + c0, v);
-                    tmem_wait_ld();
-                    if (row_ok) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]),
-                                                __uint_as_float(v[2 * i + 1]));
-                        const int col = ti.n_idx * BN + c0;
-                        __nv_bfloat16 *dst =
-                            reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * p.ld_out + col;
-                        store_row_bf16(dst, pk, col, p.N_valid);
-                    }
-                }
-            } else {
-                constexpr int CH = BN < 32 ? 16 : 32;
-#pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += CH) {
-                    uint32_t v[32];
-                    if constexpr (CH == 16) {
-                        uint32_t v16[16];
-                        tmem_ld16(taddr + c0, v16);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            v[i] = v16[i];
-                    } else {
-                        tmem_ld32(taddr + c0, v);
-                        tmem_wait_ld();
-                    }
-                    if (row_ok) {
-                        const int col = ti.n_idx * BN + c0;
-                        float *dst = reinterpret_cast<float *>(p.out) + orow * p.ld_out + col;
-#pragma unroll
-                        for (int i = 0; i < CH; ++i)
-                            if (col + i < p.N_valid)
-                                dst[i] = __uint_as_float(v[i]);
-                    }
-                }
-            }
+            epilogue_row<BN, EPI>(p, taddr, row_ok, orow, ti.n_idx);
             tc_fence_before_sync();
             mbar_arrive(&tempty[b]);
             b ^= 1u;
@@ -434,6 +444,311 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, S::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------- CTA-pair GEMM
+// The same GEMMs on pairs of CTAs (clusters of 2 on two SMs): a pair tile is
+// 256 rows x UMMA_N columns, computed by tcgen05.mma.cta_group::2 (M = 256)
+// issued by the even CTA.  Each CTA stages its own 128 rows of A and half of
+// the B rows (for GEMM1 the leader holds the gate rows and the peer the up
+// rows), so per SM a k-step moves A + B/2 instead of A + B: less L2 -> shared
+// memory traffic per FLOP and room for deeper pipelines.  Each CTA's TMEM
+// holds the accumulator rows of its own 128 A rows, all UMMA_N columns, so
+// the epilogue is that of the single-CTA kernel.
+//   - the producers of both CTAs signal the leader's "full" barriers
+//     (transaction bytes of both halves; only the leader arrives);
+//   - the leader's MMA commits arrive on the "empty" and "tfull" barriers of
+//     both CTAs (multicast);
+//   - both CTAs' epilogue warps arrive on the leader's "tempty" barriers.
+// Pair tiles are 256 rows of one segment; their per-segment counts are
+// derived here from the segment offsets.
+template <int BN, int NB, int STAGES>
+struct PairShape {
+    static constexpr int UMMA_N = BN * NB;
+    static constexpr int B_HALF_ROWS = UMMA_N / 2;   // B rows staged by each CTA
+    static constexpr int A_BYTES = kTileM * 64 * 2;
+    static constexpr int B_BYTES = B_HALF_ROWS * 64 * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = 2 * UMMA_N <= 256 ? 256 : 512;
+    static constexpr int TABLE_BYTES = 2 * (kMaxExperts + 1) * 4 + 8;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + TABLE_BYTES + 1024;
+    static_assert(UMMA_N == 128 || UMMA_N == 256, "pair UMMA N");
+    static_assert(NB == 1 || B_HALF_ROWS == BN, "gate/up halves");
+    static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+constexpr int kPairRows = 2 * kTileM;
+constexpr long long kPairMinRows = 16384;  // fewest routed GEMM rows for which pairs are used
+
+__device__ __forceinline__ int pair_tile_count(const TcParams &p, const int *s_mt)
+{
+    if (!s_mt)
+        return ((p.dense_rows + kPairRows - 1) / kPairRows) * p.n_tiles;
+    return s_mt[p.nseg] * p.n_tiles;
+}
+
+// a_row0 / rows: the pair tile's first A row and its valid rows (<= 256).
+__device__ __forceinline__ TileInfo pair_tile_info(const TcParams &p, const int *s_seg,
+                                                   const int *s_mt, int g)
+{
+    TileInfo ti;
+    if (!s_mt) {
+        const int mt = (p.dense_rows + kPairRows - 1) / kPairRows;
+        ti.n_idx = g / mt;
+        const int m = g - ti.n_idx * mt;
+        ti.seg = 0;
+        ti.a_row0 = m * kPairRows;
+        ti.rows = min(kPairRows, p.dense_rows - ti.a_row0);
+        return ti;
+    }
+    int lo = 0, hi = p.nseg;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_mt[mid] * p.n_tiles <= g)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const int mt0 = s_mt[lo], mt_e = s_mt[lo + 1] - mt0;
+    const int local = g - mt0 * p.n_tiles;
+    ti.n_idx = local / mt_e;
+    const int m = local - ti.n_idx * mt_e;
+    ti.seg = lo;
+    ti.a_row0 = s_seg[lo] + m * kPairRows;
+    ti.rows = min(kPairRows, s_seg[lo + 1] - ti.a_row0);
+    return ti;
+}
+
+template <int BN, int NB, int EPI, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap mA,
+                        const __grid_constant__ CUtensorMap mB0,
+                        const __grid_constant__ CUtensorMap mB1, const TcParams p)
+{
+    using S = PairShape<BN, NB, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * S::STAGE_BYTES);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *tfull = bars + 2 * STAGES;
+    uint64_t *tempty = bars + 2 * STAGES + 2;
+    uint64_t *mma_done = bars + 2 * STAGES + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *tables = reinterpret_cast<int *>(smem + STAGES * S::STAGE_BYTES + 256);
+    int *s_seg = p.mtile ? tables : nullptr;
+    int *s_mt = p.mtile ? tables + (kMaxExperts + 1) : nullptr;
+
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster_id = (int)(blockIdx.x >> 1), nclusters = (int)(gridDim.x >> 1);
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 2 * 4);  // one arrival per epilogue warp of each CTA
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&mA);
+        tma_prefetch_desc(&mB0);
+        if (NB == 2)
+            tma_prefetch_desc(&mB1);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, S::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    griddep_wait();
+    griddep_launch_dependents();
+    const bool failed = *(volatile const int32_t *)p.status != 0;
+    if (p.mtile && !failed)
+        for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x)
+            s_seg[i] = p.seg_off[i];
+    __syncthreads();
+    // pair tiles per segment (256 rows each), prefix-summed by warp 0
+    if (p.mtile && !failed && warp == 0) {
+        int carry = 0;
+        for (int e0 = 0; e0 < p.nseg; e0 += 32) {
+            const int e = e0 + lane;
+            const int v = e < p.nseg ? (s_seg[e + 1] - s_seg[e] + kPairRows - 1) / kPairRows : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += n;
+            }
+            if (e < p.nseg)
+                s_mt[e + 1] = carry + incl;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0)
+            s_mt[0] = 0;
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers initialised and TMEM allocated
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int ntiles = failed ? 0 : pair_tile_count(p, s_mt);
+    const int nk = (p.K + 63) / 64;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            const uint32_t full_leader = mapa_shared(smem_u32(&full[0]), 0);
+            int s = 0;
+            uint32_t ph = 0;
+            long long fills = 0;
+            bool ok = true;
+            for (int g = cluster_id; g < ntiles && ok; g += nclusters) {
+                const TileInfo ti = pair_tile_info(p, s_seg, s_mt, g);
+                const int a_row = ti.a_row0 + (int)rank * kTileM;
+                const int b_row = ti.seg * p.b_seg_rows + ti.n_idx * BN +
+                                  (NB == 1 ? (int)rank * S::B_HALF_ROWS : 0);
+                const CUtensorMap *mb = (NB == 2 && !leader) ? &mB1 : &mB0;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sa = smem + s * S::STAGE_BYTES;
+                    uint8_t *sb = sa + S::A_BYTES;
+                    const uint32_t fb = full_leader + (uint32_t)s * 8u;
+                    if (leader)
+                        mbar_arrive_expect_tx(&full[s], 2 * S::STAGE_BYTES);
+                    tma_load_2d_pair(sa, &mA, fb, kb * 64, a_row);
+                    tma_load_2d_pair(sb, mb, fb, kb * 64, b_row);
+                    ++fills;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
+                if (leader) {
+                    // wait (bounded) for the copies still in flight
+                    const long long first = fills > STAGES ? fills - STAGES : 0;
+                    for (long long f = first; f < fills; ++f)
+                        mbar_wait(&full[f % STAGES], (uint32_t)((f / STAGES) & 1), nullptr,
+                                  kDrainLimitNs);
+                } else {
+                    // this CTA's copies complete on the leader's barriers:
+                    // give them time to land before the pair's final sync
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 1000000ull)
+                        __nanosleep(1000);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------------ MMA issuer (even CTA)
+            constexpr uint32_t idesc = idesc_bf16_f32(kPairRows, S::UMMA_N);
+            int s = 0;
+            uint32_t ph = 0, b = 0, tph = 0;
+            bool ok = true;
+            for (int g = cluster_id; g < ntiles && ok; g += nclusters) {
+                if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * S::UMMA_N;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(&full[s], ph, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = smem_u32(smem + s * S::STAGE_BYTES);
+                    const uint64_t adesc = sdesc_kmajor_sw128(sa);
+                    const uint64_t bdesc = sdesc_kmajor_sw128(sa + S::A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16_pair(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                       (kb > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit_pair(&empty[s], 0x3);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                umma_commit_pair(&tfull[b], 0x3);
+                b ^= 1u;
+                if (b == 0)
+                    tph ^= 1u;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
+            }
+            // all MMAs of the pair complete before either CTA releases TMEM
+            umma_commit_pair(mma_done, 0x1);
+            mbar_wait(mma_done, 0, nullptr, kDrainLimitNs);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue (both CTAs)
+        if (p.aux.out && !failed && blockIdx.x == 0 && warp == 2)
+            balance_loss_warp(p.aux);
+        const int q = warp & 3;             // TMEM lane quarter this warp may access
+        const int r = q * 32 + lane;        // accumulator row of this thread
+        const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), 0);
+        uint32_t b = 0, tph = 0;
+        for (int g = cluster_id; g < ntiles; g += nclusters) {
+            const TileInfo ti = pair_tile_info(p, s_seg, s_mt, g);
+            if (!mbar_wait(&tfull[b], tph, abort_flag, kWaitLimitNs)) {
+                *abort_flag = 1;
+                set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + b * S::UMMA_N + ((uint32_t)(q * 32) << 16);
+            const int my_rows = ti.rows - (int)rank * kTileM;
+            const bool row_ok = r < my_rows;
+            const long long orow = (long long)ti.a_row0 + (int)rank * kTileM + r;
+            epilogue_row<BN, EPI>(p, taddr, row_ok, orow, ti.n_idx);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(&tempty[b]);
+                else
+                    mbar_arrive_cluster(tempty_leader + b * 8u);
+            }
+            b ^= 1u;
+            if (b == 0)
+                tph ^= 1u;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();  // neither CTA frees TMEM or exits while the pair may use it
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
     }
 }
 
@@ -497,6 +812,56 @@ cudaError_t launch_tc(const CUtensorMap &mA, const CUtensorMap &mB0, const CUten
                       mA, mB0, mB1, p);
 }
 
+// Launches the CTA-pair kernel as clusters of 2 (persistent: at most as
+// many pairs as can be resident at once, and no more than there are pair
+// tiles).
+template <int BN, int NB, int EPI, int STAGES>
+cudaError_t launch_tc_pair(const CUtensorMap &mA, const CUtensorMap &mB0, const CUtensorMap &mB1,
+                           const TcParams &p, long long max_tiles, cudaStream_t stream)
+{
+    using S = PairShape<BN, NB, STAGES>;
+    auto kern = tc_gemm_pair_kernel<BN, NB, EPI, STAGES>;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    static uint64_t configured = 0;  // bit per device
+    static int max_pairs[64] = {0};
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = S::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    if (dev < 64 && !(configured & (1ull << dev))) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   S::SMEM_BYTES);
+        if (err != cudaSuccess)
+            return err;
+        cfg.gridDim = dim3((unsigned)(sm_count() & ~1));
+        cfg.numAttrs = 1;
+        int n = 0;
+        err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (err != cudaSuccess)
+            return err;
+        max_pairs[dev] = std::max(1, n);
+        configured |= 1ull << dev;
+    }
+    const long long pairs =
+        std::min<long long>(max_tiles, dev < 64 ? max_pairs[dev] : sm_count() / 2);
+    if (pairs < 1)
+        return cudaSuccess;
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, mA, mB0, mB1, p);
+}
+
 }  // namespace
 
 cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r,
@@ -542,8 +907,16 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
     const int32_t *mtile = reinterpret_cast<const int32_t *>(ws + L.mtile);
     void *xp = ws + L.x_perm, *h = ws + L.h, *z = ws + L.z;
     const long long R = L.R_max;
-    const long long mt_bound = R / kTileM + E;  // >= sum_e ceil(kept_e / 128)
-    const bool wide_down = D > 1024;           // 256-column tiles for the down projection
+    const long long mt_bound = R / kTileM + E;     // >= sum_e ceil(kept_e / 128)
+    const long long mt2_bound = R / kPairRows + E; // >= sum_e ceil(kept_e / 256)
+    const bool wide_down = D > 1024;              // 256-column tiles for the down projection
+    // CTA pairs (256-row tiles) for large problems whose segments average
+    // at least 512 rows; decode-sized and small batches keep single-CTA tiles
+    // (few rows would leave most of a 256-row tile empty, and small GEMMs are
+    // bound by latency, not by shared-memory traffic)
+    const long long routed_rows = (long long)T * c.top_k;
+    const bool pair_routed = routed_rows >= kPairMinRows && routed_rows >= 2LL * kPairRows * E;
+    const bool pair_shared = T >= kPairMinRows / 4;
     cudaError_t err;
 
     // GEMM1 (routed): h = silu(x_perm W_gate^T) * (x_perm W_up^T)
@@ -565,7 +938,10 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
         p.ld_out = F;
         p.status = status;
         p.aux = aux;
-        err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_bound * p.n_tiles, stream);
+        err = pair_routed
+                  ? launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, mt2_bound * p.n_tiles,
+                                                          stream)
+                  : launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_bound * p.n_tiles, stream);
         if (err == cudaSuccess)
             err = record_stage(ev, 3, stream);
         if (err != cudaSuccess)
@@ -576,7 +952,8 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
         const int bn = wide_down ? 256 : 128;
         CUtensorMap mA, mB;
         if (!make_map(&mA, h, (uint64_t)R, (uint64_t)F, kTileM) ||
-            !make_map(&mB, W_down, (uint64_t)E * D, (uint64_t)F, (uint32_t)bn))
+            !make_map(&mB, W_down, (uint64_t)E * D, (uint64_t)F,
+                      (uint32_t)(pair_routed ? bn / 2 : bn)))
             return cudaErrorInvalidValue;
         TcParams p{};
         p.seg_off = seg;
@@ -589,16 +966,24 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
         p.out = z;
         p.ld_out = D;
         p.status = status;
-        const long long tiles = mt_bound * p.n_tiles;
+        const long long tiles = (pair_routed ? mt2_bound : mt_bound) * p.n_tiles;
         if (direct_y(c)) {
             p.out = y;
             p.row_tok = reinterpret_cast<const int32_t *>(ws + L.row_tok);
             p.row_w = reinterpret_cast<const float *>(ws + L.row_w);
-            err = wide_down ? launch_tc<256, 1, EPI_BF16_Y, 4>(mA, mB, mB, p, tiles, stream)
-                            : launch_tc<128, 1, EPI_BF16_Y, 6>(mA, mB, mB, p, tiles, stream);
+            if (pair_routed)
+                err = wide_down ? launch_tc_pair<256, 1, EPI_BF16_Y, 6>(mA, mB, mB, p, tiles, stream)
+                                : launch_tc_pair<128, 1, EPI_BF16_Y, 8>(mA, mB, mB, p, tiles, stream);
+            else
+                err = wide_down ? launch_tc<256, 1, EPI_BF16_Y, 4>(mA, mB, mB, p, tiles, stream)
+                                : launch_tc<128, 1, EPI_BF16_Y, 6>(mA, mB, mB, p, tiles, stream);
         } else {
-            err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, tiles, stream)
-                            : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream);
+            if (pair_routed)
+                err = wide_down ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream)
+                                : launch_tc_pair<128, 1, EPI_BF16, 8>(mA, mB, mB, p, tiles, stream);
+            else
+                err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, tiles, stream)
+                                : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream);
         }
         if (err == cudaSuccess)
             err = record_stage(ev, 4, stream);
@@ -623,7 +1008,10 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.out = hs;
             p.ld_out = S;
             p.status = status;
-            err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt * p.n_tiles, stream);
+            const long long mt2 = (T + kPairRows - 1) / kPairRows;
+            err = pair_shared
+                      ? launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, mt2 * p.n_tiles, stream)
+                      : launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt * p.n_tiles, stream);
             if (err == cudaSuccess)
                 err = record_stage(ev, 5, stream);
             if (err != cudaSuccess)
@@ -633,7 +1021,8 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             const int bn = wide_down ? 256 : 128;
             CUtensorMap mA, mB;
             if (!make_map(&mA, hs, (uint64_t)T, (uint64_t)S, kTileM) ||
-                !make_map(&mB, Ws_down, (uint64_t)D, (uint64_t)S, (uint32_t)bn))
+                !make_map(&mB, Ws_down, (uint64_t)D, (uint64_t)S,
+                          (uint32_t)(pair_shared ? bn / 2 : bn)))
                 return cudaErrorInvalidValue;
             TcParams p{};
             p.nseg = 1;
@@ -644,8 +1033,14 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.out = zs;
             p.ld_out = D;
             p.status = status;
-            err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt * p.n_tiles, stream)
-                            : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt * p.n_tiles, stream);
+            const long long mt2 = (T + kPairRows - 1) / kPairRows;
+            if (pair_shared)
+                err = wide_down
+                          ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, mt2 * p.n_tiles, stream)
+                          : launch_tc_pair<128, 1, EPI_BF16, 8>(mA, mB, mB, p, mt2 * p.n_tiles, stream);
+            else
+                err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt * p.n_tiles, stream)
+                                : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt * p.n_tiles, stream);
             if (err == cudaSuccess)
                 err = record_stage(ev, 6, stream);
             if (err != cudaSuccess)

@@ -25,6 +25,19 @@ SMALL = [
     ("ragged_chunk_t33", 33, 128, 8, 128, 2, 64, 0, 1.25, "none"),
 ]
 
+# Large enough for the CTA-pair GEMMs (>= 16384 rows and >= 512 rows per
+# expert), with small D and F so that the oracle stays cheap: y is checked on
+# a seeded sample of rows, routing on every token.
+PAIR = [
+    # ragged segments, partial column tiles (F = 320, D = 192), drops, and
+    # a shared expert (dense pair tiles)
+    ("pair_ragged_drops", 8200, 192, 4, 320, 2, 256, 1, 0.6, "normal_var2"),
+    # one expert per token, no shared expert: the down projection writes y
+    ("pair_top1_direct_y", 16400, 256, 8, 256, 1, 0, 2, 1.1, "none"),
+    # dropless, several experts empty or tiny, k = 4
+    ("pair_dropless_zipf", 4200, 128, 8, 192, 4, 128, 0, 0.0, "zipf1.1"),
+]
+
 
 def _w(name, T, D, E, F, k, S, mode, gamma, bias, dtype="bf16"):
     return Workload(name, T=T, D=D, E=E, F=F, k=k, S=S, mode=mode, gamma=gamma,
@@ -53,6 +66,15 @@ def test_small_bf16_layers(case):
     _, inp, outs, code = parity.run(w, seed=3)
     assert code == B.MOE_DEVICE_OK
     parity.check(w, inp, outs)
+
+
+@pytest.mark.parametrize("case", PAIR, ids=[c[0] for c in PAIR])
+def test_pair_tile_layers(case):
+    w = _w(*case)
+    _, inp, outs, code = parity.run(w, seed=6)
+    assert code == B.MOE_DEVICE_OK
+    rep = parity.check(w, inp, outs, y_sample_n=96)
+    print(case[0], rep)
 
 
 @pytest.mark.parametrize("case", SMALL[:4], ids=[c[0] for c in SMALL[:4]])
