@@ -87,9 +87,40 @@ WorkspaceLayout layout_of(const moe_config *c)
     L.h = take(esz * L.R_max * F);
     L.z = take(esz * L.R_max * D);
     L.hs = take(S > 0 ? esz * T * S : 0);
-    L.zs = take(S > 0 ? esz * T * D : 0);
+    const int zsplit = S > 0 ? shared_down_splits(*c) : 1;
+    L.zs = take(S > 0 ? (zsplit > 1 ? sizeof(float) * zsplit * T * D : esz * T * D) : 0);
+    const int lsplit = router_splits(*c);
+    L.lpart = take(lsplit > 1 ? sizeof(float) * lsplit * T * E : 0);
     L.total = off;
     return L;
+}
+
+int shared_down_splits(const moe_config &c)
+{
+    if (c.dtype != MOE_DTYPE_BF16 || c.d_shared <= 0 || c.T <= 0)
+        return 1;
+    const long long bn = c.d_model > 1024 ? 256 : 128;
+    const long long tiles = ((c.T + kTileM - 1) / kTileM) * ((c.d_model + bn - 1) / bn);
+    const long long nk = c.d_shared / 64;
+    constexpr long long kNominalSms = 148;
+    if (tiles * 2 > kNominalSms)
+        return 1;
+    long long s = std::min<long long>(8, kNominalSms / tiles);
+    s = std::min<long long>(s, nk / 16);  // at least 16 k-steps of 64 per split
+    return (int)std::max<long long>(1, s);
+}
+
+int router_splits(const moe_config &c)
+{
+    if (c.dtype != MOE_DTYPE_BF16 || c.T <= 0 || c.T >= 512 || router_fused(c))
+        return 1;
+    const long long E = c.n_experts;
+    const long long bn = E <= 16 ? 16 : E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256;
+    const long long tiles = ((c.T + kTileM - 1) / kTileM) * ((E + bn - 1) / bn);
+    const long long nk = c.d_model / 64;
+    constexpr long long kNominalSms = 148;
+    long long s = std::min<long long>(kNominalSms / tiles, nk / 4);  // >= 4 k-steps per split
+    return (int)std::max<long long>(1, std::min<long long>(s, kMaxRouterSplits));
 }
 
 std::atomic<cudaEvent_t *> g_stage_events{nullptr};
@@ -189,9 +220,12 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r,
     // 1. router scores (small routers run inside the dispatch kernel instead)
     cudaError_t err = cudaSuccess;
     const bool fused = router_fused(c) && aligned16(x) && aligned16(W_r);
+    const int lsplit = fused ? 1 : router_splits(c);
+    float *lpart = lsplit > 1 ? reinterpret_cast<float *>(ws + L.lpart) : nullptr;
     if (!fused) {
-        if (c.dtype == MOE_DTYPE_BF16 && c.T >= 512)
-            err = launch_router_tc(c, x, W_r, router_logits, status, stream);
+        if (c.dtype == MOE_DTYPE_BF16)
+            err = launch_router_tc(c, x, W_r, lsplit > 1 ? lpart : router_logits, lsplit, status,
+                                   stream);
         else
             err = launch_router_simt(c, x, W_r, router_logits, stream);
     }
@@ -199,8 +233,9 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r,
         return MOE_ERR_CUDA;
     // 2. gating, demand counts, capacity, segments, balance loss, gather of x
     //    into expert order (one cooperative kernel)
-    if (!cuda_ok(launch_dispatch(c, L, ws, x, W_r, fused, router_logits, router_bias, topk_idx,
-                                 topk_w, dropped_mask, expert_counts, kept_counts, y, stream)) ||
+    if (!cuda_ok(launch_dispatch(c, L, ws, x, W_r, fused, router_logits, lpart, lsplit,
+                                 router_bias, topk_idx, topk_w, dropped_mask, expert_counts,
+                                 kept_counts, y, stream)) ||
         !cuda_ok(record_stage(ev, 2, stream)))
         return MOE_ERR_CUDA;
     // 3. experts (routed segments and the shared expert); the first expert

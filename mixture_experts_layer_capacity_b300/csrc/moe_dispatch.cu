@@ -51,6 +51,8 @@ enum { ROUTER_NONE = 0, ROUTER_BF16 = 1, ROUTER_F32 = 2 };
 
 struct DispatchParams {
     float *logits;          // [T,E]: raw scores in (unless fused), scores (+bias) out
+    const float *lpart;     // [lsplit][T][E] router partial scores, or null
+    int lsplit;
     const float *bias;      // [E] or null
     const void *x;          // [T,D]
     const void *W_r;        // [E,D] (fused router only)
@@ -428,6 +430,17 @@ __device__ __forceinline__ void gate_token(const DispatchParams &p, const float 
                 v = rpart[e];
                 for (int q = 1; q < nparts; ++q)
                     v += rpart[q * pstride + e];
+            } else if (p.lpart) {
+                // all partial loads first, then the sum in split order
+                float part[kMaxRouterSplits];
+#pragma unroll
+                for (int q = 0; q < kMaxRouterSplits; ++q)
+                    part[q] = q < p.lsplit ? p.lpart[((size_t)q * p.T + t) * E + e] : 0.f;
+                v = part[0];
+#pragma unroll
+                for (int q = 1; q < kMaxRouterSplits; ++q)
+                    if (q < p.lsplit)
+                        v += part[q];
             } else {
                 v = p.logits[(size_t)t * E + e];
             }
@@ -448,7 +461,7 @@ __device__ __forceinline__ void gate_token(const DispatchParams &p, const float 
     for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
         if (e < E) {
-            if (RT != ROUTER_NONE || p.bias)
+            if (RT != ROUTER_NONE || p.bias || p.lpart)
                 p.logits[(size_t)t * E + e] = s[i];
             bad |= !isfinite(s[i]);
         }
@@ -892,6 +905,8 @@ static cudaError_t launch_dispatch_t(DispatchParams &p, size_t wr_bytes, cudaStr
                                               kStageMaxBytes + kChunk * 16, kMaxExperts, kMaxTopK);
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)smem_max);
+        if (err == cudaSuccess)
+            err = prefer_max_shared_carveout(kern);
         if (err != cudaSuccess)
             return err;
         int per_sm = 0;
@@ -935,13 +950,16 @@ static cudaError_t launch_dispatch_t(DispatchParams &p, size_t wr_bytes, cudaStr
 
 cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                             const void *x, const void *W_r, bool fused, float *logits,
-                            const float *bias, int32_t *topk_idx, float *topk_w,
-                            uint8_t *dropped_mask, int32_t *expert_counts, int32_t *kept_counts,
-                            void *y, cudaStream_t stream)
+                            const float *lpart, int lsplit, const float *bias,
+                            int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
+                            int32_t *expert_counts, int32_t *kept_counts, void *y,
+                            cudaStream_t stream)
 {
     DispatchParams p;
     const size_t esz = c.dtype == MOE_DTYPE_BF16 ? 2 : 4;
     p.logits = logits;
+    p.lpart = lpart;
+    p.lsplit = lsplit;
     p.bias = bias;
     p.x = x;
     p.W_r = W_r;

@@ -59,6 +59,8 @@ struct TcParams {
     const float *row_w;      // EPI_BF16_Y: gate weight of each A row
     int32_t *status;
     AuxArgs aux;             // balance loss to evaluate (aux.out null: none)
+    int ksplit;              // splits of the reduction (single-CTA kernel, EPI_F32); 0 or 1 = none
+    long long part_stride;   // elements between the splits' fp32 outputs
 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any tile
@@ -160,7 +162,7 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const uint32_
 // tile.  taddr: TMEM address of the row's first accumulator column.
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_row(const TcParams &p, uint32_t taddr, bool row_ok,
-                                             long long orow, int n_idx)
+                                             long long orow, int n_idx, int ks = 0)
 {
     if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll 1
@@ -245,11 +247,22 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, uint32_t taddr, 
             }
             if (row_ok) {
                 const int col = n_idx * BN + c0;
-                float *dst = reinterpret_cast<float *>(p.out) + orow * p.ld_out + col;
+                float *dst = reinterpret_cast<float *>(p.out) + ks * p.part_stride + orow * p.ld_out + col;
+                // 16-byte stores when the whole chunk is in range and aligned
+                const bool vec = col + CH <= p.N_valid && ((p.ld_out | p.part_stride) & 3) == 0 &&
+                                 (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
+                if (vec) {
 #pragma unroll
-                for (int i = 0; i < CH; ++i)
-                    if (col + i < p.N_valid)
-                        dst[i] = __uint_as_float(v[i]);
+                    for (int i = 0; i < CH; i += 4)
+                        *reinterpret_cast<float4 *>(dst + i) =
+                            make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                        __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < CH; ++i)
+                        if (col + i < p.N_valid)
+                            dst[i] = __uint_as_float(v[i]);
+                }
             }
         }
     }
@@ -319,8 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int ntiles = failed ? 0 : tile_count(p, s_mt);
-    const int nk = (p.K + 63) / 64;
+    // work units: tiles x reduction splits (unit u: tile u / ks_n, split u % ks_n)
+    const int ks_n = p.ksplit > 1 ? p.ksplit : 1;
+    const int ntiles = failed ? 0 : tile_count(p, s_mt) * ks_n;
+    const int nk_all = (p.K + 63) / 64;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -329,10 +344,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             long long fills = 0;
             bool ok = true;
-            for (int g = blockIdx.x; g < ntiles && ok; g += gridDim.x) {
+            for (int u = blockIdx.x; u < ntiles && ok; u += gridDim.x) {
+                const int g = u / ks_n, ks = u - g * ks_n;
+                const int kb0 = ks * nk_all / ks_n, kb1 = (ks + 1) * nk_all / ks_n;
                 const TileInfo ti = tile_info(p, s_seg, s_mt, g);
                 const int b_row = ti.seg * p.b_seg_rows + ti.n_idx * BN;
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
@@ -368,14 +385,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             int s = 0;
             uint32_t ph = 0, b = 0, tph = 0;
             bool ok = true;
-            for (int g = blockIdx.x; g < ntiles && ok; g += gridDim.x) {
+            for (int u = blockIdx.x; u < ntiles && ok; u += gridDim.x) {
+                const int ks = u % ks_n;
+                const int kb0 = ks * nk_all / ks_n, kb1 = (ks + 1) * nk_all / ks_n;
                 if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * S::UMMA_N;
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&full[s], ph, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
@@ -387,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
-                                  (kb > 0 || kk > 0) ? 1u : 0u);
+                                  (kb > kb0 || kk > 0) ? 1u : 0u);
                     umma_commit(&empty[s]);
                     if (++s == STAGES) {
                         s = 0;
@@ -418,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;             // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;        // accumulator row of this thread
         uint32_t b = 0, tph = 0;
-        for (int g = blockIdx.x; g < ntiles; g += gridDim.x) {
+        for (int u = blockIdx.x; u < ntiles; u += gridDim.x) {
+            const int g = u / ks_n, ks = u - g * ks_n;
             const TileInfo ti = tile_info(p, s_seg, s_mt, g);
             if (!mbar_wait(&tfull[b], tph, abort_flag, kWaitLimitNs)) {
                 *abort_flag = 1;
@@ -429,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t taddr = tmem_base + b * S::UMMA_N + ((uint32_t)(q * 32) << 16);
             const bool row_ok = r < ti.rows;
             const long long orow = (long long)ti.a_row0 + r;
-            epilogue_row<BN, EPI>(p, taddr, row_ok, orow, ti.n_idx);
+            epilogue_row<BN, EPI>(p, taddr, row_ok, orow, ti.n_idx, ks);
             tc_fence_before_sync();
             mbar_arrive(&tempty[b]);
             b ^= 1u;
@@ -801,6 +821,8 @@ cudaError_t launch_tc(const CUtensorMap &mA, const CUtensorMap &mB0, const CUten
     if (dev < 64 && !(configured & (1ull << dev))) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    S::SMEM_BYTES);
+        if (err == cudaSuccess)
+            err = prefer_max_shared_carveout(kern);
         if (err != cudaSuccess)
             return err;
         configured |= 1ull << dev;
@@ -842,6 +864,8 @@ cudaError_t launch_tc_pair(const CUtensorMap &mA, const CUtensorMap &mB0, const 
     if (dev < 64 && !(configured & (1ull << dev))) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    S::SMEM_BYTES);
+        if (err == cudaSuccess)
+            err = prefer_max_shared_carveout(kern);
         if (err != cudaSuccess)
             return err;
         cfg.gridDim = dim3((unsigned)(sm_count() & ~1));
@@ -864,8 +888,8 @@ cudaError_t launch_tc_pair(const CUtensorMap &mA, const CUtensorMap &mB0, const 
 
 }  // namespace
 
-cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r,
-                             float *logits, int32_t *status, cudaStream_t stream)
+cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r, float *out,
+                             int splits, int32_t *status, cudaStream_t stream)
 {
     const int E = c.n_experts, D = c.d_model, T = c.T;
     const int bn = E <= 16 ? 16 : E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256;
@@ -882,10 +906,12 @@ cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r
     p.n_tiles = 1;
     p.N_valid = E;
     p.b_seg_rows = 0;
-    p.out = logits;
+    p.out = out;
     p.ld_out = E;
     p.status = status;
-    const long long tiles = (T + kTileM - 1) / kTileM;
+    p.ksplit = splits;
+    p.part_stride = (long long)T * E;
+    const long long tiles = (T + kTileM - 1) / kTileM * std::max(1, splits);
     switch (bn) {
     case 16: return launch_tc<16, 1, EPI_F32, 6>(mA, mB, mB, p, tiles, stream);
     case 32: return launch_tc<32, 1, EPI_F32, 6>(mA, mB, mB, p, tiles, stream);
@@ -1034,13 +1060,22 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.ld_out = D;
             p.status = status;
             const long long mt2 = (T + kPairRows - 1) / kPairRows;
-            if (pair_shared)
+            const int splits = shared_down_splits(c);
+            if (splits > 1) {
+                // decode-sized: fp32 partial sums per split of S, added by the combine
+                p.ksplit = splits;
+                p.part_stride = (long long)T * D;
+                const long long units = mt * p.n_tiles * splits;
+                err = wide_down ? launch_tc<256, 1, EPI_F32, 4>(mA, mB, mB, p, units, stream)
+                                : launch_tc<128, 1, EPI_F32, 6>(mA, mB, mB, p, units, stream);
+            } else if (pair_shared) {
                 err = wide_down
                           ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, mt2 * p.n_tiles, stream)
                           : launch_tc_pair<128, 1, EPI_BF16, 8>(mA, mB, mB, p, mt2 * p.n_tiles, stream);
-            else
+            } else {
                 err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt * p.n_tiles, stream)
                                 : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt * p.n_tiles, stream);
+            }
             if (err == cudaSuccess)
                 err = record_stage(ev, 6, stream);
             if (err != cudaSuccess)

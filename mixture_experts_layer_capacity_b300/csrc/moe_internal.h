@@ -34,7 +34,8 @@ struct WorkspaceLayout {
     size_t h;        // dtype[R_max, F]   SwiGLU hidden rows of the routed experts
     size_t z;        // dtype[R_max, D]   routed expert outputs (unweighted)
     size_t hs;       // dtype[T, S]       shared-expert hidden rows
-    size_t zs;       // dtype[T, D]       shared-expert outputs
+    size_t zs;       // dtype[T, D]       shared-expert outputs (fp32 split partials at decode)
+    size_t lpart;    // float[splits][T][E] router partial scores (split router only)
     size_t total;
     int64_t R_max;   // rows of x_perm: T*k dropless, else min(T*k, E*C)
     int64_t C;       // capacity, -1 dropless
@@ -55,6 +56,23 @@ struct AuxArgs {
     float alpha;
 };
 
+// K-splits of the shared expert's down projection (bf16).  Decode-sized
+// batches give that GEMM only a few output tiles (one 128-row tile times
+// D / 256 column tiles), too few to keep the SMs streaming weights; its
+// reduction over S is then split so that about one work unit per SM results.
+// The splits write fp32 partial sums [splits][T][D], which the combine kernel
+// adds in split order.  1 = no split (bf16 output [T][D]).
+int shared_down_splits(const moe_config &c);
+
+// K-splits of the tensor-core router GEMM.  Batches below 512 tokens give
+// it one to four 128-row tiles, so its reduction over d_model is split
+// (about one work unit per SM); the splits write fp32 partial scores
+// [splits][T][E], which the dispatch kernel adds in split order.  1 = no
+// split (scores written directly).  Only for bf16 routers not fused into the
+// dispatch kernel.
+int router_splits(const moe_config &c);
+constexpr int kMaxRouterSplits = 8;
+
 moe_status validate_config(const moe_config *cfg);
 int64_t capacity_of(const moe_config *cfg);
 WorkspaceLayout layout_of(const moe_config *cfg);
@@ -69,11 +87,14 @@ bool router_fused(const moe_config &c);
 // each kept row goes straight to its token, scaled by its gate weight.
 bool direct_y(const moe_config &c);
 // Routing, capacity and dispatch in one cooperative kernel (see moe_dispatch.cu).
+// `lpart`/`lsplit`: the split router's partial scores (null/1: scores are
+// already in `logits`, or the router is fused).
 cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                             const void *x, const void *W_r, bool fused, float *logits,
-                            const float *bias, int32_t *topk_idx, float *topk_w,
-                            uint8_t *dropped_mask, int32_t *expert_counts, int32_t *kept_counts,
-                            void *y, cudaStream_t stream);
+                            const float *lpart, int lsplit, const float *bias,
+                            int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
+                            int32_t *expert_counts, int32_t *kept_counts, void *y,
+                            cudaStream_t stream);
 cudaError_t launch_combine(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                            const float *topk_w, void *y, cudaStream_t stream);
 // `aux`: the balance loss, evaluated by the first expert kernel.
@@ -100,9 +121,10 @@ inline cudaError_t record_stage(cudaEvent_t *ev, int i, cudaStream_t stream)
 }
 
 // Tensor-core (tcgen05 + TMA) paths, bf16 only.  Return cudaErrorInvalidValue
-// if a tensor map cannot be encoded.
-cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r,
-                             float *logits, int32_t *status, cudaStream_t stream);
+// if a tensor map cannot be encoded.  The router writes scores [T][E] to
+// `out` when splits == 1, else fp32 partials [splits][T][E].
+cudaError_t launch_router_tc(const moe_config &c, const void *x, const void *W_r, float *out,
+                             int splits, int32_t *status, cudaStream_t stream);
 // `ev` (nullable): stage events 3..6 are recorded after each GEMM.  `aux`:
 // the balance loss, evaluated by the first expert kernel.
 cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
@@ -131,6 +153,16 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// Asks for the largest shared-memory carveout for `kern`.  Every kernel of
+// the layer runs with the same L1/shared split, so consecutive kernels do not
+// wait for the SMs to be reconfigured (the GEMMs need ~200 KB per CTA).
+template <typename Kern>
+cudaError_t prefer_max_shared_carveout(Kern kern)
+{
+    return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared);
 }
 
 // Stage events set by moe_set_stage_events (null = not recording).
