@@ -31,6 +31,7 @@ _lib = None
 MODE_SOFTMAX_SELECTED = 0
 MODE_SOFTMAX_ALL = 1
 MODE_SOFTMAX_ALL_RENORM = 2
+MODE_SIGMOID_SELECTED = 3
 
 _ERRORS = {-1: "bad argument", -2: "out of host memory", -3: "non-finite router score"}
 
@@ -59,7 +60,7 @@ def _load():
         vp = ctypes.c_void_p
         lib.oracle_router_logits.argtypes = [i64, i64, i64, vp, vp, vp, vp]
         lib.oracle_router_logits.restype = None
-        lib.oracle_route.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp]
+        lib.oracle_route.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp]
         lib.oracle_route.restype = i32
         lib.oracle_capacity.argtypes = [i64, i64, i64, f64]
         lib.oracle_capacity.restype = i64
@@ -70,7 +71,7 @@ def _load():
         lib.oracle_swiglu_rows.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
         lib.oracle_swiglu_rows.restype = i32
         lib.oracle_moe_forward.argtypes = (
-            [i64, i64, i64, i64, i64, i64, i32, f64, f64] + [vp] * 9 + [vp] * 9)
+            [i64, i64, i64, i64, i64, i64, i32, f64, f64, i32] + [vp] * 9 + [vp] * 9)
         lib.oracle_moe_forward.restype = i32
         _lib = lib
         return lib
@@ -104,16 +105,18 @@ def router_logits(x, W_r, bias=None):
     return s
 
 
-def route(s, k, mode):
+def route(s, k, mode, sel_bias=None):
     """Top-k routing of scores s [T, E] -> (idx int32 [T,k], w f64 [T,k],
-    P_sum f64 [E], counts int64 [E])."""
+    P_sum f64 [E], counts int64 [E]).  sel_bias [E]: a bias that only the
+    selection sees (key = fp32(s + b))."""
     s = _f64(s)
     T, E = s.shape
+    b = None if sel_bias is None else _f32(sel_bias)
     idx = np.empty((T, k), dtype=np.int32)
     w = np.empty((T, k), dtype=np.float64)
     P_sum = np.empty(E, dtype=np.float64)
     counts = np.empty(E, dtype=np.int64)
-    _check(_load().oracle_route(T, E, k, mode, _ptr(s), _ptr(idx), _ptr(w),
+    _check(_load().oracle_route(T, E, k, mode, _ptr(s), _ptr(b), _ptr(idx), _ptr(w),
                                 _ptr(P_sum), _ptr(counts)))
     return idx, w, P_sum, counts
 
@@ -152,10 +155,12 @@ def swiglu_rows(x_rows, Wg, Wu, Wd):
 
 
 def moe_forward(x, W_r, W_gate, W_up, W_down, *, k, mode, gamma=0.0, alpha=0.0,
-                bias=None, Ws_gate=None, Ws_up=None, Ws_down=None, s_in=None):
+                bias=None, Ws_gate=None, Ws_up=None, Ws_down=None, s_in=None,
+                bias_selection_only=False):
     """The whole layer on the host.  Returns a dict with s, idx, w, dropped,
     counts, kept, aux, y.  s_in routes on given scores instead of the
-    oracle's own."""
+    oracle's own.  bias_selection_only: the bias shifts only the selection
+    keys (the scores and weights exclude it)."""
     x, W_r = _f32(x), _f32(W_r)
     W_gate, W_up, W_down = _f32(W_gate), _f32(W_up), _f32(W_down)
     T, D = x.shape
@@ -172,7 +177,7 @@ def moe_forward(x, W_r, W_gate, W_up, W_down, *, k, mode, gamma=0.0, alpha=0.0,
         counts=np.empty(E, np.int64), kept=np.empty(E, np.int64),
         aux=np.empty(1, np.float64), y=np.empty((T, D), np.float64))
     _check(_load().oracle_moe_forward(
-        T, D, E, F, k, S, mode, float(gamma), float(alpha),
+        T, D, E, F, k, S, mode, float(gamma), float(alpha), int(bool(bias_selection_only)),
         _ptr(x), _ptr(W_r), _ptr(b), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
         _ptr(Wsg), _ptr(Wsu), _ptr(Wsd), _ptr(sin),
         _ptr(out["s"]), _ptr(out["idx"]), _ptr(out["w"]), _ptr(out["dropped"]),

@@ -57,10 +57,16 @@
  *      ([M17] 17.2 "Switch Transformer and Qwen2"); with k = 1 this is the
  *      raw top-1 probability ([MPF] "The router", last remark);
  *   2: softmax over all E, renormalised over the chosen k
- *      ([MPF] "The router", equation MoE(x)). */
+ *      ([MPF] "The router", equation MoE(x));
+ *   3: sigmoid of each score, normalised over the chosen k ([MPF] "The
+ *      router", closing remark: DeepSeek-V3 scores experts with a sigmoid
+ *      rather than a softmax, normalised over the chosen ones).  For the
+ *      balance loss's P_e the sigmoids are normalised over all E experts
+ *      (reading: the "router probability" of a sigmoid router). */
 #define MODE_SOFTMAX_SELECTED 0
 #define MODE_SOFTMAX_ALL 1
 #define MODE_SOFTMAX_ALL_RENORM 2
+#define MODE_SIGMOID_SELECTED 3
 
 /* Router scores: s[t][e] = sum_d x[t][d] * W_r[e][d] (+ bias[e]).
  * [MPF] "The router" (one score per expert, x W_r); [FRT] "Where the experts
@@ -98,9 +104,15 @@ static void softmax_row(int64_t E, const double *s, double *p)
         p[e] /= z;
 }
 
-/* Top-k selection: k rounds, each taking the largest score not yet taken; on
- * equal scores the lower expert index wins (the pages leave tie order open;
- * this is the reading the whole build uses).  idx[0] is the largest. */
+/* Logistic sigmoid 1 / (1 + e^{-a}). */
+static double sigmoid(double a)
+{
+    return 1.0 / (1.0 + exp(-a));
+}
+
+/* Top-k selection: k rounds, each taking the largest key not yet taken; on
+ * equal keys the lower expert index wins (the pages leave tie order open;
+ * this is the reading the whole build uses).  idx[0] has the largest key. */
 static void topk_row(int64_t E, int64_t k, const double *s, unsigned char *taken,
                      int32_t *idx)
 {
@@ -119,24 +131,33 @@ static void topk_row(int64_t E, int64_t k, const double *s, unsigned char *taken
 }
 
 /* Routing of T tokens from their scores s[T][E]:
- *   idx[t][0..k-1]  chosen experts, largest score first;
+ *   idx[t][0..k-1]  chosen experts, largest selection key first;
  *   w[t][0..k-1]    gate weights for the given mode;
- *   P_sum[e]        sum over tokens of the full-softmax probability of e
- *                   (the balance loss's P_e is P_sum[e] / T);
+ *   P_sum[e]        sum over tokens of the router probability of e (the
+ *                   full softmax; mode 3: the sigmoids normalised over all E);
+ *                   the balance loss's P_e is P_sum[e] / T;
  *   counts[e]       assignments (t, j) with idx[t][j] == e, before capacity.
+ * sel_bias (nullable, [E]): a bias that only selection sees ([MPF] "Keeping
+ * the load even", bias balancing: added to the scores only when choosing the
+ * top k, never in the weights).  The selection key is then the score plus the
+ * bias rounded to fp32, as the scores and biases are fp32 on the GPU; without
+ * it the key is the score itself.  The weights always use the scores.
  * Returns ORACLE_OK, ORACLE_BAD_ARG or ORACLE_NONFINITE (a score is NaN/Inf). */
 int oracle_route(int64_t T, int64_t E, int64_t k, int mode, const double *s,
-                 int32_t *idx, double *w, double *P_sum, int64_t *counts)
+                 const float *sel_bias, int32_t *idx, double *w, double *P_sum,
+                 int64_t *counts)
 {
-    if (T < 0 || E < 1 || k < 1 || k > E || mode < 0 || mode > 2)
+    if (T < 0 || E < 1 || k < 1 || k > E || mode < 0 || mode > 3)
         return ORACLE_BAD_ARG;
     for (int64_t i = 0; i < T * E; ++i)
         if (!isfinite(s[i]))
             return ORACLE_NONFINITE;
     double *p = (double *)malloc(sizeof(double) * (size_t)E);
+    double *key = (double *)malloc(sizeof(double) * (size_t)E);
     unsigned char *taken = (unsigned char *)malloc((size_t)E);
-    if (!p || !taken) {
+    if (!p || !key || !taken) {
         free(p);
+        free(key);
         free(taken);
         return ORACLE_NO_MEMORY;
     }
@@ -148,16 +169,38 @@ int oracle_route(int64_t T, int64_t E, int64_t k, int mode, const double *s,
         const double *st = s + t * E;
         int32_t *it = idx + t * k;
         double *wt = w + t * k;
-        softmax_row(E, st, p);
-        topk_row(E, k, st, taken, it);
+        if (mode == MODE_SIGMOID_SELECTED) {
+            double z = 0.0;
+            for (int64_t e = 0; e < E; ++e) {
+                p[e] = sigmoid(st[e]);
+                z += p[e];
+            }
+            for (int64_t e = 0; e < E; ++e)
+                p[e] /= z;
+        } else {
+            softmax_row(E, st, p);
+        }
+        for (int64_t e = 0; e < E; ++e)
+            key[e] = sel_bias ? (double)(float)((float)st[e] + sel_bias[e]) : st[e];
+        topk_row(E, k, key, taken, it);
         if (mode == MODE_SOFTMAX_SELECTED) {
             /* g_i = e^{s_i} / sum_{j in top-k} e^{s_j}; the largest selected
-             * score (it[0]) is subtracted for range only. */
+             * score is subtracted for range only. */
             double m = st[it[0]], z = 0.0;
+            for (int64_t j = 1; j < k; ++j)
+                if (st[it[j]] > m)
+                    m = st[it[j]];
             for (int64_t j = 0; j < k; ++j)
                 z += exp(st[it[j]] - m);
             for (int64_t j = 0; j < k; ++j)
                 wt[j] = exp(st[it[j]] - m) / z;
+        } else if (mode == MODE_SIGMOID_SELECTED) {
+            /* w_i = sigmoid(s_i) / sum_{j in top-k} sigmoid(s_j) */
+            double z = 0.0;
+            for (int64_t j = 0; j < k; ++j)
+                z += sigmoid(st[it[j]]);
+            for (int64_t j = 0; j < k; ++j)
+                wt[j] = sigmoid(st[it[j]]) / z;
         } else if (mode == MODE_SOFTMAX_ALL) {
             for (int64_t j = 0; j < k; ++j)
                 wt[j] = p[it[j]];
@@ -175,6 +218,7 @@ int oracle_route(int64_t T, int64_t E, int64_t k, int mode, const double *s,
             counts[it[j]] += 1;
     }
     free(p);
+    free(key);
     free(taken);
     return ORACLE_OK;
 }
@@ -299,10 +343,14 @@ int oracle_swiglu_rows(int64_t n, int64_t D, int64_t F, const float *x,
  * s_in: scores to route on (e.g. another implementation's fp32 scores widened
  * to double); NULL to use the oracle's own oracle_router_logits().  The scores
  * used are written to s_out.  S = 0: no shared expert (Wsg/Wsu/Wsd unused).
+ * bias_selection_only: 0 = the bias is part of the scores (selection and
+ * weights); 1 = the bias only shifts the selection keys (oracle_route's
+ * sel_bias) and the scores exclude it.
  * Output arrays: s_out[T][E], idx[T][k], w[T][k], dropped[T][k], counts[E],
  * kept[E], aux[1], y[T][D]. */
 int oracle_moe_forward(int64_t T, int64_t D, int64_t E, int64_t F, int64_t k,
                        int64_t S, int mode, double gamma, double alpha,
+                       int bias_selection_only,
                        const float *x, const float *W_r, const float *bias,
                        const float *Wg, const float *Wu, const float *Wd,
                        const float *Wsg, const float *Wsu, const float *Wsd,
@@ -315,12 +363,13 @@ int oracle_moe_forward(int64_t T, int64_t D, int64_t E, int64_t F, int64_t k,
     if (s_in)
         memcpy(s_out, s_in, sizeof(double) * (size_t)(T * E));
     else
-        oracle_router_logits(T, D, E, x, W_r, bias, s_out);
+        oracle_router_logits(T, D, E, x, W_r, bias_selection_only ? NULL : bias, s_out);
 
     double *P_sum = (double *)malloc(sizeof(double) * (size_t)E);
     if (!P_sum)
         return ORACLE_NO_MEMORY;
-    int rc = oracle_route(T, E, k, mode, s_out, idx, w, P_sum, counts);
+    int rc = oracle_route(T, E, k, mode, s_out, bias_selection_only ? bias : NULL, idx, w,
+                          P_sum, counts);
     if (rc != ORACLE_OK) {
         free(P_sum);
         return rc;

@@ -240,22 +240,33 @@ def test_single_expert_is_the_dense_mlp(mode):
     assert np.all(out["w"] == 1.0)
 
 
-def _numpy_layer(x, Wr, Wg, Wu, Wd, k, mode, gamma, sh):
-    """Brute force: run every expert on every token, then mask by routing."""
+def _numpy_layer(x, Wr, Wg, Wu, Wd, k, mode, gamma, sh, sel_bias=None):
+    """Brute force: run every expert on every token, then mask by routing.
+    sel_bias: a bias that only the ranking sees (key = fp32(s) + fp32(b) in
+    fp32)."""
     T, E = x.shape[0], Wr.shape[0]
     s = x.astype(np.float64) @ Wr.astype(np.float64).T
-    z = np.exp(s - s.max(1, keepdims=True))
-    p = z / z.sum(1, keepdims=True)
-    order = np.array([sorted(range(E), key=lambda e: (-s[t, e], e))[:k] for t in range(T)])
+    if mode == 3:
+        a = 1.0 / (1.0 + np.exp(-s))
+        p = a / a.sum(1, keepdims=True)
+    else:
+        z = np.exp(s - s.max(1, keepdims=True))
+        p = z / z.sum(1, keepdims=True)
+    key = s if sel_bias is None else \
+        (s.astype(np.float32) + np.asarray(sel_bias, np.float32)).astype(np.float64)
+    order = np.array([sorted(range(E), key=lambda e: (-key[t, e], e))[:k] for t in range(T)])
     sel_s = np.take_along_axis(s, order, 1)
     sel_p = np.take_along_axis(p, order, 1)
     if mode == 0:
-        ez = np.exp(sel_s - sel_s[:, :1])
+        ez = np.exp(sel_s - sel_s.max(1, keepdims=True))
         w = ez / ez.sum(1, keepdims=True)
     elif mode == 1:
         w = sel_p
-    else:
+    elif mode == 2:
         w = sel_p / sel_p.sum(1, keepdims=True)
+    else:
+        sa = 1.0 / (1.0 + np.exp(-sel_s))
+        w = sa / sa.sum(1, keepdims=True)
     mask = np.ones((T, k))
     if gamma > 0:
         C = math.ceil(gamma * T * k / E)
@@ -276,7 +287,8 @@ def _numpy_layer(x, Wr, Wg, Wu, Wd, k, mode, gamma, sh):
                 counts=counts, aux=aux)
 
 
-@pytest.mark.parametrize("mode,gamma,S", [(0, 0.0, 0), (1, 0.5, 4), (2, 1.0, 0), (0, 0.75, 6)])
+@pytest.mark.parametrize("mode,gamma,S", [(0, 0.0, 0), (1, 0.5, 4), (2, 1.0, 0), (0, 0.75, 6),
+                                         (3, 0.0, 0), (3, 0.75, 4)])
 def test_layer_against_dense_bruteforce(mode, gamma, S):
     rng = np.random.default_rng(100 + mode + S)
     T, D, E, F, k = 24, 8, 5, 6, 2
@@ -351,3 +363,84 @@ def test_routing_on_given_scores():
     np.testing.assert_array_equal(out["s"], s)
     idx, w, _, _ = oracle.route(s, 2, 0)
     np.testing.assert_array_equal(out["idx"], idx)
+
+
+# --- sigmoid gating and selection-only bias ([MPF] "The router", closing
+# remark on DeepSeek-V3; [MPF] "Keeping the load even", bias balancing) ----
+
+def test_sigmoid_gating_closed_form():
+    """sigmoid(ln 9) = 0.9, sigmoid(0) = 0.5, sigmoid(ln 3) = 0.75,
+    sigmoid(-ln 3) = 0.25: top-2 = experts 0 and 2 with weights 0.9/1.65 =
+    6/11 and 0.75/1.65 = 5/11; P = the sigmoids over their sum 2.4."""
+    s = np.array([[math.log(9.0), 0.0, math.log(3.0), -math.log(3.0)]])
+    idx, w, P_sum, counts = oracle.route(s, 2, 3)
+    assert idx[0].tolist() == [0, 2]
+    np.testing.assert_allclose(w[0], [6 / 11, 5 / 11], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(P_sum, np.array([0.9, 0.5, 0.75, 0.25]) / 2.4, atol=1e-14)
+    assert counts.tolist() == [1, 0, 1, 0]
+
+
+def test_sigmoid_top1_weight_is_one_and_probabilities_sum_to_one():
+    rng = np.random.default_rng(71)
+    s = rng.standard_normal((300, 12)) * 2
+    idx, w, P_sum, _ = oracle.route(s, 1, 3)
+    assert np.all(w == 1.0)
+    np.testing.assert_array_equal(idx[:, 0], np.argmax(s, 1))  # sigmoid is monotone
+    assert abs(P_sum.sum() - 300) < 1e-9
+    idx4, w4, _, _ = oracle.route(s, 4, 3)
+    np.testing.assert_allclose(w4.sum(1), 1.0, atol=1e-14)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+def test_selection_bias_changes_selection_not_weights(mode):
+    """A large bias forces an expert into the top k; the weights are those of
+    the unbiased scores over the chosen set."""
+    s = np.array([[math.log(9.0), 0.0, math.log(3.0), -math.log(3.0)]])
+    b = np.array([0.0, 0.0, -10.0, 0.0], np.float32)
+    idx, w, P_sum, counts = oracle.route(s, 2, mode, sel_bias=b)
+    assert idx[0].tolist() == [0, 1]
+    # the same set chosen without a bias, by forcing it through the scores
+    # of a copy where expert 2 cannot win, gives the weights to compare
+    if mode == 3:
+        np.testing.assert_allclose(w[0], [0.9 / 1.4, 0.5 / 1.4], atol=1e-14)
+    elif mode == 0:
+        np.testing.assert_allclose(w[0], [0.9, 0.1], atol=1e-14)   # e^{ln 9}/(9 + 1)
+    p = np.exp(s[0]) / np.exp(s[0]).sum()
+    if mode == 1:
+        np.testing.assert_allclose(w[0], p[[0, 1]], atol=1e-14)
+    if mode == 2:
+        np.testing.assert_allclose(w[0], p[[0, 1]] / p[[0, 1]].sum(), atol=1e-14)
+    # the balance loss's probabilities ignore the bias
+    _, _, P_ref, _ = oracle.route(s, 2, mode)
+    np.testing.assert_allclose(P_sum, P_ref, atol=1e-15)
+    assert counts.tolist() == [1, 1, 0, 0]
+
+
+def test_selection_bias_constant_shift_is_neutral():
+    rng = np.random.default_rng(72)
+    s = np.round(rng.standard_normal((200, 8)) * 4) / 4        # dyadic: exact in fp32
+    b = np.round(rng.standard_normal(8) * 4).astype(np.float32) / 4
+    a = oracle.route(s, 3, 3, sel_bias=b)
+    c = oracle.route(s, 3, 3, sel_bias=b + np.float32(2.0))
+    for u, v in zip(a, c):
+        np.testing.assert_array_equal(u, v)
+
+
+@pytest.mark.parametrize("mode", [0, 3])
+def test_layer_with_selection_bias_against_bruteforce(mode):
+    rng = np.random.default_rng(81 + mode)
+    T, D, E, F, k = 24, 8, 6, 5, 2
+    x, Wr, Wg, Wu, Wd, sh = _rand_layer(rng, T, D, E, F, 3)
+    b = (rng.standard_normal(E) * 0.7).astype(np.float32)
+    out = oracle.moe_forward(x, Wr, Wg, Wu, Wd, k=k, mode=mode, gamma=0.8, alpha=0.01,
+                             bias=b, bias_selection_only=True, **sh)
+    ref = _numpy_layer(x, Wr, Wg, Wu, Wd, k, mode, 0.8, sh, sel_bias=b)
+    np.testing.assert_array_equal(out["idx"], ref["idx"])
+    np.testing.assert_array_equal(out["dropped"], ref["dropped"])
+    np.testing.assert_array_equal(out["counts"], ref["counts"])
+    np.testing.assert_allclose(out["w"], ref["w"], atol=1e-12)
+    np.testing.assert_allclose(out["y"], ref["y"], rtol=1e-10, atol=1e-10)
+    assert abs(out["aux"] - ref["aux"]) < 1e-12
+    # the scores exclude the bias
+    np.testing.assert_allclose(out["s"], x.astype(np.float64) @ Wr.astype(np.float64).T,
+                               rtol=1e-12, atol=1e-12)
