@@ -39,7 +39,8 @@ from mixture_experts_layer_capacity_b300.workloads import WORKLOADS, make_inputs
 METRIC = "MoE-layer fwd tokens/s on 1 B300; % of roofline (TC TFLOP/s or HBM GB/s)"
 DEFAULT_WORKLOAD = "switch_top1_capacity"
 L2_FLUSH_BYTES = 512 << 20
-GATING = {0: "softmax_over_selected", 1: "softmax_over_all", 2: "softmax_over_all_renormalised"}
+GATING = {0: "softmax_over_selected", 1: "softmax_over_all", 2: "softmax_over_all_renormalised",
+          3: "sigmoid_normalised_over_selected"}
 
 
 def _peaks():
@@ -212,7 +213,7 @@ def oracle_rate(w, inputs, budget_s=12.0, min_tokens=16):
             xs = f32(x[:n])
             t0 = time.perf_counter()
             oracle.moe_forward(xs, Wr, Wg, Wu, Wd, k=w.k, mode=w.mode, gamma=gamma,
-                               alpha=w.alpha, bias=b, **sh)
+                               alpha=w.alpha, bias=b, bias_selection_only=w.sel_bias, **sh)
             return time.perf_counter() - t0
 
         n0 = min(T, min_tokens)
@@ -229,8 +230,8 @@ def oracle_rate(w, inputs, budget_s=12.0, min_tokens=16):
     def run_sampled(n):
         xs = f32(x[:n])
         t0 = time.perf_counter()
-        s = oracle.router_logits(xs, Wr, b)
-        idx, wts, _, _ = oracle.route(s, w.k, w.mode)
+        s = oracle.router_logits(xs, Wr, None if w.sel_bias else b)
+        idx, wts, _, _ = oracle.route(s, w.k, w.mode, sel_bias=b if w.sel_bias else None)
         dropped, _ = oracle.apply_capacity(idx, w.E, oracle.capacity(n, w.k, w.E, gamma))
         spent = time.perf_counter() - t0
         for e in sorted(set(idx[dropped == 0].ravel().tolist())):
@@ -257,7 +258,8 @@ def workload_config(w, l2_note):
     return {"workload": w.name, "T": w.T, "d_model": w.D, "n_experts": w.E, "d_expert": w.F,
             "top_k": w.k, "d_shared": w.S, "gating": GATING[w.mode],
             "capacity_factor": w.gamma if w.gamma > 0 else None,
-            "router_bias": w.bias, "inputs": "seeded synthetic, resident in HBM", "l2": l2_note}
+            "router_bias": w.bias + (" (selection only)" if w.sel_bias else ""),
+            "inputs": "seeded synthetic, resident in HBM", "l2": l2_note}
 
 
 def run_ours(args, rank, world, device):
@@ -486,7 +488,8 @@ def run_reference(args, world):
     small = 4 * (3 * w.E * w.D * w.F + 3 * w.D * w.S) <= (6 << 30)
     if small:
         args_w = dict(k=w.k, mode=w.mode, gamma=float(np.float32(w.gamma)), alpha=w.alpha,
-                      bias=None if inputs.get("b_r") is None else f32(inputs["b_r"]))
+                      bias=None if inputs.get("b_r") is None else f32(inputs["b_r"]),
+                      bias_selection_only=w.sel_bias)
         Wr, Wg, Wu, Wd = (f32(inputs[k]) for k in ("W_r", "W_gate", "W_up", "W_down"))
         sh = {} if not w.S else dict(Ws_gate=f32(inputs["Ws_gate"]), Ws_up=f32(inputs["Ws_up"]),
                                      Ws_down=f32(inputs["Ws_down"]))

@@ -63,11 +63,16 @@ typedef enum {
  *     renormalisation (Switch Transformer / Qwen2; module 17, 17.2); with
  *     k = 1 this is the raw top-1 probability ('The router', last remark).
  *   MOE_GATE_SOFTMAX_ALL_RENORM: w_j = p_{idx_j} / sum_{j'} p_{idx_j'}
- *     ('The router', equation MoE(x)); w = 1 when k = 1. */
+ *     ('The router', equation MoE(x)); w = 1 when k = 1.
+ *   MOE_GATE_SIGMOID_SELECTED: a = sigmoid(s), w_j = a_{idx_j} / sum_{j'}
+ *     a_{idx_j'} ('The router', closing remark: DeepSeek-V3 scores experts
+ *     with a sigmoid, normalised over the chosen ones); the selection is by s
+ *     (sigmoid is monotone); for the balance loss p = a / sum over all E. */
 typedef enum {
     MOE_GATE_SOFTMAX_SELECTED = 0,
     MOE_GATE_SOFTMAX_ALL = 1,
-    MOE_GATE_SOFTMAX_ALL_RENORM = 2
+    MOE_GATE_SOFTMAX_ALL_RENORM = 2,
+    MOE_GATE_SIGMOID_SELECTED = 3
 } moe_gating_mode;
 
 typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP32 = 1 } moe_dtype;
@@ -78,7 +83,12 @@ typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP32 = 1 } moe_dtype;
  *   d_model, d_expert >= 1; d_shared >= 0 (0 = no shared expert);
  *   bf16: d_model, d_expert and d_shared multiples of 64;
  *   fp32: any sizes (SIMT path, for small layers and exact checks).
- * capacity_factor <= 0 means dropless.  aux_alpha scales aux_loss. */
+ * capacity_factor <= 0 means dropless.  aux_alpha scales aux_loss.
+ * bias_selection_only: 0 = router_bias is part of the scores (selection and
+ * weights); 1 = router_bias only shifts the top-k selection keys, fp32(s + b),
+ * and the scores and weights exclude it ("Mixture of Experts: More
+ * Parameters, Same FLOPs", 'Keeping the load even', bias balancing: the bias
+ * is added to the scores only when choosing the top k). */
 typedef struct {
     int32_t T;
     int32_t d_model;
@@ -90,6 +100,7 @@ typedef struct {
     int32_t gating_mode;    /* moe_gating_mode */
     float capacity_factor;
     float aux_alpha;
+    int32_t bias_selection_only;
 } moe_config;
 
 /* Device status codes written by kernels (read with moe_read_device_status). */
@@ -114,14 +125,17 @@ MOE_API int64_t moe_capacity(const moe_config *cfg);
  *   x            [T, d_model]
  *   W_r          [E, d_model]               router, K-major
  *   router_bias  [E] fp32, or NULL          added to the scores before
- *                                           selection and weighting
+ *                                           selection and weighting, or to
+ *                                           the selection keys only
+ *                                           (cfg->bias_selection_only)
  *   W_gate, W_up [E, d_expert, d_model]     K-major
  *   W_down       [E, d_model, d_expert]     K-major
  *   Ws_gate, Ws_up [d_shared, d_model]; Ws_down [d_model, d_shared];
  *                                           all NULL when d_shared == 0
  * Outputs (device):
  *   y             [T, d_model] dtype
- *   router_logits [T, E] fp32   the scores s the routing used (bias included)
+ *   router_logits [T, E] fp32   the scores s (bias included unless it is
+ *                               selection-only)
  *   topk_idx      [T, k] int32  selected experts, largest score first
  *   topk_w        [T, k] fp32   gate weights (not renormalised after drops)
  *   dropped_mask  [T, k] uint8  1 = dropped by capacity

@@ -43,7 +43,8 @@ class MoeConfig(ctypes.Structure):
                 ("n_experts", ctypes.c_int32), ("d_expert", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("d_shared", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("gating_mode", ctypes.c_int32),
-                ("capacity_factor", ctypes.c_float), ("aux_alpha", ctypes.c_float)]
+                ("capacity_factor", ctypes.c_float), ("aux_alpha", ctypes.c_float),
+                ("bias_selection_only", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -85,16 +86,18 @@ def status_string(status: int) -> str:
 
 
 def make_config(T, d_model, n_experts, d_expert, top_k, d_shared=0, dtype="bf16",
-                gating_mode=0, capacity_factor=0.0, aux_alpha=0.01) -> MoeConfig:
+                gating_mode=0, capacity_factor=0.0, aux_alpha=0.01,
+                bias_selection_only=False) -> MoeConfig:
     dt = {"bf16": MOE_DTYPE_BF16, "fp32": MOE_DTYPE_FP32}.get(dtype, dtype)
     return MoeConfig(int(T), int(d_model), int(n_experts), int(d_expert), int(top_k),
                      int(d_shared), int(dt), int(gating_mode), float(capacity_factor),
-                     float(aux_alpha))
+                     float(aux_alpha), int(bool(bias_selection_only)))
 
 
 def config_of(w) -> MoeConfig:
     """MoeConfig of a workloads.Workload."""
-    return make_config(w.T, w.D, w.E, w.F, w.k, w.S, w.dtype, w.mode, w.gamma, w.alpha)
+    return make_config(w.T, w.D, w.E, w.F, w.k, w.S, w.dtype, w.mode, w.gamma, w.alpha,
+                       bias_selection_only=getattr(w, "sel_bias", False))
 
 
 def router_is_fused(cfg: MoeConfig) -> bool:

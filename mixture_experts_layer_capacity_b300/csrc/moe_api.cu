@@ -27,7 +27,9 @@ moe_status validate_config(const moe_config *c)
         return MOE_ERR_INVALID_ARG;
     if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_FP32)
         return MOE_ERR_INVALID_ARG;
-    if (c->gating_mode < MOE_GATE_SOFTMAX_SELECTED || c->gating_mode > MOE_GATE_SOFTMAX_ALL_RENORM)
+    if (c->gating_mode < MOE_GATE_SOFTMAX_SELECTED || c->gating_mode > MOE_GATE_SIGMOID_SELECTED)
+        return MOE_ERR_INVALID_ARG;
+    if (c->bias_selection_only != 0 && c->bias_selection_only != 1)
         return MOE_ERR_INVALID_ARG;
     if (std::isnan(c->capacity_factor) || std::isinf(c->capacity_factor) ||
         !std::isfinite(c->aux_alpha))

@@ -54,6 +54,7 @@ struct DispatchParams {
     const float *lpart;     // [lsplit][T][E] router partial scores, or null
     int lsplit;
     const float *bias;      // [E] or null
+    int bias_sel_only;      // 1: the bias shifts only the selection keys
     const void *x;          // [T,D]
     const void *W_r;        // [E,D] (fused router only)
     int T, E, k, mode, D;
@@ -447,11 +448,13 @@ __device__ __forceinline__ void gate_token(const DispatchParams &p, const float 
         }
         s[i] = v;
     }
-    if (p.bias) {
-        float bv[EPL];
+    // the bias: part of the scores, or (selection-only) of the top-k keys
+    const bool sel_bias = p.bias && p.bias_sel_only;
+    float bv[EPL];
 #pragma unroll
-        for (int i = 0; i < EPL; ++i)
-            bv[i] = lane + 32 * i < E ? __ldg(p.bias + lane + 32 * i) : 0.f;
+    for (int i = 0; i < EPL; ++i)
+        bv[i] = p.bias && lane + 32 * i < E ? __ldg(p.bias + lane + 32 * i) : 0.f;
+    if (p.bias && !sel_bias) {
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
             s[i] += bv[i];
@@ -461,15 +464,17 @@ __device__ __forceinline__ void gate_token(const DispatchParams &p, const float 
     for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
         if (e < E) {
-            if (RT != ROUTER_NONE || p.bias || p.lpart)
+            if (RT != ROUTER_NONE || (p.bias && !sel_bias) || p.lpart)
                 p.logits[(size_t)t * E + e] = s[i];
-            bad |= !isfinite(s[i]);
+            bad |= !isfinite(s[i]) || !isfinite(bv[i]);
         }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0)
         set_status(p.status, MOE_DEVICE_NONFINITE_SCORE);
 
-    // softmax over all E (max subtracted)
+    // router probabilities over all E: softmax (max subtracted), or for the
+    // sigmoid mode the sigmoids normalised over all E (balance loss only)
+    const bool sigm = p.mode == MOE_GATE_SIGMOID_SELECTED;
     float m = -FLT_MAX;
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
@@ -480,7 +485,7 @@ __device__ __forceinline__ void gate_token(const DispatchParams &p, const float 
     float ex[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-        ex[i] = (lane + 32 * i < E) ? expf(s[i] - m) : 0.f;
+        ex[i] = (lane + 32 * i < E) ? (sigm ? 1.f / (1.f + expf(-s[i])) : expf(s[i] - m)) : 0.f;
         z += ex[i];
     }
     z = warp_sum_bcast(z);
@@ -492,12 +497,12 @@ __device__ __forceinline__ void gate_token(const DispatchParams &p, const float 
     }
 
     // top-k: k rounds of a warp arg-max over order keys (redux max), equal
-    // scores resolved to the lower expert index (redux min); lane j keeps
-    // round j's expert and score
+    // keys resolved to the lower expert index (redux min); lane j keeps
+    // round j's expert and (unbiased) score
     int key[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
-        key[i] = (lane + 32 * i < E) ? order_key(s[i]) : INT_MIN;
+        key[i] = (lane + 32 * i < E) ? order_key(sel_bias ? s[i] + bv[i] : s[i]) : INT_MIN;
     uint32_t taken = 0u;
     float my_s = 0.f, s_top = 0.f;
     int my_e = 0;
@@ -516,20 +521,32 @@ __device__ __forceinline__ void gate_token(const DispatchParams &p, const float 
             win = 0;  // unreachable with k <= E; keeps indices in bounds
         if ((win & 31) == lane)
             taken |= 1u << (win >> 5);
-        const float sv = key_value(mk);
-        if (j == 0)
-            s_top = sv;
+        float sv = key_value(mk);
+        if (sel_bias) {
+            // the winner's score without the bias, from the lane that holds it
+            float cand = 0.f;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (i == (win >> 5))
+                    cand = s[i];
+            sv = __shfl_sync(0xffffffffu, cand, win & 31);
+        }
         if (lane == j) {
             my_s = sv;
             my_e = win;
         }
     }
+    // largest selected score (subtracted for range only)
+    s_top = warp_max(lane < k ? my_s : -FLT_MAX);
 
     // gate weights, lane j for assignment j
     float w = 0.f;
     if (p.mode == MOE_GATE_SOFTMAX_SELECTED) {
         const float ev = lane < k ? expf(my_s - s_top) : 0.f;
         w = ev / warp_sum_bcast(ev);
+    } else if (sigm) {
+        const float a = lane < k ? 1.f / (1.f + expf(-my_s)) : 0.f;
+        w = a / warp_sum_bcast(a);
     } else {
         w = lane < k ? expf(my_s - m) / z : 0.f;
         if (p.mode == MOE_GATE_SOFTMAX_ALL_RENORM)
@@ -961,6 +978,7 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
     p.lpart = lpart;
     p.lsplit = lsplit;
     p.bias = bias;
+    p.bias_sel_only = c.bias_selection_only;
     p.x = x;
     p.W_r = W_r;
     p.T = c.T;

@@ -27,6 +27,7 @@ import torch
 GATING_SOFTMAX_SELECTED = 0      # Mixtral: softmax over the k chosen scores
 GATING_SOFTMAX_ALL = 1           # Switch / Qwen2: softmax over all, keep k
 GATING_SOFTMAX_ALL_RENORM = 2    # softmax over all, renormalised over the k
+GATING_SIGMOID_SELECTED = 3      # sigmoid of each score, normalised over the k
 
 
 @dataclass(frozen=True)
@@ -43,6 +44,7 @@ class Workload:
     dtype: str = "bf16"   # "bf16" or "fp32"
     alpha: float = 0.01   # balance-loss coefficient
     bias: str = "none"    # router logit bias: "none", "normal_var2", "zipf1.1"
+    sel_bias: bool = False  # the bias shifts only the top-k selection keys
     description: str = ""
 
     def with_T(self, T: int) -> "Workload":
@@ -86,6 +88,11 @@ WORKLOADS = {
         "dsv3_decode", T=64, D=7168, E=256, F=2048, k=8, S=2048,
         mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1",
         description="DeepSeek-V3-shaped, renormalised top-8, Zipf-skewed bias, T=64"),
+    "dsv3_sigmoid_decode": Workload(
+        "dsv3_sigmoid_decode", T=64, D=7168, E=256, F=2048, k=8, S=2048,
+        mode=GATING_SIGMOID_SELECTED, bias="zipf1.1", sel_bias=True,
+        description="DeepSeek-V3-shaped with its own gating: sigmoid scores "
+                    "normalised over the chosen 8, Zipf-skewed selection-only bias, T=64"),
 }
 
 _TID = {"x": 0, "W_r": 1, "b_r": 2, "W_gate": 3, "W_up": 4, "W_down": 5,

@@ -69,13 +69,14 @@ def check(w, inp, outs, sample=None, logit_rows=None, y_sample_n=None, seed=0):
     rows = np.arange(T) if logit_rows is None else np.asarray(logit_rows)
     if rows.size:
         s_ref = oracle.router_logits(f32(inp["x"][torch.as_tensor(rows, device=inp["x"].device)]),
-                                     f32(inp["W_r"]), b)
+                                     f32(inp["W_r"]), None if w.sel_bias else b)
         den = max(np.abs(s_ref).max(), 1e-30)
         rep["logits_rel"] = float(np.abs(s_gpu[rows] - s_ref).max() / den)
         assert rep["logits_rel"] <= TOL_LOGITS, rep
 
     # 2. routing, capacity and statistics re-derived from the GPU scores
-    idx, wts, P_sum, counts = oracle.route(s_gpu, k, w.mode)
+    idx, wts, P_sum, counts = oracle.route(s_gpu, k, w.mode,
+                                           sel_bias=b if w.sel_bias else None)
     C = oracle.capacity(T, k, E, gamma32)
     dropped, kept = oracle.apply_capacity(idx, E, C)
     aux = oracle.aux_loss(T, k, E, alpha32, counts, P_sum)

@@ -68,7 +68,8 @@ def test_workspace_size_and_validation():
         (dict(d_model=100), B.MOE_ERR_UNSUPPORTED),     # bf16 needs multiples of 64
         (dict(d_expert=96), B.MOE_ERR_UNSUPPORTED),
         (dict(d_shared=32), B.MOE_ERR_UNSUPPORTED),
-        (dict(gating_mode=3), B.MOE_ERR_INVALID_ARG),
+        (dict(gating_mode=4), B.MOE_ERR_INVALID_ARG),
+        (dict(gating_mode=-1), B.MOE_ERR_INVALID_ARG),
         (dict(dtype=7), B.MOE_ERR_INVALID_ARG),
         (dict(capacity_factor=float("nan")), B.MOE_ERR_INVALID_ARG),
     ]
@@ -82,6 +83,14 @@ def test_workspace_size_and_validation():
         assert ei.value.status == code, over
     # fp32 accepts any sizes
     assert B.workspace_size(B.make_config(10, 5, 3, 7, 2, dtype="fp32")) > 0
+    # the sigmoid mode and the selection-only bias flag (0 or 1)
+    assert B.workspace_size(B.make_config(64, 128, 8, 128, 2, gating_mode=3,
+                                          bias_selection_only=True)) > 0
+    cfg = B.make_config(64, 128, 8, 128, 2)
+    cfg.bias_selection_only = 2
+    with pytest.raises(B.MoeError) as ei:
+        B.workspace_size(cfg)
+    assert ei.value.status == B.MOE_ERR_INVALID_ARG
 
 
 def _call(cfg, ptrs, ws_bytes):

@@ -42,9 +42,36 @@ PAIR = [
 ]
 
 
-def _w(name, T, D, E, F, k, S, mode, gamma, bias, dtype="bf16"):
+def _w(name, T, D, E, F, k, S, mode, gamma, bias, dtype="bf16", sel_bias=False):
     return Workload(name, T=T, D=D, E=E, F=F, k=k, S=S, mode=mode, gamma=gamma,
-                    dtype=dtype, alpha=0.01, bias=bias)
+                    dtype=dtype, alpha=0.01, bias=bias, sel_bias=sel_bias)
+
+
+# Sigmoid gating normalised over the chosen experts (mode 3) and a bias that
+# only the top-k selection sees, on each router path (fused, tensor-core,
+# split tensor-core) and both dtypes: name, T, D, E, F, k, S, mode, gamma,
+# bias, sel_bias, dtype
+GATING = [
+    ("sigmoid_top8_e64", 600, 256, 64, 128, 8, 128, 3, 0.0, "zipf1.1", False, "bf16"),
+    ("sigmoid_selbias_e32_drops", 700, 192, 32, 128, 4, 0, 3, 1.0, "normal_var2", True, "bf16"),
+    ("softmax_selbias_fused_router", 900, 256, 8, 256, 2, 64, 0, 0.8, "normal_var2", True, "bf16"),
+    ("renorm_selbias_split_router", 200, 1024, 64, 128, 8, 0, 2, 0.0, "zipf1.1", True, "bf16"),
+    ("raw_top1_selbias", 1024, 128, 16, 128, 1, 0, 1, 1.0, "normal_var2", True, "bf16"),
+    ("sigmoid_selbias_fp32", 300, 64, 8, 64, 2, 32, 3, 0.5, "normal_var2", True, "fp32"),
+]
+
+
+@pytest.mark.parametrize("case", GATING, ids=[c[0] for c in GATING])
+def test_gating_variants(case):
+    name, T, D, E, F, k, S, mode, gamma, bias, sel, dtype = case
+    w = _w(name, T, D, E, F, k, S, mode, gamma, bias, dtype=dtype, sel_bias=sel)
+    _, inp, outs, code = parity.run(w, seed=12)
+    assert code == B.MOE_DEVICE_OK
+    rep = parity.check(w, inp, outs)
+    if sel:
+        # the scores exclude a selection-only bias
+        assert "logits_rel" in rep
+    print(name, rep)
 
 
 @pytest.fixture(autouse=True)
@@ -100,7 +127,8 @@ def test_switch_capacity_workload_every_token():
 
 
 @pytest.mark.parametrize("name", ["mixtral_decode", "qwen2_57b_decode", "dsv3_decode",
-                                  "mixtral_prefill", "qwen2_57b_prefill", "dsv3_prefill"])
+                                  "dsv3_sigmoid_decode", "mixtral_prefill",
+                                  "qwen2_57b_prefill", "dsv3_prefill"])
 def test_benchmark_sized_workloads_sampled(name):
     w = WORKLOADS[name]
     _, inp, outs, code = parity.run(w)
