@@ -73,6 +73,11 @@ def _load():
         lib.oracle_moe_forward.argtypes = (
             [i64, i64, i64, i64, i64, i64, i32, f64, f64, i32] + [vp] * 9 + [vp] * 9)
         lib.oracle_moe_forward.restype = i32
+        lib.oracle_linear.argtypes = [i64, i64, i64, vp, vp, vp]
+        lib.oracle_linear.restype = None
+        lib.oracle_latent_forward.argtypes = (
+            [i64, i64, i64, i64, i64, i64, i64, i32, f64, f64, i32] + [vp] * 11 + [vp] * 9)
+        lib.oracle_latent_forward.restype = i32
         _lib = lib
         return lib
 
@@ -144,8 +149,9 @@ def aux_loss(T, k, E, alpha, counts, P_sum):
 
 
 def swiglu_rows(x_rows, Wg, Wu, Wd):
-    """One SwiGLU expert on rows x [n, D]; Wg, Wu [F, D]; Wd [D, F] -> f64 [n, D]."""
-    x_rows, Wg, Wu, Wd = _f32(x_rows), _f32(Wg), _f32(Wu), _f32(Wd)
+    """One SwiGLU expert on rows x [n, D] (fp32 or fp64); Wg, Wu [F, D];
+    Wd [D, F] -> f64 [n, D]."""
+    x_rows, Wg, Wu, Wd = _f64(x_rows), _f32(Wg), _f32(Wu), _f32(Wd)
     n, D = x_rows.shape
     F = Wg.shape[0]
     out = np.empty((n, D), dtype=np.float64)
@@ -186,16 +192,56 @@ def moe_forward(x, W_r, W_gate, W_up, W_down, *, k, mode, gamma=0.0, alpha=0.0,
     return out
 
 
+def linear(x, W):
+    """Rows x [n, n_in] (fp32 or fp64) times W [n_out, n_in]^T -> f64 [n, n_out]."""
+    x, W = _f64(x), _f32(W)
+    n, n_in = x.shape
+    out = np.empty((n, W.shape[0]), dtype=np.float64)
+    _load().oracle_linear(n, n_in, W.shape[0], _ptr(x), _ptr(W), _ptr(out))
+    return out
+
+
+def latent_forward(x, W_in, W_out, W_r, W_gate, W_up, W_down, *, k, mode, gamma=0.0,
+                   alpha=0.0, bias=None, Ws_gate=None, Ws_up=None, Ws_down=None, s_in=None,
+                   bias_selection_only=False):
+    """A latent MoE: x [T, D_outer] -> x W_in^T [T, L] -> the layer at width L
+    -> y_lat W_out^T [T, D_outer].  Same outputs as moe_forward (y at D_outer)."""
+    x, W_in, W_out, W_r = _f32(x), _f32(W_in), _f32(W_out), _f32(W_r)
+    W_gate, W_up, W_down = _f32(W_gate), _f32(W_up), _f32(W_down)
+    T, Do = x.shape
+    L = W_in.shape[0]
+    E, F, _ = W_gate.shape
+    S = 0 if Ws_gate is None else int(np.asarray(Ws_gate).shape[0])
+    Wsg = None if S == 0 else _f32(Ws_gate)
+    Wsu = None if S == 0 else _f32(Ws_up)
+    Wsd = None if S == 0 else _f32(Ws_down)
+    b = None if bias is None else _f32(bias)
+    sin = None if s_in is None else _f64(s_in)
+    out = dict(
+        s=np.empty((T, E), np.float64), idx=np.empty((T, k), np.int32),
+        w=np.empty((T, k), np.float64), dropped=np.empty((T, k), np.uint8),
+        counts=np.empty(E, np.int64), kept=np.empty(E, np.int64),
+        aux=np.empty(1, np.float64), y=np.empty((T, Do), np.float64))
+    _check(_load().oracle_latent_forward(
+        T, Do, L, E, F, k, S, mode, float(gamma), float(alpha), int(bool(bias_selection_only)),
+        _ptr(x), _ptr(W_in), _ptr(W_out), _ptr(W_r), _ptr(b), _ptr(W_gate), _ptr(W_up),
+        _ptr(W_down), _ptr(Wsg), _ptr(Wsu), _ptr(Wsd), _ptr(sin),
+        _ptr(out["s"]), _ptr(out["idx"]), _ptr(out["w"]), _ptr(out["dropped"]),
+        _ptr(out["counts"]), _ptr(out["kept"]), _ptr(out["aux"]), _ptr(out["y"])))
+    out["aux"] = float(out["aux"][0])
+    return out
+
+
 def moe_rows(x_rows, idx, w, dropped, expert_weights, shared=None):
     """y rows for a sample of tokens, expert by expert.
 
-    x_rows [n, D]: the sampled tokens' inputs; idx/w/dropped [n, k]: their
+    x_rows [n, D] (fp32 or fp64): the sampled tokens' inputs; idx/w/dropped [n, k]: their
     routing (taken from a routing of the whole batch);
     expert_weights(e) -> (Wg [F,D], Wu [F,D], Wd [D,F]) as float32;
     shared: None or (Wsg, Wsu, Wsd).
     Same definition as oracle_moe_forward: y = shared + sum_j kept * w * FFN.
     """
-    x_rows = _f32(x_rows)
+    x_rows = _f64(x_rows)
     n, D = x_rows.shape
     idx = np.asarray(idx)
     w = np.asarray(w, dtype=np.float64)

@@ -72,19 +72,31 @@
  * [MPF] "The router" (one score per expert, x W_r); [FRT] "Where the experts
  * live" (s = W_r x); [SFR] Router (a bias-free linear layer).  The optional
  * per-expert bias is part of the synthetic workloads, not of the pages. */
-void oracle_router_logits(int64_t T, int64_t D, int64_t E, const float *x,
-                          const float *W_r, const float *bias, double *s)
+static void router_logits_f64(int64_t T, int64_t D, int64_t E, const double *x,
+                              const float *W_r, const float *bias, double *s)
 {
     for (int64_t t = 0; t < T; ++t) {
         for (int64_t e = 0; e < E; ++e) {
             double acc = 0.0;
             for (int64_t d = 0; d < D; ++d)
-                acc += (double)x[t * D + d] * (double)W_r[e * D + d];
+                acc += x[t * D + d] * (double)W_r[e * D + d];
             if (bias)
                 acc += (double)bias[e];
             s[t * E + e] = acc;
         }
     }
+}
+
+void oracle_router_logits(int64_t T, int64_t D, int64_t E, const float *x,
+                          const float *W_r, const float *bias, double *s)
+{
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(T * D > 0 ? T * D : 1));
+    if (!xd)
+        return;
+    for (int64_t i = 0; i < T * D; ++i)
+        xd[i] = (double)x[i];
+    router_logits_f64(T, D, E, xd, W_r, bias, s);
+    free(xd);
 }
 
 /* Softmax of one row of scores over all E experts, largest score subtracted
@@ -290,14 +302,14 @@ static double silu(double a)
  * ([MPF] "An MoE tiny GPT": (silu(h G) * (h U)) D; [FRT] "Counting the
  * parameters yourself": three weight matrices per gated expert).
  * h is caller scratch of F doubles. */
-static void swiglu_token(int64_t D, int64_t F, const float *x, const float *Wg,
+static void swiglu_token(int64_t D, int64_t F, const double *x, const float *Wg,
                          const float *Wu, const float *Wd, double *h, double *out)
 {
     for (int64_t f = 0; f < F; ++f) {
         double g = 0.0, u = 0.0;
         for (int64_t d = 0; d < D; ++d) {
-            g += (double)Wg[f * D + d] * (double)x[d];
-            u += (double)Wu[f * D + d] * (double)x[d];
+            g += (double)Wg[f * D + d] * x[d];
+            u += (double)Wu[f * D + d] * x[d];
         }
         h[f] = silu(g) * u;
     }
@@ -309,10 +321,10 @@ static void swiglu_token(int64_t D, int64_t F, const float *x, const float *Wg,
     }
 }
 
-/* One SwiGLU expert applied to n token rows x[n][D] -> out[n][D].  Rows are
- * independent; OpenMP (when compiled in) splits them over host threads
- * without changing any row's arithmetic. */
-int oracle_swiglu_rows(int64_t n, int64_t D, int64_t F, const float *x,
+/* One SwiGLU expert applied to n token rows x[n][D] (fp64) -> out[n][D].
+ * Rows are independent; OpenMP (when compiled in) splits them over host
+ * threads without changing any row's arithmetic. */
+int oracle_swiglu_rows(int64_t n, int64_t D, int64_t F, const double *x,
                        const float *Wg, const float *Wu, const float *Wd,
                        double *out)
 {
@@ -335,6 +347,24 @@ int oracle_swiglu_rows(int64_t n, int64_t D, int64_t F, const float *x,
     return err ? ORACLE_NO_MEMORY : ORACLE_OK;
 }
 
+/* A linear map of n rows: out[r][o] = sum_i in[r][i] * W[o][i], W [N_out][N_in]
+ * (fp32, each output's coefficients contiguous), in and out fp64.  Used for
+ * the projections of a latent MoE ([MPF] "Where MoE is going", latent MoE:
+ * inputs down-projected 4096 -> 1024, experts applied, outputs up-projected
+ * 1024 -> 4096). */
+void oracle_linear(int64_t n, int64_t n_in, int64_t n_out, const double *in,
+                   const float *W, double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t o = 0; o < n_out; ++o) {
+            double acc = 0.0;
+            for (int64_t i = 0; i < n_in; ++i)
+                acc += in[r * n_in + i] * (double)W[o * n_in + i];
+            out[r * n_out + o] = acc;
+        }
+}
+
 /* The whole layer ([M17] 17.2 equation with the shared expert):
  *   y_t = FFN_shared(x_t) + sum_{j < k, kept} w_tj * FFN_{idx_tj}(x_t)
  * computed token by token.  The residual connection is the caller's: y
@@ -348,10 +378,10 @@ int oracle_swiglu_rows(int64_t n, int64_t D, int64_t F, const float *x,
  * sel_bias) and the scores exclude it.
  * Output arrays: s_out[T][E], idx[T][k], w[T][k], dropped[T][k], counts[E],
  * kept[E], aux[1], y[T][D]. */
-int oracle_moe_forward(int64_t T, int64_t D, int64_t E, int64_t F, int64_t k,
+static int moe_forward_core(int64_t T, int64_t D, int64_t E, int64_t F, int64_t k,
                        int64_t S, int mode, double gamma, double alpha,
                        int bias_selection_only,
-                       const float *x, const float *W_r, const float *bias,
+                       const double *x, const float *W_r, const float *bias,
                        const float *Wg, const float *Wu, const float *Wd,
                        const float *Wsg, const float *Wsu, const float *Wsd,
                        const double *s_in, double *s_out, int32_t *idx,
@@ -363,7 +393,7 @@ int oracle_moe_forward(int64_t T, int64_t D, int64_t E, int64_t F, int64_t k,
     if (s_in)
         memcpy(s_out, s_in, sizeof(double) * (size_t)(T * E));
     else
-        oracle_router_logits(T, D, E, x, W_r, bias_selection_only ? NULL : bias, s_out);
+        router_logits_f64(T, D, E, x, W_r, bias_selection_only ? NULL : bias, s_out);
 
     double *P_sum = (double *)malloc(sizeof(double) * (size_t)E);
     if (!P_sum)
@@ -415,4 +445,71 @@ int oracle_moe_forward(int64_t T, int64_t D, int64_t E, int64_t F, int64_t k,
         free(o);
     }
     return err ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
+/* The layer on fp32 inputs (widened exactly to fp64). */
+int oracle_moe_forward(int64_t T, int64_t D, int64_t E, int64_t F, int64_t k,
+                       int64_t S, int mode, double gamma, double alpha,
+                       int bias_selection_only,
+                       const float *x, const float *W_r, const float *bias,
+                       const float *Wg, const float *Wu, const float *Wd,
+                       const float *Wsg, const float *Wsu, const float *Wsd,
+                       const double *s_in, double *s_out, int32_t *idx,
+                       double *w, uint8_t *dropped, int64_t *counts,
+                       int64_t *kept, double *aux, double *y)
+{
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(T * D > 0 ? T * D : 1));
+    if (!xd)
+        return ORACLE_NO_MEMORY;
+    for (int64_t i = 0; i < T * D; ++i)
+        xd[i] = (double)x[i];
+    int rc = moe_forward_core(T, D, E, F, k, S, mode, gamma, alpha, bias_selection_only, xd, W_r,
+                              bias, Wg, Wu, Wd, Wsg, Wsu, Wsd, s_in, s_out, idx, w, dropped,
+                              counts, kept, aux, y);
+    free(xd);
+    return rc;
+}
+
+/* A latent MoE ([MPF] "Where MoE is going": the MoE runs in a compressed
+ * space; inputs are down-projected, the experts applied, the outputs
+ * up-projected back):
+ *   x_lat = x W_in^T      (W_in [L][D_outer]),
+ *   y_lat = the layer above on x_lat (everything at width L),
+ *   y     = y_lat W_out^T (W_out [D_outer][L]).
+ * Arguments as oracle_moe_forward with D = L, plus D_outer, W_in, W_out and
+ * y [T][D_outer]; x [T][D_outer]. */
+int oracle_latent_forward(int64_t T, int64_t D_outer, int64_t L, int64_t E, int64_t F,
+                          int64_t k, int64_t S, int mode, double gamma, double alpha,
+                          int bias_selection_only, const float *x, const float *W_in,
+                          const float *W_out, const float *W_r, const float *bias,
+                          const float *Wg, const float *Wu, const float *Wd,
+                          const float *Wsg, const float *Wsu, const float *Wsd,
+                          const double *s_in, double *s_out, int32_t *idx, double *w,
+                          uint8_t *dropped, int64_t *counts, int64_t *kept, double *aux,
+                          double *y)
+{
+    if (T < 0 || D_outer < 1 || L < 1)
+        return ORACLE_BAD_ARG;
+    const size_t nT = (size_t)(T > 0 ? T : 1);
+    double *xd = (double *)malloc(sizeof(double) * nT * (size_t)D_outer);
+    double *xl = (double *)malloc(sizeof(double) * nT * (size_t)L);
+    double *yl = (double *)malloc(sizeof(double) * nT * (size_t)L);
+    if (!xd || !xl || !yl) {
+        free(xd);
+        free(xl);
+        free(yl);
+        return ORACLE_NO_MEMORY;
+    }
+    for (int64_t i = 0; i < T * D_outer; ++i)
+        xd[i] = (double)x[i];
+    oracle_linear(T, D_outer, L, xd, W_in, xl);
+    int rc = moe_forward_core(T, L, E, F, k, S, mode, gamma, alpha, bias_selection_only, xl, W_r,
+                              bias, Wg, Wu, Wd, Wsg, Wsu, Wsd, s_in, s_out, idx, w, dropped,
+                              counts, kept, aux, yl);
+    if (rc == ORACLE_OK)
+        oracle_linear(T, L, D_outer, yl, W_out, y);
+    free(xd);
+    free(xl);
+    free(yl);
+    return rc;
 }

@@ -444,3 +444,48 @@ def test_layer_with_selection_bias_against_bruteforce(mode):
     # the scores exclude the bias
     np.testing.assert_allclose(out["s"], x.astype(np.float64) @ Wr.astype(np.float64).T,
                                rtol=1e-12, atol=1e-12)
+
+
+# --- latent MoE ([MPF] "Where MoE is going": inputs down-projected, the
+# experts applied in the compressed space, outputs up-projected back) -------
+
+def test_linear_against_matmul():
+    rng = np.random.default_rng(91)
+    x = rng.standard_normal((7, 13))
+    W = rng.standard_normal((5, 13)).astype(np.float32)
+    np.testing.assert_allclose(oracle.linear(x, W), x @ W.astype(np.float64).T,
+                               rtol=1e-13, atol=1e-13)
+
+
+def test_latent_with_identity_projections_is_the_plain_layer():
+    rng = np.random.default_rng(92)
+    x, Wr, Wg, Wu, Wd, sh = _rand_layer(rng, 30, 8, 5, 6, 4)
+    eye = np.eye(8, dtype=np.float32)
+    plain = oracle.moe_forward(x, Wr, Wg, Wu, Wd, k=2, mode=2, gamma=0.7, alpha=0.01, **sh)
+    lat = oracle.latent_forward(x, eye, eye, Wr, Wg, Wu, Wd, k=2, mode=2, gamma=0.7,
+                                alpha=0.01, **sh)
+    for key in ("idx", "dropped", "counts", "kept"):
+        np.testing.assert_array_equal(lat[key], plain[key])
+    np.testing.assert_allclose(lat["y"], plain["y"], rtol=1e-13, atol=1e-13)
+    assert abs(lat["aux"] - plain["aux"]) < 1e-15
+
+
+@pytest.mark.parametrize("mode,sel", [(0, False), (3, True)])
+def test_latent_against_dense_bruteforce(mode, sel):
+    """x_lat = x W_in^T, the brute-force layer at width L, then y_lat W_out^T."""
+    rng = np.random.default_rng(93 + mode)
+    T, Do, L, E, F, k = 20, 12, 6, 5, 4, 2
+    x = rng.standard_normal((T, Do)).astype(np.float32)
+    W_in = (rng.standard_normal((L, Do)) / math.sqrt(Do)).astype(np.float32)
+    W_out = (rng.standard_normal((Do, L)) / math.sqrt(L)).astype(np.float32)
+    _, Wr, Wg, Wu, Wd, sh = _rand_layer(rng, 1, L, E, F, 3)
+    b = (rng.standard_normal(E) * 0.5).astype(np.float32) if sel else None
+    out = oracle.latent_forward(x, W_in, W_out, Wr, Wg, Wu, Wd, k=k, mode=mode, gamma=0.9,
+                                alpha=0.01, bias=b, bias_selection_only=sel, **sh)
+    x_lat = x.astype(np.float64) @ W_in.astype(np.float64).T
+    ref = _numpy_layer(x_lat, Wr, Wg, Wu, Wd, k, mode, 0.9, sh, sel_bias=b)
+    np.testing.assert_array_equal(out["idx"], ref["idx"])
+    np.testing.assert_array_equal(out["dropped"], ref["dropped"])
+    np.testing.assert_allclose(out["y"], ref["y"] @ W_out.astype(np.float64).T,
+                               rtol=1e-10, atol=1e-10)
+    assert abs(out["aux"] - ref["aux"]) < 1e-12
