@@ -255,7 +255,8 @@ def oracle_rate(w, inputs, budget_s=12.0, min_tokens=16):
 
 # ------------------------------------------------------------------ arms
 def workload_config(w, l2_note):
-    return {"workload": w.name, "T": w.T, "d_model": w.D, "n_experts": w.E, "d_expert": w.F,
+    extra = {"latent_from_d_model": w.D_outer} if w.D_outer else {}
+    return {**extra, "workload": w.name, "T": w.T, "d_model": w.D, "n_experts": w.E, "d_expert": w.F,
             "top_k": w.k, "d_shared": w.S, "gating": GATING[w.mode],
             "capacity_factor": w.gamma if w.gamma > 0 else None,
             "router_bias": w.bias + (" (selection only)" if w.sel_bias else ""),
@@ -267,7 +268,7 @@ def run_ours(args, rank, world, device):
     torch.cuda.set_device(device)
     cfg = B.config_of(w)
     inputs = make_inputs(w, args.seed + rank, device)
-    outs = B.alloc_outputs(cfg, device)
+    outs = B.alloc_outputs(cfg, device, w.D_outer)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
@@ -404,6 +405,12 @@ def run_ours(args, rank, world, device):
     # whole-layer roofline (slower of algorithmic FLOPs at TC peak and bytes at HBM)
     lf = RL.layer_flops(w.T, w.D, w.E, w.F, w.S, kept_total)
     lb = RL.layer_bytes(w.T, w.D, w.E, w.F, w.S, touched, 2 if w.dtype == "bf16" else 4)
+    if w.D_outer:
+        # the latent layer's two projections: 2*T*D_outer*D FLOPs and D_outer*D
+        # weights each; x and y at the outer width instead of the latent one
+        esz = 2 if w.dtype == "bf16" else 4
+        lf += 4 * w.T * w.D_outer * w.D
+        lb += esz * (2 * w.D_outer * w.D + 2 * w.T * (w.D_outer - w.D))
     lt, lbound = RL.roofline_time_s(lf, lb, tc_peak, peaks["hbm"])
     layer = {"bound": lbound, "roofline_ms": lt * 1e3, "frac": lt * 1e3 / ms_per_step,
              "flops": lf, "bytes": lb, "hbm_frac_of_8TBs": lb / (ms_per_step / 1e3) / 8e12}
@@ -438,7 +445,8 @@ def run_ours(args, rank, world, device):
 
     # router (unless fused into dispatch), dispatch, GEMM1, GEMM2 (+ two
     # shared-expert GEMMs), combine (unless GEMM2 writes y)
-    launches_per_step = (0 if B.router_is_fused(cfg) else 1) + 3 + (2 if w.S else 0) + \
+    launches_per_step = (2 if w.D_outer else 0) + \
+        (0 if B.router_is_fused(cfg) else 1) + 3 + (2 if w.S else 0) + \
         (0 if B.direct_y(cfg) else 1)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,

@@ -159,6 +159,36 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
                        float *aux_loss, void *workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* Workspace bytes moe_latent_forward needs for `cfg` (whose d_model is the
+ * latent width L) and outer width d_outer; MOE_ERR_UNSUPPORTED when d_outer
+ * is not a multiple of 64 for bf16. */
+MOE_API moe_status moe_latent_workspace_size(const moe_config *cfg, int32_t d_outer,
+                                             size_t *bytes);
+
+/* A latent MoE ("Mixture of Experts: More Parameters, Same FLOPs", 'Where MoE
+ * is going': the experts operate in a compressed space; inputs are
+ * down-projected, e.g. 4096 -> 1024, the experts applied, and the outputs
+ * up-projected back):
+ *   x_lat = x W_in^T,  y_lat = the layer of moe_forward on x_lat,
+ *   y     = y_lat W_out^T.
+ * cfg describes the layer at the latent width (cfg->d_model = L); the router,
+ * experts and shared expert all work at width L.
+ *   x     [T, d_outer]; W_in [L, d_outer]; W_out [d_outer, L]  (dtype, K-major)
+ *   y     [T, d_outer]
+ * The other arguments, outputs and conventions are those of moe_forward
+ * (router_logits are the latent router's scores).  workspace >=
+ * moe_latent_workspace_size(cfg, d_outer); x_lat and y_lat live in it. */
+MOE_API moe_status moe_latent_forward(const moe_config *cfg, int32_t d_outer,
+                       const void *x, const void *W_in, const void *W_out,
+                       const void *W_r, const float *router_bias,
+                       const void *W_gate, const void *W_up, const void *W_down,
+                       const void *Ws_gate, const void *Ws_up, const void *Ws_down,
+                       void *y, float *router_logits, int32_t *topk_idx,
+                       float *topk_w, uint8_t *dropped_mask,
+                       int32_t *expert_counts, int32_t *kept_counts,
+                       float *aux_loss, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
 /* Size of the library's static device scratch used by moe_forward_no_alloc. */
 #define MOE_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)
 

@@ -71,6 +71,12 @@ def lib():
         L.moe_forward.restype = ctypes.c_int
         L.moe_forward_no_alloc.argtypes = [cfgp] + [vp] * 17 + [vp]
         L.moe_forward_no_alloc.restype = ctypes.c_int
+        L.moe_latent_workspace_size.argtypes = [cfgp, ctypes.c_int32,
+                                                ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_latent_workspace_size.restype = ctypes.c_int
+        L.moe_latent_forward.argtypes = [cfgp, ctypes.c_int32] + [vp] * 20 + [ctypes.c_size_t,
+                                                                              vp]
+        L.moe_latent_forward.restype = ctypes.c_int
         L.moe_read_device_status.argtypes = [cfgp, vp, vp, ctypes.POINTER(ctypes.c_int32)]
         L.moe_read_device_status.restype = ctypes.c_int
         L.moe_set_stage_events.argtypes = [vp, ctypes.c_int]
@@ -182,6 +188,30 @@ def moe_forward_no_alloc(cfg: MoeConfig, x, W_r, router_bias, W_gate, W_up, W_do
         raise MoeError(st, "moe_forward_no_alloc")
 
 
+def latent_workspace_size(cfg: MoeConfig, d_outer: int) -> int:
+    n = ctypes.c_size_t(0)
+    st = lib().moe_latent_workspace_size(ctypes.byref(cfg), int(d_outer), ctypes.byref(n))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_latent_workspace_size")
+    return int(n.value)
+
+
+def moe_latent_forward(cfg: MoeConfig, d_outer, x, W_in, W_out, W_r, router_bias, W_gate,
+                       W_up, W_down, Ws_gate, Ws_up, Ws_down, y, router_logits, topk_idx,
+                       topk_w, dropped_mask, expert_counts, kept_counts, aux_loss, workspace,
+                       workspace_bytes=None, stream=None) -> None:
+    """Same arguments as the C function (cfg at the latent width)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    args = [x, W_in, W_out, W_r, router_bias, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y,
+            router_logits, topk_idx, topk_w, dropped_mask, expert_counts, kept_counts,
+            aux_loss, workspace]
+    st = lib().moe_latent_forward(ctypes.byref(cfg), int(d_outer), *[_ptr(a) for a in args],
+                                  ctypes.c_size_t(int(workspace_bytes)), _stream(stream))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_latent_forward")
+
+
 def read_device_status(cfg: MoeConfig, workspace, stream=None) -> int:
     """Synchronises the stream and returns the device status code."""
     code = ctypes.c_int32(0)
@@ -227,11 +257,12 @@ class StageEvents:
 
 
 # ---------------------------------------------------------------- convenience
-def alloc_outputs(cfg: MoeConfig, device="cuda"):
-    """Output tensors and workspace for one call, allocated with torch."""
-    T, D, E, k = cfg.T, cfg.d_model, cfg.n_experts, cfg.top_k
+def alloc_outputs(cfg: MoeConfig, device="cuda", d_outer: int = 0):
+    """Output tensors and workspace for one call, allocated with torch
+    (d_outer > 0: for moe_latent_forward, y at the outer width)."""
+    T, D, E, k = cfg.T, (d_outer or cfg.d_model), cfg.n_experts, cfg.top_k
     dt = torch.bfloat16 if cfg.dtype == MOE_DTYPE_BF16 else torch.float32
-    ws_bytes = workspace_size(cfg)
+    ws_bytes = latent_workspace_size(cfg, d_outer) if d_outer else workspace_size(cfg)
     return dict(
         y=torch.empty((T, D), dtype=dt, device=device),
         router_logits=torch.empty((T, E), dtype=torch.float32, device=device),
@@ -247,9 +278,20 @@ def alloc_outputs(cfg: MoeConfig, device="cuda"):
 
 def forward(cfg: MoeConfig, inputs: dict, outs: dict | None = None, stream=None) -> dict:
     """Runs the layer on `inputs` (keys as workloads.make_inputs returns) and
-    returns the output dict (allocated if not given)."""
+    returns the output dict (allocated if not given).  Inputs with W_in and
+    W_out run the latent layer (moe_latent_forward)."""
+    d_outer = int(inputs["x"].shape[1]) if inputs.get("W_in") is not None else 0
     if outs is None:
-        outs = alloc_outputs(cfg, inputs["x"].device)
+        outs = alloc_outputs(cfg, inputs["x"].device, d_outer)
+    if d_outer:
+        moe_latent_forward(cfg, d_outer, inputs["x"], inputs["W_in"], inputs["W_out"],
+                           inputs["W_r"], inputs.get("b_r"), inputs["W_gate"], inputs["W_up"],
+                           inputs["W_down"], inputs.get("Ws_gate"), inputs.get("Ws_up"),
+                           inputs.get("Ws_down"), outs["y"], outs["router_logits"],
+                           outs["topk_idx"], outs["topk_w"], outs["dropped_mask"],
+                           outs["expert_counts"], outs["kept_counts"], outs["aux_loss"],
+                           outs["workspace"], stream=stream)
+        return outs
     moe_forward(cfg, inputs["x"], inputs["W_r"], inputs.get("b_r"), inputs["W_gate"],
                 inputs["W_up"], inputs["W_down"], inputs.get("Ws_gate"), inputs.get("Ws_up"),
                 inputs.get("Ws_down"), outs["y"], outs["router_logits"], outs["topk_idx"],

@@ -167,46 +167,26 @@ int64_t moe_capacity(const moe_config *cfg)
     return capacity_of(cfg);
 }
 
-moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r,
-                       const float *router_bias, const void *W_gate, const void *W_up,
-                       const void *W_down, const void *Ws_gate, const void *Ws_up,
-                       const void *Ws_down, void *y, float *router_logits, int32_t *topk_idx,
-                       float *topk_w, uint8_t *dropped_mask, int32_t *expert_counts,
-                       int32_t *kept_counts, float *aux_loss, void *workspace,
-                       size_t workspace_bytes, cudaStream_t stream)
+}  // extern "C"
+
+namespace moe {
+
+// The layer on a validated config and workspace.  clear_status: zero the
+// status word and counters first (otherwise the caller already has, on the
+// same stream, and an earlier kernel's error is kept).
+moe_status forward_body(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                        const void *x, const void *W_r, const float *router_bias,
+                        const void *W_gate, const void *W_up, const void *W_down,
+                        const void *Ws_gate, const void *Ws_up, const void *Ws_down, void *y,
+                        float *router_logits, int32_t *topk_idx, float *topk_w,
+                        uint8_t *dropped_mask, int32_t *expert_counts, int32_t *kept_counts,
+                        float *aux_loss, bool clear_status, cudaStream_t stream)
 {
-    moe_status st = validate_config(cfg);
-    if (st != MOE_OK)
-        return st;
-    const moe_config &c = *cfg;
-    if (!expert_counts || !kept_counts || !aux_loss)
-        return MOE_ERR_INVALID_ARG;
-    // with T == 0 nothing per token or per weight is touched (empty tensors
-    // may have null data pointers)
-    if (c.T > 0) {
-        if (!x || !W_r || !W_gate || !W_up || !W_down || !y || !router_logits || !topk_idx ||
-            !topk_w || !dropped_mask)
-            return MOE_ERR_INVALID_ARG;
-        if (c.d_shared > 0 && (!Ws_gate || !Ws_up || !Ws_down))
-            return MOE_ERR_INVALID_ARG;
-    }
-    const WorkspaceLayout L = layout_of(cfg);
-    if (!workspace || workspace_bytes < L.total ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return MOE_ERR_WORKSPACE;
-    if (c.dtype == MOE_DTYPE_BF16) {
-        // tensor-map bases and 16-byte vector accesses
-        if (!aligned16(x) || !aligned16(W_r) || !aligned16(W_gate) || !aligned16(W_up) ||
-            !aligned16(W_down) || !aligned16(y) ||
-            (c.d_shared > 0 && (!aligned16(Ws_gate) || !aligned16(Ws_up) || !aligned16(Ws_down))))
-            return MOE_ERR_INVALID_ARG;
-    }
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
     const int E = c.n_experts;
 
     auto cuda_ok = [](cudaError_t e) { return e == cudaSuccess; };
-    if (!cuda_ok(cudaMemsetAsync(status, 0, 64, stream)))
+    if (clear_status && !cuda_ok(cudaMemsetAsync(status, 0, 64, stream)))
         return MOE_ERR_CUDA;
     if (c.T == 0) {
         if (!cuda_ok(cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, stream)) ||
@@ -267,6 +247,143 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r,
     if (!cuda_ok(record_stage(ev, 7, stream)))
         return MOE_ERR_CUDA;
     return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" {
+
+moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r,
+                       const float *router_bias, const void *W_gate, const void *W_up,
+                       const void *W_down, const void *Ws_gate, const void *Ws_up,
+                       const void *Ws_down, void *y, float *router_logits, int32_t *topk_idx,
+                       float *topk_w, uint8_t *dropped_mask, int32_t *expert_counts,
+                       int32_t *kept_counts, float *aux_loss, void *workspace,
+                       size_t workspace_bytes, cudaStream_t stream)
+{
+    moe_status st = validate_config(cfg);
+    if (st != MOE_OK)
+        return st;
+    const moe_config &c = *cfg;
+    if (!expert_counts || !kept_counts || !aux_loss)
+        return MOE_ERR_INVALID_ARG;
+    // with T == 0 nothing per token or per weight is touched (empty tensors
+    // may have null data pointers)
+    if (c.T > 0) {
+        if (!x || !W_r || !W_gate || !W_up || !W_down || !y || !router_logits || !topk_idx ||
+            !topk_w || !dropped_mask)
+            return MOE_ERR_INVALID_ARG;
+        if (c.d_shared > 0 && (!Ws_gate || !Ws_up || !Ws_down))
+            return MOE_ERR_INVALID_ARG;
+    }
+    const WorkspaceLayout L = layout_of(cfg);
+    if (!workspace || workspace_bytes < L.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MOE_ERR_WORKSPACE;
+    if (c.dtype == MOE_DTYPE_BF16) {
+        // tensor-map bases and 16-byte vector accesses
+        if (!aligned16(x) || !aligned16(W_r) || !aligned16(W_gate) || !aligned16(W_up) ||
+            !aligned16(W_down) || !aligned16(y) ||
+            (c.d_shared > 0 && (!aligned16(Ws_gate) || !aligned16(Ws_up) || !aligned16(Ws_down))))
+            return MOE_ERR_INVALID_ARG;
+    }
+    return forward_body(c, L, static_cast<uint8_t *>(workspace), x, W_r, router_bias, W_gate,
+                        W_up, W_down, Ws_gate, Ws_up, Ws_down, y, router_logits, topk_idx,
+                        topk_w, dropped_mask, expert_counts, kept_counts, aux_loss, true,
+                        stream);
+}
+
+// Latent layout: the layer's own workspace, then x_lat [T][L] and y_lat [T][L].
+static bool latent_layout(const moe_config *cfg, int32_t d_outer, size_t *x_lat, size_t *y_lat,
+                          size_t *total)
+{
+    if (validate_config(cfg) != MOE_OK || d_outer < 1)
+        return false;
+    if (cfg->dtype == MOE_DTYPE_BF16 && d_outer % 64)
+        return false;
+    const size_t esz = cfg->dtype == MOE_DTYPE_BF16 ? 2 : 4;
+    const size_t lat = esz * (size_t)cfg->T * (size_t)cfg->d_model;
+    *x_lat = align_up(layout_of(cfg).total, 1024);
+    *y_lat = align_up(*x_lat + lat, 1024);
+    *total = align_up(*y_lat + lat, 1024);
+    return true;
+}
+
+moe_status moe_latent_workspace_size(const moe_config *cfg, int32_t d_outer, size_t *bytes)
+{
+    if (!bytes)
+        return MOE_ERR_INVALID_ARG;
+    const moe_status st = validate_config(cfg);
+    if (st != MOE_OK)
+        return st;
+    size_t xo, yo, total;
+    if (!latent_layout(cfg, d_outer, &xo, &yo, &total))
+        return d_outer < 1 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
+    *bytes = total;
+    return MOE_OK;
+}
+
+moe_status moe_latent_forward(const moe_config *cfg, int32_t d_outer, const void *x,
+                              const void *W_in, const void *W_out, const void *W_r,
+                              const float *router_bias, const void *W_gate, const void *W_up,
+                              const void *W_down, const void *Ws_gate, const void *Ws_up,
+                              const void *Ws_down, void *y, float *router_logits,
+                              int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
+                              int32_t *expert_counts, int32_t *kept_counts, float *aux_loss,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    moe_status st = validate_config(cfg);
+    if (st != MOE_OK)
+        return st;
+    const moe_config &c = *cfg;
+    size_t xo, yo, total;
+    if (!latent_layout(cfg, d_outer, &xo, &yo, &total))
+        return d_outer < 1 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
+    if (!expert_counts || !kept_counts || !aux_loss)
+        return MOE_ERR_INVALID_ARG;
+    if (c.T > 0) {
+        if (!x || !W_in || !W_out || !W_r || !W_gate || !W_up || !W_down || !y ||
+            !router_logits || !topk_idx || !topk_w || !dropped_mask)
+            return MOE_ERR_INVALID_ARG;
+        if (c.d_shared > 0 && (!Ws_gate || !Ws_up || !Ws_down))
+            return MOE_ERR_INVALID_ARG;
+    }
+    if (!workspace || workspace_bytes < total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MOE_ERR_WORKSPACE;
+    if (c.dtype == MOE_DTYPE_BF16) {
+        if (!aligned16(x) || !aligned16(W_in) || !aligned16(W_out) || !aligned16(W_r) ||
+            !aligned16(W_gate) || !aligned16(W_up) || !aligned16(W_down) || !aligned16(y) ||
+            (c.d_shared > 0 && (!aligned16(Ws_gate) || !aligned16(Ws_up) || !aligned16(Ws_down))))
+            return MOE_ERR_INVALID_ARG;
+    }
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const WorkspaceLayout L = layout_of(cfg);
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    if (cudaMemsetAsync(status, 0, 64, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    void *x_lat = ws + xo, *y_lat = ws + yo;
+    const int T = c.T, Ld = c.d_model;
+    // x_lat = x W_in^T
+    cudaError_t err = c.dtype == MOE_DTYPE_BF16
+                          ? launch_dense_tc(T, Ld, d_outer, x, W_in, x_lat, status, stream)
+                          : launch_dense_simt(T, Ld, d_outer, static_cast<const float *>(x),
+                                              static_cast<const float *>(W_in),
+                                              static_cast<float *>(x_lat), status, stream);
+    if (err != cudaSuccess)
+        return MOE_ERR_CUDA;
+    // the layer at the latent width
+    st = forward_body(c, L, ws, x_lat, W_r, router_bias, W_gate, W_up, W_down, Ws_gate, Ws_up,
+                      Ws_down, y_lat, router_logits, topk_idx, topk_w, dropped_mask,
+                      expert_counts, kept_counts, aux_loss, false, stream);
+    if (st != MOE_OK || T == 0)
+        return st;
+    // y = y_lat W_out^T
+    err = c.dtype == MOE_DTYPE_BF16
+              ? launch_dense_tc(T, d_outer, Ld, y_lat, W_out, y, status, stream)
+              : launch_dense_simt(T, d_outer, Ld, static_cast<const float *>(y_lat),
+                                  static_cast<const float *>(W_out), static_cast<float *>(y),
+                                  status, stream);
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status moe_read_device_status(const moe_config *cfg, const void *workspace,

@@ -119,4 +119,16 @@ cudaError_t launch_experts_simt(const moe_config &c, const WorkspaceLayout &L, u
     return cudaGetLastError();
 }
 
+cudaError_t launch_dense_simt(int rows, int N, int K, const float *A, const float *B, float *out,
+                              const int32_t *status, cudaStream_t stream)
+{
+    if (rows <= 0)
+        return cudaSuccess;
+    AuxArgs none{};
+    const dim3 block(32, 8);
+    return launch_pdl(simt_seg_gemm_f32_kernel<false>, dim3((N + 31) / 32, (rows + 7) / 8), block,
+                      0, stream, A, B, (const float *)nullptr, 0LL, N, K,
+                      (const int32_t *)nullptr, 1, rows, out, status, none);
+}
+
 }  // namespace moe

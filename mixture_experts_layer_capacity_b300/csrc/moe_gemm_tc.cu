@@ -1091,4 +1091,37 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
     return cudaSuccess;
 }
 
+cudaError_t launch_dense_tc(int rows, int N, int K, const void *A, const void *B, void *out,
+                            int32_t *status, cudaStream_t stream)
+{
+    if (rows <= 0)
+        return cudaSuccess;
+    // few rows: 32-column tiles so that enough CTAs stream the weights;
+    // many rows: CTA pairs with 256-row tiles
+    const bool narrow = rows <= 2 * kTileM;
+    const bool pair = rows >= kPairMinRows / 4;
+    const int bn = narrow ? 32 : (N > 1024 ? 256 : 128);
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, A, (uint64_t)rows, (uint64_t)K, kTileM) ||
+        !make_map(&mB, B, (uint64_t)N, (uint64_t)K, (uint32_t)(pair ? bn / 2 : bn)))
+        return cudaErrorInvalidValue;
+    TcParams p{};
+    p.nseg = 1;
+    p.dense_rows = rows;
+    p.K = K;
+    p.n_tiles = (N + bn - 1) / bn;
+    p.N_valid = N;
+    p.out = out;
+    p.ld_out = N;
+    p.status = status;
+    const long long mt = (rows + kTileM - 1) / kTileM, mt2 = (rows + kPairRows - 1) / kPairRows;
+    if (pair)
+        return bn == 256 ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, mt2 * p.n_tiles, stream)
+                         : launch_tc_pair<128, 1, EPI_BF16, 8>(mA, mB, mB, p, mt2 * p.n_tiles, stream);
+    if (narrow)
+        return launch_tc<32, 1, EPI_BF16, 8>(mA, mB, mB, p, mt * p.n_tiles, stream);
+    return bn == 256 ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt * p.n_tiles, stream)
+                     : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt * p.n_tiles, stream);
+}
+
 }  // namespace moe

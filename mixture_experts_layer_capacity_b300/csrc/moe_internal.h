@@ -133,6 +133,23 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
                               const void *Ws_down, void *y, const AuxArgs &aux,
                               cudaStream_t stream, cudaEvent_t *ev = nullptr);
 
+// Dense GEMM out[rows][N] = A[rows][K] . B[N][K]^T (the latent MoE's
+// projections): bf16 on the tensor cores, fp32 on CUDA cores.  Kernels
+// check the status word and do nothing after an earlier failure.
+cudaError_t launch_dense_tc(int rows, int N, int K, const void *A, const void *B, void *out,
+                            int32_t *status, cudaStream_t stream);
+cudaError_t launch_dense_simt(int rows, int N, int K, const float *A, const float *B, float *out,
+                              const int32_t *status, cudaStream_t stream);
+
+// The layer on a validated config and workspace (moe_api.cu).
+moe_status forward_body(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                        const void *x, const void *W_r, const float *router_bias,
+                        const void *W_gate, const void *W_up, const void *W_down,
+                        const void *Ws_gate, const void *Ws_up, const void *Ws_down, void *y,
+                        float *router_logits, int32_t *topk_idx, float *topk_w,
+                        uint8_t *dropped_mask, int32_t *expert_counts, int32_t *kept_counts,
+                        float *aux_loss, bool clear_status, cudaStream_t stream);
+
 int sm_count();
 
 // Launches `kern` on `stream` with programmatic stream serialization, so

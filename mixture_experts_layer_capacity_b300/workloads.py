@@ -6,12 +6,15 @@ CPU oracle) both take their inputs from here.
 
 Recipe: one ``torch.Generator`` per tensor on the target device, seeded
 ``seed * 100 + tensor_id`` with ids x=0, W_r=1, b_r=2, W_gate=3, W_up=4,
-W_down=5, Ws_gate=6, Ws_up=7, Ws_down=8.  Each draw is fp32 N(0, 1), scaled by
+W_down=5, Ws_gate=6, Ws_up=7, Ws_down=8, W_in=9, W_out=10.  Each draw is fp32 N(0, 1), scaled by
 the standard deviation and cast to the workload dtype.  Stacked expert weights
 are drawn one expert at a time from that tensor's generator (so the fp32
 temporary stays one expert large).  x ~ N(0, 1); every weight ~ N(0, 1/d_in)
 where d_in is the reduction dimension (D for W_r, W_gate, W_up, Ws_gate,
-Ws_up; F for W_down; S for Ws_down).
+Ws_up; F for W_down; S for Ws_down; D_outer for W_in; D for W_out).
+
+A latent workload (D_outer > 0) runs the layer at width D on x W_in^T, with
+x [T, D_outer], W_in [D, D_outer] and W_out [D_outer, D].
 
 Weight layout (reduction dimension contiguous, "K-major"):
   W_r [E, D]; W_gate, W_up [E, F, D]; W_down [E, D, F];
@@ -45,6 +48,7 @@ class Workload:
     alpha: float = 0.01   # balance-loss coefficient
     bias: str = "none"    # router logit bias: "none", "normal_var2", "zipf1.1"
     sel_bias: bool = False  # the bias shifts only the top-k selection keys
+    D_outer: int = 0      # latent MoE: outer width (x and y); 0 = plain layer
     description: str = ""
 
     def with_T(self, T: int) -> "Workload":
@@ -88,6 +92,16 @@ WORKLOADS = {
         "dsv3_decode", T=64, D=7168, E=256, F=2048, k=8, S=2048,
         mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1",
         description="DeepSeek-V3-shaped, renormalised top-8, Zipf-skewed bias, T=64"),
+    # latent MoE with the page's widths (4096 down to 1024 and back); the
+    # expert count, width and k are this build's choice (not on the pages)
+    "latent_prefill": Workload(
+        "latent_prefill", T=4096, D=1024, E=64, F=2048, k=8, D_outer=4096,
+        mode=GATING_SOFTMAX_ALL_RENORM,
+        description="latent MoE: 4096 -> 1024, 64 experts d=2048, top-8, -> 4096, T=4096"),
+    "latent_decode": Workload(
+        "latent_decode", T=64, D=1024, E=64, F=2048, k=8, D_outer=4096,
+        mode=GATING_SOFTMAX_ALL_RENORM,
+        description="latent MoE: 4096 -> 1024, 64 experts d=2048, top-8, -> 4096, T=64"),
     "dsv3_sigmoid_decode": Workload(
         "dsv3_sigmoid_decode", T=64, D=7168, E=256, F=2048, k=8, S=2048,
         mode=GATING_SIGMOID_SELECTED, bias="zipf1.1", sel_bias=True,
@@ -96,7 +110,7 @@ WORKLOADS = {
 }
 
 _TID = {"x": 0, "W_r": 1, "b_r": 2, "W_gate": 3, "W_up": 4, "W_down": 5,
-        "Ws_gate": 6, "Ws_up": 7, "Ws_down": 8}
+        "Ws_gate": 6, "Ws_up": 7, "Ws_down": 8, "W_in": 9, "W_out": 10}
 
 
 def _gen(device, seed, name):
@@ -128,7 +142,12 @@ def make_inputs(w: Workload, seed: int = 0, device="cuda", weights: bool = True)
     dt = w.torch_dtype
     dev = torch.device(device)
     out = {}
-    out["x"] = _normal((w.T, w.D), 1.0, _gen(dev, seed, "x"), dev, dt)
+    out["x"] = _normal((w.T, w.D_outer or w.D), 1.0, _gen(dev, seed, "x"), dev, dt)
+    if w.D_outer:
+        out["W_in"] = _normal((w.D, w.D_outer), 1.0 / math.sqrt(w.D_outer),
+                              _gen(dev, seed, "W_in"), dev, dt)
+        out["W_out"] = _normal((w.D_outer, w.D), 1.0 / math.sqrt(w.D),
+                               _gen(dev, seed, "W_out"), dev, dt)
     out["W_r"] = _normal((w.E, w.D), 1.0 / math.sqrt(w.D), _gen(dev, seed, "W_r"), dev, dt)
     if w.bias == "normal_var2":
         out["b_r"] = _normal((w.E,), math.sqrt(2.0), _gen(dev, seed, "b_r"), dev,

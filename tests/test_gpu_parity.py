@@ -61,6 +61,25 @@ GATING = [
 ]
 
 
+# Latent MoE: name, T, L (layer width), E, F, k, S, D_outer, mode, gamma, dtype
+LATENT = [
+    ("latent_small_bf16", 600, 128, 8, 128, 2, 64, 256, 0, 0.0, "bf16"),
+    ("latent_decode_narrow_bf16", 64, 256, 16, 128, 4, 128, 512, 2, 0.0, "bf16"),
+    ("latent_capacity_fp32", 200, 64, 4, 64, 2, 32, 96, 1, 0.75, "fp32"),
+]
+
+
+@pytest.mark.parametrize("case", LATENT, ids=[c[0] for c in LATENT])
+def test_latent_layers(case):
+    name, T, L, E, F, k, S, Do, mode, gamma, dtype = case
+    w = Workload(name, T=T, D=L, E=E, F=F, k=k, S=S, mode=mode, gamma=gamma, dtype=dtype,
+                 alpha=0.01, D_outer=Do)
+    _, inp, outs, code = parity.run(w, seed=14)
+    assert code == B.MOE_DEVICE_OK
+    assert tuple(outs["y"].shape) == (T, Do)
+    print(name, parity.check(w, inp, outs))
+
+
 @pytest.mark.parametrize("case", GATING, ids=[c[0] for c in GATING])
 def test_gating_variants(case):
     name, T, D, E, F, k, S, mode, gamma, bias, sel, dtype = case
@@ -127,8 +146,8 @@ def test_switch_capacity_workload_every_token():
 
 
 @pytest.mark.parametrize("name", ["mixtral_decode", "qwen2_57b_decode", "dsv3_decode",
-                                  "dsv3_sigmoid_decode", "mixtral_prefill",
-                                  "qwen2_57b_prefill", "dsv3_prefill"])
+                                  "dsv3_sigmoid_decode", "latent_decode", "latent_prefill",
+                                  "mixtral_prefill", "qwen2_57b_prefill", "dsv3_prefill"])
 def test_benchmark_sized_workloads_sampled(name):
     w = WORKLOADS[name]
     _, inp, outs, code = parity.run(w)
