@@ -108,6 +108,8 @@ typedef struct {
 #define MOE_DEVICE_NONFINITE_SCORE 1   /* a router score was NaN/Inf */
 #define MOE_DEVICE_PIPELINE_TIMEOUT 2  /* a bounded in-kernel wait ran out */
 #define MOE_DEVICE_LAUNCH_MISMATCH 3   /* a kernel got less shared memory than its layout needs */
+#define MOE_DEVICE_SHARD_MISMATCH 4    /* split batch: the exchanged counts do not hold
+                                          this rank's own or do not add up to T_global*k */
 
 /* Bytes of scratch moe_forward needs for `cfg` (x gathered by expert, the
  * SwiGLU hidden rows, per-expert scan tables, ...).  Returns
@@ -186,6 +188,61 @@ MOE_API moe_status moe_latent_forward(const moe_config *cfg, int32_t d_outer,
                        void *y, float *router_logits, int32_t *topk_idx,
                        float *topk_w, uint8_t *dropped_mask,
                        int32_t *expert_counts, int32_t *kept_counts,
+                       float *aux_loss, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* ---- One batch split over several ranks (data parallel), same results as
+ * one moe_forward over the whole batch.
+ *
+ * The layer's tokens are independent except for two couplings: capacity is
+ * applied in token order over the WHOLE batch ("Mixture of Experts" (module
+ * 17), 17.5: C = ceil(capacity_factor * T * k / E) with T the batch, tokens
+ * past C dropped), and the balance loss uses f_e and P_e over the whole batch
+ * (17.4 equation).  Rank r holds tokens [start_r, start_r + T_r) of the batch,
+ * ranks in token order, sum of T_r = T_global.  Per rank:
+ *   1. moe_sharded_route: gating of the rank's tokens; writes its per-expert
+ *      demand counts and probability sums;
+ *   2. the caller exchanges them (an all-gather in rank order) into
+ *      all_expert_counts [n_ranks][E] and all_prob_sums [n_ranks][E];
+ *   3. moe_sharded_finish: an assignment's global position is the count of
+ *      earlier ranks' assignments to its expert plus its position here; it is
+ *      kept iff that is below C (T = T_global); then the experts, combine and
+ *      the balance loss over all ranks (probability sums added in rank order).
+ * cfg->T is this rank's token count T_r (0 allowed); T_global >= cfg->T.
+ * Both calls take the same workspace (>= moe_sharded_workspace_size bytes),
+ * whose contents must survive between them, on streams ordered route ->
+ * finish.  The outputs match moe_forward's for the rank's tokens, except
+ * that expert_counts (from the route call) are this rank's demand counts
+ * while kept_counts are this rank's kept assignments, and aux_loss is the
+ * loss of the whole batch (the same on every rank). */
+MOE_API moe_status moe_sharded_workspace_size(const moe_config *cfg, int64_t T_global,
+                                              size_t *bytes);
+
+/* Step 1.  x, W_r, router_bias, router_logits, topk_idx, topk_w as for
+ * moe_forward (this rank's T rows).  Outputs: expert_counts [E] int32 and
+ * prob_sums [E] fp64 (sum over this rank's tokens of the router
+ * probabilities, for the balance loss).  When T == 0 they are zeroed and
+ * nothing else is touched. */
+MOE_API moe_status moe_sharded_route(const moe_config *cfg, int64_t T_global,
+                       const void *x, const void *W_r, const float *router_bias,
+                       float *router_logits, int32_t *topk_idx, float *topk_w,
+                       int32_t *expert_counts, double *prob_sums,
+                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Step 3.  all_expert_counts [n_ranks][E] int32 and all_prob_sums
+ * [n_ranks][E] fp64 (device, rank order, row `rank` = this rank's step-1
+ * outputs); topk_idx and topk_w are step 1's outputs (read only).  Writes y,
+ * dropped_mask, kept_counts and aux_loss as moe_forward does.  A device check
+ * that row `rank` equals this rank's counts and that all counts add up to
+ * T_global * k sets MOE_DEVICE_SHARD_MISMATCH otherwise (later kernels then
+ * skip their work).  0 <= rank < n_ranks. */
+MOE_API moe_status moe_sharded_finish(const moe_config *cfg, int64_t T_global,
+                       int32_t n_ranks, int32_t rank,
+                       const int32_t *all_expert_counts, const double *all_prob_sums,
+                       const void *x, const void *W_gate, const void *W_up,
+                       const void *W_down, const void *Ws_gate, const void *Ws_up,
+                       const void *Ws_down, const int32_t *topk_idx, const float *topk_w,
+                       void *y, uint8_t *dropped_mask, int32_t *kept_counts,
                        float *aux_loss, void *workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 

@@ -30,6 +30,7 @@ MOE_DEVICE_OK = 0
 MOE_DEVICE_NONFINITE_SCORE = 1
 MOE_DEVICE_PIPELINE_TIMEOUT = 2
 MOE_DEVICE_LAUNCH_MISMATCH = 3
+MOE_DEVICE_SHARD_MISMATCH = 4
 
 
 class MoeError(RuntimeError):
@@ -77,6 +78,14 @@ def lib():
         L.moe_latent_forward.argtypes = [cfgp, ctypes.c_int32] + [vp] * 20 + [ctypes.c_size_t,
                                                                               vp]
         L.moe_latent_forward.restype = ctypes.c_int
+        L.moe_sharded_workspace_size.argtypes = [cfgp, ctypes.c_int64,
+                                                 ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_sharded_workspace_size.restype = ctypes.c_int
+        L.moe_sharded_route.argtypes = [cfgp, ctypes.c_int64] + [vp] * 9 + [ctypes.c_size_t, vp]
+        L.moe_sharded_route.restype = ctypes.c_int
+        L.moe_sharded_finish.argtypes = ([cfgp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+                                         + [vp] * 16 + [ctypes.c_size_t, vp])
+        L.moe_sharded_finish.restype = ctypes.c_int
         L.moe_read_device_status.argtypes = [cfgp, vp, vp, ctypes.POINTER(ctypes.c_int32)]
         L.moe_read_device_status.restype = ctypes.c_int
         L.moe_set_stage_events.argtypes = [vp, ctypes.c_int]
@@ -210,6 +219,44 @@ def moe_latent_forward(cfg: MoeConfig, d_outer, x, W_in, W_out, W_r, router_bias
                                   ctypes.c_size_t(int(workspace_bytes)), _stream(stream))
     if st != MOE_OK:
         raise MoeError(st, "moe_latent_forward")
+
+
+def sharded_workspace_size(cfg: MoeConfig, T_global: int) -> int:
+    n = ctypes.c_size_t(0)
+    st = lib().moe_sharded_workspace_size(ctypes.byref(cfg), int(T_global), ctypes.byref(n))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_sharded_workspace_size")
+    return int(n.value)
+
+
+def moe_sharded_route(cfg: MoeConfig, T_global, x, W_r, router_bias, router_logits, topk_idx,
+                      topk_w, expert_counts, prob_sums, workspace, workspace_bytes=None,
+                      stream=None) -> None:
+    """Same arguments as the C function (cfg.T = this rank's tokens)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    args = [x, W_r, router_bias, router_logits, topk_idx, topk_w, expert_counts, prob_sums,
+            workspace]
+    st = lib().moe_sharded_route(ctypes.byref(cfg), int(T_global), *[_ptr(a) for a in args],
+                                 ctypes.c_size_t(int(workspace_bytes)), _stream(stream))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_sharded_route")
+
+
+def moe_sharded_finish(cfg: MoeConfig, T_global, n_ranks, rank, all_expert_counts,
+                       all_prob_sums, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
+                       topk_idx, topk_w, y, dropped_mask, kept_counts, aux_loss, workspace,
+                       workspace_bytes=None, stream=None) -> None:
+    """Same arguments as the C function."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    args = [all_expert_counts, all_prob_sums, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
+            topk_idx, topk_w, y, dropped_mask, kept_counts, aux_loss, workspace]
+    st = lib().moe_sharded_finish(ctypes.byref(cfg), int(T_global), int(n_ranks), int(rank),
+                                  *[_ptr(a) for a in args], ctypes.c_size_t(int(workspace_bytes)),
+                                  _stream(stream))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_sharded_finish")
 
 
 def read_device_status(cfg: MoeConfig, workspace, stream=None) -> int:

@@ -50,15 +50,16 @@ moe_status validate_config(const moe_config *c)
 }
 
 // C = ceil(capacity_factor * T * k / E) in double; -1 when dropless.
-int64_t capacity_of(const moe_config *c)
+int64_t capacity_of(const moe_config *c, int64_t T_cap)
 {
     if (!(c->capacity_factor > 0.0f))
         return -1;
-    return (int64_t)std::ceil((double)c->capacity_factor * (double)((int64_t)c->T * c->top_k) /
+    const int64_t T = T_cap < 0 ? c->T : T_cap;
+    return (int64_t)std::ceil((double)c->capacity_factor * (double)(T * c->top_k) /
                               (double)c->n_experts);
 }
 
-WorkspaceLayout layout_of(const moe_config *c)
+WorkspaceLayout layout_of(const moe_config *c, int64_t T_cap)
 {
     WorkspaceLayout L{};
     const int64_t T = c->T, E = c->n_experts, k = c->top_k;
@@ -66,7 +67,7 @@ WorkspaceLayout layout_of(const moe_config *c)
     const size_t esz = c->dtype == MOE_DTYPE_BF16 ? 2 : 4;
     L.nchunk = (int)std::max<int64_t>(std::min<int64_t>(T, kMaxDispatchBlocks),
                                      (T + kChunk - 1) / kChunk);
-    L.C = capacity_of(c);
+    L.C = capacity_of(c, T_cap);
     const int64_t TK = T * k;
     L.R_max = L.C < 0 ? TK : std::min<int64_t>(TK, E * L.C);
     size_t off = 0;
@@ -80,6 +81,7 @@ WorkspaceLayout layout_of(const moe_config *c)
     L.ppart = take(sizeof(float) * E * L.nchunk);
     L.rank = take(sizeof(int32_t) * TK);
     L.psum = take(sizeof(double) * E);
+    L.gcount = take(sizeof(int32_t) * E);
     L.seg_off = take(sizeof(int32_t) * (E + 1));
     L.mtile = take(sizeof(int32_t) * (E + 1));
     L.row_of = take(sizeof(int32_t) * TK);
@@ -171,6 +173,74 @@ int64_t moe_capacity(const moe_config *cfg)
 
 namespace moe {
 
+namespace {
+
+bool cuda_ok(cudaError_t e) { return e == cudaSuccess; }
+
+// Router scores (small routers run inside the dispatch kernel instead), then
+// the dispatch kernel: gating, demand counts, capacity, segments and the
+// gather of x into expert order -- or, for one rank of a split batch, the
+// part of it that `shard->phases` names.
+moe_status route_step(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws, const void *x,
+                      const void *W_r, const float *router_bias, float *router_logits,
+                      int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
+                      int32_t *expert_counts, int32_t *kept_counts, void *y,
+                      const ShardArgs *shard, cudaEvent_t *ev, cudaStream_t stream)
+{
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    const bool gate = !shard || (shard->phases & 1);
+    const bool fused = gate && router_fused(c) && aligned16(x) && aligned16(W_r);
+    const int lsplit = fused || !gate ? 1 : router_splits(c);
+    float *lpart = lsplit > 1 ? reinterpret_cast<float *>(ws + L.lpart) : nullptr;
+    if (!cuda_ok(record_stage(ev, 0, stream)))
+        return MOE_ERR_CUDA;
+    cudaError_t err = cudaSuccess;
+    if (gate && !fused) {
+        if (c.dtype == MOE_DTYPE_BF16)
+            err = launch_router_tc(c, x, W_r, lsplit > 1 ? lpart : router_logits, lsplit, status,
+                                   stream);
+        else
+            err = launch_router_simt(c, x, W_r, router_logits, stream);
+    }
+    if (!cuda_ok(err) || !cuda_ok(record_stage(ev, 1, stream)))
+        return MOE_ERR_CUDA;
+    if (!cuda_ok(launch_dispatch(c, L, ws, x, W_r, fused, router_logits, lpart, lsplit,
+                                 router_bias, topk_idx, topk_w, dropped_mask, expert_counts,
+                                 kept_counts, y, stream, shard)) ||
+        !cuda_ok(record_stage(ev, 2, stream)))
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+// The experts (routed segments and the shared expert; the first expert
+// kernel also evaluates the balance loss of `aux`) and the weighted combine,
+// unless the down projection already wrote y.
+moe_status expert_step(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws, const void *x,
+                       const void *W_gate, const void *W_up, const void *W_down,
+                       const void *Ws_gate, const void *Ws_up, const void *Ws_down, void *y,
+                       const float *topk_w, const AuxArgs &aux, cudaEvent_t *ev,
+                       cudaStream_t stream)
+{
+    cudaError_t err;
+    if (c.dtype == MOE_DTYPE_BF16)
+        err = launch_experts_tc(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y,
+                                aux, stream, ev);
+    else
+        err = launch_experts_simt(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
+                                  aux, stream, ev);
+    if (!cuda_ok(err))
+        return MOE_ERR_CUDA;
+    if (!(direct_y(c) && c.dtype == MOE_DTYPE_BF16)) {
+        if (!cuda_ok(launch_combine(c, L, ws, topk_w, y, stream)))
+            return MOE_ERR_CUDA;
+    }
+    if (!cuda_ok(record_stage(ev, 7, stream)))
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+}  // namespace
+
 // The layer on a validated config and workspace.  clear_status: zero the
 // status word and counters first (otherwise the caller already has, on the
 // same stream, and an earlier kernel's error is kept).
@@ -184,8 +254,6 @@ moe_status forward_body(const moe_config &c, const WorkspaceLayout &L, uint8_t *
 {
     int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
     const int E = c.n_experts;
-
-    auto cuda_ok = [](cudaError_t e) { return e == cudaSuccess; };
     if (clear_status && !cuda_ok(cudaMemsetAsync(status, 0, 64, stream)))
         return MOE_ERR_CUDA;
     if (c.T == 0) {
@@ -195,33 +263,11 @@ moe_status forward_body(const moe_config &c, const WorkspaceLayout &L, uint8_t *
             return MOE_ERR_CUDA;
         return MOE_OK;
     }
-
     cudaEvent_t *ev = g_stage_events.load();
-    if (!cuda_ok(record_stage(ev, 0, stream)))
-        return MOE_ERR_CUDA;
-    // 1. router scores (small routers run inside the dispatch kernel instead)
-    cudaError_t err = cudaSuccess;
-    const bool fused = router_fused(c) && aligned16(x) && aligned16(W_r);
-    const int lsplit = fused ? 1 : router_splits(c);
-    float *lpart = lsplit > 1 ? reinterpret_cast<float *>(ws + L.lpart) : nullptr;
-    if (!fused) {
-        if (c.dtype == MOE_DTYPE_BF16)
-            err = launch_router_tc(c, x, W_r, lsplit > 1 ? lpart : router_logits, lsplit, status,
-                                   stream);
-        else
-            err = launch_router_simt(c, x, W_r, router_logits, stream);
-    }
-    if (!cuda_ok(err) || !cuda_ok(record_stage(ev, 1, stream)))
-        return MOE_ERR_CUDA;
-    // 2. gating, demand counts, capacity, segments, balance loss, gather of x
-    //    into expert order (one cooperative kernel)
-    if (!cuda_ok(launch_dispatch(c, L, ws, x, W_r, fused, router_logits, lpart, lsplit,
-                                 router_bias, topk_idx, topk_w, dropped_mask, expert_counts,
-                                 kept_counts, y, stream)) ||
-        !cuda_ok(record_stage(ev, 2, stream)))
-        return MOE_ERR_CUDA;
-    // 3. experts (routed segments and the shared expert); the first expert
-    //    kernel also evaluates the balance loss from the dispatch's sums
+    moe_status st = route_step(c, L, ws, x, W_r, router_bias, router_logits, topk_idx, topk_w,
+                               dropped_mask, expert_counts, kept_counts, y, nullptr, ev, stream);
+    if (st != MOE_OK)
+        return st;
     AuxArgs aux;
     aux.psum = reinterpret_cast<const double *>(ws + L.psum);
     aux.counts = expert_counts;
@@ -230,23 +276,8 @@ moe_status forward_body(const moe_config &c, const WorkspaceLayout &L, uint8_t *
     aux.T = c.T;
     aux.k = c.top_k;
     aux.alpha = c.aux_alpha;
-    if (c.dtype == MOE_DTYPE_BF16)
-        err = launch_experts_tc(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y,
-                                aux, stream, ev);
-    else
-        err = launch_experts_simt(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
-                                  aux, stream, ev);
-    if (!cuda_ok(err))
-        return MOE_ERR_CUDA;
-    // 4. weighted combine (+ shared expert), unless the down projection
-    //    already wrote y
-    if (!(direct_y(c) && c.dtype == MOE_DTYPE_BF16)) {
-        if (!cuda_ok(launch_combine(c, L, ws, topk_w, y, stream)))
-            return MOE_ERR_CUDA;
-    }
-    if (!cuda_ok(record_stage(ev, 7, stream)))
-        return MOE_ERR_CUDA;
-    return MOE_OK;
+    return expert_step(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y, topk_w,
+                       aux, ev, stream);
 }
 
 }  // namespace moe
@@ -384,6 +415,145 @@ moe_status moe_latent_forward(const moe_config *cfg, int32_t d_outer, const void
                                   static_cast<const float *>(W_out), static_cast<float *>(y),
                                   status, stream);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ---- one rank's share of a batch split over several ranks
+
+static moe_status validate_shard(const moe_config *cfg, int64_t T_global)
+{
+    const moe_status st = validate_config(cfg);
+    if (st != MOE_OK)
+        return st;
+    if (T_global < cfg->T)
+        return MOE_ERR_INVALID_ARG;
+    if (T_global * cfg->top_k >= (1ll << 31))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status moe_sharded_workspace_size(const moe_config *cfg, int64_t T_global, size_t *bytes)
+{
+    if (!bytes)
+        return MOE_ERR_INVALID_ARG;
+    const moe_status st = validate_shard(cfg, T_global);
+    if (st != MOE_OK)
+        return st;
+    *bytes = layout_of(cfg, T_global).total;
+    return MOE_OK;
+}
+
+moe_status moe_sharded_route(const moe_config *cfg, int64_t T_global, const void *x,
+                             const void *W_r, const float *router_bias, float *router_logits,
+                             int32_t *topk_idx, float *topk_w, int32_t *expert_counts,
+                             double *prob_sums, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream)
+{
+    moe_status st = validate_shard(cfg, T_global);
+    if (st != MOE_OK)
+        return st;
+    const moe_config &c = *cfg;
+    if (!expert_counts || !prob_sums)
+        return MOE_ERR_INVALID_ARG;
+    if (c.T > 0 && (!x || !W_r || !router_logits || !topk_idx || !topk_w))
+        return MOE_ERR_INVALID_ARG;
+    const WorkspaceLayout L = layout_of(cfg, T_global);
+    if (!workspace || workspace_bytes < L.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MOE_ERR_WORKSPACE;
+    if (c.dtype == MOE_DTYPE_BF16 && (!aligned16(x) || !aligned16(W_r)))
+        return MOE_ERR_INVALID_ARG;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (!cuda_ok(cudaMemsetAsync(ws + L.status, 0, 64, stream)))
+        return MOE_ERR_CUDA;
+    if (c.T == 0) {
+        if (!cuda_ok(cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * c.n_experts, stream)) ||
+            !cuda_ok(cudaMemsetAsync(prob_sums, 0, sizeof(double) * c.n_experts, stream)))
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    ShardArgs sh{};
+    sh.phases = 1;
+    sh.n_ranks = 1;
+    sh.T_global = T_global;
+    sh.psum_out = prob_sums;
+    return route_step(c, L, ws, x, W_r, router_bias, router_logits, topk_idx, topk_w, nullptr,
+                      expert_counts, nullptr, nullptr, &sh, nullptr, stream);
+}
+
+moe_status moe_sharded_finish(const moe_config *cfg, int64_t T_global, int32_t n_ranks,
+                              int32_t rank, const int32_t *all_expert_counts,
+                              const double *all_prob_sums, const void *x, const void *W_gate,
+                              const void *W_up, const void *W_down, const void *Ws_gate,
+                              const void *Ws_up, const void *Ws_down, const int32_t *topk_idx,
+                              const float *topk_w, void *y, uint8_t *dropped_mask,
+                              int32_t *kept_counts, float *aux_loss, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream)
+{
+    moe_status st = validate_shard(cfg, T_global);
+    if (st != MOE_OK)
+        return st;
+    const moe_config &c = *cfg;
+    if (n_ranks < 1 || rank < 0 || rank >= n_ranks || !kept_counts || !aux_loss)
+        return MOE_ERR_INVALID_ARG;
+    if (T_global > 0 && (!all_expert_counts || !all_prob_sums))
+        return MOE_ERR_INVALID_ARG;
+    if (c.T > 0) {
+        if (!x || !W_gate || !W_up || !W_down || !y || !topk_idx || !topk_w || !dropped_mask)
+            return MOE_ERR_INVALID_ARG;
+        if (c.d_shared > 0 && (!Ws_gate || !Ws_up || !Ws_down))
+            return MOE_ERR_INVALID_ARG;
+    }
+    const WorkspaceLayout L = layout_of(cfg, T_global);
+    if (!workspace || workspace_bytes < L.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MOE_ERR_WORKSPACE;
+    if (c.dtype == MOE_DTYPE_BF16) {
+        if (!aligned16(x) || !aligned16(W_gate) || !aligned16(W_up) || !aligned16(W_down) ||
+            !aligned16(y) ||
+            (c.d_shared > 0 && (!aligned16(Ws_gate) || !aligned16(Ws_up) || !aligned16(Ws_down))))
+            return MOE_ERR_INVALID_ARG;
+    }
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int E = c.n_experts;
+    if (!cuda_ok(cudaMemsetAsync(kept_counts, 0, sizeof(int32_t) * E, stream)))
+        return MOE_ERR_CUDA;
+    if (T_global == 0)
+        return cuda_ok(cudaMemsetAsync(aux_loss, 0, sizeof(float), stream)) ? MOE_OK
+                                                                             : MOE_ERR_CUDA;
+    AuxArgs aux;
+    aux.psum = reinterpret_cast<const double *>(ws + L.psum);
+    aux.counts = reinterpret_cast<const int32_t *>(ws + L.gcount);
+    aux.out = aux_loss;
+    aux.E = E;
+    aux.T = (int)T_global;
+    aux.k = c.top_k;
+    aux.alpha = c.aux_alpha;
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    if (c.T == 0) {
+        // nothing routed here: only the statistics over all ranks and the loss
+        return cuda_ok(launch_shard_stats(all_expert_counts, all_prob_sums, n_ranks, rank,
+                                          T_global * c.top_k,
+                                          reinterpret_cast<int32_t *>(ws + L.gcount),
+                                          reinterpret_cast<double *>(ws + L.psum), aux, status,
+                                          stream))
+                   ? MOE_OK
+                   : MOE_ERR_CUDA;
+    }
+    ShardArgs sh{};
+    sh.phases = 2;
+    sh.all_counts = all_expert_counts;
+    sh.all_psum = all_prob_sums;
+    sh.n_ranks = n_ranks;
+    sh.rank = rank;
+    sh.T_global = T_global;
+    // the placement phase only reads the gate's indices and weights
+    st = route_step(c, L, ws, x, nullptr, nullptr, nullptr, const_cast<int32_t *>(topk_idx),
+                    const_cast<float *>(topk_w), dropped_mask, nullptr, kept_counts, y, &sh,
+                    nullptr, stream);
+    if (st != MOE_OK)
+        return st;
+    return expert_step(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y, topk_w,
+                       aux, nullptr, stream);
 }
 
 moe_status moe_read_device_status(const moe_config *cfg, const void *workspace,

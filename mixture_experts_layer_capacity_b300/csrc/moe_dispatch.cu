@@ -25,6 +25,13 @@
 // All blocks are co-resident (cooperative launch); the barrier wait is
 // bounded in time.
 //
+// A batch split over several ranks runs the kernel twice with an exchange
+// of per-expert statistics in between (phases): the first launch gates and
+// stops after the demand counts and probability sums of this rank's tokens;
+// the second, given every rank's counts, places this rank's assignments at
+// global token-order positions (the counts of earlier ranks come first), so
+// that capacity drops fall exactly where they would for the whole batch.
+//
 // Sources: "Mixture of Experts: More Parameters, Same FLOPs" ('The router');
 // "Mixture of Experts" (module 17), 17.2 (softmax over the selected vs over
 // all experts), 17.4 (balance loss) and 17.5 (capacity equation; tokens beyond
@@ -82,6 +89,14 @@ struct DispatchParams {
     float *row_w;           // [R_max] gate weight of each row (direct-y mode), or null
     uint8_t *y_zero;        // y [T,D]: rows of fully dropped tokens are zeroed (direct-y)
     int32_t *status;        // [0] status word, [9] barrier counter
+    // split batch (all_counts non-null): phases 1 = gate and statistics only,
+    // 2 = placement only (the gate's results are in the workspace), 3 = both
+    int phases;
+    const int32_t *all_counts;  // [n_ranks][E] demand counts of every rank, or null
+    const double *all_psum;     // [n_ranks][E] probability sums of every rank
+    int n_ranks, rank_id;
+    long long TK_global;        // assignments over all ranks (T_global * k)
+    int32_t *gcount;            // [E] out: demand counts over all ranks
 };
 
 // ------------------------------------------------------------ block helpers
@@ -562,6 +577,24 @@ __device__ __forceinline__ void gate_token(const DispatchParams &p, const float 
 }
 
 // ---------------------------------------------------------- phase 2 helpers
+// Sum of v over the block (every thread receives it).
+__device__ __forceinline__ long long block_sum_ll(long long v)
+{
+    __shared__ long long sh[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0)
+        sh[warp] = v;
+    __syncthreads();
+    long long t = 0;
+    for (int w = 0; w < nw; ++w)
+        t += sh[w];
+    __syncthreads();
+    return t;
+}
+
 // Copies token t's x row (src: shared or global memory) into its kept rows
 // of x_perm; this warp handles the 16-byte vectors part*32+lane, stepping by
 // nparts*32 (four loads in flight before their stores).
@@ -662,7 +695,8 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
     int32_t *s_base = run + E;                                      // [E] counts of earlier blocks
     int32_t *s_n = s_base + E;                                      // [E] demand counts
     int32_t *s_seg = s_n + E;                                       // [E+1] segment offsets
-    float *rpart = reinterpret_cast<float *>(s_seg + E + 1);        // [8][32][16] router parts
+    int32_t *s_rb = s_seg + E + 1;                                  // [E] earlier ranks' counts
+    float *rpart = reinterpret_cast<float *>(s_rb + E);             // [8][32][16] router parts
     int32_t *rbuf = reinterpret_cast<int32_t *>(rpart + kRouterMmaWarps * kChunk * kFusedMaxE);
     float *wbuf = reinterpret_cast<float *>(rbuf + kChunk * kMaxTopK);  // [32][k] ranks, weights
     unsigned *bar_counter = reinterpret_cast<unsigned *>(p.status + 9);
@@ -675,9 +709,14 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
         return;
     }
 
+    const bool gate = (p.phases & 1) != 0;
+    // a one-chunk block keeps its assignments in shared memory from phase 1
+    // to phase 2 when both run in this launch
+    const bool held = gate && p.cpb == 1;
+
     // W_r (fused router) and this block's x rows (when staged) into shared
     // memory, four 16-byte loads in flight per thread
-    {
+    if (gate) {
         const long long vpw = wrow > 0 ? wrow / 16 : 1, vpx = (long long)(p.row_bytes / 16);
         const long long n_w = RT == ROUTER_NONE ? 0 : (long long)E * vpw;
         const long long n = n_w + (p.x_staged ? (long long)ntok * vpx : 0);
@@ -709,7 +748,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
         run[e] = 0;
 
     // ---- phase 1: gate this block's chunks in token order
-    for (int chunk = c_beg; chunk < c_end; ++chunk) {
+    for (int chunk = c_beg; gate && chunk < c_end; ++chunk) {
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             mask[e] = 0u;
         __syncthreads();
@@ -775,10 +814,12 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
             run[e] += __popc(mask[e]);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        p.bcount[(size_t)e * G + b] = run[e];
-    if (!grid_barrier(bar_counter, (unsigned)G, p.status, &sh_flag))
-        return;
+    if (gate) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            p.bcount[(size_t)e * G + b] = run[e];
+        if (!grid_barrier(bar_counter, (unsigned)G, p.status, &sh_flag))
+            return;
+    }
 
     // ---- phase 2a: per expert, tokens of earlier blocks and the total
     // (warp w: experts w, w+32, ..., four at a time)
@@ -809,12 +850,60 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
         }
     }
     __syncthreads();
+    if (p.phases == 1) {
+        // gate and statistics only: this rank's demand counts and
+        // probability sums, for the exchange between the ranks
+        if (b == 0)
+            for (int e = threadIdx.x; e < E; e += blockDim.x)
+                p.expert_counts[e] = s_n[e];
+        if (warp == 31)
+            prob_sums(p, b, G);
+        return;
+    }
+    // ---- split batch: per expert, the assignments of earlier ranks (they
+    // precede this rank's in global token order) and of all ranks; the
+    // exchanged counts must hold this rank's own and add up to T_global * k
+    if (p.all_counts) {
+        const int x = threadIdx.x;
+        long long before = 0, all = 0, own = 0;
+        double ps = 0.0;
+        if (x < E) {
+            for (int r = 0; r < p.n_ranks; ++r) {
+                const long long v = __ldg(p.all_counts + (size_t)r * E + x);
+                before += r < p.rank_id ? v : 0;
+                all += v;
+                own = r == p.rank_id ? v : own;
+                ps += __ldg(p.all_psum + (size_t)r * E + x);  // rank order: fixed rounding
+            }
+        }
+        const bool bad_e = x < E && (own != s_n[x] || before < 0 || all > INT_MAX);
+        const long long tot = block_sum_ll(all);
+        if (__syncthreads_or(bad_e) || tot != p.TK_global) {
+            if (b == 0 && threadIdx.x == 0)
+                set_status(p.status, MOE_DEVICE_SHARD_MISMATCH);
+            return;
+        }
+        if (x < E) {
+            s_rb[x] = (int32_t)min(before, (long long)INT_MAX);
+            if (b == 0) {
+                p.gcount[x] = (int32_t)all;
+                p.psum[x] = ps;
+            }
+        }
+    } else {
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            s_rb[e] = 0;
+    }
+    __syncthreads();
     // ---- phase 2b: kept counts, segment offsets, 128-row tile prefix (the
-    // same in every block; block 0 publishes them)
+    // same in every block; block 0 publishes them).  An expert keeps the
+    // assignments whose global position (earlier ranks' count + position
+    // here) is below C.
     {
         const int x = threadIdx.x;
         const int n = x < E ? s_n[x] : 0;
-        const int kept = (p.C < 0) ? n : (int)min((long long)n, p.C);
+        const long long room = x < E ? p.C - (long long)s_rb[x] : 0;
+        const int kept = (p.C < 0) ? n : (int)max(0ll, min((long long)n, room));
         int tot;
         const int off = block_excl_scan(kept, sh_int, &tot);
         if (x < E)
@@ -826,7 +915,8 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
         const int moff = block_excl_scan(mt, sh_int, &mt_total);
         if (b == 0) {
             if (x < E) {
-                p.expert_counts[x] = n;
+                if (p.expert_counts)
+                    p.expert_counts[x] = n;
                 p.kept_counts[x] = kept;
                 p.seg_off[x] = off;
                 p.mtile[x] = moff;
@@ -842,7 +932,8 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
     // ---- phase 2c/2d: the last warp computes this block's probability sums;
     // the other warps place the block's assignments and copy x into x_perm
     if (warp == 31) {
-        prob_sums(p, b, G);
+        if (gate && !p.all_counts)
+            prob_sums(p, b, G);
         return;
     }
     constexpr int kCopyWarps = 31;
@@ -854,16 +945,16 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
             const size_t tk = (size_t)t * k + lane;
             // a one-chunk block still holds its assignments in shared memory
             const int u = (t - t_beg) * k + lane;
-            const int e = p.cpb == 1 ? ibuf[u] : __ldcg(p.topk_idx + tk);
-            const long long pos = (long long)s_base[e] + (p.cpb == 1 ? rbuf[u] : __ldcg(p.rank + tk));
-            const bool kept = (p.C < 0) || (pos < p.C);
+            const int e = held ? ibuf[u] : __ldcg(p.topk_idx + tk);
+            const long long pos = (long long)s_base[e] + (held ? rbuf[u] : __ldcg(p.rank + tk));
+            const bool kept = (p.C < 0) || (pos + s_rb[e] < p.C);
             row = kept ? (long long)s_seg[e] + pos : -1;
             if (part == 0) {
                 p.dropped[tk] = kept ? 0 : 1;
                 p.row_of[tk] = (int32_t)row;
                 if (p.row_tok && row >= 0) {
                     p.row_tok[row] = t;
-                    p.row_w[row] = p.cpb == 1 ? wbuf[u] : __ldcg(p.topk_w + tk);
+                    p.row_w[row] = held ? wbuf[u] : __ldcg(p.topk_w + tk);
                 }
             }
         }
@@ -874,7 +965,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
             rows[j] = __shfl_sync(0xffffffffu, row, j);
             any |= (j < k && rows[j] >= 0);
         }
-        const uint8_t *src = p.x_staged
+        const uint8_t *src = p.x_staged && gate
                                  ? xs + (size_t)(t - t_beg) * xstride
                                  : static_cast<const uint8_t *>(p.x) + (size_t)t * p.row_bytes;
         copy_row(p, src, rows, part, nparts);
@@ -884,6 +975,50 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
                 dst[v] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
+}
+
+// A rank without tokens in a split batch: the demand counts and probability
+// sums over all ranks (rank order), then the balance loss.  One warp.
+__global__ void shard_stats_kernel(const int32_t *all_counts, const double *all_psum,
+                                   int n_ranks, int rank, long long TK_global, int32_t *gcount,
+                                   double *gpsum, AuxArgs aux, int32_t *status)
+{
+    const int lane = threadIdx.x & 31, E = aux.E;
+    long long tot = 0;
+    bool bad = false;
+    for (int e = lane; e < E; e += 32) {
+        long long all = 0;
+        double ps = 0.0;
+        for (int r = 0; r < n_ranks; ++r) {
+            const long long v = all_counts[(size_t)r * E + e];
+            bad |= (r == rank && v != 0) || v < 0;
+            all += v;
+            ps += all_psum[(size_t)r * E + e];
+        }
+        gcount[e] = (int32_t)min(all, (long long)INT_MAX);
+        gpsum[e] = ps;
+        tot += all;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (__any_sync(0xffffffffu, bad) || tot != TK_global) {
+        if (lane == 0)
+            set_status(status, MOE_DEVICE_SHARD_MISMATCH);
+        return;
+    }
+    __threadfence();
+    __syncwarp();
+    balance_loss_warp(aux);
+}
+
+cudaError_t launch_shard_stats(const int32_t *all_counts, const double *all_psum, int n_ranks,
+                               int rank, long long TK_global, int32_t *gcount, double *gpsum,
+                               const AuxArgs &aux, int32_t *status, cudaStream_t stream)
+{
+    shard_stats_kernel<<<1, 32, 0, stream>>>(all_counts, all_psum, n_ranks, rank, TK_global,
+                                             gcount, gpsum, aux, status);
+    return cudaGetLastError();
 }
 
 bool router_fused(const moe_config &c)
@@ -898,12 +1033,14 @@ bool direct_y(const moe_config &c) { return c.top_k == 1 && c.d_shared == 0; }
 // Dynamic shared memory of the dispatch kernel: staged W_r rows (fused
 // router; wr_bytes = E * (row bytes + 16)), staged x rows (xs_bytes =
 // chunk * (row bytes + 16)), pbuf [32][E] floats, ibuf [32][k], then mask,
-// run, base, n [E], the segment offsets [E+1], the router's partial sums
-// [8][32][16], and the chunk's ranks and gate weights [32][8].
+// run, base, n [E], the segment offsets [E+1], the earlier ranks' counts
+// [E], the router's partial sums [8][32][16], and the chunk's ranks and gate
+// weights [32][8].
 static size_t dispatch_smem(size_t wr_bytes, size_t xs_bytes, int E, int k)
 {
     return wr_bytes + xs_bytes + (size_t)kChunk * (E + k) * 4 + (size_t)4 * E * 4 +
-           (size_t)(E + 1) * 4 + (size_t)kRouterMmaWarps * kChunk * kFusedMaxE * 4 +
+           (size_t)(E + 1) * 4 + (size_t)E * 4 +
+           (size_t)kRouterMmaWarps * kChunk * kFusedMaxE * 4 +
            (size_t)2 * kChunk * kMaxTopK * 4;
 }
 
@@ -915,8 +1052,10 @@ static cudaError_t launch_dispatch_t(DispatchParams &p, size_t wr_bytes, cudaStr
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
+    // One block per SM (a 1024-thread block whose largest layout takes most
+    // of an SM's shared memory), so the launch geometry depends only on T and
+    // the SM count: the two launches of a split batch see the same chunks.
     static uint64_t configured = 0;
-    static int max_blocks[64] = {0};
     if (dev < 64 && !(configured & (1ull << dev))) {
         const size_t smem_max = dispatch_smem(kFusedMaxWrBytes + kFusedMaxE * 16,
                                               kStageMaxBytes + kChunk * 16, kMaxExperts, kMaxTopK);
@@ -931,11 +1070,11 @@ static cudaError_t launch_dispatch_t(DispatchParams &p, size_t wr_bytes, cudaStr
                                                             smem_max);
         if (err != cudaSuccess)
             return err;
-        max_blocks[dev] = std::max(1, per_sm) * sm_count();
+        if (per_sm < 1)
+            return cudaErrorInvalidConfiguration;
         configured |= 1ull << dev;
     }
-    const int maxb = std::max(1, std::min(kMaxDispatchBlocks,
-                                          dev < 64 ? max_blocks[dev] : sm_count()));
+    const int maxb = std::max(1, std::min(kMaxDispatchBlocks, sm_count()));
     // The smallest chunk (1, 2, ..., 32 tokens) whose chunk count fits one
     // chunk per co-resident block; else 32-token chunks, several per block.
     int cs = kChunk;
@@ -948,7 +1087,7 @@ static cudaError_t launch_dispatch_t(DispatchParams &p, size_t wr_bytes, cudaStr
     p.nchunk = (p.T + cs - 1) / cs;
     p.cpb = (p.nchunk + maxb - 1) / maxb;
     const int grid = std::max(1, (p.nchunk + p.cpb - 1) / p.cpb);
-    p.x_staged = (p.cpb == 1 && p.row_bytes % 16 == 0 &&
+    p.x_staged = ((p.phases & 1) && p.cpb == 1 && p.row_bytes % 16 == 0 &&
                   (size_t)cs * p.row_bytes <= kStageMaxBytes) ? 1 : 0;
     const size_t smem = dispatch_smem(wr_bytes, p.x_staged ? (size_t)cs * (p.row_bytes + 16) : 0,
                                       p.E, p.k);
@@ -970,9 +1109,16 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
                             const float *lpart, int lsplit, const float *bias,
                             int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
                             int32_t *expert_counts, int32_t *kept_counts, void *y,
-                            cudaStream_t stream)
+                            cudaStream_t stream, const ShardArgs *shard)
 {
     DispatchParams p;
+    p.phases = shard ? shard->phases : 3;
+    p.all_counts = shard ? shard->all_counts : nullptr;
+    p.all_psum = shard ? shard->all_psum : nullptr;
+    p.n_ranks = shard ? shard->n_ranks : 1;
+    p.rank_id = shard ? shard->rank : 0;
+    p.TK_global = (shard ? shard->T_global : (long long)c.T) * c.top_k;
+    p.gcount = shard ? reinterpret_cast<int32_t *>(ws + L.gcount) : nullptr;
     const size_t esz = c.dtype == MOE_DTYPE_BF16 ? 2 : 4;
     p.logits = logits;
     p.lpart = lpart;
@@ -997,7 +1143,7 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
     p.bcount = reinterpret_cast<int32_t *>(ws + L.bcount);
     p.ppart = reinterpret_cast<float *>(ws + L.ppart);
     p.rank = reinterpret_cast<int32_t *>(ws + L.rank);
-    p.psum = reinterpret_cast<double *>(ws + L.psum);
+    p.psum = shard && shard->psum_out ? shard->psum_out : reinterpret_cast<double *>(ws + L.psum);
     p.seg_off = reinterpret_cast<int32_t *>(ws + L.seg_off);
     p.mtile = reinterpret_cast<int32_t *>(ws + L.mtile);
     p.row_of = reinterpret_cast<int32_t *>(ws + L.row_of);

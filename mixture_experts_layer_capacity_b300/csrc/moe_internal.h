@@ -25,6 +25,7 @@ struct WorkspaceLayout {
     size_t ppart;    // float[E][nchunk]  per-chunk sums of softmax probabilities
     size_t rank;     // int32[T*k]        rank of an assignment among its block's tokens
     size_t psum;     // double[E]         sum over tokens of the softmax probabilities
+    size_t gcount;   // int32[E]          demand counts over all ranks (split batch)
     size_t seg_off;  // int32[E+1]        first x_perm row of each expert's segment
     size_t mtile;    // int32[E+1]        prefix sum of 128-row tiles per segment
     size_t row_of;   // int32[T*k]        x_perm row of an assignment, -1 if dropped
@@ -74,8 +75,20 @@ int router_splits(const moe_config &c);
 constexpr int kMaxRouterSplits = 8;
 
 moe_status validate_config(const moe_config *cfg);
-int64_t capacity_of(const moe_config *cfg);
-WorkspaceLayout layout_of(const moe_config *cfg);
+// Capacity and workspace layout.  T_cap: the tokens that set the capacity
+// (all ranks' tokens for a split batch); -1 = cfg->T.
+int64_t capacity_of(const moe_config *cfg, int64_t T_cap = -1);
+WorkspaceLayout layout_of(const moe_config *cfg, int64_t T_cap = -1);
+
+// One rank's share of a batch split over several ranks (see moe_dispatch.cu).
+struct ShardArgs {
+    int phases;                // 1: gate and statistics only; 2: placement only
+    const int32_t *all_counts; // [n_ranks][E] every rank's demand counts (phase 2)
+    const double *all_psum;    // [n_ranks][E] every rank's probability sums (phase 2)
+    int n_ranks, rank;
+    long long T_global;        // tokens over all ranks
+    double *psum_out;          // [E] this rank's probability sums (phase 1)
+};
 
 // Launchers (all enqueue on `stream`; return the launch's error).
 cudaError_t launch_router_simt(const moe_config &c, const void *x, const void *W_r,
@@ -94,7 +107,12 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
                             const float *lpart, int lsplit, const float *bias,
                             int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
                             int32_t *expert_counts, int32_t *kept_counts, void *y,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const ShardArgs *shard = nullptr);
+// Split batch, rank without tokens: counts and sums over all ranks into
+// gcount/gpsum, then the balance loss of `aux` (which points at them).
+cudaError_t launch_shard_stats(const int32_t *all_counts, const double *all_psum, int n_ranks,
+                               int rank, long long TK_global, int32_t *gcount, double *gpsum,
+                               const AuxArgs &aux, int32_t *status, cudaStream_t stream);
 cudaError_t launch_combine(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                            const float *topk_w, void *y, cudaStream_t stream);
 // `aux`: the balance loss, evaluated by the first expert kernel.

@@ -135,3 +135,42 @@ def test_status_strings():
     for s in range(6):
         assert B.status_string(s).startswith("MOE_")
     assert "unknown" in B.status_string(42)
+
+
+def test_sharded_entry_points_validate_on_the_host():
+    L = B.lib()
+    cfg = B.make_config(100, 128, 8, 128, 2, capacity_factor=1.0)
+    n = ctypes.c_size_t(0)
+    # T_global below this rank's tokens; too many assignments overall
+    assert L.moe_sharded_workspace_size(ctypes.byref(cfg), 99, ctypes.byref(n)) == \
+        B.MOE_ERR_INVALID_ARG
+    assert L.moe_sharded_workspace_size(ctypes.byref(cfg), 1 << 30, ctypes.byref(n)) == \
+        B.MOE_ERR_UNSUPPORTED
+    # the capacity of the whole batch may keep more rows on one rank than a
+    # batch of this rank's size could: the split-batch scratch is never smaller
+    need = B.sharded_workspace_size(cfg, 400)
+    assert need >= B.workspace_size(cfg)
+    fake = [4096 * (i + 1) for i in range(16)]
+    ws = 1 << 20
+
+    def finish(n_ranks, rank, ws_bytes=need, ptrs=fake, ws_ptr=ws):
+        return L.moe_sharded_finish(ctypes.byref(cfg), 400, n_ranks, rank, *ptrs[:15], ws_ptr,
+                                    ctypes.c_size_t(ws_bytes), None)
+
+    for n_ranks, rank in ((2, 2), (0, 0), (4, -1)):
+        assert finish(n_ranks, rank) == B.MOE_ERR_INVALID_ARG
+    assert finish(4, 1, ws_bytes=need - 1) == B.MOE_ERR_WORKSPACE
+    assert finish(4, 1, ws_ptr=ws + 64) == B.MOE_ERR_WORKSPACE
+    no_counts = [None] + fake[1:]
+    assert finish(4, 1, ptrs=no_counts) == B.MOE_ERR_INVALID_ARG
+
+    def route(ptrs, ws_bytes=need):
+        return L.moe_sharded_route(ctypes.byref(cfg), 400, *ptrs, ws, ctypes.c_size_t(ws_bytes),
+                                   None)
+
+    r = fake[:8]
+    missing_sums = r[:7] + [None]
+    assert route(missing_sums) == B.MOE_ERR_INVALID_ARG
+    assert route(r, ws_bytes=need - 1) == B.MOE_ERR_WORKSPACE
+    misaligned_x = [4096 + 8] + r[1:]
+    assert route(misaligned_x) == B.MOE_ERR_INVALID_ARG
