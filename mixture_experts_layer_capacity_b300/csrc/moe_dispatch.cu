@@ -667,8 +667,11 @@ __device__ __forceinline__ void prob_sums(const DispatchParams &p, int b, int G)
 
 // --------------------------------------------------------- the whole kernel
 // EPL: experts per lane (ceil(E / 32)); RT: fused router type; EM: the
-// fused router's expert count rounded up to 4, 8 or 16.
-template <int EPL, int RT, int EM>
+// fused router's expert count rounded up to 4, 8 or 16; SPLIT: 0 = the whole
+// layer's dispatch, 1 = a split batch's gate and statistics, 2 = a split
+// batch's placement (separate instantiations keep the whole-layer kernel
+// free of the split-batch code).
+template <int EPL, int RT, int EM, int SPLIT>
 __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchParams p)
 {
     extern __shared__ __align__(16) uint8_t dsm[];
@@ -709,7 +712,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
         return;
     }
 
-    const bool gate = (p.phases & 1) != 0;
+    constexpr bool gate = SPLIT != 2;
     // a one-chunk block keeps its assignments in shared memory from phase 1
     // to phase 2 when both run in this launch
     const bool held = gate && p.cpb == 1;
@@ -850,7 +853,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
         }
     }
     __syncthreads();
-    if (p.phases == 1) {
+    if constexpr (SPLIT == 1) {
         // gate and statistics only: this rank's demand counts and
         // probability sums, for the exchange between the ranks
         if (b == 0)
@@ -863,7 +866,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
     // ---- split batch: per expert, the assignments of earlier ranks (they
     // precede this rank's in global token order) and of all ranks; the
     // exchanged counts must hold this rank's own and add up to T_global * k
-    if (p.all_counts) {
+    if constexpr (SPLIT == 2) {
         const int x = threadIdx.x;
         long long before = 0, all = 0, own = 0;
         double ps = 0.0;
@@ -932,7 +935,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
     // ---- phase 2c/2d: the last warp computes this block's probability sums;
     // the other warps place the block's assignments and copy x into x_perm
     if (warp == 31) {
-        if (gate && !p.all_counts)
+        if constexpr (SPLIT == 0)
             prob_sums(p, b, G);
         return;
     }
@@ -1044,10 +1047,10 @@ static size_t dispatch_smem(size_t wr_bytes, size_t xs_bytes, int E, int k)
            (size_t)2 * kChunk * kMaxTopK * 4;
 }
 
-template <int EPL, int RT, int EM = 1>
+template <int EPL, int RT, int EM, int SPLIT>
 static cudaError_t launch_dispatch_t(DispatchParams &p, size_t wr_bytes, cudaStream_t stream)
 {
-    auto kern = dispatch_kernel<EPL, RT, EM>;
+    auto kern = dispatch_kernel<EPL, RT, EM, SPLIT>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
@@ -1104,6 +1107,33 @@ static cudaError_t launch_dispatch_t(DispatchParams &p, size_t wr_bytes, cudaStr
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// The instantiation for the router type and expert count.
+template <int SPLIT>
+static cudaError_t launch_dispatch_s(const moe_config &c, DispatchParams &p, bool fused,
+                                     size_t wr_bytes, cudaStream_t stream)
+{
+    const int E = c.n_experts;
+    if constexpr (SPLIT != 2) {
+        if (fused) {
+            if (c.dtype == MOE_DTYPE_BF16)
+                return E <= 4   ? launch_dispatch_t<1, ROUTER_BF16, 4, SPLIT>(p, wr_bytes, stream)
+                       : E <= 8 ? launch_dispatch_t<1, ROUTER_BF16, 8, SPLIT>(p, wr_bytes, stream)
+                                : launch_dispatch_t<1, ROUTER_BF16, 16, SPLIT>(p, wr_bytes, stream);
+            return E <= 4   ? launch_dispatch_t<1, ROUTER_F32, 4, SPLIT>(p, wr_bytes, stream)
+                   : E <= 8 ? launch_dispatch_t<1, ROUTER_F32, 8, SPLIT>(p, wr_bytes, stream)
+                            : launch_dispatch_t<1, ROUTER_F32, 16, SPLIT>(p, wr_bytes, stream);
+        }
+    }
+    const int epl = (E + 31) / 32;
+    if (epl <= 1)
+        return launch_dispatch_t<1, ROUTER_NONE, 1, SPLIT>(p, wr_bytes, stream);
+    if (epl <= 2)
+        return launch_dispatch_t<2, ROUTER_NONE, 1, SPLIT>(p, wr_bytes, stream);
+    if (epl <= 4)
+        return launch_dispatch_t<4, ROUTER_NONE, 1, SPLIT>(p, wr_bytes, stream);
+    return launch_dispatch_t<8, ROUTER_NONE, 1, SPLIT>(p, wr_bytes, stream);
+}
+
 cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                             const void *x, const void *W_r, bool fused, float *logits,
                             const float *lpart, int lsplit, const float *bias,
@@ -1154,24 +1184,11 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
     p.y_zero = dy ? static_cast<uint8_t *>(y) : nullptr;
     p.status = reinterpret_cast<int32_t *>(ws + L.status);
     const size_t wr_bytes = fused ? (size_t)c.n_experts * (c.d_model * esz + 16) : 0;
-    if (fused) {
-        const int E = c.n_experts;
-        if (c.dtype == MOE_DTYPE_BF16)
-            return E <= 4   ? launch_dispatch_t<1, ROUTER_BF16, 4>(p, wr_bytes, stream)
-                   : E <= 8 ? launch_dispatch_t<1, ROUTER_BF16, 8>(p, wr_bytes, stream)
-                            : launch_dispatch_t<1, ROUTER_BF16, 16>(p, wr_bytes, stream);
-        return E <= 4   ? launch_dispatch_t<1, ROUTER_F32, 4>(p, wr_bytes, stream)
-               : E <= 8 ? launch_dispatch_t<1, ROUTER_F32, 8>(p, wr_bytes, stream)
-                        : launch_dispatch_t<1, ROUTER_F32, 16>(p, wr_bytes, stream);
-    }
-    const int epl = (c.n_experts + 31) / 32;
-    if (epl <= 1)
-        return launch_dispatch_t<1, ROUTER_NONE>(p, wr_bytes, stream);
-    if (epl <= 2)
-        return launch_dispatch_t<2, ROUTER_NONE>(p, wr_bytes, stream);
-    if (epl <= 4)
-        return launch_dispatch_t<4, ROUTER_NONE>(p, wr_bytes, stream);
-    return launch_dispatch_t<8, ROUTER_NONE>(p, wr_bytes, stream);
+    const int split = !shard ? 0 : shard->phases == 1 ? 1 : 2;
+    if (split == 2)  // placement only: no router, no gating
+        return launch_dispatch_s<2>(c, p, false, wr_bytes, stream);
+    return split == 1 ? launch_dispatch_s<1>(c, p, fused, wr_bytes, stream)
+                      : launch_dispatch_s<0>(c, p, fused, wr_bytes, stream);
 }
 
 }  // namespace moe
