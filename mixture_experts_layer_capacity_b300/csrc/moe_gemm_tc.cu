@@ -89,6 +89,20 @@ struct TileInfo {
     int a_row0, rows, seg, n_idx;
 };
 
+// The fewest workers (CTAs or CTA pairs) that finish n equal units in as
+// many rounds as w workers would.  With w workers some would take one unit
+// more than the rest, and the final round would run on those few alone; an
+// HBM-bound GEMM then streams its last tiles at a few SMs' bandwidth.  With
+// every worker taking the same number of units (give or take one in the
+// first round), the bandwidth stays shared by all of them to the end.
+__device__ __forceinline__ int balanced_workers(int n, int w)
+{
+    if (n <= 0)
+        return w;
+    const int rounds = (n + w - 1) / w;
+    return (n + rounds - 1) / rounds;
+}
+
 // The segment tables (seg_off, mtile) are copied into shared memory at
 // kernel start; s_seg/s_mt point there (null when dense).
 __device__ __forceinline__ int tile_count(const TcParams &p, const int *s_mt)
@@ -334,7 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // work units: tiles x reduction splits (unit u: tile u / ks_n, split u % ks_n)
     const int ks_n = p.ksplit > 1 ? p.ksplit : 1;
-    const int ntiles = failed ? 0 : tile_count(p, s_mt) * ks_n;
+    const int tiles_all = failed ? 0 : tile_count(p, s_mt) * ks_n;
+    const int G = balanced_workers(tiles_all, (int)gridDim.x);
+    const int ntiles = (int)blockIdx.x < G ? tiles_all : 0;
     const int nk_all = (p.K + 63) / 64;
 
     if (warp == 0) {
@@ -344,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             long long fills = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < ntiles && ok; u += gridDim.x) {
+            for (int u = blockIdx.x; u < ntiles && ok; u += G) {
                 const int g = u / ks_n, ks = u - g * ks_n;
                 const int kb0 = ks * nk_all / ks_n, kb1 = (ks + 1) * nk_all / ks_n;
                 const TileInfo ti = tile_info(p, s_seg, s_mt, g);
@@ -385,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int s = 0;
             uint32_t ph = 0, b = 0, tph = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < ntiles && ok; u += gridDim.x) {
+            for (int u = blockIdx.x; u < ntiles && ok; u += G) {
                 const int ks = u % ks_n;
                 const int kb0 = ks * nk_all / ks_n, kb1 = (ks + 1) * nk_all / ks_n;
                 if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -437,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;             // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;        // accumulator row of this thread
         uint32_t b = 0, tph = 0;
-        for (int u = blockIdx.x; u < ntiles; u += gridDim.x) {
+        for (int u = blockIdx.x; u < ntiles; u += G) {
             const int g = u / ks_n, ks = u - g * ks_n;
             const TileInfo ti = tile_info(p, s_seg, s_mt, g);
             if (!mbar_wait(&tfull[b], tph, abort_flag, kWaitLimitNs)) {
@@ -625,7 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int ntiles = failed ? 0 : pair_tile_count(p, s_mt);
+    const int tiles_all = failed ? 0 : pair_tile_count(p, s_mt);
+    const int NC = balanced_workers(tiles_all, nclusters);
+    const int ntiles = cluster_id < NC ? tiles_all : 0;
     const int nk = (p.K + 63) / 64;
 
     if (warp == 0) {
@@ -636,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             long long fills = 0;
             bool ok = true;
-            for (int g = cluster_id; g < ntiles && ok; g += nclusters) {
+            for (int g = cluster_id; g < ntiles && ok; g += NC) {
                 const TileInfo ti = pair_tile_info(p, s_seg, s_mt, g);
                 const int a_row = ti.a_row0 + (int)rank * kTileM;
                 const int b_row = ti.seg * p.b_seg_rows + ti.n_idx * BN +
@@ -686,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int s = 0;
             uint32_t ph = 0, b = 0, tph = 0;
             bool ok = true;
-            for (int g = cluster_id; g < ntiles && ok; g += nclusters) {
+            for (int g = cluster_id; g < ntiles && ok; g += NC) {
                 if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
@@ -735,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q * 32 + lane;        // accumulator row of this thread
         const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), 0);
         uint32_t b = 0, tph = 0;
-        for (int g = cluster_id; g < ntiles; g += nclusters) {
+        for (int g = cluster_id; g < ntiles; g += NC) {
             const TileInfo ti = pair_tile_info(p, s_seg, s_mt, g);
             if (!mbar_wait(&tfull[b], tph, abort_flag, kWaitLimitNs)) {
                 *abort_flag = 1;
