@@ -138,11 +138,13 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- roofline
-def stage_work(w, kept_total, touched):
-    """Algorithmic (flops, bytes) of each stage of one forward pass."""
+def stage_work(w, kept_total, touched, shared_fused=False):
+    """Algorithmic (flops, bytes) of each stage of one forward pass.  With the
+    shared expert's tiles inside the routed GEMM launches (shared_fused), the
+    routed stages carry the shared work and the shared stages are empty."""
     b = 2 if w.dtype == "bf16" else 4
     D, F, S, T, E, k = w.D, w.F, w.S, w.T, w.E, w.k
-    return {
+    work = {
         "router": (2 * T * D * E, b * (T * D + E * D) + 4 * T * E),
         "gemm1_routed": (4 * D * F * kept_total,
                          b * (2 * F * D * touched + kept_total * D + kept_total * F)),
@@ -153,6 +155,11 @@ def stage_work(w, kept_total, touched):
         "dispatch": (0, b * (T * D + kept_total * D)),
         "combine": (0, b * (kept_total * D + (T * D if S else 0) + T * D)),
     }
+    if shared_fused:
+        for r, s in (("gemm1_routed", "gemm1_shared"), ("gemm2_routed", "gemm2_shared")):
+            work[r] = (work[r][0] + work[s][0], work[r][1] + work[s][1])
+            del work[s]
+    return work
 
 
 def profile_traffic(stage, workload):
@@ -372,7 +379,7 @@ def run_ours(args, rank, world, device):
     # dominant kernel and its roofline.  Tensor peak: the burst figure for
     # steps under 1 ms; the sustained (power-capped) figure when the kernel
     # runs inside multi-ms steps replayed back to back for seconds.
-    work = stage_work(w, kept_total, touched)
+    work = stage_work(w, kept_total, touched, B.launch_plan(cfg)["shared_fused"])
     dom = max((n for n in stages if n in work), key=lambda n: stages[n])
     flops, nbytes = work[dom]
     dur_s = stages[dom] / 1e3
@@ -445,9 +452,10 @@ def run_ours(args, rank, world, device):
 
     # router (unless fused into dispatch), dispatch, GEMM1, GEMM2 (+ two
     # shared-expert GEMMs), combine (unless GEMM2 writes y)
+    plan = B.launch_plan(cfg)
     launches_per_step = (2 if w.D_outer else 0) + \
-        (0 if B.router_is_fused(cfg) else 1) + 3 + (2 if w.S else 0) + \
-        (0 if B.direct_y(cfg) else 1)
+        (0 if plan["router_fused"] else 1) + 3 + \
+        (2 if w.S and not plan["shared_fused"] else 0) + (0 if plan["direct_y"] else 1)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,

@@ -161,6 +161,16 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
                        float *aux_loss, void *workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* Which kernels moe_forward launches for `cfg` (for profiling and launch
+ * counts; host only, no GPU needed).  *flags is a bit set of: */
+#define MOE_PLAN_ROUTER_FUSED 1   /* router GEMM inside the gating kernel */
+#define MOE_PLAN_DIRECT_Y 2       /* down projection writes y; no combine kernel */
+#define MOE_PLAN_PAIR_ROUTED 4    /* routed GEMMs on CTA pairs (256-row tiles) */
+#define MOE_PLAN_PAIR_SHARED 8    /* shared-expert GEMMs on CTA pairs */
+#define MOE_PLAN_SHARED_FUSED 16  /* shared-expert tiles run inside the routed GEMM
+                                     launches (no separate shared launches) */
+MOE_API moe_status moe_launch_plan(const moe_config *cfg, int32_t *flags);
+
 /* Workspace bytes moe_latent_forward needs for `cfg` (whose d_model is the
  * latent width L) and outer width d_outer; MOE_ERR_UNSUPPORTED when d_outer
  * is not a multiple of 64 for bf16. */

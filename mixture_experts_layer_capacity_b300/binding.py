@@ -68,6 +68,8 @@ def lib():
         L.moe_workspace_size.restype = ctypes.c_int
         L.moe_capacity.argtypes = [cfgp]
         L.moe_capacity.restype = ctypes.c_int64
+        L.moe_launch_plan.argtypes = [cfgp, ctypes.POINTER(ctypes.c_int32)]
+        L.moe_launch_plan.restype = ctypes.c_int
         L.moe_forward.argtypes = [cfgp] + [vp] * 18 + [ctypes.c_size_t, vp]
         L.moe_forward.restype = ctypes.c_int
         L.moe_forward_no_alloc.argtypes = [cfgp] + [vp] * 17 + [vp]
@@ -115,17 +117,27 @@ def config_of(w) -> MoeConfig:
                        bias_selection_only=getattr(w, "sel_bias", False))
 
 
+PLAN_FLAGS = {"router_fused": 1, "direct_y": 2, "pair_routed": 4, "pair_shared": 8,
+              "shared_fused": 16}
+
+
+def launch_plan(cfg: MoeConfig) -> dict:
+    """Which kernels moe_forward launches for cfg (moe_launch_plan)."""
+    flags = ctypes.c_int32(0)
+    st = lib().moe_launch_plan(ctypes.byref(cfg), ctypes.byref(flags))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_launch_plan")
+    return {name: bool(flags.value & bit) for name, bit in PLAN_FLAGS.items()}
+
+
 def router_is_fused(cfg: MoeConfig) -> bool:
-    """Whether moe_forward computes the router scores inside its gating kernel
-    (E <= 16 and E*d_model*elem_size <= 64 KiB) rather than in a router kernel."""
-    esz = 2 if cfg.dtype == MOE_DTYPE_BF16 else 4
-    return cfg.n_experts <= 16 and cfg.d_model % 8 == 0 and \
-        cfg.n_experts * cfg.d_model * esz <= 64 * 1024
+    """Whether moe_forward computes the router scores inside its gating kernel."""
+    return launch_plan(cfg)["router_fused"]
 
 
 def direct_y(cfg: MoeConfig) -> bool:
     """Whether the down projection writes y itself (no combine kernel)."""
-    return cfg.top_k == 1 and cfg.d_shared == 0 and cfg.dtype == MOE_DTYPE_BF16
+    return launch_plan(cfg)["direct_y"]
 
 
 def workspace_size(cfg: MoeConfig) -> int:

@@ -101,17 +101,25 @@ WorkspaceLayout layout_of(const moe_config *c, int64_t T_cap)
 
 int shared_down_splits(const moe_config &c)
 {
-    if (c.dtype != MOE_DTYPE_BF16 || c.d_shared <= 0 || c.T <= 0)
+    if (!plan_of(c).shared_fused)
         return 1;
-    const long long bn = c.d_model > 1024 ? 256 : 128;
-    const long long tiles = ((c.T + kTileM - 1) / kTileM) * ((c.d_model + bn - 1) / bn);
-    const long long nk = c.d_shared / 64;
-    constexpr long long kNominalSms = 148;
-    if (tiles * 2 > kNominalSms)
-        return 1;
-    long long s = std::min<long long>(8, kNominalSms / tiles);
-    s = std::min<long long>(s, nk / 16);  // at least 16 k-steps of 64 per split
-    return (int)std::max<long long>(1, s);
+    const int s = (c.d_shared + c.d_expert - 1) / c.d_expert;
+    return std::max(1, std::min(s, kMaxSharedSplits));
+}
+
+LaunchPlan plan_of(const moe_config &c)
+{
+    LaunchPlan pl{};
+    const bool bf16 = c.dtype == MOE_DTYPE_BF16;
+    pl.router_fused = router_fused(c);
+    pl.direct_y = bf16 && direct_y(c);
+    const long long routed_rows = (long long)c.T * c.top_k;
+    pl.pair_routed = bf16 && routed_rows >= kPairMinRows &&
+                     routed_rows >= 2LL * 2 * kTileM * c.n_experts;
+    pl.pair_shared = bf16 && c.d_shared > 0 && c.T >= kPairMinRows / 4;
+    pl.shared_fused = bf16 && c.d_shared > 0 && !pl.pair_routed && !pl.pair_shared;
+    pl.router_splits = router_splits(c);
+    return pl;
 }
 
 int router_splits(const moe_config &c)
@@ -167,6 +175,21 @@ int64_t moe_capacity(const moe_config *cfg)
     if (validate_config(cfg) != MOE_OK)
         return -1;
     return capacity_of(cfg);
+}
+
+moe_status moe_launch_plan(const moe_config *cfg, int32_t *flags)
+{
+    if (!flags)
+        return MOE_ERR_INVALID_ARG;
+    const moe_status st = validate_config(cfg);
+    if (st != MOE_OK)
+        return st;
+    const LaunchPlan pl = plan_of(*cfg);
+    *flags = (pl.router_fused ? MOE_PLAN_ROUTER_FUSED : 0) | (pl.direct_y ? MOE_PLAN_DIRECT_Y : 0) |
+             (pl.pair_routed ? MOE_PLAN_PAIR_ROUTED : 0) |
+             (pl.pair_shared ? MOE_PLAN_PAIR_SHARED : 0) |
+             (pl.shared_fused ? MOE_PLAN_SHARED_FUSED : 0);
+    return MOE_OK;
 }
 
 }  // extern "C"

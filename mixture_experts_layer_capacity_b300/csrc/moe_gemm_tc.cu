@@ -61,6 +61,15 @@ struct TcParams {
     AuxArgs aux;             // balance loss to evaluate (aux.out null: none)
     int ksplit;              // splits of the reduction (single-CTA kernel, EPI_F32); 0 or 1 = none
     long long part_stride;   // elements between the splits' fp32 outputs
+    // single-CTA kernel: a second, dense problem (the shared expert next to
+    // the routed ones) whose tiles come first in the tile list; its operands
+    // are the kernel's second set of tensor maps.  sh_tiles = 0: none.
+    int sh_tiles;            // dense tiles of the second problem (row tiles x column tiles)
+    int sh_rows, sh_K, sh_n_tiles, sh_N_valid;
+    int sh_ksplit;           // splits of the second problem's reduction (fp32 partial
+                             // outputs part_stride apart, EPI_BF16 kernels only); 0/1 = none
+    void *sh_out;
+    long long sh_ld_out;
 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any tile
@@ -144,6 +153,49 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams &p, const int *s_se
     return ti;
 }
 
+// Work unit u of the combined list: the second problem's units first
+// (tile u / sh_ksplit, split u % sh_ksplit; ti.seg = -1), then the first
+// problem's (tile v / ks_n, split v % ks_n).  [kb0, kb1): the unit's 64-wide
+// reduction steps.
+struct UnitInfo {
+    TileInfo ti;
+    int ks, kb0, kb1;
+    bool second;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const TcParams &p, const int *s_seg,
+                                              const int *s_mt, int u, int ks_n)
+{
+    UnitInfo w;
+    const int sh_ks = p.sh_ksplit > 1 ? p.sh_ksplit : 1;
+    const int sh_units = p.sh_tiles * sh_ks;
+    int n_split, nk;
+    if (u < sh_units) {
+        const int g = u / sh_ks;
+        w.ks = u - g * sh_ks;
+        const int mt = (p.sh_rows + kTileM - 1) / kTileM;
+        w.ti.n_idx = g / mt;
+        const int m = g - w.ti.n_idx * mt;
+        w.ti.seg = -1;
+        w.ti.a_row0 = m * kTileM;
+        w.ti.rows = min(kTileM, p.sh_rows - w.ti.a_row0);
+        w.second = true;
+        n_split = sh_ks;
+        nk = (p.sh_K + 63) / 64;
+    } else {
+        const int v = u - sh_units;
+        const int g = v / ks_n;
+        w.ks = v - g * ks_n;
+        w.ti = tile_info(p, s_seg, s_mt, g);
+        w.second = false;
+        n_split = ks_n;
+        nk = (p.K + 63) / 64;
+    }
+    w.kb0 = w.ks * nk / n_split;
+    w.kb1 = (w.ks + 1) * nk / n_split;
+    return w;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -175,7 +227,8 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const uint32_
 // output row `orow` (stored only when row_ok), columns n_idx*BN ... of the
 // tile.  taddr: TMEM address of the row's first accumulator column.
 template <int BN, int EPI>
-__device__ __forceinline__ void epilogue_row(const TcParams &p, uint32_t taddr, bool row_ok,
+__device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long long ld_out,
+                                             int n_valid, uint32_t taddr, bool row_ok,
                                              long long orow, int n_idx, int ks = 0)
 {
     if constexpr (EPI == EPI_SWIGLU) {
@@ -197,8 +250,8 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, uint32_t taddr, 
                 }
                 const int col = n_idx * BN + c0;
                 __nv_bfloat16 *dst =
-                    reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * p.ld_out + col;
-                store_row_bf16(dst, pk, col, p.N_valid);
+                    reinterpret_cast<__nv_bfloat16 *>(out) + orow * ld_out + col;
+                store_row_bf16(dst, pk, col, n_valid);
             }
         }
     } else if constexpr (EPI == EPI_BF16_Y) {
@@ -221,8 +274,8 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, uint32_t taddr, 
                                         wr * __uint_as_float(v[2 * i + 1]));
                 const int col = n_idx * BN + c0;
                 __nv_bfloat16 *dst =
-                    reinterpret_cast<__nv_bfloat16 *>(p.out) + (long long)tok * p.ld_out + col;
-                store_row_bf16(dst, pk, col, p.N_valid);
+                    reinterpret_cast<__nv_bfloat16 *>(out) + (long long)tok * ld_out + col;
+                store_row_bf16(dst, pk, col, n_valid);
             }
         }
     } else if constexpr (EPI == EPI_BF16) {
@@ -239,8 +292,8 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, uint32_t taddr, 
                                         __uint_as_float(v[2 * i + 1]));
                 const int col = n_idx * BN + c0;
                 __nv_bfloat16 *dst =
-                    reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * p.ld_out + col;
-                store_row_bf16(dst, pk, col, p.N_valid);
+                    reinterpret_cast<__nv_bfloat16 *>(out) + orow * ld_out + col;
+                store_row_bf16(dst, pk, col, n_valid);
             }
         }
     } else {
@@ -261,10 +314,10 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, uint32_t taddr, 
             }
             if (row_ok) {
                 const int col = n_idx * BN + c0;
-                float *dst = reinterpret_cast<float *>(p.out) + ks * p.part_stride + orow * p.ld_out + col;
+                float *dst = reinterpret_cast<float *>(out) + ks * p.part_stride + orow * ld_out + col;
                 // 16-byte stores when the whole chunk is in range and aligned
-                const bool vec = col + CH <= p.N_valid && ((p.ld_out | p.part_stride) & 3) == 0 &&
-                                 (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
+                const bool vec = col + CH <= n_valid && ((ld_out | p.part_stride) & 3) == 0 &&
+                                 (reinterpret_cast<uintptr_t>(out) & 15) == 0;
                 if (vec) {
 #pragma unroll
                     for (int i = 0; i < CH; i += 4)
@@ -274,7 +327,7 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, uint32_t taddr, 
                 } else {
 #pragma unroll
                     for (int i = 0; i < CH; ++i)
-                        if (col + i < p.N_valid)
+                        if (col + i < n_valid)
                             dst[i] = __uint_as_float(v[i]);
                 }
             }
@@ -285,7 +338,9 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, uint32_t taddr, 
 template <int BN, int NB, int EPI, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
-                   const __grid_constant__ CUtensorMap mB1, const TcParams p)
+                   const __grid_constant__ CUtensorMap mB1, const __grid_constant__ CUtensorMap sA,
+                   const __grid_constant__ CUtensorMap sB0, const __grid_constant__ CUtensorMap sB1,
+                   const TcParams p)
 {
     using S = TcShape<BN, NB, STAGES>;
     extern __shared__ uint8_t smem_raw[];
@@ -324,6 +379,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&mB0);
         if (NB == 2)
             tma_prefetch_desc(&mB1);
+        if (p.sh_tiles > 0) {
+            tma_prefetch_desc(&sA);
+            tma_prefetch_desc(&sB0);
+            if (NB == 2)
+                tma_prefetch_desc(&sB1);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, S::TMEM_COLS);
@@ -348,10 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // work units: tiles x reduction splits (unit u: tile u / ks_n, split u % ks_n)
     const int ks_n = p.ksplit > 1 ? p.ksplit : 1;
-    const int tiles_all = failed ? 0 : tile_count(p, s_mt) * ks_n;
+    const int tiles_all =
+        failed ? 0 : p.sh_tiles * (p.sh_ksplit > 1 ? p.sh_ksplit : 1) + tile_count(p, s_mt) * ks_n;
     const int G = balanced_workers(tiles_all, (int)gridDim.x);
     const int ntiles = (int)blockIdx.x < G ? tiles_all : 0;
-    const int nk_all = (p.K + 63) / 64;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -361,10 +422,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long fills = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < ntiles && ok; u += G) {
-                const int g = u / ks_n, ks = u - g * ks_n;
-                const int kb0 = ks * nk_all / ks_n, kb1 = (ks + 1) * nk_all / ks_n;
-                const TileInfo ti = tile_info(p, s_seg, s_mt, g);
-                const int b_row = ti.seg * p.b_seg_rows + ti.n_idx * BN;
+                const UnitInfo w = unit_info(p, s_seg, s_mt, u, ks_n);
+                const TileInfo &ti = w.ti;
+                const bool second = w.second;
+                const int kb0 = w.kb0, kb1 = w.kb1;
+                const int b_row = second ? ti.n_idx * BN : ti.seg * p.b_seg_rows + ti.n_idx * BN;
+                const CUtensorMap *ma = second ? &sA : &mA;
+                const CUtensorMap *mb0 = second ? &sB0 : &mB0;
+                const CUtensorMap *mb1 = second ? &sB1 : &mB1;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitLimitNs)) {
                         ok = false;
@@ -373,10 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *sa = smem + s * S::STAGE_BYTES;
                     uint8_t *sb = sa + S::A_BYTES;
                     mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
-                    tma_load_2d(sa, &mA, &full[s], kb * 64, ti.a_row0);
-                    tma_load_2d(sb, &mB0, &full[s], kb * 64, b_row);
+                    tma_load_2d(sa, ma, &full[s], kb * 64, ti.a_row0);
+                    tma_load_2d(sb, mb0, &full[s], kb * 64, b_row);
                     if (NB == 2)
-                        tma_load_2d(sb + S::B_BYTES, &mB1, &full[s], kb * 64, b_row);
+                        tma_load_2d(sb + S::B_BYTES, mb1, &full[s], kb * 64, b_row);
                     ++fills;
                     if (++s == STAGES) {
                         s = 0;
@@ -402,8 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0, b = 0, tph = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < ntiles && ok; u += G) {
-                const int ks = u % ks_n;
-                const int kb0 = ks * nk_all / ks_n, kb1 = (ks + 1) * nk_all / ks_n;
+                const UnitInfo w = unit_info(p, s_seg, s_mt, u, ks_n);
+                const int kb0 = w.kb0, kb1 = w.kb1;
                 if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
@@ -454,8 +519,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q * 32 + lane;        // accumulator row of this thread
         uint32_t b = 0, tph = 0;
         for (int u = blockIdx.x; u < ntiles; u += G) {
-            const int g = u / ks_n, ks = u - g * ks_n;
-            const TileInfo ti = tile_info(p, s_seg, s_mt, g);
+            const UnitInfo w = unit_info(p, s_seg, s_mt, u, ks_n);
+            const TileInfo &ti = w.ti;
+            const int ks = w.ks;
             if (!mbar_wait(&tfull[b], tph, abort_flag, kWaitLimitNs)) {
                 *abort_flag = 1;
                 set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
@@ -465,7 +531,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t taddr = tmem_base + b * S::UMMA_N + ((uint32_t)(q * 32) << 16);
             const bool row_ok = r < ti.rows;
             const long long orow = (long long)ti.a_row0 + r;
-            epilogue_row<BN, EPI>(p, taddr, row_ok, orow, ti.n_idx, ks);
+            if (w.second) {
+                if constexpr (EPI == EPI_BF16) {
+                    if (p.sh_ksplit > 1)  // fp32 partial sums of a piece of the reduction
+                        epilogue_row<BN, EPI_F32>(p, p.sh_out, p.sh_ld_out, p.sh_N_valid, taddr,
+                                                  row_ok, orow, ti.n_idx, ks);
+                    else
+                        epilogue_row<BN, EPI>(p, p.sh_out, p.sh_ld_out, p.sh_N_valid, taddr,
+                                              row_ok, orow, ti.n_idx, ks);
+                } else {
+                    epilogue_row<BN, EPI>(p, p.sh_out, p.sh_ld_out, p.sh_N_valid, taddr, row_ok,
+                                          orow, ti.n_idx, ks);
+                }
+            } else
+                epilogue_row<BN, EPI>(p, p.out, p.ld_out, p.N_valid, taddr, row_ok, orow,
+                                      ti.n_idx, ks);
             tc_fence_before_sync();
             mbar_arrive(&tempty[b]);
             b ^= 1u;
@@ -516,7 +596,6 @@ struct PairShape {
 };
 
 constexpr int kPairRows = 2 * kTileM;
-constexpr long long kPairMinRows = 16384;  // fewest routed GEMM rows for which pairs are used
 
 __device__ __forceinline__ int pair_tile_count(const TcParams &p, const int *s_mt)
 {
@@ -765,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int my_rows = ti.rows - (int)rank * kTileM;
             const bool row_ok = r < my_rows;
             const long long orow = (long long)ti.a_row0 + (int)rank * kTileM + r;
-            epilogue_row<BN, EPI>(p, taddr, row_ok, orow, ti.n_idx);
+            epilogue_row<BN, EPI>(p, p.out, p.ld_out, p.N_valid, taddr, row_ok, orow, ti.n_idx);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -825,9 +904,15 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t k, uint3
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The second problem's operands (TcParams::sh_tiles > 0).
+struct SecondMaps {
+    CUtensorMap a, b0, b1;
+};
+
 template <int BN, int NB, int EPI, int STAGES>
 cudaError_t launch_tc(const CUtensorMap &mA, const CUtensorMap &mB0, const CUtensorMap &mB1,
-                      const TcParams &p, long long max_tiles, cudaStream_t stream)
+                      const TcParams &p, long long max_tiles, cudaStream_t stream,
+                      const SecondMaps *second = nullptr)
 {
     using S = TcShape<BN, NB, STAGES>;
     auto kern = tc_gemm_kernel<BN, NB, EPI, STAGES>;
@@ -845,11 +930,13 @@ cudaError_t launch_tc(const CUtensorMap &mA, const CUtensorMap &mB0, const CUten
             return err;
         configured |= 1ull << dev;
     }
-    const long long grid = std::min<long long>(max_tiles, sm_count());
+    const long long grid =
+        std::min<long long>(max_tiles + (long long)p.sh_tiles * std::max(1, p.sh_ksplit), sm_count());
     if (grid < 1)
         return cudaSuccess;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), (size_t)S::SMEM_BYTES, stream,
-                      mA, mB0, mB1, p);
+                      mA, mB0, mB1, second ? second->a : mA, second ? second->b0 : mB0,
+                      second ? second->b1 : mB1, p);
 }
 
 // Launches the CTA-pair kernel as clusters of 2 (persistent: at most as
@@ -950,20 +1037,23 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
     const int32_t *seg = reinterpret_cast<const int32_t *>(ws + L.seg_off);
     const int32_t *mtile = reinterpret_cast<const int32_t *>(ws + L.mtile);
     void *xp = ws + L.x_perm, *h = ws + L.h, *z = ws + L.z;
+    void *hs = ws + L.hs, *zs = ws + L.zs;
     const long long R = L.R_max;
     const long long mt_bound = R / kTileM + E;     // >= sum_e ceil(kept_e / 128)
     const long long mt2_bound = R / kPairRows + E; // >= sum_e ceil(kept_e / 256)
+    const long long mt_s = (T + kTileM - 1) / kTileM, mt2_s = (T + kPairRows - 1) / kPairRows;
     const bool wide_down = D > 1024;              // 256-column tiles for the down projection
-    // CTA pairs (256-row tiles) for large problems whose segments average
-    // at least 512 rows; decode-sized and small batches keep single-CTA tiles
-    // (few rows would leave most of a 256-row tile empty, and small GEMMs are
-    // bound by latency, not by shared-memory traffic)
-    const long long routed_rows = (long long)T * c.top_k;
-    const bool pair_routed = routed_rows >= kPairMinRows && routed_rows >= 2LL * kPairRows * E;
-    const bool pair_shared = T >= kPairMinRows / 4;
+    const int bn_down = wide_down ? 256 : 128;
+    const LaunchPlan plan = plan_of(c);
+    const bool pair_routed = plan.pair_routed, pair_shared = plan.pair_shared;
+    // shared expert tiles in the routed launches (single-CTA kernels): they
+    // share the machine with the routed tiles instead of running alone on a
+    // few SMs (at decode sizes the shared GEMMs have only a handful of tiles)
+    const bool fused = plan.shared_fused;
     cudaError_t err;
 
     // GEMM1 (routed): h = silu(x_perm W_gate^T) * (x_perm W_up^T)
+    //   (+ fused: hs = silu(x Ws_gate^T) * (x Ws_up^T))
     {
         CUtensorMap mA, mG, mU;
         if (!make_map(&mA, xp, (uint64_t)R, (uint64_t)D, kTileM) ||
@@ -982,36 +1072,67 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
         p.ld_out = F;
         p.status = status;
         p.aux = aux;
+        SecondMaps sm;
+        if (fused) {
+            if (!make_map(&sm.a, x, (uint64_t)T, (uint64_t)D, kTileM) ||
+                !make_map(&sm.b0, Ws_gate, (uint64_t)S, (uint64_t)D, 128) ||
+                !make_map(&sm.b1, Ws_up, (uint64_t)S, (uint64_t)D, 128))
+                return cudaErrorInvalidValue;
+            p.sh_n_tiles = (S + 127) / 128;
+            p.sh_tiles = (int)(mt_s * p.sh_n_tiles);
+            p.sh_rows = T;
+            p.sh_K = D;
+            p.sh_N_valid = S;
+            p.sh_out = hs;
+            p.sh_ld_out = S;
+        }
         err = pair_routed
                   ? launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, mt2_bound * p.n_tiles,
                                                           stream)
-                  : launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_bound * p.n_tiles, stream);
+                  : launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_bound * p.n_tiles, stream,
+                                                     fused ? &sm : nullptr);
         if (err == cudaSuccess)
             err = record_stage(ev, 3, stream);
         if (err != cudaSuccess)
             return err;
     }
-    // GEMM2 (routed): z = h W_down^T
+    // GEMM2 (routed): z = h W_down^T  (+ fused: zs = hs Ws_down^T)
     {
-        const int bn = wide_down ? 256 : 128;
         CUtensorMap mA, mB;
         if (!make_map(&mA, h, (uint64_t)R, (uint64_t)F, kTileM) ||
             !make_map(&mB, W_down, (uint64_t)E * D, (uint64_t)F,
-                      (uint32_t)(pair_routed ? bn / 2 : bn)))
+                      (uint32_t)(pair_routed ? bn_down / 2 : bn_down)))
             return cudaErrorInvalidValue;
         TcParams p{};
         p.seg_off = seg;
         p.mtile = mtile;
         p.nseg = E;
         p.K = F;
-        p.n_tiles = (D + bn - 1) / bn;
+        p.n_tiles = (D + bn_down - 1) / bn_down;
         p.N_valid = D;
         p.b_seg_rows = D;
         p.out = z;
         p.ld_out = D;
         p.status = status;
+        SecondMaps sm;
+        if (fused) {
+            if (!make_map(&sm.a, hs, (uint64_t)T, (uint64_t)S, kTileM) ||
+                !make_map(&sm.b0, Ws_down, (uint64_t)D, (uint64_t)S, (uint32_t)bn_down))
+                return cudaErrorInvalidValue;
+            sm.b1 = sm.b0;
+            p.sh_n_tiles = p.n_tiles;
+            p.sh_tiles = (int)(mt_s * p.sh_n_tiles);
+            p.sh_rows = T;
+            p.sh_K = S;
+            p.sh_N_valid = D;
+            p.sh_out = zs;
+            p.sh_ld_out = D;
+            p.sh_ksplit = shared_down_splits(c);
+            p.part_stride = (long long)T * D;
+        }
+        const SecondMaps *second = fused ? &sm : nullptr;
         const long long tiles = (pair_routed ? mt2_bound : mt_bound) * p.n_tiles;
-        if (direct_y(c)) {
+        if (plan.direct_y) {
             p.out = y;
             p.row_tok = reinterpret_cast<const int32_t *>(ws + L.row_tok);
             p.row_w = reinterpret_cast<const float *>(ws + L.row_w);
@@ -1026,17 +1147,18 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
                 err = wide_down ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream)
                                 : launch_tc_pair<128, 1, EPI_BF16, 8>(mA, mB, mB, p, tiles, stream);
             else
-                err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, tiles, stream)
-                                : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream);
+                err = wide_down
+                          ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, tiles, stream, second)
+                          : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream, second);
         }
         if (err == cudaSuccess)
             err = record_stage(ev, 4, stream);
         if (err != cudaSuccess)
             return err;
     }
-    if (S > 0) {
-        void *hs = ws + L.hs, *zs = ws + L.zs;
-        const long long mt = (T + kTileM - 1) / kTileM;
+    if (S > 0 && !fused) {
+        // the shared expert on its own: CTA pairs for large T, else one CTA
+        // per tile
         {
             CUtensorMap mA, mG, mU;
             if (!make_map(&mA, x, (uint64_t)T, (uint64_t)D, kTileM) ||
@@ -1052,48 +1174,36 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.out = hs;
             p.ld_out = S;
             p.status = status;
-            const long long mt2 = (T + kPairRows - 1) / kPairRows;
             err = pair_shared
-                      ? launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, mt2 * p.n_tiles, stream)
-                      : launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt * p.n_tiles, stream);
+                      ? launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, mt2_s * p.n_tiles, stream)
+                      : launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_s * p.n_tiles, stream);
             if (err == cudaSuccess)
                 err = record_stage(ev, 5, stream);
             if (err != cudaSuccess)
                 return err;
         }
         {
-            const int bn = wide_down ? 256 : 128;
             CUtensorMap mA, mB;
             if (!make_map(&mA, hs, (uint64_t)T, (uint64_t)S, kTileM) ||
                 !make_map(&mB, Ws_down, (uint64_t)D, (uint64_t)S,
-                          (uint32_t)(pair_shared ? bn / 2 : bn)))
+                          (uint32_t)(pair_shared ? bn_down / 2 : bn_down)))
                 return cudaErrorInvalidValue;
             TcParams p{};
             p.nseg = 1;
             p.dense_rows = T;
             p.K = S;
-            p.n_tiles = (D + bn - 1) / bn;
+            p.n_tiles = (D + bn_down - 1) / bn_down;
             p.N_valid = D;
             p.out = zs;
             p.ld_out = D;
             p.status = status;
-            const long long mt2 = (T + kPairRows - 1) / kPairRows;
-            const int splits = shared_down_splits(c);
-            if (splits > 1) {
-                // decode-sized: fp32 partial sums per split of S, added by the combine
-                p.ksplit = splits;
-                p.part_stride = (long long)T * D;
-                const long long units = mt * p.n_tiles * splits;
-                err = wide_down ? launch_tc<256, 1, EPI_F32, 4>(mA, mB, mB, p, units, stream)
-                                : launch_tc<128, 1, EPI_F32, 6>(mA, mB, mB, p, units, stream);
-            } else if (pair_shared) {
+            if (pair_shared)
                 err = wide_down
-                          ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, mt2 * p.n_tiles, stream)
-                          : launch_tc_pair<128, 1, EPI_BF16, 8>(mA, mB, mB, p, mt2 * p.n_tiles, stream);
-            } else {
-                err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt * p.n_tiles, stream)
-                                : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt * p.n_tiles, stream);
-            }
+                          ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, mt2_s * p.n_tiles, stream)
+                          : launch_tc_pair<128, 1, EPI_BF16, 8>(mA, mB, mB, p, mt2_s * p.n_tiles, stream);
+            else
+                err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt_s * p.n_tiles, stream)
+                                : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt_s * p.n_tiles, stream);
             if (err == cudaSuccess)
                 err = record_stage(ev, 6, stream);
             if (err != cudaSuccess)

@@ -57,13 +57,29 @@ struct AuxArgs {
     float alpha;
 };
 
-// K-splits of the shared expert's down projection (bf16).  Decode-sized
-// batches give that GEMM only a few output tiles (one 128-row tile times
-// D / 256 column tiles), too few to keep the SMs streaming weights; its
-// reduction over S is then split so that about one work unit per SM results.
-// The splits write fp32 partial sums [splits][T][D], which the combine kernel
-// adds in split order.  1 = no split (bf16 output [T][D]).
+// Which kernels a forward pass on `c` launches (bf16 tensor-core path).
+struct LaunchPlan {
+    bool router_fused;  // router GEMM inside the dispatch kernel
+    bool direct_y;      // the down projection writes y (no combine kernel)
+    bool pair_routed;   // routed GEMMs on CTA pairs (256-row tiles)
+    bool pair_shared;   // shared-expert GEMMs on CTA pairs
+    bool shared_fused;  // shared-expert tiles inside the routed single-CTA launches
+    int router_splits;  // K-splits of the tensor-core router (1 = none)
+};
+// CTA pairs for large problems whose segments average at least 512 rows;
+// decode-sized and small batches keep single-CTA tiles (few rows would
+// leave most of a 256-row tile empty, and small GEMMs are bound by latency,
+// not by shared-memory traffic).
+constexpr long long kPairMinRows = 16384;  // fewest routed GEMM rows for pairs
+LaunchPlan plan_of(const moe_config &c);
+
+// K-splits of the shared expert's down projection when its tiles run inside
+// the routed launch: a tile reduces over S while a routed tile reduces over
+// F, so S is cut into ceil(S / F) pieces (at most 8) to give every work unit
+// about the same length.  The pieces write fp32 partial sums [splits][T][D]
+// that the combine kernel adds in split order.  1 = no split (bf16 [T][D]).
 int shared_down_splits(const moe_config &c);
+constexpr int kMaxSharedSplits = 8;
 
 // K-splits of the tensor-core router GEMM.  Batches below 512 tokens give
 // it one to four 128-row tiles, so its reduction over d_model is split

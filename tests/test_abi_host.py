@@ -174,3 +174,20 @@ def test_sharded_entry_points_validate_on_the_host():
     assert route(r, ws_bytes=need - 1) == B.MOE_ERR_WORKSPACE
     misaligned_x = [4096 + 8] + r[1:]
     assert route(misaligned_x) == B.MOE_ERR_INVALID_ARG
+
+
+def test_launch_plan():
+    plan = lambda name: B.launch_plan(B.config_of(WORKLOADS[name]))
+    sw = plan("switch_top1_capacity")
+    assert sw["router_fused"] and sw["direct_y"] and not sw["shared_fused"]
+    # decode-sized layers run the shared expert's tiles inside the routed launches
+    for name in ("qwen2_57b_decode", "dsv3_decode"):
+        p = plan(name)
+        assert p["shared_fused"] and not p["pair_routed"] and not p["pair_shared"], name
+    # large layers: CTA pairs, shared expert in its own launches
+    q = plan("qwen2_57b_prefill")
+    assert q["pair_shared"] and not q["shared_fused"]
+    assert plan("mixtral_prefill")["pair_routed"]
+    assert not plan("mixtral_decode")["pair_routed"]
+    with pytest.raises(B.MoeError):
+        B.launch_plan(B.make_config(64, 128, 8, 128, 0))

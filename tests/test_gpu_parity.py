@@ -23,9 +23,12 @@ SMALL = [
     ("top1_heavy_drops", 1536, 256, 8, 256, 1, 128, 1, 0.5, "normal_var2"),
     ("k_equals_e", 640, 128, 4, 192, 4, 0, 0, 0.0, "none"),
     ("ragged_chunk_t33", 33, 128, 8, 128, 2, 64, 0, 1.25, "none"),
-    # small batch, wide d_model: the router GEMM and the shared expert's down
-    # projection both split their reductions (fp32 partial sums)
+    # small batch, wide d_model: the router GEMM splits its reduction (fp32
+    # partial sums) and the shared expert's tiles run inside the routed GEMMs
     ("split_router_and_shared", 200, 1024, 32, 128, 4, 2048, 2, 0.0, "zipf1.1"),
+    # wide down projection (256-column tiles) with fused shared tiles whose
+    # rows (T = 300) span three row tiles and whose S is not a multiple of 128
+    ("fused_shared_wide_down", 300, 1088, 16, 192, 2, 320, 1, 1.0, "normal_var2"),
 ]
 
 # Large enough for the CTA-pair GEMMs (>= 16384 rows and >= 512 rows per
