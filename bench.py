@@ -141,17 +141,22 @@ class ClockSampler:
 def stage_work(w, kept_total, touched, shared_fused=False):
     """Algorithmic (flops, bytes) of each stage of one forward pass.  With the
     shared expert's tiles inside the routed GEMM launches (shared_fused), the
-    routed stages carry the shared work and the shared stages are empty."""
+    routed stages carry the shared work and the shared stages are empty.
+    E4M3 expert weights count 1 byte per weight plus a 4-byte scale per row."""
     b = 2 if w.dtype == "bf16" else 4
     D, F, S, T, E, k = w.D, w.F, w.S, w.T, w.E, w.k
+
+    def wbytes(rows, cols):
+        return rows * cols + 4 * rows if w.weights == "e4m3" else b * rows * cols
+
     work = {
         "router": (2 * T * D * E, b * (T * D + E * D) + 4 * T * E),
         "gemm1_routed": (4 * D * F * kept_total,
-                         b * (2 * F * D * touched + kept_total * D + kept_total * F)),
+                         touched * wbytes(2 * F, D) + b * (kept_total * D + kept_total * F)),
         "gemm2_routed": (2 * D * F * kept_total,
-                         b * (F * D * touched + kept_total * F + kept_total * D)),
-        "gemm1_shared": (4 * D * S * T, b * (2 * S * D + T * D + T * S)),
-        "gemm2_shared": (2 * D * S * T, b * (S * D + T * S + T * D)),
+                         touched * wbytes(D, F) + b * (kept_total * F + kept_total * D)),
+        "gemm1_shared": (4 * D * S * T, wbytes(2 * S, D) + b * (T * D + T * S)),
+        "gemm2_shared": (2 * D * S * T, wbytes(D, S) + b * (T * S + T * D)),
         "dispatch": (0, b * (T * D + kept_total * D)),
         "combine": (0, b * (kept_total * D + (T * D if S else 0) + T * D)),
     }
@@ -211,7 +216,19 @@ def oracle_rate(w, inputs, budget_s=12.0, min_tokens=16):
         shared = (f32(inputs["Ws_gate"]), f32(inputs["Ws_up"]), f32(inputs["Ws_down"]))
     gamma = float(np.float32(w.gamma))
 
-    if full_weight_bytes <= (6 << 30):
+    e4m3 = w.weights == "e4m3"
+    if e4m3 and shared is not None:
+        # the oracle's own E4M3 codes of the same bf16 weights (untimed)
+        shared = tuple(a for W in shared for a in oracle.quantize_e4m3_rows(W))
+
+    def expert(e):
+        Ws = (f32(inputs["W_gate"][e]), f32(inputs["W_up"][e]), f32(inputs["W_down"][e]))
+        return tuple(a for W in Ws for a in oracle.quantize_e4m3_rows(W)) if e4m3 else Ws
+
+    def rows_fn(xr, ws):
+        return oracle.swiglu_rows_q8(xr, *ws) if len(ws) == 6 else oracle.swiglu_rows(xr, *ws)
+
+    if full_weight_bytes <= (6 << 30) and not e4m3:
         Wg, Wu, Wd = f32(inputs["W_gate"]), f32(inputs["W_up"]), f32(inputs["W_down"])
         sh = {} if shared is None else dict(Ws_gate=shared[0], Ws_up=shared[1],
                                             Ws_down=shared[2])
@@ -242,27 +259,30 @@ def oracle_rate(w, inputs, budget_s=12.0, min_tokens=16):
         dropped, _ = oracle.apply_capacity(idx, w.E, oracle.capacity(n, w.k, w.E, gamma))
         spent = time.perf_counter() - t0
         for e in sorted(set(idx[dropped == 0].ravel().tolist())):
-            Wg, Wu, Wd = f32(inputs["W_gate"][e]), f32(inputs["W_up"][e]), f32(inputs["W_down"][e])
+            ws = expert(e)
             rows = np.nonzero(((idx == e) & (dropped == 0)).any(1))[0]
             t0 = time.perf_counter()
-            oracle.swiglu_rows(xs[rows], Wg, Wu, Wd)
+            rows_fn(xs[rows], ws)
             spent += time.perf_counter() - t0
         if shared is not None:
             t0 = time.perf_counter()
-            oracle.swiglu_rows(xs, *shared)
+            rows_fn(xs, shared)
             spent += time.perf_counter() - t0
         return spent
 
     n = min(T, 8)
     dt = run_sampled(n)
     note = (f"first {n} of {T} tokens: router, gating and capacity over the sample, then each "
-            f"touched expert and the shared expert in the fp64 oracle (weight copies untimed)")
+            f"touched expert and the shared expert in the fp64 oracle (weight copies"
+            f"{' and the oracle E4M3 quantization' if e4m3 else ''} untimed)")
     return n / dt, note, n
 
 
 # ------------------------------------------------------------------ arms
 def workload_config(w, l2_note):
     extra = {"latent_from_d_model": w.D_outer} if w.D_outer else {}
+    if w.weights == "e4m3":
+        extra["expert_weights"] = "e4m3, one fp32 scale per weight row (bf16 activations)"
     return {**extra, "workload": w.name, "T": w.T, "d_model": w.D, "n_experts": w.E, "d_expert": w.F,
             "top_k": w.k, "d_shared": w.S, "gating": GATING[w.mode],
             "capacity_factor": w.gamma if w.gamma > 0 else None,
@@ -275,6 +295,10 @@ def run_ours(args, rank, world, device):
     torch.cuda.set_device(device)
     cfg = B.config_of(w)
     inputs = make_inputs(w, args.seed + rank, device)
+    bf16_inputs = inputs
+    if w.weights == "e4m3":
+        # the stored weights are E4M3 (quantized once by the library, untimed)
+        inputs = B.quantize_expert_weights(bf16_inputs)
     outs = B.alloc_outputs(cfg, device, w.D_outer)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
@@ -411,7 +435,8 @@ def run_ours(args, rank, world, device):
 
     # whole-layer roofline (slower of algorithmic FLOPs at TC peak and bytes at HBM)
     lf = RL.layer_flops(w.T, w.D, w.E, w.F, w.S, kept_total)
-    lb = RL.layer_bytes(w.T, w.D, w.E, w.F, w.S, touched, 2 if w.dtype == "bf16" else 4)
+    lb = RL.layer_bytes(w.T, w.D, w.E, w.F, w.S, touched, 2 if w.dtype == "bf16" else 4,
+                        weight_bytes=1 if w.weights == "e4m3" else None)
     if w.D_outer:
         # the latent layer's two projections: 2*T*D_outer*D FLOPs and D_outer*D
         # weights each; x and y at the outer width instead of the latent one
@@ -480,7 +505,7 @@ def run_ours(args, rank, world, device):
         "wall_s_timed_loop": wall,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, note, n = oracle_rate(w, inputs, budget_s=args.cpu_budget_s)
+        rate, note, n = oracle_rate(w, bf16_inputs, budget_s=args.cpu_budget_s)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": _omp_threads(),
                                 "kind": "oracle", "sample": note}
     return line
@@ -501,7 +526,7 @@ def run_reference(args, world):
     def f32(t):
         return t.detach().float().cpu().numpy()
 
-    small = 4 * (3 * w.E * w.D * w.F + 3 * w.D * w.S) <= (6 << 30)
+    small = 4 * (3 * w.E * w.D * w.F + 3 * w.D * w.S) <= (6 << 30) and w.weights != "e4m3"
     if small:
         args_w = dict(k=w.k, mode=w.mode, gamma=float(np.float32(w.gamma)), alpha=w.alpha,
                       bias=None if inputs.get("b_r") is None else f32(inputs["b_r"]),

@@ -201,6 +201,55 @@ MOE_API moe_status moe_latent_forward(const moe_config *cfg, int32_t d_outer,
                        float *aux_loss, void *workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* ---- e4m3 (FP8) expert weights for decode-sized batches.
+ *
+ * At small T the expert GEMMs are bound by the bytes of the touched expert
+ * weights ("Mixture of Experts: More Parameters, Same FLOPs", 'What experts
+ * cost at serving time': decoding reads each weight for ~2 FLOPs, and serving
+ * memory is sized at 8 bits per weight).  These entry points store every
+ * routed and shared expert weight matrix as e4m3 codes with one fp32 scale
+ * per weight row (output feature): W[r][c] = decode(q[r][c]) * scale[r].
+ * Activations, the router and all accumulation stay as in moe_forward (bf16
+ * inputs, fp32 accumulation); the e4m3 values enter the tensor cores exactly
+ * (every e4m3 value is a bf16 value). */
+
+/* Row-wise quantization of a bf16 matrix W [rows, cols] (device, row-major):
+ *   scale[r] = max_c |W[r][c]| / 448 in fp32 (1 when the row is all zero),
+ *   q[r][c]  = e4m3(W[r][c] / scale[r]): fp32 division, round to nearest
+ *              even, saturating to +-448 (OCP FP8 E4M3, no infinities).
+ * q [rows, cols] uint8 and scale [rows] fp32 are device outputs.  W and q
+ * 16-byte aligned, cols a multiple of 16 (MOE_ERR_INVALID_ARG otherwise).
+ * Stacked expert weights [E, n, m] are rows = E*n, cols = m. */
+MOE_API moe_status moe_quantize_e4m3_rows(int64_t rows, int64_t cols, const void *W,
+                                          uint8_t *q, float *scale, cudaStream_t stream);
+
+/* The forward pass of moe_forward with e4m3 expert weights (cfg->dtype must
+ * be MOE_DTYPE_BF16, else MOE_ERR_UNSUPPORTED):
+ *   W_gate_q, W_up_q [E, d_expert, d_model], W_down_q [E, d_model, d_expert]
+ *   uint8 (16-byte aligned); W_gate_scale, W_up_scale [E * d_expert],
+ *   W_down_scale [E * d_model] fp32; likewise Ws_*_q / Ws_*_scale for the
+ *   shared expert ([d_shared, d_model] / [d_model, d_shared], scales
+ *   [d_shared] / [d_model]; all NULL when d_shared == 0).
+ * Every other argument, output and convention is that of moe_forward, with
+ * the same workspace size (moe_workspace_size).  The expert GEMMs run one
+ * tensor-core kernel per projection with the weights as the operand held in
+ * tensor memory, sized for batches of up to a few hundred tokens; larger
+ * batches are correct but stream each weight tile once per 64 rows of an
+ * expert. */
+MOE_API moe_status moe_forward_w8(const moe_config *cfg,
+                       const void *x, const void *W_r, const float *router_bias,
+                       const uint8_t *W_gate_q, const float *W_gate_scale,
+                       const uint8_t *W_up_q, const float *W_up_scale,
+                       const uint8_t *W_down_q, const float *W_down_scale,
+                       const uint8_t *Ws_gate_q, const float *Ws_gate_scale,
+                       const uint8_t *Ws_up_q, const float *Ws_up_scale,
+                       const uint8_t *Ws_down_q, const float *Ws_down_scale,
+                       void *y, float *router_logits, int32_t *topk_idx,
+                       float *topk_w, uint8_t *dropped_mask,
+                       int32_t *expert_counts, int32_t *kept_counts,
+                       float *aux_loss, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
 /* ---- One batch split over several ranks (data parallel), same results as
  * one moe_forward over the whole batch.
  *

@@ -80,6 +80,10 @@ def lib():
         L.moe_latent_forward.argtypes = [cfgp, ctypes.c_int32] + [vp] * 20 + [ctypes.c_size_t,
                                                                               vp]
         L.moe_latent_forward.restype = ctypes.c_int
+        L.moe_quantize_e4m3_rows.argtypes = [ctypes.c_int64, ctypes.c_int64, vp, vp, vp, vp]
+        L.moe_quantize_e4m3_rows.restype = ctypes.c_int
+        L.moe_forward_w8.argtypes = [cfgp] + [vp] * 24 + [ctypes.c_size_t, vp]
+        L.moe_forward_w8.restype = ctypes.c_int
         L.moe_sharded_workspace_size.argtypes = [cfgp, ctypes.c_int64,
                                                  ctypes.POINTER(ctypes.c_size_t)]
         L.moe_sharded_workspace_size.restype = ctypes.c_int
@@ -207,6 +211,52 @@ def moe_forward_no_alloc(cfg: MoeConfig, x, W_r, router_bias, W_gate, W_up, W_do
                                     _stream(stream))
     if st != MOE_OK:
         raise MoeError(st, "moe_forward_no_alloc")
+
+
+W8_KEYS = ("W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down")
+
+
+def quantize_e4m3_rows(W: torch.Tensor, stream=None):
+    """Row-wise E4M3 codes and fp32 scales of a bf16 device tensor whose last
+    dimension is the row (moe_quantize_e4m3_rows): returns (q uint8 of W's
+    shape, scale fp32 of W's shape without the last dimension)."""
+    if W.dtype != torch.bfloat16 or not W.is_contiguous():
+        raise ValueError("quantize_e4m3_rows wants a contiguous bf16 tensor")
+    cols = int(W.shape[-1])
+    rows = W.numel() // cols
+    q = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
+    s = torch.empty(W.shape[:-1], dtype=torch.float32, device=W.device)
+    st = lib().moe_quantize_e4m3_rows(rows, cols, _ptr(W), _ptr(q), _ptr(s), _stream(stream))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_quantize_e4m3_rows")
+    return q, s
+
+
+def quantize_expert_weights(inputs: dict, stream=None) -> dict:
+    """A copy of `inputs` whose expert weights (routed and shared) are E4M3:
+    keys W_gate_q / W_gate_s, ... replace W_gate, ..."""
+    out = {k: v for k, v in inputs.items() if k not in W8_KEYS}
+    for k in W8_KEYS:
+        W = inputs.get(k)
+        q, s = (None, None) if W is None else quantize_e4m3_rows(W, stream)
+        out[k + "_q"], out[k + "_s"] = q, s
+    return out
+
+
+def moe_forward_w8(cfg: MoeConfig, x, W_r, router_bias, W_gate_q, W_gate_s, W_up_q, W_up_s,
+                   W_down_q, W_down_s, Ws_gate_q, Ws_gate_s, Ws_up_q, Ws_up_s, Ws_down_q,
+                   Ws_down_s, y, router_logits, topk_idx, topk_w, dropped_mask, expert_counts,
+                   kept_counts, aux_loss, workspace, workspace_bytes=None, stream=None) -> None:
+    """Same arguments as the C function."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    args = [x, W_r, router_bias, W_gate_q, W_gate_s, W_up_q, W_up_s, W_down_q, W_down_s,
+            Ws_gate_q, Ws_gate_s, Ws_up_q, Ws_up_s, Ws_down_q, Ws_down_s, y, router_logits,
+            topk_idx, topk_w, dropped_mask, expert_counts, kept_counts, aux_loss, workspace]
+    st = lib().moe_forward_w8(ctypes.byref(cfg), *[_ptr(a) for a in args],
+                              ctypes.c_size_t(int(workspace_bytes)), _stream(stream))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_forward_w8")
 
 
 def latent_workspace_size(cfg: MoeConfig, d_outer: int) -> int:
@@ -338,10 +388,18 @@ def alloc_outputs(cfg: MoeConfig, device="cuda", d_outer: int = 0):
 def forward(cfg: MoeConfig, inputs: dict, outs: dict | None = None, stream=None) -> dict:
     """Runs the layer on `inputs` (keys as workloads.make_inputs returns) and
     returns the output dict (allocated if not given).  Inputs with W_in and
-    W_out run the latent layer (moe_latent_forward)."""
+    W_out run the latent layer (moe_latent_forward); inputs with E4M3 expert
+    weights (quantize_expert_weights) run moe_forward_w8."""
     d_outer = int(inputs["x"].shape[1]) if inputs.get("W_in") is not None else 0
     if outs is None:
         outs = alloc_outputs(cfg, inputs["x"].device, d_outer)
+    if inputs.get("W_gate_q") is not None:
+        moe_forward_w8(cfg, inputs["x"], inputs["W_r"], inputs.get("b_r"),
+                       *[inputs.get(k + sfx) for k in W8_KEYS for sfx in ("_q", "_s")],
+                       outs["y"], outs["router_logits"], outs["topk_idx"], outs["topk_w"],
+                       outs["dropped_mask"], outs["expert_counts"], outs["kept_counts"],
+                       outs["aux_loss"], outs["workspace"], stream=stream)
+        return outs
     if d_outer:
         moe_latent_forward(cfg, d_outer, inputs["x"], inputs["W_in"], inputs["W_out"],
                            inputs["W_r"], inputs.get("b_r"), inputs["W_gate"], inputs["W_up"],

@@ -242,10 +242,12 @@ moe_status expert_step(const moe_config &c, const WorkspaceLayout &L, uint8_t *w
                        const void *W_gate, const void *W_up, const void *W_down,
                        const void *Ws_gate, const void *Ws_up, const void *Ws_down, void *y,
                        const float *topk_w, const AuxArgs &aux, cudaEvent_t *ev,
-                       cudaStream_t stream)
+                       cudaStream_t stream, const ExpertW8 *w8)
 {
     cudaError_t err;
-    if (c.dtype == MOE_DTYPE_BF16)
+    if (w8)
+        err = launch_experts_w8(c, L, ws, x, *w8, y, aux, stream, ev);
+    else if (c.dtype == MOE_DTYPE_BF16)
         err = launch_experts_tc(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y,
                                 aux, stream, ev);
     else
@@ -273,7 +275,8 @@ moe_status forward_body(const moe_config &c, const WorkspaceLayout &L, uint8_t *
                         const void *Ws_gate, const void *Ws_up, const void *Ws_down, void *y,
                         float *router_logits, int32_t *topk_idx, float *topk_w,
                         uint8_t *dropped_mask, int32_t *expert_counts, int32_t *kept_counts,
-                        float *aux_loss, bool clear_status, cudaStream_t stream)
+                        float *aux_loss, bool clear_status, cudaStream_t stream,
+                        const ExpertW8 *w8)
 {
     int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
     const int E = c.n_experts;
@@ -300,7 +303,7 @@ moe_status forward_body(const moe_config &c, const WorkspaceLayout &L, uint8_t *
     aux.k = c.top_k;
     aux.alpha = c.aux_alpha;
     return expert_step(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y, topk_w,
-                       aux, ev, stream);
+                       aux, ev, stream, w8);
 }
 
 }  // namespace moe
@@ -576,7 +579,78 @@ moe_status moe_sharded_finish(const moe_config *cfg, int64_t T_global, int32_t n
     if (st != MOE_OK)
         return st;
     return expert_step(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y, topk_w,
-                       aux, nullptr, stream);
+                       aux, nullptr, stream, nullptr);
+}
+
+// ---- e4m3 expert weights
+
+moe_status moe_quantize_e4m3_rows(int64_t rows, int64_t cols, const void *W, uint8_t *q,
+                                  float *scale, cudaStream_t stream)
+{
+    if (rows < 0 || cols < 1 || cols % 16 || rows * cols >= (1ll << 40))
+        return MOE_ERR_INVALID_ARG;
+    if (rows == 0)
+        return MOE_OK;
+    if (!W || !q || !scale || !aligned16(W) || !aligned16(q) ||
+        (reinterpret_cast<uintptr_t>(scale) & 3u))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_ok(launch_quantize_e4m3(rows, cols, W, q, scale, stream)) ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_forward_w8(const moe_config *cfg, const void *x, const void *W_r,
+                          const float *router_bias, const uint8_t *W_gate_q,
+                          const float *W_gate_scale, const uint8_t *W_up_q,
+                          const float *W_up_scale, const uint8_t *W_down_q,
+                          const float *W_down_scale, const uint8_t *Ws_gate_q,
+                          const float *Ws_gate_scale, const uint8_t *Ws_up_q,
+                          const float *Ws_up_scale, const uint8_t *Ws_down_q,
+                          const float *Ws_down_scale, void *y, float *router_logits,
+                          int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
+                          int32_t *expert_counts, int32_t *kept_counts, float *aux_loss,
+                          void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    moe_status st = validate_config(cfg);
+    if (st != MOE_OK)
+        return st;
+    const moe_config &c = *cfg;
+    if (c.dtype != MOE_DTYPE_BF16)
+        return MOE_ERR_UNSUPPORTED;
+    if (!expert_counts || !kept_counts || !aux_loss)
+        return MOE_ERR_INVALID_ARG;
+    const bool shared = c.d_shared > 0;
+    if (c.T > 0) {
+        if (!x || !W_r || !W_gate_q || !W_gate_scale || !W_up_q || !W_up_scale || !W_down_q ||
+            !W_down_scale || !y || !router_logits || !topk_idx || !topk_w || !dropped_mask)
+            return MOE_ERR_INVALID_ARG;
+        if (shared && (!Ws_gate_q || !Ws_gate_scale || !Ws_up_q || !Ws_up_scale || !Ws_down_q ||
+                       !Ws_down_scale))
+            return MOE_ERR_INVALID_ARG;
+        if (!aligned16(x) || !aligned16(W_r) || !aligned16(y) || !aligned16(W_gate_q) ||
+            !aligned16(W_up_q) || !aligned16(W_down_q) ||
+            (shared && (!aligned16(Ws_gate_q) || !aligned16(Ws_up_q) || !aligned16(Ws_down_q))))
+            return MOE_ERR_INVALID_ARG;
+    }
+    const WorkspaceLayout L = layout_of(cfg);
+    if (!workspace || workspace_bytes < L.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MOE_ERR_WORKSPACE;
+    ExpertW8 w{};
+    w.gate = W_gate_q;
+    w.up = W_up_q;
+    w.down = W_down_q;
+    w.gate_s = W_gate_scale;
+    w.up_s = W_up_scale;
+    w.down_s = W_down_scale;
+    w.sgate = Ws_gate_q;
+    w.sup = Ws_up_q;
+    w.sdown = Ws_down_q;
+    w.sgate_s = Ws_gate_scale;
+    w.sup_s = Ws_up_scale;
+    w.sdown_s = Ws_down_scale;
+    return forward_body(c, L, static_cast<uint8_t *>(workspace), x, W_r, router_bias, nullptr,
+                        nullptr, nullptr, nullptr, nullptr, nullptr, y, router_logits, topk_idx,
+                        topk_w, dropped_mask, expert_counts, kept_counts, aux_loss, true, stream,
+                        &w);
 }
 
 moe_status moe_read_device_status(const moe_config *cfg, const void *workspace,

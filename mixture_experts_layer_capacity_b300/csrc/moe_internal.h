@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/moe.h"
@@ -175,6 +176,31 @@ cudaError_t launch_dense_tc(int rows, int N, int K, const void *A, const void *B
 cudaError_t launch_dense_simt(int rows, int N, int K, const float *A, const float *B, float *out,
                               const int32_t *status, cudaStream_t stream);
 
+// Tensor maps for TMA (moe_gemm_tc.cu): a bf16 [rows, k] tensor in boxes of
+// 64 x box_rows with 128-byte swizzle, and a byte (e4m3) [rows, k] tensor in
+// boxes of 64 x box_rows with 64-byte swizzle.  false: cannot be encoded.
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t k, uint32_t box_rows);
+bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t k, uint32_t box_rows);
+
+// e4m3 expert weights with one fp32 scale per weight row (output feature):
+// W[r][c] = decode(q[r][c]) * scale[r].  Shared-expert fields null when
+// d_shared == 0.
+struct ExpertW8 {
+    const uint8_t *gate, *up, *down;        // [E,F,D], [E,F,D], [E,D,F]
+    const float *gate_s, *up_s, *down_s;    // [E*F], [E*F], [E*D]
+    const uint8_t *sgate, *sup, *sdown;     // [S,D], [S,D], [D,S]
+    const float *sgate_s, *sup_s, *sdown_s; // [S], [S], [D]
+};
+// The routed and shared SwiGLU experts with e4m3 weights (moe_gemm_w8.cu);
+// `ev`: stage events 3..6 as in launch_experts_tc.
+cudaError_t launch_experts_w8(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                              const void *x, const ExpertW8 &w, void *y, const AuxArgs &aux,
+                              cudaStream_t stream, cudaEvent_t *ev = nullptr);
+// q[r][c] = e4m3(W[r][c] / scale[r]), scale[r] = max_c |W[r][c]| / 448
+// (moe_gemm_w8.cu).
+cudaError_t launch_quantize_e4m3(long long rows, long long cols, const void *W, uint8_t *q,
+                                 float *scale, cudaStream_t stream);
+
 // The layer on a validated config and workspace (moe_api.cu).
 moe_status forward_body(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                         const void *x, const void *W_r, const float *router_bias,
@@ -182,7 +208,8 @@ moe_status forward_body(const moe_config &c, const WorkspaceLayout &L, uint8_t *
                         const void *Ws_gate, const void *Ws_up, const void *Ws_down, void *y,
                         float *router_logits, int32_t *topk_idx, float *topk_w,
                         uint8_t *dropped_mask, int32_t *expert_counts, int32_t *kept_counts,
-                        float *aux_loss, bool clear_status, cudaStream_t stream);
+                        float *aux_loss, bool clear_status, cudaStream_t stream,
+                        const ExpertW8 *w8 = nullptr);
 
 int sm_count();
 

@@ -45,9 +45,16 @@ def layer_flops(T: int, D: int, E: int, F: int, S: int, kept_total: int) -> int:
     return 6 * D * F * kept_total + 6 * D * S * T + 2 * T * D * E
 
 
-def layer_bytes(T: int, D: int, E: int, F: int, S: int, touched: int, b: int) -> int:
-    """Algorithmic HBM bytes: touched expert weights, shared weights, router, x, y."""
-    return b * (3 * D * F * touched + 3 * D * S + D * E + 2 * T * D)
+def layer_bytes(T: int, D: int, E: int, F: int, S: int, touched: int, b: int,
+                weight_bytes: int | None = None) -> int:
+    """Algorithmic HBM bytes: touched expert weights, shared weights, router, x, y.
+    weight_bytes: bytes per expert weight when they are stored narrower than
+    the activations (1 for E4M3, plus a 4-byte scale per weight row)."""
+    if weight_bytes is None:
+        return b * (3 * D * F * touched + 3 * D * S + D * E + 2 * T * D)
+    expert = weight_bytes * (3 * D * F * touched + 3 * D * S) + \
+        4 * ((2 * F + D) * touched + (2 * S + D if S else 0))
+    return expert + b * (D * E + 2 * T * D)
 
 
 def expert_flops(D: int, F: int, S: int, T: int, kept_total: int) -> int:

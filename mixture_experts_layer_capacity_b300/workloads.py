@@ -49,6 +49,8 @@ class Workload:
     bias: str = "none"    # router logit bias: "none", "normal_var2", "zipf1.1"
     sel_bias: bool = False  # the bias shifts only the top-k selection keys
     D_outer: int = 0      # latent MoE: outer width (x and y); 0 = plain layer
+    weights: str = "bf16"  # expert weight storage: "bf16", or "e4m3" (row-scaled FP8,
+                           # quantized from the same seeded bf16 weights)
     description: str = ""
 
     def with_T(self, T: int) -> "Workload":
@@ -102,6 +104,19 @@ WORKLOADS = {
         "latent_decode", T=64, D=1024, E=64, F=2048, k=8, D_outer=4096,
         mode=GATING_SOFTMAX_ALL_RENORM,
         description="latent MoE: 4096 -> 1024, 64 experts d=2048, top-8, -> 4096, T=64"),
+    # the decode shapes with E4M3 expert weights (one fp32 scale per weight row)
+    "mixtral_decode_fp8": Workload(
+        "mixtral_decode_fp8", T=64, D=4096, E=8, F=14336, k=2,
+        mode=GATING_SOFTMAX_SELECTED, weights="e4m3",
+        description="Mixtral-8x7B-shaped, T=64, E4M3 expert weights"),
+    "qwen2_57b_decode_fp8": Workload(
+        "qwen2_57b_decode_fp8", T=64, D=3584, E=64, F=2560, k=8, S=20480,
+        mode=GATING_SOFTMAX_ALL, weights="e4m3",
+        description="Qwen2-57B-A14B-shaped, T=64, E4M3 expert weights"),
+    "dsv3_decode_fp8": Workload(
+        "dsv3_decode_fp8", T=64, D=7168, E=256, F=2048, k=8, S=2048,
+        mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1", weights="e4m3",
+        description="DeepSeek-V3-shaped, T=64, E4M3 expert weights"),
     "dsv3_sigmoid_decode": Workload(
         "dsv3_sigmoid_decode", T=64, D=7168, E=256, F=2048, k=8, S=2048,
         mode=GATING_SIGMOID_SELECTED, bias="zipf1.1", sel_bias=True,

@@ -78,6 +78,14 @@ def _load():
         lib.oracle_latent_forward.argtypes = (
             [i64, i64, i64, i64, i64, i64, i64, i32, f64, f64, i32] + [vp] * 11 + [vp] * 9)
         lib.oracle_latent_forward.restype = i32
+        lib.oracle_e4m3_decode.argtypes = [i64, vp, vp]
+        lib.oracle_e4m3_decode.restype = None
+        lib.oracle_e4m3_encode.argtypes = [i64, vp, vp]
+        lib.oracle_e4m3_encode.restype = None
+        lib.oracle_quantize_e4m3_rows.argtypes = [i64, i64, vp, vp, vp]
+        lib.oracle_quantize_e4m3_rows.restype = None
+        lib.oracle_swiglu_rows_q8.argtypes = [i64, i64, i64] + [vp] * 8
+        lib.oracle_swiglu_rows_q8.restype = i32
         _lib = lib
         return lib
 
@@ -232,13 +240,63 @@ def latent_forward(x, W_in, W_out, W_r, W_gate, W_up, W_down, *, k, mode, gamma=
     return out
 
 
+def e4m3_decode(codes):
+    """Values (fp64) of E4M3 codes (uint8 array of any shape)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_e4m3_decode(c.size, _ptr(c), _ptr(out))
+    return out
+
+
+def e4m3_encode(values):
+    """E4M3 codes of fp32 values: round to nearest even, saturating."""
+    v = _f32(values)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode(v.size, _ptr(v), _ptr(out))
+    return out
+
+
+def quantize_e4m3_rows(W):
+    """Row-wise E4M3 quantization of W [rows, cols] (fp32 values): returns
+    (codes uint8 [rows, cols], scales fp32 [rows])."""
+    W = _f32(W)
+    rows, cols = W.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    s = np.empty(rows, dtype=np.float32)
+    _load().oracle_quantize_e4m3_rows(rows, cols, _ptr(W), _ptr(q), _ptr(s))
+    return q, s
+
+
+def swiglu_rows_q8(x_rows, qg, sg, qu, su, qd, sd):
+    """swiglu_rows with E4M3 weights: codes qg, qu [F, D], qd [D, F] and row
+    scales sg, su [F], sd [D] -> f64 [n, D]."""
+    x_rows = _f64(x_rows)
+    qg, qu, qd = (np.ascontiguousarray(a, dtype=np.uint8) for a in (qg, qu, qd))
+    sg, su, sd = _f32(sg), _f32(su), _f32(sd)
+    n, D = x_rows.shape
+    F = qg.shape[0]
+    out = np.empty((n, D), dtype=np.float64)
+    _check(_load().oracle_swiglu_rows_q8(n, D, F, _ptr(x_rows), _ptr(qg), _ptr(sg), _ptr(qu),
+                                         _ptr(su), _ptr(qd), _ptr(sd), _ptr(out)))
+    return out
+
+
+def _expert_rows(x_rows, weights):
+    """One expert on rows: weights = (Wg, Wu, Wd) fp32, or the six arrays
+    (qg, sg, qu, su, qd, sd) of E4M3 weights."""
+    if len(weights) == 6:
+        return swiglu_rows_q8(x_rows, *weights)
+    return swiglu_rows(x_rows, *weights)
+
+
 def moe_rows(x_rows, idx, w, dropped, expert_weights, shared=None):
     """y rows for a sample of tokens, expert by expert.
 
     x_rows [n, D] (fp32 or fp64): the sampled tokens' inputs; idx/w/dropped [n, k]: their
     routing (taken from a routing of the whole batch);
-    expert_weights(e) -> (Wg [F,D], Wu [F,D], Wd [D,F]) as float32;
-    shared: None or (Wsg, Wsu, Wsd).
+    expert_weights(e) -> (Wg [F,D], Wu [F,D], Wd [D,F]) as float32, or the six
+    E4M3 arrays (qg, sg, qu, su, qd, sd) of swiglu_rows_q8;
+    shared: None or a tuple of the same two kinds.
     Same definition as oracle_moe_forward: y = shared + sum_j kept * w * FFN.
     """
     x_rows = _f64(x_rows)
@@ -249,9 +307,8 @@ def moe_rows(x_rows, idx, w, dropped, expert_weights, shared=None):
     y = np.zeros((n, D), dtype=np.float64)
     for e in sorted(set(int(v) for v in idx[dropped == 0].ravel())):
         rows, slots = np.nonzero((idx == e) & (dropped == 0))
-        Wg, Wu, Wd = expert_weights(e)
-        out = swiglu_rows(x_rows[rows], Wg, Wu, Wd)
+        out = _expert_rows(x_rows[rows], expert_weights(e))
         y[rows] += w[rows, slots][:, None] * out
     if shared is not None:
-        y += swiglu_rows(x_rows, *shared)
+        y += _expert_rows(x_rows, shared)
     return y

@@ -32,7 +32,11 @@
  *     knowing about");
  *   - a dense "run every expert on every token, mask by routing" brute force
  *     on tiny inputs, and top-k selection against a full sort;
- *   - permuting the experts permutes the indices and leaves y unchanged.
+ *   - permuting the experts permutes the indices and leaves y unchanged;
+ *   - E4M3 decode and encode against PyTorch's float8_e4m3fn (every code,
+ *     every tie and its neighbours, random values), the row quantizer against
+ *     its defining properties, and the E4M3 expert against the fp32 expert on
+ *     weights that dequantize exactly.
  * Every exported function below is pinned by at least one of these.
  *
  * Weight layout: W_gate and W_up hold, per expert, F rows of D values
@@ -512,4 +516,136 @@ int oracle_latent_forward(int64_t T, int64_t D_outer, int64_t L, int64_t E, int6
     free(xl);
     free(yl);
     return rc;
+}
+
+/* ------------------------------------------------------------------------
+ * e4m3 (FP8) expert weights.
+ *
+ * [MPF] "What experts cost at serving time" sizes serving memory at 8 bits
+ * per weight and shows that decoding reads each expert weight for about two
+ * FLOPs; the pages fix no 8-bit format.  Reading used here (and by the CUDA
+ * path): the OCP FP8 E4M3 format -- sign bit, 4 exponent bits with bias 7,
+ * 3 mantissa bits, exponent field 0 holding subnormals m/8 * 2^-6, no
+ * infinities, S.1111.111 = NaN, largest finite value 448 -- with one fp32
+ * scale per weight row (output feature):
+ *   scale_r = max_c |W[r][c]| / 448 (fp32 division; 1 for an all-zero row),
+ *   q[r][c] = E4M3(W[r][c] / scale_r) (fp32 division, round to nearest,
+ *             ties to even, magnitudes above 448 saturate to 448),
+ * and the layer computes with W[r][c] = decode(q[r][c]) * scale_r.
+ * ------------------------------------------------------------------------ */
+
+/* Value of one E4M3 code. */
+static double e4m3_value(uint8_t b)
+{
+    const int e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = (double)m * ldexp(1.0, -9);          /* m/8 * 2^-6 */
+    else
+        v = (1.0 + (double)m / 8.0) * ldexp(1.0, e - 7);
+    return (b & 0x80) ? -v : v;
+}
+
+/* E4M3 code of a fp32 value: round to nearest (ties to even) on the E4M3
+ * grid, saturating to +-448; NaN stays NaN.  The grid spacing is 2^(e-3) for
+ * a value in [2^e, 2^(e+1)) with e >= -6, and 2^-9 below 2^-6. */
+static uint8_t e4m3_code(float v)
+{
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    if (isnan(v))
+        return (uint8_t)(sign | 0x7F);
+    const double a = fabs((double)v);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    int ex;
+    frexp(a, &ex);                        /* a = f * 2^ex, f in [0.5, 1) */
+    const int e = a == 0.0 ? -6 : (ex - 1 < -6 ? -6 : ex - 1);
+    const double quantum = ldexp(1.0, e - 3);
+    const double k = rint(a / quantum);   /* exact quotient; ties to even */
+    const double r = k * quantum;
+    if (r < ldexp(1.0, -6))               /* subnormal (k = 8 is 2^-6, code 8) */
+        return (uint8_t)(sign | (uint8_t)k);
+    frexp(r, &ex);
+    const int er = ex - 1;                /* rounding may reach the next binade */
+    const int mant = (int)((r / ldexp(1.0, er) - 1.0) * 8.0);
+    return (uint8_t)(sign | ((er + 7) << 3) | mant);
+}
+
+void oracle_e4m3_decode(int64_t n, const uint8_t *codes, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_value(codes[i]);
+}
+
+void oracle_e4m3_encode(int64_t n, const float *v, uint8_t *codes)
+{
+    for (int64_t i = 0; i < n; ++i)
+        codes[i] = e4m3_code(v[i]);
+}
+
+/* Row-wise quantization of W [rows][cols] (fp32 values of the bf16 weights)
+ * by the definition above. */
+void oracle_quantize_e4m3_rows(int64_t rows, int64_t cols, const float *W, uint8_t *q,
+                               float *scale)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *w = W + r * cols;
+        float amax = 0.0f;
+        for (int64_t c = 0; c < cols; ++c)
+            amax = fabsf(w[c]) > amax ? fabsf(w[c]) : amax;
+        const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scale[r] = s;
+        for (int64_t c = 0; c < cols; ++c)
+            q[r * cols + c] = e4m3_code(w[c] / s);
+    }
+}
+
+/* swiglu_token with W = decode(q) * scale (one scale per weight row); each
+ * dequantized weight is exact in double. */
+static void swiglu_token_q8(int64_t D, int64_t F, const double *x, const uint8_t *qg,
+                            const float *sg, const uint8_t *qu, const float *su,
+                            const uint8_t *qd, const float *sd, double *h, double *out)
+{
+    for (int64_t f = 0; f < F; ++f) {
+        double g = 0.0, u = 0.0;
+        for (int64_t d = 0; d < D; ++d) {
+            g += e4m3_value(qg[f * D + d]) * (double)sg[f] * x[d];
+            u += e4m3_value(qu[f * D + d]) * (double)su[f] * x[d];
+        }
+        h[f] = silu(g) * u;
+    }
+    for (int64_t d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int64_t f = 0; f < F; ++f)
+            acc += e4m3_value(qd[d * F + f]) * (double)sd[d] * h[f];
+        out[d] = acc;
+    }
+}
+
+/* oracle_swiglu_rows with e4m3 weights: qg, qu [F][D], qd [D][F] codes,
+ * sg, su [F], sd [D] row scales. */
+int oracle_swiglu_rows_q8(int64_t n, int64_t D, int64_t F, const double *x, const uint8_t *qg,
+                          const float *sg, const uint8_t *qu, const float *su,
+                          const uint8_t *qd, const float *sd, double *out)
+{
+    if (n < 0 || D < 1 || F < 1)
+        return ORACLE_BAD_ARG;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *h = (double *)malloc(sizeof(double) * (size_t)F);
+        if (!h) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < n; ++r)
+            if (h)
+                swiglu_token_q8(D, F, x + r * D, qg, sg, qu, su, qd, sd, h, out + r * D);
+        free(h);
+    }
+    return err ? ORACLE_NO_MEMORY : ORACLE_OK;
 }

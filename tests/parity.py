@@ -35,9 +35,13 @@ def f32(t):
 
 
 def run(w, seed=0, inputs=None, stream=None):
+    """Runs the layer; returns (cfg, inputs, outputs, device status).  For
+    E4M3 workloads the library quantizes the bf16 weights first and the
+    returned inputs are the bf16 ones (the oracle quantizes them itself)."""
     cfg = B.config_of(w)
     inp = inputs if inputs is not None else make_inputs(w, seed, "cuda")
-    outs = B.forward(cfg, inp, stream=stream)
+    run_inp = B.quantize_expert_weights(inp, stream) if w.weights == "e4m3" else inp
+    outs = B.forward(cfg, run_inp, stream=stream)
     code = B.read_device_status(cfg, outs["workspace"], stream=stream)
     return cfg, inp, outs, code
 
@@ -60,8 +64,16 @@ def pick_sample(w, dropped, idx, kept_mask_rows, n, seed=0):
     return np.array(sorted(pick), dtype=np.int64)
 
 
-def check(w, inp, outs, sample=None, logit_rows=None, y_sample_n=None, seed=0):
-    """Asserts every parity criterion; returns a dict of the measured errors."""
+def e4m3_weights(W):
+    """The oracle's own E4M3 codes and scales of a bf16 weight matrix (device
+    tensor [rows, cols]): (codes, scales) as numpy arrays."""
+    return oracle.quantize_e4m3_rows(f32(W))
+
+
+def check(w, inp, outs, sample=None, logit_rows=None, y_sample_n=None, seed=0, e4m3=False):
+    """Asserts every parity criterion; returns a dict of the measured errors.
+    e4m3: the layer ran with E4M3 expert weights; the oracle quantizes the
+    same bf16 weights itself and computes with the dequantized values."""
     T, E, k = w.T, w.E, w.k
     gamma32 = float(np.float32(w.gamma))
     alpha32 = float(np.float32(w.alpha))
@@ -113,11 +125,17 @@ def check(w, inp, outs, sample=None, logit_rows=None, y_sample_n=None, seed=0):
     sel = torch.as_tensor(sample, device=inp["x"].device)
     x_rows = layer_input(f32(inp["x"][sel]))
     Wg, Wu, Wd = inp["W_gate"], inp["W_up"], inp["W_down"]
+    if e4m3:
+        def weights(*Ws):
+            return tuple(a for W in Ws for a in e4m3_weights(W))
+    else:
+        def weights(*Ws):
+            return tuple(f32(W) for W in Ws)
     shared = None
     if w.S > 0:
-        shared = (f32(inp["Ws_gate"]), f32(inp["Ws_up"]), f32(inp["Ws_down"]))
+        shared = weights(inp["Ws_gate"], inp["Ws_up"], inp["Ws_down"])
     y_ref = oracle.moe_rows(x_rows, idx[sample], wts[sample], dropped[sample],
-                            lambda e: (f32(Wg[e]), f32(Wu[e]), f32(Wd[e])), shared=shared)
+                            lambda e: weights(Wg[e], Wu[e], Wd[e]), shared=shared)
     if latent:
         y_ref = oracle.linear(y_ref, f32(inp["W_out"]))
     y_gpu = f32(outs["y"][sel]).astype(np.float64)

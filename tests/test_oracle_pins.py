@@ -489,3 +489,90 @@ def test_latent_against_dense_bruteforce(mode, sel):
     np.testing.assert_allclose(out["y"], ref["y"] @ W_out.astype(np.float64).T,
                                rtol=1e-10, atol=1e-10)
     assert abs(out["aux"] - ref["aux"]) < 1e-12
+
+
+# ---------------------------------------------------------------- e4m3 weights
+# The E4M3 functions are pinned against PyTorch's float8_e4m3fn type (an
+# independent implementation of the same OCP format), against the format's
+# own grid (every representable value encodes to itself, ties go to the even
+# code), and the row quantizer against its defining properties.
+
+def _torch_e4m3_codes(v):
+    import torch
+    return torch.from_numpy(np.asarray(v, dtype=np.float32)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+
+
+def test_e4m3_decode_matches_torch():
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    same = (mine == ref) | (np.isnan(mine) & np.isnan(ref))
+    assert same.all()
+    assert np.nanmax(mine) == 448.0 and np.isnan(mine[0x7F]) and np.isnan(mine[0xFF])
+    assert mine[1] == 2.0 ** -9 and mine[8] == 2.0 ** -6   # smallest subnormal, normal
+
+
+def test_e4m3_encode_matches_torch_on_grid_ties_and_random():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes).astype(np.float32)
+    # every representable value encodes to its own code (+0 and -0 distinct)
+    np.testing.assert_array_equal(oracle.e4m3_encode(vals), codes)
+    pos = np.sort(np.unique(oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))))
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)          # exact ties in fp32
+    up = np.nextafter(mids, np.float32(np.inf))
+    down = np.nextafter(mids, np.float32(-np.inf))
+    rng = np.random.default_rng(5)
+    rnd = (np.exp(rng.uniform(np.log(2.0 ** -12), np.log(448.0), 20000)) *
+           rng.choice([-1.0, 1.0], 20000)).astype(np.float32)
+    for v in (mids, -mids, up, down, rnd, np.float32([0.0, -0.0, 2.0 ** -11, -2.0 ** -10])):
+        np.testing.assert_array_equal(oracle.e4m3_encode(v), _torch_e4m3_codes(v))
+    # ties go to the even code (mantissa lsb 0)
+    assert (oracle.e4m3_encode(mids) & 1 == 0).all()
+
+
+def test_e4m3_encode_saturates():
+    v = np.float32([448.0, 449.0, 463.9, 464.0, 1e6, -500.0, -1e30])
+    np.testing.assert_array_equal(oracle.e4m3_encode(v),
+                                  np.uint8([0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE]))
+
+
+def test_quantize_rows_properties():
+    rng = np.random.default_rng(6)
+    W = (rng.standard_normal((40, 96)) * np.exp(rng.uniform(-8, 4, (40, 1)))).astype(np.float32)
+    W[3] = 0.0
+    W[7, :5] = [1e-30, -1e-30, 0.0, 3.0, -3.0]
+    q, s = oracle.quantize_e4m3_rows(W)
+    amax = np.abs(W).max(axis=1)
+    nz = amax > 0
+    np.testing.assert_array_equal(s[nz], (amax[nz] / np.float32(448.0)).astype(np.float32))
+    assert s[3] == 1.0 and (q[3] == 0).all()
+    deq = oracle.e4m3_decode(q) * s[:, None].astype(np.float64)
+    # the largest magnitude of every row lands on the largest code
+    assert np.all(np.abs(oracle.e4m3_decode(q[nz])).max(axis=1) == 448.0)
+    # rounding error: half a grid step of E4M3 at the value's binade
+    v = W.astype(np.float64) / s[:, None]
+    e = np.maximum(np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -30))), -6)
+    assert np.all(np.abs(v - oracle.e4m3_decode(q)) <= 2.0 ** (e - 4) * (1 + 1e-12))
+    assert np.all(np.abs(deq - W) <= np.abs(W) / 16 + s[:, None] * 2.0 ** -10 + 1e-45)
+
+
+def test_swiglu_q8_equals_dense_with_dequantized_weights():
+    # power-of-two scales make every dequantized weight exact in fp32, so the
+    # E4M3 expert must equal the (pinned) fp32 expert on those weights
+    rng = np.random.default_rng(7)
+    D, F, n = 48, 40, 6
+    qg = rng.integers(0, 256, (F, D), dtype=np.uint8)
+    qu = rng.integers(0, 256, (F, D), dtype=np.uint8)
+    qd = rng.integers(0, 256, (D, F), dtype=np.uint8)
+    for q in (qg, qu, qd):
+        q[(q & 0x7F) == 0x7F] = 0x40          # no NaN codes
+    sg = np.float32(2.0) ** rng.integers(-12, -4, F)
+    su = np.float32(2.0) ** rng.integers(-12, -4, F)
+    sd = np.float32(2.0) ** rng.integers(-12, -4, D)
+    x = rng.standard_normal((n, D))
+    deq = lambda q, s: (oracle.e4m3_decode(q) * s[:, None]).astype(np.float32)
+    got = oracle.swiglu_rows_q8(x, qg, sg, qu, su, qd, sd)
+    want = oracle.swiglu_rows(x, deq(qg, sg), deq(qu, su), deq(qd, sd))
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
