@@ -234,7 +234,7 @@ MOE_API moe_status moe_quantize_e4m3_rows(int64_t rows, int64_t cols, const void
  * the same workspace size (moe_workspace_size).  The expert GEMMs run one
  * tensor-core kernel per projection with the weights as the operand held in
  * tensor memory, sized for batches of up to a few hundred tokens; larger
- * batches are correct but stream each weight tile once per 64 rows of an
+ * batches are correct but stream each weight tile once per 32 rows of an
  * expert. */
 MOE_API moe_status moe_forward_w8(const moe_config *cfg,
                        const void *x, const void *W_r, const float *router_bias,

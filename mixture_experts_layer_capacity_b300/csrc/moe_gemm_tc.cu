@@ -902,8 +902,8 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t k, uint3
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D byte tensor [rows, k] (e4m3 weights, k contiguous), boxes of 64 x
-// box_rows with 64-byte swizzle; out-of-range bytes read as zero.
+// 2-D byte tensor [rows, k] (e4m3 weights, k contiguous), boxes of 128 x
+// box_rows with 128-byte swizzle; out-of-range bytes read as zero.
 bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t k, uint32_t box_rows)
 {
     auto fn = encode_fn();
@@ -911,10 +911,10 @@ bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t k, ui
         return false;
     cuuint64_t dims[2] = {k, rows};
     cuuint64_t strides[1] = {k};
-    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t box[2] = {128, box_rows};
     cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
-              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

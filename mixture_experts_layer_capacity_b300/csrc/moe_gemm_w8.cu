@@ -13,12 +13,15 @@
 // Design (one CTA per SM, persistent over a unit list built on the device):
 //   - roles are swapped relative to the bf16 kernels: the weights are the
 //     MMA's A operand (M = 128 output features per tile) and the token rows
-//     are B (N = 16..64 rows, one unit covers up to 64 rows of a segment), so
+//     are B (N = 16 or 32 rows, one unit covers up to 32 rows of a segment), so
 //     a decode batch with a few rows per expert does not pad A to 128 rows;
-//   - warp 0: TMA producer: per 64-wide reduction step, two 128-row e4m3
-//     weight tiles (64-byte swizzle) and the token rows in 16-row boxes
-//     (128-byte swizzle, K-major) into an 8-stage shared-memory ring;
-//   - warps 6-9: converters: each thread owns one weight row of a tile (its
+//   - warp 0: TMA producer: per 128-wide reduction step, two 128-row e4m3
+//     weight tiles (128-byte rows, 128-byte swizzle) and the token rows in
+//     16-row boxes (two 64-element halves, 128-byte swizzle, K-major) into a
+//     5-stage shared-memory ring (160 KB of weights in flight per SM);
+//   - warps 6-13: converters, two groups of four taking alternate reduction
+//     steps (so that two steps convert at once): each thread owns one weight
+//     row of a tile (its
 //     TMEM lane), reads its 64 e4m3 bytes, converts them to f16 (one cvt per
 //     pair; every e4m3 value is an f16 value) and writes them into TMEM with
 //     tcgen05.st, where the MMA reads A directly (no second pass through
@@ -54,14 +57,17 @@ namespace {
 
 enum { W8_SWIGLU = 0, W8_BF16 = 1, W8_BF16_Y = 2 };
 
-constexpr int kW8Threads = 320;  // warps 0 TMA, 1 MMA, 2-5 epilogue, 6-9 converters
-constexpr int kW8Tok = 64;       // most token rows per unit (MMA N)
-constexpr int kW8Stages = 8;     // shared-memory ring
-constexpr int kW8AStages = 4;    // converted weight stages in TMEM
+constexpr int kW8Threads = 448;  // warps 0 TMA, 1 MMA, 2-5 epilogue, 6-13 converters
+constexpr int kW8Tok = 32;       // most token rows per unit (MMA N)
+constexpr int kW8K = 128;        // reduction elements per stage
+constexpr int kW8Stages = 5;     // shared-memory ring
+constexpr int kW8AStages = 3;    // converted weight stages in TMEM
 constexpr int kW8Rows = 128;     // weight rows per A tile (MMA M)
-constexpr int kW8FP8Bytes = kW8Rows * 64;                          // 8 KB
-constexpr int kW8StageBytes = 2 * kW8FP8Bytes + kW8Tok * 128;      // 24 KB
+constexpr int kW8FP8Bytes = kW8Rows * kW8K;                        // 16 KB per A tile
+constexpr int kW8BHalf = kW8Tok * 128;                             // token rows x 64 elements
+constexpr int kW8StageBytes = 2 * kW8FP8Bytes + 2 * kW8BHalf;      // 40 KB
 constexpr int kW8DCols = 2 * kW8Tok;                               // accumulator buffer
+constexpr int kW8ACols = kW8K / 2;                                 // TMEM columns of an A tile
 constexpr int kW8ACol0 = 2 * kW8DCols;                             // first A column
 constexpr int kW8TmemCols = 512;
 constexpr int kW8Bars = 2 * kW8Stages + 2 * kW8AStages + 4 + 1;
@@ -69,7 +75,8 @@ constexpr int kW8TableInts = 2 * (kMaxExperts + 1);
 constexpr int kW8SmemBytes = kW8Stages * kW8StageBytes + 512 + kW8TableInts * 4 + 1024;
 constexpr uint64_t kW8WaitNs = 2000000000ull;
 constexpr uint64_t kW8DrainNs = 200000000ull;
-static_assert(kW8ACol0 + kW8AStages * 2 * 32 <= kW8TmemCols, "TMEM columns");
+static_assert(kW8ACol0 + kW8AStages * 2 * kW8ACols <= kW8TmemCols, "TMEM columns");
+static_assert(kW8StageBytes % 1024 == 0 && kW8BHalf % 1024 == 0, "1024-byte swizzle atoms");
 static_assert(kW8Bars * 8 + 8 <= 512, "barrier area");
 static_assert(kW8SmemBytes <= 227 * 1024, "shared memory");
 
@@ -141,7 +148,7 @@ __device__ __forceinline__ W8Unit w8_unit(const W8Params &p, const int *s_seg, c
         w.row0 = s_seg[lo] + m * kW8Tok;
         w.n = min(kW8Tok, s_seg[lo + 1] - w.row0);
     }
-    const int nk = (pr.K + 63) / 64;
+    const int nk = (pr.K + kW8K - 1) / kW8K;
     w.kb0 = w.ks * nk / pr.ksplit;
     w.kb1 = (w.ks + 1) * nk / pr.ksplit;
     return w;
@@ -331,15 +338,17 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                         break;
                     }
                     uint8_t *st = smem + s * kW8StageBytes;
-                    mbar_arrive_expect_tx(&full[s], 2 * kW8FP8Bytes + nb * 16 * 128);
-                    tma_load_2d(st, mw0, &full[s], kb * 64, wrow);
+                    mbar_arrive_expect_tx(&full[s], 2 * kW8FP8Bytes + 2 * nb * 16 * 128);
+                    tma_load_2d(st, mw0, &full[s], kb * kW8K, wrow);
                     if (EPI == W8_SWIGLU)
-                        tma_load_2d(st + kW8FP8Bytes, mw1, &full[s], kb * 64, wrow);
+                        tma_load_2d(st + kW8FP8Bytes, mw1, &full[s], kb * kW8K, wrow);
                     else
-                        tma_load_2d(st + kW8FP8Bytes, mw0, &full[s], kb * 64, wrow + kW8Rows);
-                    for (int j = 0; j < nb; ++j)
-                        tma_load_2d(st + 2 * kW8FP8Bytes + j * 16 * 128, mb, &full[s], kb * 64,
-                                    w.row0 + 16 * j);
+                        tma_load_2d(st + kW8FP8Bytes, mw0, &full[s], kb * kW8K, wrow + kW8Rows);
+                    // reduction elements past K (a last half block) read as zero
+                    for (int h = 0; h < 2; ++h)
+                        for (int j = 0; j < nb; ++j)
+                            tma_load_2d(st + 2 * kW8FP8Bytes + h * kW8BHalf + j * 16 * 128, mb,
+                                        &full[s], kb * kW8K + h * 64, w.row0 + 16 * j);
                     ++fills;
                     if (++s == kW8Stages) {
                         s = 0;
@@ -379,15 +388,16 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint64_t bdesc =
-                        sdesc_kmajor_sw128(smem_u32(smem + s * kW8StageBytes + 2 * kW8FP8Bytes));
+                    const uint32_t sb = smem_u32(smem + s * kW8StageBytes + 2 * kW8FP8Bytes);
+                    const uint64_t bdesc[2] = {sdesc_kmajor_sw128(sb),
+                                               sdesc_kmajor_sw128(sb + kW8BHalf)};
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
-                        const uint32_t a = tmem_base + kW8ACol0 + (uint32_t)(sa * 2 + t) * 32;
+                        const uint32_t a = tmem_base + kW8ACol0 + (uint32_t)(sa * 2 + t) * kW8ACols;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            umma_bf16_ta(d0 + t * kW8Tok, a + kk * 8, bdesc + 2u * kk, idesc,
-                                         (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kW8K / 16; ++kk)
+                            umma_bf16_ta(d0 + t * kW8Tok, a + kk * 8, bdesc[kk >> 2] + 2u * (kk & 3),
+                                         idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(&empty[s]);
                     umma_commit(&aempty[sa]);
@@ -416,15 +426,22 @@ __global__ void __launch_bounds__(kW8Threads, 1)
         }
     } else if (warp >= 6) {
         // ---------------------------------------------------- converters
+        // group grp converts the reduction steps i with i % 2 == grp (i counts
+        // this CTA's steps over all its units)
+        const int grp = (warp - 6) >> 2;
         const int q = warp & 3;
         const int r = q * 32 + lane;  // weight row within each A tile = TMEM lane
         const uint32_t lanes = (uint32_t)(q * 32) << 16;
-        int s = 0, sa = 0;
-        uint32_t ph = 0, aph = 0;
+        long long i = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += G) {
             const W8Unit w = w8_unit(p, s_seg, s_tt, u, n0);
-            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++i) {
+                if ((int)(i & 1) != grp)
+                    continue;
+                const int s = (int)(i % kW8Stages), sa = (int)(i % kW8AStages);
+                const uint32_t ph = (uint32_t)((i / kW8Stages) & 1);
+                const uint32_t aph = (uint32_t)((i / kW8AStages) & 1);
                 if (!mbar_wait(&full[s], ph, abort_flag, kW8WaitNs) ||
                     !mbar_wait(&aempty[sa], aph ^ 1u, abort_flag, kW8WaitNs)) {
                     ok = false;
@@ -434,53 +451,54 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                 const uint8_t *st = smem + s * kW8StageBytes;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
-                    // row r's 16-byte chunk c sits at chunk c ^ ((r >> 1) & 3)
-                    // (64-byte swizzle of the TMA box)
-                    const uint8_t *row = st + t * kW8FP8Bytes + r * 64;
-                    uint32_t v[32];
+                    // row r's 16-byte chunk c sits at chunk c ^ (r & 7)
+                    // (128-byte swizzle of the TMA box)
+                    const uint8_t *row = st + t * kW8FP8Bytes + r * 128;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint4 qv =
-                            *reinterpret_cast<const uint4 *>(row + ((c ^ ((r >> 1) & 3)) << 4));
-                        v[8 * c + 0] = e4m3x2_to_f16x2(qv.x);
-                        v[8 * c + 1] = e4m3x2_to_f16x2(qv.x >> 16);
-                        v[8 * c + 2] = e4m3x2_to_f16x2(qv.y);
-                        v[8 * c + 3] = e4m3x2_to_f16x2(qv.y >> 16);
-                        v[8 * c + 4] = e4m3x2_to_f16x2(qv.z);
-                        v[8 * c + 5] = e4m3x2_to_f16x2(qv.z >> 16);
-                        v[8 * c + 6] = e4m3x2_to_f16x2(qv.w);
-                        v[8 * c + 7] = e4m3x2_to_f16x2(qv.w >> 16);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t v[32];
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            const int c = hh * 4 + c4;
+                            const uint4 qv =
+                                *reinterpret_cast<const uint4 *>(row + ((c ^ (r & 7)) << 4));
+                            v[8 * c4 + 0] = e4m3x2_to_f16x2(qv.x);
+                            v[8 * c4 + 1] = e4m3x2_to_f16x2(qv.x >> 16);
+                            v[8 * c4 + 2] = e4m3x2_to_f16x2(qv.y);
+                            v[8 * c4 + 3] = e4m3x2_to_f16x2(qv.y >> 16);
+                            v[8 * c4 + 4] = e4m3x2_to_f16x2(qv.z);
+                            v[8 * c4 + 5] = e4m3x2_to_f16x2(qv.z >> 16);
+                            v[8 * c4 + 6] = e4m3x2_to_f16x2(qv.w);
+                            v[8 * c4 + 7] = e4m3x2_to_f16x2(qv.w >> 16);
+                        }
+                        tmem_st32(tmem_base + lanes + kW8ACol0 +
+                                      (uint32_t)(sa * 2 + t) * kW8ACols + hh * 32,
+                                  v);
                     }
-                    tmem_st32(tmem_base + lanes + kW8ACol0 + (uint32_t)(sa * 2 + t) * 32, v);
                 }
                 if constexpr (EPI == W8_SWIGLU) {
                     // GEMM1's token rows arrive as bf16: to f16 in place (element
                     // by element, so the swizzled layout is kept), then make the
                     // writes visible to the tensor cores' reads
                     const int nb = (w.n + 15) / 16;
-                    uint4 *bt = reinterpret_cast<uint4 *>(smem + s * kW8StageBytes + 2 * kW8FP8Bytes);
-                    const int tc = (warp - 6) * 32 + lane;
-                    for (int i = tc; i < nb * 16 * 8; i += 128) {
-                        uint4 x = bt[i];
-                        x.x = bf16x2_to_f16x2(x.x);
-                        x.y = bf16x2_to_f16x2(x.y);
-                        x.z = bf16x2_to_f16x2(x.z);
-                        x.w = bf16x2_to_f16x2(x.w);
-                        bt[i] = x;
+                    const int tc = (warp - 6 - 4 * grp) * 32 + lane;
+                    for (int h = 0; h < 2; ++h) {
+                        uint4 *bt = reinterpret_cast<uint4 *>(smem + s * kW8StageBytes +
+                                                              2 * kW8FP8Bytes + h * kW8BHalf);
+                        for (int ci = tc; ci < nb * 16 * 8; ci += 128) {
+                            uint4 x = bt[ci];
+                            x.x = bf16x2_to_f16x2(x.x);
+                            x.y = bf16x2_to_f16x2(x.y);
+                            x.z = bf16x2_to_f16x2(x.z);
+                            x.w = bf16x2_to_f16x2(x.w);
+                            bt[ci] = x;
+                        }
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
                 tmem_wait_st();
                 tc_fence_before_sync();
                 mbar_arrive(&afull[sa]);
-                if (++s == kW8Stages) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-                if (++sa == kW8AStages) {
-                    sa = 0;
-                    aph ^= 1u;
-                }
             }
         }
         if (!ok) {
@@ -675,7 +693,7 @@ cudaError_t launch_experts_w8(const moe_config &c, const WorkspaceLayout &L, uin
     void *xp = ws + L.x_perm, *h = ws + L.h, *z = ws + L.z;
     void *hs = ws + L.hs, *zs = ws + L.zs;
     const long long R = L.R_max;
-    const long long tt_bound = R / kW8Tok + E;            // >= sum_e ceil(kept_e / 64)
+    const long long tt_bound = R / kW8Tok + E;            // >= sum_e ceil(kept_e / 32)
     const long long tt_s = (T + kW8Tok - 1) / kW8Tok;
     const LaunchPlan plan = plan_of(c);
     cudaError_t err;

@@ -178,7 +178,7 @@ cudaError_t launch_dense_simt(int rows, int N, int K, const float *A, const floa
 
 // Tensor maps for TMA (moe_gemm_tc.cu): a bf16 [rows, k] tensor in boxes of
 // 64 x box_rows with 128-byte swizzle, and a byte (e4m3) [rows, k] tensor in
-// boxes of 64 x box_rows with 64-byte swizzle.  false: cannot be encoded.
+// boxes of 128 x box_rows with 128-byte swizzle.  false: cannot be encoded.
 bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t k, uint32_t box_rows);
 bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t k, uint32_t box_rows);
 
