@@ -171,8 +171,11 @@ def profile_traffic(stage, workload):
     """DRAM bytes per launch of `stage` from a committed ncu summary, if the
     summary was taken on the current source of that stage's kernel (else
     None)."""
+    gemm_src = "moe_gemm_w8.cu" if (workload in WORKLOADS and
+                                     WORKLOADS[workload].weights == "e4m3" and
+                                     stage.startswith("gemm")) else "moe_gemm_tc.cu"
     src_name = {"dispatch": "moe_dispatch.cu", "combine": "moe_combine.cu",
-                "router": "moe_gemm_tc.cu"}.get(stage, "moe_gemm_tc.cu")
+                "router": "moe_gemm_tc.cu"}.get(stage, gemm_src)
     src = os.path.join(ROOT, "mixture_experts_layer_capacity_b300", "csrc", src_name)
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
