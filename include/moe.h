@@ -169,6 +169,9 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
 #define MOE_PLAN_PAIR_SHARED 8    /* shared-expert GEMMs on CTA pairs */
 #define MOE_PLAN_SHARED_FUSED 16  /* shared-expert tiles run inside the routed GEMM
                                      launches (no separate shared launches) */
+#define MOE_PLAN_PAIR_TAILS 32    /* with CTA pairs, each routed GEMM is two launches:
+                                     full 256-row tiles on pairs, each expert's
+                                     remaining rows in 128-row tiles on single CTAs */
 MOE_API moe_status moe_launch_plan(const moe_config *cfg, int32_t *flags);
 
 /* Workspace bytes moe_latent_forward needs for `cfg` (whose d_model is the

@@ -122,7 +122,7 @@ def config_of(w) -> MoeConfig:
 
 
 PLAN_FLAGS = {"router_fused": 1, "direct_y": 2, "pair_routed": 4, "pair_shared": 8,
-              "shared_fused": 16}
+              "shared_fused": 16, "pair_tails": 32}
 
 
 def launch_plan(cfg: MoeConfig) -> dict:

@@ -118,6 +118,11 @@ LaunchPlan plan_of(const moe_config &c)
                      routed_rows >= 2LL * 2 * kTileM * c.n_experts;
     pl.pair_shared = bf16 && c.d_shared > 0 && c.T >= kPairMinRows / 4;
     pl.shared_fused = bf16 && c.d_shared > 0 && !pl.pair_routed && !pl.pair_shared;
+    // 256-row pair tiles pad about E * 128 rows over all segments; with many
+    // experts (>= 128) the remainders run better as 128-row tiles in a second
+    // launch (DeepSeek-V3-shaped prefill: 25 % padding, routed GEMMs 7 %
+    // faster); with 64 experts the second launch cost more than it saved
+    pl.pair_tails = pl.pair_routed && c.n_experts >= 128;
     pl.router_splits = router_splits(c);
     return pl;
 }
@@ -188,7 +193,8 @@ moe_status moe_launch_plan(const moe_config *cfg, int32_t *flags)
     *flags = (pl.router_fused ? MOE_PLAN_ROUTER_FUSED : 0) | (pl.direct_y ? MOE_PLAN_DIRECT_Y : 0) |
              (pl.pair_routed ? MOE_PLAN_PAIR_ROUTED : 0) |
              (pl.pair_shared ? MOE_PLAN_PAIR_SHARED : 0) |
-             (pl.shared_fused ? MOE_PLAN_SHARED_FUSED : 0);
+             (pl.shared_fused ? MOE_PLAN_SHARED_FUSED : 0) |
+             (pl.pair_tails ? MOE_PLAN_PAIR_TAILS : 0);
     return MOE_OK;
 }
 

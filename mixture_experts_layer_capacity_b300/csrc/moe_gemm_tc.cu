@@ -66,6 +66,11 @@ struct TcParams {
     // are the kernel's second set of tensor maps.  sh_tiles = 0: none.
     int sh_tiles;            // dense tiles of the second problem (row tiles x column tiles)
     int sh_rows, sh_K, sh_n_tiles, sh_N_valid;
+    // grouped problems split between the CTA-pair kernel (full 256-row tiles)
+    // and the single-CTA kernel (each segment's remaining rows, 128-row tiles):
+    int pair_full_only;      // pair kernel: only the floor(n / 256) full tiles of a segment
+    int tail_after;          // single-CTA kernel: > 0: only the rows after the first
+                             // floor(n / tail_after) * tail_after rows of each segment
     int sh_ksplit;           // splits of the second problem's reduction (fp32 partial
                              // outputs part_stride apart, EPI_BF16 kernels only); 0/1 = none
     void *sh_out;
@@ -147,7 +152,9 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams &p, const int *s_se
     ti.n_idx = local / mt_e;
     const int m = local - ti.n_idx * mt_e;
     ti.seg = lo;
-    const int s0 = s_seg[lo];
+    int s0 = s_seg[lo];
+    if (p.tail_after > 0)
+        s0 += (s_seg[lo + 1] - s_seg[lo]) / p.tail_after * p.tail_after;
     ti.a_row0 = s0 + m * kTileM;
     ti.rows = min(kTileM, s_seg[lo + 1] - ti.a_row0);
     return ti;
@@ -399,8 +406,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.mtile && !failed) {
         for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
             tables[i] = p.seg_off[i];
-            tables[kMaxExperts + 1 + i] = p.mtile[i];
+            if (p.tail_after <= 0)
+                tables[kMaxExperts + 1 + i] = p.mtile[i];
         }
+    }
+    __syncthreads();
+    if (p.tail_after > 0 && p.mtile && !failed && warp == 0) {
+        // 128-row tiles of each segment's rows past its last full
+        // tail_after-row block, prefix-summed
+        int carry = 0;
+        for (int e0 = 0; e0 < p.nseg; e0 += 32) {
+            const int e = e0 + lane;
+            const int n = e < p.nseg ? tables[e + 1] - tables[e] : 0;
+            const int v = (n - n / p.tail_after * p.tail_after + kTileM - 1) / kTileM;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += t;
+            }
+            if (e < p.nseg)
+                tables[kMaxExperts + 1 + e + 1] = carry + incl;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0)
+            tables[kMaxExperts + 1] = 0;
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -699,7 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int carry = 0;
         for (int e0 = 0; e0 < p.nseg; e0 += 32) {
             const int e = e0 + lane;
-            const int v = e < p.nseg ? (s_seg[e + 1] - s_seg[e] + kPairRows - 1) / kPairRows : 0;
+            const int n = e < p.nseg ? s_seg[e + 1] - s_seg[e] : 0;
+            const int v = p.pair_full_only ? n / kPairRows : (n + kPairRows - 1) / kPairRows;
             int incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -1104,11 +1136,27 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.sh_out = hs;
             p.sh_ld_out = S;
         }
-        err = pair_routed
-                  ? launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, mt2_bound * p.n_tiles,
-                                                          stream)
-                  : launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_bound * p.n_tiles, stream,
-                                                     fused ? &sm : nullptr);
+        if (pair_routed && plan.pair_tails) {
+            // full 256-row tiles on CTA pairs, then each segment's remaining
+            // rows (< 256) in 128-row single-CTA tiles: a 256-row tile over a
+            // short remainder would compute mostly padding
+            p.pair_full_only = 1;
+            err = launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, mt2_bound * p.n_tiles,
+                                                        stream);
+            if (err == cudaSuccess) {
+                TcParams q = p;
+                q.pair_full_only = 0;
+                q.tail_after = kPairRows;
+                q.aux.out = nullptr;  // evaluated by the pair launch
+                err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, q, 2LL * E * q.n_tiles, stream);
+            }
+        } else if (pair_routed) {
+            err = launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, mt2_bound * p.n_tiles,
+                                                        stream);
+        } else {
+            err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_bound * p.n_tiles, stream,
+                                                   fused ? &sm : nullptr);
+        }
         if (err == cudaSuccess)
             err = record_stage(ev, 3, stream);
         if (err != cudaSuccess)
@@ -1150,21 +1198,42 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
         }
         const SecondMaps *second = fused ? &sm : nullptr;
         const long long tiles = (pair_routed ? mt2_bound : mt_bound) * p.n_tiles;
+        // pair tails: full 256-row tiles on pairs, the remainders on single CTAs
+        const bool tails = pair_routed && plan.pair_tails;
+        p.pair_full_only = tails ? 1 : 0;
+        TcParams q = p;
+        q.pair_full_only = 0;
+        q.tail_after = kPairRows;
+        const long long tail_tiles = 2LL * E * p.n_tiles;
+        CUtensorMap mBt;  // the single-CTA kernel's B boxes hold bn_down rows
+        if (tails && !make_map(&mBt, W_down, (uint64_t)E * D, (uint64_t)F, (uint32_t)bn_down))
+            return cudaErrorInvalidValue;
         if (plan.direct_y) {
             p.out = y;
             p.row_tok = reinterpret_cast<const int32_t *>(ws + L.row_tok);
             p.row_w = reinterpret_cast<const float *>(ws + L.row_w);
-            if (pair_routed)
+            q.out = p.out;
+            q.row_tok = p.row_tok;
+            q.row_w = p.row_w;
+            if (pair_routed) {
                 err = wide_down ? launch_tc_pair<256, 1, EPI_BF16_Y, 6>(mA, mB, mB, p, tiles, stream)
                                 : launch_tc_pair<128, 1, EPI_BF16_Y, 8>(mA, mB, mB, p, tiles, stream);
-            else
+                if (err == cudaSuccess && tails)
+                    err = wide_down
+                              ? launch_tc<256, 1, EPI_BF16_Y, 4>(mA, mBt, mBt, q, tail_tiles, stream)
+                              : launch_tc<128, 1, EPI_BF16_Y, 6>(mA, mBt, mBt, q, tail_tiles, stream);
+            } else
                 err = wide_down ? launch_tc<256, 1, EPI_BF16_Y, 4>(mA, mB, mB, p, tiles, stream)
                                 : launch_tc<128, 1, EPI_BF16_Y, 6>(mA, mB, mB, p, tiles, stream);
         } else {
-            if (pair_routed)
+            if (pair_routed) {
                 err = wide_down ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream)
                                 : launch_tc_pair<128, 1, EPI_BF16, 8>(mA, mB, mB, p, tiles, stream);
-            else
+                if (err == cudaSuccess && tails)
+                    err = wide_down
+                              ? launch_tc<256, 1, EPI_BF16, 4>(mA, mBt, mBt, q, tail_tiles, stream)
+                              : launch_tc<128, 1, EPI_BF16, 6>(mA, mBt, mBt, q, tail_tiles, stream);
+            } else
                 err = wide_down
                           ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, tiles, stream, second)
                           : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream, second);

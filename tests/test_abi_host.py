@@ -188,6 +188,8 @@ def test_launch_plan():
     q = plan("qwen2_57b_prefill")
     assert q["pair_shared"] and not q["shared_fused"]
     assert plan("mixtral_prefill")["pair_routed"]
+    # 256 experts: pair tiles plus 128-row remainder tiles; 64 experts: pairs only
+    assert plan("dsv3_prefill")["pair_tails"] and not q["pair_tails"]
     assert not plan("mixtral_decode")["pair_routed"]
     with pytest.raises(B.MoeError):
         B.launch_plan(B.make_config(64, 128, 8, 128, 0))

@@ -42,6 +42,9 @@ PAIR = [
     ("pair_top1_direct_y", 16400, 256, 8, 256, 1, 0, 2, 1.1, "none"),
     # dropless, several experts empty or tiny, k = 4
     ("pair_dropless_zipf", 4200, 128, 8, 192, 4, 128, 0, 0.0, "zipf1.1"),
+    # 128 experts: full 256-row tiles on pairs, each segment's remainder in a
+    # second, single-CTA launch (skewed segments: some below 256 rows)
+    ("pair_tails_e128_zipf", 8200, 128, 128, 192, 8, 0, 2, 0.0, "zipf1.1"),
 ]
 
 
