@@ -510,9 +510,19 @@ def run_ours(args, rank, world, device):
         "wall_s_timed_loop": wall,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle  # test infrastructure: only the CPU-baseline leg uses it
         rate, note, n = oracle_rate(w, bf16_inputs, budget_s=args.cpu_budget_s)
-        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": _omp_threads(),
-                                "kind": "oracle", "sample": note}
+        # the same oracle on one host thread (a smaller bounded sample)
+        cores = oracle.set_threads(1)
+        try:
+            rate1, note1, _ = oracle_rate(w, bf16_inputs, budget_s=args.cpu_budget_s / 2,
+                                          min_tokens=4)
+        finally:
+            oracle.set_threads(cores)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores,
+                                "kind": "oracle", "sample": note,
+                                "single_thread": {"value": rate1, "unit": "tokens/s",
+                                                  "cores": 1, "sample": note1}}
     return line
 
 

@@ -90,6 +90,17 @@ def _load():
         return lib
 
 
+def set_threads(n: int) -> int:
+    """Sets the number of OpenMP threads the oracle's parallel loops use
+    (the process's libgomp) and returns the previous maximum."""
+    _load()
+    gomp = ctypes.CDLL("libgomp.so.1")
+    gomp.omp_get_max_threads.restype = ctypes.c_int
+    prev = int(gomp.omp_get_max_threads())
+    gomp.omp_set_num_threads(ctypes.c_int(int(n)))
+    return prev
+
+
 def _f32(a):
     return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
 
