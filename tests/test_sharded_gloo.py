@@ -108,3 +108,51 @@ def test_token_slices():
     assert sharded.token_slices(10, 3) == [(0, 4), (4, 3), (7, 3)]
     assert sharded.token_slices(2, 4) == [(0, 1), (1, 1), (2, 0), (2, 0)]
     assert sharded.token_slices(0, 2) == [(0, 0), (0, 0)]
+
+
+def _plumbing_main(rank, world, port, results):
+    """sharded.forward on CPU tensors with the library's two calls replaced
+    by recorders: the exchange between them must hand every rank's counts and
+    sums, in rank order, to the finish call of every rank."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from mixture_experts_layer_capacity_b300 import binding as B
+        E, T_global = 8, 37
+        start, n = sharded.token_slices(T_global, world)[rank]
+        cfg = B.make_config(n, 64, E, 64, 2)
+        calls = {}
+
+        def fake_route(cfg_, T_g, x, W_r, bias, logits, idx, w, counts, psum, ws, **kw):
+            calls["route"] = (int(cfg_.T), int(T_g), tuple(x.shape))
+            counts.copy_(torch.arange(E, dtype=torch.int32) + 100 * rank)
+            psum.copy_(torch.full((E,), 0.5 + rank, dtype=torch.float64))
+
+        def fake_finish(cfg_, T_g, n_ranks, r, all_c, all_p, *rest, **kw):
+            calls["finish"] = (int(T_g), int(n_ranks), int(r), all_c.clone(), all_p.clone())
+
+        B.moe_sharded_route = fake_route
+        B.moe_sharded_finish = fake_finish
+        inputs = {"x": torch.zeros((n, 64)), "W_r": None, "W_gate": None, "W_up": None,
+                  "W_down": None}
+        sharded.forward(cfg, T_global, inputs)
+        assert calls["route"] == (n, T_global, (n, 64))
+        T_g, n_ranks, r, all_c, all_p = calls["finish"]
+        assert (T_g, n_ranks, r) == (T_global, world, rank)
+        for rr in range(world):
+            assert torch.equal(all_c[rr], torch.arange(E, dtype=torch.int32) + 100 * rr)
+            assert torch.all(all_p[rr] == 0.5 + rr)
+        results[rank] = True
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.timeout(300)
+def test_sharded_forward_plumbing():
+    world = 2
+    ctx = mp.get_context("spawn")
+    results = ctx.Manager().dict()
+    mp.start_processes(_plumbing_main, args=(world, _free_port(), results), nprocs=world,
+                       join=True, start_method="spawn")
+    assert dict(results) == {0: True, 1: True}
