@@ -1,0 +1,104 @@
+"""Host-side checks of the bench's accounting (no GPU).
+
+The per-stage algorithmic work must add up to the layer's closed forms, and
+a DRAM-traffic figure from a committed profile summary may only be used
+while the kernel source it was taken on is unchanged."""
+import hashlib
+import os
+import re
+
+import pytest
+
+import bench
+from mixture_experts_layer_capacity_b300 import roofline as RL
+from mixture_experts_layer_capacity_b300.workloads import WORKLOADS, Workload
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _cases():
+    yield Workload("a", T=300, D=128, E=8, F=192, k=2, mode=0, gamma=0.0, dtype="bf16")
+    yield Workload("b", T=64, D=256, E=16, F=128, k=4, mode=1, gamma=1.0, dtype="bf16", S=512)
+    yield Workload("c", T=96, D=64, E=4, F=128, k=1, mode=2, gamma=0.0, dtype="fp32", S=128)
+    yield Workload("d", T=64, D=512, E=32, F=256, k=8, mode=1, gamma=0.0, dtype="bf16",
+                   S=256, weights="e4m3")
+    yield from WORKLOADS.values()
+
+
+@pytest.mark.parametrize("w", list(_cases()), ids=lambda w: w.name)
+@pytest.mark.parametrize("fused", [False, True])
+def test_stage_flops_add_up_to_the_layer(w, fused):
+    kept_total, touched = w.T * w.k - 7, min(w.E, 5)
+    work = bench.stage_work(w, kept_total, touched, shared_fused=fused and w.S > 0)
+    flops = sum(f for f, _ in work.values())
+    assert flops == RL.layer_flops(w.T, w.D, w.E, w.F, w.S, kept_total)
+    gemm = sum(f for n, (f, _) in work.items() if n.startswith("gemm"))
+    assert gemm == RL.expert_flops(w.D, w.F, w.S, w.T, kept_total)
+
+
+@pytest.mark.parametrize("w", list(_cases()), ids=lambda w: w.name)
+def test_stage_weight_bytes_match_the_layer(w):
+    """The expert and shared weight bytes counted by the GEMM stages equal
+    the layer's closed form (bf16/fp32 weights at the activation width, E4M3
+    at one byte plus a 4-byte scale per weight row)."""
+    kept_total, touched = 0, min(w.E, 3)      # no rows: the GEMM stages hold only weights
+    b = 2 if w.dtype == "bf16" else 4
+    work = bench.stage_work(w, kept_total, touched)
+    gemm_bytes = sum(v for n, (_, v) in work.items() if n.startswith("gemm"))
+    shared_act = b * 2 * (w.T * w.D + w.T * w.S) if w.S else 0
+    if not w.S:
+        gemm_bytes -= work["gemm1_shared"][1] + work["gemm2_shared"][1]
+    wb = 1 if w.weights == "e4m3" else None
+    layer = RL.layer_bytes(w.T, w.D, w.E, w.F, w.S, touched, b, weight_bytes=wb)
+    # the layer's form adds the router weights, x and y
+    assert gemm_bytes - shared_act == layer - b * (w.D * w.E + 2 * w.T * w.D)
+
+
+def _traffic_lines():
+    pat = re.compile(r"bench_traffic:\s*stage=(\S+)\s+workload=(\S+)\s+"
+                     r"dram_bytes_per_launch=(\d+)\s+source_sha256=(\w+)")
+    pdir = os.path.join(ROOT, "profiles")
+    out = []
+    for name in sorted(os.listdir(pdir)):
+        if name.endswith((".md", ".txt")):
+            out += [(name,) + m.groups() for m in pat.finditer(open(os.path.join(pdir, name)).read())]
+    return out
+
+
+def _source_sha(stage, workload):
+    if stage in ("dispatch",):
+        src = "moe_dispatch.cu"
+    elif stage == "combine":
+        src = "moe_combine.cu"
+    elif WORKLOADS[workload].weights == "e4m3" and stage.startswith("gemm"):
+        src = "moe_gemm_w8.cu"
+    else:
+        src = "moe_gemm_tc.cu"
+    path = os.path.join(ROOT, "mixture_experts_layer_capacity_b300", "csrc", src)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def test_profile_traffic_only_from_current_sources():
+    lines = _traffic_lines()
+    assert lines, "no bench_traffic lines under profiles/"
+    current = 0
+    for name, stage, workload, nbytes, sha in lines:
+        assert workload in WORKLOADS, (name, workload)
+        got = bench.profile_traffic(stage, workload)
+        if sha == _source_sha(stage, workload):
+            current += 1
+            assert got == int(nbytes), (name, stage, workload)
+        elif got is not None:
+            # another summary holds a current figure for the same stage
+            assert any(s == _source_sha(stage, workload) and st == stage and wl == workload
+                       for _, st, wl, _, s in lines), (name, stage, workload)
+    # the default workload's dominant kernel has a current figure
+    assert bench.profile_traffic("gemm1_routed", bench.DEFAULT_WORKLOAD) is not None
+    assert current > 0
+
+
+def test_peaks_are_the_measured_file():
+    p = bench._peaks()
+    if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")):
+        assert p["source"] == "measured"
+    assert p["hbm"] > 1000 and p["tc"] > 100 and p["tc_sustained"] <= p["tc"]
