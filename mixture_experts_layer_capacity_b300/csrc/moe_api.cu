@@ -144,17 +144,21 @@ std::atomic<cudaEvent_t *> g_stage_events{nullptr};
 
 int sm_count()
 {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return 1;
-    if (dev < 64 && cached[dev] > 0)
-        return cached[dev];
+    const bool slot = dev >= 0 && dev < 64;
+    if (slot) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0)
+            return c;
+    }
     int n = 1;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
         n = 1;
-    if (dev < 64)
-        cached[dev] = n;
+    if (slot)
+        cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

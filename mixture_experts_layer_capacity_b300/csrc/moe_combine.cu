@@ -136,18 +136,18 @@ __global__ void __launch_bounds__(128)
 cudaError_t launch_combine(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                            const float *topk_w, void *y, cudaStream_t stream)
 {
-    static uint64_t configured = 0;  // bit per device
+    static DeviceOnce configured;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    if (dev < 64 && !(configured & (1ull << dev))) {
+    if (configured.pending(dev)) {
         err = prefer_max_shared_carveout(combine_bf16_kernel);
         if (err == cudaSuccess)
             err = prefer_max_shared_carveout(combine_f32_kernel);
         if (err != cudaSuccess)
             return err;
-        configured |= 1ull << dev;
+        configured.done(dev);
     }
     const int32_t *row_of = reinterpret_cast<const int32_t *>(ws + L.row_of);
     const int32_t *status = reinterpret_cast<const int32_t *>(ws + L.status);

@@ -1058,8 +1058,8 @@ static cudaError_t launch_dispatch_t(DispatchParams &p, size_t wr_bytes, cudaStr
     // One block per SM (a 1024-thread block whose largest layout takes most
     // of an SM's shared memory), so the launch geometry depends only on T and
     // the SM count: the two launches of a split batch see the same chunks.
-    static uint64_t configured = 0;
-    if (dev < 64 && !(configured & (1ull << dev))) {
+    static DeviceOnce configured;
+    if (configured.pending(dev)) {
         const size_t smem_max = dispatch_smem(kFusedMaxWrBytes + kFusedMaxE * 16,
                                               kStageMaxBytes + kChunk * 16, kMaxExperts, kMaxTopK);
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1075,7 +1075,7 @@ static cudaError_t launch_dispatch_t(DispatchParams &p, size_t wr_bytes, cudaStr
             return err;
         if (per_sm < 1)
             return cudaErrorInvalidConfiguration;
-        configured |= 1ull << dev;
+        configured.done(dev);
     }
     const int maxb = std::max(1, std::min(kMaxDispatchBlocks, sm_count()));
     // The smallest chunk (1, 2, ..., 32 tokens) whose chunk count fits one

@@ -970,15 +970,15 @@ cudaError_t launch_tc(const CUtensorMap &mA, const CUtensorMap &mB0, const CUten
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    static uint64_t configured = 0;  // bit per device
-    if (dev < 64 && !(configured & (1ull << dev))) {
+    static DeviceOnce configured;
+    if (configured.pending(dev)) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    S::SMEM_BYTES);
         if (err == cudaSuccess)
             err = prefer_max_shared_carveout(kern);
         if (err != cudaSuccess)
             return err;
-        configured |= 1ull << dev;
+        configured.done(dev);
     }
     const long long grid =
         std::min<long long>(max_tiles + (long long)p.sh_tiles * std::max(1, p.sh_ksplit), sm_count());
@@ -1002,8 +1002,8 @@ cudaError_t launch_tc_pair(const CUtensorMap &mA, const CUtensorMap &mB0, const 
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    static uint64_t configured = 0;  // bit per device
-    static int max_pairs[64] = {0};
+    static DeviceOnce configured;
+    static std::atomic<int> max_pairs[64];
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1016,7 +1016,8 @@ cudaError_t launch_tc_pair(const CUtensorMap &mA, const CUtensorMap &mB0, const 
     cfg.dynamicSmemBytes = S::SMEM_BYTES;
     cfg.stream = stream;
     cfg.attrs = attr;
-    if (dev < 64 && !(configured & (1ull << dev))) {
+    int pairs_max = 0;
+    if (configured.pending(dev)) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    S::SMEM_BYTES);
         if (err == cudaSuccess)
@@ -1029,11 +1030,15 @@ cudaError_t launch_tc_pair(const CUtensorMap &mA, const CUtensorMap &mB0, const 
         err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
         if (err != cudaSuccess)
             return err;
-        max_pairs[dev] = std::max(1, n);
-        configured |= 1ull << dev;
+        n = std::max(1, n);
+        if (dev >= 0 && dev < 64)
+            max_pairs[dev].store(n, std::memory_order_relaxed);
+        configured.done(dev);
+        pairs_max = n;
+    } else {
+        pairs_max = max_pairs[dev].load(std::memory_order_relaxed);
     }
-    const long long pairs =
-        std::min<long long>(max_tiles, dev < 64 ? max_pairs[dev] : sm_count() / 2);
+    const long long pairs = std::min<long long>(max_tiles, pairs_max);
     if (pairs < 1)
         return cudaSuccess;
     cfg.gridDim = dim3((unsigned)(2 * pairs));

@@ -609,15 +609,15 @@ cudaError_t launch_w8(const CUtensorMap (&m)[6], const W8Params &p, long long ma
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    static uint64_t configured = 0;  // bit per device
-    if (dev < 64 && !(configured & (1ull << dev))) {
+    static DeviceOnce configured;
+    if (configured.pending(dev)) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kW8SmemBytes);
         if (err == cudaSuccess)
             err = prefer_max_shared_carveout(kern);
         if (err != cudaSuccess)
             return err;
-        configured |= 1ull << dev;
+        configured.done(dev);
     }
     const long long grid = std::min<long long>(max_units, sm_count());
     if (grid < 1)

@@ -215,6 +215,26 @@ moe_status forward_body(const moe_config &c, const WorkspaceLayout &L, uint8_t *
 
 int sm_count();
 
+// One-time launch setup per device (function attributes, occupancy
+// queries), safe to use from several host threads: pending(dev) is true
+// until done(dev) has been called for that device.  Devices from 64 up are
+// set up on every call.
+class DeviceOnce {
+public:
+    bool pending(int dev) const
+    {
+        return dev < 0 || dev >= 64 || !(bits_.load(std::memory_order_acquire) & (1ull << dev));
+    }
+    void done(int dev)
+    {
+        if (dev >= 0 && dev < 64)
+            bits_.fetch_or(1ull << dev, std::memory_order_release);
+    }
+
+private:
+    std::atomic<uint64_t> bits_{0};
+};
+
 // Launches `kern` on `stream` with programmatic stream serialization, so
 // that it may be scheduled while the previous kernel drains.  Every kernel
 // launched this way calls griddep_wait() before touching global memory.

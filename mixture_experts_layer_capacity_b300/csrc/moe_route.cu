@@ -70,18 +70,18 @@ __global__ void router_simt_f32_kernel(const float *__restrict__ x, const float 
 cudaError_t launch_router_simt(const moe_config &c, const void *x, const void *W_r,
                                float *logits, cudaStream_t stream)
 {
-    static uint64_t configured = 0;  // bit per device
+    static DeviceOnce configured;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    if (dev < 64 && !(configured & (1ull << dev))) {
+    if (configured.pending(dev)) {
         err = prefer_max_shared_carveout(router_simt_bf16_kernel);
         if (err == cudaSuccess)
             err = prefer_max_shared_carveout(router_simt_f32_kernel);
         if (err != cudaSuccess)
             return err;
-        configured |= 1ull << dev;
+        configured.done(dev);
     }
     const long long warps = (long long)c.T * c.n_experts;
     const int threads = 256;
