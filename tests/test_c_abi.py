@@ -1,8 +1,9 @@
 """The boundary from plain C (no GPU): a C11 program that includes only
 include/moe.h, links libmoe.so and calls the host-side entry points.  It
 checks that the header is valid C and that the library is usable without
-Python.  The capacity check uses the worked numbers of "Mixture of Experts"
-(module 17), 17.5: T=4096, k=8, E=64 and capacity factor 1.25 give C=640;
+Python.  The capacity check applies the capacity equation of "Mixture of
+Experts" (module 17), 17.5, to the module's closing exercise: T=4096, k=8,
+E=64 and capacity factor 1.25 give C=640;
 rejected arguments must come back before any launch."""
 import os
 import shutil
