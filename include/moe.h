@@ -25,6 +25,9 @@
  *     entry point except moe_read_device_status synchronises.
  *   - Errors the host can detect return a non-zero moe_status before anything
  *     is launched and leave every output untouched.
+ *   - Entry points may be called from several host threads at once; calls
+ *     that run concurrently on the GPU need their own outputs and workspace
+ *     (moe_forward_no_alloc shares one static scratch: see there).
  *   - Row-major, dense, contiguous tensors.  "K-major" weights: each output
  *     row is contiguous over the reduction dimension.
  *   - dtype applies to x, the expert weights, W_r and y; router scores, gate
