@@ -1,8 +1,9 @@
 """Host-side checks of the bench's accounting (no GPU).
 
-The per-stage algorithmic work must add up to the layer's closed forms, and
-a DRAM-traffic figure from a committed profile summary may only be used
-while the kernel source it was taken on is unchanged."""
+The per-stage algorithmic work must add up to the layer's closed forms, a
+DRAM-traffic figure from a committed profile summary may only be used while
+the kernel source it was taken on is unchanged, and the reference arm (the
+oracle on the host) prints its one line on rank 0 only."""
 import hashlib
 import os
 import re
@@ -102,3 +103,32 @@ def test_peaks_are_the_measured_file():
     if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")):
         assert p["source"] == "measured"
     assert p["hbm"] > 1000 and p["tc"] > 100 and p["tc_sustained"] <= p["tc"]
+
+
+def _reference_arm(rank, world):
+    import subprocess
+    import sys
+    env = dict(os.environ, RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                           "--workload", "tiny_fp32", "--steps", "2", "--warmup", "3",
+                           "--gpus", str(world)],
+                          capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+
+
+def test_reference_arm_prints_one_line_on_rank_zero_only():
+    """The reference arm is the oracle on the host; under N ranks only rank 0
+    runs it and prints, the others exit 0 without output."""
+    import json
+    r1 = _reference_arm(1, 2)
+    assert r1.returncode == 0, r1.stderr[-2000:]
+    assert r1.stdout.strip() == ""
+    r0 = _reference_arm(0, 2)
+    assert r0.returncode == 0, r0.stderr[-2000:]
+    lines = [ln for ln in r0.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 2
+    assert d["value"] > 0 and d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
