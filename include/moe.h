@@ -183,10 +183,11 @@ MOE_API moe_status moe_launch_plan(const moe_config *cfg, int32_t *flags);
 MOE_API moe_status moe_latent_workspace_size(const moe_config *cfg, int32_t d_outer,
                                              size_t *bytes);
 
-/* A latent MoE ("Mixture of Experts: More Parameters, Same FLOPs", 'Where MoE
- * is going': the experts operate in a compressed space; inputs are
- * down-projected, e.g. 4096 -> 1024, the experts applied, and the outputs
- * up-projected back):
+/* A latent MoE ("Mixture of Experts: Sparse FFNs, Routers, and Shared
+ * Experts", the Nemotron 3 Super variant that closes the page after 'The 2026
+ * configuration table': the whole MoE layer runs at a narrower width L, e.g.
+ * L = 1024 inside a 4096-wide model, between a projection down to L and one
+ * back up):
  *   x_lat = x W_in^T,  y_lat = the layer of moe_forward on x_lat,
  *   y     = y_lat W_out^T.
  * cfg describes the layer at the latent width (cfg->d_model = L); the router,
@@ -206,6 +207,17 @@ MOE_API moe_status moe_latent_forward(const moe_config *cfg, int32_t d_outer,
                        int32_t *expert_counts, int32_t *kept_counts,
                        float *aux_loss, void *workspace, size_t workspace_bytes,
                        cudaStream_t stream);
+
+/* Where moe_latent_forward keeps the latent activations inside its
+ * workspace (same cfg and d_outer): x_lat = x W_in^T at byte offset
+ * *x_lat_offset and y_lat (the layer's output at width L) at *y_lat_offset,
+ * each [T][L] row-major in the config's dtype.  Both stay there after the
+ * call until the workspace is used again, so a caller can read them, e.g. to
+ * check the router scores against the exact latent rows the router saw.
+ * MOE_ERR_INVALID_ARG for null pointers or d_outer < 1; MOE_ERR_UNSUPPORTED
+ * as moe_latent_workspace_size.  Host only; launches nothing. */
+MOE_API moe_status moe_latent_offsets(const moe_config *cfg, int32_t d_outer,
+                                      size_t *x_lat_offset, size_t *y_lat_offset);
 
 /* ---- e4m3 (FP8) expert weights for decode-sized batches.
  *
@@ -329,9 +341,12 @@ MOE_API moe_status moe_sharded_finish(const moe_config *cfg, int64_t T_global,
  *     rejected with MOE_ERR_WORKSPACE before anything is launched (for bf16:
  *     roughly decode-sized batches of the large layers, and batches of a few
  *     thousand tokens of small layers, fit).
- *   - The first call on a device looks up the array's device address on that
- *     device (cudaGetSymbolAddress, with the device current); make that first
- *     call before any stream capture.
+ *   - Every call made outside stream capture looks up the array's device
+ *     address on the current device (cudaGetSymbolAddress); a call made
+ *     while its stream is capturing uses the address found by the last call
+ *     outside capture on that device.  So make the first call on a device
+ *     before any stream capture, and after a cudaDeviceReset make one call
+ *     outside capture before capturing again (a reset may move the array).
  *   - All calls share the one array and it keeps the last call's contents;
  *     each call clears what must start at zero on its own stream.  Calls whose
  *     work overlaps on the GPU (other streams, other host threads) race on
@@ -353,6 +368,21 @@ MOE_API moe_status moe_forward_no_alloc(const moe_config *cfg,
  * MOE_ERR_CUDA if the stream reported an error. */
 MOE_API moe_status moe_read_device_status(const moe_config *cfg, const void *workspace,
                                   cudaStream_t stream, int32_t *code);
+
+/* Test hook for the bounded waits (not for production use).  With
+ * extra_arrivals = 1 every later moe_forward (and latent / split-batch
+ * forward) makes the routing kernel's grid-wide barrier wait for one block
+ * more than the grid has, so the barrier cannot complete: each block gives up
+ * after limit_ns (0 = the default of 2 s; else 1 us ... 2 s), records
+ * MOE_DEVICE_PIPELINE_TIMEOUT in the status word and returns, and the later
+ * kernels of that forward pass see the status and do no work.  No copy or
+ * other asynchronous work is in flight at that barrier, and the next call
+ * clears the status word, so the context stays usable.
+ * moe_debug_barrier_fault(0, 0) restores normal operation.  The setting is
+ * process-wide and read when a forward pass is launched (a captured graph
+ * keeps the setting it was captured with).  MOE_ERR_INVALID_ARG for other
+ * values.  Host only; launches nothing. */
+MOE_API moe_status moe_debug_barrier_fault(int32_t extra_arrivals, uint64_t limit_ns);
 
 /* Stage timing (optional; for benchmarks and profiling).  While `events`
  * is non-NULL, every moe_forward call records events[i] on its stream at the

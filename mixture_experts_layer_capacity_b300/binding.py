@@ -77,6 +77,9 @@ def lib():
         L.moe_latent_workspace_size.argtypes = [cfgp, ctypes.c_int32,
                                                 ctypes.POINTER(ctypes.c_size_t)]
         L.moe_latent_workspace_size.restype = ctypes.c_int
+        L.moe_latent_offsets.argtypes = [cfgp, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t),
+                                         ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_latent_offsets.restype = ctypes.c_int
         L.moe_latent_forward.argtypes = [cfgp, ctypes.c_int32] + [vp] * 20 + [ctypes.c_size_t,
                                                                               vp]
         L.moe_latent_forward.restype = ctypes.c_int
@@ -94,6 +97,8 @@ def lib():
         L.moe_sharded_finish.restype = ctypes.c_int
         L.moe_read_device_status.argtypes = [cfgp, vp, vp, ctypes.POINTER(ctypes.c_int32)]
         L.moe_read_device_status.restype = ctypes.c_int
+        L.moe_debug_barrier_fault.argtypes = [ctypes.c_int32, ctypes.c_uint64]
+        L.moe_debug_barrier_fault.restype = ctypes.c_int
         L.moe_set_stage_events.argtypes = [vp, ctypes.c_int]
         L.moe_set_stage_events.restype = ctypes.c_int
         L.moe_status_string.argtypes = [ctypes.c_int]
@@ -267,6 +272,27 @@ def latent_workspace_size(cfg: MoeConfig, d_outer: int) -> int:
     return int(n.value)
 
 
+def latent_offsets(cfg: MoeConfig, d_outer: int):
+    """(x_lat, y_lat) byte offsets of the latent activations inside the
+    workspace of moe_latent_forward (moe_latent_offsets)."""
+    xo, yo = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    st = lib().moe_latent_offsets(ctypes.byref(cfg), int(d_outer), ctypes.byref(xo),
+                                  ctypes.byref(yo))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_latent_offsets")
+    return int(xo.value), int(yo.value)
+
+
+def latent_activations(cfg: MoeConfig, d_outer: int, workspace: torch.Tensor):
+    """Views of x_lat and y_lat [T, L] inside a moe_latent_forward workspace."""
+    xo, yo = latent_offsets(cfg, d_outer)
+    dt = torch.bfloat16 if cfg.dtype == MOE_DTYPE_BF16 else torch.float32
+    n = int(cfg.T) * int(cfg.d_model) * (2 if dt == torch.bfloat16 else 4)
+    shape = (int(cfg.T), int(cfg.d_model))
+    return (workspace[xo:xo + n].view(dt).view(shape),
+            workspace[yo:yo + n].view(dt).view(shape))
+
+
 def moe_latent_forward(cfg: MoeConfig, d_outer, x, W_in, W_out, W_r, router_bias, W_gate,
                        W_up, W_down, Ws_gate, Ws_up, Ws_down, y, router_logits, topk_idx,
                        topk_w, dropped_mask, expert_counts, kept_counts, aux_loss, workspace,
@@ -329,6 +355,15 @@ def read_device_status(cfg: MoeConfig, workspace, stream=None) -> int:
     if st not in (MOE_OK, MOE_ERR_DEVICE_STATUS):
         raise MoeError(st, "moe_read_device_status")
     return int(code.value)
+
+
+def debug_barrier_fault(extra_arrivals: int, limit_ns: int) -> None:
+    """Test hook (moe_debug_barrier_fault): make the routing kernel's grid
+    barrier wait for `extra_arrivals` blocks more than exist, giving up after
+    limit_ns; (0, 0) restores normal operation."""
+    st = lib().moe_debug_barrier_fault(int(extra_arrivals), int(limit_ns))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_debug_barrier_fault")
 
 
 NUM_STAGE_EVENTS = 8

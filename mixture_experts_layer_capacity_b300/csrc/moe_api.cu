@@ -390,6 +390,22 @@ moe_status moe_latent_workspace_size(const moe_config *cfg, int32_t d_outer, siz
     return MOE_OK;
 }
 
+moe_status moe_latent_offsets(const moe_config *cfg, int32_t d_outer, size_t *x_lat_offset,
+                              size_t *y_lat_offset)
+{
+    if (!x_lat_offset || !y_lat_offset)
+        return MOE_ERR_INVALID_ARG;
+    const moe_status st = validate_config(cfg);
+    if (st != MOE_OK)
+        return st;
+    size_t xo, yo, total;
+    if (!latent_layout(cfg, d_outer, &xo, &yo, &total))
+        return d_outer < 1 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
+    *x_lat_offset = xo;
+    *y_lat_offset = yo;
+    return MOE_OK;
+}
+
 moe_status moe_latent_forward(const moe_config *cfg, int32_t d_outer, const void *x,
                               const void *W_in, const void *W_out, const void *W_r,
                               const float *router_bias, const void *W_gate, const void *W_up,

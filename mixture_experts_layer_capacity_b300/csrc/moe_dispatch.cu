@@ -38,6 +38,7 @@
 // C are dropped by that expert only); "Mixture of Experts: Sparse FFNs,
 // Routers, and Shared Experts" ('Capacity factor'); "Mixture of experts"
 // (frontiers track), gate equation of 'Where the experts live'.
+#include <atomic>
 #include <cfloat>
 #include <climits>
 #include <cuda_bf16.h>
@@ -97,6 +98,11 @@ struct DispatchParams {
     int n_ranks, rank_id;
     long long TK_global;        // assignments over all ranks (T_global * k)
     int32_t *gcount;            // [E] out: demand counts over all ranks
+    // the grid barrier waits for gridDim.x + barrier_extra arrivals, for at
+    // most barrier_limit_ns (barrier_extra is 0 except under the test hook
+    // moe_debug_barrier_fault, which makes the barrier run out)
+    unsigned barrier_extra;
+    unsigned long long barrier_limit_ns;
 };
 
 // ------------------------------------------------------------ block helpers
@@ -145,10 +151,11 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
 }
 
 // Grid-wide barrier on a counter that starts at zero; `target` = number of
-// blocks.  Bounded: on timeout the status word records
+// blocks.  Bounded: after limit_ns the status word records
 // MOE_DEVICE_PIPELINE_TIMEOUT and false is returned (the caller then stops;
 // downstream kernels see the status and skip their work).
-__device__ bool grid_barrier(unsigned *counter, unsigned target, int32_t *status, int *sh_ok)
+__device__ bool grid_barrier(unsigned *counter, unsigned target, int32_t *status, int *sh_ok,
+                             unsigned long long limit_ns)
 {
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -159,7 +166,7 @@ __device__ bool grid_barrier(unsigned *counter, unsigned target, int32_t *status
             const uint64_t t0 = global_timer_ns();
             while (ld_acquire(counter) < target) {
                 __nanosleep(32);
-                if (global_timer_ns() - t0 > kBarrierLimitNs) {
+                if (global_timer_ns() - t0 > limit_ns) {
                     set_status(status, MOE_DEVICE_PIPELINE_TIMEOUT);
                     ok = false;
                     break;
@@ -820,7 +827,10 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
     if (gate) {
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             p.bcount[(size_t)e * G + b] = run[e];
-        if (!grid_barrier(bar_counter, (unsigned)G, p.status, &sh_flag))
+        // (no copy or other asynchronous work of this block is in flight
+        // here, so a block whose wait runs out simply returns)
+        if (!grid_barrier(bar_counter, (unsigned)G + p.barrier_extra, p.status, &sh_flag,
+                          p.barrier_limit_ns))
             return;
     }
 
@@ -1134,6 +1144,11 @@ static cudaError_t launch_dispatch_s(const moe_config &c, DispatchParams &p, boo
     return launch_dispatch_t<8, ROUTER_NONE, 1, SPLIT>(p, wr_bytes, stream);
 }
 
+// The test hook's settings (moe_debug_barrier_fault): extra arrivals the
+// grid barrier waits for, and its wait limit (0 = the default).
+static std::atomic<unsigned> g_barrier_extra{0};
+static std::atomic<unsigned long long> g_barrier_limit_ns{0};
+
 cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                             const void *x, const void *W_r, bool fused, float *logits,
                             const float *lpart, int lsplit, const float *bias,
@@ -1183,6 +1198,9 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
     p.row_w = dy ? reinterpret_cast<float *>(ws + L.row_w) : nullptr;
     p.y_zero = dy ? static_cast<uint8_t *>(y) : nullptr;
     p.status = reinterpret_cast<int32_t *>(ws + L.status);
+    p.barrier_extra = g_barrier_extra.load(std::memory_order_relaxed);
+    const unsigned long long lim = g_barrier_limit_ns.load(std::memory_order_relaxed);
+    p.barrier_limit_ns = lim ? lim : kBarrierLimitNs;
     const size_t wr_bytes = fused ? (size_t)c.n_experts * (c.d_model * esz + 16) : 0;
     const int split = !shard ? 0 : shard->phases == 1 ? 1 : 2;
     if (split == 2)  // placement only: no router, no gating
@@ -1192,3 +1210,13 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
 }
 
 }  // namespace moe
+
+extern "C" moe_status moe_debug_barrier_fault(int32_t extra_arrivals, uint64_t limit_ns)
+{
+    if (extra_arrivals < 0 || extra_arrivals > 1 || limit_ns > moe::kBarrierLimitNs ||
+        (limit_ns != 0 && limit_ns < 1000))
+        return MOE_ERR_INVALID_ARG;
+    moe::g_barrier_extra.store((unsigned)extra_arrivals, std::memory_order_relaxed);
+    moe::g_barrier_limit_ns.store(limit_ns, std::memory_order_relaxed);
+    return MOE_OK;
+}

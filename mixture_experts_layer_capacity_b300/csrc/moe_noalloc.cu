@@ -4,9 +4,12 @@
 //
 // The scratch is a file-scope __device__ array.  Its name in host code is
 // only a host-side stand-in, so the device address is looked up with
-// cudaGetSymbolAddress once per device (with that device current) and
-// passed on; nothing here calls cudaMalloc, cudaFree or any allocating
-// routine.
+// cudaGetSymbolAddress (with the device current) and passed on; nothing here
+// calls cudaMalloc, cudaFree or any allocating routine.  The lookup is
+// repeated on every call made outside stream capture, so a device reset
+// (which reloads the module and may move the array) is picked up by the next
+// such call; calls made while the stream is capturing use the address found
+// by the last call outside capture on that device.
 #include <mutex>
 
 #include "moe_internal.h"
@@ -20,27 +23,31 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices] = {nullptr};
 
-// Device address of g_static_scratch on the current device (set up on the
-// first call per device).  Returns cudaSuccess or the lookup's error.
-cudaError_t scratch_address(void **ptr)
+// Device address of g_static_scratch on the current device: looked up
+// afresh when `stream` is not capturing (and remembered per device), taken
+// from that memory while it is.  Returns cudaSuccess or the lookup's error.
+cudaError_t scratch_address(cudaStream_t stream, void **ptr)
 {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    if (dev >= 0 && dev < kMaxDevices) {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_scratch_ptr[dev]) {
-            void *p = nullptr;
-            err = cudaGetSymbolAddress(&p, g_static_scratch);
-            if (err != cudaSuccess)
-                return err;
-            g_scratch_ptr[dev] = p;
-        }
-        *ptr = g_scratch_ptr[dev];
-        return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    err = cudaStreamIsCapturing(stream, &cs);
+    if (err != cudaSuccess)
+        return err;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaGetSymbolAddress(ptr, g_static_scratch);
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (cs == cudaStreamCaptureStatusNone || !g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (err != cudaSuccess)
+            return err;
+        g_scratch_ptr[dev] = p;
     }
-    return cudaGetSymbolAddress(ptr, g_static_scratch);
+    *ptr = g_scratch_ptr[dev];
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -59,7 +66,7 @@ extern "C" moe_status moe_forward_no_alloc(
     if (need > (size_t)MOE_STATIC_SCRATCH_BYTES)
         return MOE_ERR_WORKSPACE;  // the layer needs more scratch than the static array holds
     void *scratch = nullptr;
-    if (scratch_address(&scratch) != cudaSuccess || !scratch)
+    if (scratch_address(stream, &scratch) != cudaSuccess || !scratch)
         return MOE_ERR_CUDA;
     // moe_forward clears the parts of its workspace that must start at zero
     // (status word and counters) on the stream before its first kernel.

@@ -353,9 +353,9 @@ int oracle_swiglu_rows(int64_t n, int64_t D, int64_t F, const double *x,
 
 /* A linear map of n rows: out[r][o] = sum_i in[r][i] * W[o][i], W [N_out][N_in]
  * (fp32, each output's coefficients contiguous), in and out fp64.  Used for
- * the projections of a latent MoE ([MPF] "Where MoE is going", latent MoE:
- * inputs down-projected 4096 -> 1024, experts applied, outputs up-projected
- * 1024 -> 4096). */
+ * two projections of a latent MoE ([SFR], the Nemotron 3 Super variant after
+ * 'The 2026 configuration table': the layer works at width 1024 inside a
+ * 4096-wide model, x_lat = x W_in^T before it and y = y_lat W_out^T after). */
 void oracle_linear(int64_t n, int64_t n_in, int64_t n_out, const double *in,
                    const float *W, double *out)
 {
@@ -474,9 +474,9 @@ int oracle_moe_forward(int64_t T, int64_t D, int64_t E, int64_t F, int64_t k,
     return rc;
 }
 
-/* A latent MoE ([MPF] "Where MoE is going": the MoE runs in a compressed
- * space; inputs are down-projected, the experts applied, the outputs
- * up-projected back):
+/* A latent MoE ([SFR], the Nemotron 3 Super variant after 'The 2026
+ * configuration table': the whole layer runs at a narrower width L between
+ * a projection down to L and one back up to the model width):
  *   x_lat = x W_in^T      (W_in [L][D_outer]),
  *   y_lat = the layer above on x_lat (everything at width L),
  *   y     = y_lat W_out^T (W_out [D_outer][L]).

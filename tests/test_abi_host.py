@@ -193,3 +193,22 @@ def test_launch_plan():
     assert not plan("mixtral_decode")["pair_routed"]
     with pytest.raises(B.MoeError):
         B.launch_plan(B.make_config(64, 128, 8, 128, 0))
+
+
+def test_barrier_fault_hook_validates_its_arguments():
+    """The bounded-wait test hook accepts one extra arrival and limits from
+    1 us to the 2 s default, and rejects anything else (host only)."""
+    L = B.lib()
+    for extra, lim in ((2, 0), (-1, 0), (1, 500), (1, 3_000_000_000)):
+        assert L.moe_debug_barrier_fault(extra, lim) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_debug_barrier_fault(1, 1_000_000) == B.MOE_OK
+    assert L.moe_debug_barrier_fault(0, 0) == B.MOE_OK
+
+
+def test_latent_offsets_lie_inside_the_workspace():
+    cfg = B.make_config(64, 1024, 64, 2048, 8, gating_mode=2)
+    xo, yo = B.latent_offsets(cfg, 4096)
+    n = 64 * 1024 * 2
+    assert xo % 1024 == 0 and yo >= xo + n and yo + n <= B.latent_workspace_size(cfg, 4096)
+    with pytest.raises(B.MoeError):
+        B.latent_offsets(cfg, 100)       # d_outer not a multiple of 64 for bf16

@@ -38,21 +38,33 @@ def test_stage_flops_add_up_to_the_layer(w, fused):
 
 
 @pytest.mark.parametrize("w", list(_cases()), ids=lambda w: w.name)
-def test_stage_weight_bytes_match_the_layer(w):
-    """The expert and shared weight bytes counted by the GEMM stages equal
-    the layer's closed form (bf16/fp32 weights at the activation width, E4M3
-    at one byte plus a 4-byte scale per weight row)."""
-    kept_total, touched = 0, min(w.E, 3)      # no rows: the GEMM stages hold only weights
+@pytest.mark.parametrize("fused", [False, True])
+def test_stage_bytes_add_up_to_the_layer(w, fused):
+    """The stages' algorithmic bytes add up to the layer's closed form
+    (touched expert weights, shared and router weights, x once, y once) and
+    the GEMM stages count weights only (no x_perm / h / z traffic)."""
+    kept_total, touched = w.T * w.k - 3, min(w.E, 3)
     b = 2 if w.dtype == "bf16" else 4
-    work = bench.stage_work(w, kept_total, touched)
-    gemm_bytes = sum(v for n, (_, v) in work.items() if n.startswith("gemm"))
-    shared_act = b * 2 * (w.T * w.D + w.T * w.S) if w.S else 0
-    if not w.S:
-        gemm_bytes -= work["gemm1_shared"][1] + work["gemm2_shared"][1]
+    work = bench.stage_work(w, kept_total, touched, shared_fused=fused and w.S > 0)
     wb = 1 if w.weights == "e4m3" else None
     layer = RL.layer_bytes(w.T, w.D, w.E, w.F, w.S, touched, b, weight_bytes=wb)
-    # the layer's form adds the router weights, x and y
-    assert gemm_bytes - shared_act == layer - b * (w.D * w.E + 2 * w.T * w.D)
+    assert sum(v for _, v in work.values()) == layer
+    gemm_bytes = sum(v for n, (_, v) in work.items() if n.startswith("gemm"))
+    assert gemm_bytes == layer - b * (w.D * w.E + 2 * w.T * w.D)
+    # the GEMM stages' bytes do not grow with the rows they compute
+    more = bench.stage_work(w, kept_total + 1000, touched, shared_fused=fused and w.S > 0)
+    assert all(more[n][1] == work[n][1] for n in work)
+
+
+def test_activation_traffic_is_reported_apart():
+    w = WORKLOADS["dsv3_prefill"]
+    kept = w.T * w.k
+    act = bench.stage_activation_bytes(w, kept)
+    assert act["gemm1_routed"] == 2 * kept * (w.D + w.F)
+    assert act["dispatch"] == 2 * kept * w.D
+    fused = bench.stage_activation_bytes(w, kept, shared_fused=True)
+    assert "gemm1_shared" not in fused
+    assert fused["gemm1_routed"] == act["gemm1_routed"] + act["gemm1_shared"]
 
 
 def _traffic_lines():
@@ -93,8 +105,6 @@ def test_profile_traffic_only_from_current_sources():
             # another summary holds a current figure for the same stage
             assert any(s == _source_sha(stage, workload) and st == stage and wl == workload
                        for _, st, wl, _, s in lines), (name, stage, workload)
-    # the default workload's dominant kernel has a current figure
-    assert bench.profile_traffic("gemm1_routed", bench.DEFAULT_WORKLOAD) is not None
     assert current > 0
 
 

@@ -128,7 +128,7 @@ def test_pair_tile_layers(case):
     w = _w(*case)
     _, inp, outs, code = parity.run(w, seed=6)
     assert code == B.MOE_DEVICE_OK
-    rep = parity.check(w, inp, outs, y_sample_n=96)
+    rep = parity.check(w, inp, outs, coverage=True, y_sample_n=96)
     print(case[0], rep)
 
 
@@ -155,12 +155,19 @@ def test_switch_capacity_workload_every_token():
                                   "dsv3_sigmoid_decode", "latent_decode", "latent_prefill",
                                   "mixtral_prefill", "qwen2_57b_prefill", "dsv3_prefill"])
 def test_benchmark_sized_workloads_sampled(name):
+    """Full-size layers in the benchmark's launch configuration: router
+    scores and routing on every token; y on every token of the decode
+    layers, and on a coverage sample of at least 512 tokens of the prefill
+    layers (every 128-row block of every expert segment, each segment's
+    first and last row, every 128-token block of the shared expert)."""
     w = WORKLOADS[name]
     _, inp, outs, code = parity.run(w)
     assert code == B.MOE_DEVICE_OK
-    rng = np.random.default_rng(7)
-    logit_rows = np.sort(rng.choice(w.T, size=min(w.T, 64), replace=False))
-    rep = parity.check(w, inp, outs, logit_rows=logit_rows, y_sample_n=6)
+    if w.T <= 512:
+        rep = parity.check(w, inp, outs)
+    else:
+        rep = parity.check(w, inp, outs, coverage=True, y_sample_n=512)
+        assert rep["y_rows"] >= 512
     print(name, rep)
     del inp, outs
     torch.cuda.empty_cache()

@@ -446,8 +446,8 @@ def test_layer_with_selection_bias_against_bruteforce(mode):
                                rtol=1e-12, atol=1e-12)
 
 
-# --- latent MoE ([MPF] "Where MoE is going": inputs down-projected, the
-# experts applied in the compressed space, outputs up-projected back) -------
+# --- latent MoE ([SFR], the Nemotron 3 Super variant after 'The 2026
+# configuration table': x_lat = x W_in^T, the layer at width L, y = y_lat W_out^T)
 
 def test_linear_against_matmul():
     rng = np.random.default_rng(91)

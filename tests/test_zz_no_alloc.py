@@ -5,7 +5,8 @@ program with no device allocator of its own, or a serving loop that must not
 call cudaMalloc): it runs the same layer with the library's static device
 scratch instead of a caller workspace.  Its outputs must match the existing
 entry point's, on two calls in a row (the scratch keeps the previous call's
-contents, which must not leak into the next call).  This file is collected
+contents, which must not leak into the next call); the two entry points run
+the same kernels, so the outputs must be bit-identical.  This file is collected
 last so that a run stopping at the first failure has run every other test.
 """
 import numpy as np
@@ -16,8 +17,6 @@ from mixture_experts_layer_capacity_b300 import binding as B
 from mixture_experts_layer_capacity_b300.workloads import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
-
-TOL_Y = {"bf16": 2e-2, "fp32": 1e-4}
 
 CASES = [
     WORKLOADS["switch_top1_capacity"],   # k = 1, drops, down projection writes y
@@ -54,19 +53,13 @@ def test_matches_moe_forward_on_two_calls(w):
     inp = make_inputs(w, 11, "cuda")
     ref = B.forward(cfg, inp)
     torch.cuda.synchronize()
+    # the same kernels on the same inputs: every output is bit-identical
+    # (the library's results do not vary from run to run on one device)
     for _ in range(2):
         got = _no_alloc(cfg, inp)
-        for key in ("topk_idx", "dropped_mask", "expert_counts", "kept_counts"):
+        for key in ("y", "router_logits", "topk_idx", "topk_w", "dropped_mask",
+                    "expert_counts", "kept_counts", "aux_loss"):
             assert torch.equal(got[key], ref[key]), key
-        s_ref = ref["router_logits"].double()
-        assert float((got["router_logits"].double() - s_ref).abs().max()) <= \
-            1e-3 * float(s_ref.abs().max())
-        assert float((got["topk_w"] - ref["topk_w"]).abs().max()) <= 1e-5
-        a, b = float(got["aux_loss"][0]), float(ref["aux_loss"][0])
-        assert abs(a - b) <= 1e-5 * abs(b) + 1e-9
-        y_ref = ref["y"].double()
-        err = float((got["y"].double() - y_ref).abs().max()) / max(float(y_ref.abs().max()), 1e-30)
-        assert err <= TOL_Y[w.dtype], err
 
 
 def test_rejects_layers_larger_than_the_static_scratch():
