@@ -603,12 +603,11 @@ def run_ours(args, rank, world, device):
         rates[name] = nb / (best / 1e3) / 1e9
 
     # router (unless fused into dispatch), dispatch, GEMM1, GEMM2 (+ two
-    # shared-expert GEMMs), combine (unless GEMM2 writes y)
+    # shared-expert GEMMs), combine (unless GEMM2 writes y); a latent layer
+    # adds its two projections
     plan = B.launch_plan(cfg)
-    # (with pair tails each routed GEMM is two launches: full 256-row tiles on
-    # pairs, segment remainders on single CTAs)
     launches_per_step = (2 if w.D_outer else 0) + \
-        (0 if plan["router_fused"] else 1) + 3 + (2 if plan["pair_tails"] else 0) + \
+        (0 if plan["router_fused"] else 1) + 3 + \
         (2 if w.S and not plan["shared_fused"] else 0) + (0 if plan["direct_y"] else 1)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,

@@ -113,6 +113,11 @@ typedef struct {
 #define MOE_DEVICE_LAUNCH_MISMATCH 3   /* a kernel got less shared memory than its layout needs */
 #define MOE_DEVICE_SHARD_MISMATCH 4    /* split batch: the exchanged counts do not hold
                                           this rank's own or do not add up to T_global*k */
+#define MOE_DEVICE_INDEX_OUT_OF_RANGE 5 /* an expert index outside [0, E), or a row that
+                                          falls outside its expert's segment: checked on
+                                          the topk_idx a caller hands to moe_sharded_finish,
+                                          and on every index the routing and combine
+                                          kernels use in a build with MOE_DEBUG_BOUNDS */
 
 /* Bytes of scratch moe_forward needs for `cfg` (x gathered by expert, the
  * SwiGLU hidden rows, per-expert scan tables, ...).  Returns
@@ -172,9 +177,12 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
 #define MOE_PLAN_PAIR_SHARED 8    /* shared-expert GEMMs on CTA pairs */
 #define MOE_PLAN_SHARED_FUSED 16  /* shared-expert tiles run inside the routed GEMM
                                      launches (no separate shared launches) */
-#define MOE_PLAN_PAIR_TAILS 32    /* with CTA pairs, each routed GEMM is two launches:
-                                     full 256-row tiles on pairs, each expert's
-                                     remaining rows in 128-row tiles on single CTAs */
+#define MOE_PLAN_PAIR_TAILS 32    /* with CTA pairs, each expert's rows past its last
+                                     full 256-row tile run as "swap" units in the
+                                     same launch: its weights are the MMA's 256-row
+                                     operand and those few token rows (rounded up
+                                     to 32) the other, so they are not padded to
+                                     256 rows */
 MOE_API moe_status moe_launch_plan(const moe_config *cfg, int32_t *flags);
 
 /* Workspace bytes moe_latent_forward needs for `cfg` (whose d_model is the

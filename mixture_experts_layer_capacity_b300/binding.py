@@ -14,7 +14,9 @@ import threading
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libmoe.so")
+# MOE_LIBRARY selects another build of the same library, e.g. the one with
+# index range checks (libmoe_debug_bounds.so, see build.py)
+LIB_PATH = os.environ.get("MOE_LIBRARY") or os.path.join(_PKG, "libmoe.so")
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
@@ -31,6 +33,7 @@ MOE_DEVICE_NONFINITE_SCORE = 1
 MOE_DEVICE_PIPELINE_TIMEOUT = 2
 MOE_DEVICE_LAUNCH_MISMATCH = 3
 MOE_DEVICE_SHARD_MISMATCH = 4
+MOE_DEVICE_INDEX_OUT_OF_RANGE = 5
 
 
 class MoeError(RuntimeError):

@@ -1,12 +1,18 @@
 """Build ``libmoe.so`` in-tree with nvcc for sm_103a.
 
-    python -m mixture_experts_layer_capacity_b300.build [--force]
+    python -m mixture_experts_layer_capacity_b300.build [--force] [--debug-bounds]
 
 Each ``csrc/*.cu`` compiles to an object under ``_build/`` (rebuilt when the
 source or any header is newer), then the objects link into
 ``mixture_experts_layer_capacity_b300/libmoe.so`` against the shared CUDA
 runtime.  The driver API (tensor-map encoding) is reached through the
 runtime's entry-point query, so libcuda is not linked.
+
+``--debug-bounds`` builds the same sources with ``-DMOE_DEBUG_BOUNDS`` into
+``libmoe_debug_bounds.so``: the routing and combine kernels then check every
+expert and row index against its range and record
+MOE_DEVICE_INDEX_OUT_OF_RANGE instead of making the access.  Load it by
+setting ``MOE_LIBRARY`` to its path before the binding is first used.
 """
 from __future__ import annotations
 
@@ -21,6 +27,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build", "libmoe")
 LIB = os.path.join(PKG, "libmoe.so")
+BUILD_DEBUG = os.path.join(ROOT, "_build", "libmoe_debug_bounds")
+LIB_DEBUG = os.path.join(PKG, "libmoe_debug_bounds.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
@@ -36,18 +44,20 @@ def _newest(paths):
     return max((os.path.getmtime(p) for p in paths), default=0.0)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug_bounds: bool = False) -> str:
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug_bounds else (BUILD, LIB)
+    flags = FLAGS + (["-DMOE_DEBUG_BOUNDS"] if debug_bounds else [])
+    os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr_time = _newest(_headers())
     jobs = []
     objs = []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or not os.path.exists(obj) or os.path.getmtime(obj) < max(
                 os.path.getmtime(src), hdr_time):
-            jobs.append([NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj])
+            jobs.append([NVCC, *ARCH, *flags, "-c", src, "-o", obj])
 
     def run(cmd):
         if verbose:
@@ -60,14 +70,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=min(8, max(1, len(jobs)))) as ex:
         list(ex.map(run, jobs))
-    if jobs or not os.path.exists(LIB) or os.path.getmtime(LIB) < _newest(objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if jobs or not os.path.exists(lib) or os.path.getmtime(lib) < _newest(objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([NVCC, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
              "-Xlinker", "-rpath,/usr/local/cuda/lib64"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose=True,
+                debug_bounds="--debug-bounds" in sys.argv))

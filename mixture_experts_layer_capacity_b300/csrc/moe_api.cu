@@ -118,11 +118,11 @@ LaunchPlan plan_of(const moe_config &c)
                      routed_rows >= 2LL * 2 * kTileM * c.n_experts;
     pl.pair_shared = bf16 && c.d_shared > 0 && c.T >= kPairMinRows / 4;
     pl.shared_fused = bf16 && c.d_shared > 0 && !pl.pair_routed && !pl.pair_shared;
-    // 256-row pair tiles pad about E * 128 rows over all segments; with many
-    // experts (>= 128) the remainders run better as 128-row tiles in a second
-    // launch (DeepSeek-V3-shaped prefill: 25 % padding, routed GEMMs 7 %
-    // faster); with 64 experts the second launch cost more than it saved
-    pl.pair_tails = pl.pair_routed && c.n_experts >= 128;
+    // 256-row pair tiles over whole segments would pad about E * 128 rows;
+    // each segment's remainder runs instead as swap units (weights as the
+    // 256-row operand, the remaining token rows rounded up to 32 as the
+    // other) interleaved with the full tiles of the same launch
+    pl.pair_tails = pl.pair_routed;
     pl.router_splits = router_splits(c);
     return pl;
 }

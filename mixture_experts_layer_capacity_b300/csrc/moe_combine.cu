@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(kCombineThreads)
                         const float *__restrict__ zs_part, int zsplit,
                         const float *__restrict__ topk_w, const int32_t *__restrict__ row_of,
                         __nv_bfloat16 *__restrict__ y, int T, int k, int D, int nchunk,
-                        const int32_t *status)
+                        long long R_max, int32_t *status)
 {
     __shared__ int rows[kMaxTopK];
     __shared__ float ws[kMaxTopK];
@@ -39,7 +39,12 @@ __global__ void __launch_bounds__(kCombineThreads)
         return;  // an earlier kernel failed; y is left unspecified
     const int t = blockIdx.x / nchunk, chunk = blockIdx.x - (blockIdx.x / nchunk) * nchunk;
     if ((int)threadIdx.x < k) {
-        rows[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
+        int r = row_of[(size_t)t * k + threadIdx.x];
+        if (kDebugBounds && r >= R_max) {
+            set_status(status, MOE_DEVICE_INDEX_OUT_OF_RANGE);
+            r = -1;
+        }
+        rows[threadIdx.x] = r;
         ws[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
     }
     __syncthreads();
@@ -106,7 +111,7 @@ __global__ void __launch_bounds__(kCombineThreads)
 __global__ void __launch_bounds__(128)
     combine_f32_kernel(const float *__restrict__ z, const float *__restrict__ zs,
                        const float *__restrict__ topk_w, const int32_t *__restrict__ row_of,
-                       float *__restrict__ y, int k, int D, const int32_t *status)
+                       float *__restrict__ y, int k, int D, long long R_max, int32_t *status)
 {
     __shared__ int rows[kMaxTopK];
     __shared__ float ws[kMaxTopK];
@@ -116,7 +121,12 @@ __global__ void __launch_bounds__(128)
         return;  // an earlier kernel failed; y is left unspecified
     const int t = blockIdx.x;
     if ((int)threadIdx.x < k) {
-        rows[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
+        int r = row_of[(size_t)t * k + threadIdx.x];
+        if (kDebugBounds && r >= R_max) {
+            set_status(status, MOE_DEVICE_INDEX_OUT_OF_RANGE);
+            r = -1;
+        }
+        rows[threadIdx.x] = r;
         ws[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
     }
     __syncthreads();
@@ -150,7 +160,7 @@ cudaError_t launch_combine(const moe_config &c, const WorkspaceLayout &L, uint8_
         configured.done(dev);
     }
     const int32_t *row_of = reinterpret_cast<const int32_t *>(ws + L.row_of);
-    const int32_t *status = reinterpret_cast<const int32_t *>(ws + L.status);
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
     const bool shared = c.d_shared > 0;
     if (c.dtype == MOE_DTYPE_BF16) {
         const int nchunk = (c.d_model / 8 + kCombineThreads - 1) / kCombineThreads;
@@ -164,12 +174,12 @@ cudaError_t launch_combine(const moe_config &c, const WorkspaceLayout &L, uint8_
                           dim3(kCombineThreads), 0, stream,
                           reinterpret_cast<const __nv_bfloat16 *>(ws + L.z), zs, zs_part, zsplit,
                           topk_w, row_of, (__nv_bfloat16 *)y, c.T, c.top_k, c.d_model, nchunk,
-                          status);
+                          (long long)L.R_max, status);
     }
     return launch_pdl(combine_f32_kernel, dim3(c.T), dim3(128), 0, stream,
                       reinterpret_cast<const float *>(ws + L.z),
                       shared ? reinterpret_cast<const float *>(ws + L.zs) : nullptr, topk_w,
-                      row_of, (float *)y, c.top_k, c.d_model, status);
+                      row_of, (float *)y, c.top_k, c.d_model, (long long)L.R_max, status);
 }
 
 }  // namespace moe

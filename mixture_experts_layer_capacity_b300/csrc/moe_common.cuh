@@ -8,6 +8,16 @@
 
 namespace moe {
 
+// Builds with MOE_DEBUG_BOUNDS check every expert and row index the routing
+// and combine kernels use against its range, record
+// MOE_DEVICE_INDEX_OUT_OF_RANGE in the status word and skip the access
+// instead of performing it.
+#ifdef MOE_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 

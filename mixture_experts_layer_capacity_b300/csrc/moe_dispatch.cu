@@ -103,6 +103,7 @@ struct DispatchParams {
     // moe_debug_barrier_fault, which makes the barrier run out)
     unsigned barrier_extra;
     unsigned long long barrier_limit_ns;
+    long long R_max;            // rows of x_perm (bound of every row index)
 };
 
 // ------------------------------------------------------------ block helpers
@@ -807,7 +808,11 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
             const int u = i / k, j = i - (i / k) * k;
             const int tok = chunk * cs + u;
             if (tok < p.T) {
-                const int e = ibuf[u * k + j];
+                int e = ibuf[u * k + j];
+                if (kDebugBounds && (unsigned)e >= (unsigned)E) {
+                    set_status(p.status, MOE_DEVICE_INDEX_OUT_OF_RANGE);
+                    e = 0;
+                }
                 const int r = run[e] + __popc(mask[e] & ((1u << u) - 1u));
                 p.rank[(size_t)tok * k + j] = r;
                 rbuf[u * k + j] = r;
@@ -959,9 +964,22 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
             // a one-chunk block still holds its assignments in shared memory
             const int u = (t - t_beg) * k + lane;
             const int e = held ? ibuf[u] : __ldcg(p.topk_idx + tk);
-            const long long pos = (long long)s_base[e] + (held ? rbuf[u] : __ldcg(p.rank + tk));
-            const bool kept = (p.C < 0) || (pos + s_rb[e] < p.C);
-            row = kept ? (long long)s_seg[e] + pos : -1;
+            // the finish launch of a split batch reads topk_idx as the caller
+            // hands it back: an expert index outside [0, E), or a kept row
+            // outside its expert's segment, is refused rather than followed
+            // (every index is checked in a MOE_DEBUG_BOUNDS build)
+            constexpr bool kCheck = SPLIT == 2 || kDebugBounds;
+            bool idx_ok = !kCheck || (unsigned)e < (unsigned)E;
+            const int es = idx_ok ? e : 0;
+            const long long pos = (long long)s_base[es] + (held ? rbuf[u] : __ldcg(p.rank + tk));
+            bool kept = idx_ok && ((p.C < 0) || (pos + s_rb[es] < p.C));
+            row = kept ? (long long)s_seg[es] + pos : -1;
+            if (kCheck && kept && (pos < 0 || row >= s_seg[es + 1] || row >= p.R_max)) {
+                idx_ok = kept = false;
+                row = -1;
+            }
+            if (kCheck && !idx_ok)
+                set_status(p.status, MOE_DEVICE_INDEX_OUT_OF_RANGE);
             if (part == 0) {
                 p.dropped[tk] = kept ? 0 : 1;
                 p.row_of[tk] = (int32_t)row;
@@ -1193,6 +1211,7 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
     p.mtile = reinterpret_cast<int32_t *>(ws + L.mtile);
     p.row_of = reinterpret_cast<int32_t *>(ws + L.row_of);
     p.x_perm = ws + L.x_perm;
+    p.R_max = L.R_max;
     const bool dy = direct_y(c) && c.dtype == MOE_DTYPE_BF16;
     p.row_tok = dy ? reinterpret_cast<int32_t *>(ws + L.row_tok) : nullptr;
     p.row_w = dy ? reinterpret_cast<float *>(ws + L.row_w) : nullptr;

@@ -66,15 +66,15 @@ struct TcParams {
     // are the kernel's second set of tensor maps.  sh_tiles = 0: none.
     int sh_tiles;            // dense tiles of the second problem (row tiles x column tiles)
     int sh_rows, sh_K, sh_n_tiles, sh_N_valid;
-    // grouped problems split between the CTA-pair kernel (full 256-row tiles)
-    // and the single-CTA kernel (each segment's remaining rows, 128-row tiles):
-    int pair_full_only;      // pair kernel: only the floor(n / 256) full tiles of a segment
-    int tail_after;          // single-CTA kernel: > 0: only the rows after the first
-                             // floor(n / tail_after) * tail_after rows of each segment
     int sh_ksplit;           // splits of the second problem's reduction (fp32 partial
                              // outputs part_stride apart, EPI_BF16 kernels only); 0/1 = none
     void *sh_out;
     long long sh_ld_out;
+    // pair kernel, grouped: each segment's full 256-row tiles as usual, and
+    // its remaining rows (fewer than 256) as swap units in the same launch:
+    // the weights become the MMA's M = 256 operand and the few token rows
+    // its N operand (padded to a multiple of 32, not to 256 rows)
+    int swap_tails;
 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any tile
@@ -152,10 +152,7 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams &p, const int *s_se
     ti.n_idx = local / mt_e;
     const int m = local - ti.n_idx * mt_e;
     ti.seg = lo;
-    int s0 = s_seg[lo];
-    if (p.tail_after > 0)
-        s0 += (s_seg[lo + 1] - s_seg[lo]) / p.tail_after * p.tail_after;
-    ti.a_row0 = s0 + m * kTileM;
+    ti.a_row0 = s_seg[lo] + m * kTileM;
     ti.rows = min(kTileM, s_seg[lo + 1] - ti.a_row0);
     return ti;
 }
@@ -406,32 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.mtile && !failed) {
         for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
             tables[i] = p.seg_off[i];
-            if (p.tail_after <= 0)
-                tables[kMaxExperts + 1 + i] = p.mtile[i];
+            tables[kMaxExperts + 1 + i] = p.mtile[i];
         }
-    }
-    __syncthreads();
-    if (p.tail_after > 0 && p.mtile && !failed && warp == 0) {
-        // 128-row tiles of each segment's rows past its last full
-        // tail_after-row block, prefix-summed
-        int carry = 0;
-        for (int e0 = 0; e0 < p.nseg; e0 += 32) {
-            const int e = e0 + lane;
-            const int n = e < p.nseg ? tables[e + 1] - tables[e] : 0;
-            const int v = (n - n / p.tail_after * p.tail_after + kTileM - 1) / kTileM;
-            int incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o)
-                    incl += t;
-            }
-            if (e < p.nseg)
-                tables[kMaxExperts + 1 + e + 1] = carry + incl;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0)
-            tables[kMaxExperts + 1] = 0;
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -616,17 +589,32 @@ struct PairShape {
     static constexpr int B_HALF_ROWS = UMMA_N / 2;   // B rows staged by each CTA
     static constexpr int A_BYTES = kTileM * 64 * 2;
     static constexpr int B_BYTES = B_HALF_ROWS * 64 * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    // a stage: the A slot and the B slot (full tiles), then the token rows of
+    // a swap unit, which fills both slots with weight rows
+    static constexpr int TOK_BYTES = 4096;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + TOK_BYTES;
     static constexpr int TMEM_COLS = 2 * UMMA_N <= 256 ? 256 : 512;
-    static constexpr int TABLE_BYTES = 2 * (kMaxExperts + 1) * 4 + 8;
+    // segment offsets, full-tile prefix, swap-chunk prefix
+    static constexpr int TABLE_BYTES = 3 * (kMaxExperts + 1) * 4 + 8;
+    // reduction steps (64 wide) per swap stage: GEMM1 takes one (gate rows in
+    // the A slot, up rows in the B slot), GEMM2 two when the B slot holds 128
+    // weight rows (a 64-wide step each in the A and B slots), else one
+    static constexpr int SWAP_KPS = (NB == 1 && B_HALF_ROWS == kTileM) ? 2 : 1;
+    // token rows per swap unit: each CTA stages half of them per step
+    static constexpr int SWAP_ROWS = 2 * TOK_BYTES / (SWAP_KPS * 128);
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + TABLE_BYTES + 1024;
     static_assert(UMMA_N == 128 || UMMA_N == 256, "pair UMMA N");
     static_assert(NB == 1 || B_HALF_ROWS == BN, "gate/up halves");
     static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
+    static_assert(SWAP_ROWS % 32 == 0 && SWAP_ROWS <= UMMA_N && SWAP_ROWS <= 128,
+                  "swap unit columns fit the accumulator (GEMM1: gate and up halves)");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
 constexpr int kPairRows = 2 * kTileM;
+constexpr int kSwapBoxRows = 16;   // token rows per TMA box of a swap unit
+constexpr int kSwapFeat = 256;     // features per swap unit: 128 weight rows per CTA
+                                   // (GEMM1: of both the gate and the up matrix)
 
 __device__ __forceinline__ int pair_tile_count(const TcParams &p, const int *s_mt)
 {
@@ -667,13 +655,122 @@ __device__ __forceinline__ TileInfo pair_tile_info(const TcParams &p, const int 
     return ti;
 }
 
+// One CTA pair's work list with swap units: its share of the full tiles
+// (g = cluster, cluster + NC, ...) and of the swap units (likewise),
+// interleaved evenly in time.  Every role of both CTAs walks the same
+// sequence.
+struct PairSched {
+    int cid, NC, a, b, i, j;
+    __device__ __forceinline__ PairSched(int cid_, int NC_, int n_full, int n_swap)
+        : cid(cid_), NC(NC_), i(0), j(0)
+    {
+        a = n_full > cid ? (n_full - cid + NC - 1) / NC : 0;
+        b = n_swap > cid ? (n_swap - cid + NC - 1) / NC : 0;
+    }
+    // Next unit: returns false when none is left; `swap` tells the kind and
+    // `g` its index in that kind's list.
+    __device__ __forceinline__ bool next(bool &swap, int &g)
+    {
+        if (i >= a && j >= b)
+            return false;
+        // unit i of a at time (2i+1)/(2a), unit j of b at (2j+1)/(2b)
+        swap = i >= a || (j < b && (long long)(2 * j + 1) * a < (long long)(2 * i + 1) * b);
+        g = cid + NC * (swap ? j++ : i++);
+        return true;
+    }
+};
+
+// A swap unit: token rows [r0, r0 + rv) of segment `seg` (rv <= swap_rows,
+// n = rv rounded up to 32, the MMA's N), feature block fb (kSwapFeat
+// features: weight rows fb * kSwapFeat + rank * 128 ... of each CTA).
+struct SwapInfo {
+    int seg, fb, r0, rv, n;
+};
+
+// Swap unit u: chunk-major (a segment of fewer than 256 rows is cut into
+// chunks of swap_rows), feature block minor, so the units of one chunk run
+// at about the same time on neighbouring pairs and share its token rows in
+// L2.  s_sw: prefix sum of chunks per segment.
+__device__ __forceinline__ SwapInfo swap_info(const int *s_seg, const int *s_sw, int nseg,
+                                              int n_fb, int swap_rows, int u)
+{
+    SwapInfo si;
+    const int gc = u / n_fb;
+    si.fb = u - gc * n_fb;
+    int lo = 0, hi = nseg;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_sw[mid] <= gc)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    si.seg = lo;
+    si.r0 = s_seg[lo] + (gc - s_sw[lo]) * swap_rows;
+    si.rv = min(swap_rows, s_seg[lo + 1] - si.r0);
+    si.n = (si.rv + 31) & ~31;
+    return si;
+}
+
+// Epilogue of a swap unit (pair kernel).  The accumulator holds weight rows
+// (this CTA's 128 features) in TMEM lanes and token rows in columns: column c
+// is token row si.r0 + c, valid for c < si.rv.
+//   GEMM1 (EPI_SWIGLU): gate in columns [0, n), up in [128, 128 + n) of the
+//     same lanes, so each thread combines its own two values;
+//   GEMM2 (EPI_BF16 / EPI_BF16_Y): one output feature per lane.
+// A thread stores one value per token row; a warp's 32 lanes write 64
+// contiguous bytes of the row.  taddr: this warp's lane quarter of the buffer.
+template <int EPI>
+__device__ __forceinline__ void swap_epilogue(const TcParams &p, uint32_t taddr, int q, int lane,
+                                              int rank, const SwapInfo &si)
+{
+    __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.out);
+    const int f = si.fb * kSwapFeat + rank * kTileM + q * 32 + lane;
+    const bool f_ok = f < p.N_valid;
+#pragma unroll 1
+    for (int c0 = 0; c0 < si.n; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + c0, v);
+        if constexpr (EPI == EPI_SWIGLU) {
+            uint32_t u[32];
+            tmem_ld32(taddr + kTileM + c0, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                v[c] = __float_as_uint(silu_f32(__uint_as_float(v[c])) * __uint_as_float(u[c]));
+        } else {
+            tmem_wait_ld();
+        }
+        if (f_ok) {
+            const int nc = si.rv - c0;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                if (c >= nc)
+                    break;
+                const int row = si.r0 + c0 + c;
+                if constexpr (EPI == EPI_BF16_Y) {
+                    const int tok = p.row_tok[row];
+                    out[(long long)tok * p.ld_out + f] =
+                        __float2bfloat16_rn(p.row_w[row] * __uint_as_float(v[c]));
+                } else {
+                    out[(long long)row * p.ld_out + f] = __float2bfloat16_rn(__uint_as_float(v[c]));
+                }
+            }
+        }
+    }
+}
+
 template <int BN, int NB, int EPI, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap mA,
                         const __grid_constant__ CUtensorMap mB0,
-                        const __grid_constant__ CUtensorMap mB1, const TcParams p)
+                        const __grid_constant__ CUtensorMap mB1,
+                        const __grid_constant__ CUtensorMap wS0,
+                        const __grid_constant__ CUtensorMap wS1,
+                        const __grid_constant__ CUtensorMap tS, const TcParams p)
 {
     using S = PairShape<BN, NB, STAGES>;
+    static_assert(EPI == EPI_SWIGLU ? NB == 2 : NB == 1, "pair epilogues");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
@@ -688,12 +785,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *tables = reinterpret_cast<int *>(smem + STAGES * S::STAGE_BYTES + 256);
     int *s_seg = p.mtile ? tables : nullptr;
     int *s_mt = p.mtile ? tables + (kMaxExperts + 1) : nullptr;
+    int *s_sw = p.mtile ? tables + 2 * (kMaxExperts + 1) : nullptr;
 
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const int cluster_id = (int)(blockIdx.x >> 1), nclusters = (int)(gridDim.x >> 1);
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
+    const bool swap_mode = p.swap_tails && p.mtile;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -713,6 +812,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&mB0);
         if (NB == 2)
             tma_prefetch_desc(&mB1);
+        if (swap_mode) {
+            tma_prefetch_desc(&wS0);
+            if (NB == 2)
+                tma_prefetch_desc(&wS1);
+            tma_prefetch_desc(&tS);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, S::TMEM_COLS);
@@ -725,26 +830,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x)
             s_seg[i] = p.seg_off[i];
     __syncthreads();
-    // pair tiles per segment (256 rows each), prefix-summed by warp 0
+    // pair tiles per segment (256 rows each, the last one padded) and, with
+    // swap units, the chunks of each segment of fewer than 256 rows (which
+    // then has no pair tile), prefix-summed by warp 0.  A segment with pair
+    // tiles keeps its remainder in a padded pair tile next to its other row
+    // tiles, so its weight tiles are still shared through L2.
     if (p.mtile && !failed && warp == 0) {
-        int carry = 0;
+        int carry = 0, carry_sw = 0;
         for (int e0 = 0; e0 < p.nseg; e0 += 32) {
             const int e = e0 + lane;
             const int n = e < p.nseg ? s_seg[e + 1] - s_seg[e] : 0;
-            const int v = p.pair_full_only ? n / kPairRows : (n + kPairRows - 1) / kPairRows;
-            int incl = v;
+            const bool small = swap_mode && n < kPairRows;
+            const int v = small ? 0 : (n + kPairRows - 1) / kPairRows;
+            const int vs = small ? (n + S::SWAP_ROWS - 1) / S::SWAP_ROWS : 0;
+            int incl = v, incl_s = vs;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o)
-                    incl += n;
+                const int n1 = __shfl_up_sync(0xffffffffu, incl, o);
+                const int n2 = __shfl_up_sync(0xffffffffu, incl_s, o);
+                if (lane >= o) {
+                    incl += n1;
+                    incl_s += n2;
+                }
             }
-            if (e < p.nseg)
+            if (e < p.nseg) {
                 s_mt[e + 1] = carry + incl;
+                s_sw[e + 1] = carry_sw + incl_s;
+            }
             carry += __shfl_sync(0xffffffffu, incl, 31);
+            carry_sw += __shfl_sync(0xffffffffu, incl_s, 31);
         }
-        if (lane == 0)
+        if (lane == 0) {
             s_mt[0] = 0;
+            s_sw[0] = 0;
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -752,9 +871,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int tiles_all = failed ? 0 : pair_tile_count(p, s_mt);
-    const int NC = balanced_workers(tiles_all, nclusters);
-    const int ntiles = cluster_id < NC ? tiles_all : 0;
+    // feature blocks of the swap units (kSwapFeat features each)
+    const int n_fb = (p.N_valid + kSwapFeat - 1) / kSwapFeat;
+    const int n_full = failed ? 0 : pair_tile_count(p, s_mt);
+    const int n_swap = (failed || !swap_mode) ? 0 : s_sw[p.nseg] * n_fb;
+    const int NC = balanced_workers(n_full + n_swap, nclusters);
+    const bool active = cluster_id < NC;
     const int nk = (p.K + 63) / 64;
 
     if (warp == 0) {
@@ -765,24 +887,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             long long fills = 0;
             bool ok = true;
-            for (int g = cluster_id; g < ntiles && ok; g += NC) {
-                const TileInfo ti = pair_tile_info(p, s_seg, s_mt, g);
-                const int a_row = ti.a_row0 + (int)rank * kTileM;
-                const int b_row = ti.seg * p.b_seg_rows + ti.n_idx * BN +
-                                  (NB == 1 ? (int)rank * S::B_HALF_ROWS : 0);
-                const CUtensorMap *mb = (NB == 2 && !leader) ? &mB1 : &mB0;
-                for (int kb = 0; kb < nk; ++kb) {
+            PairSched sched(cluster_id, NC, active ? n_full : 0, active ? n_swap : 0);
+            bool sw;
+            int g;
+            while (ok && sched.next(sw, g)) {
+                int a_row, b_row, t_row = 0, half = 0;
+                const CUtensorMap *ma = &mA, *mb = (NB == 2 && !leader) ? &mB1 : &mB0;
+                uint32_t tx;
+                if (!sw) {
+                    const TileInfo ti = pair_tile_info(p, s_seg, s_mt, g);
+                    a_row = ti.a_row0 + (int)rank * kTileM;
+                    b_row = ti.seg * p.b_seg_rows + ti.n_idx * BN +
+                            (NB == 1 ? (int)rank * S::B_HALF_ROWS : 0);
+                    tx = 2 * (S::A_BYTES + S::B_BYTES);   // both CTAs' slots
+                } else {
+                    const SwapInfo si = swap_info(s_seg, s_sw, p.nseg, n_fb, S::SWAP_ROWS, g);
+                    // this CTA's 128 weight rows of the unit's features (GEMM1:
+                    // of W_gate into the A slot and of W_up into the B slot;
+                    // GEMM2: of W_down, one reduction step per slot) and its
+                    // half of the token rows into the token area
+                    a_row = si.seg * p.b_seg_rows + si.fb * kSwapFeat + (int)rank * kTileM;
+                    half = si.n / 2;
+                    t_row = si.r0 + (int)rank * half;
+                    b_row = 0;
+                    tx = 0;   // per stage below: its last one may hold a single step
+                }
+                const int n_stages = sw ? (nk + S::SWAP_KPS - 1) / S::SWAP_KPS : nk;
+                for (int st = 0; st < n_stages; ++st) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     uint8_t *sa = smem + s * S::STAGE_BYTES;
                     uint8_t *sb = sa + S::A_BYTES;
+                    uint8_t *stok = sb + S::B_BYTES;
                     const uint32_t fb = full_leader + (uint32_t)s * 8u;
-                    if (leader)
-                        mbar_arrive_expect_tx(&full[s], 2 * S::STAGE_BYTES);
-                    tma_load_2d_pair(sa, &mA, fb, kb * 64, a_row);
-                    tma_load_2d_pair(sb, mb, fb, kb * 64, b_row);
+                    if (!sw) {
+                        if (leader)
+                            mbar_arrive_expect_tx(&full[s], tx);
+                        tma_load_2d_pair(sa, ma, fb, st * 64, a_row);
+                        tma_load_2d_pair(sb, mb, fb, st * 64, b_row);
+                    } else {
+                        const int k0 = st * S::SWAP_KPS;
+                        const int steps = min(S::SWAP_KPS, nk - k0);
+                        const uint32_t wbytes = NB == 2 ? 2u * S::A_BYTES : (uint32_t)steps * S::A_BYTES;
+                        if (leader)
+                            mbar_arrive_expect_tx(&full[s],
+                                                  2u * (wbytes + (uint32_t)(steps * half * 128)));
+                        if (NB == 2) {
+                            tma_load_2d_pair(sa, &wS0, fb, k0 * 64, a_row);
+                            tma_load_2d_pair(sb, &wS1, fb, k0 * 64, a_row);
+                        } else {
+                            for (int j = 0; j < steps; ++j)
+                                tma_load_2d_pair(sa + j * S::A_BYTES, &wS0, fb, (k0 + j) * 64, a_row);
+                        }
+                        for (int j = 0; j < steps; ++j)
+                            for (int r = 0; r < half; r += kSwapBoxRows)
+                                tma_load_2d_pair(stok + j * (S::TOK_BYTES / S::SWAP_KPS) + r * 128,
+                                                 &tS, fb, (k0 + j) * 64, t_row + r);
+                    }
                     ++fills;
                     if (++s == STAGES) {
                         s = 0;
@@ -811,30 +974,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer (even CTA)
-            constexpr uint32_t idesc = idesc_bf16_f32(kPairRows, S::UMMA_N);
+            constexpr uint32_t idesc_full = idesc_bf16_f32(kPairRows, S::UMMA_N);
             int s = 0;
             uint32_t ph = 0, b = 0, tph = 0;
             bool ok = true;
-            for (int g = cluster_id; g < ntiles && ok; g += NC) {
+            PairSched sched(cluster_id, NC, active ? n_full : 0, active ? n_swap : 0);
+            bool sw;
+            int g;
+            while (ok && sched.next(sw, g)) {
+                uint32_t idesc = idesc_full;
+                if (sw) {
+                    const SwapInfo si = swap_info(s_seg, s_sw, p.nseg, n_fb, S::SWAP_ROWS, g);
+                    idesc = idesc_bf16_f32(kPairRows, si.n);
+                }
                 if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * S::UMMA_N;
-                for (int kb = 0; kb < nk; ++kb) {
+                const int n_stages = sw ? (nk + S::SWAP_KPS - 1) / S::SWAP_KPS : nk;
+                for (int st = 0; st < n_stages; ++st) {
                     if (!mbar_wait(&full[s], ph, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
                     const uint32_t sa = smem_u32(smem + s * S::STAGE_BYTES);
-                    const uint64_t adesc = sdesc_kmajor_sw128(sa);
-                    const uint64_t bdesc = sdesc_kmajor_sw128(sa + S::A_BYTES);
+                    if (!sw) {
+                        const uint64_t adesc = sdesc_kmajor_sw128(sa);
+                        const uint64_t bdesc = sdesc_kmajor_sw128(sa + S::A_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_pair(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
-                                       (kb > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_bf16_pair(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                           (st > 0 || kk > 0) ? 1u : 0u);
+                    } else if (NB == 2) {
+                        // gate rows (A slot) into columns [0, n), up rows (B
+                        // slot) into [128, 128 + n); tokens from the token area
+                        const uint64_t gdesc = sdesc_kmajor_sw128(sa);
+                        const uint64_t udesc = sdesc_kmajor_sw128(sa + S::A_BYTES);
+                        const uint64_t tdesc = sdesc_kmajor_sw128(sa + S::A_BYTES + S::B_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t acc = (st > 0 || kk > 0) ? 1u : 0u;
+                            umma_bf16_pair(d_tmem, gdesc + 2u * kk, tdesc + 2u * kk, idesc, acc);
+                            umma_bf16_pair(d_tmem + kTileM, udesc + 2u * kk, tdesc + 2u * kk,
+                                           idesc, acc);
+                        }
+                    } else {
+                        // one or two reduction steps: weights in the A (and B)
+                        // slot, their token rows in the halves of the token area
+                        const int steps = min(S::SWAP_KPS, nk - st * S::SWAP_KPS);
+                        for (int j = 0; j < steps; ++j) {
+                            const uint64_t wdesc = sdesc_kmajor_sw128(sa + j * S::A_BYTES);
+                            const uint64_t tdesc = sdesc_kmajor_sw128(
+                                sa + S::A_BYTES + S::B_BYTES + j * (S::TOK_BYTES / S::SWAP_KPS));
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                umma_bf16_pair(d_tmem, wdesc + 2u * kk, tdesc + 2u * kk, idesc,
+                                               (st > 0 || j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
                     umma_commit_pair(&empty[s], 0x3);
                     if (++s == STAGES) {
                         s = 0;
@@ -864,8 +1064,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q * 32 + lane;        // accumulator row of this thread
         const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), 0);
         uint32_t b = 0, tph = 0;
-        for (int g = cluster_id; g < ntiles; g += NC) {
-            const TileInfo ti = pair_tile_info(p, s_seg, s_mt, g);
+        PairSched sched(cluster_id, NC, active ? n_full : 0, active ? n_swap : 0);
+        bool sw;
+        int g;
+        while (sched.next(sw, g)) {
             if (!mbar_wait(&tfull[b], tph, abort_flag, kWaitLimitNs)) {
                 *abort_flag = 1;
                 set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
@@ -873,10 +1075,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + b * S::UMMA_N + ((uint32_t)(q * 32) << 16);
-            const int my_rows = ti.rows - (int)rank * kTileM;
-            const bool row_ok = r < my_rows;
-            const long long orow = (long long)ti.a_row0 + (int)rank * kTileM + r;
-            epilogue_row<BN, EPI>(p, p.out, p.ld_out, p.N_valid, taddr, row_ok, orow, ti.n_idx);
+            if (!sw) {
+                const TileInfo ti = pair_tile_info(p, s_seg, s_mt, g);
+                const int my_rows = ti.rows - (int)rank * kTileM;
+                const bool row_ok = r < my_rows;
+                const long long orow = (long long)ti.a_row0 + (int)rank * kTileM + r;
+                epilogue_row<BN, EPI>(p, p.out, p.ld_out, p.N_valid, taddr, row_ok, orow,
+                                      ti.n_idx);
+            } else {
+                const SwapInfo si = swap_info(s_seg, s_sw, p.nseg, n_fb, S::SWAP_ROWS, g);
+                swap_epilogue<EPI>(p, taddr, q, lane, (int)rank, si);
+            }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -989,12 +1198,19 @@ cudaError_t launch_tc(const CUtensorMap &mA, const CUtensorMap &mB0, const CUten
                       second ? second->b1 : mB1, p);
 }
 
+// The swap units' operands (TcParams::swap_tails): weight maps (GEMM1: W_gate
+// and W_up in 16-row boxes; GEMM2: W_down in 128-row boxes) and the token
+// rows (x_perm or h) in 16-row boxes.
+struct SwapMaps {
+    CUtensorMap w0, w1, t;
+};
+
 // Launches the CTA-pair kernel as clusters of 2 (persistent: at most as
-// many pairs as can be resident at once, and no more than there are pair
-// tiles).
+// many pairs as can be resident at once, and no more than there are units).
 template <int BN, int NB, int EPI, int STAGES>
 cudaError_t launch_tc_pair(const CUtensorMap &mA, const CUtensorMap &mB0, const CUtensorMap &mB1,
-                           const TcParams &p, long long max_tiles, cudaStream_t stream)
+                           const TcParams &p, long long max_tiles, cudaStream_t stream,
+                           const SwapMaps *swap = nullptr)
 {
     using S = PairShape<BN, NB, STAGES>;
     auto kern = tc_gemm_pair_kernel<BN, NB, EPI, STAGES>;
@@ -1043,7 +1259,10 @@ cudaError_t launch_tc_pair(const CUtensorMap &mA, const CUtensorMap &mB0, const 
         return cudaSuccess;
     cfg.gridDim = dim3((unsigned)(2 * pairs));
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, mA, mB0, mB1, p);
+    if (p.swap_tails && !swap)
+        return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, kern, mA, mB0, mB1, swap ? swap->w0 : mA, swap ? swap->w1 : mA,
+                              swap ? swap->t : mA, p);
 }
 
 }  // namespace
@@ -1141,23 +1360,18 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.sh_out = hs;
             p.sh_ld_out = S;
         }
-        if (pair_routed && plan.pair_tails) {
-            // full 256-row tiles on CTA pairs, then each segment's remaining
-            // rows (< 256) in 128-row single-CTA tiles: a 256-row tile over a
-            // short remainder would compute mostly padding
-            p.pair_full_only = 1;
-            err = launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, mt2_bound * p.n_tiles,
-                                                        stream);
-            if (err == cudaSuccess) {
-                TcParams q = p;
-                q.pair_full_only = 0;
-                q.tail_after = kPairRows;
-                q.aux.out = nullptr;  // evaluated by the pair launch
-                err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, q, 2LL * E * q.n_tiles, stream);
-            }
-        } else if (pair_routed) {
-            err = launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, mt2_bound * p.n_tiles,
-                                                        stream);
+        if (pair_routed) {
+            // 256-row tiles on CTA pairs and, in the same launch, the
+            // experts with fewer than 256 rows as swap units: a 256-row tile
+            // over a few rows would compute mostly padding
+            SwapMaps sw;
+            if (!make_map(&sw.w0, W_gate, (uint64_t)E * F, (uint64_t)D, kTileM) ||
+                !make_map(&sw.w1, W_up, (uint64_t)E * F, (uint64_t)D, kTileM) ||
+                !make_map(&sw.t, xp, (uint64_t)R, (uint64_t)D, kSwapBoxRows))
+                return cudaErrorInvalidValue;
+            p.swap_tails = 1;
+            const long long units = mt2_bound * p.n_tiles + 8LL * E * ((F + kSwapFeat - 1) / kSwapFeat);
+            err = launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, units, stream, &sw);
         } else {
             err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_bound * p.n_tiles, stream,
                                                    fused ? &sm : nullptr);
@@ -1202,43 +1416,35 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.part_stride = (long long)T * D;
         }
         const SecondMaps *second = fused ? &sm : nullptr;
-        const long long tiles = (pair_routed ? mt2_bound : mt_bound) * p.n_tiles;
-        // pair tails: full 256-row tiles on pairs, the remainders on single CTAs
-        const bool tails = pair_routed && plan.pair_tails;
-        p.pair_full_only = tails ? 1 : 0;
-        TcParams q = p;
-        q.pair_full_only = 0;
-        q.tail_after = kPairRows;
-        const long long tail_tiles = 2LL * E * p.n_tiles;
-        CUtensorMap mBt;  // the single-CTA kernel's B boxes hold bn_down rows
-        if (tails && !make_map(&mBt, W_down, (uint64_t)E * D, (uint64_t)F, (uint32_t)bn_down))
-            return cudaErrorInvalidValue;
+        long long tiles = (pair_routed ? mt2_bound : mt_bound) * p.n_tiles;
+        // pairs: 256-row tiles and the experts with fewer than 256 rows as
+        // swap units (W_down rows in 128-row boxes, h rows in 16-row boxes)
+        SwapMaps sw;
+        if (pair_routed) {
+            if (!make_map(&sw.w0, W_down, (uint64_t)E * D, (uint64_t)F, kTileM) ||
+                !make_map(&sw.t, h, (uint64_t)R, (uint64_t)F, kSwapBoxRows))
+                return cudaErrorInvalidValue;
+            sw.w1 = sw.w0;
+            p.swap_tails = 1;
+            tiles += 8LL * E * ((D + kSwapFeat - 1) / kSwapFeat);
+        }
         if (plan.direct_y) {
             p.out = y;
             p.row_tok = reinterpret_cast<const int32_t *>(ws + L.row_tok);
             p.row_w = reinterpret_cast<const float *>(ws + L.row_w);
-            q.out = p.out;
-            q.row_tok = p.row_tok;
-            q.row_w = p.row_w;
-            if (pair_routed) {
-                err = wide_down ? launch_tc_pair<256, 1, EPI_BF16_Y, 6>(mA, mB, mB, p, tiles, stream)
-                                : launch_tc_pair<128, 1, EPI_BF16_Y, 8>(mA, mB, mB, p, tiles, stream);
-                if (err == cudaSuccess && tails)
-                    err = wide_down
-                              ? launch_tc<256, 1, EPI_BF16_Y, 4>(mA, mBt, mBt, q, tail_tiles, stream)
-                              : launch_tc<128, 1, EPI_BF16_Y, 6>(mA, mBt, mBt, q, tail_tiles, stream);
-            } else
+            if (pair_routed)
+                err = wide_down
+                          ? launch_tc_pair<256, 1, EPI_BF16_Y, 6>(mA, mB, mB, p, tiles, stream, &sw)
+                          : launch_tc_pair<128, 1, EPI_BF16_Y, 7>(mA, mB, mB, p, tiles, stream, &sw);
+            else
                 err = wide_down ? launch_tc<256, 1, EPI_BF16_Y, 4>(mA, mB, mB, p, tiles, stream)
                                 : launch_tc<128, 1, EPI_BF16_Y, 6>(mA, mB, mB, p, tiles, stream);
         } else {
-            if (pair_routed) {
-                err = wide_down ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream)
-                                : launch_tc_pair<128, 1, EPI_BF16, 8>(mA, mB, mB, p, tiles, stream);
-                if (err == cudaSuccess && tails)
-                    err = wide_down
-                              ? launch_tc<256, 1, EPI_BF16, 4>(mA, mBt, mBt, q, tail_tiles, stream)
-                              : launch_tc<128, 1, EPI_BF16, 6>(mA, mBt, mBt, q, tail_tiles, stream);
-            } else
+            if (pair_routed)
+                err = wide_down
+                          ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream, &sw)
+                          : launch_tc_pair<128, 1, EPI_BF16, 7>(mA, mB, mB, p, tiles, stream, &sw);
+            else
                 err = wide_down
                           ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, tiles, stream, second)
                           : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream, second);
@@ -1292,7 +1498,7 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             if (pair_shared)
                 err = wide_down
                           ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, mt2_s * p.n_tiles, stream)
-                          : launch_tc_pair<128, 1, EPI_BF16, 8>(mA, mB, mB, p, mt2_s * p.n_tiles, stream);
+                          : launch_tc_pair<128, 1, EPI_BF16, 7>(mA, mB, mB, p, mt2_s * p.n_tiles, stream);
             else
                 err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt_s * p.n_tiles, stream)
                                 : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt_s * p.n_tiles, stream);
@@ -1337,7 +1543,7 @@ cudaError_t launch_dense_tc(int rows, int N, int K, const void *A, const void *B
     const long long mt = (rows + kTileM - 1) / kTileM, mt2 = (rows + kPairRows - 1) / kPairRows;
     if (pair)
         return bn == 256 ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, mt2 * p.n_tiles, stream)
-                         : launch_tc_pair<128, 1, EPI_BF16, 8>(mA, mB, mB, p, mt2 * p.n_tiles, stream);
+                         : launch_tc_pair<128, 1, EPI_BF16, 7>(mA, mB, mB, p, mt2 * p.n_tiles, stream);
     if (narrow)
         return launch_tc<32, 1, EPI_BF16, 8>(mA, mB, mB, p, mt * p.n_tiles, stream);
     return bn == 256 ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt * p.n_tiles, stream)

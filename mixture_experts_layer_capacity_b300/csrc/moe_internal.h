@@ -65,8 +65,8 @@ struct LaunchPlan {
     bool pair_routed;   // routed GEMMs on CTA pairs (256-row tiles)
     bool pair_shared;   // shared-expert GEMMs on CTA pairs
     bool shared_fused;  // shared-expert tiles inside the routed single-CTA launches
-    bool pair_tails;    // pairs run only full 256-row tiles; each segment's remaining
-                        // rows go to a single-CTA launch with 128-row tiles
+    bool pair_tails;    // pairs run each segment's full 256-row tiles, and its
+                        // remaining rows as swap units in the same launch
     int router_splits;  // K-splits of the tensor-core router (1 = none)
 };
 // CTA pairs for large problems whose segments average at least 512 rows;

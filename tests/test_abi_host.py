@@ -189,7 +189,9 @@ def test_launch_plan():
     assert q["pair_shared"] and not q["shared_fused"]
     assert plan("mixtral_prefill")["pair_routed"]
     # 256 experts: pair tiles plus 128-row remainder tiles; 64 experts: pairs only
-    assert plan("dsv3_prefill")["pair_tails"] and not q["pair_tails"]
+    # every launch on CTA pairs runs the segments' remainders as swap units
+    assert plan("dsv3_prefill")["pair_tails"] and q["pair_tails"]
+    assert not plan("mixtral_decode")["pair_tails"]
     assert not plan("mixtral_decode")["pair_routed"]
     with pytest.raises(B.MoeError):
         B.launch_plan(B.make_config(64, 128, 8, 128, 0))
@@ -212,3 +214,17 @@ def test_latent_offsets_lie_inside_the_workspace():
     assert xo % 1024 == 0 and yo >= xo + n and yo + n <= B.latent_workspace_size(cfg, 4096)
     with pytest.raises(B.MoeError):
         B.latent_offsets(cfg, 100)       # d_outer not a multiple of 64 for bf16
+
+
+def test_debug_bounds_build_exports_the_same_symbols():
+    """libmoe_debug_bounds.so (the sources built with MOE_DEBUG_BOUNDS) is a
+    drop-in replacement: it exports exactly the entry points of libmoe.so."""
+    from mixture_experts_layer_capacity_b300 import build
+    dbg = build.build(debug_bounds=True)
+
+    def exported(path):
+        out = os.popen(f"nm -D --defined-only {path}").read().split("\n")
+        return sorted(l.split()[-1] for l in out if " T " in l)
+
+    assert exported(dbg) == exported(B.LIB_PATH)
+    assert set(_declared_symbols()) <= set(exported(dbg))

@@ -124,3 +124,59 @@ def test_exchanged_counts_are_checked():
     for cfg, o in zip(cfgs, outs):
         assert B.read_device_status(cfg, o["workspace"]) == B.MOE_DEVICE_SHARD_MISMATCH
 
+
+
+def _corrupt_last_token(outs, rank, E, how):
+    """Gives the last token of `rank` an expert index the finish launch must
+    refuse: one outside [0, E) ("range"), or a valid expert that does not
+    occur among the rank's last 32 tokens ("segment": that token's row would
+    then fall past the expert's segment, since every routing-kernel block
+    holds at most 32 tokens at these sizes)."""
+    idx = outs[rank]["topk_idx"]
+    last = idx[-1].clone()
+    if how == "range":
+        idx[-1, 0] = E + 3
+        return
+    recent = set(idx[-32:].flatten().tolist())
+    spare = [e for e in range(E) if e not in recent]
+    assert spare, "every expert occurs among the last 32 tokens"
+    idx[-1, 0] = spare[0]
+    assert not torch.equal(idx[-1], last)
+
+
+@pytest.mark.parametrize("how", ["range", "segment"])
+def test_finish_refuses_bad_expert_indices(how):
+    """moe_sharded_finish reads topk_idx as the caller hands it back.  An
+    index outside [0, E), or one whose row would fall outside its expert's
+    segment, is refused by the kernel's own check (status word, no access),
+    and the next normal split call on the same workspaces is correct."""
+    w = Workload("bad_idx", T=800, D=128, E=64, F=128, k=2, S=0, mode=2, gamma=0.0,
+                 dtype="bf16", alpha=0.01, bias="zipf1.1")
+    inp = make_inputs(w, 23, "cuda")
+    counts = [400, 400]
+    T = w.T
+    starts = [0, 400]
+    cfgs, outs, views = [], [], []
+    for s, n in zip(starts, counts):
+        cfg = B.make_config(n, w.D, w.E, w.F, w.k, w.S, w.dtype, w.mode, w.gamma, w.alpha)
+        v = dict(inp)
+        v["x"] = inp["x"][s:s + n]
+        o = sharded.alloc_outputs(cfg, T, "cuda")
+        sharded.route(cfg, T, v, o)
+        cfgs.append(cfg)
+        outs.append(o)
+        views.append(v)
+    all_c = torch.stack([o["expert_counts"] for o in outs]).contiguous()
+    all_p = torch.stack([o["prob_sums"] for o in outs]).contiguous()
+    torch.cuda.synchronize()
+    _corrupt_last_token(outs, 1, w.E, how)
+    for r in range(2):
+        sharded.finish(cfgs[r], T, 2, r, all_c, all_p, views[r], outs[r])
+    assert B.read_device_status(cfgs[0], outs[0]["workspace"]) == B.MOE_DEVICE_OK
+    assert B.read_device_status(cfgs[1], outs[1]["workspace"]) == \
+        B.MOE_DEVICE_INDEX_OUT_OF_RANGE
+    # the same workspaces, a clean split call: the whole-batch oracle again
+    cfgs2, outs2, _ = _run_ranks(w, inp, counts)
+    for cfg, o in zip(cfgs2, outs2):
+        assert B.read_device_status(cfg, o["workspace"]) == B.MOE_DEVICE_OK
+    parity.check(w, inp, _concat(outs2))
