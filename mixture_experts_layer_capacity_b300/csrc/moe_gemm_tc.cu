@@ -623,15 +623,36 @@ __device__ __forceinline__ int pair_tile_count(const TcParams &p, const int *s_m
     return s_mt[p.nseg] * p.n_tiles;
 }
 
+// Row tiles per raster group of a pair launch.  Pairs running at the same
+// time take consecutive tiles; within a group of kRowGroup row tiles the
+// column tile changes slowest, so the ~74 concurrent tiles touch about
+// kRowGroup A row tiles and 74 / kRowGroup B column tiles.  At the
+// DeepSeek-V3 shape (D = 7168: 3.7 MB per A or B tile) that is ~63 MB, which
+// L2 holds; walking all of a large expert's row tiles per column tile
+// instead (its x rows: up to ~230 MB) re-read them from DRAM for every
+// column tile (GEMM1 read 2.9x its weight bytes).
+constexpr int kRowGroup = 8;
+
+// Tile `local` of an mt x nt grid of row and column tiles in grouped raster
+// order: groups of kRowGroup row tiles; within a group, column-major.
+__device__ __forceinline__ void grouped_raster(int local, int mt, int nt, int &m, int &n)
+{
+    const int grp = local / (kRowGroup * nt);
+    const int rows = min(kRowGroup, mt - grp * kRowGroup);
+    const int within = local - grp * kRowGroup * nt;
+    n = within / rows;
+    m = grp * kRowGroup + (within - n * rows);
+}
+
 // a_row0 / rows: the pair tile's first A row and its valid rows (<= 256).
 __device__ __forceinline__ TileInfo pair_tile_info(const TcParams &p, const int *s_seg,
                                                    const int *s_mt, int g)
 {
     TileInfo ti;
+    int m;
     if (!s_mt) {
         const int mt = (p.dense_rows + kPairRows - 1) / kPairRows;
-        ti.n_idx = g / mt;
-        const int m = g - ti.n_idx * mt;
+        grouped_raster(g, mt, p.n_tiles, m, ti.n_idx);
         ti.seg = 0;
         ti.a_row0 = m * kPairRows;
         ti.rows = min(kPairRows, p.dense_rows - ti.a_row0);
@@ -646,9 +667,7 @@ __device__ __forceinline__ TileInfo pair_tile_info(const TcParams &p, const int 
             hi = mid;
     }
     const int mt0 = s_mt[lo], mt_e = s_mt[lo + 1] - mt0;
-    const int local = g - mt0 * p.n_tiles;
-    ti.n_idx = local / mt_e;
-    const int m = local - ti.n_idx * mt_e;
+    grouped_raster(g - mt0 * p.n_tiles, mt_e, p.n_tiles, m, ti.n_idx);
     ti.seg = lo;
     ti.a_row0 = s_seg[lo] + m * kPairRows;
     ti.rows = min(kPairRows, s_seg[lo + 1] - ti.a_row0);

@@ -105,6 +105,8 @@ def test_profile_traffic_only_from_current_sources():
             # another summary holds a current figure for the same stage
             assert any(s == _source_sha(stage, workload) and st == stage and wl == workload
                        for _, st, wl, _, s in lines), (name, stage, workload)
+    # the default workload's dominant kernel has a current figure
+    assert bench.profile_traffic("gemm1_routed", bench.DEFAULT_WORKLOAD) is not None
     assert current > 0
 
 
