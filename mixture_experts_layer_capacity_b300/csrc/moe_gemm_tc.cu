@@ -590,8 +590,12 @@ struct PairShape {
     static constexpr int A_BYTES = kTileM * 64 * 2;
     static constexpr int B_BYTES = B_HALF_ROWS * 64 * 2;
     // a stage: the A slot and the B slot (full tiles), then the token rows of
-    // a swap unit, which fills both slots with weight rows
-    static constexpr int TOK_BYTES = 4096;
+    // a swap unit, which fills both slots with weight rows.  8 KB: GEMM1 swap
+    // units take up to 128 token rows, GEMM2's up to 64 (two reduction steps
+    // per stage); a smaller area cut the small experts into more chunks,
+    // each streaming the same weight rows (4 KB: 218 + 288 chunks at the
+    // DeepSeek-V3 shape, 8 KB: 189 + 218, both GEMMs ~4 % faster)
+    static constexpr int TOK_BYTES = 8192;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + TOK_BYTES;
     static constexpr int TMEM_COLS = 2 * UMMA_N <= 256 ? 256 : 512;
     // segment offsets, full-tile prefix, swap-chunk prefix
@@ -1390,7 +1394,7 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
                 return cudaErrorInvalidValue;
             p.swap_tails = 1;
             const long long units = mt2_bound * p.n_tiles + 8LL * E * ((F + kSwapFeat - 1) / kSwapFeat);
-            err = launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, units, stream, &sw);
+            err = launch_tc_pair<128, 2, EPI_SWIGLU, 5>(mA, mG, mU, p, units, stream, &sw);
         } else {
             err = launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_bound * p.n_tiles, stream,
                                                    fused ? &sm : nullptr);
@@ -1453,16 +1457,16 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.row_w = reinterpret_cast<const float *>(ws + L.row_w);
             if (pair_routed)
                 err = wide_down
-                          ? launch_tc_pair<256, 1, EPI_BF16_Y, 6>(mA, mB, mB, p, tiles, stream, &sw)
-                          : launch_tc_pair<128, 1, EPI_BF16_Y, 7>(mA, mB, mB, p, tiles, stream, &sw);
+                          ? launch_tc_pair<256, 1, EPI_BF16_Y, 5>(mA, mB, mB, p, tiles, stream, &sw)
+                          : launch_tc_pair<128, 1, EPI_BF16_Y, 6>(mA, mB, mB, p, tiles, stream, &sw);
             else
                 err = wide_down ? launch_tc<256, 1, EPI_BF16_Y, 4>(mA, mB, mB, p, tiles, stream)
                                 : launch_tc<128, 1, EPI_BF16_Y, 6>(mA, mB, mB, p, tiles, stream);
         } else {
             if (pair_routed)
                 err = wide_down
-                          ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream, &sw)
-                          : launch_tc_pair<128, 1, EPI_BF16, 7>(mA, mB, mB, p, tiles, stream, &sw);
+                          ? launch_tc_pair<256, 1, EPI_BF16, 5>(mA, mB, mB, p, tiles, stream, &sw)
+                          : launch_tc_pair<128, 1, EPI_BF16, 6>(mA, mB, mB, p, tiles, stream, &sw);
             else
                 err = wide_down
                           ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, tiles, stream, second)
@@ -1492,7 +1496,7 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.ld_out = S;
             p.status = status;
             err = pair_shared
-                      ? launch_tc_pair<128, 2, EPI_SWIGLU, 6>(mA, mG, mU, p, mt2_s * p.n_tiles, stream)
+                      ? launch_tc_pair<128, 2, EPI_SWIGLU, 5>(mA, mG, mU, p, mt2_s * p.n_tiles, stream)
                       : launch_tc<128, 2, EPI_SWIGLU, 4>(mA, mG, mU, p, mt_s * p.n_tiles, stream);
             if (err == cudaSuccess)
                 err = record_stage(ev, 5, stream);
@@ -1516,8 +1520,8 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.status = status;
             if (pair_shared)
                 err = wide_down
-                          ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, mt2_s * p.n_tiles, stream)
-                          : launch_tc_pair<128, 1, EPI_BF16, 7>(mA, mB, mB, p, mt2_s * p.n_tiles, stream);
+                          ? launch_tc_pair<256, 1, EPI_BF16, 5>(mA, mB, mB, p, mt2_s * p.n_tiles, stream)
+                          : launch_tc_pair<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt2_s * p.n_tiles, stream);
             else
                 err = wide_down ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt_s * p.n_tiles, stream)
                                 : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt_s * p.n_tiles, stream);
@@ -1561,8 +1565,8 @@ cudaError_t launch_dense_tc(int rows, int N, int K, const void *A, const void *B
     p.status = status;
     const long long mt = (rows + kTileM - 1) / kTileM, mt2 = (rows + kPairRows - 1) / kPairRows;
     if (pair)
-        return bn == 256 ? launch_tc_pair<256, 1, EPI_BF16, 6>(mA, mB, mB, p, mt2 * p.n_tiles, stream)
-                         : launch_tc_pair<128, 1, EPI_BF16, 7>(mA, mB, mB, p, mt2 * p.n_tiles, stream);
+        return bn == 256 ? launch_tc_pair<256, 1, EPI_BF16, 5>(mA, mB, mB, p, mt2 * p.n_tiles, stream)
+                         : launch_tc_pair<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt2 * p.n_tiles, stream);
     if (narrow)
         return launch_tc<32, 1, EPI_BF16, 8>(mA, mB, mB, p, mt * p.n_tiles, stream);
     return bn == 256 ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt * p.n_tiles, stream)
