@@ -90,6 +90,13 @@ WORKLOADS = {
         "dsv3_prefill", T=16384, D=7168, E=256, F=2048, k=8, S=2048,
         mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1",
         description="DeepSeek-V3-shaped, renormalised top-8, Zipf-skewed bias, T=16384"),
+    # the DeepSeek-V3 widths with 32 experts and T=4096 (2.9 GB of weights):
+    # a profiling case for the CTA-pair GEMMs (256-row tiles and swap units)
+    # small enough for multi-pass counter captures
+    "dsv3_prefill_e32": Workload(
+        "dsv3_prefill_e32", T=4096, D=7168, E=32, F=2048, k=8, S=2048,
+        mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1",
+        description="DeepSeek-V3 widths, 32 experts, T=4096: profiling case"),
     "dsv3_decode": Workload(
         "dsv3_decode", T=64, D=7168, E=256, F=2048, k=8, S=2048,
         mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1",
