@@ -42,9 +42,13 @@ PAIR = [
     ("pair_top1_direct_y", 16400, 256, 8, 256, 1, 0, 2, 1.1, "none"),
     # dropless, several experts empty or tiny, k = 4
     ("pair_dropless_zipf", 4200, 128, 8, 192, 4, 128, 0, 0.0, "zipf1.1"),
-    # 128 experts: full 256-row tiles on pairs, each segment's remainder in a
-    # second, single-CTA launch (skewed segments: some below 256 rows)
+    # 128 experts, skewed: many experts under 256 rows run as swap units
+    # (narrow down projection: one 64-wide reduction step per swap stage)
     ("pair_tails_e128_zipf", 8200, 128, 128, 192, 8, 0, 2, 0.0, "zipf1.1"),
+    # wide down projection (D = 1088 > 1024: 256-column tiles, two reduction
+    # steps per swap stage) over F = 320 (five steps: the last stage holds
+    # one), partial feature blocks in both GEMMs, small experts as swap units
+    ("pair_wide_down_odd_k", 4100, 1088, 16, 320, 4, 0, 2, 0.0, "zipf1.1"),
 ]
 
 
