@@ -86,6 +86,8 @@ def _load():
         lib.oracle_quantize_e4m3_rows.restype = None
         lib.oracle_swiglu_rows_q8.argtypes = [i64, i64, i64] + [vp] * 8
         lib.oracle_swiglu_rows_q8.restype = i32
+        lib.oracle_swiglu_rows_w8a8.argtypes = [i64, i64, i64] + [vp] * 8
+        lib.oracle_swiglu_rows_w8a8.restype = i32
         _lib = lib
         return lib
 
@@ -292,9 +294,27 @@ def swiglu_rows_q8(x_rows, qg, sg, qu, su, qd, sd):
     return out
 
 
+def swiglu_rows_w8a8(x_rows, qg, sg, qu, su, qd, sd):
+    """swiglu_rows_q8 with E4M3 activations: each token row and each hidden
+    row (rounded to fp32) is quantized row-wise before its projection.
+    x_rows [n, D] holds fp32-representable values -> f64 [n, D]."""
+    x_rows = _f64(x_rows)
+    qg, qu, qd = (np.ascontiguousarray(a, dtype=np.uint8) for a in (qg, qu, qd))
+    sg, su, sd = _f32(sg), _f32(su), _f32(sd)
+    n, D = x_rows.shape
+    F = qg.shape[0]
+    out = np.empty((n, D), dtype=np.float64)
+    _check(_load().oracle_swiglu_rows_w8a8(n, D, F, _ptr(x_rows), _ptr(qg), _ptr(sg),
+                                           _ptr(qu), _ptr(su), _ptr(qd), _ptr(sd), _ptr(out)))
+    return out
+
+
 def _expert_rows(x_rows, weights):
-    """One expert on rows: weights = (Wg, Wu, Wd) fp32, or the six arrays
-    (qg, sg, qu, su, qd, sd) of E4M3 weights."""
+    """One expert on rows: weights = (Wg, Wu, Wd) fp32, the six arrays
+    (qg, sg, qu, su, qd, sd) of E4M3 weights, or those six and the string
+    "a8" (E4M3 activations too)."""
+    if len(weights) == 7 and weights[6] == "a8":
+        return swiglu_rows_w8a8(x_rows, *weights[:6])
     if len(weights) == 6:
         return swiglu_rows_q8(x_rows, *weights)
     return swiglu_rows(x_rows, *weights)

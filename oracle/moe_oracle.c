@@ -36,7 +36,11 @@
  *   - E4M3 decode and encode against PyTorch's float8_e4m3fn (every code,
  *     every tie and its neighbours, random values), the row quantizer against
  *     its defining properties, and the E4M3 expert against the fp32 expert on
- *     weights that dequantize exactly.
+ *     weights that dequantize exactly;
+ *   - the E4M3-activation expert against a recomputation with PyTorch's
+ *     float8_e4m3fn casts and numpy matrix products, and, with an identity
+ *     down projection, against the E4M3-weight expert and the row quantizer
+ *     composed by hand.
  * Every exported function below is pinned by at least one of these.
  *
  * Weight layout: W_gate and W_up hold, per expert, F rows of D values
@@ -645,6 +649,96 @@ int oracle_swiglu_rows_q8(int64_t n, int64_t D, int64_t F, const double *x, cons
         for (int64_t r = 0; r < n; ++r)
             if (h)
                 swiglu_token_q8(D, F, x + r * D, qg, sg, qu, su, qd, sd, h, out + r * D);
+        free(h);
+    }
+    return err ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * E4M3 activations as well as E4M3 weights.
+ *
+ * [MPF] "What experts cost at serving time", in its arithmetic of published
+ * configurations: DeepSeek-V3 sends the dispatched token rows in FP8.  The
+ * pages fix no format or scaling for activations either.  Reading used here
+ * (and by the CUDA path): every token row entering an expert, and the
+ * expert's hidden row h between its two projections, is quantized with the
+ * row rule above (one fp32 scale per row, scale = max|row| / 448); h is first
+ * rounded to fp32 (the precision it is quantized in).  With dequantized
+ * values x~ = decode(qx) * s_x and h~ = decode(qh) * s_h:
+ *   h_f   = silu(sum_d Wg~[f][d] x~_d) * (sum_d Wu~[f][d] x~_d)   (fp64),
+ *   out_d = sum_f Wd~[d][f] h~_f                                   (fp64),
+ *   h~    = dequant(quantize(fp32(h))).
+ * ------------------------------------------------------------------------ */
+
+/* A row of n fp32 values replaced by its dequantized E4M3 values. */
+static void dequantized_row(int64_t n, const float *v, double *out)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i)
+        amax = fabsf(v[i]) > amax ? fabsf(v[i]) : amax;
+    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_value(e4m3_code(v[i] / s)) * (double)s;
+}
+
+/* The value of every E4M3 code (e4m3_value), looked up in the expert loops
+ * below. */
+static double e4m3_table[256];
+
+static void swiglu_token_w8a8(int64_t D, int64_t F, const double *x, const uint8_t *qg,
+                              const float *sg, const uint8_t *qu, const float *su,
+                              const uint8_t *qd, const float *sd, float *v32, double *xq,
+                              double *h, double *out)
+{
+    for (int64_t d = 0; d < D; ++d)
+        v32[d] = (float)x[d];          /* exact for bf16 and fp32 inputs */
+    dequantized_row(D, v32, xq);
+    for (int64_t f = 0; f < F; ++f) {
+        double g = 0.0, u = 0.0;
+        for (int64_t d = 0; d < D; ++d) {
+            g += e4m3_table[qg[f * D + d]] * (double)sg[f] * xq[d];
+            u += e4m3_table[qu[f * D + d]] * (double)su[f] * xq[d];
+        }
+        v32[f] = (float)(silu(g) * u);
+    }
+    dequantized_row(F, v32, h);
+    for (int64_t d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int64_t f = 0; f < F; ++f)
+            acc += e4m3_table[qd[d * F + f]] * (double)sd[d] * h[f];
+        out[d] = acc;
+    }
+}
+
+/* oracle_swiglu_rows_q8 with the token rows and the hidden rows quantized
+ * too: x [n][D] (values of fp32 or bf16 inputs), codes and scales as there. */
+int oracle_swiglu_rows_w8a8(int64_t n, int64_t D, int64_t F, const double *x,
+                            const uint8_t *qg, const float *sg, const uint8_t *qu,
+                            const float *su, const uint8_t *qd, const float *sd, double *out)
+{
+    if (n < 0 || D < 1 || F < 1)
+        return ORACLE_BAD_ARG;
+    const int64_t W = D > F ? D : F;
+    for (int c = 0; c < 256; ++c)
+        e4m3_table[c] = e4m3_value((uint8_t)c);
+    int err = 0;
+#pragma omp parallel
+    {
+        float *v32 = (float *)malloc(sizeof(float) * (size_t)W);
+        double *xq = (double *)malloc(sizeof(double) * (size_t)D);
+        double *h = (double *)malloc(sizeof(double) * (size_t)F);
+        const int ok = v32 && xq && h;
+        if (!ok) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < n; ++r)
+            if (ok)
+                swiglu_token_w8a8(D, F, x + r * D, qg, sg, qu, su, qd, sd, v32, xq, h,
+                                  out + r * D);
+        free(v32);
+        free(xq);
         free(h);
     }
     return err ? ORACLE_NO_MEMORY : ORACLE_OK;

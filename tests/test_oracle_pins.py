@@ -576,3 +576,75 @@ def test_swiglu_q8_equals_dense_with_dequantized_weights():
     got = oracle.swiglu_rows_q8(x, qg, sg, qu, su, qd, sd)
     want = oracle.swiglu_rows(x, deq(qg, sg), deq(qu, su), deq(qd, sd))
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+
+
+# ------------------------------------------------------- e4m3 activations too
+def _torch_dequant_rows(v32):
+    """Row-wise E4M3 round trip of fp32 rows with PyTorch's float8_e4m3fn:
+    scale = max|row| / 448 in fp32 (1 for a zero row), values v / scale in
+    fp32 (clamped to the format's range; the division can land a hair above
+    448), cast, widened, times the scale -> fp64."""
+    import torch
+    v32 = np.asarray(v32, dtype=np.float32)
+    amax = np.abs(v32).max(axis=1)
+    s = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    q = torch.from_numpy((v32 / s[:, None]).astype(np.float32)).clamp(-448.0, 448.0)
+    return q.to(torch.float8_e4m3fn).to(torch.float64).numpy() * s[:, None].astype(np.float64)
+
+
+def _random_codes(rng, shape):
+    q = rng.integers(0, 256, shape, dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x40              # no NaN codes
+    return q
+
+
+def test_swiglu_w8a8_matches_torch_float8_recomputation():
+    rng = np.random.default_rng(11)
+    D, F, n = 64, 48, 7
+    qg, qu, qd = _random_codes(rng, (F, D)), _random_codes(rng, (F, D)), _random_codes(rng, (D, F))
+    sg = (rng.uniform(0.5, 2.0, F) * 2.0 ** -9).astype(np.float32)
+    su = (rng.uniform(0.5, 2.0, F) * 2.0 ** -9).astype(np.float32)
+    sd = (rng.uniform(0.5, 2.0, D) * 2.0 ** -8).astype(np.float32)
+    x = (rng.standard_normal((n, D)) * np.exp(rng.uniform(-3, 3, (n, 1)))).astype(np.float32)
+    x[2] = 0.0                                 # a zero row: scale 1, all codes 0
+    x[4, :3] = [1e-30, -200.0, 7.5]            # wide dynamic range, subnormal codes
+    got = oracle.swiglu_rows_w8a8(x, qg, sg, qu, su, qd, sd)
+    import torch
+    deq = lambda q, s: (torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64)
+                        .numpy() * s[:, None].astype(np.float64))
+    Wg, Wu, Wd = deq(qg, sg), deq(qu, su), deq(qd, sd)
+    xt = _torch_dequant_rows(x)
+    g, u = xt @ Wg.T, xt @ Wu.T
+    h32 = (g / (1.0 + np.exp(-g)) * u).astype(np.float32)
+    want = _torch_dequant_rows(h32) @ Wd.T
+    assert np.all(got[2] == 0.0)
+    np.testing.assert_allclose(got, want, rtol=1e-9, atol=1e-9 * np.abs(want).max())
+    # and the activation rounding matters: the E4M3-weight expert differs
+    plain = oracle.swiglu_rows_q8(x, qg, sg, qu, su, qd, sd)
+    assert np.abs(plain - got).max() > 1e-4 * np.abs(want).max()
+
+
+def test_swiglu_w8a8_is_q8_expert_between_row_quantizers():
+    # with W_down = I (code 0x38 = 1.0 on the diagonal, scale 1) the expert's
+    # output is its dequantized hidden row, so it must equal: quantize the
+    # token rows, run the (pinned) E4M3-weight expert with an identity down
+    # projection, round to fp32, quantize the rows again
+    rng = np.random.default_rng(12)
+    D = F = 40
+    n = 9
+    qg, qu = _random_codes(rng, (F, D)), _random_codes(rng, (F, D))
+    sg = (2.0 ** rng.integers(-10, -6, F)).astype(np.float32)
+    su = (rng.uniform(0.5, 2.0, F) * 2.0 ** -8).astype(np.float32)
+    qd = np.zeros((D, F), dtype=np.uint8)
+    np.fill_diagonal(qd, 0x38)
+    sd = np.ones(D, dtype=np.float32)
+    assert oracle.e4m3_decode(np.uint8([0x38]))[0] == 1.0
+    x = (rng.standard_normal((n, D)) * 3.0).astype(np.float32)
+    got = oracle.swiglu_rows_w8a8(x, qg, sg, qu, su, qd, sd)
+
+    def round_trip(v):
+        q, s = oracle.quantize_e4m3_rows(np.asarray(v, dtype=np.float32))
+        return oracle.e4m3_decode(q) * s[:, None].astype(np.float64)
+
+    h = oracle.swiglu_rows_q8(round_trip(x), qg, sg, qu, su, qd, sd)
+    np.testing.assert_array_equal(got, round_trip(h.astype(np.float32)))
