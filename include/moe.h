@@ -235,9 +235,10 @@ MOE_API moe_status moe_latent_offsets(const moe_config *cfg, int32_t d_outer,
  * memory is sized at 8 bits per weight).  These entry points store every
  * routed and shared expert weight matrix as e4m3 codes with one fp32 scale
  * per weight row (output feature): W[r][c] = decode(q[r][c]) * scale[r].
- * Activations, the router and all accumulation stay as in moe_forward (bf16
- * inputs, fp32 accumulation); the e4m3 values enter the tensor cores exactly
- * (every e4m3 value is a bf16 value). */
+ * In moe_forward_w8 the activations, the router and all accumulation stay as
+ * in moe_forward (bf16 inputs, fp32 accumulation); the e4m3 values enter the
+ * tensor cores exactly (every e4m3 value is a bf16 value).  moe_forward_w8a8
+ * quantizes the expert GEMMs' activation rows to e4m3 as well. */
 
 /* Row-wise quantization of a bf16 matrix W [rows, cols] (device, row-major):
  *   scale[r] = max_c |W[r][c]| / 448 in fp32 (1 when the row is all zero),
@@ -275,6 +276,48 @@ MOE_API moe_status moe_forward_w8(const moe_config *cfg,
                        int32_t *expert_counts, int32_t *kept_counts,
                        float *aux_loss, void *workspace, size_t workspace_bytes,
                        cudaStream_t stream);
+
+/* The forward pass of moe_forward_w8 with E4M3 activations too ("Mixture of
+ * Experts: More Parameters, Same FLOPs", 'What experts cost at serving
+ * time' and its arithmetic of published configurations: DeepSeek-V3 sends
+ * the dispatched token rows in FP8).  The permuted token rows, the
+ * shared expert's token rows and the hidden rows h between the two expert
+ * GEMMs are quantized row by row with moe_quantize_e4m3_rows's rule (fp32
+ * scale = max|row| / 448, codes round to nearest even of v / scale,
+ * saturating; h is quantized from its fp32 value), and each expert GEMM
+ * multiplies E4M3 codes by E4M3 codes on the tensor cores with an fp32
+ * accumulator, scaled by the token row's and the weight row's scales.
+ * Arguments, outputs and conventions are those of moe_forward_w8, except the
+ * workspace: >= moe_w8a8_workspace_size(cfg) bytes, 256-byte aligned
+ * (MOE_ERR_WORKSPACE otherwise).  A layer with a shared expert and
+ * d_expert < 128 is MOE_ERR_UNSUPPORTED.  Batches of any size run the
+ * 128-row tile GEMMs with the weights as the wide operand. */
+MOE_API moe_status moe_w8a8_workspace_size(const moe_config *cfg, size_t *bytes);
+MOE_API moe_status moe_forward_w8a8(const moe_config *cfg,
+                       const void *x, const void *W_r, const float *router_bias,
+                       const uint8_t *W_gate_q, const float *W_gate_scale,
+                       const uint8_t *W_up_q, const float *W_up_scale,
+                       const uint8_t *W_down_q, const float *W_down_scale,
+                       const uint8_t *Ws_gate_q, const float *Ws_gate_scale,
+                       const uint8_t *Ws_up_q, const float *Ws_up_scale,
+                       const uint8_t *Ws_down_q, const float *Ws_down_scale,
+                       void *y, float *router_logits, int32_t *topk_idx,
+                       float *topk_w, uint8_t *dropped_mask,
+                       int32_t *expert_counts, int32_t *kept_counts,
+                       float *aux_loss, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* Where moe_forward_w8a8 keeps its quantized activations inside its
+ * workspace (same cfg), as byte offsets: the permuted token rows' codes
+ * (uint8 [R][d_model]) and scales (fp32 [R]), the hidden rows before
+ * quantization (fp32 [R][d_expert]), their codes (uint8 [R][d_expert]) and
+ * scales (fp32 [R]).  Row r is the r-th kept (token, expert) assignment in
+ * expert order, tokens ascending within an expert; R = the sum of
+ * kept_counts.  They stay there after the call until the workspace is used
+ * again.  MOE_ERR_INVALID_ARG for a null pointer; other errors as
+ * moe_w8a8_workspace_size.  Host only; launches nothing. */
+MOE_API moe_status moe_w8a8_offsets(const moe_config *cfg, size_t *x_codes, size_t *x_scales,
+                                    size_t *h_values, size_t *h_codes, size_t *h_scales);
 
 /* ---- One batch split over several ranks (data parallel), same results as
  * one moe_forward over the whole batch.

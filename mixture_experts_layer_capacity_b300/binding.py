@@ -90,6 +90,12 @@ def lib():
         L.moe_quantize_e4m3_rows.restype = ctypes.c_int
         L.moe_forward_w8.argtypes = [cfgp] + [vp] * 24 + [ctypes.c_size_t, vp]
         L.moe_forward_w8.restype = ctypes.c_int
+        L.moe_w8a8_workspace_size.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_w8a8_workspace_size.restype = ctypes.c_int
+        L.moe_forward_w8a8.argtypes = [cfgp] + [vp] * 24 + [ctypes.c_size_t, vp]
+        L.moe_forward_w8a8.restype = ctypes.c_int
+        L.moe_w8a8_offsets.argtypes = [cfgp] + [ctypes.POINTER(ctypes.c_size_t)] * 5
+        L.moe_w8a8_offsets.restype = ctypes.c_int
         L.moe_sharded_workspace_size.argtypes = [cfgp, ctypes.c_int64,
                                                  ctypes.POINTER(ctypes.c_size_t)]
         L.moe_sharded_workspace_size.restype = ctypes.c_int
@@ -240,14 +246,16 @@ def quantize_e4m3_rows(W: torch.Tensor, stream=None):
     return q, s
 
 
-def quantize_expert_weights(inputs: dict, stream=None) -> dict:
+def quantize_expert_weights(inputs: dict, stream=None, a8: bool = False) -> dict:
     """A copy of `inputs` whose expert weights (routed and shared) are E4M3:
-    keys W_gate_q / W_gate_s, ... replace W_gate, ..."""
+    keys W_gate_q / W_gate_s, ... replace W_gate, ...  a8: the layer runs
+    with E4M3 activations too (forward calls moe_forward_w8a8)."""
     out = {k: v for k, v in inputs.items() if k not in W8_KEYS}
     for k in W8_KEYS:
         W = inputs.get(k)
         q, s = (None, None) if W is None else quantize_e4m3_rows(W, stream)
         out[k + "_q"], out[k + "_s"] = q, s
+    out["a8"] = bool(a8)
     return out
 
 
@@ -265,6 +273,55 @@ def moe_forward_w8(cfg: MoeConfig, x, W_r, router_bias, W_gate_q, W_gate_s, W_up
                               ctypes.c_size_t(int(workspace_bytes)), _stream(stream))
     if st != MOE_OK:
         raise MoeError(st, "moe_forward_w8")
+
+
+def w8a8_workspace_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t(0)
+    st = lib().moe_w8a8_workspace_size(ctypes.byref(cfg), ctypes.byref(n))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_w8a8_workspace_size")
+    return int(n.value)
+
+
+def moe_forward_w8a8(cfg: MoeConfig, x, W_r, router_bias, W_gate_q, W_gate_s, W_up_q, W_up_s,
+                     W_down_q, W_down_s, Ws_gate_q, Ws_gate_s, Ws_up_q, Ws_up_s, Ws_down_q,
+                     Ws_down_s, y, router_logits, topk_idx, topk_w, dropped_mask, expert_counts,
+                     kept_counts, aux_loss, workspace, workspace_bytes=None, stream=None) -> None:
+    """Same arguments as the C function."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    args = [x, W_r, router_bias, W_gate_q, W_gate_s, W_up_q, W_up_s, W_down_q, W_down_s,
+            Ws_gate_q, Ws_gate_s, Ws_up_q, Ws_up_s, Ws_down_q, Ws_down_s, y, router_logits,
+            topk_idx, topk_w, dropped_mask, expert_counts, kept_counts, aux_loss, workspace]
+    st = lib().moe_forward_w8a8(ctypes.byref(cfg), *[_ptr(a) for a in args],
+                                ctypes.c_size_t(int(workspace_bytes)), _stream(stream))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_forward_w8a8")
+
+
+def w8a8_activations(cfg: MoeConfig, workspace: torch.Tensor, rows: int) -> dict:
+    """Views of moe_forward_w8a8's quantized activations in `workspace`
+    (moe_w8a8_offsets) over the call's first `rows` rows (rows =
+    sum(kept_counts)): x_codes uint8 [rows, d_model], x_scales fp32 [rows],
+    h_values fp32 [rows, d_expert], h_codes uint8 [rows, d_expert], h_scales
+    fp32 [rows]."""
+    offs = [ctypes.c_size_t(0) for _ in range(5)]
+    st = lib().moe_w8a8_offsets(ctypes.byref(cfg), *[ctypes.byref(o) for o in offs])
+    if st != MOE_OK:
+        raise MoeError(st, "moe_w8a8_offsets")
+    if not 0 <= rows <= cfg.T * cfg.top_k:
+        raise ValueError("rows out of range")
+    D, F = cfg.d_model, cfg.d_expert
+    specs = [("x_codes", torch.uint8, (rows, D), 1), ("x_scales", torch.float32, (rows,), 4),
+             ("h_values", torch.float32, (rows, F), 4), ("h_codes", torch.uint8, (rows, F), 1),
+             ("h_scales", torch.float32, (rows,), 4)]
+    out = {}
+    for (name, dt, shape, size), o in zip(specs, offs):
+        n = size
+        for d in shape:
+            n *= d
+        out[name] = workspace[o.value:o.value + n].view(dt).view(shape)
+    return out
 
 
 def latent_workspace_size(cfg: MoeConfig, d_outer: int) -> int:
@@ -404,12 +461,14 @@ class StageEvents:
 
 
 # ---------------------------------------------------------------- convenience
-def alloc_outputs(cfg: MoeConfig, device="cuda", d_outer: int = 0):
+def alloc_outputs(cfg: MoeConfig, device="cuda", d_outer: int = 0, a8: bool = False):
     """Output tensors and workspace for one call, allocated with torch
-    (d_outer > 0: for moe_latent_forward, y at the outer width)."""
+    (d_outer > 0: for moe_latent_forward, y at the outer width; a8: for
+    moe_forward_w8a8)."""
     T, D, E, k = cfg.T, (d_outer or cfg.d_model), cfg.n_experts, cfg.top_k
     dt = torch.bfloat16 if cfg.dtype == MOE_DTYPE_BF16 else torch.float32
-    ws_bytes = latent_workspace_size(cfg, d_outer) if d_outer else workspace_size(cfg)
+    ws_bytes = (latent_workspace_size(cfg, d_outer) if d_outer
+                else w8a8_workspace_size(cfg) if a8 else workspace_size(cfg))
     return dict(
         y=torch.empty((T, D), dtype=dt, device=device),
         router_logits=torch.empty((T, E), dtype=torch.float32, device=device),
@@ -427,16 +486,19 @@ def forward(cfg: MoeConfig, inputs: dict, outs: dict | None = None, stream=None)
     """Runs the layer on `inputs` (keys as workloads.make_inputs returns) and
     returns the output dict (allocated if not given).  Inputs with W_in and
     W_out run the latent layer (moe_latent_forward); inputs with E4M3 expert
-    weights (quantize_expert_weights) run moe_forward_w8."""
+    weights (quantize_expert_weights) run moe_forward_w8, or moe_forward_w8a8
+    when they were quantized with a8."""
     d_outer = int(inputs["x"].shape[1]) if inputs.get("W_in") is not None else 0
+    a8 = bool(inputs.get("a8"))
     if outs is None:
-        outs = alloc_outputs(cfg, inputs["x"].device, d_outer)
+        outs = alloc_outputs(cfg, inputs["x"].device, d_outer, a8)
     if inputs.get("W_gate_q") is not None:
-        moe_forward_w8(cfg, inputs["x"], inputs["W_r"], inputs.get("b_r"),
-                       *[inputs.get(k + sfx) for k in W8_KEYS for sfx in ("_q", "_s")],
-                       outs["y"], outs["router_logits"], outs["topk_idx"], outs["topk_w"],
-                       outs["dropped_mask"], outs["expert_counts"], outs["kept_counts"],
-                       outs["aux_loss"], outs["workspace"], stream=stream)
+        fn = moe_forward_w8a8 if a8 else moe_forward_w8
+        fn(cfg, inputs["x"], inputs["W_r"], inputs.get("b_r"),
+           *[inputs.get(k + sfx) for k in W8_KEYS for sfx in ("_q", "_s")],
+           outs["y"], outs["router_logits"], outs["topk_idx"], outs["topk_w"],
+           outs["dropped_mask"], outs["expert_counts"], outs["kept_counts"],
+           outs["aux_loss"], outs["workspace"], stream=stream)
         return outs
     if d_outer:
         moe_latent_forward(cfg, d_outer, inputs["x"], inputs["W_in"], inputs["W_out"],

@@ -99,6 +99,30 @@ WorkspaceLayout layout_of(const moe_config *c, int64_t T_cap)
     return L;
 }
 
+A8Layout a8_layout_of(const moe_config &c, const WorkspaceLayout &L)
+{
+    A8Layout A{};
+    const int64_t T = c.T, D = c.d_model, F = c.d_expert, S = c.d_shared, R = L.R_max;
+    size_t off = L.total;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 1024);
+        return o;
+    };
+    A.xq = take((size_t)R * D);
+    A.xs = take(sizeof(float) * R);
+    A.hf = take(sizeof(float) * R * F);
+    A.hq = take((size_t)R * F);
+    A.hsc = take(sizeof(float) * R);
+    A.sxq = take(S > 0 ? (size_t)T * D : 0);
+    A.sxs = take(S > 0 ? sizeof(float) * T : 0);
+    A.shf = take(S > 0 ? sizeof(float) * T * S : 0);
+    A.shq = take(S > 0 ? (size_t)T * S : 0);
+    A.shs = take(S > 0 ? sizeof(float) * T : 0);
+    A.total = off;
+    return A;
+}
+
 int shared_down_splits(const moe_config &c)
 {
     if (!plan_of(c).shared_fused)
@@ -255,7 +279,9 @@ moe_status expert_step(const moe_config &c, const WorkspaceLayout &L, uint8_t *w
                        cudaStream_t stream, const ExpertW8 *w8)
 {
     cudaError_t err;
-    if (w8)
+    if (w8 && w8->a8)
+        err = launch_experts_w8a8(c, L, ws, x, *w8, y, aux, stream, ev);
+    else if (w8)
         err = launch_experts_w8(c, L, ws, x, *w8, y, aux, stream, ev);
     else if (c.dtype == MOE_DTYPE_BF16)
         err = launch_experts_tc(c, L, ws, x, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y,
@@ -623,23 +649,31 @@ moe_status moe_quantize_e4m3_rows(int64_t rows, int64_t cols, const void *W, uin
     return cuda_ok(launch_quantize_e4m3(rows, cols, W, q, scale, stream)) ? MOE_OK : MOE_ERR_CUDA;
 }
 
-moe_status moe_forward_w8(const moe_config *cfg, const void *x, const void *W_r,
-                          const float *router_bias, const uint8_t *W_gate_q,
-                          const float *W_gate_scale, const uint8_t *W_up_q,
-                          const float *W_up_scale, const uint8_t *W_down_q,
-                          const float *W_down_scale, const uint8_t *Ws_gate_q,
-                          const float *Ws_gate_scale, const uint8_t *Ws_up_q,
-                          const float *Ws_up_scale, const uint8_t *Ws_down_q,
-                          const float *Ws_down_scale, void *y, float *router_logits,
-                          int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
-                          int32_t *expert_counts, int32_t *kept_counts, float *aux_loss,
-                          void *workspace, size_t workspace_bytes, cudaStream_t stream)
+namespace {
+
+// Shared argument checks and the call of the E4M3-weight forward passes.
+moe_status forward_e4m3(const moe_config *cfg, const void *x, const void *W_r,
+                        const float *router_bias, const uint8_t *W_gate_q,
+                        const float *W_gate_scale, const uint8_t *W_up_q, const float *W_up_scale,
+                        const uint8_t *W_down_q, const float *W_down_scale,
+                        const uint8_t *Ws_gate_q, const float *Ws_gate_scale,
+                        const uint8_t *Ws_up_q, const float *Ws_up_scale,
+                        const uint8_t *Ws_down_q, const float *Ws_down_scale, void *y,
+                        float *router_logits, int32_t *topk_idx, float *topk_w,
+                        uint8_t *dropped_mask, int32_t *expert_counts, int32_t *kept_counts,
+                        float *aux_loss, void *workspace, size_t workspace_bytes,
+                        cudaStream_t stream, bool a8)
 {
     moe_status st = validate_config(cfg);
     if (st != MOE_OK)
         return st;
     const moe_config &c = *cfg;
     if (c.dtype != MOE_DTYPE_BF16)
+        return MOE_ERR_UNSUPPORTED;
+    // E4M3 operands: 128-element reduction steps, and the shared down
+    // projection is cut into as many pieces as for the bf16 layer; with
+    // d_expert = 64 a piece could get no step
+    if (a8 && c.d_shared > 0 && c.d_expert < 128)
         return MOE_ERR_UNSUPPORTED;
     if (!expert_counts || !kept_counts || !aux_loss)
         return MOE_ERR_INVALID_ARG;
@@ -657,8 +691,8 @@ moe_status moe_forward_w8(const moe_config *cfg, const void *x, const void *W_r,
             return MOE_ERR_INVALID_ARG;
     }
     const WorkspaceLayout L = layout_of(cfg);
-    if (!workspace || workspace_bytes < L.total ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    const size_t need = a8 ? a8_layout_of(c, L).total : L.total;
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MOE_ERR_WORKSPACE;
     ExpertW8 w{};
     w.gate = W_gate_q;
@@ -673,10 +707,83 @@ moe_status moe_forward_w8(const moe_config *cfg, const void *x, const void *W_r,
     w.sgate_s = Ws_gate_scale;
     w.sup_s = Ws_up_scale;
     w.sdown_s = Ws_down_scale;
+    w.a8 = a8;
     return forward_body(c, L, static_cast<uint8_t *>(workspace), x, W_r, router_bias, nullptr,
                         nullptr, nullptr, nullptr, nullptr, nullptr, y, router_logits, topk_idx,
                         topk_w, dropped_mask, expert_counts, kept_counts, aux_loss, true, stream,
                         &w);
+}
+
+}  // namespace
+
+moe_status moe_forward_w8(const moe_config *cfg, const void *x, const void *W_r,
+                          const float *router_bias, const uint8_t *W_gate_q,
+                          const float *W_gate_scale, const uint8_t *W_up_q,
+                          const float *W_up_scale, const uint8_t *W_down_q,
+                          const float *W_down_scale, const uint8_t *Ws_gate_q,
+                          const float *Ws_gate_scale, const uint8_t *Ws_up_q,
+                          const float *Ws_up_scale, const uint8_t *Ws_down_q,
+                          const float *Ws_down_scale, void *y, float *router_logits,
+                          int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
+                          int32_t *expert_counts, int32_t *kept_counts, float *aux_loss,
+                          void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    return forward_e4m3(cfg, x, W_r, router_bias, W_gate_q, W_gate_scale, W_up_q, W_up_scale,
+                        W_down_q, W_down_scale, Ws_gate_q, Ws_gate_scale, Ws_up_q, Ws_up_scale,
+                        Ws_down_q, Ws_down_scale, y, router_logits, topk_idx, topk_w,
+                        dropped_mask, expert_counts, kept_counts, aux_loss, workspace,
+                        workspace_bytes, stream, false);
+}
+
+moe_status moe_w8a8_workspace_size(const moe_config *cfg, size_t *bytes)
+{
+    if (!bytes)
+        return MOE_ERR_INVALID_ARG;
+    const moe_status st = validate_config(cfg);
+    if (st != MOE_OK)
+        return st;
+    if (cfg->dtype != MOE_DTYPE_BF16)
+        return MOE_ERR_UNSUPPORTED;
+    *bytes = a8_layout_of(*cfg, layout_of(cfg)).total;
+    return MOE_OK;
+}
+
+moe_status moe_w8a8_offsets(const moe_config *cfg, size_t *x_codes, size_t *x_scales,
+                            size_t *h_values, size_t *h_codes, size_t *h_scales)
+{
+    if (!x_codes || !x_scales || !h_values || !h_codes || !h_scales)
+        return MOE_ERR_INVALID_ARG;
+    const moe_status st = validate_config(cfg);
+    if (st != MOE_OK)
+        return st;
+    if (cfg->dtype != MOE_DTYPE_BF16)
+        return MOE_ERR_UNSUPPORTED;
+    const A8Layout A = a8_layout_of(*cfg, layout_of(cfg));
+    *x_codes = A.xq;
+    *x_scales = A.xs;
+    *h_values = A.hf;
+    *h_codes = A.hq;
+    *h_scales = A.hsc;
+    return MOE_OK;
+}
+
+moe_status moe_forward_w8a8(const moe_config *cfg, const void *x, const void *W_r,
+                            const float *router_bias, const uint8_t *W_gate_q,
+                            const float *W_gate_scale, const uint8_t *W_up_q,
+                            const float *W_up_scale, const uint8_t *W_down_q,
+                            const float *W_down_scale, const uint8_t *Ws_gate_q,
+                            const float *Ws_gate_scale, const uint8_t *Ws_up_q,
+                            const float *Ws_up_scale, const uint8_t *Ws_down_q,
+                            const float *Ws_down_scale, void *y, float *router_logits,
+                            int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
+                            int32_t *expert_counts, int32_t *kept_counts, float *aux_loss,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    return forward_e4m3(cfg, x, W_r, router_bias, W_gate_q, W_gate_scale, W_up_q, W_up_scale,
+                        W_down_q, W_down_scale, Ws_gate_q, Ws_gate_scale, Ws_up_q, Ws_up_scale,
+                        Ws_down_q, Ws_down_scale, y, router_logits, topk_idx, topk_w,
+                        dropped_mask, expert_counts, kept_counts, aux_loss, workspace,
+                        workspace_bytes, stream, true);
 }
 
 moe_status moe_read_device_status(const moe_config *cfg, const void *workspace,

@@ -40,9 +40,10 @@
 namespace moe {
 
 // Epilogues: fp32 store (router scores), bf16 store (z), SiLU(gate) * up in
-// bf16 (h), and bf16 store of w_row * acc straight into the row's token of y
-// (down projection when every token has one expert and no shared expert).
-enum { EPI_F32 = 0, EPI_BF16 = 1, EPI_SWIGLU = 2, EPI_BF16_Y = 3 };
+// bf16 (h), bf16 store of w_row * acc straight into the row's token of y
+// (down projection when every token has one expert and no shared expert),
+// and SiLU(gate) * up in fp32 (h of the E4M3-activation path, quantized next).
+enum { EPI_F32 = 0, EPI_BF16 = 1, EPI_SWIGLU = 2, EPI_BF16_Y = 3, EPI_SWIGLU_F32 = 4 };
 
 struct TcParams {
     const int32_t *seg_off;  // grouped: [nseg+1] first A row of each segment; null = dense
@@ -70,6 +71,12 @@ struct TcParams {
                              // outputs part_stride apart, EPI_BF16 kernels only); 0/1 = none
     void *sh_out;
     long long sh_ld_out;
+    // single-CTA kernel with E4M3 operands (its F8 instantiation): the fp32
+    // row scales of A (one per A row: token or hidden row) and of B (one per
+    // B row, i.e. output column; for GEMM1 the gate and the up rows), for the
+    // main and the second problem; the accumulator is scaled by both
+    const float *a_scale, *b_scale0, *b_scale1;
+    const float *sh_a_scale, *sh_b_scale0, *sh_b_scale1;
     // pair kernel, grouped: each segment's full 256-row tiles as usual, and
     // its remaining rows (fewer than 256) as swap units in the same launch:
     // the weights become the MMA's M = 256 operand and the few token rows
@@ -168,7 +175,7 @@ struct UnitInfo {
 };
 
 __device__ __forceinline__ UnitInfo unit_info(const TcParams &p, const int *s_seg,
-                                              const int *s_mt, int u, int ks_n)
+                                              const int *s_mt, int u, int ks_n, int kstep = 64)
 {
     UnitInfo w;
     const int sh_ks = p.sh_ksplit > 1 ? p.sh_ksplit : 1;
@@ -185,7 +192,7 @@ __device__ __forceinline__ UnitInfo unit_info(const TcParams &p, const int *s_se
         w.ti.rows = min(kTileM, p.sh_rows - w.ti.a_row0);
         w.second = true;
         n_split = sh_ks;
-        nk = (p.sh_K + 63) / 64;
+        nk = (p.sh_K + kstep - 1) / kstep;
     } else {
         const int v = u - sh_units;
         const int g = v / ks_n;
@@ -193,7 +200,7 @@ __device__ __forceinline__ UnitInfo unit_info(const TcParams &p, const int *s_se
         w.ti = tile_info(p, s_seg, s_mt, g);
         w.second = false;
         n_split = ks_n;
-        nk = (p.K + 63) / 64;
+        nk = (p.K + kstep - 1) / kstep;
     }
     w.kb0 = w.ks * nk / n_split;
     w.kb1 = (w.ks + 1) * nk / n_split;
@@ -227,15 +234,34 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const uint32_
     }
 }
 
+// Scales of an E4M3 tile's accumulator row: the A row's scale and the B
+// rows' scales of the tile's first column (gate and up for GEMM1); b0 null:
+// the operands are bf16 and nothing is scaled.
+struct EpiScale {
+    float a;
+    const float *b0, *b1;
+};
+
+// Scale of one column of an E4M3 tile: the row scale times the B row's
+// scale; `col` is the column's index in the output, `c` its index in the
+// tile (b points at the tile's first B row scale); 0 past the valid columns.
+__device__ __forceinline__ float col_scale(const float *b, float a, int col, int c, int n_valid)
+{
+    return col < n_valid ? a * __ldg(b + c) : 0.f;
+}
+
 // Epilogue of one accumulator row (TMEM lane) of a tile: this thread owns
 // output row `orow` (stored only when row_ok), columns n_idx*BN ... of the
 // tile.  taddr: TMEM address of the row's first accumulator column.
-template <int BN, int EPI>
+// SCALED: E4M3 operands, the accumulator is multiplied by the row's and the
+// column's scales (sc) first.
+template <int BN, int EPI, bool SCALED = false>
 __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long long ld_out,
                                              int n_valid, uint32_t taddr, bool row_ok,
-                                             long long orow, int n_idx, int ks = 0)
+                                             long long orow, int n_idx, int ks = 0,
+                                             EpiScale sc = EpiScale{1.f, nullptr, nullptr})
 {
-    if constexpr (EPI == EPI_SWIGLU) {
+    if constexpr (EPI == EPI_SWIGLU_F32) {
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
             uint32_t gv[32], uv[32];
@@ -243,16 +269,55 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
             tmem_ld32(taddr + BN + c0, uv);
             tmem_wait_ld();
             if (row_ok) {
+                const int col = n_idx * BN + c0;
+                float hv[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float g = __uint_as_float(gv[i]), u = __uint_as_float(uv[i]);
+                    if constexpr (SCALED) {
+                        g *= col_scale(sc.b0, sc.a, col + i, c0 + i, n_valid);
+                        u *= col_scale(sc.b1, sc.a, col + i, c0 + i, n_valid);
+                    }
+                    hv[i] = silu_f32(g) * u;
+                }
+                float *dst = reinterpret_cast<float *>(out) + orow * ld_out + col;
+                if (col + 32 <= n_valid && (ld_out & 3) == 0) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4 *>(dst + i) =
+                            make_float4(hv[i], hv[i + 1], hv[i + 2], hv[i + 3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (col + i < n_valid)
+                            dst[i] = hv[i];
+                }
+            }
+        }
+    } else if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(taddr + c0, gv);
+            tmem_ld32(taddr + BN + c0, uv);
+            tmem_wait_ld();
+            if (row_ok) {
+                const int col = n_idx * BN + c0;
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float g0 = __uint_as_float(gv[2 * i]);
-                    const float g1 = __uint_as_float(gv[2 * i + 1]);
-                    const float u0 = __uint_as_float(uv[2 * i]);
-                    const float u1 = __uint_as_float(uv[2 * i + 1]);
+                    float g0 = __uint_as_float(gv[2 * i]);
+                    float g1 = __uint_as_float(gv[2 * i + 1]);
+                    float u0 = __uint_as_float(uv[2 * i]);
+                    float u1 = __uint_as_float(uv[2 * i + 1]);
+                    if constexpr (SCALED) {
+                        g0 *= col_scale(sc.b0, sc.a, col + 2 * i, c0 + 2 * i, n_valid);
+                        g1 *= col_scale(sc.b0, sc.a, col + 2 * i + 1, c0 + 2 * i + 1, n_valid);
+                        u0 *= col_scale(sc.b1, sc.a, col + 2 * i, c0 + 2 * i, n_valid);
+                        u1 *= col_scale(sc.b1, sc.a, col + 2 * i + 1, c0 + 2 * i + 1, n_valid);
+                    }
                     pk[i] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
                 }
-                const int col = n_idx * BN + c0;
                 __nv_bfloat16 *dst =
                     reinterpret_cast<__nv_bfloat16 *>(out) + orow * ld_out + col;
                 store_row_bf16(dst, pk, col, n_valid);
@@ -271,12 +336,18 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
             tmem_ld32(taddr + c0, v);
             tmem_wait_ld();
             if (row_ok) {
+                const int col = n_idx * BN + c0;
                 uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(wr * __uint_as_float(v[2 * i]),
-                                        wr * __uint_as_float(v[2 * i + 1]));
-                const int col = n_idx * BN + c0;
+                for (int i = 0; i < 16; ++i) {
+                    float a0 = wr * __uint_as_float(v[2 * i]);
+                    float a1 = wr * __uint_as_float(v[2 * i + 1]);
+                    if constexpr (SCALED) {
+                        a0 *= col_scale(sc.b0, sc.a, col + 2 * i, c0 + 2 * i, n_valid);
+                        a1 *= col_scale(sc.b0, sc.a, col + 2 * i + 1, c0 + 2 * i + 1, n_valid);
+                    }
+                    pk[i] = pack_bf16x2(a0, a1);
+                }
                 __nv_bfloat16 *dst =
                     reinterpret_cast<__nv_bfloat16 *>(out) + (long long)tok * ld_out + col;
                 store_row_bf16(dst, pk, col, n_valid);
@@ -289,12 +360,18 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
             tmem_ld32(taddr + c0, v);
             tmem_wait_ld();
             if (row_ok) {
+                const int col = n_idx * BN + c0;
                 uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]),
-                                        __uint_as_float(v[2 * i + 1]));
-                const int col = n_idx * BN + c0;
+                for (int i = 0; i < 16; ++i) {
+                    float a0 = __uint_as_float(v[2 * i]);
+                    float a1 = __uint_as_float(v[2 * i + 1]);
+                    if constexpr (SCALED) {
+                        a0 *= col_scale(sc.b0, sc.a, col + 2 * i, c0 + 2 * i, n_valid);
+                        a1 *= col_scale(sc.b0, sc.a, col + 2 * i + 1, c0 + 2 * i + 1, n_valid);
+                    }
+                    pk[i] = pack_bf16x2(a0, a1);
+                }
                 __nv_bfloat16 *dst =
                     reinterpret_cast<__nv_bfloat16 *>(out) + orow * ld_out + col;
                 store_row_bf16(dst, pk, col, n_valid);
@@ -318,6 +395,12 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
             }
             if (row_ok) {
                 const int col = n_idx * BN + c0;
+                if constexpr (SCALED) {
+#pragma unroll
+                    for (int i = 0; i < CH; ++i)
+                        v[i] = __float_as_uint(__uint_as_float(v[i]) *
+                                               col_scale(sc.b0, sc.a, col + i, c0 + i, n_valid));
+                }
                 float *dst = reinterpret_cast<float *>(out) + ks * p.part_stride + orow * ld_out + col;
                 // 16-byte stores when the whole chunk is in range and aligned
                 const bool vec = col + CH <= n_valid && ((ld_out | p.part_stride) & 3) == 0 &&
@@ -339,7 +422,10 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
     }
 }
 
-template <int BN, int NB, int EPI, int STAGES>
+// F8: E4M3 operands (tensor maps of bytes, 128-element reduction steps in
+// the same 128-byte rows, kind::f8f6f4 MMAs with K = 32) and the scaled
+// epilogue; otherwise bf16 operands, 64-element steps, kind::f16 with K = 16.
+template <int BN, int NB, int EPI, int STAGES, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
                    const __grid_constant__ CUtensorMap mB1, const __grid_constant__ CUtensorMap sA,
@@ -347,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const TcParams p)
 {
     using S = TcShape<BN, NB, STAGES>;
+    constexpr int KSTEP = F8 ? 128 : 64;   // reduction elements per 128-byte row of a stage
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
@@ -426,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long fills = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < ntiles && ok; u += G) {
-                const UnitInfo w = unit_info(p, s_seg, s_mt, u, ks_n);
+                const UnitInfo w = unit_info(p, s_seg, s_mt, u, ks_n, KSTEP);
                 const TileInfo &ti = w.ti;
                 const bool second = w.second;
                 const int kb0 = w.kb0, kb1 = w.kb1;
@@ -442,10 +529,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *sa = smem + s * S::STAGE_BYTES;
                     uint8_t *sb = sa + S::A_BYTES;
                     mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
-                    tma_load_2d(sa, ma, &full[s], kb * 64, ti.a_row0);
-                    tma_load_2d(sb, mb0, &full[s], kb * 64, b_row);
+                    tma_load_2d(sa, ma, &full[s], kb * KSTEP, ti.a_row0);
+                    tma_load_2d(sb, mb0, &full[s], kb * KSTEP, b_row);
                     if (NB == 2)
-                        tma_load_2d(sb + S::B_BYTES, mb1, &full[s], kb * 64, b_row);
+                        tma_load_2d(sb + S::B_BYTES, mb1, &full[s], kb * KSTEP, b_row);
                     ++fills;
                     if (++s == STAGES) {
                         s = 0;
@@ -466,12 +553,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = idesc_bf16_f32(kTileM, S::UMMA_N);
+            constexpr uint32_t idesc =
+                F8 ? idesc_e4m3_f32(kTileM, S::UMMA_N) : idesc_bf16_f32(kTileM, S::UMMA_N);
             int s = 0;
             uint32_t ph = 0, b = 0, tph = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < ntiles && ok; u += G) {
-                const UnitInfo w = unit_info(p, s_seg, s_mt, u, ks_n);
+                const UnitInfo w = unit_info(p, s_seg, s_mt, u, ks_n, KSTEP);
                 const int kb0 = w.kb0, kb1 = w.kb1;
                 if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, kWaitLimitNs)) {
                     ok = false;
@@ -488,10 +576,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sa = smem_u32(smem + s * S::STAGE_BYTES);
                     const uint64_t adesc = sdesc_kmajor_sw128(sa);
                     const uint64_t bdesc = sdesc_kmajor_sw128(sa + S::A_BYTES);
+                    // four MMAs per stage, each over a 32-byte slice of the
+                    // 128-byte rows (16 bf16 or 32 E4M3 elements)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
-                                  (kb > kb0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if constexpr (F8)
+                            umma_e4m3(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                      (kb > kb0 || kk > 0) ? 1u : 0u);
+                        else
+                            umma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                      (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
                     umma_commit(&empty[s]);
                     if (++s == STAGES) {
                         s = 0;
@@ -523,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q * 32 + lane;        // accumulator row of this thread
         uint32_t b = 0, tph = 0;
         for (int u = blockIdx.x; u < ntiles; u += G) {
-            const UnitInfo w = unit_info(p, s_seg, s_mt, u, ks_n);
+            const UnitInfo w = unit_info(p, s_seg, s_mt, u, ks_n, KSTEP);
             const TileInfo &ti = w.ti;
             const int ks = w.ks;
             if (!mbar_wait(&tfull[b], tph, abort_flag, kWaitLimitNs)) {
@@ -535,21 +630,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t taddr = tmem_base + b * S::UMMA_N + ((uint32_t)(q * 32) << 16);
             const bool row_ok = r < ti.rows;
             const long long orow = (long long)ti.a_row0 + r;
+            // E4M3 operands: the row's and the tile's column scales
+            EpiScale sc{1.f, nullptr, nullptr};
+            if constexpr (F8) {
+                const float *as = w.second ? p.sh_a_scale : p.a_scale;
+                const long long b0 = (long long)(w.second ? 0 : ti.seg * p.b_seg_rows) +
+                                     (long long)ti.n_idx * BN;
+                sc.a = row_ok ? __ldg(as + orow) : 0.f;
+                sc.b0 = (w.second ? p.sh_b_scale0 : p.b_scale0) + b0;
+                sc.b1 = NB == 2 ? (w.second ? p.sh_b_scale1 : p.b_scale1) + b0 : sc.b0;
+            }
             if (w.second) {
                 if constexpr (EPI == EPI_BF16) {
                     if (p.sh_ksplit > 1)  // fp32 partial sums of a piece of the reduction
-                        epilogue_row<BN, EPI_F32>(p, p.sh_out, p.sh_ld_out, p.sh_N_valid, taddr,
-                                                  row_ok, orow, ti.n_idx, ks);
+                        epilogue_row<BN, EPI_F32, F8>(p, p.sh_out, p.sh_ld_out, p.sh_N_valid,
+                                                      taddr, row_ok, orow, ti.n_idx, ks, sc);
                     else
-                        epilogue_row<BN, EPI>(p, p.sh_out, p.sh_ld_out, p.sh_N_valid, taddr,
-                                              row_ok, orow, ti.n_idx, ks);
+                        epilogue_row<BN, EPI, F8>(p, p.sh_out, p.sh_ld_out, p.sh_N_valid, taddr,
+                                                  row_ok, orow, ti.n_idx, ks, sc);
                 } else {
-                    epilogue_row<BN, EPI>(p, p.sh_out, p.sh_ld_out, p.sh_N_valid, taddr, row_ok,
-                                          orow, ti.n_idx, ks);
+                    epilogue_row<BN, EPI, F8>(p, p.sh_out, p.sh_ld_out, p.sh_N_valid, taddr,
+                                              row_ok, orow, ti.n_idx, ks, sc);
                 }
             } else
-                epilogue_row<BN, EPI>(p, p.out, p.ld_out, p.N_valid, taddr, row_ok, orow,
-                                      ti.n_idx, ks);
+                epilogue_row<BN, EPI, F8>(p, p.out, p.ld_out, p.N_valid, taddr, row_ok, orow,
+                                          ti.n_idx, ks, sc);
             tc_fence_before_sync();
             mbar_arrive(&tempty[b]);
             b ^= 1u;
@@ -1191,13 +1296,13 @@ struct SecondMaps {
     CUtensorMap a, b0, b1;
 };
 
-template <int BN, int NB, int EPI, int STAGES>
+template <int BN, int NB, int EPI, int STAGES, bool F8 = false>
 cudaError_t launch_tc(const CUtensorMap &mA, const CUtensorMap &mB0, const CUtensorMap &mB1,
                       const TcParams &p, long long max_tiles, cudaStream_t stream,
                       const SecondMaps *second = nullptr)
 {
     using S = TcShape<BN, NB, STAGES>;
-    auto kern = tc_gemm_kernel<BN, NB, EPI, STAGES>;
+    auto kern = tc_gemm_kernel<BN, NB, EPI, STAGES, F8>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
@@ -1571,6 +1676,151 @@ cudaError_t launch_dense_tc(int rows, int N, int K, const void *A, const void *B
         return launch_tc<32, 1, EPI_BF16, 8>(mA, mB, mB, p, mt * p.n_tiles, stream);
     return bn == 256 ? launch_tc<256, 1, EPI_BF16, 4>(mA, mB, mB, p, mt * p.n_tiles, stream)
                      : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt * p.n_tiles, stream);
+}
+
+cudaError_t launch_experts_w8a8(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                                const void *x, const ExpertW8 &w, void *y, const AuxArgs &aux,
+                                cudaStream_t stream, cudaEvent_t *ev)
+{
+    const int D = c.d_model, F = c.d_expert, S = c.d_shared, E = c.n_experts, T = c.T;
+    const A8Layout A = a8_layout_of(c, L);
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    const int32_t *seg = reinterpret_cast<const int32_t *>(ws + L.seg_off);
+    const int32_t *mtile = reinterpret_cast<const int32_t *>(ws + L.mtile);
+    const long long R = L.R_max;
+    const long long mt_bound = R / kTileM + E;
+    const long long mt_s = (T + kTileM - 1) / kTileM;
+    const LaunchPlan plan = plan_of(c);
+    const bool shared = S > 0;
+    // the shared expert always runs as the second problem of the routed
+    // launches; its down projection is cut into fp32 pieces exactly when the
+    // combine expects them (shared_down_splits)
+    const int zsplit = shared ? shared_down_splits(c) : 1;
+    const bool wide_down = D > 1024;
+    const int bn_down = wide_down ? 256 : 128;
+    uint8_t *xq = ws + A.xq, *hq = ws + A.hq, *sxq = ws + A.sxq, *shq = ws + A.shq;
+    float *xs = reinterpret_cast<float *>(ws + A.xs), *hsc = reinterpret_cast<float *>(ws + A.hsc);
+    float *sxs = reinterpret_cast<float *>(ws + A.sxs), *shs = reinterpret_cast<float *>(ws + A.shs);
+    float *hf = reinterpret_cast<float *>(ws + A.hf), *shf = reinterpret_cast<float *>(ws + A.shf);
+    cudaError_t err;
+
+    // the kept token rows (their count is the dispatch kernel's seg_off[E])
+    // and, for the shared expert, every token row to E4M3
+    err = launch_quantize_e4m3_act(R, D, ws + L.x_perm, false, xq, xs, seg + E, stream);
+    if (err == cudaSuccess && shared)
+        err = launch_quantize_e4m3_act(T, D, x, false, sxq, sxs, nullptr, stream);
+    if (err != cudaSuccess)
+        return err;
+    // GEMM1: hf = silu(xq Wg^T) * (xq Wu^T), fp32 (+ shf from the shared expert)
+    {
+        CUtensorMap mA, mG, mU;
+        if (!make_map_u8(&mA, xq, (uint64_t)R, (uint64_t)D, kTileM) ||
+            !make_map_u8(&mG, w.gate, (uint64_t)E * F, (uint64_t)D, 128) ||
+            !make_map_u8(&mU, w.up, (uint64_t)E * F, (uint64_t)D, 128))
+            return cudaErrorInvalidValue;
+        TcParams p{};
+        p.seg_off = seg;
+        p.mtile = mtile;
+        p.nseg = E;
+        p.K = D;
+        p.n_tiles = (F + 127) / 128;
+        p.N_valid = F;
+        p.b_seg_rows = F;
+        p.out = hf;
+        p.ld_out = F;
+        p.status = status;
+        p.aux = aux;
+        p.a_scale = xs;
+        p.b_scale0 = w.gate_s;
+        p.b_scale1 = w.up_s;
+        SecondMaps sm;
+        if (shared) {
+            if (!make_map_u8(&sm.a, sxq, (uint64_t)T, (uint64_t)D, kTileM) ||
+                !make_map_u8(&sm.b0, w.sgate, (uint64_t)S, (uint64_t)D, 128) ||
+                !make_map_u8(&sm.b1, w.sup, (uint64_t)S, (uint64_t)D, 128))
+                return cudaErrorInvalidValue;
+            p.sh_n_tiles = (S + 127) / 128;
+            p.sh_tiles = (int)(mt_s * p.sh_n_tiles);
+            p.sh_rows = T;
+            p.sh_K = D;
+            p.sh_N_valid = S;
+            p.sh_out = shf;
+            p.sh_ld_out = S;
+            p.sh_a_scale = sxs;
+            p.sh_b_scale0 = w.sgate_s;
+            p.sh_b_scale1 = w.sup_s;
+        }
+        err = launch_tc<128, 2, EPI_SWIGLU_F32, 4, true>(mA, mG, mU, p, mt_bound * p.n_tiles,
+                                                         stream, shared ? &sm : nullptr);
+        if (err == cudaSuccess)
+            err = launch_quantize_e4m3_act(R, F, hf, true, hq, hsc, seg + E, stream);
+        if (err == cudaSuccess && shared)
+            err = launch_quantize_e4m3_act(T, S, shf, true, shq, shs, nullptr, stream);
+        if (err == cudaSuccess)
+            err = record_stage(ev, 3, stream);
+        if (err != cudaSuccess)
+            return err;
+    }
+    // GEMM2: z = hq Wd^T (or w * ... into y), (+ zs from the shared expert)
+    {
+        CUtensorMap mA, mB;
+        if (!make_map_u8(&mA, hq, (uint64_t)R, (uint64_t)F, kTileM) ||
+            !make_map_u8(&mB, w.down, (uint64_t)E * D, (uint64_t)F, (uint32_t)bn_down))
+            return cudaErrorInvalidValue;
+        TcParams p{};
+        p.seg_off = seg;
+        p.mtile = mtile;
+        p.nseg = E;
+        p.K = F;
+        p.n_tiles = (D + bn_down - 1) / bn_down;
+        p.N_valid = D;
+        p.b_seg_rows = D;
+        p.out = ws + L.z;
+        p.ld_out = D;
+        p.status = status;
+        p.a_scale = hsc;
+        p.b_scale0 = w.down_s;
+        p.b_scale1 = w.down_s;
+        SecondMaps sm;
+        if (shared) {
+            if (!make_map_u8(&sm.a, shq, (uint64_t)T, (uint64_t)S, kTileM) ||
+                !make_map_u8(&sm.b0, w.sdown, (uint64_t)D, (uint64_t)S, (uint32_t)bn_down))
+                return cudaErrorInvalidValue;
+            sm.b1 = sm.b0;
+            p.sh_n_tiles = p.n_tiles;
+            p.sh_tiles = (int)(mt_s * p.sh_n_tiles);
+            p.sh_rows = T;
+            p.sh_K = S;
+            p.sh_N_valid = D;
+            p.sh_out = ws + L.zs;
+            p.sh_ld_out = D;
+            p.sh_ksplit = zsplit;
+            p.part_stride = (long long)T * D;
+            p.sh_a_scale = shs;
+            p.sh_b_scale0 = w.sdown_s;
+            p.sh_b_scale1 = w.sdown_s;
+        }
+        const SecondMaps *second = shared ? &sm : nullptr;
+        const long long tiles = mt_bound * p.n_tiles;
+        if (plan.direct_y) {
+            p.out = y;
+            p.row_tok = reinterpret_cast<const int32_t *>(ws + L.row_tok);
+            p.row_w = reinterpret_cast<const float *>(ws + L.row_w);
+            err = wide_down ? launch_tc<256, 1, EPI_BF16_Y, 4, true>(mA, mB, mB, p, tiles, stream)
+                            : launch_tc<128, 1, EPI_BF16_Y, 6, true>(mA, mB, mB, p, tiles, stream);
+        } else {
+            err = wide_down
+                      ? launch_tc<256, 1, EPI_BF16, 4, true>(mA, mB, mB, p, tiles, stream, second)
+                      : launch_tc<128, 1, EPI_BF16, 6, true>(mA, mB, mB, p, tiles, stream, second);
+        }
+        if (err == cudaSuccess)
+            err = record_stage(ev, 4, stream);
+        if (err == cudaSuccess)
+            err = record_stage(ev, 5, stream);
+        if (err == cudaSuccess)
+            err = record_stage(ev, 6, stream);
+    }
+    return err;
 }
 
 }  // namespace moe

@@ -626,28 +626,54 @@ cudaError_t launch_w8(const CUtensorMap (&m)[6], const W8Params &p, long long ma
                       m[0], m[1], m[2], m[3], m[4], m[5], p);
 }
 
+// Eight consecutive values of a row as fp32 (v-th group of eight).
+__device__ __forceinline__ void load8(const __nv_bfloat16 *row, long long v, float (&f)[8])
+{
+    const uint4 x = reinterpret_cast<const uint4 *>(row)[v];
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&x);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ void load8(const float *row, long long v, float (&f)[8])
+{
+    const float4 a = reinterpret_cast<const float4 *>(row)[2 * v];
+    const float4 b = reinterpret_cast<const float4 *>(row)[2 * v + 1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
 // q[r][c] = e4m3(W[r][c] / s_r), s_r = max_c |W[r][c]| / 448 (1 for an
 // all-zero row); fp32 division, round to nearest even, saturating to +-448.
-// One warp per row, 8 columns per lane and step.
+// One warp per row, 8 columns per lane and step.  TIN: bf16 (weights, token
+// rows) or fp32 (hidden rows).  rows_dev non-null: only the first
+// min(rows, *rows_dev) rows (a row count the previous kernel wrote).
+template <typename TIN>
 __global__ void __launch_bounds__(256)
-    quantize_e4m3_kernel(long long rows, long long cols, const __nv_bfloat16 *__restrict__ W,
-                         uint8_t *__restrict__ q, float *__restrict__ scale)
+    quantize_e4m3_kernel(long long rows, long long cols, const TIN *__restrict__ W,
+                         uint8_t *__restrict__ q, float *__restrict__ scale,
+                         const int32_t *__restrict__ rows_dev)
 {
+    griddep_wait();   // the rows (and their count) come from the previous kernel
+    if (rows_dev)
+        rows = min(rows, (long long)*(volatile const int32_t *)rows_dev);
     const int lane = threadIdx.x & 31;
     const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
     for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
          r += warps) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(W + r * cols);
+        const TIN *src = W + r * cols;
         const long long nv = cols / 8;
         float amax = 0.f;
         for (long long v = lane; v < nv; v += 32) {
-            const uint4 x = src[v];
-            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&x);
+            float f[8];
+            load8(src, v, f);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 f = __bfloat1622float2(h[i]);
-                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-            }
+            for (int i = 0; i < 4; ++i)
+                amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
         }
         amax = warp_max(amax);
         const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
@@ -655,14 +681,13 @@ __global__ void __launch_bounds__(256)
             scale[r] = s;
         uint2 *dst = reinterpret_cast<uint2 *>(q + r * cols);
         for (long long v = lane; v < nv; v += 32) {
-            const uint4 x = src[v];
-            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&x);
+            float f[8];
+            load8(src, v, f);
             uint32_t word[2] = {0u, 0u};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float2 f = __bfloat1622float2(h[i]);
-                const uint32_t c0 = __nv_cvt_float_to_fp8(__fdiv_rn(f.x, s), __NV_SATFINITE, __NV_E4M3);
-                const uint32_t c1 = __nv_cvt_float_to_fp8(__fdiv_rn(f.y, s), __NV_SATFINITE, __NV_E4M3);
+                const uint32_t c0 = __nv_cvt_float_to_fp8(__fdiv_rn(f[2 * i], s), __NV_SATFINITE, __NV_E4M3);
+                const uint32_t c1 = __nv_cvt_float_to_fp8(__fdiv_rn(f[2 * i + 1], s), __NV_SATFINITE, __NV_E4M3);
                 word[i >> 1] |= (c0 | (c1 << 8)) << (16 * (i & 1));
             }
             dst[v] = make_uint2(word[0], word[1]);
@@ -678,9 +703,23 @@ cudaError_t launch_quantize_e4m3(long long rows, long long cols, const void *W, 
     if (rows <= 0)
         return cudaSuccess;
     const long long blocks = std::min<long long>((rows + 7) / 8, 16LL * sm_count());
-    quantize_e4m3_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-        rows, cols, static_cast<const __nv_bfloat16 *>(W), q, scale);
+    quantize_e4m3_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(
+        rows, cols, static_cast<const __nv_bfloat16 *>(W), q, scale, nullptr);
     return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_e4m3_act(long long rows, long long cols, const void *X, bool fp32,
+                                     uint8_t *q, float *scale, const int32_t *rows_dev,
+                                     cudaStream_t stream)
+{
+    if (rows <= 0)
+        return cudaSuccess;
+    const unsigned blocks = (unsigned)std::min<long long>((rows + 7) / 8, 16LL * sm_count());
+    if (fp32)
+        return launch_pdl(quantize_e4m3_kernel<float>, dim3(blocks), dim3(256), 0, stream, rows,
+                          cols, static_cast<const float *>(X), q, scale, rows_dev);
+    return launch_pdl(quantize_e4m3_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, stream,
+                      rows, cols, static_cast<const __nv_bfloat16 *>(X), q, scale, rows_dev);
 }
 
 cudaError_t launch_experts_w8(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,

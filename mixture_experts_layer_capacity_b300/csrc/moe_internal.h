@@ -192,16 +192,45 @@ struct ExpertW8 {
     const float *gate_s, *up_s, *down_s;    // [E*F], [E*F], [E*D]
     const uint8_t *sgate, *sup, *sdown;     // [S,D], [S,D], [D,S]
     const float *sgate_s, *sup_s, *sdown_s; // [S], [S], [D]
+    bool a8;                                // activations in E4M3 too (launch_experts_w8a8)
 };
 // The routed and shared SwiGLU experts with e4m3 weights (moe_gemm_w8.cu);
 // `ev`: stage events 3..6 as in launch_experts_tc.
 cudaError_t launch_experts_w8(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                               const void *x, const ExpertW8 &w, void *y, const AuxArgs &aux,
                               cudaStream_t stream, cudaEvent_t *ev = nullptr);
+// Extra workspace of the E4M3-activation path (after WorkspaceLayout::total):
+// E4M3 codes and fp32 row scales of the token rows, of the hidden rows (kept
+// in fp32 before they are quantized), and of the shared expert's x and
+// hidden rows.
+struct A8Layout {
+    size_t xq, xs;     // uint8[R_max][D], float[R_max]
+    size_t hf;         // float[R_max][F]
+    size_t hq, hsc;    // uint8[R_max][F], float[R_max]
+    size_t sxq, sxs;   // uint8[T][D], float[T]         (shared expert)
+    size_t shf;        // float[T][S]
+    size_t shq, shs;   // uint8[T][S], float[T]
+    size_t total;
+};
+A8Layout a8_layout_of(const moe_config &c, const WorkspaceLayout &L);
+// The routed and shared SwiGLU experts with E4M3 weights and E4M3
+// activations (moe_gemm_tc.cu): the token rows, and the hidden rows between
+// the two GEMMs, are quantized row-wise; the tensor-core GEMMs take both
+// operands in E4M3 (kind::f8f6f4) and scale the accumulator by the row's and
+// the weight row's scales.  `ev`: stage events 3..6 as in launch_experts_tc.
+cudaError_t launch_experts_w8a8(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                                const void *x, const ExpertW8 &w, void *y, const AuxArgs &aux,
+                                cudaStream_t stream, cudaEvent_t *ev = nullptr);
 // q[r][c] = e4m3(W[r][c] / scale[r]), scale[r] = max_c |W[r][c]| / 448
 // (moe_gemm_w8.cu).
 cudaError_t launch_quantize_e4m3(long long rows, long long cols, const void *W, uint8_t *q,
                                  float *scale, cudaStream_t stream);
+// Row-wise E4M3 quantization of activation rows X [rows, cols] (bf16, or
+// fp32 when fp32), launched with programmatic serialization; rows_dev non-null:
+// only the first min(rows, *rows_dev) rows.
+cudaError_t launch_quantize_e4m3_act(long long rows, long long cols, const void *X, bool fp32,
+                                     uint8_t *q, float *scale, const int32_t *rows_dev,
+                                     cudaStream_t stream);
 
 // The layer on a validated config and workspace (moe_api.cu).
 moe_status forward_body(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,

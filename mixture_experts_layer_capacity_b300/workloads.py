@@ -51,6 +51,8 @@ class Workload:
     D_outer: int = 0      # latent MoE: outer width (x and y); 0 = plain layer
     weights: str = "bf16"  # expert weight storage: "bf16", or "e4m3" (row-scaled FP8,
                            # quantized from the same seeded bf16 weights)
+    acts: str = "bf16"     # expert GEMM activations: "bf16", or "e4m3" (row-scaled FP8
+                           # token and hidden rows; needs weights="e4m3")
     description: str = ""
 
     def with_T(self, T: int) -> "Workload":
@@ -124,6 +126,24 @@ WORKLOADS = {
         "dsv3_decode_fp8", T=64, D=7168, E=256, F=2048, k=8, S=2048,
         mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1", weights="e4m3",
         description="DeepSeek-V3-shaped, T=64, E4M3 expert weights"),
+    # E4M3 token and hidden rows as well as E4M3 expert weights (both GEMM
+    # operands in FP8 on the tensor cores)
+    "mixtral_decode_w8a8": Workload(
+        "mixtral_decode_w8a8", T=64, D=4096, E=8, F=14336, k=2,
+        mode=GATING_SOFTMAX_SELECTED, weights="e4m3", acts="e4m3",
+        description="Mixtral-8x7B-shaped, T=64, E4M3 expert weights and activations"),
+    "qwen2_57b_decode_w8a8": Workload(
+        "qwen2_57b_decode_w8a8", T=64, D=3584, E=64, F=2560, k=8, S=20480,
+        mode=GATING_SOFTMAX_ALL, weights="e4m3", acts="e4m3",
+        description="Qwen2-57B-A14B-shaped, T=64, E4M3 expert weights and activations"),
+    "dsv3_decode_w8a8": Workload(
+        "dsv3_decode_w8a8", T=64, D=7168, E=256, F=2048, k=8, S=2048,
+        mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1", weights="e4m3", acts="e4m3",
+        description="DeepSeek-V3-shaped, T=64, E4M3 expert weights and activations"),
+    "dsv3_prefill_w8a8": Workload(
+        "dsv3_prefill_w8a8", T=16384, D=7168, E=256, F=2048, k=8, S=2048,
+        mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1", weights="e4m3", acts="e4m3",
+        description="DeepSeek-V3-shaped, T=16384, E4M3 expert weights and activations"),
     "dsv3_sigmoid_decode": Workload(
         "dsv3_sigmoid_decode", T=64, D=7168, E=256, F=2048, k=8, S=2048,
         mode=GATING_SIGMOID_SELECTED, bias="zipf1.1", sel_bias=True,

@@ -41,7 +41,8 @@ def run(w, seed=0, inputs=None, stream=None):
     returned inputs are the bf16 ones (the oracle quantizes them itself)."""
     cfg = B.config_of(w)
     inp = inputs if inputs is not None else make_inputs(w, seed, "cuda")
-    run_inp = B.quantize_expert_weights(inp, stream) if w.weights == "e4m3" else inp
+    run_inp = (B.quantize_expert_weights(inp, stream, a8=w.acts == "e4m3")
+               if w.weights == "e4m3" else inp)
     outs = B.forward(cfg, run_inp, stream=stream)
     code = B.read_device_status(cfg, outs["workspace"], stream=stream)
     return cfg, inp, outs, code
@@ -142,12 +143,13 @@ def e4m3_weights(W):
 
 
 def check(w, inp, outs, sample=None, logit_rows=None, y_sample_n=None, seed=0, e4m3=False,
-          coverage=False):
+          coverage=False, a8=False):
     """Asserts every parity criterion; returns a dict of the measured errors.
     coverage: y on coverage_sample's tokens (at least y_sample_n, default
     512) instead of a plain random sample.
     e4m3: the layer ran with E4M3 expert weights; the oracle quantizes the
-    same bf16 weights itself and computes with the dequantized values."""
+    same bf16 weights itself and computes with the dequantized values.
+    a8: E4M3 activations too (the oracle's swiglu_rows_w8a8)."""
     T, E, k = w.T, w.E, w.k
     gamma32 = float(np.float32(w.gamma))
     alpha32 = float(np.float32(w.alpha))
@@ -214,7 +216,7 @@ def check(w, inp, outs, sample=None, logit_rows=None, y_sample_n=None, seed=0, e
     Wg, Wu, Wd = inp["W_gate"], inp["W_up"], inp["W_down"]
     if e4m3:
         def weights(*Ws):
-            return tuple(a for W in Ws for a in e4m3_weights(W))
+            return tuple(a for W in Ws for a in e4m3_weights(W)) + (("a8",) if a8 else ())
     else:
         def weights(*Ws):
             return tuple(f32(W) for W in Ws)

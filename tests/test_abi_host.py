@@ -228,3 +228,41 @@ def test_debug_bounds_build_exports_the_same_symbols():
 
     assert exported(dbg) == exported(B.LIB_PATH)
     assert set(_declared_symbols()) <= set(exported(dbg))
+
+
+def _call_w8a8(cfg, ws, ws_bytes, shared=True):
+    """moe_forward_w8a8 with fake (never dereferenced) 16-byte aligned
+    pointers; returns the status."""
+    vals = [4096 * (i + 1) for i in range(23)]
+    if not shared:
+        for i in range(12, 18):       # Ws_gate_q ... Ws_down_scale
+            vals[i - 3] = None
+    args = [ctypes.c_void_p(v) if v else None for v in vals] + [ctypes.c_void_p(ws) if ws else None]
+    return B.lib().moe_forward_w8a8(ctypes.byref(cfg), *args, ctypes.c_size_t(ws_bytes), None)
+
+
+def test_w8a8_workspace_and_validation():
+    cfg = B.make_config(64, 512, 8, 256, 2, d_shared=256)
+    need = B.w8a8_workspace_size(cfg)
+    base = B.workspace_size(cfg)
+    R, D, F, T, S = 64 * 2, 512, 256, 64, 256
+    # the quantized rows, the fp32 hidden rows and their shared-expert copies
+    assert need >= base + R * (D + F + 4 * F + 8) + T * (D + S + 4 * S + 8)
+    L = B.lib()
+    offs = [ctypes.c_size_t(0) for _ in range(5)]
+    assert L.moe_w8a8_offsets(ctypes.byref(cfg), *[ctypes.byref(o) for o in offs]) == B.MOE_OK
+    xq, xs, hf, hq, hs = (o.value for o in offs)
+    assert base <= xq and xq + R * D <= xs and xs + 4 * R <= hf and hf + 4 * R * F <= hq
+    assert hq + R * F <= hs and hs + 4 * R <= need
+    assert L.moe_w8a8_offsets(ctypes.byref(cfg), None, *[ctypes.byref(o) for o in offs[1:]]) \
+        == B.MOE_ERR_INVALID_ARG
+    # the bf16 layer's workspace is too small for the quantized activations
+    assert _call_w8a8(cfg, 1 << 20, base) == B.MOE_ERR_WORKSPACE
+    assert _call_w8a8(cfg, (1 << 20) + 128, need) == B.MOE_ERR_WORKSPACE
+    # fp32 layers, and a shared expert with d_expert < 128, are not supported
+    f32 = B.make_config(64, 512, 8, 256, 2, d_shared=256, dtype="fp32")
+    assert _call_w8a8(f32, 1 << 20, need) == B.MOE_ERR_UNSUPPORTED
+    narrow = B.make_config(64, 512, 8, 64, 2, d_shared=256)
+    assert _call_w8a8(narrow, 1 << 20, 1 << 30) == B.MOE_ERR_UNSUPPORTED
+    # a missing shared weight when the layer has a shared expert
+    assert _call_w8a8(cfg, 1 << 20, need, shared=False) == B.MOE_ERR_INVALID_ARG

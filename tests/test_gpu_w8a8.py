@@ -1,0 +1,152 @@
+"""E4M3 activations as well as E4M3 expert weights (moe_forward_w8a8)
+against the CPU oracle, through the C ABI.
+
+The quantized activations the library leaves in its workspace are checked
+bit for bit: the permuted token rows' codes and scales against the oracle's
+row quantizer applied to the same token rows in expert order, and the hidden
+rows' codes and scales against the oracle's quantizer applied to the
+library's own fp32 hidden rows (the hidden values themselves come out of a
+GPU reduction whose rounding order differs from the oracle's, so they are
+compared within tolerance through y).  Routing is checked as for bf16
+weights and y against the oracle's fp64 layer with quantized activations
+(oracle.swiglu_rows_w8a8), at the bf16 tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from mixture_experts_layer_capacity_b300 import binding as B
+from mixture_experts_layer_capacity_b300.workloads import WORKLOADS, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    torch.cuda.synchronize()
+
+
+def _expert_order(idx, dropped, E):
+    """Token of each kept assignment in the layer's expert order (experts
+    ascending, tokens ascending within an expert)."""
+    T, k = idx.shape
+    t_all = np.repeat(np.arange(T), k)
+    e_all = idx.ravel().astype(np.int64)
+    kept = dropped.ravel() == 0
+    t_k, e_k = t_all[kept], e_all[kept]
+    return t_k[np.lexsort((t_k, e_k))]
+
+
+def _check_quantized_rows(w, inp, outs, max_rows=None):
+    """Bit-exact checks of the quantized token and hidden rows: all of them,
+    or (max_rows) the first, the last and a seeded sample."""
+    cfg = B.config_of(w)
+    idx = outs["topk_idx"].cpu().numpy()
+    dropped = outs["dropped_mask"].cpu().numpy()
+    order = _expert_order(idx, dropped, w.E)
+    R = int(outs["kept_counts"].sum())
+    assert order.size == R
+    rows = np.arange(R)
+    if max_rows is not None and R > max_rows:
+        rng = np.random.default_rng(3)
+        rows = np.unique(np.concatenate([[0, R - 1], rng.choice(R, max_rows, replace=False)]))
+    sel = torch.as_tensor(rows, device=inp["x"].device)
+    act = B.w8a8_activations(cfg, outs["workspace"], R)
+    x = parity.f32(inp["x"])
+    q_ref, s_ref = oracle.quantize_e4m3_rows(x[order[rows]])
+    np.testing.assert_array_equal(act["x_scales"][sel].cpu().numpy(), s_ref)
+    np.testing.assert_array_equal(act["x_codes"][sel].cpu().numpy(), q_ref)
+    h = act["h_values"][sel].cpu().numpy()
+    assert np.isfinite(h).all()
+    hq_ref, hs_ref = oracle.quantize_e4m3_rows(h)
+    np.testing.assert_array_equal(act["h_scales"][sel].cpu().numpy(), hs_ref)
+    np.testing.assert_array_equal(act["h_codes"][sel].cpu().numpy(), hq_ref)
+    return R
+
+
+# name, T, D, E, F, k, S, mode, gamma, bias
+CASES = [
+    # shared expert narrower than the routed ones; several token tiles
+    ("a8_multi_tile_top2", 1000, 256, 8, 384, 2, 192, 0, 0.0, "none"),
+    # F = 320 and D = 192 leave partial tiles and a half-empty last 128-wide
+    # reduction step; capacity drops
+    ("a8_ragged_capacity_e16", 777, 192, 16, 320, 4, 0, 1, 0.75, "normal_var2"),
+    # decode-like: 64 experts, shared down projection cut into S / F = 8 pieces
+    ("a8_decode_e64_shared_pieces", 64, 512, 64, 128, 8, 1024, 2, 0.0, "zipf1.1"),
+    # k = 1 without a shared expert: the down projection writes y
+    ("a8_top1_direct_y", 300, 256, 8, 256, 1, 0, 1, 1.0, "normal_var2"),
+    # one token, wide d_model (256-wide output tiles, a ragged one)
+    ("a8_one_token_wide", 1, 1088, 8, 192, 2, 320, 0, 0.0, "none"),
+    # segments of ~250 rows: several 128-row tiles per expert
+    ("a8_long_segments", 500, 128, 4, 128, 2, 0, 0, 0.0, "none"),
+    # d_expert = 64 without a shared expert (one half-filled reduction step)
+    ("a8_narrow_expert", 200, 256, 8, 64, 2, 0, 0, 0.0, "none"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_w8a8_layers(case):
+    name, T, D, E, F, k, S, mode, gamma, bias = case
+    w = Workload(name, T=T, D=D, E=E, F=F, k=k, S=S, mode=mode, gamma=gamma, dtype="bf16",
+                 alpha=0.01, bias=bias, weights="e4m3", acts="e4m3")
+    _, inp, outs, code = parity.run(w, seed=23)
+    assert code == B.MOE_DEVICE_OK
+    R = _check_quantized_rows(w, inp, outs)
+    rep = parity.check(w, inp, outs, e4m3=True, a8=True)
+    rep["rows"] = R
+    print(name, rep)
+
+
+def test_w8a8_zero_tokens():
+    w = Workload("a8_empty", T=0, D=128, E=8, F=128, k=2, S=128, mode=0, gamma=1.0,
+                 weights="e4m3", acts="e4m3")
+    cfg = B.config_of(w)
+    inp = B.quantize_expert_weights(make_inputs(w, 0, "cuda"), a8=True)
+    outs = B.alloc_outputs(cfg, a8=True)
+    outs["expert_counts"].fill_(7)
+    outs["aux_loss"].fill_(3.0)
+    B.forward(cfg, inp, outs)
+    torch.cuda.synchronize()
+    assert int(outs["expert_counts"].abs().sum()) == 0
+    assert float(outs["aux_loss"][0]) == 0.0
+
+
+def test_w8a8_rejects_the_bf16_workspace():
+    w = Workload("a8_ws", T=32, D=128, E=4, F=128, k=2, weights="e4m3", acts="e4m3")
+    cfg = B.config_of(w)
+    inp = B.quantize_expert_weights(make_inputs(w, 0, "cuda"), a8=True)
+    outs = B.alloc_outputs(cfg)                  # sized for moe_forward
+    with pytest.raises(B.MoeError) as ei:
+        B.forward(cfg, inp, outs)
+    assert ei.value.status == B.MOE_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("name", ["mixtral_decode_w8a8", "qwen2_57b_decode_w8a8",
+                                  "dsv3_decode_w8a8"])
+def test_w8a8_benchmark_sized_decode(name):
+    w = WORKLOADS[name]
+    _, inp, outs, code = parity.run(w)
+    assert code == B.MOE_DEVICE_OK
+    _check_quantized_rows(w, inp, outs)
+    # decode-sized: scores, routing and y on every token
+    rep = parity.check(w, inp, outs, e4m3=True, a8=True)
+    assert rep["y_rows"] == w.T
+    print(name, rep)
+    del inp, outs
+    torch.cuda.empty_cache()
+
+
+def test_w8a8_benchmark_sized_prefill():
+    w = WORKLOADS["dsv3_prefill_w8a8"]
+    _, inp, outs, code = parity.run(w)
+    assert code == B.MOE_DEVICE_OK
+    _check_quantized_rows(w, inp, outs, max_rows=8192)
+    rep = parity.check(w, inp, outs, e4m3=True, a8=True, coverage=True, y_sample_n=256,
+                       logit_rows=np.arange(w.T))
+    print(w.name, rep)
+    del inp, outs
+    torch.cuda.empty_cache()
