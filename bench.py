@@ -177,20 +177,21 @@ def stage_activation_bytes(w, kept_total, shared_fused=False):
     """Activation bytes each stage moves on top of its algorithmic bytes
     (diagnostic only): the routed GEMMs read x_perm / h and write h / z, the
     shared GEMMs read x / hs and write hs / zs, the dispatch writes x_perm,
-    the combine reads z (and zs).  With E4M3 activations the GEMM1 stage
-    also quantizes x_perm (and x) and its fp32 hidden rows: it reads bf16
-    token rows, writes codes and scales, writes and reads back the fp32
-    hidden rows and writes their codes; GEMM2 reads the hidden codes."""
+    the combine reads z (and zs).  With E4M3 activations the router stage
+    also quantizes every token row (reads x, writes codes and scales), the
+    dispatch gathers codes and scales instead of bf16 rows, GEMM1 reads
+    codes, writes fp32 hidden rows and quantizes them (reads them back,
+    writes codes and scales), and GEMM2 reads the hidden codes."""
     b = 2 if w.dtype == "bf16" else 4
     D, F, S, T = w.D, w.F, w.S, w.T
     if w.acts == "e4m3":
-        def a8(n, d_in, f):   # one row set through quantize, GEMM1, quantize, GEMM2
-            return {"g1": n * (b * d_in + (d_in + 4) + d_in + 4 * f + 4 * f + (f + 4)),
+        def a8(n, f):   # one row set through GEMM1, the hidden quantizer, GEMM2
+            return {"g1": n * (D + 4 + 4 * f + 4 * f + (f + 4)),
                     "g2": n * (f + 4 + b * D)}
-        r, sh = a8(kept_total, D, F), a8(T, D, S) if S else {"g1": 0, "g2": 0}
-        return {"router": b * T * D + 4 * T * w.E,
+        r, sh = a8(kept_total, F), a8(T, S) if S else {"g1": 0, "g2": 0}
+        return {"router": b * T * D + 4 * T * w.E + T * (b * D + D + 4),
                 "gemm1_routed": r["g1"] + sh["g1"], "gemm2_routed": r["g2"] + sh["g2"],
-                "dispatch": b * kept_total * D,
+                "dispatch": kept_total * (D + 4),
                 "combine": b * (kept_total * D + (T * D if S else 0))}
     extra = {
         "router": b * T * D + 4 * T * w.E,
@@ -641,14 +642,14 @@ def run_ours(args, rank, world, device):
     # shared-expert GEMMs), combine (unless GEMM2 writes y); a latent layer
     # adds its two projections
     # E4M3 layers run the shared expert inside the routed GEMM launches; with
-    # E4M3 activations the token rows (routed, shared) and the hidden rows
+    # E4M3 activations the token rows (once per token) and the hidden rows
     # (routed, shared) are quantized by one launch each
     plan = B.launch_plan(cfg)
     shared_apart = w.S and not plan["shared_fused"] and w.weights != "e4m3"
     launches_per_step = (2 if w.D_outer else 0) + \
         (0 if plan["router_fused"] else 1) + 3 + \
         (2 if shared_apart else 0) + (0 if plan["direct_y"] else 1) + \
-        ((2 + (2 if w.S else 0)) if a8 else 0)
+        ((2 + (1 if w.S else 0)) if a8 else 0)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,

@@ -114,8 +114,8 @@ A8Layout a8_layout_of(const moe_config &c, const WorkspaceLayout &L)
     A.hf = take(sizeof(float) * R * F);
     A.hq = take((size_t)R * F);
     A.hsc = take(sizeof(float) * R);
-    A.sxq = take(S > 0 ? (size_t)T * D : 0);
-    A.sxs = take(S > 0 ? sizeof(float) * T : 0);
+    A.sxq = take((size_t)T * D);
+    A.sxs = take(sizeof(float) * T);
     A.shf = take(S > 0 ? sizeof(float) * T * S : 0);
     A.shq = take(S > 0 ? (size_t)T * S : 0);
     A.shs = take(S > 0 ? sizeof(float) * T : 0);
@@ -242,7 +242,8 @@ moe_status route_step(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws
                       const void *W_r, const float *router_bias, float *router_logits,
                       int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
                       int32_t *expert_counts, int32_t *kept_counts, void *y,
-                      const ShardArgs *shard, cudaEvent_t *ev, cudaStream_t stream)
+                      const ShardArgs *shard, cudaEvent_t *ev, cudaStream_t stream,
+                      const GatherArgs *gather = nullptr)
 {
     int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
     const bool gate = !shard || (shard->phases & 1);
@@ -252,6 +253,12 @@ moe_status route_step(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws
     if (!cuda_ok(record_stage(ev, 0, stream)))
         return MOE_ERR_CUDA;
     cudaError_t err = cudaSuccess;
+    // E4M3 token rows for the gather: every token row quantized once
+    if (gather)
+        err = launch_quantize_e4m3_act(c.T, c.d_model, x, false, gather->src, gather->scale,
+                                       nullptr, stream);
+    if (!cuda_ok(err))
+        return MOE_ERR_CUDA;
     if (gate && !fused) {
         if (c.dtype == MOE_DTYPE_BF16)
             err = launch_router_tc(c, x, W_r, lsplit > 1 ? lpart : router_logits, lsplit, status,
@@ -263,7 +270,7 @@ moe_status route_step(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws
         return MOE_ERR_CUDA;
     if (!cuda_ok(launch_dispatch(c, L, ws, x, W_r, fused, router_logits, lpart, lsplit,
                                  router_bias, topk_idx, topk_w, dropped_mask, expert_counts,
-                                 kept_counts, y, stream, shard)) ||
+                                 kept_counts, y, stream, shard, gather)) ||
         !cuda_ok(record_stage(ev, 2, stream)))
         return MOE_ERR_CUDA;
     return MOE_OK;
@@ -326,8 +333,20 @@ moe_status forward_body(const moe_config &c, const WorkspaceLayout &L, uint8_t *
         return MOE_OK;
     }
     cudaEvent_t *ev = g_stage_events.load();
+    // E4M3 activations: every token row is quantized once, and the dispatch
+    // gathers its codes (and scale) into expert order instead of the bf16 row
+    GatherArgs g{};
+    if (w8 && w8->a8) {
+        const A8Layout A = a8_layout_of(c, L);
+        g.src = ws + A.sxq;
+        g.row_bytes = (size_t)c.d_model;
+        g.scale = reinterpret_cast<float *>(ws + A.sxs);
+        g.dst = ws + A.xq;
+        g.scale_dst = reinterpret_cast<float *>(ws + A.xs);
+    }
     moe_status st = route_step(c, L, ws, x, W_r, router_bias, router_logits, topk_idx, topk_w,
-                               dropped_mask, expert_counts, kept_counts, y, nullptr, ev, stream);
+                               dropped_mask, expert_counts, kept_counts, y, nullptr, ev, stream,
+                               w8 && w8->a8 ? &g : nullptr);
     if (st != MOE_OK)
         return st;
     AuxArgs aux;

@@ -104,6 +104,13 @@ struct DispatchParams {
     unsigned barrier_extra;
     unsigned long long barrier_limit_ns;
     long long R_max;            // rows of x_perm (bound of every row index)
+    // gather source other than x (E4M3 token rows): rows of g_row_bytes
+    // copied into x_perm (then rows of g_row_bytes too), and each row's
+    // scale gscale[t] into gscale_perm[row]; gx null: x rows are copied
+    const uint8_t *gx;
+    size_t g_row_bytes;
+    const float *gscale;
+    float *gscale_perm;
 };
 
 // ------------------------------------------------------------ block helpers
@@ -603,15 +610,17 @@ __device__ __forceinline__ long long block_sum_ll(long long v)
     return t;
 }
 
-// Copies token t's x row (src: shared or global memory) into its kept rows
-// of x_perm; this warp handles the 16-byte vectors part*32+lane, stepping by
-// nparts*32 (four loads in flight before their stores).
+// Copies token t's row (src: shared or global memory, row_bytes long) into
+// its kept rows of x_perm; this warp handles the 16-byte vectors
+// part*32+lane, stepping by nparts*32 (four loads in flight before their
+// stores).
 __device__ __forceinline__ void copy_row(const DispatchParams &p, const uint8_t *src,
-                                         const long long (&rows)[kMaxTopK], int part, int nparts)
+                                         size_t row_bytes, const long long (&rows)[kMaxTopK],
+                                         int part, int nparts)
 {
     const int lane = threadIdx.x & 31, k = p.k;
-    const size_t nv = p.row_bytes / 16;
-    if (nv * 16 == p.row_bytes) {
+    const size_t nv = row_bytes / 16;
+    if (nv * 16 == row_bytes) {
         const size_t step = (size_t)nparts * 32;
         size_t v = (size_t)part * 32 + lane;
         for (; v + 3 * step < nv; v += 4 * step) {
@@ -622,7 +631,7 @@ __device__ __forceinline__ void copy_row(const DispatchParams &p, const uint8_t 
 #pragma unroll
             for (int j = 0; j < kMaxTopK; ++j)
                 if (j < k && rows[j] >= 0) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.x_perm + (size_t)rows[j] * p.row_bytes);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.x_perm + (size_t)rows[j] * row_bytes);
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
                         dst[v + u * step] = q[u];
@@ -633,16 +642,16 @@ __device__ __forceinline__ void copy_row(const DispatchParams &p, const uint8_t 
 #pragma unroll
             for (int j = 0; j < kMaxTopK; ++j)
                 if (j < k && rows[j] >= 0)
-                    reinterpret_cast<uint4 *>(p.x_perm + (size_t)rows[j] * p.row_bytes)[v] = q;
+                    reinterpret_cast<uint4 *>(p.x_perm + (size_t)rows[j] * row_bytes)[v] = q;
         }
     } else {  // fp32 rows whose size is not a multiple of 16 bytes
-        const size_t nw = p.row_bytes / 4;
+        const size_t nw = row_bytes / 4;
         for (size_t v = (size_t)part * 32 + lane; v < nw; v += (size_t)nparts * 32) {
             const uint32_t q = reinterpret_cast<const uint32_t *>(src)[v];
 #pragma unroll
             for (int j = 0; j < kMaxTopK; ++j)
                 if (j < k && rows[j] >= 0)
-                    reinterpret_cast<uint32_t *>(p.x_perm + (size_t)rows[j] * p.row_bytes)[v] = q;
+                    reinterpret_cast<uint32_t *>(p.x_perm + (size_t)rows[j] * row_bytes)[v] = q;
         }
     }
 }
@@ -987,6 +996,8 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
                     p.row_tok[row] = t;
                     p.row_w[row] = held ? wbuf[u] : __ldcg(p.topk_w + tk);
                 }
+                if (p.gscale_perm && row >= 0)
+                    p.gscale_perm[row] = __ldg(p.gscale + t);
             }
         }
         long long rows[kMaxTopK];
@@ -996,10 +1007,11 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
             rows[j] = __shfl_sync(0xffffffffu, row, j);
             any |= (j < k && rows[j] >= 0);
         }
-        const uint8_t *src = p.x_staged && gate
+        const uint8_t *src = p.gx ? p.gx + (size_t)t * p.g_row_bytes
+                             : p.x_staged && gate
                                  ? xs + (size_t)(t - t_beg) * xstride
                                  : static_cast<const uint8_t *>(p.x) + (size_t)t * p.row_bytes;
-        copy_row(p, src, rows, part, nparts);
+        copy_row(p, src, p.gx ? p.g_row_bytes : p.row_bytes, rows, part, nparts);
         if (p.y_zero && !any) {
             uint4 *dst = reinterpret_cast<uint4 *>(p.y_zero + (size_t)t * p.row_bytes);
             for (size_t v = (size_t)part * 32 + lane; v < p.row_bytes / 16; v += (size_t)nparts * 32)
@@ -1172,9 +1184,9 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
                             const float *lpart, int lsplit, const float *bias,
                             int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
                             int32_t *expert_counts, int32_t *kept_counts, void *y,
-                            cudaStream_t stream, const ShardArgs *shard)
+                            cudaStream_t stream, const ShardArgs *shard, const GatherArgs *gather)
 {
-    DispatchParams p;
+    DispatchParams p{};
     p.phases = shard ? shard->phases : 3;
     p.all_counts = shard ? shard->all_counts : nullptr;
     p.all_psum = shard ? shard->all_psum : nullptr;
@@ -1210,8 +1222,14 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
     p.seg_off = reinterpret_cast<int32_t *>(ws + L.seg_off);
     p.mtile = reinterpret_cast<int32_t *>(ws + L.mtile);
     p.row_of = reinterpret_cast<int32_t *>(ws + L.row_of);
-    p.x_perm = ws + L.x_perm;
+    p.x_perm = gather ? gather->dst : ws + L.x_perm;
     p.R_max = L.R_max;
+    if (gather) {
+        p.gx = gather->src;
+        p.g_row_bytes = gather->row_bytes;
+        p.gscale = gather->scale;
+        p.gscale_perm = gather->scale_dst;
+    }
     const bool dy = direct_y(c) && c.dtype == MOE_DTYPE_BF16;
     p.row_tok = dy ? reinterpret_cast<int32_t *>(ws + L.row_tok) : nullptr;
     p.row_w = dy ? reinterpret_cast<float *>(ws + L.row_w) : nullptr;

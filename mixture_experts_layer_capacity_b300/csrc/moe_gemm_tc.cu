@@ -1704,13 +1704,9 @@ cudaError_t launch_experts_w8a8(const moe_config &c, const WorkspaceLayout &L, u
     float *hf = reinterpret_cast<float *>(ws + A.hf), *shf = reinterpret_cast<float *>(ws + A.shf);
     cudaError_t err;
 
-    // the kept token rows (their count is the dispatch kernel's seg_off[E])
-    // and, for the shared expert, every token row to E4M3
-    err = launch_quantize_e4m3_act(R, D, ws + L.x_perm, false, xq, xs, seg + E, stream);
-    if (err == cudaSuccess && shared)
-        err = launch_quantize_e4m3_act(T, D, x, false, sxq, sxs, nullptr, stream);
-    if (err != cudaSuccess)
-        return err;
+    // the token rows' codes and scales were written before the dispatch
+    // (sxq, sxs: one per token) and gathered by it into expert order (xq, xs)
+    (void)x;
     // GEMM1: hf = silu(xq Wg^T) * (xq Wu^T), fp32 (+ shf from the shared expert)
     {
         CUtensorMap mA, mG, mU;

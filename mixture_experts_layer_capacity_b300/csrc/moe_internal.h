@@ -121,12 +121,24 @@ bool direct_y(const moe_config &c);
 // Routing, capacity and dispatch in one cooperative kernel (see moe_dispatch.cu).
 // `lpart`/`lsplit`: the split router's partial scores (null/1: scores are
 // already in `logits`, or the router is fused).
+// What the dispatch copies into expert order when it is not the x rows:
+// E4M3 token rows src [T][row_bytes] into dst [R_max][row_bytes], and each
+// token's scale scale[t] into scale_dst[row].  src and scale are written
+// first, in the same forward pass, by the row quantizer (route_step).
+struct GatherArgs {
+    uint8_t *src;
+    size_t row_bytes;
+    float *scale;
+    uint8_t *dst;
+    float *scale_dst;
+};
 cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                             const void *x, const void *W_r, bool fused, float *logits,
                             const float *lpart, int lsplit, const float *bias,
                             int32_t *topk_idx, float *topk_w, uint8_t *dropped_mask,
                             int32_t *expert_counts, int32_t *kept_counts, void *y,
-                            cudaStream_t stream, const ShardArgs *shard = nullptr);
+                            cudaStream_t stream, const ShardArgs *shard = nullptr,
+                            const GatherArgs *gather = nullptr);
 // Split batch, rank without tokens: counts and sums over all ranks into
 // gcount/gpsum, then the balance loss of `aux` (which points at them).
 cudaError_t launch_shard_stats(const int32_t *all_counts, const double *all_psum, int n_ranks,
