@@ -183,6 +183,11 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
                                      operand and those few token rows (rounded up
                                      to 32) the other, so they are not padded to
                                      256 rows */
+#define MOE_PLAN_W8A8_SWAP 64     /* moe_forward_w8a8 only: at most 64 rows per
+                                     expert on average (T * k <= 64 * E), so its
+                                     expert GEMMs take the weights as the 128-row
+                                     MMA operand and up to 32 token rows of an
+                                     expert as the other; else 128-row token tiles */
 MOE_API moe_status moe_launch_plan(const moe_config *cfg, int32_t *flags);
 
 /* Workspace bytes moe_latent_forward needs for `cfg` (whose d_model is the

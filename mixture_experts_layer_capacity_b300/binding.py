@@ -136,7 +136,7 @@ def config_of(w) -> MoeConfig:
 
 
 PLAN_FLAGS = {"router_fused": 1, "direct_y": 2, "pair_routed": 4, "pair_shared": 8,
-              "shared_fused": 16, "pair_tails": 32}
+              "shared_fused": 16, "pair_tails": 32, "w8a8_swap": 64}
 
 
 def launch_plan(cfg: MoeConfig) -> dict:

@@ -123,6 +123,11 @@ A8Layout a8_layout_of(const moe_config &c, const WorkspaceLayout &L)
     return A;
 }
 
+bool w8a8_swap(const moe_config &c)
+{
+    return (long long)c.T * c.top_k <= 64LL * c.n_experts;
+}
+
 int shared_down_splits(const moe_config &c)
 {
     if (!plan_of(c).shared_fused)
@@ -222,7 +227,8 @@ moe_status moe_launch_plan(const moe_config *cfg, int32_t *flags)
              (pl.pair_routed ? MOE_PLAN_PAIR_ROUTED : 0) |
              (pl.pair_shared ? MOE_PLAN_PAIR_SHARED : 0) |
              (pl.shared_fused ? MOE_PLAN_SHARED_FUSED : 0) |
-             (pl.pair_tails ? MOE_PLAN_PAIR_TAILS : 0);
+             (pl.pair_tails ? MOE_PLAN_PAIR_TAILS : 0) |
+             (w8a8_swap(*cfg) ? MOE_PLAN_W8A8_SWAP : 0);
     return MOE_OK;
 }
 

@@ -1704,6 +1704,9 @@ cudaError_t launch_experts_w8a8(const moe_config &c, const WorkspaceLayout &L, u
     float *hf = reinterpret_cast<float *>(ws + A.hf), *shf = reinterpret_cast<float *>(ws + A.shf);
     cudaError_t err;
 
+    // few rows per expert: weights as the 128-row MMA operand instead
+    if (w8a8_swap(c))
+        return launch_experts_w8a8_swap(c, L, ws, w, y, aux, stream, ev);
     // the token rows' codes and scales were written before the dispatch
     // (sxq, sxs: one per token) and gathered by it into expert order (xq, xs)
     (void)x;

@@ -36,7 +36,15 @@
 //     scale, SiLU * up (GEMM1, f16 h), bf16 z or y (GEMM2); 32 consecutive
 //     features per warp and token row.
 // GEMM1 units hold the gate and up tiles of the same 128 features; GEMM2
-// units hold 256 consecutive output features.  A second, dense problem (the
+// units hold 256 consecutive output features.
+// A8 form (E4M3 token rows too, moe_forward_w8a8 at decode sizes): both
+// operands are E4M3, so the MMA (kind::f8f6f4, K = 32) reads the weight
+// tiles straight from the shared-memory ring as its A operand: no
+// converters, no TMEM staging of A.  The token rows arrive as codes (one
+// 16-row box of 128-byte rows per 16 rows and reduction step), a 6-stage
+// ring of 36 KB stages; the epilogue scales each accumulator by the weight
+// row's and the token row's scales, and GEMM1 writes h in fp32 for the row
+// quantizer.  A second, dense problem (the
 // shared expert) may precede the grouped one in the unit list, as in the
 // bf16 kernels.  Every wait is bounded; on timeout the CTA records
 // MOE_DEVICE_PIPELINE_TIMEOUT, drains its own copies and MMAs, frees TMEM and
@@ -65,20 +73,29 @@ constexpr int kW8AStages = 3;    // converted weight stages in TMEM
 constexpr int kW8Rows = 128;     // weight rows per A tile (MMA M)
 constexpr int kW8FP8Bytes = kW8Rows * kW8K;                        // 16 KB per A tile
 constexpr int kW8BHalf = kW8Tok * 128;                             // token rows x 64 elements
-constexpr int kW8StageBytes = 2 * kW8FP8Bytes + 2 * kW8BHalf;      // 40 KB
 constexpr int kW8DCols = 2 * kW8Tok;                               // accumulator buffer
 constexpr int kW8ACols = kW8K / 2;                                 // TMEM columns of an A tile
 constexpr int kW8ACol0 = 2 * kW8DCols;                             // first A column
 constexpr int kW8TmemCols = 512;
-constexpr int kW8Bars = 2 * kW8Stages + 2 * kW8AStages + 4 + 1;
 constexpr int kW8TableInts = 2 * (kMaxExperts + 1);
-constexpr int kW8SmemBytes = kW8Stages * kW8StageBytes + 512 + kW8TableInts * 4 + 1024;
 constexpr uint64_t kW8WaitNs = 2000000000ull;
 constexpr uint64_t kW8DrainNs = 200000000ull;
 static_assert(kW8ACol0 + kW8AStages * 2 * kW8ACols <= kW8TmemCols, "TMEM columns");
-static_assert(kW8StageBytes % 1024 == 0 && kW8BHalf % 1024 == 0, "1024-byte swizzle atoms");
-static_assert(kW8Bars * 8 + 8 <= 512, "barrier area");
-static_assert(kW8SmemBytes <= 227 * 1024, "shared memory");
+static_assert(kW8BHalf % 1024 == 0, "1024-byte swizzle atoms");
+
+// The shared-memory ring of each form: bf16 token rows (two 64-element
+// halves per stage) or E4M3 token rows (one 128-byte half, A8).
+template <bool A8>
+struct W8Ring {
+    static constexpr int STAGES = A8 ? 6 : kW8Stages;
+    static constexpr int B_BYTES = A8 ? kW8BHalf : 2 * kW8BHalf;
+    static constexpr int STAGE_BYTES = 2 * kW8FP8Bytes + B_BYTES;
+    static constexpr int BARS = 2 * STAGES + 2 * kW8AStages + 4 + 1;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 512 + kW8TableInts * 4 + 1024;
+    static_assert(STAGE_BYTES % 1024 == 0, "1024-byte swizzle atoms");
+    static_assert(BARS * 8 + 8 <= 512, "barrier area");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
 
 struct W8Problem {
     const int32_t *seg_off;  // [nseg+1] first row of each segment; null = dense
@@ -89,6 +106,7 @@ struct W8Problem {
     int ftiles;              // feature tiles (128 features for SwiGLU, 256 otherwise)
     int ksplit;              // reduction pieces, fp32 partial outputs (1 = none)
     const float *s0, *s1;    // per weight row scales: gate/up, or down/unused
+    const float *tscale;     // A8: per token row scales (rows of the B operand)
     void *out;
     long long ld_out;        // output row stride, elements
     long long part_stride;   // ksplit > 1: elements between the pieces' outputs
@@ -219,33 +237,34 @@ __device__ __forceinline__ int balanced_w8(int n, int w)
     return (n + rounds - 1) / rounds;
 }
 
-template <int EPI>
+template <int EPI, bool A8>
 __global__ void __launch_bounds__(kW8Threads, 1)
     w8_gemm_kernel(const __grid_constant__ CUtensorMap w00, const __grid_constant__ CUtensorMap w01,
                    const __grid_constant__ CUtensorMap b0, const __grid_constant__ CUtensorMap w10,
                    const __grid_constant__ CUtensorMap w11, const __grid_constant__ CUtensorMap b1,
                    const W8Params p)
 {
+    using RG = W8Ring<A8>;
     extern __shared__ uint8_t smem_raw[];
     // the layout below must fit the shared memory this launch received
-    if (dynamic_smem_bytes() < (uint32_t)kW8SmemBytes) {
+    if (dynamic_smem_bytes() < (uint32_t)RG::SMEM_BYTES) {
         if (threadIdx.x == 0)
             set_status(p.status, MOE_DEVICE_LAUNCH_MISMATCH);
         return;
     }
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kW8Stages * kW8StageBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + RG::STAGES * RG::STAGE_BYTES);
     uint64_t *full = bars;
-    uint64_t *empty = full + kW8Stages;
-    uint64_t *afull = empty + kW8Stages;
+    uint64_t *empty = full + RG::STAGES;
+    uint64_t *afull = empty + RG::STAGES;
     uint64_t *aempty = afull + kW8AStages;
     uint64_t *tfull = aempty + kW8AStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *mma_done = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int *tables = reinterpret_cast<int *>(smem + kW8Stages * kW8StageBytes + 512);
+    int *tables = reinterpret_cast<int *>(smem + RG::STAGES * RG::STAGE_BYTES + 512);
     int *s_seg = tables;                    // [nseg+1] segment offsets of pr[1]
     int *s_tt = tables + kMaxExperts + 1;   // [nseg+1] prefix of 64-row token tiles
 
@@ -253,7 +272,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kW8Stages; ++s) {
+        for (int s = 0; s < RG::STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -337,20 +356,22 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t *st = smem + s * kW8StageBytes;
-                    mbar_arrive_expect_tx(&full[s], 2 * kW8FP8Bytes + 2 * nb * 16 * 128);
+                    uint8_t *st = smem + s * RG::STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[s],
+                                          2 * kW8FP8Bytes + (A8 ? 1 : 2) * nb * 16 * 128);
                     tma_load_2d(st, mw0, &full[s], kb * kW8K, wrow);
                     if (EPI == W8_SWIGLU)
                         tma_load_2d(st + kW8FP8Bytes, mw1, &full[s], kb * kW8K, wrow);
                     else
                         tma_load_2d(st + kW8FP8Bytes, mw0, &full[s], kb * kW8K, wrow + kW8Rows);
-                    // reduction elements past K (a last half block) read as zero
-                    for (int h = 0; h < 2; ++h)
+                    // reduction elements past K (a last half block) read as zero;
+                    // E4M3 token rows: one 128-byte box row per token row
+                    for (int h = 0; h < (A8 ? 1 : 2); ++h)
                         for (int j = 0; j < nb; ++j)
                             tma_load_2d(st + 2 * kW8FP8Bytes + h * kW8BHalf + j * 16 * 128, mb,
                                         &full[s], kb * kW8K + h * 64, w.row0 + 16 * j);
                     ++fills;
-                    if (++s == kW8Stages) {
+                    if (++s == RG::STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -359,9 +380,9 @@ __global__ void __launch_bounds__(kW8Threads, 1)
             if (!ok) {
                 *abort_flag = 1;
                 set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
-                const long long first = fills > kW8Stages ? fills - kW8Stages : 0;
+                const long long first = fills > RG::STAGES ? fills - RG::STAGES : 0;
                 for (long long f = first; f < fills; ++f)
-                    mbar_wait(&full[f % kW8Stages], (uint32_t)((f / kW8Stages) & 1), nullptr,
+                    mbar_wait(&full[f % RG::STAGES], (uint32_t)((f / RG::STAGES) & 1), nullptr,
                               kW8DrainNs);
             }
         }
@@ -374,7 +395,8 @@ __global__ void __launch_bounds__(kW8Threads, 1)
             for (int u = blockIdx.x; u < nunits && ok; u += G) {
                 const W8Unit w = w8_unit(p, s_seg, s_tt, u, n0);
                 const int nb = (w.n + 15) / 16;
-                const uint32_t idesc = idesc_f16_f32(kW8Rows, 16 * nb);
+                const uint32_t idesc =
+                    A8 ? idesc_e4m3_f32(kW8Rows, 16 * nb) : idesc_f16_f32(kW8Rows, 16 * nb);
                 if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, kW8WaitNs)) {
                     ok = false;
                     break;
@@ -382,32 +404,50 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                 tc_fence_after_sync();
                 const uint32_t d0 = tmem_base + b * kW8DCols;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(&afull[sa], aph, abort_flag, kW8WaitNs) ||
+                    if ((!A8 && !mbar_wait(&afull[sa], aph, abort_flag, kW8WaitNs)) ||
                         !mbar_wait(&full[s], ph, abort_flag, kW8WaitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sb = smem_u32(smem + s * kW8StageBytes + 2 * kW8FP8Bytes);
-                    const uint64_t bdesc[2] = {sdesc_kmajor_sw128(sb),
-                                               sdesc_kmajor_sw128(sb + kW8BHalf)};
+                    const uint32_t st = smem_u32(smem + s * RG::STAGE_BYTES);
+                    const uint32_t sb = st + 2 * kW8FP8Bytes;
+                    if constexpr (A8) {
+                        // weights (A) and token rows (B) from the ring, both
+                        // 128-byte rows of 128 codes: four K = 32 steps each
+                        const uint64_t bdesc = sdesc_kmajor_sw128(sb);
 #pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        const uint32_t a = tmem_base + kW8ACol0 + (uint32_t)(sa * 2 + t) * kW8ACols;
+                        for (int t = 0; t < 2; ++t) {
+                            const uint64_t adesc = sdesc_kmajor_sw128(st + t * kW8FP8Bytes);
 #pragma unroll
-                        for (int kk = 0; kk < kW8K / 16; ++kk)
-                            umma_bf16_ta(d0 + t * kW8Tok, a + kk * 8, bdesc[kk >> 2] + 2u * (kk & 3),
-                                         idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < 4; ++kk)
+                                umma_e4m3(d0 + t * kW8Tok, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                          (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        }
+                        umma_commit(&empty[s]);
+                    } else {
+                        const uint64_t bdesc[2] = {sdesc_kmajor_sw128(sb),
+                                                   sdesc_kmajor_sw128(sb + kW8BHalf)};
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            const uint32_t a =
+                                tmem_base + kW8ACol0 + (uint32_t)(sa * 2 + t) * kW8ACols;
+#pragma unroll
+                            for (int kk = 0; kk < kW8K / 16; ++kk)
+                                umma_bf16_ta(d0 + t * kW8Tok, a + kk * 8,
+                                             bdesc[kk >> 2] + 2u * (kk & 3), idesc,
+                                             (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        }
+                        umma_commit(&empty[s]);
+                        umma_commit(&aempty[sa]);
+                        if (++sa == kW8AStages) {
+                            sa = 0;
+                            aph ^= 1u;
+                        }
                     }
-                    umma_commit(&empty[s]);
-                    umma_commit(&aempty[sa]);
-                    if (++s == kW8Stages) {
+                    if (++s == RG::STAGES) {
                         s = 0;
                         ph ^= 1u;
-                    }
-                    if (++sa == kW8AStages) {
-                        sa = 0;
-                        aph ^= 1u;
                     }
                 }
                 if (!ok)
@@ -426,6 +466,8 @@ __global__ void __launch_bounds__(kW8Threads, 1)
         }
     } else if (warp >= 6) {
         // ---------------------------------------------------- converters
+        // (none in the A8 form: the MMA reads the E4M3 weights directly)
+        if constexpr (!A8) {
         // group grp converts the reduction steps i with i % 2 == grp (i counts
         // this CTA's steps over all its units)
         const int grp = (warp - 6) >> 2;
@@ -439,8 +481,8 @@ __global__ void __launch_bounds__(kW8Threads, 1)
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++i) {
                 if ((int)(i & 1) != grp)
                     continue;
-                const int s = (int)(i % kW8Stages), sa = (int)(i % kW8AStages);
-                const uint32_t ph = (uint32_t)((i / kW8Stages) & 1);
+                const int s = (int)(i % RG::STAGES), sa = (int)(i % kW8AStages);
+                const uint32_t ph = (uint32_t)((i / RG::STAGES) & 1);
                 const uint32_t aph = (uint32_t)((i / kW8AStages) & 1);
                 if (!mbar_wait(&full[s], ph, abort_flag, kW8WaitNs) ||
                     !mbar_wait(&aempty[sa], aph ^ 1u, abort_flag, kW8WaitNs)) {
@@ -448,7 +490,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint8_t *st = smem + s * kW8StageBytes;
+                const uint8_t *st = smem + s * RG::STAGE_BYTES;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     // row r's 16-byte chunk c sits at chunk c ^ (r & 7)
@@ -483,7 +525,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                     const int nb = (w.n + 15) / 16;
                     const int tc = (warp - 6 - 4 * grp) * 32 + lane;
                     for (int h = 0; h < 2; ++h) {
-                        uint4 *bt = reinterpret_cast<uint4 *>(smem + s * kW8StageBytes +
+                        uint4 *bt = reinterpret_cast<uint4 *>(smem + s * RG::STAGE_BYTES +
                                                               2 * kW8FP8Bytes + h * kW8BHalf);
                         for (int ci = tc; ci < nb * 16 * 8; ci += 128) {
                             uint4 x = bt[ci];
@@ -504,6 +546,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
         if (!ok) {
             *abort_flag = 1;
             set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
+        }
         }
     } else {
         // ---------------------------------------------------- epilogue
@@ -529,7 +572,6 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                 const bool fok = f < pr.feat;
                 const float sg = fok ? pr.s0[(long long)w.seg * pr.w_seg_rows + f] : 0.f;
                 const float su = fok ? pr.s1[(long long)w.seg * pr.w_seg_rows + f] : 0.f;
-                __half *out = static_cast<__half *>(pr.out);
                 for (int j0 = 0; j0 < ncol; j0 += 16) {
                     uint32_t gv[16], uv[16];
                     tmem_ld16(tb + j0, gv);
@@ -540,10 +582,22 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                         for (int jj = 0; jj < 16; ++jj) {
                             const int j = j0 + jj;
                             if (j < w.n) {
-                                const float g = __uint_as_float(gv[jj]) * sg;
-                                const float uu = __uint_as_float(uv[jj]) * su;
-                                const float hv = fminf(fmaxf(silu_f32(g) * uu, -65504.f), 65504.f);
-                                out[(long long)(w.row0 + j) * pr.ld_out + f] = __float2half_rn(hv);
+                                const long long row = w.row0 + j;
+                                if constexpr (A8) {
+                                    // fp32 h for the row quantizer
+                                    const float ts = __ldg(pr.tscale + row);
+                                    const float g = __uint_as_float(gv[jj]) * (sg * ts);
+                                    const float uu = __uint_as_float(uv[jj]) * (su * ts);
+                                    static_cast<float *>(pr.out)[row * pr.ld_out + f] =
+                                        silu_f32(g) * uu;
+                                } else {
+                                    const float g = __uint_as_float(gv[jj]) * sg;
+                                    const float uu = __uint_as_float(uv[jj]) * su;
+                                    const float hv =
+                                        fminf(fmaxf(silu_f32(g) * uu, -65504.f), 65504.f);
+                                    static_cast<__half *>(pr.out)[row * pr.ld_out + f] =
+                                        __float2half_rn(hv);
+                                }
                             }
                         }
                     }
@@ -565,8 +619,9 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                             const int j = j0 + jj;
                             if (j >= w.n)
                                 continue;
-                            const float a = __uint_as_float(v[jj]) * sc;
                             const long long row = w.row0 + j;
+                            const float a = __uint_as_float(v[jj]) *
+                                            (A8 ? sc * __ldg(pr.tscale + row) : sc);
                             if (pr.ksplit > 1) {
                                 static_cast<float *>(pr.out)[w.ks * pr.part_stride +
                                                              row * pr.ld_out + f] = a;
@@ -600,11 +655,12 @@ __global__ void __launch_bounds__(kW8Threads, 1)
     }
 }
 
-template <int EPI>
+template <int EPI, bool A8 = false>
 cudaError_t launch_w8(const CUtensorMap (&m)[6], const W8Params &p, long long max_units,
                       cudaStream_t stream)
 {
-    auto kern = w8_gemm_kernel<EPI>;
+    using RG = W8Ring<A8>;
+    auto kern = w8_gemm_kernel<EPI, A8>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
@@ -612,7 +668,7 @@ cudaError_t launch_w8(const CUtensorMap (&m)[6], const W8Params &p, long long ma
     static DeviceOnce configured;
     if (configured.pending(dev)) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kW8SmemBytes);
+                                   RG::SMEM_BYTES);
         if (err == cudaSuccess)
             err = prefer_max_shared_carveout(kern);
         if (err != cudaSuccess)
@@ -622,7 +678,7 @@ cudaError_t launch_w8(const CUtensorMap (&m)[6], const W8Params &p, long long ma
     const long long grid = std::min<long long>(max_units, sm_count());
     if (grid < 1)
         return cudaSuccess;
-    return launch_pdl(kern, dim3((unsigned)grid), dim3(kW8Threads), (size_t)kW8SmemBytes, stream,
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kW8Threads), (size_t)RG::SMEM_BYTES, stream,
                       m[0], m[1], m[2], m[3], m[4], m[5], p);
 }
 
@@ -649,38 +705,62 @@ __device__ __forceinline__ void load8(const float *row, long long v, float (&f)[
 
 // q[r][c] = e4m3(W[r][c] / s_r), s_r = max_c |W[r][c]| / 448 (1 for an
 // all-zero row); fp32 division, round to nearest even, saturating to +-448.
-// One warp per row, 8 columns per lane and step.  TIN: bf16 (weights, token
-// rows) or fp32 (hidden rows).  rows_dev non-null: only the first
+// GROUP warps per row (1, 2, 4 or 8 of the block's 8; long rows take more
+// warps, so that a few long rows still spread over many SMs), 8 columns per
+// lane and step; the row maximum is combined over the group in shared
+// memory (a maximum: the same value in any order).  TIN: bf16 (weights,
+// token rows) or fp32 (hidden rows).  rows_dev non-null: only the first
 // min(rows, *rows_dev) rows (a row count the previous kernel wrote).
-template <typename TIN>
+template <typename TIN, int GROUP>
 __global__ void __launch_bounds__(256)
     quantize_e4m3_kernel(long long rows, long long cols, const TIN *__restrict__ W,
                          uint8_t *__restrict__ q, float *__restrict__ scale,
                          const int32_t *__restrict__ rows_dev)
 {
+    constexpr int RPB = 8 / GROUP;   // rows per block and pass
+    __shared__ float s_max[8];
     griddep_wait();   // the rows (and their count) come from the previous kernel
     if (rows_dev)
         rows = min(rows, (long long)*(volatile const int32_t *)rows_dev);
-    const int lane = threadIdx.x & 31;
-    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-    for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-         r += warps) {
-        const TIN *src = W + r * cols;
-        const long long nv = cols / 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slot = warp / GROUP, gw = warp - slot * GROUP;
+    const long long nv = cols / 8;
+    const long long per_pass = (long long)gridDim.x * RPB;
+    // the same number of passes for every thread of the block (barriers)
+    const long long passes = (rows + per_pass - 1) / per_pass;
+    for (long long it = 0; it < passes; ++it) {
+        const long long r = it * per_pass + (long long)blockIdx.x * RPB + slot;
+        const bool valid = r < rows;
+        const TIN *src = W + (valid ? r : 0) * cols;
         float amax = 0.f;
-        for (long long v = lane; v < nv; v += 32) {
-            float f[8];
-            load8(src, v, f);
+        if (valid) {
+#pragma unroll 4
+            for (long long v = gw * 32 + lane; v < nv; v += GROUP * 32) {
+                float f[8];
+                load8(src, v, f);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+                for (int i = 0; i < 4; ++i)
+                    amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+            }
         }
         amax = warp_max(amax);
+        if constexpr (GROUP > 1) {
+            if (lane == 0)
+                s_max[warp] = amax;
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < GROUP; ++i)
+                amax = fmaxf(amax, s_max[slot * GROUP + i]);
+            __syncthreads();   // s_max is rewritten in the next pass
+        }
+        if (!valid)
+            continue;
         const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-        if (lane == 0)
+        if (gw == 0 && lane == 0)
             scale[r] = s;
         uint2 *dst = reinterpret_cast<uint2 *>(q + r * cols);
-        for (long long v = lane; v < nv; v += 32) {
+#pragma unroll 4
+        for (long long v = gw * 32 + lane; v < nv; v += GROUP * 32) {
             float f[8];
             load8(src, v, f);
             uint32_t word[2] = {0u, 0u};
@@ -695,6 +775,33 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Warps per row for rows of `cols` values: at least two 8-value steps per
+// lane, at most the block's 8 warps.
+int quantize_group(long long cols)
+{
+    const long long steps = cols / (8 * 32);   // per warp
+    return steps >= 16 ? 8 : steps >= 8 ? 4 : steps >= 4 ? 2 : 1;
+}
+
+template <typename TIN>
+cudaError_t launch_quantize_t(long long rows, long long cols, const TIN *X, uint8_t *q,
+                              float *scale, const int32_t *rows_dev, bool pdl,
+                              cudaStream_t stream)
+{
+    const int group = quantize_group(cols);
+    const long long rpb = 8 / group;
+    const unsigned blocks = (unsigned)std::min<long long>((rows + rpb - 1) / rpb, 16LL * sm_count());
+    auto kern = group == 8   ? quantize_e4m3_kernel<TIN, 8>
+                : group == 4 ? quantize_e4m3_kernel<TIN, 4>
+                : group == 2 ? quantize_e4m3_kernel<TIN, 2>
+                             : quantize_e4m3_kernel<TIN, 1>;
+    if (pdl)
+        return launch_pdl(kern, dim3(blocks), dim3(256), 0, stream, rows, cols, X, q, scale,
+                          rows_dev);
+    kern<<<blocks, 256, 0, stream>>>(rows, cols, X, q, scale, rows_dev);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_e4m3(long long rows, long long cols, const void *W, uint8_t *q,
@@ -702,10 +809,8 @@ cudaError_t launch_quantize_e4m3(long long rows, long long cols, const void *W, 
 {
     if (rows <= 0)
         return cudaSuccess;
-    const long long blocks = std::min<long long>((rows + 7) / 8, 16LL * sm_count());
-    quantize_e4m3_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(
-        rows, cols, static_cast<const __nv_bfloat16 *>(W), q, scale, nullptr);
-    return cudaGetLastError();
+    return launch_quantize_t(rows, cols, static_cast<const __nv_bfloat16 *>(W), q, scale,
+                             nullptr, false, stream);
 }
 
 cudaError_t launch_quantize_e4m3_act(long long rows, long long cols, const void *X, bool fp32,
@@ -714,12 +819,11 @@ cudaError_t launch_quantize_e4m3_act(long long rows, long long cols, const void 
 {
     if (rows <= 0)
         return cudaSuccess;
-    const unsigned blocks = (unsigned)std::min<long long>((rows + 7) / 8, 16LL * sm_count());
     if (fp32)
-        return launch_pdl(quantize_e4m3_kernel<float>, dim3(blocks), dim3(256), 0, stream, rows,
-                          cols, static_cast<const float *>(X), q, scale, rows_dev);
-    return launch_pdl(quantize_e4m3_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, stream,
-                      rows, cols, static_cast<const __nv_bfloat16 *>(X), q, scale, rows_dev);
+        return launch_quantize_t(rows, cols, static_cast<const float *>(X), q, scale, rows_dev,
+                                 true, stream);
+    return launch_quantize_t(rows, cols, static_cast<const __nv_bfloat16 *>(X), q, scale,
+                             rows_dev, true, stream);
 }
 
 cudaError_t launch_experts_w8(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
@@ -838,6 +942,146 @@ cudaError_t launch_experts_w8(const moe_config &c, const WorkspaceLayout &L, uin
             err = launch_w8<W8_BF16_Y>(m, p, units, stream);
         } else {
             err = launch_w8<W8_BF16>(m, p, units, stream);
+        }
+        if (err == cudaSuccess)
+            err = record_stage(ev, 4, stream);
+        if (err == cudaSuccess)
+            err = record_stage(ev, 5, stream);
+        if (err == cudaSuccess)
+            err = record_stage(ev, 6, stream);
+    }
+    return err;
+}
+
+cudaError_t launch_experts_w8a8_swap(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                                     const ExpertW8 &w, void *y, const AuxArgs &aux,
+                                     cudaStream_t stream, cudaEvent_t *ev)
+{
+    const int D = c.d_model, F = c.d_expert, S = c.d_shared, E = c.n_experts, T = c.T;
+    const A8Layout A = a8_layout_of(c, L);
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    const int32_t *seg = reinterpret_cast<const int32_t *>(ws + L.seg_off);
+    uint8_t *xq = ws + A.xq, *hq = ws + A.hq, *sxq = ws + A.sxq, *shq = ws + A.shq;
+    const float *xs = reinterpret_cast<const float *>(ws + A.xs);
+    const float *sxs = reinterpret_cast<const float *>(ws + A.sxs);
+    float *hf = reinterpret_cast<float *>(ws + A.hf), *shf = reinterpret_cast<float *>(ws + A.shf);
+    float *hsc = reinterpret_cast<float *>(ws + A.hsc), *shs = reinterpret_cast<float *>(ws + A.shs);
+    const long long R = L.R_max;
+    const long long tt_bound = R / kW8Tok + E;            // >= sum_e ceil(kept_e / 32)
+    const long long tt_s = (T + kW8Tok - 1) / kW8Tok;
+    const LaunchPlan plan = plan_of(c);
+    cudaError_t err;
+
+    // GEMM1: hf = silu(xq Wg^T) * (xq Wu^T) in fp32; shf likewise from the
+    // token rows' codes; then both quantized row-wise
+    {
+        CUtensorMap m[6];
+        W8Params p{};
+        W8Problem &g = p.pr[1];
+        g.seg_off = seg;
+        g.nseg = E;
+        g.K = D;
+        g.feat = F;
+        g.w_seg_rows = F;
+        g.ftiles = (F + kW8Rows - 1) / kW8Rows;
+        g.ksplit = 1;
+        g.s0 = w.gate_s;
+        g.s1 = w.up_s;
+        g.tscale = xs;
+        g.out = hf;
+        g.ld_out = F;
+        if (!make_map_u8(&m[3], w.gate, (uint64_t)E * F, (uint64_t)D, kW8Rows) ||
+            !make_map_u8(&m[4], w.up, (uint64_t)E * F, (uint64_t)D, kW8Rows) ||
+            !make_map_u8(&m[5], xq, (uint64_t)R, (uint64_t)D, 16))
+            return cudaErrorInvalidValue;
+        W8Problem &sh = p.pr[0];
+        sh.ftiles = 1;
+        sh.ksplit = 1;
+        sh.K = D;
+        if (S > 0) {
+            sh.rows = T;
+            sh.feat = S;
+            sh.ftiles = (S + kW8Rows - 1) / kW8Rows;
+            sh.s0 = w.sgate_s;
+            sh.s1 = w.sup_s;
+            sh.tscale = sxs;
+            sh.out = shf;
+            sh.ld_out = S;
+            if (!make_map_u8(&m[0], w.sgate, (uint64_t)S, (uint64_t)D, kW8Rows) ||
+                !make_map_u8(&m[1], w.sup, (uint64_t)S, (uint64_t)D, kW8Rows) ||
+                !make_map_u8(&m[2], sxq, (uint64_t)T, (uint64_t)D, 16))
+                return cudaErrorInvalidValue;
+        } else {
+            m[0] = m[3];
+            m[1] = m[4];
+            m[2] = m[5];
+        }
+        p.status = status;
+        p.aux = aux;
+        const long long units = tt_bound * g.ftiles + (S > 0 ? tt_s * sh.ftiles : 0);
+        err = launch_w8<W8_SWIGLU, true>(m, p, units, stream);
+        if (err == cudaSuccess)
+            err = launch_quantize_e4m3_act(R, F, hf, true, hq, hsc, seg + E, stream);
+        if (err == cudaSuccess && S > 0)
+            err = launch_quantize_e4m3_act(T, S, shf, true, shq, shs, nullptr, stream);
+        if (err == cudaSuccess)
+            err = record_stage(ev, 3, stream);
+        if (err != cudaSuccess)
+            return err;
+    }
+    // GEMM2: z = hq Wd^T (or y directly); zs = shq Ws_down^T
+    {
+        CUtensorMap m[6];
+        W8Params p{};
+        W8Problem &g = p.pr[1];
+        g.seg_off = seg;
+        g.nseg = E;
+        g.K = F;
+        g.feat = D;
+        g.w_seg_rows = D;
+        g.ftiles = (D + 2 * kW8Rows - 1) / (2 * kW8Rows);
+        g.ksplit = 1;
+        g.s0 = w.down_s;
+        g.tscale = hsc;
+        g.out = plan.direct_y ? y : ws + L.z;
+        g.ld_out = D;
+        if (!make_map_u8(&m[3], w.down, (uint64_t)E * D, (uint64_t)F, kW8Rows) ||
+            !make_map_u8(&m[5], hq, (uint64_t)R, (uint64_t)F, 16))
+            return cudaErrorInvalidValue;
+        m[4] = m[3];
+        W8Problem &sh = p.pr[0];
+        sh.ftiles = 1;
+        sh.ksplit = 1;
+        sh.K = F;
+        if (S > 0) {
+            sh.rows = T;
+            sh.K = S;
+            sh.feat = D;
+            sh.ftiles = g.ftiles;
+            sh.ksplit = shared_down_splits(c);
+            sh.s0 = w.sdown_s;
+            sh.tscale = shs;
+            sh.out = ws + L.zs;
+            sh.ld_out = D;
+            sh.part_stride = (long long)T * D;
+            if (!make_map_u8(&m[0], w.sdown, (uint64_t)D, (uint64_t)S, kW8Rows) ||
+                !make_map_u8(&m[2], shq, (uint64_t)T, (uint64_t)S, 16))
+                return cudaErrorInvalidValue;
+            m[1] = m[0];
+        } else {
+            m[0] = m[3];
+            m[1] = m[4];
+            m[2] = m[5];
+        }
+        p.status = status;
+        p.aux.out = nullptr;
+        const long long units = tt_bound * g.ftiles + (S > 0 ? tt_s * sh.ftiles * sh.ksplit : 0);
+        if (plan.direct_y) {
+            p.row_tok = reinterpret_cast<const int32_t *>(ws + L.row_tok);
+            p.row_w = reinterpret_cast<const float *>(ws + L.row_w);
+            err = launch_w8<W8_BF16_Y, true>(m, p, units, stream);
+        } else {
+            err = launch_w8<W8_BF16, true>(m, p, units, stream);
         }
         if (err == cudaSuccess)
             err = record_stage(ev, 4, stream);

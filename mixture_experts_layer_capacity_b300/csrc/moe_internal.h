@@ -233,6 +233,15 @@ A8Layout a8_layout_of(const moe_config &c, const WorkspaceLayout &L);
 cudaError_t launch_experts_w8a8(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                                 const void *x, const ExpertW8 &w, void *y, const AuxArgs &aux,
                                 cudaStream_t stream, cudaEvent_t *ev = nullptr);
+// The same with the E4M3-weight kernel's unit layout (moe_gemm_w8.cu): the
+// weights are the MMA's 128-row operand and up to 32 token rows of a segment
+// the other, for layers with few rows per expert (w8a8_swap).
+cudaError_t launch_experts_w8a8_swap(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                                     const ExpertW8 &w, void *y, const AuxArgs &aux,
+                                     cudaStream_t stream, cudaEvent_t *ev = nullptr);
+// True when moe_forward_w8a8 runs launch_experts_w8a8_swap: at most 64 rows
+// per expert on average (T * k <= 64 * E).
+bool w8a8_swap(const moe_config &c);
 // q[r][c] = e4m3(W[r][c] / scale[r]), scale[r] = max_c |W[r][c]| / 448
 // (moe_gemm_w8.cu).
 cudaError_t launch_quantize_e4m3(long long rows, long long cols, const void *W, uint8_t *q,

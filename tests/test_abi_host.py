@@ -266,3 +266,12 @@ def test_w8a8_workspace_and_validation():
     assert _call_w8a8(narrow, 1 << 20, 1 << 30) == B.MOE_ERR_UNSUPPORTED
     # a missing shared weight when the layer has a shared expert
     assert _call_w8a8(cfg, 1 << 20, need, shared=False) == B.MOE_ERR_INVALID_ARG
+
+
+def test_w8a8_swap_plan_follows_rows_per_expert():
+    # at most 64 rows per expert on average: the weights-as-M-operand kernels
+    assert B.launch_plan(B.make_config(64, 7168, 256, 2048, 8))["w8a8_swap"]
+    assert B.launch_plan(B.make_config(2048, 7168, 256, 2048, 8))["w8a8_swap"]
+    assert not B.launch_plan(B.make_config(2049, 7168, 256, 2048, 8))["w8a8_swap"]
+    assert not B.launch_plan(B.make_config(16384, 7168, 256, 2048, 8))["w8a8_swap"]
+    assert B.launch_plan(B.make_config(64, 4096, 8, 14336, 2))["w8a8_swap"]

@@ -83,9 +83,8 @@ def _source_sha(stage, workload):
         src = "moe_dispatch.cu"
     elif stage == "combine":
         src = "moe_combine.cu"
-    elif (WORKLOADS[workload].weights == "e4m3" and WORKLOADS[workload].acts != "e4m3"
-          and stage.startswith("gemm")):
-        src = "moe_gemm_w8.cu"      # the E4M3-weight kernels; E4M3 activations use the tc GEMMs
+    elif stage.startswith("gemm"):
+        src = bench.gemm_source(WORKLOADS[workload])
     else:
         src = "moe_gemm_tc.cu"
     path = os.path.join(ROOT, "mixture_experts_layer_capacity_b300", "csrc", src)

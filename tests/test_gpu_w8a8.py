@@ -68,24 +68,39 @@ def _check_quantized_rows(w, inp, outs, max_rows=None):
     return R
 
 
-# name, T, D, E, F, k, S, mode, gamma, bias
+# name, T, D, E, F, k, S, mode, gamma, bias.  Layers with at most 64 rows per
+# expert on average run the weights-as-M-operand kernels (launch plan
+# w8a8_swap: 32-row token units), the others 128-row token tiles.
 CASES = [
-    # shared expert narrower than the routed ones; several token tiles
+    # tiles: shared expert narrower than the routed ones; several token tiles
     ("a8_multi_tile_top2", 1000, 256, 8, 384, 2, 192, 0, 0.0, "none"),
-    # F = 320 and D = 192 leave partial tiles and a half-empty last 128-wide
-    # reduction step; capacity drops
+    # tiles: F = 320 and D = 192 leave partial tiles and a half-empty last
+    # 128-wide reduction step; capacity drops
     ("a8_ragged_capacity_e16", 777, 192, 16, 320, 4, 0, 1, 0.75, "normal_var2"),
-    # decode-like: 64 experts, shared down projection cut into S / F = 8 pieces
-    ("a8_decode_e64_shared_pieces", 64, 512, 64, 128, 8, 1024, 2, 0.0, "zipf1.1"),
-    # k = 1 without a shared expert: the down projection writes y
-    ("a8_top1_direct_y", 300, 256, 8, 256, 1, 0, 1, 1.0, "normal_var2"),
-    # one token, wide d_model (256-wide output tiles, a ragged one)
-    ("a8_one_token_wide", 1, 1088, 8, 192, 2, 320, 0, 0.0, "none"),
-    # segments of ~250 rows: several 128-row tiles per expert
+    # tiles: segments of ~250 rows, several 128-row tiles per expert
     ("a8_long_segments", 500, 128, 4, 128, 2, 0, 0, 0.0, "none"),
-    # d_expert = 64 without a shared expert (one half-filled reduction step)
+    # swap: decode-like, 64 experts, shared down projection cut into
+    # S / F = 8 pieces
+    ("a8_decode_e64_shared_pieces", 64, 512, 64, 128, 8, 1024, 2, 0.0, "zipf1.1"),
+    # swap: k = 1 without a shared expert, the down projection writes y
+    ("a8_top1_direct_y", 300, 256, 8, 256, 1, 0, 1, 1.0, "normal_var2"),
+    # swap: one token, wide d_model (256-feature units, a ragged one)
+    ("a8_one_token_wide", 1, 1088, 8, 192, 2, 320, 0, 0.0, "none"),
+    # swap: d_expert = 64 without a shared expert (a half-filled reduction step)
     ("a8_narrow_expert", 200, 256, 8, 64, 2, 0, 0, 0.0, "none"),
+    # swap: ragged features and d_model with capacity drops; segments of
+    # 30-70 rows (one or two 32-row units, 16-row MMAs for the rest)
+    ("a8_swap_capacity_e16", 200, 192, 16, 320, 4, 0, 1, 0.75, "normal_var2"),
+    # swap: wide d_model, shared expert wider than the routed ones (two
+    # pieces of its down projection)
+    ("a8_swap_shared_wide", 40, 1088, 8, 256, 2, 384, 0, 0.0, "none"),
 ]
+
+
+def test_cases_cover_both_kernel_forms():
+    forms = {B.launch_plan(B.make_config(T, D, E, F, k, d_shared=S))["w8a8_swap"]
+             for _, T, D, E, F, k, S, *_ in CASES}
+    assert forms == {True, False}
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
