@@ -221,6 +221,20 @@ def gemm_source(w):
     return "moe_gemm_tc.cu"
 
 
+def shared_in_routed(w, plan):
+    """Whether the shared expert's GEMMs run inside the routed GEMM launches
+    (as their second problem) rather than in launches of their own: the bf16
+    layers by the launch plan, the E4M3-weight layers always, the E4M3-
+    activation layers except on CTA pairs."""
+    if not w.S:
+        return False
+    if w.weights != "e4m3":
+        return plan["shared_fused"]
+    if w.acts == "e4m3":
+        return plan["w8a8_swap"] or not plan["pair_routed"]
+    return True
+
+
 def profile_traffic(stage, workload):
     """DRAM bytes per launch of `stage` from a committed ncu summary, if the
     summary was taken on the current source of that stage's kernel (else
@@ -520,8 +534,7 @@ def run_ours(args, rank, world, device):
     # default step count it lasts well under a second, so the tensor figure
     # is held to the burst peak; the fraction of the sustained (power-capped)
     # peak is reported beside it.
-    # the E4M3 layers always run the shared expert inside the routed launches
-    fused = B.launch_plan(cfg)["shared_fused"] or (w.weights == "e4m3" and w.S > 0)
+    fused = shared_in_routed(w, B.launch_plan(cfg))
     work = stage_work(w, kept_total, touched, fused)
     act = stage_activation_bytes(w, kept_total, fused)
     dom = max((n for n in stages if n in work), key=lambda n: stages[n])
@@ -660,11 +673,10 @@ def run_ours(args, rank, world, device):
     # router (unless fused into dispatch), dispatch, GEMM1, GEMM2 (+ two
     # shared-expert GEMMs), combine (unless GEMM2 writes y); a latent layer
     # adds its two projections
-    # E4M3 layers run the shared expert inside the routed GEMM launches; with
-    # E4M3 activations the token rows (once per token) and the hidden rows
-    # (routed, shared) are quantized by one launch each
+    # with E4M3 activations the token rows (once per token) and the hidden
+    # rows (routed, shared) are quantized by one launch each
     plan = B.launch_plan(cfg)
-    shared_apart = w.S and not plan["shared_fused"] and w.weights != "e4m3"
+    shared_apart = w.S and not shared_in_routed(w, plan)
     launches_per_step = (2 if w.D_outer else 0) + \
         (0 if plan["router_fused"] else 1) + 3 + \
         (2 if shared_apart else 0) + (0 if plan["direct_y"] else 1) + \

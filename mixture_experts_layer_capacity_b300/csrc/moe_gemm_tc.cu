@@ -242,12 +242,29 @@ struct EpiScale {
     const float *b0, *b1;
 };
 
-// Scale of one column of an E4M3 tile: the row scale times the B row's
-// scale; `col` is the column's index in the output, `c` its index in the
-// tile (b points at the tile's first B row scale); 0 past the valid columns.
-__device__ __forceinline__ float col_scale(const float *b, float a, int col, int c, int n_valid)
+// Scales of 32 consecutive columns of an E4M3 tile: the row scale a times
+// each B row's scale.  b: the first column's B row scale; col: that
+// column's index in the output; 0 past the valid columns.  All lanes of a
+// warp read the same addresses (a broadcast); a whole in-range, 16-byte
+// aligned run is read as eight float4.
+__device__ __forceinline__ void chunk_scales(const float *b, float a, int col, int n_valid,
+                                             float (&cs)[32])
 {
-    return col < n_valid ? a * __ldg(b + c) : 0.f;
+    if (col + 32 <= n_valid && (reinterpret_cast<uintptr_t>(b) & 15u) == 0) {
+        const float4 *b4 = reinterpret_cast<const float4 *>(b);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 t = __ldg(b4 + j);
+            cs[4 * j] = a * t.x;
+            cs[4 * j + 1] = a * t.y;
+            cs[4 * j + 2] = a * t.z;
+            cs[4 * j + 3] = a * t.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            cs[i] = col + i < n_valid ? a * __ldg(b + i) : 0.f;
+    }
 }
 
 // Epilogue of one accumulator row (TMEM lane) of a tile: this thread owns
@@ -270,13 +287,17 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
             tmem_wait_ld();
             if (row_ok) {
                 const int col = n_idx * BN + c0;
-                float hv[32];
+                float hv[32], gs[32], us[32];
+                if constexpr (SCALED) {
+                    chunk_scales(sc.b0 + c0, sc.a, col, n_valid, gs);
+                    chunk_scales(sc.b1 + c0, sc.a, col, n_valid, us);
+                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     float g = __uint_as_float(gv[i]), u = __uint_as_float(uv[i]);
                     if constexpr (SCALED) {
-                        g *= col_scale(sc.b0, sc.a, col + i, c0 + i, n_valid);
-                        u *= col_scale(sc.b1, sc.a, col + i, c0 + i, n_valid);
+                        g *= gs[i];
+                        u *= us[i];
                     }
                     hv[i] = silu_f32(g) * u;
                 }
@@ -304,6 +325,11 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
             if (row_ok) {
                 const int col = n_idx * BN + c0;
                 uint32_t pk[16];
+                float gs[32], us[32];
+                if constexpr (SCALED) {
+                    chunk_scales(sc.b0 + c0, sc.a, col, n_valid, gs);
+                    chunk_scales(sc.b1 + c0, sc.a, col, n_valid, us);
+                }
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     float g0 = __uint_as_float(gv[2 * i]);
@@ -311,10 +337,10 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
                     float u0 = __uint_as_float(uv[2 * i]);
                     float u1 = __uint_as_float(uv[2 * i + 1]);
                     if constexpr (SCALED) {
-                        g0 *= col_scale(sc.b0, sc.a, col + 2 * i, c0 + 2 * i, n_valid);
-                        g1 *= col_scale(sc.b0, sc.a, col + 2 * i + 1, c0 + 2 * i + 1, n_valid);
-                        u0 *= col_scale(sc.b1, sc.a, col + 2 * i, c0 + 2 * i, n_valid);
-                        u1 *= col_scale(sc.b1, sc.a, col + 2 * i + 1, c0 + 2 * i + 1, n_valid);
+                        g0 *= gs[2 * i];
+                        g1 *= gs[2 * i + 1];
+                        u0 *= us[2 * i];
+                        u1 *= us[2 * i + 1];
                     }
                     pk[i] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
                 }
@@ -338,13 +364,16 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
             if (row_ok) {
                 const int col = n_idx * BN + c0;
                 uint32_t pk[16];
+                float cs[32];
+                if constexpr (SCALED)
+                    chunk_scales(sc.b0 + c0, sc.a, col, n_valid, cs);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     float a0 = wr * __uint_as_float(v[2 * i]);
                     float a1 = wr * __uint_as_float(v[2 * i + 1]);
                     if constexpr (SCALED) {
-                        a0 *= col_scale(sc.b0, sc.a, col + 2 * i, c0 + 2 * i, n_valid);
-                        a1 *= col_scale(sc.b0, sc.a, col + 2 * i + 1, c0 + 2 * i + 1, n_valid);
+                        a0 *= cs[2 * i];
+                        a1 *= cs[2 * i + 1];
                     }
                     pk[i] = pack_bf16x2(a0, a1);
                 }
@@ -362,13 +391,16 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
             if (row_ok) {
                 const int col = n_idx * BN + c0;
                 uint32_t pk[16];
+                float cs[32];
+                if constexpr (SCALED)
+                    chunk_scales(sc.b0 + c0, sc.a, col, n_valid, cs);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     float a0 = __uint_as_float(v[2 * i]);
                     float a1 = __uint_as_float(v[2 * i + 1]);
                     if constexpr (SCALED) {
-                        a0 *= col_scale(sc.b0, sc.a, col + 2 * i, c0 + 2 * i, n_valid);
-                        a1 *= col_scale(sc.b0, sc.a, col + 2 * i + 1, c0 + 2 * i + 1, n_valid);
+                        a0 *= cs[2 * i];
+                        a1 *= cs[2 * i + 1];
                     }
                     pk[i] = pack_bf16x2(a0, a1);
                 }
@@ -396,10 +428,15 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
             if (row_ok) {
                 const int col = n_idx * BN + c0;
                 if constexpr (SCALED) {
+                    static_assert(CH % 32 == 0 || !SCALED, "scaled fp32 chunks of 32 columns");
 #pragma unroll
-                    for (int i = 0; i < CH; ++i)
-                        v[i] = __float_as_uint(__uint_as_float(v[i]) *
-                                               col_scale(sc.b0, sc.a, col + i, c0 + i, n_valid));
+                    for (int h = 0; h < CH; h += 32) {
+                        float cs[32];
+                        chunk_scales(sc.b0 + c0 + h, sc.a, col + h, n_valid, cs);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[h + i] = __float_as_uint(__uint_as_float(v[h + i]) * cs[i]);
+                    }
                 }
                 float *dst = reinterpret_cast<float *>(out) + ks * p.part_stride + orow * ld_out + col;
                 // 16-byte stores when the whole chunk is in range and aligned
@@ -847,27 +884,52 @@ __device__ __forceinline__ SwapInfo swap_info(const int *s_seg, const int *s_sw,
 //     same lanes, so each thread combines its own two values;
 //   GEMM2 (EPI_BF16 / EPI_BF16_Y): one output feature per lane.
 // A thread stores one value per token row; a warp's 32 lanes write 64
-// contiguous bytes of the row.  taddr: this warp's lane quarter of the buffer.
-template <int EPI>
+// contiguous bytes of the row (128 for EPI_SWIGLU_F32's fp32 h).  taddr: this
+// warp's lane quarter of the buffer.  F8: E4M3 operands; each accumulator is
+// scaled by its weight row's scale (b_scale0 / b_scale1: gate / up, or down)
+// and its token row's scale (a_scale) first.
+template <int EPI, bool F8 = false>
 __device__ __forceinline__ void swap_epilogue(const TcParams &p, uint32_t taddr, int q, int lane,
                                               int rank, const SwapInfo &si)
 {
+    constexpr bool kGlu = EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_F32;
     __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.out);
     const int f = si.fb * kSwapFeat + rank * kTileM + q * 32 + lane;
     const bool f_ok = f < p.N_valid;
+    float wg = 1.f, wu = 1.f;
+    if constexpr (F8) {
+        const long long wr = (long long)si.seg * p.b_seg_rows + f;
+        wg = f_ok ? __ldg(p.b_scale0 + wr) : 0.f;
+        if constexpr (kGlu)
+            wu = f_ok ? __ldg(p.b_scale1 + wr) : 0.f;
+    }
 #pragma unroll 1
     for (int c0 = 0; c0 < si.n; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(taddr + c0, v);
-        if constexpr (EPI == EPI_SWIGLU) {
+        if constexpr (kGlu) {
             uint32_t u[32];
             tmem_ld32(taddr + kTileM + c0, u);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-                v[c] = __float_as_uint(silu_f32(__uint_as_float(v[c])) * __uint_as_float(u[c]));
+            for (int c = 0; c < 32; ++c) {
+                float g = __uint_as_float(v[c]), uu = __uint_as_float(u[c]);
+                if constexpr (F8) {
+                    // token rows past the unit's valid ones read a clamped scale
+                    const float ts = __ldg(p.a_scale + si.r0 + min(c0 + c, si.rv - 1));
+                    g *= wg * ts;
+                    uu *= wu * ts;
+                }
+                v[c] = __float_as_uint(silu_f32(g) * uu);
+            }
         } else {
             tmem_wait_ld();
+            if constexpr (F8) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    v[c] = __float_as_uint(__uint_as_float(v[c]) * wg *
+                                           __ldg(p.a_scale + si.r0 + min(c0 + c, si.rv - 1)));
+            }
         }
         if (f_ok) {
             const int nc = si.rv - c0;
@@ -876,7 +938,10 @@ __device__ __forceinline__ void swap_epilogue(const TcParams &p, uint32_t taddr,
                 if (c >= nc)
                     break;
                 const int row = si.r0 + c0 + c;
-                if constexpr (EPI == EPI_BF16_Y) {
+                if constexpr (EPI == EPI_SWIGLU_F32) {
+                    reinterpret_cast<float *>(p.out)[(long long)row * p.ld_out + f] =
+                        __uint_as_float(v[c]);
+                } else if constexpr (EPI == EPI_BF16_Y) {
                     const int tok = p.row_tok[row];
                     out[(long long)tok * p.ld_out + f] =
                         __float2bfloat16_rn(p.row_w[row] * __uint_as_float(v[c]));
@@ -888,7 +953,9 @@ __device__ __forceinline__ void swap_epilogue(const TcParams &p, uint32_t taddr,
     }
 }
 
-template <int BN, int NB, int EPI, int STAGES>
+// F8: E4M3 operands as in tc_gemm_kernel (128-element reduction steps in the
+// same 128-byte rows, kind::f8f6f4 MMAs, both scales in the epilogues).
+template <int BN, int NB, int EPI, int STAGES, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap mA,
                         const __grid_constant__ CUtensorMap mB0,
@@ -898,7 +965,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tS, const TcParams p)
 {
     using S = PairShape<BN, NB, STAGES>;
-    static_assert(EPI == EPI_SWIGLU ? NB == 2 : NB == 1, "pair epilogues");
+    static_assert((EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_F32) ? NB == 2 : NB == 1,
+                  "pair epilogues");
+    static_assert(!F8 || EPI != EPI_SWIGLU, "E4M3 GEMM1 writes fp32 h");
+    constexpr int KSTEP = F8 ? 128 : 64;   // reduction elements per 128-byte row
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
@@ -1005,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_swap = (failed || !swap_mode) ? 0 : s_sw[p.nseg] * n_fb;
     const int NC = balanced_workers(n_full + n_swap, nclusters);
     const bool active = cluster_id < NC;
-    const int nk = (p.K + 63) / 64;
+    const int nk = (p.K + KSTEP - 1) / KSTEP;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -1053,8 +1123,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!sw) {
                         if (leader)
                             mbar_arrive_expect_tx(&full[s], tx);
-                        tma_load_2d_pair(sa, ma, fb, st * 64, a_row);
-                        tma_load_2d_pair(sb, mb, fb, st * 64, b_row);
+                        tma_load_2d_pair(sa, ma, fb, st * KSTEP, a_row);
+                        tma_load_2d_pair(sb, mb, fb, st * KSTEP, b_row);
                     } else {
                         const int k0 = st * S::SWAP_KPS;
                         const int steps = min(S::SWAP_KPS, nk - k0);
@@ -1063,16 +1133,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mbar_arrive_expect_tx(&full[s],
                                                   2u * (wbytes + (uint32_t)(steps * half * 128)));
                         if (NB == 2) {
-                            tma_load_2d_pair(sa, &wS0, fb, k0 * 64, a_row);
-                            tma_load_2d_pair(sb, &wS1, fb, k0 * 64, a_row);
+                            tma_load_2d_pair(sa, &wS0, fb, k0 * KSTEP, a_row);
+                            tma_load_2d_pair(sb, &wS1, fb, k0 * KSTEP, a_row);
                         } else {
                             for (int j = 0; j < steps; ++j)
-                                tma_load_2d_pair(sa + j * S::A_BYTES, &wS0, fb, (k0 + j) * 64, a_row);
+                                tma_load_2d_pair(sa + j * S::A_BYTES, &wS0, fb, (k0 + j) * KSTEP,
+                                                 a_row);
                         }
                         for (int j = 0; j < steps; ++j)
                             for (int r = 0; r < half; r += kSwapBoxRows)
                                 tma_load_2d_pair(stok + j * (S::TOK_BYTES / S::SWAP_KPS) + r * 128,
-                                                 &tS, fb, (k0 + j) * 64, t_row + r);
+                                                 &tS, fb, (k0 + j) * KSTEP, t_row + r);
                     }
                     ++fills;
                     if (++s == STAGES) {
@@ -1102,7 +1173,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer (even CTA)
-            constexpr uint32_t idesc_full = idesc_bf16_f32(kPairRows, S::UMMA_N);
+            constexpr uint32_t idesc_full = F8 ? idesc_e4m3_f32(kPairRows, S::UMMA_N)
+                                               : idesc_bf16_f32(kPairRows, S::UMMA_N);
+            // one K = 16 (bf16) or K = 32 (E4M3) step of the pair
+            auto mma = [](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+                if constexpr (F8)
+                    umma_e4m3_pair(d, a, b, id, acc);
+                else
+                    umma_bf16_pair(d, a, b, id, acc);
+            };
             int s = 0;
             uint32_t ph = 0, b = 0, tph = 0;
             bool ok = true;
@@ -1113,7 +1192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t idesc = idesc_full;
                 if (sw) {
                     const SwapInfo si = swap_info(s_seg, s_sw, p.nseg, n_fb, S::SWAP_ROWS, g);
-                    idesc = idesc_bf16_f32(kPairRows, si.n);
+                    idesc = F8 ? idesc_e4m3_f32(kPairRows, si.n) : idesc_bf16_f32(kPairRows, si.n);
                 }
                 if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, kWaitLimitNs)) {
                     ok = false;
@@ -1134,8 +1213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t bdesc = sdesc_kmajor_sw128(sa + S::A_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            umma_bf16_pair(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
-                                           (st > 0 || kk > 0) ? 1u : 0u);
+                            mma(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                (st > 0 || kk > 0) ? 1u : 0u);
                     } else if (NB == 2) {
                         // gate rows (A slot) into columns [0, n), up rows (B
                         // slot) into [128, 128 + n); tokens from the token area
@@ -1145,9 +1224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint32_t acc = (st > 0 || kk > 0) ? 1u : 0u;
-                            umma_bf16_pair(d_tmem, gdesc + 2u * kk, tdesc + 2u * kk, idesc, acc);
-                            umma_bf16_pair(d_tmem + kTileM, udesc + 2u * kk, tdesc + 2u * kk,
-                                           idesc, acc);
+                            mma(d_tmem, gdesc + 2u * kk, tdesc + 2u * kk, idesc, acc);
+                            mma(d_tmem + kTileM, udesc + 2u * kk, tdesc + 2u * kk, idesc, acc);
                         }
                     } else {
                         // one or two reduction steps: weights in the A (and B)
@@ -1159,8 +1237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 sa + S::A_BYTES + S::B_BYTES + j * (S::TOK_BYTES / S::SWAP_KPS));
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                umma_bf16_pair(d_tmem, wdesc + 2u * kk, tdesc + 2u * kk, idesc,
-                                               (st > 0 || j > 0 || kk > 0) ? 1u : 0u);
+                                mma(d_tmem, wdesc + 2u * kk, tdesc + 2u * kk, idesc,
+                                    (st > 0 || j > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
                     umma_commit_pair(&empty[s], 0x3);
@@ -1208,11 +1286,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int my_rows = ti.rows - (int)rank * kTileM;
                 const bool row_ok = r < my_rows;
                 const long long orow = (long long)ti.a_row0 + (int)rank * kTileM + r;
-                epilogue_row<BN, EPI>(p, p.out, p.ld_out, p.N_valid, taddr, row_ok, orow,
-                                      ti.n_idx);
+                EpiScale sc{1.f, nullptr, nullptr};
+                if constexpr (F8) {
+                    const long long b0 =
+                        (long long)ti.seg * p.b_seg_rows + (long long)ti.n_idx * BN;
+                    sc.a = row_ok ? __ldg(p.a_scale + orow) : 0.f;
+                    sc.b0 = p.b_scale0 + b0;
+                    sc.b1 = NB == 2 ? p.b_scale1 + b0 : sc.b0;
+                }
+                epilogue_row<BN, EPI, F8>(p, p.out, p.ld_out, p.N_valid, taddr, row_ok, orow,
+                                          ti.n_idx, 0, sc);
             } else {
                 const SwapInfo si = swap_info(s_seg, s_sw, p.nseg, n_fb, S::SWAP_ROWS, g);
-                swap_epilogue<EPI>(p, taddr, q, lane, (int)rank, si);
+                swap_epilogue<EPI, F8>(p, taddr, q, lane, (int)rank, si);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -1335,13 +1421,13 @@ struct SwapMaps {
 
 // Launches the CTA-pair kernel as clusters of 2 (persistent: at most as
 // many pairs as can be resident at once, and no more than there are units).
-template <int BN, int NB, int EPI, int STAGES>
+template <int BN, int NB, int EPI, int STAGES, bool F8 = false>
 cudaError_t launch_tc_pair(const CUtensorMap &mA, const CUtensorMap &mB0, const CUtensorMap &mB1,
                            const TcParams &p, long long max_tiles, cudaStream_t stream,
                            const SwapMaps *swap = nullptr)
 {
     using S = PairShape<BN, NB, STAGES>;
-    auto kern = tc_gemm_pair_kernel<BN, NB, EPI, STAGES>;
+    auto kern = tc_gemm_pair_kernel<BN, NB, EPI, STAGES, F8>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
@@ -1678,6 +1764,185 @@ cudaError_t launch_dense_tc(int rows, int N, int K, const void *A, const void *B
                      : launch_tc<128, 1, EPI_BF16, 6>(mA, mB, mB, p, mt * p.n_tiles, stream);
 }
 
+namespace {
+
+// launch_experts_w8a8 for layers large enough for CTA pairs (plan.pair_routed):
+// the routed GEMMs on the pair kernel (256-row tiles, experts under 256 rows
+// as swap units), the shared expert's GEMMs on their own launches (pairs
+// when plan.pair_shared).
+cudaError_t experts_w8a8_pairs(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
+                               const ExpertW8 &w, void *y, const AuxArgs &aux,
+                               cudaStream_t stream, cudaEvent_t *ev)
+{
+    const int D = c.d_model, F = c.d_expert, S = c.d_shared, E = c.n_experts, T = c.T;
+    const A8Layout A = a8_layout_of(c, L);
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    const int32_t *seg = reinterpret_cast<const int32_t *>(ws + L.seg_off);
+    const int32_t *mtile = reinterpret_cast<const int32_t *>(ws + L.mtile);
+    const long long R = L.R_max;
+    const long long mt2_bound = R / kPairRows + E;
+    const long long mt_s = (T + kTileM - 1) / kTileM, mt2_s = (T + kPairRows - 1) / kPairRows;
+    const LaunchPlan plan = plan_of(c);
+    const bool shared = S > 0, pair_shared = plan.pair_shared;
+    const bool wide_down = D > 1024;
+    const int bn_down = wide_down ? 256 : 128;
+    uint8_t *xq = ws + A.xq, *hq = ws + A.hq, *sxq = ws + A.sxq, *shq = ws + A.shq;
+    float *xs = reinterpret_cast<float *>(ws + A.xs), *hsc = reinterpret_cast<float *>(ws + A.hsc);
+    float *sxs = reinterpret_cast<float *>(ws + A.sxs), *shs = reinterpret_cast<float *>(ws + A.shs);
+    float *hf = reinterpret_cast<float *>(ws + A.hf), *shf = reinterpret_cast<float *>(ws + A.shf);
+    cudaError_t err;
+
+    // GEMM1, routed: hf = silu(xq Wg^T) * (xq Wu^T), fp32
+    {
+        CUtensorMap mA, mG, mU;
+        SwapMaps sw;
+        if (!make_map_u8(&mA, xq, (uint64_t)R, (uint64_t)D, kTileM) ||
+            !make_map_u8(&mG, w.gate, (uint64_t)E * F, (uint64_t)D, 128) ||
+            !make_map_u8(&mU, w.up, (uint64_t)E * F, (uint64_t)D, 128) ||
+            !make_map_u8(&sw.w0, w.gate, (uint64_t)E * F, (uint64_t)D, kTileM) ||
+            !make_map_u8(&sw.w1, w.up, (uint64_t)E * F, (uint64_t)D, kTileM) ||
+            !make_map_u8(&sw.t, xq, (uint64_t)R, (uint64_t)D, kSwapBoxRows))
+            return cudaErrorInvalidValue;
+        TcParams p{};
+        p.seg_off = seg;
+        p.mtile = mtile;
+        p.nseg = E;
+        p.K = D;
+        p.n_tiles = (F + 127) / 128;
+        p.N_valid = F;
+        p.b_seg_rows = F;
+        p.out = hf;
+        p.ld_out = F;
+        p.status = status;
+        p.aux = aux;
+        p.a_scale = xs;
+        p.b_scale0 = w.gate_s;
+        p.b_scale1 = w.up_s;
+        p.swap_tails = 1;
+        const long long units =
+            mt2_bound * p.n_tiles + 8LL * E * ((F + kSwapFeat - 1) / kSwapFeat);
+        err = launch_tc_pair<128, 2, EPI_SWIGLU_F32, 5, true>(mA, mG, mU, p, units, stream, &sw);
+        if (err != cudaSuccess)
+            return err;
+    }
+    err = launch_quantize_e4m3_act(R, F, hf, true, hq, hsc, seg + E, stream);
+    if (err == cudaSuccess)
+        err = record_stage(ev, 3, stream);
+    if (err != cudaSuccess)
+        return err;
+    // GEMM2, routed: z = hq Wd^T (or w * ... into y)
+    {
+        CUtensorMap mA, mB;
+        SwapMaps sw;
+        if (!make_map_u8(&mA, hq, (uint64_t)R, (uint64_t)F, kTileM) ||
+            !make_map_u8(&mB, w.down, (uint64_t)E * D, (uint64_t)F, (uint32_t)(bn_down / 2)) ||
+            !make_map_u8(&sw.w0, w.down, (uint64_t)E * D, (uint64_t)F, kTileM) ||
+            !make_map_u8(&sw.t, hq, (uint64_t)R, (uint64_t)F, kSwapBoxRows))
+            return cudaErrorInvalidValue;
+        sw.w1 = sw.w0;
+        TcParams p{};
+        p.seg_off = seg;
+        p.mtile = mtile;
+        p.nseg = E;
+        p.K = F;
+        p.n_tiles = (D + bn_down - 1) / bn_down;
+        p.N_valid = D;
+        p.b_seg_rows = D;
+        p.out = ws + L.z;
+        p.ld_out = D;
+        p.status = status;
+        p.a_scale = hsc;
+        p.b_scale0 = w.down_s;
+        p.b_scale1 = w.down_s;
+        p.swap_tails = 1;
+        const long long units =
+            mt2_bound * p.n_tiles + 8LL * E * ((D + kSwapFeat - 1) / kSwapFeat);
+        if (plan.direct_y) {
+            p.out = y;
+            p.row_tok = reinterpret_cast<const int32_t *>(ws + L.row_tok);
+            p.row_w = reinterpret_cast<const float *>(ws + L.row_w);
+            err = wide_down
+                      ? launch_tc_pair<256, 1, EPI_BF16_Y, 5, true>(mA, mB, mB, p, units, stream, &sw)
+                      : launch_tc_pair<128, 1, EPI_BF16_Y, 6, true>(mA, mB, mB, p, units, stream, &sw);
+        } else {
+            err = wide_down
+                      ? launch_tc_pair<256, 1, EPI_BF16, 5, true>(mA, mB, mB, p, units, stream, &sw)
+                      : launch_tc_pair<128, 1, EPI_BF16, 6, true>(mA, mB, mB, p, units, stream, &sw);
+        }
+        if (err == cudaSuccess)
+            err = record_stage(ev, 4, stream);
+        if (err != cudaSuccess)
+            return err;
+    }
+    // GEMM1, shared expert: shf = silu(sxq Wsg^T) * (sxq Wsu^T), fp32
+    if (shared) {
+        CUtensorMap mA, mG, mU;
+        if (!make_map_u8(&mA, sxq, (uint64_t)T, (uint64_t)D, kTileM) ||
+            !make_map_u8(&mG, w.sgate, (uint64_t)S, (uint64_t)D, 128) ||
+            !make_map_u8(&mU, w.sup, (uint64_t)S, (uint64_t)D, 128))
+            return cudaErrorInvalidValue;
+        TcParams p{};
+        p.nseg = 1;
+        p.dense_rows = T;
+        p.K = D;
+        p.n_tiles = (S + 127) / 128;
+        p.N_valid = S;
+        p.out = shf;
+        p.ld_out = S;
+        p.status = status;
+        p.a_scale = sxs;
+        p.b_scale0 = w.sgate_s;
+        p.b_scale1 = w.sup_s;
+        err = pair_shared ? launch_tc_pair<128, 2, EPI_SWIGLU_F32, 5, true>(
+                                mA, mG, mU, p, mt2_s * p.n_tiles, stream)
+                          : launch_tc<128, 2, EPI_SWIGLU_F32, 4, true>(mA, mG, mU, p,
+                                                                       mt_s * p.n_tiles, stream);
+        if (err != cudaSuccess)
+            return err;
+    }
+    if (shared)
+        err = launch_quantize_e4m3_act(T, S, shf, true, shq, shs, nullptr, stream);
+    if (err == cudaSuccess)
+        err = record_stage(ev, 5, stream);
+    if (err != cudaSuccess)
+        return err;
+    // GEMM2, shared expert: zs = shq Wsd^T (bf16: the combine adds it)
+    if (shared) {
+        CUtensorMap mA, mB;
+        if (!make_map_u8(&mA, shq, (uint64_t)T, (uint64_t)S, kTileM) ||
+            !make_map_u8(&mB, w.sdown, (uint64_t)D, (uint64_t)S,
+                         (uint32_t)(pair_shared ? bn_down / 2 : bn_down)))
+            return cudaErrorInvalidValue;
+        TcParams p{};
+        p.nseg = 1;
+        p.dense_rows = T;
+        p.K = S;
+        p.n_tiles = (D + bn_down - 1) / bn_down;
+        p.N_valid = D;
+        p.out = ws + L.zs;
+        p.ld_out = D;
+        p.status = status;
+        p.a_scale = shs;
+        p.b_scale0 = w.sdown_s;
+        p.b_scale1 = w.sdown_s;
+        if (pair_shared)
+            err = wide_down ? launch_tc_pair<256, 1, EPI_BF16, 5, true>(mA, mB, mB, p,
+                                                                        mt2_s * p.n_tiles, stream)
+                            : launch_tc_pair<128, 1, EPI_BF16, 6, true>(mA, mB, mB, p,
+                                                                        mt2_s * p.n_tiles, stream);
+        else
+            err = wide_down ? launch_tc<256, 1, EPI_BF16, 4, true>(mA, mB, mB, p,
+                                                                   mt_s * p.n_tiles, stream)
+                            : launch_tc<128, 1, EPI_BF16, 6, true>(mA, mB, mB, p,
+                                                                   mt_s * p.n_tiles, stream);
+    }
+    if (err == cudaSuccess)
+        err = record_stage(ev, 6, stream);
+    return err;
+}
+
+}  // namespace
+
 cudaError_t launch_experts_w8a8(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                                 const void *x, const ExpertW8 &w, void *y, const AuxArgs &aux,
                                 cudaStream_t stream, cudaEvent_t *ev)
@@ -1707,6 +1972,9 @@ cudaError_t launch_experts_w8a8(const moe_config &c, const WorkspaceLayout &L, u
     // few rows per expert: weights as the 128-row MMA operand instead
     if (w8a8_swap(c))
         return launch_experts_w8a8_swap(c, L, ws, w, y, aux, stream, ev);
+    // many rows: CTA pairs
+    if (plan_of(c).pair_routed)
+        return experts_w8a8_pairs(c, L, ws, w, y, aux, stream, ev);
     // the token rows' codes and scales were written before the dispatch
     // (sxq, sxs: one per token) and gathered by it into expert order (xq, xs)
     (void)x;

@@ -304,6 +304,19 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
         : "memory");
 }
 
+// umma_bf16_pair with E4M3 A and B (kind::f8f6f4, K = 32 elements: one
+// 32-byte slice of each 128-byte row).
+__device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once, when the pair's tcgen05 ops issued so far by this thread have
 // completed, on the mbarrier at the same shared-memory offset in every CTA
 // of `cta_mask` (bit r = cluster rank r).

@@ -99,6 +99,12 @@ WORKLOADS = {
         "dsv3_prefill_e32", T=4096, D=7168, E=32, F=2048, k=8, S=2048,
         mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1",
         description="DeepSeek-V3 widths, 32 experts, T=4096: profiling case"),
+    # the same profiling case with E4M3 weights and activations
+    "dsv3_prefill_e32_w8a8": Workload(
+        "dsv3_prefill_e32_w8a8", T=4096, D=7168, E=32, F=2048, k=8, S=2048,
+        mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1", weights="e4m3", acts="e4m3",
+        description="DeepSeek-V3 widths, 32 experts, T=4096, E4M3 weights and "
+                    "activations: profiling case"),
     "dsv3_decode": Workload(
         "dsv3_decode", T=64, D=7168, E=256, F=2048, k=8, S=2048,
         mode=GATING_SOFTMAX_ALL_RENORM, bias="zipf1.1",

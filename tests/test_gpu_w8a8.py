@@ -97,6 +97,37 @@ CASES = [
 ]
 
 
+# Large enough for the CTA-pair GEMMs (>= 16384 routed rows, >= 512 per
+# expert): 256-row pair tiles, experts under 256 rows as swap units, the
+# shared expert's dense pair tiles; small D and F keep the oracle cheap.
+PAIR = [
+    # ragged segments, partial column tiles (F = 320, D = 192), drops, and
+    # a shared expert (dense pair tiles)
+    ("a8_pair_ragged_drops", 8200, 192, 4, 320, 2, 256, 1, 0.6, "normal_var2"),
+    # one expert per token, no shared expert: the down projection writes y
+    ("a8_pair_top1_direct_y", 16400, 256, 8, 256, 1, 0, 2, 1.1, "none"),
+    # 128 experts, skewed: many experts under 256 rows run as swap units
+    ("a8_pair_tails_e128_zipf", 8200, 128, 128, 192, 8, 0, 2, 0.0, "zipf1.1"),
+    # wide down projection (256-column tiles, two reduction steps per swap
+    # stage) over F = 320 (three 128-wide steps, the last half empty)
+    ("a8_pair_wide_down_odd_k", 4100, 1088, 16, 320, 4, 0, 2, 0.0, "zipf1.1"),
+]
+
+
+@pytest.mark.parametrize("case", PAIR, ids=[c[0] for c in PAIR])
+def test_w8a8_pair_layers(case):
+    name, T, D, E, F, k, S, mode, gamma, bias = case
+    w = Workload(name, T=T, D=D, E=E, F=F, k=k, S=S, mode=mode, gamma=gamma, dtype="bf16",
+                 alpha=0.01, bias=bias, weights="e4m3", acts="e4m3")
+    assert B.launch_plan(B.config_of(w))["pair_routed"]
+    _, inp, outs, code = parity.run(w, seed=29)
+    assert code == B.MOE_DEVICE_OK
+    R = _check_quantized_rows(w, inp, outs, max_rows=4096)
+    rep = parity.check(w, inp, outs, e4m3=True, a8=True, coverage=True, y_sample_n=96)
+    rep["rows"] = R
+    print(name, rep)
+
+
 def test_cases_cover_both_kernel_forms():
     forms = {B.launch_plan(B.make_config(T, D, E, F, k, d_shared=S))["w8a8_swap"]
              for _, T, D, E, F, k, S, *_ in CASES}
