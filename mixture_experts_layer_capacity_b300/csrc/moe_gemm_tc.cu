@@ -88,6 +88,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any tile
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s
 constexpr int kThreads = 192;
 
+// Per-warp staging tile of the epilogues: 32 rows of one 32-column chunk
+// (64 bytes of bf16 or 128 of fp32 per row), rows padded by 16 bytes so that
+// the row-per-lane writes and the row-major reads spread over the banks.
+constexpr int kEpiRowBytes = 128 + 16;
+// and, for E4M3 tiles, the warp's copy of the tile's 256 column scales
+constexpr int kEpiScaleFloats = 256;
+constexpr int kEpiStageBytes = 4 * (32 * kEpiRowBytes + kEpiScaleFloats * 4);   // four warps
+
 template <int BN, int NB, int STAGES>
 struct TcShape {
     static constexpr int UMMA_N = BN * NB;
@@ -100,7 +108,9 @@ struct TcShape {
                                      : 2 * UMMA_N <= 256 ? 256
                                                          : 512;
     static constexpr int TABLE_BYTES = 2 * (kMaxExperts + 1) * 4 + 8;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + TABLE_BYTES + 1024;
+    // the epilogue warps' staging tiles, after the ring, barriers and tables
+    static constexpr int EPI_OFF = (STAGES * STAGE_BYTES + 256 + TABLE_BYTES + 127) / 128 * 128;
+    static constexpr int SMEM_BYTES = EPI_OFF + kEpiStageBytes + 1024;
     static_assert(UMMA_N % 16 == 0 && UMMA_N >= 16 && UMMA_N <= 256, "UMMA N");
     static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -235,179 +245,210 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const uint32_
 }
 
 // Scales of an E4M3 tile's accumulator row: the A row's scale and the B
-// rows' scales of the tile's first column (gate and up for GEMM1); b0 null:
-// the operands are bf16 and nothing is scaled.
+// rows' scales of the tile's columns (gate and up for GEMM1), copied into
+// the epilogue warp's shared-memory scale buffer before the tile's
+// accumulators are ready (stage_col_scales); b0 null: the operands are bf16
+// and nothing is scaled.
 struct EpiScale {
     float a;
     const float *b0, *b1;
 };
 
-// Scales of 32 consecutive columns of an E4M3 tile: the row scale a times
-// each B row's scale.  b: the first column's B row scale; col: that
-// column's index in the output; 0 past the valid columns.  All lanes of a
-// warp read the same addresses (a broadcast); a whole in-range, 16-byte
-// aligned run is read as eight float4.
-__device__ __forceinline__ void chunk_scales(const float *b, float a, int col, int n_valid,
-                                             float (&cs)[32])
+// Copies n column scales of a tile (b: the first column's B row scale; col:
+// that column's index in the output) into sb, 0 past the n_valid columns.
+// Every lane of the warp calls it, between tiles; the warp's later reads
+// see the copy.
+__device__ __forceinline__ void stage_col_scales(const float *b, int col, int n_valid, float *sb,
+                                                 int n)
 {
-    if (col + 32 <= n_valid && (reinterpret_cast<uintptr_t>(b) & 15u) == 0) {
-        const float4 *b4 = reinterpret_cast<const float4 *>(b);
+    const int lane = threadIdx.x & 31;
+    __syncwarp();   // the previous tile's reads of sb are done
+    for (int c = lane; c < n; c += 32)
+        sb[c] = col + c < n_valid ? __ldg(b + c) : 0.f;
+    __syncwarp();
+}
+
+// Scales of 32 consecutive columns: the row scale a times each staged column
+// scale (sb: the chunk's first entry of the warp's scale buffer in shared
+// memory, 16-byte aligned; all lanes read the same words).
+__device__ __forceinline__ void chunk_scales(const float *sb, float a, float (&cs)[32])
+{
+    const float4 *b4 = reinterpret_cast<const float4 *>(sb);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float4 t = __ldg(b4 + j);
-            cs[4 * j] = a * t.x;
-            cs[4 * j + 1] = a * t.y;
-            cs[4 * j + 2] = a * t.z;
-            cs[4 * j + 3] = a * t.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            cs[i] = col + i < n_valid ? a * __ldg(b + i) : 0.f;
+    for (int j = 0; j < 8; ++j) {
+        const float4 t = b4[j];
+        cs[4 * j] = a * t.x;
+        cs[4 * j + 1] = a * t.y;
+        cs[4 * j + 2] = a * t.z;
+        cs[4 * j + 3] = a * t.w;
     }
+}
+
+// Stores one 32-column chunk of the warp's 32 rows: each lane holds its own
+// row's NW packed words (w) and that row's destination (dst, valid when
+// row_ok); the words pass through the warp's staging tile so that each
+// store instruction writes whole 64- or 128-byte row segments (4 or 8 lanes
+// per row) instead of one 16-byte piece of 32 different rows.  valid_bytes:
+// bytes of each row inside the output's columns (<= NW * 4); es: element
+// size (2 or 4) for a ragged tail.  Every lane of the warp calls it.
+template <int NW>
+__device__ __forceinline__ void warp_store_chunk(uint8_t *stile, const uint32_t (&w)[NW],
+                                                 bool row_ok, uint8_t *dst, int valid_bytes,
+                                                 int es)
+{
+    constexpr int PPR = NW / 4;                 // 16-byte pieces per row
+    const int lane = threadIdx.x & 31;
+    uint4 *srow = reinterpret_cast<uint4 *>(stile + lane * kEpiRowBytes);
+#pragma unroll
+    for (int j = 0; j < PPR; ++j)
+        srow[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < PPR; ++it) {
+        const int piece = it * 32 + lane;
+        const int r = piece / PPR, c = piece - (piece / PPR) * PPR;
+        uint8_t *d = reinterpret_cast<uint8_t *>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(dst), r));
+        const bool ok = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, r) != 0;
+        if (!ok || c * 16 >= valid_bytes)
+            continue;
+        const uint8_t *src = stile + r * kEpiRowBytes + c * 16;
+        uint8_t *g = d + c * 16;
+        if ((c + 1) * 16 <= valid_bytes && (reinterpret_cast<uintptr_t>(g) & 15) == 0) {
+            *reinterpret_cast<uint4 *>(g) = *reinterpret_cast<const uint4 *>(src);
+        } else if (es == 2) {
+            for (int e = 0; e < 8 && c * 16 + e * 2 < valid_bytes; ++e)
+                reinterpret_cast<uint16_t *>(g)[e] = reinterpret_cast<const uint16_t *>(src)[e];
+        } else {
+            for (int e = 0; e < 4 && c * 16 + e * 4 < valid_bytes; ++e)
+                reinterpret_cast<uint32_t *>(g)[e] = reinterpret_cast<const uint32_t *>(src)[e];
+        }
+    }
+    __syncwarp();   // the tile is rewritten by the next chunk
+}
+
+// Bytes of a 32-column chunk starting at output column `col` that lie inside
+// n_valid columns of es-byte elements.
+__device__ __forceinline__ int chunk_valid_bytes(int col, int n_valid, int es)
+{
+    return max(0, min(32, n_valid - col)) * es;
 }
 
 // Epilogue of one accumulator row (TMEM lane) of a tile: this thread owns
 // output row `orow` (stored only when row_ok), columns n_idx*BN ... of the
 // tile.  taddr: TMEM address of the row's first accumulator column.
 // SCALED: E4M3 operands, the accumulator is multiplied by the row's and the
-// column's scales (sc) first.
+// column's scales (sc) first.  stile: the warp's staging tile (all lanes of
+// the warp call this together; bf16 and fp32-h outputs are stored through
+// it, whole row segments at a time).
 template <int BN, int EPI, bool SCALED = false>
 __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long long ld_out,
                                              int n_valid, uint32_t taddr, bool row_ok,
                                              long long orow, int n_idx, int ks = 0,
-                                             EpiScale sc = EpiScale{1.f, nullptr, nullptr})
+                                             EpiScale sc = EpiScale{1.f, nullptr, nullptr},
+                                             uint8_t *stile = nullptr)
 {
     if constexpr (EPI == EPI_SWIGLU_F32) {
+        uint8_t *row_base =
+            reinterpret_cast<uint8_t *>(reinterpret_cast<float *>(out) + orow * ld_out);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
             uint32_t gv[32], uv[32];
             tmem_ld32(taddr + c0, gv);
             tmem_ld32(taddr + BN + c0, uv);
             tmem_wait_ld();
-            if (row_ok) {
-                const int col = n_idx * BN + c0;
-                float hv[32], gs[32], us[32];
-                if constexpr (SCALED) {
-                    chunk_scales(sc.b0 + c0, sc.a, col, n_valid, gs);
-                    chunk_scales(sc.b1 + c0, sc.a, col, n_valid, us);
-                }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float g = __uint_as_float(gv[i]), u = __uint_as_float(uv[i]);
-                    if constexpr (SCALED) {
-                        g *= gs[i];
-                        u *= us[i];
-                    }
-                    hv[i] = silu_f32(g) * u;
-                }
-                float *dst = reinterpret_cast<float *>(out) + orow * ld_out + col;
-                if (col + 32 <= n_valid && (ld_out & 3) == 0) {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4 *>(dst + i) =
-                            make_float4(hv[i], hv[i + 1], hv[i + 2], hv[i + 3]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (col + i < n_valid)
-                            dst[i] = hv[i];
-                }
+            const int col = n_idx * BN + c0;
+            float gs[32], us[32];
+            if constexpr (SCALED) {   // sc.a is 0 for rows outside the tile
+                chunk_scales(sc.b0 + c0, sc.a, gs);
+                chunk_scales(sc.b1 + c0, sc.a, us);
             }
+            uint32_t hw[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float g = __uint_as_float(gv[i]), u = __uint_as_float(uv[i]);
+                if constexpr (SCALED) {
+                    g *= gs[i];
+                    u *= us[i];
+                }
+                hw[i] = __float_as_uint(silu_f32(g) * u);
+            }
+            warp_store_chunk<32>(stile, hw, row_ok, row_base + (long long)col * 4,
+                                 chunk_valid_bytes(col, n_valid, 4), 4);
         }
     } else if constexpr (EPI == EPI_SWIGLU) {
+        uint8_t *row_base = reinterpret_cast<uint8_t *>(
+            reinterpret_cast<__nv_bfloat16 *>(out) + orow * ld_out);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
             uint32_t gv[32], uv[32];
             tmem_ld32(taddr + c0, gv);
             tmem_ld32(taddr + BN + c0, uv);
             tmem_wait_ld();
-            if (row_ok) {
-                const int col = n_idx * BN + c0;
-                uint32_t pk[16];
-                float gs[32], us[32];
+            const int col = n_idx * BN + c0;
+            uint32_t pk[16];
+            float gs[32], us[32];
+            if constexpr (SCALED) {   // sc.a is 0 for rows outside the tile
+                chunk_scales(sc.b0 + c0, sc.a, gs);
+                chunk_scales(sc.b1 + c0, sc.a, us);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float g0 = __uint_as_float(gv[2 * i]);
+                float g1 = __uint_as_float(gv[2 * i + 1]);
+                float u0 = __uint_as_float(uv[2 * i]);
+                float u1 = __uint_as_float(uv[2 * i + 1]);
                 if constexpr (SCALED) {
-                    chunk_scales(sc.b0 + c0, sc.a, col, n_valid, gs);
-                    chunk_scales(sc.b1 + c0, sc.a, col, n_valid, us);
+                    g0 *= gs[2 * i];
+                    g1 *= gs[2 * i + 1];
+                    u0 *= us[2 * i];
+                    u1 *= us[2 * i + 1];
                 }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float g0 = __uint_as_float(gv[2 * i]);
-                    float g1 = __uint_as_float(gv[2 * i + 1]);
-                    float u0 = __uint_as_float(uv[2 * i]);
-                    float u1 = __uint_as_float(uv[2 * i + 1]);
-                    if constexpr (SCALED) {
-                        g0 *= gs[2 * i];
-                        g1 *= gs[2 * i + 1];
-                        u0 *= us[2 * i];
-                        u1 *= us[2 * i + 1];
-                    }
-                    pk[i] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
-                }
-                __nv_bfloat16 *dst =
-                    reinterpret_cast<__nv_bfloat16 *>(out) + orow * ld_out + col;
-                store_row_bf16(dst, pk, col, n_valid);
+                pk[i] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
             }
+            warp_store_chunk<16>(stile, pk, row_ok, row_base + (long long)col * 2,
+                                 chunk_valid_bytes(col, n_valid, 2), 2);
         }
-    } else if constexpr (EPI == EPI_BF16_Y) {
+    } else if constexpr (EPI == EPI_BF16_Y || EPI == EPI_BF16) {
+        // EPI_BF16_Y: the row goes, times its gate weight, to its token's row of y
         int tok = 0;
-        float wr = 0.f;
-        if (row_ok) {
-            tok = p.row_tok[orow];
-            wr = p.row_w[orow];
+        float wr = 1.f;
+        if constexpr (EPI == EPI_BF16_Y) {
+            wr = 0.f;
+            if (row_ok) {
+                tok = p.row_tok[orow];
+                wr = p.row_w[orow];
+            }
         }
+        const long long drow = EPI == EPI_BF16_Y ? (long long)tok : orow;
+        uint8_t *row_base = reinterpret_cast<uint8_t *>(
+            reinterpret_cast<__nv_bfloat16 *>(out) + drow * ld_out);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
             uint32_t v[32];
             tmem_ld32(taddr + c0, v);
             tmem_wait_ld();
-            if (row_ok) {
-                const int col = n_idx * BN + c0;
-                uint32_t pk[16];
-                float cs[32];
-                if constexpr (SCALED)
-                    chunk_scales(sc.b0 + c0, sc.a, col, n_valid, cs);
+            const int col = n_idx * BN + c0;
+            uint32_t pk[16];
+            float cs[32];
+            if constexpr (SCALED)   // sc.a is 0 for rows outside the tile
+                chunk_scales(sc.b0 + c0, sc.a, cs);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float a0 = wr * __uint_as_float(v[2 * i]);
-                    float a1 = wr * __uint_as_float(v[2 * i + 1]);
-                    if constexpr (SCALED) {
-                        a0 *= cs[2 * i];
-                        a1 *= cs[2 * i + 1];
-                    }
-                    pk[i] = pack_bf16x2(a0, a1);
+            for (int i = 0; i < 16; ++i) {
+                float a0 = __uint_as_float(v[2 * i]);
+                float a1 = __uint_as_float(v[2 * i + 1]);
+                if constexpr (EPI == EPI_BF16_Y) {
+                    a0 *= wr;
+                    a1 *= wr;
                 }
-                __nv_bfloat16 *dst =
-                    reinterpret_cast<__nv_bfloat16 *>(out) + (long long)tok * ld_out + col;
-                store_row_bf16(dst, pk, col, n_valid);
-            }
-        }
-    } else if constexpr (EPI == EPI_BF16) {
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(taddr + c0, v);
-            tmem_wait_ld();
-            if (row_ok) {
-                const int col = n_idx * BN + c0;
-                uint32_t pk[16];
-                float cs[32];
-                if constexpr (SCALED)
-                    chunk_scales(sc.b0 + c0, sc.a, col, n_valid, cs);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float a0 = __uint_as_float(v[2 * i]);
-                    float a1 = __uint_as_float(v[2 * i + 1]);
-                    if constexpr (SCALED) {
-                        a0 *= cs[2 * i];
-                        a1 *= cs[2 * i + 1];
-                    }
-                    pk[i] = pack_bf16x2(a0, a1);
+                if constexpr (SCALED) {
+                    a0 *= cs[2 * i];
+                    a1 *= cs[2 * i + 1];
                 }
-                __nv_bfloat16 *dst =
-                    reinterpret_cast<__nv_bfloat16 *>(out) + orow * ld_out + col;
-                store_row_bf16(dst, pk, col, n_valid);
+                pk[i] = pack_bf16x2(a0, a1);
             }
+            warp_store_chunk<16>(stile, pk, row_ok, row_base + (long long)col * 2,
+                                 chunk_valid_bytes(col, n_valid, 2), 2);
         }
     } else {
         constexpr int CH = BN < 32 ? 16 : 32;
@@ -432,7 +473,7 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
 #pragma unroll
                     for (int h = 0; h < CH; h += 32) {
                         float cs[32];
-                        chunk_scales(sc.b0 + c0 + h, sc.a, col + h, n_valid, cs);
+                        chunk_scales(sc.b0 + c0 + h, sc.a, cs);
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             v[h + i] = __float_as_uint(__uint_as_float(v[h + i]) * cs[i]);
@@ -653,11 +694,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             balance_loss_warp(p.aux);
         const int q = warp & 3;             // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;        // accumulator row of this thread
+        // this warp's staging tile for the stores and its column-scale
+        // buffer (warps 2-5)
+        uint8_t *stile = smem + S::EPI_OFF + (warp - 2) * 32 * kEpiRowBytes;
+        float *sbuf = reinterpret_cast<float *>(smem + S::EPI_OFF + 4 * 32 * kEpiRowBytes) +
+                      (warp - 2) * kEpiScaleFloats;
+        (void)sbuf;
         uint32_t b = 0, tph = 0;
         for (int u = blockIdx.x; u < ntiles; u += G) {
             const UnitInfo w = unit_info(p, s_seg, s_mt, u, ks_n, KSTEP);
             const TileInfo &ti = w.ti;
             const int ks = w.ks;
+            if constexpr (F8) {
+                // the tile's column scales into this warp's buffer while its
+                // accumulators are still being computed
+                const long long b0 = (long long)(w.second ? 0 : ti.seg * p.b_seg_rows) +
+                                     (long long)ti.n_idx * BN;
+                const int nv = w.second ? p.sh_N_valid : p.N_valid;
+                stage_col_scales((w.second ? p.sh_b_scale0 : p.b_scale0) + b0, ti.n_idx * BN, nv,
+                                 sbuf, BN);
+                if (NB == 2)
+                    stage_col_scales((w.second ? p.sh_b_scale1 : p.b_scale1) + b0,
+                                     ti.n_idx * BN, nv, sbuf + BN, BN);
+            }
             if (!mbar_wait(&tfull[b], tph, abort_flag, kWaitLimitNs)) {
                 *abort_flag = 1;
                 set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
@@ -671,11 +730,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             EpiScale sc{1.f, nullptr, nullptr};
             if constexpr (F8) {
                 const float *as = w.second ? p.sh_a_scale : p.a_scale;
-                const long long b0 = (long long)(w.second ? 0 : ti.seg * p.b_seg_rows) +
-                                     (long long)ti.n_idx * BN;
                 sc.a = row_ok ? __ldg(as + orow) : 0.f;
-                sc.b0 = (w.second ? p.sh_b_scale0 : p.b_scale0) + b0;
-                sc.b1 = NB == 2 ? (w.second ? p.sh_b_scale1 : p.b_scale1) + b0 : sc.b0;
+                sc.b0 = sbuf;
+                sc.b1 = NB == 2 ? sbuf + BN : sbuf;
             }
             if (w.second) {
                 if constexpr (EPI == EPI_BF16) {
@@ -684,14 +741,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                       taddr, row_ok, orow, ti.n_idx, ks, sc);
                     else
                         epilogue_row<BN, EPI, F8>(p, p.sh_out, p.sh_ld_out, p.sh_N_valid, taddr,
-                                                  row_ok, orow, ti.n_idx, ks, sc);
+                                                  row_ok, orow, ti.n_idx, ks, sc, stile);
                 } else {
                     epilogue_row<BN, EPI, F8>(p, p.sh_out, p.sh_ld_out, p.sh_N_valid, taddr,
-                                              row_ok, orow, ti.n_idx, ks, sc);
+                                              row_ok, orow, ti.n_idx, ks, sc, stile);
                 }
             } else
                 epilogue_row<BN, EPI, F8>(p, p.out, p.ld_out, p.N_valid, taddr, row_ok, orow,
-                                          ti.n_idx, ks, sc);
+                                          ti.n_idx, ks, sc, stile);
             tc_fence_before_sync();
             mbar_arrive(&tempty[b]);
             b ^= 1u;
@@ -748,7 +805,8 @@ struct PairShape {
     static constexpr int SWAP_KPS = (NB == 1 && B_HALF_ROWS == kTileM) ? 2 : 1;
     // token rows per swap unit: each CTA stages half of them per step
     static constexpr int SWAP_ROWS = 2 * TOK_BYTES / (SWAP_KPS * 128);
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + TABLE_BYTES + 1024;
+    static constexpr int EPI_OFF = (STAGES * STAGE_BYTES + 256 + TABLE_BYTES + 127) / 128 * 128;
+    static constexpr int SMEM_BYTES = EPI_OFF + kEpiStageBytes + 1024;
     static_assert(UMMA_N == 128 || UMMA_N == 256, "pair UMMA N");
     static_assert(NB == 1 || B_HALF_ROWS == BN, "gate/up halves");
     static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
@@ -1268,12 +1326,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             balance_loss_warp(p.aux);
         const int q = warp & 3;             // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;        // accumulator row of this thread
+        // this warp's staging tile for the stores and its column-scale
+        // buffer (warps 2-5)
+        uint8_t *stile = smem + S::EPI_OFF + (warp - 2) * 32 * kEpiRowBytes;
+        float *sbuf = reinterpret_cast<float *>(smem + S::EPI_OFF + 4 * 32 * kEpiRowBytes) +
+                      (warp - 2) * kEpiScaleFloats;
+        (void)sbuf;
         const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), 0);
         uint32_t b = 0, tph = 0;
         PairSched sched(cluster_id, NC, active ? n_full : 0, active ? n_swap : 0);
         bool sw;
         int g;
         while (sched.next(sw, g)) {
+            TileInfo ti{};
+            if (!sw) {
+                ti = pair_tile_info(p, s_seg, s_mt, g);
+                if constexpr (F8) {
+                    // the tile's column scales into this warp's buffer while
+                    // its accumulators are still being computed
+                    const long long b0 =
+                        (long long)ti.seg * p.b_seg_rows + (long long)ti.n_idx * BN;
+                    stage_col_scales(p.b_scale0 + b0, ti.n_idx * BN, p.N_valid, sbuf, BN);
+                    if (NB == 2)
+                        stage_col_scales(p.b_scale1 + b0, ti.n_idx * BN, p.N_valid, sbuf + BN,
+                                         BN);
+                }
+            }
             if (!mbar_wait(&tfull[b], tph, abort_flag, kWaitLimitNs)) {
                 *abort_flag = 1;
                 set_status(p.status, MOE_DEVICE_PIPELINE_TIMEOUT);
@@ -1282,20 +1360,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + b * S::UMMA_N + ((uint32_t)(q * 32) << 16);
             if (!sw) {
-                const TileInfo ti = pair_tile_info(p, s_seg, s_mt, g);
                 const int my_rows = ti.rows - (int)rank * kTileM;
                 const bool row_ok = r < my_rows;
                 const long long orow = (long long)ti.a_row0 + (int)rank * kTileM + r;
                 EpiScale sc{1.f, nullptr, nullptr};
                 if constexpr (F8) {
-                    const long long b0 =
-                        (long long)ti.seg * p.b_seg_rows + (long long)ti.n_idx * BN;
                     sc.a = row_ok ? __ldg(p.a_scale + orow) : 0.f;
-                    sc.b0 = p.b_scale0 + b0;
-                    sc.b1 = NB == 2 ? p.b_scale1 + b0 : sc.b0;
+                    sc.b0 = sbuf;
+                    sc.b1 = NB == 2 ? sbuf + BN : sbuf;
                 }
                 epilogue_row<BN, EPI, F8>(p, p.out, p.ld_out, p.N_valid, taddr, row_ok, orow,
-                                          ti.n_idx, 0, sc);
+                                          ti.n_idx, 0, sc, stile);
             } else {
                 const SwapInfo si = swap_info(s_seg, s_sw, p.nseg, n_fb, S::SWAP_ROWS, g);
                 swap_epilogue<EPI, F8>(p, taddr, q, lane, (int)rank, si);
