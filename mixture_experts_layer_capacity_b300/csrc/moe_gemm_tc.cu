@@ -334,12 +334,33 @@ __device__ __forceinline__ int chunk_valid_bytes(int col, int n_valid, int es)
     return max(0, min(32, n_valid - col)) * es;
 }
 
+// Stores a 32-column bf16 chunk of this lane's row (row_base: the row's
+// first byte).  E4M3 tiles (STAGED), whose epilogue runs about as long as
+// their short main loop, pass it through the warp's staging tile; bf16
+// tiles store their 64 contiguous bytes directly (their epilogue hides
+// behind the main loop, and staging measured slower for the small layers
+// whose last epilogue is on the critical path).
+template <bool STAGED>
+__device__ __forceinline__ void store_chunk_bf16(uint8_t *stile, const uint32_t (&pk)[16],
+                                                 bool row_ok, uint8_t *row_base, int col,
+                                                 int n_valid)
+{
+    if constexpr (STAGED) {
+        warp_store_chunk<16>(stile, pk, row_ok, row_base + (long long)col * 2,
+                             chunk_valid_bytes(col, n_valid, 2), 2);
+    } else {
+        if (row_ok)
+            store_row_bf16(reinterpret_cast<__nv_bfloat16 *>(row_base) + col, pk, col,
+                           n_valid);
+    }
+}
+
 // Epilogue of one accumulator row (TMEM lane) of a tile: this thread owns
 // output row `orow` (stored only when row_ok), columns n_idx*BN ... of the
 // tile.  taddr: TMEM address of the row's first accumulator column.
 // SCALED: E4M3 operands, the accumulator is multiplied by the row's and the
 // column's scales (sc) first.  stile: the warp's staging tile (all lanes of
-// the warp call this together; bf16 and fp32-h outputs are stored through
+// the warp call this together; the E4M3 tiles' outputs are stored through
 // it, whole row segments at a time).
 template <int BN, int EPI, bool SCALED = false>
 __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long long ld_out,
@@ -406,8 +427,7 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
                 }
                 pk[i] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
             }
-            warp_store_chunk<16>(stile, pk, row_ok, row_base + (long long)col * 2,
-                                 chunk_valid_bytes(col, n_valid, 2), 2);
+            store_chunk_bf16<SCALED>(stile, pk, row_ok, row_base, col, n_valid);
         }
     } else if constexpr (EPI == EPI_BF16_Y || EPI == EPI_BF16) {
         // EPI_BF16_Y: the row goes, times its gate weight, to its token's row of y
@@ -447,8 +467,7 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
                 }
                 pk[i] = pack_bf16x2(a0, a1);
             }
-            warp_store_chunk<16>(stile, pk, row_ok, row_base + (long long)col * 2,
-                                 chunk_valid_bytes(col, n_valid, 2), 2);
+            store_chunk_bf16<SCALED>(stile, pk, row_ok, row_base, col, n_valid);
         }
     } else {
         constexpr int CH = BN < 32 ? 16 : 32;
