@@ -144,3 +144,33 @@ def test_reference_arm_prints_one_line_on_rank_zero_only():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_shared_expert_placement_follows_the_launch_plan():
+    """Where the bench books the shared expert's GEMMs: inside the routed
+    launches (their stage) or in launches of their own."""
+    from mixture_experts_layer_capacity_b300 import binding as B
+
+    def placed(name):
+        w = WORKLOADS[name]
+        return bench.shared_in_routed(w, B.launch_plan(B.config_of(w)))
+
+    assert not placed("mixtral_decode")            # no shared expert
+    assert placed("qwen2_57b_decode")               # bf16, decode: fused tiles
+    assert not placed("dsv3_prefill")                # bf16, CTA pairs: own launches
+    assert placed("dsv3_decode_fp8")                 # E4M3 weights: always inside
+    assert placed("dsv3_decode_w8a8")                # E4M3 activations, few rows
+    assert not placed("dsv3_prefill_w8a8")           # E4M3 activations on pairs
+
+
+def test_e4m3_activation_traffic_counts_the_quantizers():
+    w = WORKLOADS["dsv3_prefill_w8a8"]
+    kept = w.T * w.k
+    act = bench.stage_activation_bytes(w, kept, shared_fused=False)
+    bf = bench.stage_activation_bytes(WORKLOADS["dsv3_prefill"], kept, shared_fused=True)
+    # the dispatch gathers 1-byte codes and a scale per row instead of bf16 rows
+    assert act["dispatch"] == kept * (w.D + 4) < bf["dispatch"]
+    # GEMM1 writes fp32 hidden rows and its quantizer reads them back
+    assert act["gemm1_routed"] >= kept * 8 * w.F
+    # the router stage quantizes every token row once
+    assert act["router"] > bf["router"]
