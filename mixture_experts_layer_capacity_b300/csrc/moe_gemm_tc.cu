@@ -18,10 +18,17 @@
 //     barriers and to the accumulator's "full" barrier;
 //   - warps 2-5: epilogue; each thread owns one accumulator row (TMEM lane),
 //     loads it with tcgen05.ld, applies SiLU*up (GEMM1) or converts, and
-//     stores straight to global memory, then frees the accumulator so the
-//     next tile's MMAs overlap this epilogue.
+//     stores it, then frees the accumulator so the next tile's MMAs overlap
+//     this epilogue.
 // For GEMM1 the gate and up tiles of the same columns are stacked in one
-// 256-row B operand, so one N=256 MMA produces both accumulators.
+// 256-row B operand, so one N=256 MMA produces both accumulators.  The
+// CTA-pair kernel (tc_gemm_pair_kernel, below) runs the same roles on
+// 256-row tiles with cta_group::2 MMAs.  Both kernels have an E4M3 form for
+// moe_forward_w8a8 (E4M3 token or hidden rows times E4M3 weights,
+// kind::f8f6f4 with 128-element reduction steps in the same 128-byte rows;
+// the epilogue scales by the row's and the weight row's fp32 scales and, as
+// its main loop is short, stages its output rows and column scales in shared
+// memory).
 // Every mbarrier wait is bounded; on timeout the CTA records
 // MOE_DEVICE_PIPELINE_TIMEOUT, drains its own copies and MMAs, frees TMEM and
 // returns.
@@ -1106,16 +1113,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_seg[i] = p.seg_off[i];
     __syncthreads();
     // pair tiles per segment (256 rows each, the last one padded) and, with
-    // swap units, the chunks of each segment of fewer than 256 rows (which
-    // then has no pair tile), prefix-summed by warp 0.  A segment with pair
-    // tiles keeps its remainder in a padded pair tile next to its other row
-    // tiles, so its weight tiles are still shared through L2.
+    // swap units, the chunks of each small segment (which then has no pair
+    // tile), prefix-summed by warp 0.  A segment with pair tiles keeps its
+    // remainder in a padded pair tile next to its other row tiles, so its
+    // weight tiles are still shared through L2.  Small: fewer than 256 rows
+    // in the gate/up GEMM; in the down projection at most one swap chunk
+    // (SWAP_ROWS, 64 rows for the wide form), since every chunk streams the
+    // expert's W_down rows again (DeepSeek-V3 prefill shape, same box: GEMM2
+    // 3.98 -> 3.81 ms in bf16, 2.10 -> 2.08 ms in E4M3, against the 256-row
+    // threshold; 32 rows or none was slower).
     if (p.mtile && !failed && warp == 0) {
         int carry = 0, carry_sw = 0;
         for (int e0 = 0; e0 < p.nseg; e0 += 32) {
             const int e = e0 + lane;
             const int n = e < p.nseg ? s_seg[e + 1] - s_seg[e] : 0;
-            const bool small = swap_mode && n < kPairRows;
+            const bool small = swap_mode && n < (NB == 2 ? kPairRows : S::SWAP_ROWS);
             const int v = small ? 0 : (n + kPairRows - 1) / kPairRows;
             const int vs = small ? (n + S::SWAP_ROWS - 1) / S::SWAP_ROWS : 0;
             int incl = v, incl_s = vs;

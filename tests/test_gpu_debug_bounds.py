@@ -34,13 +34,19 @@ cases = [
     ("empty_experts_e64", 300, 128, 64, 128, 8, 0, 2, 0.0, "zipf1.1"),
     ("pair_tails_e128", 8200, 128, 128, 192, 8, 0, 2, 0.0, "zipf1.1"),
     ("fp32_top1", 256, 64, 4, 128, 1, 32, 2, 1.0, "none"),
+    # E4M3 weights and activations: the dispatch gathers 1-byte codes
+    ("a8_swap_capacity", 200, 192, 16, 320, 4, 0, 1, 0.75, "normal_var2"),
+    ("a8_tiles_shared", 1000, 256, 8, 384, 2, 192, 0, 0.0, "none"),
 ]
 out = {}
 for name, T, D, E, F, k, S, mode, gamma, bias in cases:
+    a8 = name.startswith("a8")
     w = Workload(name, T=T, D=D, E=E, F=F, k=k, S=S, mode=mode, gamma=gamma,
-                 dtype="fp32" if name.startswith("fp32") else "bf16", alpha=0.01, bias=bias)
+                 dtype="fp32" if name.startswith("fp32") else "bf16", alpha=0.01, bias=bias,
+                 weights="e4m3" if a8 else "bf16", acts="e4m3" if a8 else "bf16")
     _, inp, outs, code = parity.run(w, seed=31)
-    rep = parity.check(w, inp, outs, coverage=T > 4096, y_sample_n=96 if T > 4096 else None)
+    rep = parity.check(w, inp, outs, coverage=T > 4096, y_sample_n=96 if T > 4096 else None,
+                       e4m3=a8, a8=a8)
     out[name] = dict(code=code, y_rel=rep["y_rel"],
                      y_sum=float(outs["y"].double().sum()))
 print("RESULT " + json.dumps(out))
