@@ -177,12 +177,14 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
 #define MOE_PLAN_PAIR_SHARED 8    /* shared-expert GEMMs on CTA pairs */
 #define MOE_PLAN_SHARED_FUSED 16  /* shared-expert tiles run inside the routed GEMM
                                      launches (no separate shared launches) */
-#define MOE_PLAN_PAIR_TAILS 32    /* with CTA pairs, each expert's rows past its last
-                                     full 256-row tile run as "swap" units in the
-                                     same launch: its weights are the MMA's 256-row
-                                     operand and those few token rows (rounded up
-                                     to 32) the other, so they are not padded to
-                                     256 rows */
+#define MOE_PLAN_PAIR_TAILS 32    /* with CTA pairs, the small experts (fewer rows
+                                     than one swap chunk: 128 in the gate/up GEMM,
+                                     64 or 128 in the down projection) run as
+                                     "swap" units in the same launch: their
+                                     weights are the MMA's 256-row operand and
+                                     their token rows (rounded up to 32) the
+                                     other, so they are not padded to 256 rows;
+                                     larger experts keep 256-row tiles */
 #define MOE_PLAN_W8A8_SWAP 64     /* moe_forward_w8a8 only: at most 64 rows per
                                      expert on average (T * k <= 64 * E), so its
                                      expert GEMMs take the weights as the 128-row

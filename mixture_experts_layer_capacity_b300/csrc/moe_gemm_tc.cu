@@ -84,10 +84,11 @@ struct TcParams {
     // main and the second problem; the accumulator is scaled by both
     const float *a_scale, *b_scale0, *b_scale1;
     const float *sh_a_scale, *sh_b_scale0, *sh_b_scale1;
-    // pair kernel, grouped: each segment's full 256-row tiles as usual, and
-    // its remaining rows (fewer than 256) as swap units in the same launch:
-    // the weights become the MMA's M = 256 operand and the few token rows
-    // its N operand (padded to a multiple of 32, not to 256 rows)
+    // pair kernel, grouped: each segment's 256-row tiles as usual, except
+    // that a small segment (fewer rows than one swap chunk) runs as swap
+    // units in the same launch: the weights become the MMA's M = 256
+    // operand and the few token rows its N operand (padded to a multiple of
+    // 32, not to 256 rows)
     int swap_tails;
 };
 
@@ -936,8 +937,8 @@ struct SwapInfo {
     int seg, fb, r0, rv, n;
 };
 
-// Swap unit u: chunk-major (a segment of fewer than 256 rows is cut into
-// chunks of swap_rows), feature block minor, so the units of one chunk run
+// Swap unit u: chunk-major (a small segment is one chunk of at most
+// swap_rows rows), feature block minor, so the units of one chunk run
 // at about the same time on neighbouring pairs and share its token rows in
 // L2.  s_sw: prefix sum of chunks per segment.
 __device__ __forceinline__ SwapInfo swap_info(const int *s_seg, const int *s_sw, int nseg,
@@ -1116,18 +1117,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // swap units, the chunks of each small segment (which then has no pair
     // tile), prefix-summed by warp 0.  A segment with pair tiles keeps its
     // remainder in a padded pair tile next to its other row tiles, so its
-    // weight tiles are still shared through L2.  Small: fewer than 256 rows
-    // in the gate/up GEMM; in the down projection at most one swap chunk
-    // (SWAP_ROWS, 64 rows for the wide form), since every chunk streams the
-    // expert's W_down rows again (DeepSeek-V3 prefill shape, same box: GEMM2
-    // 3.98 -> 3.81 ms in bf16, 2.10 -> 2.08 ms in E4M3, against the 256-row
-    // threshold; 32 rows or none was slower).
+    // weight tiles are still shared through L2.  Small: fewer rows than one
+    // swap chunk holds (SWAP_ROWS: 128 in the gate/up GEMM, 64 in the wide
+    // down projection), since every further chunk streams the expert's
+    // weight rows again while a padded pair tile streams them once per
+    // column tile (DeepSeek-V3 prefill shape, same box, alternating runs,
+    // against a 256-row threshold: GEMM1 7.29 -> 7.10 ms and GEMM2 3.98 ->
+    // 3.81 ms in bf16, GEMM1 3.88 -> 3.78 ms with E4M3 activations; 192 rows
+    // for GEMM1, 32 or none for GEMM2 were slower).
     if (p.mtile && !failed && warp == 0) {
         int carry = 0, carry_sw = 0;
         for (int e0 = 0; e0 < p.nseg; e0 += 32) {
             const int e = e0 + lane;
             const int n = e < p.nseg ? s_seg[e + 1] - s_seg[e] : 0;
-            const bool small = swap_mode && n < (NB == 2 ? kPairRows : S::SWAP_ROWS);
+            const bool small = swap_mode && n < S::SWAP_ROWS;
             const int v = small ? 0 : (n + kPairRows - 1) / kPairRows;
             const int vs = small ? (n + S::SWAP_ROWS - 1) / S::SWAP_ROWS : 0;
             int incl = v, incl_s = vs;
@@ -1681,9 +1684,9 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
             p.sh_ld_out = S;
         }
         if (pair_routed) {
-            // 256-row tiles on CTA pairs and, in the same launch, the
-            // experts with fewer than 256 rows as swap units: a 256-row tile
-            // over a few rows would compute mostly padding
+            // 256-row tiles on CTA pairs and, in the same launch, the small
+            // experts as swap units: a 256-row tile over a few rows would
+            // compute mostly padding
             SwapMaps sw;
             if (!make_map(&sw.w0, W_gate, (uint64_t)E * F, (uint64_t)D, kTileM) ||
                 !make_map(&sw.w1, W_up, (uint64_t)E * F, (uint64_t)D, kTileM) ||
@@ -1737,8 +1740,8 @@ cudaError_t launch_experts_tc(const moe_config &c, const WorkspaceLayout &L, uin
         }
         const SecondMaps *second = fused ? &sm : nullptr;
         long long tiles = (pair_routed ? mt2_bound : mt_bound) * p.n_tiles;
-        // pairs: 256-row tiles and the experts with fewer than 256 rows as
-        // swap units (W_down rows in 128-row boxes, h rows in 16-row boxes)
+        // pairs: 256-row tiles and the small experts as swap units (W_down
+        // rows in 128-row boxes, h rows in 16-row boxes)
         SwapMaps sw;
         if (pair_routed) {
             if (!make_map(&sw.w0, W_down, (uint64_t)E * D, (uint64_t)F, kTileM) ||
@@ -1873,8 +1876,8 @@ cudaError_t launch_dense_tc(int rows, int N, int K, const void *A, const void *B
 namespace {
 
 // launch_experts_w8a8 for layers large enough for CTA pairs (plan.pair_routed):
-// the routed GEMMs on the pair kernel (256-row tiles, experts under 256 rows
-// as swap units), the shared expert's GEMMs on their own launches (pairs
+// the routed GEMMs on the pair kernel (256-row tiles, small experts as swap
+// units), the shared expert's GEMMs on their own launches (pairs
 // when plan.pair_shared).
 cudaError_t experts_w8a8_pairs(const moe_config &c, const WorkspaceLayout &L, uint8_t *ws,
                                const ExpertW8 &w, void *y, const AuxArgs &aux,
