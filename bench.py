@@ -406,6 +406,27 @@ def workload_config(w):
             "inputs": "seeded synthetic, resident in HBM"}
 
 
+class nvtx_range:
+    """An NVTX range around a phase of the bench (seen by nsys or ncu's
+    NVTX filters; a no-op when no profiler is attached)."""
+
+    def __init__(self, name):
+        self.name = name
+
+    def __enter__(self):
+        try:
+            torch.cuda.nvtx.range_push(self.name)
+            self.pushed = True
+        except Exception:   # NVTX unavailable in this build
+            self.pushed = False
+        return self
+
+    def __exit__(self, *exc):
+        if self.pushed:
+            torch.cuda.nvtx.range_pop()
+        return False
+
+
 def run_ours(args, rank, world, device):
     w = WORKLOADS[args.workload]
     torch.cuda.set_device(device)
@@ -469,12 +490,13 @@ def run_ours(args, rank, world, device):
     barrier()
     clocks.start()
     wall0 = time.perf_counter()
-    for i in range(K):
-        evict(i)                                    # L2 between steps (above)
-        ev_s[i].record(stream)
-        graph.replay()
-        ev_e[i].record(stream)
-    barrier()
+    with nvtx_range("moe timed steps"):
+        for i in range(K):
+            evict(i)                                # L2 between steps (above)
+            ev_s[i].record(stream)
+            graph.replay()
+            ev_e[i].record(stream)
+        barrier()
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
 
@@ -497,15 +519,16 @@ def run_ours(args, rank, world, device):
     st_e = torch.cuda.Event(enable_timing=True)
     st_total = 0.0
     barrier()
-    for i in range(Ks):
-        evict(i)
-        st_s.record(stream)
-        graph_st.replay()
-        st_e.record(stream)
-        st_e.synchronize()                          # stage events are re-recorded each replay
-        st_total += st_s.elapsed_time(st_e)
-        for n, v in stage_ev.elapsed_ms().items():
-            stage_sum[n] += v
+    with nvtx_range("moe instrumented steps"):
+        for i in range(Ks):
+            evict(i)
+            st_s.record(stream)
+            graph_st.replay()
+            st_e.record(stream)
+            st_e.synchronize()                      # stage events are re-recorded each replay
+            st_total += st_s.elapsed_time(st_e)
+            for n, v in stage_ev.elapsed_ms().items():
+                stage_sum[n] += v
     stages = {n: v / Ks for n, v in stage_sum.items()}
     staged_ms = st_total / Ks
 
@@ -647,7 +670,8 @@ def run_ours(args, rank, world, device):
     e_end = torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
     s_up.wait_stream(stream)
-    e2e_steps(Ke)
+    with nvtx_range("moe end-to-end steps"):
+        e2e_steps(Ke)
     e_end.record(stream)
     barrier()
     t = torch.tensor([e_start.elapsed_time(e_end)], dtype=torch.float64, device=device)
