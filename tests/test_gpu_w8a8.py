@@ -196,3 +196,20 @@ def test_w8a8_benchmark_sized_prefill():
     print(w.name, rep)
     del inp, outs
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[3], PAIR[0]], ids=lambda c: c[0])
+def test_w8a8_runs_are_bit_identical(case):
+    """No float atomics and fixed reduction orders: two calls on the same
+    inputs give the same bits (tile, weights-as-M and CTA-pair forms)."""
+    name, T, D, E, F, k, S, mode, gamma, bias = case
+    w = Workload(name, T=T, D=D, E=E, F=F, k=k, S=S, mode=mode, gamma=gamma, dtype="bf16",
+                 alpha=0.01, bias=bias, weights="e4m3", acts="e4m3")
+    cfg = B.config_of(w)
+    inp = B.quantize_expert_weights(make_inputs(w, 37, "cuda"), a8=True)
+    a = B.forward(cfg, inp)
+    b = B.forward(cfg, inp)
+    torch.cuda.synchronize()
+    for key in ("y", "router_logits", "topk_idx", "topk_w", "dropped_mask", "expert_counts",
+                "kept_counts", "aux_loss"):
+        assert torch.equal(a[key], b[key]), key
