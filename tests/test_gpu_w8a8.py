@@ -213,3 +213,20 @@ def test_w8a8_runs_are_bit_identical(case):
     for key in ("y", "router_logits", "topk_idx", "topk_w", "dropped_mask", "expert_counts",
                 "kept_counts", "aux_loss"):
         assert torch.equal(a[key], b[key]), key
+
+
+@pytest.mark.parametrize("rows", [200, 9000], ids=["swap_form", "pair_form"])
+def test_w8a8_sigmoid_gating_with_selection_bias(rows):
+    """DeepSeek-V3's own gating (sigmoid scores normalised over the chosen
+    experts, a bias that shifts only the selection) with E4M3 activations,
+    in the weights-as-M form and on CTA pairs."""
+    w = Workload(f"a8_sigmoid_{rows}", T=rows, D=256, E=16, F=256, k=4, S=256, mode=3,
+                 gamma=0.0, dtype="bf16", alpha=0.01, bias="zipf1.1", sel_bias=True,
+                 weights="e4m3", acts="e4m3")
+    plan = B.launch_plan(B.config_of(w))
+    assert plan["w8a8_swap"] == (rows == 200) and plan["pair_routed"] == (rows == 9000)
+    _, inp, outs, code = parity.run(w, seed=41)
+    assert code == B.MOE_DEVICE_OK
+    _check_quantized_rows(w, inp, outs, max_rows=4096)
+    rep = parity.check(w, inp, outs, e4m3=True, a8=True, coverage=rows > 4096, y_sample_n=96)
+    print(w.name, rep)
