@@ -169,6 +169,24 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
                        float *aux_loss, void *workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* Per-unit timeline of the routed CTA-pair GEMMs, for profiling.  Only the
+ * library built with MOE_TIMELINE (libmoe_timeline.so; python -m
+ * mixture_experts_layer_capacity_b300.build --timeline) records it; other
+ * builds return MOE_ERR_UNSUPPORTED.  CTA 0 of each routed pair launch
+ * writes, for its i-th unit, 8 words of globaltimer nanoseconds at
+ * [region * 32768 + i * 8], region 0 for the gate/up GEMM and 1 for the down
+ * projection, i < 4096:
+ *   [0] the MMA thread starts waiting for a free accumulator, [1] it has one,
+ *   [2] the unit's first ring stage is full, [3] its last MMA is issued,
+ *   [7] the epilogue starts waiting for the accumulator, [4] it is full,
+ *   [5] the epilogue is done; [6] is 1 for a swap unit, 0 for a pair tile.
+ * Unwritten words stay 0.  moe_timeline_clear zeroes all 65536 words;
+ * moe_timeline_read copies the first n_words (<= 65536) to host memory.
+ * Both synchronise with the device. */
+#define MOE_TIMELINE_WORDS 65536
+MOE_API moe_status moe_timeline_clear(void);
+MOE_API moe_status moe_timeline_read(uint64_t *host_words, int64_t n_words);
+
 /* Which kernels moe_forward launches for `cfg` (for profiling and launch
  * counts; host only, no GPU needed).  *flags is a bit set of: */
 #define MOE_PLAN_ROUTER_FUSED 1   /* router GEMM inside the gating kernel */

@@ -110,6 +110,10 @@ def lib():
         L.moe_debug_barrier_fault.restype = ctypes.c_int
         L.moe_set_stage_events.argtypes = [vp, ctypes.c_int]
         L.moe_set_stage_events.restype = ctypes.c_int
+        L.moe_timeline_clear.argtypes = []
+        L.moe_timeline_clear.restype = ctypes.c_int
+        L.moe_timeline_read.argtypes = [vp, ctypes.c_int64]
+        L.moe_timeline_read.restype = ctypes.c_int
         L.moe_status_string.argtypes = [ctypes.c_int]
         L.moe_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -461,6 +465,28 @@ class StageEvents:
 
 
 # ---------------------------------------------------------------- convenience
+TIMELINE_WORDS = 65536
+
+
+def timeline_clear() -> None:
+    """Zero the per-unit timeline of the routed pair GEMMs (only the library
+    built with MOE_TIMELINE has one; others raise MOE_ERR_UNSUPPORTED)."""
+    st = lib().moe_timeline_clear()
+    if st != MOE_OK:
+        raise MoeError(st, "moe_timeline_clear")
+
+
+def timeline_read(n_words: int = TIMELINE_WORDS):
+    """The first n_words of the timeline as a numpy uint64 array (8 words per
+    unit: MMA and epilogue phase stamps, see include/moe.h)."""
+    import numpy as np
+    buf = np.zeros(n_words, dtype=np.uint64)
+    st = lib().moe_timeline_read(buf.ctypes.data, n_words)
+    if st != MOE_OK:
+        raise MoeError(st, "moe_timeline_read")
+    return buf
+
+
 def alloc_outputs(cfg: MoeConfig, device="cuda", d_outer: int = 0, a8: bool = False):
     """Output tensors and workspace for one call, allocated with torch
     (d_outer > 0: for moe_latent_forward, y at the outer width; a8: for

@@ -1,6 +1,6 @@
 """Build ``libmoe.so`` in-tree with nvcc for sm_103a.
 
-    python -m mixture_experts_layer_capacity_b300.build [--force] [--debug-bounds]
+    python -m mixture_experts_layer_capacity_b300.build [--force] [--debug-bounds | --timeline]
 
 Each ``csrc/*.cu`` compiles to an object under ``_build/`` (rebuilt when the
 source or any header is newer), then the objects link into
@@ -13,6 +13,12 @@ runtime's entry-point query, so libcuda is not linked.
 expert and row index against its range and record
 MOE_DEVICE_INDEX_OUT_OF_RANGE instead of making the access.  Load it by
 setting ``MOE_LIBRARY`` to its path before the binding is first used.
+
+``--timeline`` builds them with ``-DMOE_TIMELINE`` into
+``libmoe_timeline.so``: CTA 0 of every routed CTA-pair GEMM launch then
+stamps each unit's MMA and epilogue phases with the global timer, read back
+with ``moe_timeline_read`` (``timeline.py`` prints them).  The stamps cost a
+few stores per unit, so this library is for profiling, not for timing.
 """
 from __future__ import annotations
 
@@ -29,6 +35,8 @@ BUILD = os.path.join(ROOT, "_build", "libmoe")
 LIB = os.path.join(PKG, "libmoe.so")
 BUILD_DEBUG = os.path.join(ROOT, "_build", "libmoe_debug_bounds")
 LIB_DEBUG = os.path.join(PKG, "libmoe_debug_bounds.so")
+BUILD_TIMELINE = os.path.join(ROOT, "_build", "libmoe_timeline")
+LIB_TIMELINE = os.path.join(PKG, "libmoe_timeline.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
@@ -44,9 +52,16 @@ def _newest(paths):
     return max((os.path.getmtime(p) for p in paths), default=0.0)
 
 
-def build(force: bool = False, verbose: bool = False, debug_bounds: bool = False) -> str:
-    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug_bounds else (BUILD, LIB)
-    flags = FLAGS + (["-DMOE_DEBUG_BOUNDS"] if debug_bounds else [])
+def build(force: bool = False, verbose: bool = False, debug_bounds: bool = False,
+          timeline: bool = False) -> str:
+    if debug_bounds and timeline:
+        raise ValueError("debug_bounds and timeline are separate builds")
+    if debug_bounds:
+        build_dir, lib, flags = BUILD_DEBUG, LIB_DEBUG, FLAGS + ["-DMOE_DEBUG_BOUNDS"]
+    elif timeline:
+        build_dir, lib, flags = BUILD_TIMELINE, LIB_TIMELINE, FLAGS + ["-DMOE_TIMELINE"]
+    else:
+        build_dir, lib, flags = BUILD, LIB, FLAGS
     os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr_time = _newest(_headers())
@@ -80,4 +95,4 @@ def build(force: bool = False, verbose: bool = False, debug_bounds: bool = False
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True,
-                debug_bounds="--debug-bounds" in sys.argv))
+                debug_bounds="--debug-bounds" in sys.argv, timeline="--timeline" in sys.argv))

@@ -18,6 +18,15 @@ constexpr bool kDebugBounds = true;
 constexpr bool kDebugBounds = false;
 #endif
 
+// Builds with MOE_TIMELINE record, for CTA 0 of every routed CTA-pair GEMM
+// launch, globaltimer stamps of each unit's MMA and epilogue phases
+// (moe_timeline_read); other builds record nothing.
+#ifdef MOE_TIMELINE
+constexpr bool kTimeline = true;
+#else
+constexpr bool kTimeline = false;
+#endif
+
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 

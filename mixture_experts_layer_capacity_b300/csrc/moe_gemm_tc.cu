@@ -46,6 +46,17 @@
 
 namespace moe {
 
+// Per-unit timeline of the routed pair GEMMs (builds with MOE_TIMELINE; see
+// moe_timeline_read): 2 regions x 4096 units x 8 words, region 1 for the
+// down projection.
+constexpr int kTimelineUnits = 4096;
+static_assert(2 * kTimelineUnits * 8 == MOE_TIMELINE_WORDS, "timeline layout");
+#ifdef MOE_TIMELINE
+__device__ unsigned long long g_timeline[MOE_TIMELINE_WORDS];
+#else
+__device__ unsigned long long g_timeline[8];
+#endif
+
 // Epilogues: fp32 store (router scores), bf16 store (z), SiLU(gate) * up in
 // bf16 (h), bf16 store of w_row * acc straight into the row's token of y
 // (down projection when every token has one expert and no shared expert),
@@ -1282,7 +1293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             PairSched sched(cluster_id, NC, active ? n_full : 0, active ? n_swap : 0);
             bool sw;
             int g;
+            int tl_i = 0;
             while (ok && sched.next(sw, g)) {
+                const uint64_t tl0 = kTimeline ? global_timer_ns() : 0;
                 uint32_t idesc = idesc_full;
                 if (sw) {
                     const SwapInfo si = swap_info(s_seg, s_sw, p.nseg, n_fb, S::SWAP_ROWS, g);
@@ -1293,6 +1306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
+                const uint64_t tl1 = kTimeline ? global_timer_ns() : 0;
+                uint64_t tl2 = 0;
                 const uint32_t d_tmem = tmem_base + b * S::UMMA_N;
                 const int n_stages = sw ? (nk + S::SWAP_KPS - 1) / S::SWAP_KPS : nk;
                 for (int st = 0; st < n_stages; ++st) {
@@ -1301,6 +1316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
+                    if (kTimeline && st == 0)
+                        tl2 = global_timer_ns();
                     const uint32_t sa = smem_u32(smem + s * S::STAGE_BYTES);
                     if (!sw) {
                         const uint64_t adesc = sdesc_kmajor_sw128(sa);
@@ -1343,6 +1360,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok)
                     break;
+                if constexpr (kTimeline) {
+                    if (blockIdx.x == 0 && p.mtile && tl_i < kTimelineUnits) {
+                        unsigned long long *rec =
+                            g_timeline + (EPI == EPI_BF16 || EPI == EPI_BF16_Y ? kTimelineUnits * 8 : 0) +
+                            tl_i * 8;
+                        rec[0] = tl0;
+                        rec[1] = tl1;
+                        rec[2] = tl2;
+                        rec[3] = global_timer_ns();
+                        rec[6] = sw ? 1 : 0;
+                    }
+                    ++tl_i;
+                }
                 umma_commit_pair(&tfull[b], 0x3);
                 b ^= 1u;
                 if (b == 0)
@@ -1373,7 +1403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         PairSched sched(cluster_id, NC, active ? n_full : 0, active ? n_swap : 0);
         bool sw;
         int g;
+        int tl_e = 0;
         while (sched.next(sw, g)) {
+            const uint64_t te0 = kTimeline ? global_timer_ns() : 0;
             TileInfo ti{};
             if (!sw) {
                 ti = pair_tile_info(p, s_seg, s_mt, g);
@@ -1395,6 +1427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + b * S::UMMA_N + ((uint32_t)(q * 32) << 16);
+            const uint64_t te1 = kTimeline ? global_timer_ns() : 0;
             if (!sw) {
                 const int my_rows = ti.rows - (int)rank * kTileM;
                 const bool row_ok = r < my_rows;
@@ -1410,6 +1443,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 const SwapInfo si = swap_info(s_seg, s_sw, p.nseg, n_fb, S::SWAP_ROWS, g);
                 swap_epilogue<EPI, F8>(p, taddr, q, lane, (int)rank, si);
+            }
+            if constexpr (kTimeline) {
+                if (blockIdx.x == 0 && p.mtile && warp == 2 && lane == 0 && tl_e < kTimelineUnits) {
+                    unsigned long long *rec =
+                        g_timeline + (EPI == EPI_BF16 || EPI == EPI_BF16_Y ? kTimelineUnits * 8 : 0) +
+                        tl_e * 8;
+                    rec[4] = te1;
+                    rec[5] = global_timer_ns();
+                    rec[7] = te0;
+                }
+                ++tl_e;
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -2202,3 +2246,24 @@ cudaError_t launch_experts_w8a8(const moe_config &c, const WorkspaceLayout &L, u
 }
 
 }  // namespace moe
+
+extern "C" moe_status moe_timeline_clear(void)
+{
+    if (!moe::kTimeline)
+        return MOE_ERR_UNSUPPORTED;
+    static const unsigned long long zero[MOE_TIMELINE_WORDS] = {};
+    return cudaMemcpyToSymbol(moe::g_timeline, zero, sizeof(zero)) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}
+
+extern "C" moe_status moe_timeline_read(uint64_t *host_words, int64_t n_words)
+{
+    if (!moe::kTimeline)
+        return MOE_ERR_UNSUPPORTED;
+    if (!host_words || n_words < 0 || n_words > MOE_TIMELINE_WORDS)
+        return MOE_ERR_INVALID_ARG;
+    return cudaMemcpyFromSymbol(host_words, moe::g_timeline, (size_t)n_words * 8) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}

@@ -228,6 +228,19 @@ def test_debug_bounds_build_exports_the_same_symbols():
 
     assert exported(dbg) == exported(B.LIB_PATH)
     assert set(_declared_symbols()) <= set(exported(dbg))
+    tl = build.build(timeline=True)
+    assert exported(tl) == exported(B.LIB_PATH)
+
+
+def test_timeline_is_unsupported_outside_its_build():
+    """Only libmoe_timeline.so records the pair GEMMs' unit timeline; the
+    normal library refuses both calls before touching the device."""
+    L = B.lib()
+    assert L.moe_timeline_clear() == B.MOE_ERR_UNSUPPORTED
+    buf = np.zeros(8, dtype=np.uint64)
+    assert L.moe_timeline_read(buf.ctypes.data, 8) == B.MOE_ERR_UNSUPPORTED
+    with pytest.raises(B.MoeError):
+        B.timeline_read(8)
 
 
 def _call_w8a8(cfg, ws, ws_bytes, shared=True):
