@@ -303,17 +303,44 @@ __device__ __forceinline__ void chunk_scales(const float *sb, float a, float (&c
     }
 }
 
+// The rows a lane stores in warp_store_chunk: with PPR 16-byte pieces per
+// row, pass `it` of a chunk stores piece lane % PPR of the warp's row
+// it * (32 / PPR) + lane / PPR.  Those rows' first bytes and validity are
+// fetched from their lanes once per tile (warp_rows), not once per chunk.
+template <int PPR>
+struct WarpRows {
+    uint8_t *base[PPR];
+    uint32_t ok;   // bit `it`: pass it's row is inside the tile
+};
+
+template <int PPR>
+__device__ __forceinline__ WarpRows<PPR> warp_rows(uint8_t *row_base, bool row_ok)
+{
+    const int lane = threadIdx.x & 31;
+    WarpRows<PPR> w;
+    w.ok = 0;
+#pragma unroll
+    for (int it = 0; it < PPR; ++it) {
+        const int r = it * (32 / PPR) + lane / PPR;
+        w.base[it] = reinterpret_cast<uint8_t *>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(row_base), r));
+        w.ok |= (__shfl_sync(0xffffffffu, row_ok ? 1u : 0u, r) & 1u) << it;
+    }
+    return w;
+}
+
 // Stores one 32-column chunk of the warp's 32 rows: each lane holds its own
-// row's NW packed words (w) and that row's destination (dst, valid when
-// row_ok); the words pass through the warp's staging tile so that each
-// store instruction writes whole 64- or 128-byte row segments (4 or 8 lanes
-// per row) instead of one 16-byte piece of 32 different rows.  valid_bytes:
-// bytes of each row inside the output's columns (<= NW * 4); es: element
-// size (2 or 4) for a ragged tail.  Every lane of the warp calls it.
+// row's NW packed words (w); the words pass through the warp's staging tile
+// so that each store instruction writes whole 64- or 128-byte row segments
+// (4 or 8 lanes per row) instead of one 16-byte piece of 32 different rows.
+// rows: the destinations (warp_rows of each row's first byte); off: the
+// chunk's byte offset in its row; valid_bytes: bytes of each row inside the
+// output's columns (<= NW * 4); es: element size (2 or 4) for a ragged tail.
+// Every lane of the warp calls it.
 template <int NW>
 __device__ __forceinline__ void warp_store_chunk(uint8_t *stile, const uint32_t (&w)[NW],
-                                                 bool row_ok, uint8_t *dst, int valid_bytes,
-                                                 int es)
+                                                 const WarpRows<NW / 4> &rows, long long off,
+                                                 int valid_bytes, int es)
 {
     constexpr int PPR = NW / 4;                 // 16-byte pieces per row
     const int lane = threadIdx.x & 31;
@@ -322,17 +349,14 @@ __device__ __forceinline__ void warp_store_chunk(uint8_t *stile, const uint32_t 
     for (int j = 0; j < PPR; ++j)
         srow[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
     __syncwarp();
+    const int c = lane % PPR;
 #pragma unroll
     for (int it = 0; it < PPR; ++it) {
-        const int piece = it * 32 + lane;
-        const int r = piece / PPR, c = piece - (piece / PPR) * PPR;
-        uint8_t *d = reinterpret_cast<uint8_t *>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(dst), r));
-        const bool ok = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, r) != 0;
-        if (!ok || c * 16 >= valid_bytes)
+        if (!((rows.ok >> it) & 1u) || c * 16 >= valid_bytes)
             continue;
+        const int r = it * (32 / PPR) + lane / PPR;
         const uint8_t *src = stile + r * kEpiRowBytes + c * 16;
-        uint8_t *g = d + c * 16;
+        uint8_t *g = rows.base[it] + off + c * 16;
         if ((c + 1) * 16 <= valid_bytes && (reinterpret_cast<uintptr_t>(g) & 15) == 0) {
             *reinterpret_cast<uint4 *>(g) = *reinterpret_cast<const uint4 *>(src);
         } else if (es == 2) {
@@ -361,11 +385,11 @@ __device__ __forceinline__ int chunk_valid_bytes(int col, int n_valid, int es)
 // whose last epilogue is on the critical path).
 template <bool STAGED>
 __device__ __forceinline__ void store_chunk_bf16(uint8_t *stile, const uint32_t (&pk)[16],
-                                                 bool row_ok, uint8_t *row_base, int col,
-                                                 int n_valid)
+                                                 const WarpRows<4> &rows, bool row_ok,
+                                                 uint8_t *row_base, int col, int n_valid)
 {
     if constexpr (STAGED) {
-        warp_store_chunk<16>(stile, pk, row_ok, row_base + (long long)col * 2,
+        warp_store_chunk<16>(stile, pk, rows, (long long)col * 2,
                              chunk_valid_bytes(col, n_valid, 2), 2);
     } else {
         if (row_ok)
@@ -391,6 +415,7 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
     if constexpr (EPI == EPI_SWIGLU_F32) {
         uint8_t *row_base =
             reinterpret_cast<uint8_t *>(reinterpret_cast<float *>(out) + orow * ld_out);
+        const WarpRows<8> rows = warp_rows<8>(row_base, row_ok);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
             uint32_t gv[32], uv[32];
@@ -413,12 +438,15 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
                 }
                 hw[i] = __float_as_uint(silu_f32(g) * u);
             }
-            warp_store_chunk<32>(stile, hw, row_ok, row_base + (long long)col * 4,
+            warp_store_chunk<32>(stile, hw, rows, (long long)col * 4,
                                  chunk_valid_bytes(col, n_valid, 4), 4);
         }
     } else if constexpr (EPI == EPI_SWIGLU) {
         uint8_t *row_base = reinterpret_cast<uint8_t *>(
             reinterpret_cast<__nv_bfloat16 *>(out) + orow * ld_out);
+        WarpRows<4> rows{};
+        if constexpr (SCALED)
+            rows = warp_rows<4>(row_base, row_ok);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
             uint32_t gv[32], uv[32];
@@ -446,7 +474,7 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
                 }
                 pk[i] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
             }
-            store_chunk_bf16<SCALED>(stile, pk, row_ok, row_base, col, n_valid);
+            store_chunk_bf16<SCALED>(stile, pk, rows, row_ok, row_base, col, n_valid);
         }
     } else if constexpr (EPI == EPI_BF16_Y || EPI == EPI_BF16) {
         // EPI_BF16_Y: the row goes, times its gate weight, to its token's row of y
@@ -462,31 +490,62 @@ __device__ __forceinline__ void epilogue_row(const TcParams &p, void *out, long 
         const long long drow = EPI == EPI_BF16_Y ? (long long)tok : orow;
         uint8_t *row_base = reinterpret_cast<uint8_t *>(
             reinterpret_cast<__nv_bfloat16 *>(out) + drow * ld_out);
+        if constexpr (SCALED) {
+            // E4M3 tiles: 64 columns per pass, so that each staged store
+            // instruction writes four whole 128-byte row segments (with 32
+            // columns, eight half segments: the down projection's 256-column
+            // tiles then drained slowly enough to hold up the next tile's
+            // MMAs)
+            static_assert(BN % 64 == 0, "E4M3 bf16 tiles are multiples of 64 columns");
+            const WarpRows<8> rows = warp_rows<8>(row_base, row_ok);
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(taddr + c0, v);
-            tmem_wait_ld();
-            const int col = n_idx * BN + c0;
-            uint32_t pk[16];
-            float cs[32];
-            if constexpr (SCALED)   // sc.a is 0 for rows outside the tile
-                chunk_scales(sc.b0 + c0, sc.a, cs);
+            for (int c0 = 0; c0 < BN; c0 += 64) {
+                uint32_t v[2][32];
+                tmem_ld32(taddr + c0, v[0]);
+                tmem_ld32(taddr + c0 + 32, v[1]);
+                tmem_wait_ld();
+                uint32_t pk[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float a0 = __uint_as_float(v[2 * i]);
-                float a1 = __uint_as_float(v[2 * i + 1]);
-                if constexpr (EPI == EPI_BF16_Y) {
-                    a0 *= wr;
-                    a1 *= wr;
+                for (int h = 0; h < 2; ++h) {
+                    float cs[32];   // sc.a is 0 for rows outside the tile
+                    chunk_scales(sc.b0 + c0 + 32 * h, sc.a, cs);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float a0 = __uint_as_float(v[h][2 * i]);
+                        float a1 = __uint_as_float(v[h][2 * i + 1]);
+                        if constexpr (EPI == EPI_BF16_Y) {
+                            a0 *= wr;
+                            a1 *= wr;
+                        }
+                        pk[16 * h + i] = pack_bf16x2(a0 * cs[2 * i], a1 * cs[2 * i + 1]);
+                    }
                 }
-                if constexpr (SCALED) {
-                    a0 *= cs[2 * i];
-                    a1 *= cs[2 * i + 1];
-                }
-                pk[i] = pack_bf16x2(a0, a1);
+                const int col = n_idx * BN + c0;
+                warp_store_chunk<32>(stile, pk, rows, (long long)col * 2,
+                                     max(0, min(64, n_valid - col)) * 2, 2);
             }
-            store_chunk_bf16<SCALED>(stile, pk, row_ok, row_base, col, n_valid);
+        } else {
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(taddr + c0, v);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float a0 = __uint_as_float(v[2 * i]);
+                    float a1 = __uint_as_float(v[2 * i + 1]);
+                    if constexpr (EPI == EPI_BF16_Y) {
+                        a0 *= wr;
+                        a1 *= wr;
+                    }
+                    pk[i] = pack_bf16x2(a0, a1);
+                }
+                const int col = n_idx * BN + c0;
+                if (row_ok)
+                    store_row_bf16(reinterpret_cast<__nv_bfloat16 *>(row_base) + col, pk, col,
+                                   n_valid);
+            }
         }
     } else {
         constexpr int CH = BN < 32 ? 16 : 32;
