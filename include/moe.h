@@ -178,11 +178,14 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
  * projection, i < 4096:
  *   [0] the MMA thread starts waiting for a free accumulator, [1] it has one,
  *   [2] the unit's first ring stage is full, [3] its last MMA is issued,
- *   [7] the epilogue starts waiting for the accumulator, [4] it is full,
- *   [5] the epilogue is done; [6] is 1 for a swap unit, 0 for a pair tile.
- * Unwritten words stay 0.  moe_timeline_clear zeroes all 65536 words;
- * moe_timeline_read copies the first n_words (<= 65536) to host memory.
- * Both synchronise with the device. */
+ *   [7] the epilogue starts the unit (E4M3 tiles first copy their column
+ *   scales) and waits for the accumulator, [4] it is full, [5] the epilogue
+ *   is done; [6] is 1 for a swap unit, 0 for a pair tile.
+ * Unwritten words stay 0; a later launch of the same GEMM overwrites the
+ * records, so read them after the forward pass of interest.
+ * moe_timeline_clear zeroes all 65536 words; moe_timeline_read copies the
+ * first n_words (<= 65536) to host memory.  Both synchronise with the
+ * device. */
 #define MOE_TIMELINE_WORDS 65536
 MOE_API moe_status moe_timeline_clear(void);
 MOE_API moe_status moe_timeline_read(uint64_t *host_words, int64_t n_words);
