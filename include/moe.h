@@ -169,24 +169,30 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
                        float *aux_loss, void *workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
-/* Per-unit timeline of the routed CTA-pair GEMMs, for profiling.  Only the
- * library built with MOE_TIMELINE (libmoe_timeline.so; python -m
- * mixture_experts_layer_capacity_b300.build --timeline) records it; other
- * builds return MOE_ERR_UNSUPPORTED.  CTA 0 of each routed pair launch
- * writes, for its i-th unit, 8 words of globaltimer nanoseconds at
- * [region * 32768 + i * 8], region 0 for the gate/up GEMM and 1 for the down
- * projection, i < 4096:
+/* Per-unit timeline of the routed CTA-pair GEMMs and per-block timeline of
+ * the dispatch kernel, for profiling.  Only the library built with
+ * MOE_TIMELINE (libmoe_timeline.so; python -m
+ * mixture_experts_layer_capacity_b300.build --timeline) records them; other
+ * builds return MOE_ERR_UNSUPPORTED.  All words are globaltimer
+ * nanoseconds.  CTA 0 of each routed pair launch writes, for its i-th unit,
+ * 8 words at [region * 32768 + i * 8], region 0 for the gate/up GEMM and 1
+ * for the down projection, i < 4096:
  *   [0] the MMA thread starts waiting for a free accumulator, [1] it has one,
  *   [2] the unit's first ring stage is full, [3] its last MMA is issued,
  *   [7] the epilogue starts the unit (E4M3 tiles first copy their column
  *   scales) and waits for the accumulator, [4] it is full, [5] the epilogue
  *   is done; [6] is 1 for a swap unit, 0 for a pair tile.
- * Unwritten words stay 0; a later launch of the same GEMM overwrites the
+ * Dispatch block b < 4096 writes 8 words at [65536 + b * 8]: [0] its start,
+ * [1] its rows staged, [2] its router scores done, [3] its tokens gated
+ * (these three for its first chunk of tokens; equal to [0] for a block
+ * without tokens), [4] its gating done, [5] past the grid barrier, [6] the
+ * segment tables done, [7] its last row copy done.
+ * Unwritten words stay 0; a later launch of the same kernel overwrites the
  * records, so read them after the forward pass of interest.
- * moe_timeline_clear zeroes all 65536 words; moe_timeline_read copies the
- * first n_words (<= 65536) to host memory.  Both synchronise with the
+ * moe_timeline_clear zeroes all 98304 words; moe_timeline_read copies the
+ * first n_words (<= 98304) to host memory.  Both synchronise with the
  * device. */
-#define MOE_TIMELINE_WORDS 65536
+#define MOE_TIMELINE_WORDS 98304
 MOE_API moe_status moe_timeline_clear(void);
 MOE_API moe_status moe_timeline_read(uint64_t *host_words, int64_t n_words);
 

@@ -465,7 +465,7 @@ class StageEvents:
 
 
 # ---------------------------------------------------------------- convenience
-TIMELINE_WORDS = 65536
+TIMELINE_WORDS = 98304
 
 
 def timeline_clear() -> None:

@@ -38,6 +38,7 @@
 // C are dropped by that expert only); "Mixture of Experts: Sparse FFNs,
 // Routers, and Shared Experts" ('Capacity factor'); "Mixture of experts"
 // (frontiers track), gate equation of 'Where the experts live'.
+#include <algorithm>
 #include <atomic>
 #include <cfloat>
 #include <climits>
@@ -112,6 +113,23 @@ struct DispatchParams {
     const float *gscale;
     float *gscale_perm;
 };
+
+// Phase stamps of each dispatch block (builds with MOE_TIMELINE; read
+// through moe_timeline_read): 8 global-timer words per block, block < 4096.
+constexpr int kDispatchTimelineBlocks = 4096;
+#ifdef MOE_TIMELINE
+__device__ unsigned long long g_dispatch_timeline[kDispatchTimelineBlocks * 8];
+#else
+__device__ unsigned long long g_dispatch_timeline[8];
+#endif
+
+__device__ __forceinline__ void dispatch_stamp(int word)
+{
+    if constexpr (kTimeline) {
+        if (threadIdx.x == 0 && blockIdx.x < kDispatchTimelineBlocks)
+            g_dispatch_timeline[blockIdx.x * 8 + word] = global_timer_ns();
+    }
+}
 
 // ------------------------------------------------------------ block helpers
 // Exclusive scan over the block (blockDim.x a multiple of 32, <= 1024);
@@ -733,6 +751,18 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
     // a one-chunk block keeps its assignments in shared memory from phase 1
     // to phase 2 when both run in this launch
     const bool held = gate && p.cpb == 1;
+    // timeline: [0] start; [1] rows staged, [2] router done, [3] tokens
+    // gated (the block's first chunk; a block without chunks keeps [0]);
+    // [4] phase 1 done, [5] past the grid barrier, [6] segment tables done,
+    // [7] the block's last copy warp done
+    if constexpr (kTimeline) {
+        if (threadIdx.x == 0 && b < kDispatchTimelineBlocks) {
+            const unsigned long long t0 = global_timer_ns();
+            unsigned long long *rec = g_dispatch_timeline + b * 8;
+            rec[0] = rec[1] = rec[2] = rec[3] = t0;
+            rec[7] = 0;
+        }
+    }
 
     // W_r (fused router) and this block's x rows (when staged) into shared
     // memory, four 16-byte loads in flight per thread
@@ -772,6 +802,8 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             mask[e] = 0u;
         __syncthreads();
+        if (chunk == c_beg)
+            dispatch_stamp(1);
         // fused router: on the tensor cores for staged bf16 rows, else on
         // the CUDA cores with 32 / cs warps per token, each over a slice of D
         const bool mma_router = RT == ROUTER_BF16 && p.x_staged && cs >= 8;
@@ -796,6 +828,8 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
             }
             __syncthreads();
         }
+        if (chunk == c_beg)
+            dispatch_stamp(2);
         const int t = chunk * cs + warp;
         if (warp < cs) {
             if (t < p.T) {
@@ -811,6 +845,8 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
             }
         }
         __syncthreads();
+        if (chunk == c_beg)
+            dispatch_stamp(3);
         // ranks: tokens of earlier chunks of this block (run, before this
         // chunk's counts are added) plus earlier tokens of this chunk
         for (int i = threadIdx.x; i < cs * k; i += blockDim.x) {
@@ -838,6 +874,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
             run[e] += __popc(mask[e]);
     }
     __syncthreads();
+    dispatch_stamp(4);
     if (gate) {
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             p.bcount[(size_t)e * G + b] = run[e];
@@ -847,6 +884,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
                           p.barrier_limit_ns))
             return;
     }
+    dispatch_stamp(5);
 
     // ---- phase 2a: per expert, tokens of earlier blocks and the total
     // (warp w: experts w, w+32, ..., four at a time)
@@ -955,6 +993,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
         }
     }
     __syncthreads();
+    dispatch_stamp(6);
 
     // ---- phase 2c/2d: the last warp computes this block's probability sums;
     // the other warps place the block's assignments and copy x into x_perm
@@ -1017,6 +1056,10 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(DispatchP
             for (size_t v = (size_t)part * 32 + lane; v < p.row_bytes / 16; v += (size_t)nparts * 32)
                 dst[v] = make_uint4(0u, 0u, 0u, 0u);
         }
+    }
+    if constexpr (kTimeline) {
+        if (lane == 0 && b < kDispatchTimelineBlocks)
+            atomicMax(g_dispatch_timeline + b * 8 + 7, (unsigned long long)global_timer_ns());
     }
 }
 
@@ -1244,6 +1287,18 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
         return launch_dispatch_s<2>(c, p, false, wr_bytes, stream);
     return split == 1 ? launch_dispatch_s<1>(c, p, fused, wr_bytes, stream)
                       : launch_dispatch_s<0>(c, p, fused, wr_bytes, stream);
+}
+
+cudaError_t dispatch_timeline_copy(uint64_t *host, size_t words)
+{
+    return cudaMemcpyFromSymbol(host, g_dispatch_timeline,
+                                std::min(words, sizeof(g_dispatch_timeline) / 8) * 8);
+}
+
+cudaError_t dispatch_timeline_clear()
+{
+    static const unsigned long long zero[sizeof(g_dispatch_timeline) / 8] = {};
+    return cudaMemcpyToSymbol(g_dispatch_timeline, zero, sizeof(zero));
 }
 
 }  // namespace moe

@@ -50,9 +50,10 @@ namespace moe {
 // moe_timeline_read): 2 regions x 4096 units x 8 words, region 1 for the
 // down projection.
 constexpr int kTimelineUnits = 4096;
-static_assert(2 * kTimelineUnits * 8 == MOE_TIMELINE_WORDS, "timeline layout");
+constexpr int kTimelineGemmWords = 2 * kTimelineUnits * 8;
+static_assert(kTimelineGemmWords + 4096 * 8 == MOE_TIMELINE_WORDS, "timeline layout");
 #ifdef MOE_TIMELINE
-__device__ unsigned long long g_timeline[MOE_TIMELINE_WORDS];
+__device__ unsigned long long g_timeline[2 * 4096 * 8];
 #else
 __device__ unsigned long long g_timeline[8];
 #endif
@@ -2310,8 +2311,9 @@ extern "C" moe_status moe_timeline_clear(void)
 {
     if (!moe::kTimeline)
         return MOE_ERR_UNSUPPORTED;
-    static const unsigned long long zero[MOE_TIMELINE_WORDS] = {};
-    return cudaMemcpyToSymbol(moe::g_timeline, zero, sizeof(zero)) == cudaSuccess
+    static const unsigned long long zero[2 * 4096 * 8] = {};
+    return cudaMemcpyToSymbol(moe::g_timeline, zero, sizeof(zero)) == cudaSuccess &&
+                   moe::dispatch_timeline_clear() == cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;
 }
@@ -2322,7 +2324,11 @@ extern "C" moe_status moe_timeline_read(uint64_t *host_words, int64_t n_words)
         return MOE_ERR_UNSUPPORTED;
     if (!host_words || n_words < 0 || n_words > MOE_TIMELINE_WORDS)
         return MOE_ERR_INVALID_ARG;
-    return cudaMemcpyFromSymbol(host_words, moe::g_timeline, (size_t)n_words * 8) == cudaSuccess
-               ? MOE_OK
-               : MOE_ERR_CUDA;
+    const int64_t g = std::min<int64_t>(n_words, moe::kTimelineGemmWords);
+    if (g > 0 && cudaMemcpyFromSymbol(host_words, moe::g_timeline, (size_t)g * 8) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (n_words > g &&
+        moe::dispatch_timeline_copy(host_words + g, (size_t)(n_words - g)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }

@@ -141,6 +141,10 @@ cudaError_t launch_dispatch(const moe_config &c, const WorkspaceLayout &L, uint8
                             const GatherArgs *gather = nullptr);
 // Split batch, rank without tokens: counts and sums over all ranks into
 // gcount/gpsum, then the balance loss of `aux` (which points at them).
+// The dispatch kernel's per-block phase stamps (MOE_TIMELINE builds):
+// copy the first `words` words to host memory, or zero them.
+cudaError_t dispatch_timeline_copy(uint64_t *host, size_t words);
+cudaError_t dispatch_timeline_clear();
 cudaError_t launch_shard_stats(const int32_t *all_counts, const double *all_psum, int n_ranks,
                                int rank, long long TK_global, int32_t *gcount, double *gpsum,
                                const AuxArgs &aux, int32_t *status, cudaStream_t stream);

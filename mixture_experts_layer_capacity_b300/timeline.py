@@ -1,4 +1,5 @@
-"""Per-unit timeline of the routed CTA-pair expert GEMMs.
+"""Per-unit timeline of the routed CTA-pair expert GEMMs and per-block
+timeline of the dispatch kernel.
 
     python -m mixture_experts_layer_capacity_b300.timeline --workload dsv3_prefill [--json]
 
@@ -11,7 +12,9 @@ pair's time goes: the MMA thread waiting for a free accumulator or for its
 first operand stage, issuing the unit's MMAs, and the epilogue warps waiting
 for the accumulator and draining it to HBM.  A GEMM whose epilogue drain is
 longer than its MMA issue span is bound by its epilogue, not by the tensor
-pipe.
+pipe.  For the dispatch kernel it gives, per phase, the median and the
+latest time (over the blocks) at which a block finished it, counted from
+the first block's start.
 
 The stamps are the GPU's global nanosecond timer; each record holds eight
 words (see ``moe_timeline_read`` in include/moe.h).  The instrumented library
@@ -36,6 +39,12 @@ REGIONS = ("gemm1", "gemm2")   # gate/up, down projection
 MMA_START, MMA_HAS_ACC, FIRST_STAGE_FULL, LAST_MMA_ISSUED = 0, 1, 2, 3
 EPI_ACC_FULL, EPI_DONE, IS_SWAP, EPI_START = 4, 5, 6, 7
 
+# the dispatch kernel's per-block records follow the GEMM regions
+DISPATCH_BASE = len(REGIONS) * MAX_UNITS * WORDS_PER_UNIT
+# word index -> phase a dispatch block has finished at that stamp
+DISPATCH_PHASES = {1: "rows_staged", 2: "router", 3: "gated_first_chunk", 4: "gating",
+                   5: "grid_barrier", 6: "segment_tables", 7: "row_copies"}
+
 # phase name -> (end word, start word)
 PHASES = {
     "mma_waits_accumulator": (MMA_HAS_ACC, MMA_START),
@@ -57,6 +66,34 @@ def units(words: np.ndarray, region: int) -> np.ndarray:
     done = (rec[:, MMA_START] != 0) & (rec[:, EPI_DONE] != 0)
     n = int(np.argmin(done)) if not done.all() else MAX_UNITS
     return rec[:n].astype(np.int64)
+
+
+def dispatch_blocks(words: np.ndarray) -> np.ndarray:
+    """The dispatch kernel's per-block records as an (n, 8) int64 array,
+    block order; recording stops at the first block that did not start."""
+    r = np.asarray(words, dtype=np.uint64)
+    rec = r[DISPATCH_BASE:DISPATCH_BASE + MAX_UNITS * WORDS_PER_UNIT]
+    if len(rec) < MAX_UNITS * WORDS_PER_UNIT:
+        return np.zeros((0, WORDS_PER_UNIT), dtype=np.int64)
+    rec = rec.reshape(MAX_UNITS, WORDS_PER_UNIT)
+    started = rec[:, 0] != 0
+    n = int(np.argmin(started)) if not started.all() else MAX_UNITS
+    return rec[:n].astype(np.int64)
+
+
+def summarize_dispatch(rec: np.ndarray) -> dict:
+    """Per phase, the median and the maximum over blocks of the time (ns)
+    from the first block's start to the block's stamp, and the span to the
+    last row copy."""
+    rec = np.asarray(rec, dtype=np.int64)
+    if len(rec) == 0:
+        return {"blocks": 0}
+    t0 = int(rec[:, 0].min())
+    out = {"blocks": len(rec), "span_ns": int(rec[:, 7].max() - t0), "phases": {}}
+    for word, name in DISPATCH_PHASES.items():
+        d = rec[:, word] - t0
+        out["phases"][name] = {"median_ns": float(np.median(d)), "max_ns": int(d.max())}
+    return out
 
 
 def summarize(rec: np.ndarray) -> dict:
@@ -91,6 +128,12 @@ def summarize(rec: np.ndarray) -> dict:
 
 def format_summary(name: str, summ: dict) -> str:
     lines = [f"== {name}"]
+    d = summ.get("dispatch", {"blocks": 0})
+    if d["blocks"]:
+        lines.append(f" dispatch: {d['blocks']} blocks, span {d['span_ns'] / 1e3:.1f} us; "
+                     "median (latest) block end of each phase from the first start:")
+        lines.append("   " + ", ".join(f"{ph} {v['median_ns'] / 1e3:.1f} ({v['max_ns'] / 1e3:.1f})"
+                                       for ph, v in d["phases"].items()))
     for region in REGIONS:
         s = summ.get(region, {"units": 0})
         if not s["units"]:
@@ -110,8 +153,9 @@ def format_summary(name: str, summ: dict) -> str:
 
 def collect(w, seed: int = 0, warmup: int = 2, device: str = "cuda"):
     """Run `warmup` forward passes of workload `w`, clear the timeline, run
-    one more, and return ({region: records}, outputs).  Needs the binding to
-    have loaded the timeline library (MOE_LIBRARY)."""
+    one more, and return ({region: records}, outputs); the regions are the
+    two GEMMs and "dispatch".  Needs the binding to have loaded the timeline
+    library (MOE_LIBRARY)."""
     import torch
 
     from . import binding as B
@@ -130,7 +174,9 @@ def collect(w, seed: int = 0, warmup: int = 2, device: str = "cuda"):
     B.forward(cfg, inp, outs)
     torch.cuda.synchronize()
     words = B.timeline_read()
-    return {region: units(words, i) for i, region in enumerate(REGIONS)}, outs
+    recs = {region: units(words, i) for i, region in enumerate(REGIONS)}
+    recs["dispatch"] = dispatch_blocks(words)
+    return recs, outs
 
 
 def main(argv=None) -> int:
@@ -145,7 +191,8 @@ def main(argv=None) -> int:
     from .workloads import WORKLOADS
     for name in args.workload:
         recs, _ = collect(WORKLOADS[name], seed=args.seed)
-        summ = {region: summarize(r) for region, r in recs.items()}
+        summ = {region: summarize(recs[region]) for region in REGIONS}
+        summ["dispatch"] = summarize_dispatch(recs["dispatch"])
         if args.json:
             print(json.dumps({"workload": name, **summ}))
         else:

@@ -1,10 +1,12 @@
 """The MOE_TIMELINE build (libmoe_timeline.so): CTA 0 of each routed CTA-pair
-GEMM launch stamps its units' MMA and epilogue phases.
+GEMM launch stamps its units' MMA and epilogue phases, and every dispatch
+block its phases.
 
 The stamps must not change a result (the layer's y equals the normal
-build's bit for bit), every recorded unit's stamps must be in the order the
-pipeline runs them, and the pair's scheduler must hand out all its full
-tiles before its swap units.  The timeline build is loaded in a child
+build's bit for bit), every recorded unit's and block's stamps must be in
+the order the kernels run them (no dispatch block past the grid barrier
+before every block has gated its tokens), and the pair's scheduler must
+hand out all its full tiles before its swap units.  The timeline build is loaded in a child
 process (MOE_LIBRARY), since one process loads one build of the library."""
 import hashlib
 import json
@@ -27,9 +29,11 @@ TL_LIB = os.path.join(ROOT, "mixture_experts_layer_capacity_b300", "libmoe_timel
 
 # (name, T, D, E, F, k, S, mode, gamma, bias, E4M3 weights and activations)
 CASES = [
-    # 128 skewed experts: pair tiles, then many swap units
+    # 128 skewed experts: pair tiles, then many swap units; router GEMM
+    # apart from the dispatch kernel
     ("pair_tails_e128_zipf", 8200, 128, 128, 192, 8, 0, 2, 0.0, "zipf1.1", False),
-    # E4M3 pair tiles with drops and a shared expert (not recorded: dense)
+    # E4M3 pair tiles with drops and a shared expert (not recorded: dense);
+    # the router fused into the dispatch kernel (E = 4)
     ("a8_pair_ragged_drops", 8200, 192, 4, 320, 2, 256, 1, 0.6, "normal_var2", True),
 ]
 
@@ -112,6 +116,15 @@ def test_timeline_build_records_units_in_pipeline_order():
             assert s["tiles_before_swaps"], (name, region)
             print(name, region, s["units"], s["swap_units"], s["bound"],
                   round(s["mma_issue_frac"], 3), round(s["epilogue_drain_frac"], 3))
+        d = np.asarray(v["recs"]["dispatch"], dtype=np.int64)
+        assert len(d) > 0, name
+        # per block: start <= staged <= router <= gated <= ... <= copies done
+        assert (np.diff(d, axis=1) >= 0).all(), name
+        # the grid barrier: no block passes it before every block has
+        # finished gating (1 us of slack for the timer's reads on other SMs)
+        assert d[:, 5].min() >= d[:, 4].max() - 1000, name
+        sd = TL.summarize_dispatch(d)
+        print(name, "dispatch", sd["blocks"], round(sd["span_ns"] / 1e3, 1))
     # the skewed 128-expert layer has experts under 256 rows: swap units
     assert any(np.asarray(res["pair_tails_e128_zipf"]["recs"][r])[:, TL.IS_SWAP].any()
                for r in TL.REGIONS)

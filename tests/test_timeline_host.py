@@ -1,6 +1,6 @@
-"""The unit-timeline summary (timeline.py) on hand-made records (no GPU):
-phase durations, the span, the pair-tile / swap-unit split, the bound, and
-where a region's recording stops."""
+"""The timeline summaries (timeline.py) on hand-made records (no GPU): the
+GEMM units' phase durations, span, pair-tile / swap-unit split and bound,
+the dispatch blocks' phase ends, and where each region's recording stops."""
 import numpy as np
 import pytest
 
@@ -66,3 +66,25 @@ def test_summary_flags_a_swap_unit_ahead_of_a_tile():
     assert s["bound"] == "mma" and not s["tiles_before_swaps"]
     assert s["phases"]["epilogue_drain"]["swap_mean_ns"] == 10
     assert TL.summarize(np.zeros((0, 8), dtype=np.int64)) == {"units": 0}
+
+
+def test_dispatch_summary_and_layout():
+    w = np.zeros(TL.DISPATCH_BASE + TL.MAX_UNITS * TL.WORDS_PER_UNIT, dtype=np.uint64)
+    assert TL.DISPATCH_BASE + TL.MAX_UNITS * TL.WORDS_PER_UNIT == 98304
+    blocks = []
+    for b in range(3):
+        t0 = 1000 + 10 * b
+        r = np.array([t0, t0 + 5, t0 + 7, t0 + 9, t0 + 20, 2000, 2100 + b, 2500 + 100 * b],
+                     dtype=np.int64)
+        blocks.append(r)
+        w[TL.DISPATCH_BASE + 8 * b: TL.DISPATCH_BASE + 8 * b + 8] = r
+    rec = TL.dispatch_blocks(w)
+    assert rec.shape == (3, 8) and (rec == np.stack(blocks)).all()
+    s = TL.summarize_dispatch(rec)
+    assert s["blocks"] == 3 and s["span_ns"] == 2700 - 1000
+    assert s["phases"]["rows_staged"] == {"median_ns": 15.0, "max_ns": 25}
+    assert s["phases"]["grid_barrier"] == {"median_ns": 1000.0, "max_ns": 1000}
+    assert s["phases"]["row_copies"]["median_ns"] == 1600.0
+    assert TL.summarize_dispatch(np.zeros((0, 8))) == {"blocks": 0}
+    text = TL.format_summary("x", {"dispatch": s, "gemm1": {"units": 0}, "gemm2": {"units": 0}})
+    assert "dispatch: 3 blocks, span 1.7 us" in text
