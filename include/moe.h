@@ -170,7 +170,8 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
                        cudaStream_t stream);
 
 /* Per-unit timeline of the routed CTA-pair GEMMs and per-block timeline of
- * the dispatch kernel, for profiling.  Only the library built with
+ * the dispatch kernel, for profiling (a measurement aid, not an operation of
+ * the layer the pages define).  Only the library built with
  * MOE_TIMELINE (libmoe_timeline.so; python -m
  * mixture_experts_layer_capacity_b300.build --timeline) records them; other
  * builds return MOE_ERR_UNSUPPORTED.  All words are globaltimer
@@ -190,8 +191,10 @@ MOE_API moe_status moe_forward(const moe_config *cfg,
  * Unwritten words stay 0; a later launch of the same kernel overwrites the
  * records, so read them after the forward pass of interest.
  * moe_timeline_clear zeroes all 98304 words; moe_timeline_read copies the
- * first n_words (<= 98304) to host memory.  Both synchronise with the
- * device. */
+ * first n_words (<= 98304) into host_words, caller-owned host memory of at
+ * least n_words words.  Both synchronise with the device.  Errors: a null
+ * host_words or n_words outside [0, 98304] -> MOE_ERR_INVALID_ARG (checked
+ * after MOE_ERR_UNSUPPORTED); a failed copy -> MOE_ERR_CUDA. */
 #define MOE_TIMELINE_WORDS 98304
 MOE_API moe_status moe_timeline_clear(void);
 MOE_API moe_status moe_timeline_read(uint64_t *host_words, int64_t n_words);

@@ -241,6 +241,29 @@ def test_timeline_is_unsupported_outside_its_build():
     assert L.moe_timeline_read(buf.ctypes.data, 8) == B.MOE_ERR_UNSUPPORTED
     with pytest.raises(B.MoeError):
         B.timeline_read(8)
+    assert B.TIMELINE_WORDS == 98304
+
+
+def test_timeline_build_validates_before_touching_the_device():
+    """libmoe_timeline.so refuses a null buffer or a word count outside
+    [0, MOE_TIMELINE_WORDS] before any CUDA call (run in a child process,
+    which loads that build instead of libmoe.so)."""
+    import subprocess
+    import sys
+    from mixture_experts_layer_capacity_b300 import build
+    lib = build.build(timeline=True)
+    child = (
+        "import ctypes, sys\n"
+        "import numpy as np\n"
+        "L = ctypes.CDLL(sys.argv[1])\n"
+        "L.moe_timeline_read.argtypes = [ctypes.c_void_p, ctypes.c_int64]\n"
+        "buf = np.zeros(8, dtype=np.uint64)\n"
+        "print(L.moe_timeline_read(None, 8), L.moe_timeline_read(buf.ctypes.data, -1),\n"
+        "      L.moe_timeline_read(buf.ctypes.data, 98305))\n")
+    r = subprocess.run([sys.executable, "-c", child, lib], capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.split() == [str(B.MOE_ERR_INVALID_ARG)] * 3
 
 
 def _call_w8a8(cfg, ws, ws_bytes, shared=True):
