@@ -126,7 +126,9 @@ MOE_API moe_status moe_workspace_size(const moe_config *cfg, size_t *bytes);
 
 /* Expert capacity the library uses for `cfg`: ceil(capacity_factor * T *
  * top_k / n_experts) computed in double, or -1 when dropless
- * (module 17, 17.5 equation).  Host only; no GPU needed. */
+ * (module 17, 17.5 equation); a value of 9.2e18 or more (larger than any
+ * demand, so nothing is dropped) saturates at INT64_MAX.  Host only; no GPU
+ * needed. */
 MOE_API int64_t moe_capacity(const moe_config *cfg);
 
 /* The forward pass (one call = the whole layer, enqueued on `stream`).

@@ -4,6 +4,7 @@
 // on the caller's stream, with no host synchronisation.
 #include <atomic>
 #include <cmath>
+#include <cstdint>
 #include <cstring>
 
 #include "moe_internal.h"
@@ -55,8 +56,11 @@ int64_t capacity_of(const moe_config *c, int64_t T_cap)
     if (!(c->capacity_factor > 0.0f))
         return -1;
     const int64_t T = T_cap < 0 ? c->T : T_cap;
-    return (int64_t)std::ceil((double)c->capacity_factor * (double)(T * c->top_k) /
-                              (double)c->n_experts);
+    const double cap = std::ceil((double)c->capacity_factor * (double)(T * c->top_k) /
+                                 (double)c->n_experts);
+    // a capacity beyond int64 exceeds every expert's demand (at most T*k),
+    // so it keeps every assignment, as INT64_MAX does
+    return cap >= 9.2e18 ? INT64_MAX : (int64_t)cap;
 }
 
 WorkspaceLayout layout_of(const moe_config *c, int64_t T_cap)
@@ -69,7 +73,7 @@ WorkspaceLayout layout_of(const moe_config *c, int64_t T_cap)
                                      (T + kChunk - 1) / kChunk);
     L.C = capacity_of(c, T_cap);
     const int64_t TK = T * k;
-    L.R_max = L.C < 0 ? TK : std::min<int64_t>(TK, E * L.C);
+    L.R_max = (L.C < 0 || L.C >= TK) ? TK : std::min<int64_t>(TK, E * L.C);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;

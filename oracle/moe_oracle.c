@@ -250,7 +250,10 @@ int64_t oracle_capacity(int64_t T, int64_t k, int64_t E, double gamma)
 {
     if (gamma <= 0.0)
         return -1;
-    return (int64_t)ceil(gamma * (double)(T * k) / (double)E);
+    const double c = ceil(gamma * (double)(T * k) / (double)E);
+    /* no expert can be asked for more than T*k rows, so a capacity too large
+     * for int64 drops nothing: saturate rather than overflow the cast */
+    return c >= 9.2e18 ? INT64_MAX : (int64_t)c;
 }
 
 /* Capacity truncation in token order: walk t = 0..T-1 and j = 0..k-1; the

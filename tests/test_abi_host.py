@@ -53,6 +53,20 @@ def test_capacity_formula(T, k, E, gamma):
     assert B.capacity(cfg) == oracle.capacity(T, k, E, float(np.float32(gamma)))
 
 
+def test_capacity_beyond_int64_saturates():
+    """A capacity factor so large that ceil(gamma*T*k/E) leaves int64 keeps
+    every assignment: library and oracle both report INT64_MAX, and the
+    scratch is that of a layer that drops nothing."""
+    big = B.make_config(4096, 512, 8, 2048, 2, capacity_factor=3.0e38)
+    assert B.capacity(big) == 2**63 - 1 == oracle.capacity(4096, 2, 8, 3.0e38)
+    roomy = B.make_config(4096, 512, 8, 2048, 2, capacity_factor=8.0)   # C = 8192 = T*k
+    assert B.capacity(roomy) == 4096 * 2
+    assert B.workspace_size(big) == B.workspace_size(roomy)
+    idx = np.random.default_rng(0).integers(0, 8, size=(64, 2)).astype(np.int32)
+    dropped, kept = oracle.apply_capacity(idx, 8, 2**63 - 1)
+    assert not dropped.any() and kept.sum() == 128
+
+
 def test_workspace_size_and_validation():
     ok = B.make_config(4096, 512, 8, 2048, 1, capacity_factor=1.0)
     n1 = B.workspace_size(ok)
