@@ -83,7 +83,8 @@ typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP32 = 1 } moe_dtype;
 /* Layer shape and options.  Supported:
  *   T >= 0 tokens, T * top_k < 2^31;
  *   1 <= n_experts <= 256; 1 <= top_k <= min(8, n_experts);
- *   d_model, d_expert >= 1; d_shared >= 0 (0 = no shared expert);
+ *   1 <= d_model, d_expert <= 2^20; 0 <= d_shared <= 2^20 (0 = no shared
+ *   expert);
  *   bf16: d_model, d_expert and d_shared multiples of 64;
  *   fp32: any sizes (SIMT path, for small layers and exact checks).
  * capacity_factor <= 0 means dropless.  aux_alpha scales aux_loss.

@@ -37,6 +37,10 @@ moe_status validate_config(const moe_config *c)
         return MOE_ERR_INVALID_ARG;
     if (c->n_experts > kMaxExperts || c->top_k > kMaxTopK)
         return MOE_ERR_UNSUPPORTED;
+    // widths up to 2^20 keep every workspace term (at most 4 bytes x 2^31
+    // rows x 2^20) and their sum far inside size_t
+    if (c->d_model > kMaxWidth || c->d_expert > kMaxWidth || c->d_shared > kMaxWidth)
+        return MOE_ERR_UNSUPPORTED;
     if ((long long)c->T * c->top_k >= (1ll << 31))
         return MOE_ERR_UNSUPPORTED;
     if (c->dtype == MOE_DTYPE_BF16) {
@@ -419,7 +423,7 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r,
 static bool latent_layout(const moe_config *cfg, int32_t d_outer, size_t *x_lat, size_t *y_lat,
                           size_t *total)
 {
-    if (validate_config(cfg) != MOE_OK || d_outer < 1)
+    if (validate_config(cfg) != MOE_OK || d_outer < 1 || d_outer > kMaxWidth)
         return false;
     if (cfg->dtype == MOE_DTYPE_BF16 && d_outer % 64)
         return false;

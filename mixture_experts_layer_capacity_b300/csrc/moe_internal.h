@@ -16,6 +16,7 @@ constexpr int kChunk = 32;       // most tokens per routing chunk (one bit each 
 constexpr int kMaxDispatchBlocks = 256;  // most blocks of the dispatch kernel
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
+constexpr int kMaxWidth = 1 << 20;  // largest d_model, d_expert, d_shared, d_outer
 constexpr int kTileM = 128;      // rows per tensor-core tile (UMMA M)
 
 // Byte offsets of the scratch regions inside the caller's workspace.  Every

@@ -67,6 +67,23 @@ def test_capacity_beyond_int64_saturates():
     assert not dropped.any() and kept.sum() == 128
 
 
+def test_widths_beyond_two_to_the_twenty_are_unsupported():
+    """Widths are bounded so that no workspace term can leave size_t."""
+    w = 1 << 20
+    ok = B.make_config(64, w, 8, 64, 2)
+    assert B.workspace_size(ok) > 0
+    for cfg in (B.make_config(64, w + 64, 8, 64, 2), B.make_config(64, 64, 8, w + 64, 2),
+                B.make_config(64, 64, 8, 64, 2, d_shared=w + 64)):
+        n = ctypes.c_size_t(0)
+        assert B.lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == \
+            B.MOE_ERR_UNSUPPORTED
+    n = ctypes.c_size_t(0)
+    small = B.make_config(64, 64, 8, 64, 2)
+    assert B.lib().moe_latent_workspace_size(ctypes.byref(small), w + 64, ctypes.byref(n)) == \
+        B.MOE_ERR_UNSUPPORTED
+    assert B.lib().moe_latent_workspace_size(ctypes.byref(small), w, ctypes.byref(n)) == B.MOE_OK
+
+
 def test_workspace_size_and_validation():
     ok = B.make_config(4096, 512, 8, 2048, 1, capacity_factor=1.0)
     n1 = B.workspace_size(ok)
