@@ -50,6 +50,20 @@ int main(void)
            (int)moe_forward(&sw, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
                             NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 0));
     printf("status_string %s\n", moe_status_string(MOE_ERR_WORKSPACE));
+    {
+        uint64_t words[8];
+        size_t w8 = 0;
+        moe_config wide = sw;
+        wide.d_model = (1 << 20) + 64;
+        printf("timeline_clear %d\n", (int)moe_timeline_clear());
+        printf("timeline_read %d\n", (int)moe_timeline_read(words, 8));
+        printf("w8a8_workspace_status %d\n", (int)moe_w8a8_workspace_size(&sw, &w8));
+        printf("w8a8_workspace_covers %d\n", w8 >= ws);
+        printf("wide_status %d\n", (int)moe_workspace_size(&wide, &ws));
+        printf("capacity_huge %lld\n",
+               (long long)moe_capacity(&(moe_config){4096, 512, 8, 2048, 2, 0, MOE_DTYPE_BF16,
+                                                      MOE_GATE_SOFTMAX_ALL, 3.0e38f, 0.01f, 0}));
+    }
     return 0;
 }
 """
@@ -83,3 +97,8 @@ def test_host_entry_points_from_c(tmp_path):
     assert got["bad_k_status"] == "2"            # MOE_ERR_UNSUPPORTED: 8 < k <= E
     assert got["null_x_status"] == "1"           # MOE_ERR_INVALID_ARG
     assert "workspace" in got["status_string"].lower()
+    # the timeline readers exist in every build and refuse outside theirs
+    assert got["timeline_clear"] == "2" and got["timeline_read"] == "2"
+    assert got["w8a8_workspace_status"] == "0" and got["w8a8_workspace_covers"] == "1"
+    assert got["wide_status"] == "2"             # widths above 2^20
+    assert got["capacity_huge"] == str(2**63 - 1)  # saturates, drops nothing
